@@ -1,0 +1,84 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that a pin catches each.
+
+Every mutant replaces one oracle function for the duration of one test; the
+pin tests of ``test_oracle_pins.py`` are then run against it and must fail.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle.diffattn_oracle as om
+import tests.test_oracle_pins as pins
+
+
+def _transposed_scores(q, k, scale, causal, rows=None):
+    q, k = om._f64(q), om._f64(k)
+    rows = om._rows(rows, q.shape[0])
+    s = (k @ q.T)[rows] * scale  # operands swapped
+    if causal:
+        j = np.arange(k.shape[0])[None, :]
+        s = np.where(j <= rows[:, None], s, -np.inf)
+    return om.softmax_rows(s)
+
+
+def _off_by_one_mask(q, k, scale, causal, rows=None):
+    q, k = om._f64(q), om._f64(k)
+    rows = om._rows(rows, q.shape[0])
+    s = (q[rows] @ k.T) * scale
+    if causal:
+        j = np.arange(k.shape[0])[None, :]
+        s = np.where(j <= rows[:, None] + 1, s, -np.inf)  # sees one future key
+    return om.softmax_rows(s)
+
+
+def _plus_lambda(q1, k1, q2, k2, lam, causal, rows=None, scale=None):
+    scale = 1 / math.sqrt(om._f64(q1).shape[-1]) if scale is None else scale
+    return om.attention_map(q1, k1, scale, causal, rows) + lam * om.attention_map(q2, k2, scale, causal, rows)
+
+
+def _norm_with_lambda_not_init(o, gamma, eps, lam_init):
+    o = om._f64(o)
+    ms = np.mean(o * o, axis=-1, keepdims=True)
+    return gamma_or_one(gamma, o) * o / np.sqrt(ms + eps)  # drops the (1 - lambda_init) factor
+
+
+def gamma_or_one(gamma, o):
+    return np.ones(o.shape[-1]) if gamma is None else om._f64(gamma)
+
+
+def _norm_over_tokens(o, gamma, eps, lam_init):
+    o = om._f64(o)
+    ms = np.mean(o * o, axis=0, keepdims=True)  # wrong axis
+    return (1 - lam_init) * gamma_or_one(gamma, o) * o / np.sqrt(ms + eps)
+
+
+MUTANTS = [
+    ("attention_map", _transposed_scores, lambda: pins.test_lambda_zero_is_sdpa(False)),
+    ("attention_map", _off_by_one_mask, lambda: pins.test_lambda_zero_is_sdpa(True)),
+    ("difference_map", _plus_lambda, lambda: pins.test_rows_sum_to_one_minus_lambda(False, 0.8)),
+    ("head_rmsnorm", _norm_with_lambda_not_init, pins.test_causal_row_zero_closed_form),
+    ("head_rmsnorm", _norm_over_tokens, pins.test_head_rmsnorm_matches_torch_rms_norm),
+]
+
+
+@pytest.mark.parametrize("name,mutant,pin", MUTANTS, ids=[m[1].__name__ for m in MUTANTS])
+def test_pin_catches_mutant(monkeypatch, name, mutant, pin):
+    pin()  # passes on the real oracle
+    monkeypatch.setattr(om, name, mutant)
+    monkeypatch.setattr(pins.oracle, name, mutant)
+    with pytest.raises(AssertionError):
+        pin()
+
+
+def test_v2_pin_catches_halves_pairing(monkeypatch):
+    real = om.diff_attn_v2
+
+    def halves(*a, **k):
+        k["pairing"] = "halves"
+        return real(*a, **k)
+
+    monkeypatch.setattr(pins.oracle, "diff_attn_v2", halves)
+    with pytest.raises(AssertionError):
+        pins.test_v2_against_sdpa(True)
