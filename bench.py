@@ -1,0 +1,392 @@
+"""Benchmark of the differential-attention forward on GB300 (one JSON line).
+
+A step is one DIFF V1 layer forward of the selected workload: lambda_init and
+the lambda re-parameterisation (one warp), then the fused forward (two
+softmax maps, their lambda-weighted difference times V, the per-head RMSNorm
+with (1 - lambda_init)) on inputs already resident in HBM.  For the DIFF V2
+workload a step is the V2 forward.  The default workload is the one the
+metric is normally quoted on (B4 H16 n2048 d64); ``--config`` selects
+another, and the line's ``configs`` object reports every workload measured in
+the same run.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config C]
+       python bench.py --impl reference ...   (the fp64 CPU oracle, timed on
+       the host cores on a bounded sample of the same workload)
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "diff-attn fwd TFLOP/s (bf16) and % of GB300 dense tensor peak; tokens/s"
+DEFAULT_CONFIG = 2
+FLUSH_BYTES = 512 << 20  # > 129 MB L2
+
+
+def flops(w) -> float:
+    """Algorithmic FLOPs of one forward: V1 12 n^2 d per (b, h), V2 4 n^2 d per query head; x1/2 causal."""
+    if w.kind == "v1":
+        f = 12.0 * w.n * w.n * w.d * w.B * w.H
+    else:
+        f = 4.0 * w.n * w.n * w.d * w.B * w.Hq
+    return f / 2 if w.causal else f
+
+
+def hbm_bytes(w) -> float:
+    """Algorithmic HBM bytes: every input read once, the output written once."""
+    e = 4 if w.dtype == "f32" else 2
+    if w.kind == "v1":
+        return float(w.B * w.H * w.n * w.d * 8 * e)  # q1 q2 k1 k2 (4d) + v (2d) + out (2d)
+    return float(w.B * w.n * w.d * (w.Hq + 2 * w.Hkv + w.Hq // 2) * e)
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- our path
+def make_step(w, x, da):
+    """Returns (step(), kernel-only call, output) for workload w on device tensors x."""
+    import torch
+    if w.kind == "v1":
+        lam = torch.empty(1, device=x["q1"].device, dtype=torch.float32)
+        out = torch.empty(x["v"].shape, device=x["v"].device, dtype=x["v"].dtype)
+
+        def lam_call():
+            lin = da.lambda_init(w.layer)
+            da.lambda_reparam(x["lq1"], x["lk1"], x["lq2"], x["lk2"], lin, out=lam)
+
+        def fwd_call():
+            da.diffattn_forward(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], lam, da.lambda_init(w.layer),
+                                gamma=x["gamma"], causal=w.causal, out=out)
+        return lam_call, fwd_call, out
+    out = torch.empty((w.B, w.n, w.Hq // 2, w.d), device=x["q"].device, dtype=x["q"].dtype)
+
+    def fwd_call():
+        da.diffattn_v2_forward(x["q"], x["k"], x["v"], x["lam_logits"], causal=w.causal, out=out)
+    return (lambda: None), fwd_call, out
+
+
+def time_device(w, x, da, steps, warmup, flush, dist=None):
+    """Device timing with CUDA events on the launching stream; L2 flushed between steps."""
+    import torch
+    lam_call, fwd_call, out = make_step(w, x, da)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        lam_call()
+        fwd_call()
+    da.device_status()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    c0 = da.launch_count()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    t0 = time.perf_counter()
+    for k in range(steps):
+        flush.zero_()
+        ev[k][0].record(stream)
+        lam_call()
+        ev[k][1].record(stream)
+        fwd_call()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    launches = da.launch_count() - c0
+    if dist is not None:
+        dist.barrier()
+    da.device_status()
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    kern_ms = [b.elapsed_time(c) for a, b, c in ev]
+    return {"step_ms": sum(step_ms) / steps, "kernel_ms": sum(kern_ms) / steps,
+            "kernel_ms_median": statistics.median(kern_ms), "wall_s": wall, "launches": launches, "out": out}
+
+
+def time_e2e(w, x, da, steps):
+    """End-to-end through the public API: pinned host inputs -> device -> forward -> host output."""
+    import torch
+    host = {k: t.cpu().pin_memory() for k, t in x.items()}
+    dev = {k: torch.empty_like(t) for k, t in x.items()}
+    lam_call, fwd_call, out = make_step(w, dev, da)
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out.numel() * out.element_size()
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        lam_call()
+        fwd_call()
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+def cpu_baseline(w, x, budget_s=12.0):
+    """The fp64 oracle as it stands, on a bounded sample of query blocks of the same workload."""
+    import numpy as np
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    rows_done, fl, t0 = 0, 0.0, time.perf_counter()
+    n = w.n
+    blocks = list(range(0, n, 128))
+    order = blocks[::-1]  # heaviest causal blocks first, like the GPU
+    b, u = 0, 0
+    if w.kind == "v1":
+        xs = {k: (t[b:b + 1, :, u:u + 1] if t.dim() == 4 else t) for k, t in x.items()}
+        xs = {k: t.cpu() for k, t in xs.items()}
+        lin = oracle.lambda_init(w.layer)
+        lam = oracle.lambda_reparam(xs["lq1"], xs["lk1"], xs["lq2"], xs["lk2"], lin)
+        arrs = {k: oracle.diffattn_oracle._f64(xs[k]) for k in ("q1", "q2", "k1", "k2", "v")}
+        for s in order:
+            rows = np.arange(s, min(s + 128, n))
+            oracle.diff_attn_v1(arrs["q1"], arrs["q2"], arrs["k1"], arrs["k2"], arrs["v"], lam, lin,
+                                xs["gamma"], 1e-5, w.causal, rows)
+            rows_done += rows.size
+            fl += sum(12.0 * w.d * ((r + 1) if w.causal else n) for r in rows)
+            if time.perf_counter() - t0 > budget_s:
+                break
+    else:
+        g = w.Hq // w.Hkv
+        xs = {"q": x["q"][0:1, :, 0:2].cpu(), "k": x["k"][0:1, :, 0:1].cpu(), "v": x["v"][0:1, :, 0:1].cpu()}
+        arrs = {k: oracle.diffattn_oracle._f64(t) for k, t in xs.items()}
+        lg = np.broadcast_to(x["lam_logits"][0:1].cpu().double().numpy(), (1, n, 1))
+        for s in order:
+            rows = np.arange(s, min(s + 128, n))
+            oracle.diff_attn_v2(arrs["q"], arrs["k"], arrs["v"], lg, w.causal, rows=rows)
+            rows_done += rows.size
+            fl += sum(2 * 4.0 * w.d * ((r + 1) if w.causal else n) for r in rows)
+            if time.perf_counter() - t0 > budget_s:
+                break
+        del g
+    dt = time.perf_counter() - t0
+    unit = "head pair" if w.kind == "v2" else "head"
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows_done} of {n} query rows of one (batch, {unit}) unit, heaviest 128-row blocks first, "
+                      f"{dt:.1f} s; algorithmic causal FLOPs of those rows",
+            "seconds": dt}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as tdist
+    from differential_attention_03_gb300 import binding as da, build
+    from differential_attention_03_gb300.inputs import WORKLOADS, make_v1, make_v2, shrink
+    from differential_attention_03_gb300.sharding import weak_scaling_seed
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = tdist
+    if rank == 0:
+        build.build()
+    if dist is not None:
+        dist.barrier()
+    da.lib()
+    peaks = read_peaks()
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
+
+    def inputs(w):
+        w = shrink(w, seed=weak_scaling_seed(w.seed, rank))
+        return make_v1(w, "cuda") if w.kind == "v1" else make_v2(w, "cuda")
+
+    w = WORKLOADS[args.config]
+    x = inputs(w)
+    sampler = ClockSampler(local)
+    sampler.start()
+    res = time_device(w, x, da, args.steps, args.warmup, flush, dist)
+    clocks = sampler.stop()
+    step_ms = torch.tensor([res["step_ms"], res["kernel_ms"]], device="cuda", dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(step_ms, op=tdist.ReduceOp.MAX)
+    step_ms, kern_ms = float(step_ms[0]), float(step_ms[1])
+    f = flops(w)
+    value = world * f / (step_ms * 1e-3) / 1e12
+    e2e_ms, h2d, d2h = time_e2e(w, x, da, max(3, min(args.steps, 10)))
+    e2e_t = torch.tensor([e2e_ms], device="cuda", dtype=torch.float64)
+    if dist is not None:
+        dist.all_reduce(e2e_t, op=tdist.ReduceOp.MAX)
+    e2e_value = world * f / (float(e2e_t[0]) * 1e-3) / 1e12
+
+    kernel_tflops = f / (kern_ms * 1e-3) / 1e12
+    if w.dtype == "bf16":
+        roof = {"bound": "tensor", "achieved": round(kernel_tflops, 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(kernel_tflops / peaks["bf16_tflops"], 4),
+                "traffic": None, "peak_source": peaks["source"] + " (burst bf16 dense)"}
+    else:
+        gbs = hbm_bytes(w) / (kern_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None, "peak_source": peaks["source"]}
+
+    configs = {}
+    if rank == 0 and world == 1 and not args.no_all_configs:
+        for cid, wc in WORKLOADS.items():
+            xc = x if cid == args.config else inputs(wc)
+            r = time_device(wc, xc, da, max(5, min(args.steps, 20)), 3, flush)
+            fc = flops(wc)
+            tf = fc / (r["kernel_ms"] * 1e-3) / 1e12
+            configs[wc.name] = {
+                "kernel_ms": round(r["kernel_ms"], 4), "step_ms": round(r["step_ms"], 4),
+                "tflops": round(tf, 2), "pct_peak": round(100 * tf / peaks["bf16_tflops"], 2),
+                "tokens_per_s": round(wc.B * wc.n / (r["step_ms"] * 1e-3), 1),
+                "hbm_gbs": round(hbm_bytes(wc) / (r["kernel_ms"] * 1e-3) / 1e9, 1)}
+            if cid != args.config:
+                del xc
+            torch.cuda.empty_cache()
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded N(0,1) inputs, shapes of the workload)",
+        "config": {"workload": w.name, "global_batch": w.B * world, "seq_len": w.n,
+                   "heads": w.H or w.Hq, "head_dim": w.d, "causal": w.causal,
+                   "parallelism": f"dp{world} (batch split, no collective)",
+                   "l2": "flushed between timed steps (512 MB write)"},
+        "tokens_per_s": round(world * w.B * w.n / (step_ms * 1e-3), 1),
+        "pct_of_peak": round(100 * kernel_tflops / peaks["bf16_tflops"], 2) if w.dtype == "bf16" else None,
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(float(e2e_t[0]), 4)},
+        "gpu_launches": res["launches"],
+        "roofline": roof,
+        "clocks": clocks,
+    }
+    if configs:
+        line["configs"] = configs
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(w, x)
+        cb.pop("seconds", None)
+        line["cpu_baseline"] = cb
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores, same workload/metric/unit (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+    from differential_attention_03_gb300.inputs import WORKLOADS, make_v1, make_v2
+    w = WORKLOADS[args.config]
+    x = make_v1(w, "cpu") if w.kind == "v1" else make_v2(w, "cpu")
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_baseline(w, x, budget_s=min(per_step, 2.0))
+    vals, secs, last = [], [], None
+    for _ in range(args.steps):
+        last = cpu_baseline(w, x, budget_s=per_step)
+        vals.append(last["value"])
+        secs.append(last["seconds"])
+    v = statistics.mean(vals)
+    f_step = flops(w)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": f_step / (v * 1e12) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) inputs, shapes of the workload)",
+            "config": {"workload": w.name, "global_batch": w.B, "seq_len": w.n, "heads": w.H or w.Hq,
+                       "head_dim": w.d, "causal": w.causal, "parallelism": "host cores"},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": last["cores"], "kind": "oracle",
+                             "sample": last["sample"] + "; each step one such bounded sample"},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    del torch
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-all-configs", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

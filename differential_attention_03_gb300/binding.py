@@ -1,0 +1,189 @@
+"""Thin ctypes binding over libdiffattn.so (argument marshalling only).
+
+Every computation runs in the library's CUDA kernels; this module checks
+tensor placement/dtype/contiguity, passes raw device pointers, sizes and the
+current CUDA stream, and turns a non-OK status into an exception.  PyTorch is
+used only for device memory and streams.  If the library is missing this
+module raises on first use: there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdiffattn.so")
+
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(8)
+STATUS_NAMES = ["OK", "ERR_NULL", "ERR_SHAPE", "ERR_ALIGN", "ERR_DTYPE", "ERR_UNSUPPORTED", "ERR_CUDA",
+                "ERR_TIMEOUT"]
+F32, BF16 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DiffAttnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        self.status = status
+        name = STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else str(status)
+        super().__init__(f"{name}: {msg}")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libdiffattn.so (built in-tree by ``build.py``); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -m differential_attention_03_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i, f, ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
+            L.diffattn_lambda_init.argtypes = [i]
+            L.diffattn_lambda_init.restype = f
+            L.lambda_reparam.argtypes = [vp, vp, vp, vp, i, f, vp, vp]
+            L.lambda_reparam.restype = i
+            L.diffattn_forward.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, f, vp, f, i, vp, vp]
+            L.diffattn_forward.restype = i
+            L.diffattn_v2_forward.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, ll, ll, f, i, vp, vp]
+            L.diffattn_v2_forward.restype = i
+            L.diffattn_device_status.argtypes = [vp]
+            L.diffattn_device_status.restype = i
+            L.diffattn_last_error.argtypes = []
+            L.diffattn_last_error.restype = ctypes.c_char_p
+            L.diffattn_debug_wait_timeout.argtypes = [ll, vp]
+            L.diffattn_debug_wait_timeout.restype = i
+            L.diffattn_launch_count.argtypes = []
+            L.diffattn_launch_count.restype = ll
+            _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != OK:
+        raise DiffAttnError(status, lib().diffattn_last_error().decode(errors="replace"))
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise ValueError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def lambda_init(layer_index: int) -> float:
+    """lambda_init = 0.8 - 0.6 exp(-0.3 (l - 1)) for the 1-based layer index (host)."""
+    return float(lib().diffattn_lambda_init(int(layer_index)))
+
+
+def lambda_reparam(lq1, lk1, lq2, lk2, lambda_init_value: float, out=None, stream=None) -> torch.Tensor:
+    """Device scalar lambda = exp(lq1.lk1) - exp(lq2.lk2) + lambda_init (fp32, one element)."""
+    for name, t in (("lq1", lq1), ("lk1", lk1), ("lq2", lq2), ("lk2", lk2)):
+        _need(t, name, torch.float32, (lq1.numel(),))
+    if out is None:
+        out = torch.empty(1, device=lq1.device, dtype=torch.float32)
+    _need(out, "out", torch.float32, (1,))
+    _check(lib().lambda_reparam(_ptr(lq1), _ptr(lk1), _ptr(lq2), _ptr(lk2), lq1.numel(),
+                                float(lambda_init_value), _ptr(out), _stream(stream)))
+    return out
+
+
+def diffattn_forward(q1, q2, k1, k2, v, lam, lambda_init_value: float, gamma=None, eps: float = 1e-5,
+                     causal: bool = True, out=None, stream=None) -> torch.Tensor:
+    """DIFF V1 forward with per-head RMSNorm x (1 - lambda_init); BSHD tensors.
+
+    q1, q2, k1, k2: [B, n, H, d]; v: [B, n, H, 2d]; lam: device fp32 scalar
+    tensor; gamma: fp32 [2d] or None.  Returns out [B, n, H, 2d] (input dtype).
+    """
+    B, n, H, d = q1.shape
+    dt = q1.dtype
+    for name, t in (("q1", q1), ("q2", q2), ("k1", k1), ("k2", k2)):
+        _need(t, name, dt, (B, n, H, d))
+    _need(v, "v", dt, (B, n, H, 2 * d))
+    _need(lam, "lambda", torch.float32, (1,))
+    if gamma is not None:
+        _need(gamma, "gamma", torch.float32, (2 * d,))
+    if out is None:
+        out = torch.empty((B, n, H, 2 * d), device=q1.device, dtype=dt)
+    _need(out, "out", dt, (B, n, H, 2 * d))
+    _check(lib().diffattn_forward(_dt(q1), B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v),
+                                  _ptr(lam), float(lambda_init_value), _ptr(gamma), float(eps),
+                                  1 if causal else 0, _ptr(out), _stream(stream)))
+    return out
+
+
+def diffattn_v2_forward(q, k, v, lam_logits, causal: bool = True, softmax_scale: float = 0.0, out=None,
+                        stream=None) -> torch.Tensor:
+    """DIFF V2 forward: out_g = attn[2g] - sigmoid(logit) attn[2g+1]; BSHD tensors.
+
+    q: [B, n, Hq, d]; k, v: [B, n, Hkv, d]; lam_logits: fp32 [Hq/2] (one per
+    pair), [n, Hq/2] or [B, n, Hq/2].  Returns out [B, n, Hq/2, d].
+    """
+    B, n, Hq, d = q.shape
+    Hkv = k.shape[2]
+    dt = q.dtype
+    _need(q, "q", dt)
+    _need(k, "k", dt, (B, n, Hkv, d))
+    _need(v, "v", dt, (B, n, Hkv, d))
+    G = Hq // 2
+    _need(lam_logits, "lam_logits", torch.float32)
+    if lam_logits.shape == (G,):
+        sb, st = 0, 0
+    elif lam_logits.shape == (n, G):
+        sb, st = 0, G
+    elif lam_logits.shape == (B, n, G):
+        sb, st = n * G, G
+    else:
+        raise ValueError(f"lam_logits must be [Hq/2], [n, Hq/2] or [B, n, Hq/2]; got {tuple(lam_logits.shape)}")
+    if out is None:
+        out = torch.empty((B, n, G, d), device=q.device, dtype=dt)
+    _need(out, "out", dt, (B, n, G, d))
+    _check(lib().diffattn_v2_forward(_dt(q), B, Hq, Hkv, n, d, _ptr(q), _ptr(k), _ptr(v), _ptr(lam_logits),
+                                     sb, st, float(softmax_scale), 1 if causal else 0, _ptr(out),
+                                     _stream(stream)))
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream, read and clear the device status word (raises on error)."""
+    st = lib().diffattn_device_status(_stream(stream))
+    _check(st)
+    return st
+
+
+def debug_wait_timeout(budget_ns: int, stream=None) -> None:
+    """Launch the bounded-wait self-test kernel (its wait must run out)."""
+    _check(lib().diffattn_debug_wait_timeout(int(budget_ns), _stream(stream)))
+
+
+def launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(lib().diffattn_launch_count())

@@ -1,0 +1,338 @@
+// C ABI of libdiffattn.so: argument validation, TMA descriptor encoding,
+// kernel selection and launch, and the device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/diffattn.h"
+#include "launch.h"
+
+// Device status word (one per device that loads the library).  Kernels record
+// DIFFATTN_ERR_TIMEOUT here when a bounded wait runs out.
+__device__ int g_diffattn_status = 0;
+
+namespace {
+
+thread_local std::string t_last_error;
+std::atomic<long long> g_launches{0};
+
+diffattn_status fail(diffattn_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return s;
+}
+
+diffattn_status ok() {
+  t_last_error.clear();
+  return DIFFATTN_OK;
+}
+
+diffattn_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(DIFFATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+// Device address of g_diffattn_status on the current device.
+diffattn_status status_word(int** out) {
+  static std::mutex mu;
+  static int* ptrs[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DIFFATTN_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_diffattn_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  *out = ptrs[dev];
+  return DIFFATTN_OK;
+}
+
+// ---------------------------------------------------------------- TMA maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+diffattn_status get_encoder(EncodeTiledFn* fn) {
+  static std::once_flag once;
+  static EncodeTiledFn cached = nullptr;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) cached = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (cached == nullptr)
+    return fail(DIFFATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(err));
+  *fn = cached;
+  return DIFFATTN_OK;
+}
+
+// 4-D map over a BSHD bf16 tensor [B, n, heads, W]; box = 64 columns x 1 head
+// x `rows` tokens x 1 batch, 128-byte swizzle; reads past n return zeros.
+diffattn_status make_map(CUtensorMap* m, const void* base, int B, int n, int heads, int W, int rows) {
+  EncodeTiledFn enc;
+  diffattn_status s = get_encoder(&enc);
+  if (s != DIFFATTN_OK) return s;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(W) * 2, static_cast<cuuint64_t>(W) * heads * 2,
+                                 static_cast<cuuint64_t>(W) * heads * n * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(rows), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DIFFATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return DIFFATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Tile order: unit-major keeps all query tiles of one head together so that its
+// K/V stream is shared in L2; query-tile-major runs the heaviest causal tiles
+// of every head first.  Unit-major is used once the K/V bytes of all units
+// exceed what L2 keeps comfortably.
+int pick_order(long long units, long long n, int kv_row_bytes) {
+  const long long total = units * n * kv_row_bytes;
+  return total > (96ll << 20) ? 0 : 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+float diffattn_lambda_init(int layer_index) {
+  if (layer_index < 1) return NAN;
+  return static_cast<float>(0.8 - 0.6 * std::exp(-0.3 * (layer_index - 1)));
+}
+
+diffattn_status lambda_reparam(const float* lq1, const float* lk1, const float* lq2, const float* lk2, int dim,
+                               float lambda_init, float* lambda_out, void* stream) {
+  if (!lq1 || !lk1 || !lq2 || !lk2 || !lambda_out) return fail(DIFFATTN_ERR_NULL, "lambda_reparam: NULL pointer");
+  if (dim < 1) return fail(DIFFATTN_ERR_SHAPE, "lambda_reparam: dim must be >= 1 (got %d)", dim);
+  cudaError_t e = da::launch_lambda_reparam(lq1, lk1, lq2, lk2, dim, lambda_init, lambda_out,
+                                            static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lambda_reparam launch");
+  g_launches.fetch_add(1);
+  return ok();
+}
+
+diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d, const void* q1, const void* q2,
+                                 const void* k1, const void* k2, const void* v, const float* lambda,
+                                 float lambda_init, const float* gamma, float eps, int causal, void* out,
+                                 void* stream) {
+  if (dt != DIFFATTN_F32 && dt != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "diffattn_forward: bad dtype %d", (int)dt);
+  if (B < 0 || H < 0 || n < 0 || d < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_forward: bad sizes B=%d H=%d n=%d d=%d", B, H, n, d);
+  if (B == 0 || H == 0 || n == 0) return ok();
+  if (!q1 || !q2 || !k1 || !k2 || !v || !lambda || !out)
+    return fail(DIFFATTN_ERR_NULL, "diffattn_forward: NULL pointer");
+  if (!std::isfinite(lambda_init)) return fail(DIFFATTN_ERR_SHAPE, "diffattn_forward: lambda_init not finite");
+  if (eps <= 0.f) eps = 1e-5f;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int dv = 2 * d;
+  int* status = nullptr;
+
+  if (dt == DIFFATTN_F32) {
+    if (d > da::kSimtMaxD) return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_forward: f32 needs d <= 256 (got %d)", d);
+    diffattn_status st = status_word(&status);
+    if (st != DIFFATTN_OK) return st;
+    da::SimtParams p{};
+    p.q1 = static_cast<const float*>(q1);
+    p.q2 = static_cast<const float*>(q2);
+    p.k1 = static_cast<const float*>(k1);
+    p.k2 = static_cast<const float*>(k2);
+    p.v = static_cast<const float*>(v);
+    p.out = static_cast<float*>(out);
+    p.lambda = lambda;
+    p.gamma = gamma;
+    p.scale = 1.f / std::sqrt(static_cast<float>(d));
+    p.norm_mult = 1.f - lambda_init;
+    p.eps = eps;
+    p.B = B;
+    p.n = n;
+    p.d = d;
+    p.dv = dv;
+    p.causal = causal ? 1 : 0;
+    p.v2 = 0;
+    p.heads_q = p.heads_kv = p.units_per_batch = H;
+    p.group = 1;
+    p.rows_total = static_cast<long long>(B) * H * n;
+    cudaError_t e = da::launch_simt_f32(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward (f32) launch");
+    g_launches.fetch_add(1);
+    return ok();
+  }
+
+  // bf16: tcgen05 kernels
+  if (d != 64 && d != 128) return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_forward: bf16 needs d in {64, 128} (got %d)", d);
+  if (!aligned16(q1) || !aligned16(q2) || !aligned16(k1) || !aligned16(k2) || !aligned16(v) || !aligned16(out))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_forward: bf16 tensors must be 16-byte aligned");
+  diffattn_status st = status_word(&status);
+  if (st != DIFFATTN_OK) return st;
+  da::TwoPassParams p;
+  memset(&p, 0, sizeof(p));
+  if ((st = make_map(&p.tm_q1, q1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&p.tm_q2, q2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&p.tm_k1, k1, B, n, H, d, 64)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&p.tm_k2, k2, B, n, H, d, 64)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&p.tm_v, v, B, n, H, dv, 64)) != DIFFATTN_OK) return st;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lambda = lambda;
+  p.gamma = gamma;
+  p.lam_logits = nullptr;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  p.norm_mult = 1.f - lambda_init;
+  p.eps = eps;
+  p.B = B;
+  p.n = n;
+  p.causal = causal ? 1 : 0;
+  p.units_per_batch = H;
+  p.group = 1;
+  p.num_q_tiles = (n + 127) / 128;
+  p.order = pick_order(static_cast<long long>(B) * H, n, (2 * d + dv) * 2);
+  p.status = status;
+  const long long grid = static_cast<long long>(p.num_q_tiles) * B * H;
+  if (grid > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "diffattn_forward: too many tiles");
+  cudaError_t e = (d == 64) ? da::launch_twopass_v1_d64(p, static_cast<int>(grid), s)
+                            : da::launch_twopass_v1_d128(p, static_cast<int>(grid), s);
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward (bf16) launch");
+  g_launches.fetch_add(1);
+  return ok();
+}
+
+diffattn_status diffattn_v2_forward(diffattn_dtype dt, int B, int Hq, int Hkv, int n, int d, const void* q,
+                                    const void* k, const void* v, const float* lam_logits, long long sb,
+                                    long long st_, float softmax_scale, int causal, void* out, void* stream) {
+  if (dt != DIFFATTN_F32 && dt != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "diffattn_v2_forward: bad dtype %d", (int)dt);
+  if (B < 0 || Hq < 0 || Hkv < 1 || n < 0 || d < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_forward: bad sizes B=%d Hq=%d Hkv=%d n=%d d=%d", B, Hq, Hkv, n, d);
+  if (Hq % 2 != 0 || Hq % Hkv != 0 || (Hq / Hkv) % 2 != 0)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_forward: need Hq even, Hq %% Hkv == 0 and Hq/Hkv even (Hq=%d Hkv=%d)",
+                Hq, Hkv);
+  if (sb < 0 || st_ < 0) return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_forward: negative logit stride");
+  if (B == 0 || Hq == 0 || n == 0) return ok();
+  if (!q || !k || !v || !lam_logits || !out) return fail(DIFFATTN_ERR_NULL, "diffattn_v2_forward: NULL pointer");
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.f / std::sqrt(static_cast<float>(d));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int* status = nullptr;
+  diffattn_status st = status_word(&status);
+  if (st != DIFFATTN_OK) return st;
+  const int G = Hq / 2;
+
+  if (dt == DIFFATTN_F32) {
+    if (d > da::kSimtMaxD) return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_v2_forward: f32 needs d <= 256");
+    da::SimtParams p{};
+    p.q1 = p.q2 = static_cast<const float*>(q);
+    p.k1 = p.k2 = static_cast<const float*>(k);
+    p.v = static_cast<const float*>(v);
+    p.out = static_cast<float*>(out);
+    p.lam_logits = lam_logits;
+    p.sb = sb;
+    p.st = st_;
+    p.scale = scale;
+    p.norm_mult = 1.f;
+    p.eps = 0.f;
+    p.B = B;
+    p.n = n;
+    p.d = d;
+    p.dv = d;
+    p.causal = causal ? 1 : 0;
+    p.v2 = 1;
+    p.heads_q = Hq;
+    p.heads_kv = Hkv;
+    p.units_per_batch = G;
+    p.group = Hq / Hkv;
+    p.rows_total = static_cast<long long>(B) * G * n;
+    cudaError_t e = da::launch_simt_f32(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_forward (f32) launch");
+    g_launches.fetch_add(1);
+    return ok();
+  }
+
+  if (d != 128) return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_v2_forward: bf16 needs d = 128 (got %d)", d);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_v2_forward: bf16 tensors must be 16-byte aligned");
+  da::TwoPassParams p;
+  memset(&p, 0, sizeof(p));
+  if ((st = make_map(&p.tm_q1, q, B, n, Hq, d, 128)) != DIFFATTN_OK) return st;
+  p.tm_q2 = p.tm_q1;
+  if ((st = make_map(&p.tm_k1, k, B, n, Hkv, d, 64)) != DIFFATTN_OK) return st;
+  p.tm_k2 = p.tm_k1;
+  if ((st = make_map(&p.tm_v, v, B, n, Hkv, d, 64)) != DIFFATTN_OK) return st;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lam_logits = lam_logits;
+  p.sb = sb;
+  p.st = st_;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 * scale);
+  p.norm_mult = 1.f;
+  p.eps = 0.f;
+  p.B = B;
+  p.n = n;
+  p.causal = causal ? 1 : 0;
+  p.units_per_batch = G;
+  p.group = Hq / Hkv;
+  p.num_q_tiles = (n + 127) / 128;
+  // K/V bytes per pair: the pairs of one KV head share its stream.
+  p.order = pick_order(static_cast<long long>(B) * Hkv, n, 2 * d * 2);
+  p.status = status;
+  const long long grid = static_cast<long long>(p.num_q_tiles) * B * G;
+  if (grid > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_forward: too many tiles");
+  cudaError_t e = da::launch_twopass_v2_d128(p, static_cast<int>(grid), s);
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_forward (bf16) launch");
+  g_launches.fetch_add(1);
+  return ok();
+}
+
+diffattn_status diffattn_device_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int* status = nullptr;
+  diffattn_status st = status_word(&status);
+  if (st != DIFFATTN_OK) return st;
+  int host = 0;
+  e = cudaMemcpy(&host, status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read status word");
+  const int zero = 0;
+  e = cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+  if (host == DIFFATTN_ERR_TIMEOUT) return fail(DIFFATTN_ERR_TIMEOUT, "a bounded in-kernel wait ran out");
+  if (host != 0) return fail(DIFFATTN_ERR_CUDA, "device status word holds %d", host);
+  return ok();
+}
+
+const char* diffattn_last_error(void) { return t_last_error.c_str(); }
+
+diffattn_status diffattn_debug_wait_timeout(long long budget_ns, void* stream) {
+  if (budget_ns < 1 || budget_ns > 1000000000ll)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_debug_wait_timeout: budget must be in [1, 1e9] ns");
+  int* status = nullptr;
+  diffattn_status st = status_word(&status);
+  if (st != DIFFATTN_OK) return st;
+  cudaError_t e = da::launch_wait_selftest(static_cast<unsigned long long>(budget_ns), status,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_debug_wait_timeout launch");
+  g_launches.fetch_add(1);
+  return ok();
+}
+
+long long diffattn_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

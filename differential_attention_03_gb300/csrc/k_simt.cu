@@ -1,0 +1,18 @@
+#include "launch.h"
+#include "simt.cuh"
+namespace da {
+cudaError_t launch_simt_f32(const SimtParams& p, cudaStream_t s) {
+  const long long blocks = (p.rows_total + kSimtWarps - 1) / kSimtWarps;
+  simt_fwd_f32_kernel<<<static_cast<unsigned>(blocks), kSimtWarps * 32, 0, s>>>(p);
+  return cudaGetLastError();
+}
+cudaError_t launch_lambda_reparam(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
+                                  int dim, float lambda_init, float* out, cudaStream_t s) {
+  lambda_reparam_kernel<<<1, 32, 0, s>>>(lq1, lk1, lq2, lk2, dim, lambda_init, out);
+  return cudaGetLastError();
+}
+cudaError_t launch_wait_selftest(unsigned long long budget_ns, int* status, cudaStream_t s) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(budget_ns, status);
+  return cudaGetLastError();
+}
+}  // namespace da

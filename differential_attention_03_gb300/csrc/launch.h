@@ -1,0 +1,23 @@
+// Host-side launchers of the kernel instantiations (one translation unit each,
+// so that they compile in parallel).  Each returns the cudaError_t of the launch.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "params.h"
+
+namespace da {
+
+// V1, d = 64, value width 128.
+cudaError_t launch_twopass_v1_d64(const TwoPassParams& p, int grid, cudaStream_t s);
+// V1, d = 128, value width 256.
+cudaError_t launch_twopass_v1_d128(const TwoPassParams& p, int grid, cudaStream_t s);
+// V2, d = 128 (query/key/value width 128), one K/V head per query-head pair.
+cudaError_t launch_twopass_v2_d128(const TwoPassParams& p, int grid, cudaStream_t s);
+
+cudaError_t launch_simt_f32(const SimtParams& p, cudaStream_t s);
+cudaError_t launch_lambda_reparam(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
+                                  int dim, float lambda_init, float* out, cudaStream_t s);
+cudaError_t launch_wait_selftest(unsigned long long budget_ns, int* status, cudaStream_t s);
+
+}  // namespace da

@@ -1,0 +1,54 @@
+// Kernel parameter blocks shared by the launchers and the host API.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+namespace da {
+
+enum : int { kEpiRmsNorm = 0, kEpiV2 = 1 };
+
+struct TwoPassParams {
+  CUtensorMap tm_q1;  // 4-D maps over BSHD tensors: dims {W, heads, n, B}
+  CUtensorMap tm_q2;
+  CUtensorMap tm_k1;
+  CUtensorMap tm_k2;
+  CUtensorMap tm_v;
+  __nv_bfloat16* out;       // [B, n, units_per_batch, DV]
+  const float* lambda;      // V1: device scalar lambda
+  const float* gamma;       // V1: [DV] or nullptr
+  const float* lam_logits;  // V2: logit of (b, t, g) at b*sb + t*st + g
+  long long sb, st;
+  float scale_log2;  // softmax scale * log2(e)
+  float norm_mult;   // V1: 1 - lambda_init
+  float eps;         // V1: RMSNorm epsilon
+  int B, n, causal;
+  int units_per_batch;  // V1: H; V2: Hq / 2
+  int group;            // V2: query heads per KV head
+  int num_q_tiles;
+  int order;  // 0: unit-major tile order, 1: query-tile-major
+  int* status;
+};
+
+struct SimtParams {
+  const float* q1;  // V1: [B, n, H, d]; V2: q [B, n, Hq, d] (q1 == q2)
+  const float* q2;
+  const float* k1;  // V1: [B, n, H, d]; V2: k [B, n, Hkv, d] (k1 == k2)
+  const float* k2;
+  const float* v;   // V1: [B, n, H, 2d]; V2: [B, n, Hkv, d]
+  float* out;       // [B, n, units_per_batch, dv]
+  const float* lambda;      // V1 device scalar
+  const float* gamma;       // V1 [dv] or nullptr
+  const float* lam_logits;  // V2
+  long long sb, st;
+  float scale, norm_mult, eps;
+  int B, n, d, dv, causal, v2;
+  int heads_q, heads_kv, units_per_batch, group;
+  long long rows_total;
+};
+
+constexpr int kSimtMaxD = 256;
+constexpr int kSimtMaxVPerLane = 16;  // value width <= 512
+constexpr int kSimtWarps = 4;
+
+}  // namespace da

@@ -1,0 +1,161 @@
+/*
+ * diffattn.h -- C ABI of the GB300 (sm_103a) multi-head differential-attention
+ * forward library (libdiffattn.so).
+ *
+ * The operator, as the pages on the Differential Transformer state it:
+ *
+ *   DiffAttn(Q1,Q2,K1,K2,V) = (softmax(Q1 K1^T / sqrt d) - lambda softmax(Q2 K2^T / sqrt d)) V
+ *
+ * ("Differential Transformer", ultralytics.com glossary, section "How
+ * differential attention works", with its worked example; "Differential
+ * Transformer V2 (DIFF V2) 기술적 혁신 분석", section "차등 어텐션 메커니즘의 핵심 원리").
+ *
+ * Conventions shared by every entry point
+ *  - Layout is BSHD, contiguous, row-major: element (b, t, h, c) of a tensor
+ *    [B, n, H, W] sits at ((b*n + t)*H + h)*W + c.
+ *  - Every pointer argument except those documented as host values is a
+ *    DEVICE pointer owned by the caller.  The library allocates no device
+ *    memory and keeps no pointer after the call returns.
+ *  - All entry points are asynchronous on `stream` (a cudaStream_t passed as
+ *    void*; NULL means the legacy default stream), except
+ *    diffattn_lambda_init (pure host) and diffattn_device_status (syncs).
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns a non-zero status and leaves all buffers untouched.
+ *    diffattn_last_error() then returns a message (thread-local).
+ *  - Kernels never trap.  Every wait inside a kernel is bounded; a wait that
+ *    runs out records DIFFATTN_ERR_TIMEOUT in a device status word that
+ *    diffattn_device_status() reads and clears.
+ */
+#ifndef DIFFATTN_H
+#define DIFFATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DIFFATTN_OK = 0,
+    DIFFATTN_ERR_NULL = 1,        /* a required pointer is NULL                      */
+    DIFFATTN_ERR_SHAPE = 2,       /* a size is negative, zero where it may not be,
+                                     or inconsistent (e.g. Hq not a multiple of Hkv) */
+    DIFFATTN_ERR_ALIGN = 3,       /* a bf16 tensor is not 16-byte aligned            */
+    DIFFATTN_ERR_DTYPE = 4,       /* unknown dtype code                              */
+    DIFFATTN_ERR_UNSUPPORTED = 5, /* valid but not implemented (e.g. bf16 with d not
+                                     in {64, 128})                                   */
+    DIFFATTN_ERR_CUDA = 6,        /* a CUDA runtime/driver call failed               */
+    DIFFATTN_ERR_TIMEOUT = 7      /* a bounded in-kernel wait ran out                */
+} diffattn_status;
+
+typedef enum {
+    DIFFATTN_F32 = 0,  /* fp32 in, fp32 out, fp32 arithmetic (CUDA-core kernel)         */
+    DIFFATTN_BF16 = 1  /* bf16 in, bf16 out; fp32 accumulation on tcgen05 tensor cores */
+} diffattn_dtype;
+
+/*
+ * lambda_init for the 1-based layer index l: 0.8 - 0.6 * exp(-0.3 * (l - 1)).
+ * Differential Transformer news article (esgcw.com.cn), section "差分注意力";
+ * DIFF V2 analysis page, section "DIFF V1의 한계와 문제점".
+ * Pure host function.  Returns NaN for l < 1.  A constant lambda_init (the
+ * article's alternative, e.g. 0.8 in every layer) is passed directly as a
+ * float to the calls below.
+ */
+float diffattn_lambda_init(int layer_index);
+
+/*
+ * lambda = exp(<lq1, lk1>) - exp(<lq2, lk2>) + lambda_init, computed on the
+ * device in fp32 by one warp (the re-parameterisation of the learnable scalar;
+ * news article section "差分注意力", DIFF V2 analysis page section 5 of
+ * "DIFF V2의 핵심 기술적 혁신").
+ *   lq1, lk1, lq2, lk2 : device fp32 vectors of length `dim` (dim >= 1).
+ *   lambda_out         : device fp32 scalar, written by the kernel.  Pass it to
+ *                        diffattn_forward on the same stream; no host sync.
+ * Errors: NULL pointers -> ERR_NULL; dim < 1 -> ERR_SHAPE.
+ */
+diffattn_status lambda_reparam(const float* lq1, const float* lk1, const float* lq2,
+                               const float* lk2, int dim, float lambda_init,
+                               float* lambda_out, void* stream);
+
+/*
+ * Multi-head DIFF V1 forward with the per-head RMSNorm (the pages' "GroupNorm")
+ * scaled by the fixed multiplier (1 - lambda_init):
+ *
+ *   O   = (softmax(Q1 K1^T / sqrt d) - lambda softmax(Q2 K2^T / sqrt d)) V   per (b, h)
+ *   out = (1 - lambda_init) * gamma * O / sqrt(mean_c O^2 + eps)             per (b, t, h)
+ *
+ * (news article section "差分注意力": multi-head, lambda shared across the heads
+ * of a layer, LN = RMSNorm per head, concat along channels.)
+ *   dt          : DIFFATTN_BF16 or DIFFATTN_F32; q*, k*, v and out share it.
+ *   B, H, n, d  : batch, diff heads, tokens, per-map query/key width.  The
+ *                 value width is 2d.  bf16 needs d in {64, 128}; f32 needs
+ *                 d in [1, 256].  n = 0 or B = 0 or H = 0 is a no-op.
+ *   q1, q2, k1, k2 : [B, n, H, d];  v, out : [B, n, H, 2d].
+ *   lambda      : device fp32 scalar (e.g. written by lambda_reparam).
+ *   lambda_init : host float, the fixed norm multiplier is (1 - lambda_init).
+ *   gamma       : device fp32 [2d] RMSNorm weight shared by all heads, or NULL
+ *                 for all ones.
+ *   eps         : RMSNorm epsilon; eps <= 0 selects 1e-5.
+ *   causal      : non-zero: query t sees key j iff j <= t.
+ * Errors: NULL -> ERR_NULL; bad sizes -> ERR_SHAPE; bf16 pointers not 16-byte
+ * aligned -> ERR_ALIGN; unsupported d -> ERR_UNSUPPORTED; launch failure ->
+ * ERR_CUDA.  `out` may not alias an input.
+ */
+diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d,
+                                 const void* q1, const void* q2, const void* k1,
+                                 const void* k2, const void* v, const float* lambda,
+                                 float lambda_init, const float* gamma, float eps,
+                                 int causal, void* out, void* stream);
+
+/*
+ * DIFF V2 forward (DIFF V2 analysis page, sections "2. 커스텀 커널 제거",
+ * "5. 간소화된 λ 매개변수화" and "GQA와의 호환성"): 2h query heads over h KV
+ * heads, grouped-query attention, each even/odd pair of query heads inside
+ * one KV group differenced with a sigmoid lambda, no norm:
+ *
+ *   A_j   = softmax(q_j K_kv(j)^T * scale) V_kv(j),   kv(j) = j / (Hq / Hkv)
+ *   out_g = A_{2g} - sigmoid(logit[b, t, g]) * A_{2g+1},   g < Hq/2
+ *
+ *   q   : [B, n, Hq, d];  k, v : [B, n, Hkv, d];  out : [B, n, Hq/2, d].
+ *   Hq even, Hq % Hkv == 0 and (Hq / Hkv) even (so a pair never straddles
+ *   two KV heads).  bf16 needs d = 128; f32 needs d in [1, 256].
+ *   lam_logits : device fp32; the logit of (b, t, g) is
+ *                lam_logits[b*sb + t*st + g]  (sb = st = 0: one logit per pair).
+ *   softmax_scale : <= 0 selects 1/sqrt(d).
+ * Errors as for diffattn_forward.
+ */
+diffattn_status diffattn_v2_forward(diffattn_dtype dt, int B, int Hq, int Hkv, int n, int d,
+                                    const void* q, const void* k, const void* v,
+                                    const float* lam_logits, long long sb, long long st,
+                                    float softmax_scale, int causal, void* out,
+                                    void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word on the current device.  Returns DIFFATTN_OK, DIFFATTN_ERR_TIMEOUT if a
+ * bounded in-kernel wait ran out since the last call, or DIFFATTN_ERR_CUDA if
+ * the stream reported an error.
+ */
+diffattn_status diffattn_device_status(void* stream);
+
+/* Message for the last non-OK status returned on this host thread ("" if none). */
+const char* diffattn_last_error(void);
+
+/*
+ * Diagnostics: launches one CTA whose thread waits on an mbarrier that nothing
+ * arrives on, with a budget of `budget_ns` nanoseconds (1 .. 1e9).  The wait
+ * must run out and record DIFFATTN_ERR_TIMEOUT in the status word; this is how
+ * the bounded-wait path is exercised without hanging a GPU.  No copy is in
+ * flight while it waits.
+ */
+diffattn_status diffattn_debug_wait_timeout(long long budget_ns, void* stream);
+
+/*
+ * Number of kernels the library has launched in this process (all devices).
+ * Lets a caller count the kernels of a timed region.
+ */
+long long diffattn_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DIFFATTN_H */

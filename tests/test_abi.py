@@ -1,0 +1,109 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every
+symbol include/diffattn.h declares, and rejects bad arguments on the host
+before any CUDA call (these calls never reach the device)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from differential_attention_03_gb300 import binding as da
+from differential_attention_03_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "diffattn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return da.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for want in ("diffattn_forward", "diffattn_v2_forward", "lambda_reparam", "diffattn_lambda_init",
+                 "diffattn_device_status", "diffattn_last_error"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared():
+        assert hasattr(L, name), f"{name} not exported"
+
+
+def test_lambda_init_host(L):
+    for l in (1, 4, 12, 20):
+        assert da.lambda_init(l) == pytest.approx(oracle.lambda_init(l), abs=1e-7)
+    import math
+    assert math.isnan(da.lambda_init(0))
+
+
+P = ctypes.c_void_p
+A = P(0x10000)        # 16-byte aligned fake device address (never dereferenced)
+MIS = P(0x10008)      # misaligned fake address
+
+
+def _fwd(L, dt=1, B=1, H=1, n=8, d=64, ptrs=None, lam=A, out=A):
+    q = ptrs or [A] * 5
+    return L.diffattn_forward(dt, B, H, n, d, *q, lam, ctypes.c_float(0.2), None, ctypes.c_float(1e-5), 1,
+                              out, None)
+
+
+def _v2(L, dt=1, B=1, Hq=4, Hkv=2, n=8, d=128, q=A, logits=A, sb=0, st=0):
+    return L.diffattn_v2_forward(dt, B, Hq, Hkv, n, d, q, A, A, logits, sb, st, ctypes.c_float(0.0), 1, A, None)
+
+
+def test_forward_host_validation(L):
+    assert _fwd(L, dt=7) == da.ERR_DTYPE
+    assert _fwd(L, n=-1) == da.ERR_SHAPE
+    assert _fwd(L, d=0) == da.ERR_SHAPE
+    assert _fwd(L, n=0) == da.OK           # empty input: no launch
+    assert _fwd(L, B=0) == da.OK
+    assert _fwd(L, ptrs=[A, None, A, A, A]) == da.ERR_NULL
+    assert _fwd(L, lam=None) == da.ERR_NULL
+    assert _fwd(L, out=None) == da.ERR_NULL
+    assert _fwd(L, d=96) == da.ERR_UNSUPPORTED
+    assert _fwd(L, dt=0, d=300) == da.ERR_UNSUPPORTED
+    assert _fwd(L, ptrs=[A, A, MIS, A, A]) == da.ERR_ALIGN
+    assert _fwd(L, out=MIS) == da.ERR_ALIGN
+    assert b"16-byte" in L.diffattn_last_error()
+
+
+def test_v2_host_validation(L):
+    assert _v2(L, Hq=3, Hkv=1) == da.ERR_SHAPE        # odd query heads
+    assert _v2(L, Hq=6, Hkv=2) == da.ERR_SHAPE        # group of 3 would straddle a pair
+    assert _v2(L, Hq=4, Hkv=3) == da.ERR_SHAPE
+    assert _v2(L, Hkv=0) == da.ERR_SHAPE
+    assert _v2(L, sb=-1) == da.ERR_SHAPE
+    assert _v2(L, n=0) == da.OK
+    assert _v2(L, q=None) == da.ERR_NULL
+    assert _v2(L, logits=None) == da.ERR_NULL
+
+
+def test_lambda_reparam_host_validation(L):
+    assert L.lambda_reparam(A, A, A, None, 8, ctypes.c_float(0.2), A, None) == da.ERR_NULL
+    assert L.lambda_reparam(A, A, A, A, 0, ctypes.c_float(0.2), A, None) == da.ERR_SHAPE
+
+
+def test_debug_wait_budget_validation(L):
+    assert L.diffattn_debug_wait_timeout(0, None) == da.ERR_SHAPE
+    assert L.diffattn_debug_wait_timeout(2 * 10**9, None) == da.ERR_SHAPE
+
+
+def test_product_path_has_no_fallback():
+    """The binding never imports the oracle and raises if the library is missing."""
+    src = open(os.path.join(ROOT, "differential_attention_03_gb300", "binding.py")).read()
+    assert "oracle" not in src.replace("no fallback", "")
+    for f in os.listdir(os.path.join(ROOT, "differential_attention_03_gb300")):
+        if f.endswith(".py"):
+            assert "import oracle" not in open(os.path.join(ROOT, "differential_attention_03_gb300", f)).read()
