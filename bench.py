@@ -60,48 +60,56 @@ def read_peaks():
 
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Polls nvidia-smi from a thread while the timed region runs."""
 
-    def __init__(self, index: int):
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int, period_s: float = 0.05):
+        import threading
         self.index = index
-        self.proc = None
+        self.period = period_s
+        self.rows = []
+        self.stop_evt = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.error = None
+
+    def _run(self):
+        while not self.stop_evt.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                      "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                                     timeout=10).stdout
+                for line in out.splitlines():
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 7:
+                        self.rows.append(parts)
+            except Exception as e:  # noqa: BLE001
+                self.error = str(e)
+                return
+            self.stop_evt.wait(self.period)
 
     def start(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+        self.thread.start()
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
+        self.stop_evt.set()
+        self.thread.join(timeout=15)
         sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
+        for parts in self.rows:
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
+            for name, val in zip(self.NAMES, parts[3:7]):
                 if val.lower() == "active":
                     reasons.add(name)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [self.error or "no samples"], "samples": 0}
+        loaded = [x for x in sm if x > 0.5 * max(sm)] or sm
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
 
@@ -194,47 +202,54 @@ def time_e2e(w, x, da, steps):
 
 
 def cpu_baseline(w, x, budget_s=12.0):
-    """The fp64 oracle as it stands, on a bounded sample of query blocks of the same workload."""
+    """The fp64 oracle as it stands, on a bounded sample of the same workload.
+
+    Units (one (batch, head) for V1, one (batch, head pair) for V2) are taken in
+    order, each with all its query rows in 128-row blocks (heaviest causal
+    blocks first), until the time budget is spent; the value is the
+    algorithmic causal FLOPs of the rows done divided by the time taken.
+    """
     import numpy as np
     import oracle
     cores = len(os.sched_getaffinity(0))
-    rows_done, fl, t0 = 0, 0.0, time.perf_counter()
     n = w.n
-    blocks = list(range(0, n, 128))
-    order = blocks[::-1]  # heaviest causal blocks first, like the GPU
-    b, u = 0, 0
-    if w.kind == "v1":
-        xs = {k: (t[b:b + 1, :, u:u + 1] if t.dim() == 4 else t) for k, t in x.items()}
-        xs = {k: t.cpu() for k, t in xs.items()}
-        lin = oracle.lambda_init(w.layer)
-        lam = oracle.lambda_reparam(xs["lq1"], xs["lk1"], xs["lq2"], xs["lk2"], lin)
-        arrs = {k: oracle.diffattn_oracle._f64(xs[k]) for k in ("q1", "q2", "k1", "k2", "v")}
+    order = list(range(0, n, 128))[::-1]
+    rows_done, units_done, fl = 0, 0, 0.0
+    t0 = time.perf_counter()
+    units = [(b, u) for b in range(w.B) for u in range(w.H if w.kind == "v1" else w.Hq // 2)]
+    for b, u in units:
+        if w.kind == "v1":
+            xs = {k: (t[b:b + 1, :, u:u + 1] if t.dim() == 4 else t).cpu() for k, t in x.items()}
+            lin = oracle.lambda_init(w.layer)
+            lam = oracle.lambda_reparam(xs["lq1"], xs["lk1"], xs["lq2"], xs["lk2"], lin)
+            arrs = {k: oracle.diffattn_oracle._f64(xs[k]) for k in ("q1", "q2", "k1", "k2", "v")}
+        else:
+            kvh = (2 * u) // (w.Hq // w.Hkv)
+            xs = {"q": x["q"][b:b + 1, :, 2 * u:2 * u + 2].cpu(), "k": x["k"][b:b + 1, :, kvh:kvh + 1].cpu(),
+                  "v": x["v"][b:b + 1, :, kvh:kvh + 1].cpu()}
+            arrs = {k: oracle.diffattn_oracle._f64(t) for k, t in xs.items()}
+            lg = np.broadcast_to(x["lam_logits"][u:u + 1].cpu().double().numpy(), (1, n, 1))
         for s in order:
             rows = np.arange(s, min(s + 128, n))
-            oracle.diff_attn_v1(arrs["q1"], arrs["q2"], arrs["k1"], arrs["k2"], arrs["v"], lam, lin,
-                                xs["gamma"], 1e-5, w.causal, rows)
+            if w.kind == "v1":
+                oracle.diff_attn_v1(arrs["q1"], arrs["q2"], arrs["k1"], arrs["k2"], arrs["v"], lam, lin,
+                                    xs["gamma"], 1e-5, w.causal, rows)
+                per = 12.0 * w.d
+            else:
+                oracle.diff_attn_v2(arrs["q"], arrs["k"], arrs["v"], lg, w.causal, rows=rows)
+                per = 8.0 * w.d
             rows_done += rows.size
-            fl += sum(12.0 * w.d * ((r + 1) if w.causal else n) for r in rows)
+            fl += float(sum(per * ((r + 1) if w.causal else n) for r in rows))
             if time.perf_counter() - t0 > budget_s:
                 break
-    else:
-        g = w.Hq // w.Hkv
-        xs = {"q": x["q"][0:1, :, 0:2].cpu(), "k": x["k"][0:1, :, 0:1].cpu(), "v": x["v"][0:1, :, 0:1].cpu()}
-        arrs = {k: oracle.diffattn_oracle._f64(t) for k, t in xs.items()}
-        lg = np.broadcast_to(x["lam_logits"][0:1].cpu().double().numpy(), (1, n, 1))
-        for s in order:
-            rows = np.arange(s, min(s + 128, n))
-            oracle.diff_attn_v2(arrs["q"], arrs["k"], arrs["v"], lg, w.causal, rows=rows)
-            rows_done += rows.size
-            fl += sum(2 * 4.0 * w.d * ((r + 1) if w.causal else n) for r in rows)
-            if time.perf_counter() - t0 > budget_s:
-                break
-        del g
+        units_done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
     dt = time.perf_counter() - t0
     unit = "head pair" if w.kind == "v2" else "head"
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{rows_done} of {n} query rows of one (batch, {unit}) unit, heaviest 128-row blocks first, "
-                      f"{dt:.1f} s; algorithmic causal FLOPs of those rows",
+            "sample": f"{rows_done} query rows over {units_done} (batch, {unit}) units of {len(units)}, "
+                      f"heaviest 128-row blocks first, {dt:.1f} s; algorithmic causal FLOPs of those rows",
             "seconds": dt}
 
 
@@ -266,9 +281,9 @@ def run_ours(args):
         return make_v1(w, "cuda") if w.kind == "v1" else make_v2(w, "cuda")
 
     w = WORKLOADS[args.config]
-    x = inputs(w)
     sampler = ClockSampler(local)
-    sampler.start()
+    sampler.start()  # polls from before the warm-up to the end of the timed steps
+    x = inputs(w)
     res = time_device(w, x, da, args.steps, args.warmup, flush, dist)
     clocks = sampler.stop()
     step_ms = torch.tensor([res["step_ms"], res["kernel_ms"]], device="cuda", dtype=torch.float64)
@@ -373,7 +388,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
