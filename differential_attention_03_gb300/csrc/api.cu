@@ -11,7 +11,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/diffattn.h"
+#include "diffattn.h"
 #include "launch.h"
 
 // Device status word (one per device that loads the library).  Kernels record
@@ -191,8 +191,9 @@ diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d, 
   memset(&p, 0, sizeof(p));
   if ((st = make_map(&p.tm_q1, q1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
   if ((st = make_map(&p.tm_q2, q2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
-  if ((st = make_map(&p.tm_k1, k1, B, n, H, d, 64)) != DIFFATTN_OK) return st;
-  if ((st = make_map(&p.tm_k2, k2, B, n, H, d, 64)) != DIFFATTN_OK) return st;
+  // Query and key tiles are 128 rows; a value tile is split into two 64-row slots.
+  if ((st = make_map(&p.tm_k1, k1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&p.tm_k2, k2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
   if ((st = make_map(&p.tm_v, v, B, n, H, dv, 64)) != DIFFATTN_OK) return st;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lambda = lambda;
@@ -274,9 +275,10 @@ diffattn_status diffattn_v2_forward(diffattn_dtype dt, int B, int Hq, int Hkv, i
   memset(&p, 0, sizeof(p));
   if ((st = make_map(&p.tm_q1, q, B, n, Hq, d, 128)) != DIFFATTN_OK) return st;
   p.tm_q2 = p.tm_q1;
-  if ((st = make_map(&p.tm_k1, k, B, n, Hkv, d, 64)) != DIFFATTN_OK) return st;
+  // Key and value tiles are 128 rows (one ring slot each).
+  if ((st = make_map(&p.tm_k1, k, B, n, Hkv, d, 128)) != DIFFATTN_OK) return st;
   p.tm_k2 = p.tm_k1;
-  if ((st = make_map(&p.tm_v, v, B, n, Hkv, d, 64)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&p.tm_v, v, B, n, Hkv, d, 128)) != DIFFATTN_OK) return st;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lam_logits = lam_logits;
   p.sb = sb;

@@ -21,18 +21,31 @@
 // accumulator instead of two, which is what lets d = 128 / V = 256 fit the
 // 512 TMEM columns of an SM; it also removes every rescale of O.
 //
-// Roles (384 threads, one CTA per SM):
-//   warp 0      TMA producer: Q_1, Q_2 once; K_1, K_2 (+ V in sweep 2) per
-//               64-key tile into a STAGES-deep ring of shared memory.
+// Tiles are 128 queries x 128 keys: every QK^T MMA is M128 N128 K16, the
+// narrowest shape that runs at the full tensor rate on this part (N = 64 reads
+// the Q operand from shared memory twice as often per flop and runs at 2/3).
+// The two maps get separate TMEM buffers (A for S_1, B for S_2), so the QK^T
+// of one map runs while the softmax warps read the other.  Sweep-2 issue order
+//     QK2(j+1)  PV(j)  QK1(j+1)  QK2(j+2)  PV(j+1) ...
+// lets the softmax start the S_2 half of tile j+1 while PV(j) runs.
+//
+// Roles (640 threads, one CTA per SM):
+//   warp 0      TMA producer: Q_1, Q_2 once, then K_1 / K_2 / V tiles into a
+//               ring of NSLOT equal slots, in exactly the order warp 1
+//               consumes them; a slot is released by a tcgen05.commit after
+//               the last MMA reading it.
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer.
-//   warps 4-11  two warpgroups; thread = one query row (TMEM lane).
-//               Sweep 1: warpgroup r keeps the statistics of map r.
-//               Sweep 2: warpgroup w owns key columns [32w, 32w+32) of both
-//               maps, writes its bf16 P into TMEM over its own S_1 columns.
-//               Epilogue: warpgroup w normalises/stores channels of half w.
-// TMEM (512 columns x 128 lanes, fp32): O at [0, DV); S stage s at
-// DV + 128 s: S_1 in [0, 64), S_2 in [64, 128) of the stage; P of stage s
-// (bf16 pairs) at stage columns [0, 16) and [32, 48).
+//   warps 4-19  four softmax warpgroups; thread = one query row (TMEM lane).
+//               Sweep 1: warpgroup w keeps running (max, sum) of map w/2 over
+//               key columns [64 (w%2), +64) of each tile.
+//               Sweep 2: warpgroup w owns key columns [32 w, +32) of both
+//               maps and writes its bf16 P over its own S_1 columns.
+//               Epilogue: warpgroup w normalises/stores channels [w DV/4, +DV/4).
+// TMEM (512 columns x 128 lanes, fp32): O at [0, DV), A at [DV, DV+128),
+// B at [DV+128, DV+256).  P (bf16 pairs) of key columns 32 w .. 32 w + 31 sits
+// in A columns 32 w .. 32 w + 15.  Between the sweeps the per-warpgroup
+// statistics travel through the (still unused) O columns; the epilogue's sums
+// of squares through the A columns.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -42,41 +55,94 @@
 
 namespace da {
 
-
-template <int D, int DV, bool SHARED_K, int EPI, int STAGES>
+template <int D, int DV, bool SHARED_K, int EPI, int NSLOT>
 struct TwoPassCfg {
-  static constexpr int BM = 128;  // queries per CTA (TMEM lanes)
-  static constexpr int BN = 64;   // keys per tile
-  static constexpr int NTHREADS = 384;
+  static constexpr int BM = 128;   // queries per CTA (TMEM lanes)
+  static constexpr int BN = 128;   // keys per tile
+  static constexpr int NSMWG = 4;  // softmax warpgroups
+  static constexpr int NTHREADS = (4 + 4 * NSMWG) * 32;
   static constexpr int QB = D / 64;  // 128-byte swizzle boxes across a Q/K row
   static constexpr int VB = DV / 64;
   static constexpr int Q_TILE = BM * D * 2;
   static constexpr int K_TILE = BN * D * 2;
   static constexpr int V_TILE = BN * DV * 2;
-  static constexpr int NK = SHARED_K ? 1 : 2;
-  static constexpr int STAGE = NK * K_TILE + V_TILE;
+  static constexpr int SLOT = K_TILE;
+  static constexpr int VF = V_TILE / SLOT;  // slots per V tile
+  static constexpr int VKEYS = BN / VF;     // keys per V slot
   static constexpr int OFF_Q1 = 0;
   static constexpr int OFF_Q2 = Q_TILE;
-  static constexpr int OFF_STAGES = 2 * Q_TILE;
-  static constexpr int OFF_BARS = OFF_STAGES + STAGES * STAGE;
-  static constexpr int NBARS = 2 + 2 * STAGES + 4;
+  static constexpr int OFF_RING = 2 * Q_TILE;
+  static constexpr int OFF_BARS = OFF_RING + NSLOT * SLOT;
+  static constexpr int NBARS = 2 + 2 * NSLOT + 6;
   static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
-  static constexpr int OFF_STATS = ((OFF_MISC + 16) + 15) / 16 * 16;
-  static constexpr int STATS_BYTES = 6 * 128 * 4;  // m[2][128], l[2][128], ss[2][128]
-  static constexpr int SMEM_BYTES = OFF_STATS + STATS_BYTES + 1024;  // + 1 KB alignment slack
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TM_O = 0;
-  static constexpr uint32_t TM_S = DV;
+  static constexpr uint32_t TM_A = DV;
+  static constexpr uint32_t TM_B = DV + 128;
   static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(BM, DV, false, true);
   static_assert(D == 64 || D == 128, "query/key width");
-  static_assert(DV % 64 == 0 && DV <= 256 && DV + 256 <= 512, "value width");
-  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  static_assert(DV % 64 == 0 && DV <= 256, "value width");
+  static_assert(V_TILE % SLOT == 0 && (VF == 1 || VF == 2), "value tile split");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(NSLOT >= 4, "ring depth");
 };
 
-template <int D, int DV, bool SHARED_K, int EPI, int STAGES>
-__global__ void __launch_bounds__(384, 1) twopass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
-  using C = TwoPassCfg<D, DV, SHARED_K, EPI, STAGES>;
+// Merge two partial softmax states (max in the scaled log2 domain, sum).
+__device__ __forceinline__ void merge_state(float& m, float& l, float m2, float l2) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;
+  l = l * ex2(m - mn) + l2 * ex2(m2 - mn);
+  m = mn;
+}
+
+// Running (max, sum) of 64 scores of one row (scaled log2 domain); columns at
+// or beyond nvis are masked out.
+__device__ __forceinline__ void row_stats64(uint32_t (&r0)[32], uint32_t (&r1)[32], int nvis, float sc, float& m,
+                                            float& l) {
+  if (nvis < 64) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      if (c >= nvis) r0[c] = __float_as_uint(-INFINITY);
+      if (c + 32 >= nvis) r1[c] = __float_as_uint(-INFINITY);
+    }
+  }
+  float t[22];
+#pragma unroll
+  for (int c = 0; c < 10; ++c)
+    t[c] = max3(__uint_as_float(r0[3 * c]), __uint_as_float(r0[3 * c + 1]), __uint_as_float(r0[3 * c + 2]));
+  t[10] = max3(__uint_as_float(r0[30]), __uint_as_float(r0[31]), __uint_as_float(r1[0]));
+#pragma unroll
+  for (int c = 0; c < 10; ++c)
+    t[11 + c] = max3(__uint_as_float(r1[3 * c + 1]), __uint_as_float(r1[3 * c + 2]), __uint_as_float(r1[3 * c + 3]));
+  t[21] = __uint_as_float(r1[31]);
+#pragma unroll
+  for (int c = 0; c < 7; ++c) t[c] = max3(t[3 * c], t[3 * c + 1], t[3 * c + 2]);
+  t[7] = t[21];
+  const float mx = max3(max3(t[0], t[1], t[2]), max3(t[3], t[4], t[5]), fmaxf(t[6], t[7]));
+  const float m_new = fmaxf(m, mx * sc);
+  const float base = (m_new == -INFINITY) ? 0.f : m_new;
+  const uint64_t sc2 = f2pack(sc, sc);
+  const uint64_t nb2 = f2pack(-base, -base);
+  uint64_t acc0 = 0, acc1 = 0;
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    float a0, a1, b0, b1;
+    f2unpack(fma2(f2pack(__uint_as_float(r0[c]), __uint_as_float(r0[c + 1])), sc2, nb2), a0, a1);
+    f2unpack(fma2(f2pack(__uint_as_float(r1[c]), __uint_as_float(r1[c + 1])), sc2, nb2), b0, b1);
+    acc0 = add2(acc0, f2pack(ex2(a0), ex2(a1)));
+    acc1 = add2(acc1, f2pack(ex2(b0), ex2(b1)));
+  }
+  float s0, s1;
+  f2unpack(add2(acc0, acc1), s0, s1);
+  l = l * ex2(m - base) + (s0 + s1);
+  m = m_new;
+}
+
+template <int D, int DV, bool SHARED_K, int EPI, int NSLOT>
+__global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
+  using C = TwoPassCfg<D, DV, SHARED_K, EPI, NSLOT>;
   constexpr int BM = C::BM, BN = C::BN;
 
   extern __shared__ uint8_t smem_raw[];
@@ -88,15 +154,16 @@ __global__ void __launch_bounds__(384, 1) twopass_fwd_kernel(const __grid_consta
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
   uint64_t* q_full = bars + 0;
   uint64_t* o_full = bars + 1;
-  uint64_t* kv_full = bars + 2;
-  uint64_t* kv_empty = bars + 2 + STAGES;
-  uint64_t* s_full = bars + 2 + 2 * STAGES;
-  uint64_t* s_free = s_full + 2;
+  uint64_t* full = bars + 2;             // [NSLOT] slot loaded
+  uint64_t* empty = full + NSLOT;        // [NSLOT] slot released by the MMAs
+  uint64_t* a_full = empty + NSLOT;      // S_1 of the current tile in TMEM buffer A
+  uint64_t* b_full = a_full + 1;         // S_2 of the current tile in TMEM buffer B
+  uint64_t* a_free1 = b_full + 1;        // sweep 1: map-1 warps have read A
+  uint64_t* b_free1 = a_free1 + 1;       // sweep 1: map-2 warps have read B
+  uint64_t* b_free2 = b_free1 + 1;       // sweep 2: all softmax warps have read B
+  uint64_t* p_ready = b_free2 + 1;       // sweep 2: P of the tile is in buffer A
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  float* stat_m = reinterpret_cast<float*>(smem + C::OFF_STATS);
-  float* stat_l = stat_m + 256;
-  float* stat_ss = stat_m + 512;
 
   // ---- which tile this CTA owns
   const int units = p.B * p.units_per_batch;
@@ -121,20 +188,21 @@ __global__ void __launch_bounds__(384, 1) twopass_fwd_kernel(const __grid_consta
   const int q0 = qt * BM;
   const int kv_end = p.causal ? min(p.n, q0 + BM) : p.n;
   const int T = (kv_end + BN - 1) / BN;  // key tiles per sweep (>= 1)
-  const int NI = 2 * T;
 
   // ---- set-up
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(o_full, 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 8);  // one arrival per softmax warp
-    }
+    mbar_init(a_full, 1);
+    mbar_init(b_full, 1);
+    mbar_init(a_free1, 8);  // the 8 warps of warpgroups 0-1
+    mbar_init(b_free1, 8);  // the 8 warps of warpgroups 2-3
+    mbar_init(b_free2, 4 * C::NSMWG);
+    mbar_init(p_ready, 4 * C::NSMWG);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -161,150 +229,221 @@ __global__ void __launch_bounds__(384, 1) twopass_fwd_kernel(const __grid_consta
         tma_load_4d(smem + C::OFF_Q1 + bx * BM * 128, &p.tm_q1, q_full, bx * 64, hq1, q0, b);
         tma_load_4d(smem + C::OFF_Q2 + bx * BM * 128, &p.tm_q2, q_full, bx * 64, hq2, q0, b);
       }
-      int issued = 0;
-      for (int it = 0; it < NI; ++it) {
-        const int st = it % STAGES;
-        const uint32_t use = static_cast<uint32_t>(it / STAGES);
-        if (use > 0 && !mbar_wait(&kv_empty[st], (use - 1) & 1u, ab)) break;
-        const bool sweep2 = it >= T;
-        const int j = sweep2 ? it - T : it;
-        uint8_t* stage = smem + C::OFF_STAGES + st * C::STAGE;
-        mbar_arrive_expect_tx(&kv_full[st], C::NK * C::K_TILE + (sweep2 ? C::V_TILE : 0));
-        for (int bx = 0; bx < C::QB; ++bx)
-          tma_load_4d(stage + bx * BN * 128, &p.tm_k1, &kv_full[st], bx * 64, hk, j * BN, b);
-        if (!SHARED_K)
-          for (int bx = 0; bx < C::QB; ++bx)
-            tma_load_4d(stage + C::K_TILE + bx * BN * 128, &p.tm_k2, &kv_full[st], bx * 64, hk, j * BN, b);
-        if (sweep2)
-          for (int bx = 0; bx < C::VB; ++bx)
-            tma_load_4d(stage + C::NK * C::K_TILE + bx * BN * 128, &p.tm_v, &kv_full[st], bx * 64, hk, j * BN,
-                        b);
-        issued = it + 1;
+      int fill = 0;
+      bool ok = true;
+      // One slot fill: `nbox` boxes of [rows][64 columns] at key row `key0`.
+      auto load = [&](const CUtensorMap* map, int key0, int rows, int nbox) {
+        if (!ok) return;
+        const int s = fill % NSLOT;
+        const uint32_t use = static_cast<uint32_t>(fill / NSLOT);
+        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, ab)) {
+          ok = false;
+          return;
+        }
+        uint8_t* dst = smem + C::OFF_RING + s * C::SLOT;
+        mbar_arrive_expect_tx(&full[s], C::SLOT);
+        for (int bx = 0; bx < nbox; ++bx) tma_load_4d(dst + bx * rows * 128, map, &full[s], bx * 64, hk, key0, b);
+        ++fill;
+      };
+      auto load_k1 = [&](int j) { load(&p.tm_k1, j * BN, BN, C::QB); };
+      auto load_k2 = [&](int j) { load(&p.tm_k2, j * BN, BN, C::QB); };
+      auto load_v = [&](int j) {
+        for (int part = 0; part < C::VF; ++part) load(&p.tm_v, j * BN + part * C::VKEYS, C::VKEYS, C::VB);
+      };
+      for (int j = 0; j < T; ++j) {  // sweep 1
+        load_k1(j);
+        if (!SHARED_K) load_k2(j);
+      }
+      if (SHARED_K) {  // sweep 2
+        load_k1(0);
+      } else {
+        load_k2(0);
+        load_k1(0);
+      }
+      for (int j = 0; j < T; ++j) {
+        if (j + 1 < T) SHARED_K ? load_k1(j + 1) : load_k2(j + 1);
+        load_v(j);
+        if (j + 1 < T && !SHARED_K) load_k1(j + 1);
       }
       if (*ab.flag) {
         // Aborted: let the copies already issued land before the CTA exits.
         mbar_wait_drain(q_full, 0, kWaitBudgetNs);
-        for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
-          mbar_wait_drain(&kv_full[it % STAGES], static_cast<uint32_t>(it / STAGES) & 1u, kWaitBudgetNs);
+        for (int f = (fill > NSLOT ? fill - NSLOT : 0); f < fill; ++f)
+          mbar_wait_drain(&full[f % NSLOT], static_cast<uint32_t>(f / NSLOT) & 1u, kWaitBudgetNs);
       }
     }
   } else if (warp == 1) {
     // =============================================================== MMA issuer
     if (lane == 0) {
-      const uint32_t sQ1 = smem_u32(smem + C::OFF_Q1);
-      const uint32_t sQ2 = smem_u32(smem + C::OFF_Q2);
-      const uint32_t sStages = smem_u32(smem + C::OFF_STAGES);
+      // Descriptors are built once; a k-step or a ring slot only adds its
+      // byte offset >> 4 to the start-address field (addresses stay below
+      // 256 KB, so the 14-bit field never carries into the next one).
+      const uint64_t dQ1 = sdesc_sw128(smem_u32(smem + C::OFF_Q1), 16, 1024);
+      const uint64_t dQ2 = sdesc_sw128(smem_u32(smem + C::OFF_Q2), 16, 1024);
+      const uint64_t dRingK = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
+      const uint64_t dRingV = sdesc_sw128(smem_u32(smem + C::OFF_RING), C::VKEYS * 128, 1024);
+      const uint32_t tA = tmem + C::TM_A, tB = tmem + C::TM_B, tO = tmem + C::TM_O;
+      int cons = 0;
+      uint32_t n_afree1 = 0, n_bfree1 = 0, n_bfree2 = 0, n_pready = 0;
       bool ok = mbar_wait(q_full, 0, ab);
       tc_fence_after();
-
-      auto issue_qk = [&](int it) -> bool {
-        const int st = it % STAGES;
-        if (!mbar_wait(&kv_full[st], static_cast<uint32_t>(it / STAGES) & 1u, ab)) return false;
+      auto acquire = [&](int& s) -> bool {
+        s = cons % NSLOT;
+        const uint32_t use = static_cast<uint32_t>(cons / NSLOT);
+        ++cons;
+        if (!mbar_wait(&full[s], use & 1u, ab)) return false;
         tc_fence_after();
-        const int s = it & 1;
-        const uint32_t dS1 = tmem + C::TM_S + 128u * s;
-        const uint32_t dS2 = dS1 + 64u;
-        const uint32_t k1 = sStages + st * C::STAGE;
-        const uint32_t k2 = SHARED_K ? k1 : k1 + C::K_TILE;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t oq = (k >> 2) * (BM * 128) + (k & 3) * 32;
-          const uint32_t ok_ = (k >> 2) * (BN * 128) + (k & 3) * 32;
-          mma_ss(dS1, sdesc_sw128(sQ1 + oq, 16, 1024), sdesc_sw128(k1 + ok_, 16, 1024), C::IDESC_QK, k > 0);
-        }
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t oq = (k >> 2) * (BM * 128) + (k & 3) * 32;
-          const uint32_t ok_ = (k >> 2) * (BN * 128) + (k & 3) * 32;
-          mma_ss(dS2, sdesc_sw128(sQ2 + oq, 16, 1024), sdesc_sw128(k2 + ok_, 16, 1024), C::IDESC_QK, k > 0);
-        }
-        tc_commit(&s_full[s]);
         return true;
       };
-
-      if (ok) ok = issue_qk(0);
-      for (int it = 0; ok && it < NI; ++it) {
-        if (it + 1 < NI) {
-          // S stage (it+1)&1 was last used by iteration it-1; a sweep-1
-          // iteration releases it here, a sweep-2 one was awaited before its PV.
-          if (it >= 1 && it - 1 < T) {
-            if (!mbar_wait(&s_free[(it - 1) & 1], static_cast<uint32_t>((it - 1) >> 1) & 1u, ab)) break;
-          }
-          if (!issue_qk(it + 1)) break;
-        }
-        if (it >= T) {
-          const int s = it & 1;
-          if (!mbar_wait(&s_free[s], static_cast<uint32_t>(it >> 1) & 1u, ab)) break;
-          tc_fence_after();
-          const int st = it % STAGES;
-          const int j = it - T;
-          const uint32_t vb = sStages + st * C::STAGE + C::NK * C::K_TILE;
-          const uint32_t aP = tmem + C::TM_S + 128u * s;
+      auto waitc = [&](uint64_t* bar, uint32_t& n) -> bool {
+        const bool r = mbar_wait(bar, n & 1u, ab);
+        ++n;
+        tc_fence_after();
+        return r;
+      };
+      auto qk = [&](uint32_t dst, uint64_t dq, int s) {
+        const uint64_t dk = dRingK + static_cast<uint64_t>((s * C::SLOT) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint32_t acol = (kk < 2) ? kk * 8 : 32 + (kk - 2) * 8;
-            mma_ts(tmem + C::TM_O, aP + acol, sdesc_sw128(vb + kk * 2048, BN * 128, 1024), C::IDESC_PV,
-                   (j > 0 || kk > 0) ? 1u : 0u);
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(dst, dq + static_cast<uint64_t>((((k >> 2) * (BM * 128)) + (k & 3) * 32) >> 4),
+                 dk + static_cast<uint64_t>((((k >> 2) * (BN * 128)) + (k & 3) * 32) >> 4), C::IDESC_QK,
+                 k > 0 ? 1u : 0u);
+      };
+      // ---- sweep 1
+      for (int j = 0; ok && j < T; ++j) {
+        int s1, s2;
+        if (!acquire(s1)) break;
+        if (j > 0 && !waitc(a_free1, n_afree1)) break;
+        qk(tA, dQ1, s1);
+        tc_commit(a_full);
+        if (SHARED_K) {
+          s2 = s1;
+        } else {
+          tc_commit(&empty[s1]);
+          if (!acquire(s2)) break;
+        }
+        if (j > 0 && !waitc(b_free1, n_bfree1)) break;
+        qk(tB, dQ2, s2);
+        tc_commit(b_full);
+        tc_commit(&empty[s2]);
+      }
+      // ---- sweep 2
+      if (ok) ok = waitc(a_free1, n_afree1) && waitc(b_free1, n_bfree1);
+      if (ok) {
+        int s1, s2;
+        if (SHARED_K) {
+          ok = acquire(s2);
+          s1 = s2;
+          if (ok) {
+            qk(tB, dQ2, s2);
+            tc_commit(b_full);
+            qk(tA, dQ1, s1);
+            tc_commit(a_full);
+            tc_commit(&empty[s1]);
+          }
+        } else {
+          ok = acquire(s2);
+          if (ok) {
+            qk(tB, dQ2, s2);
+            tc_commit(b_full);
+            tc_commit(&empty[s2]);
+            ok = acquire(s1);
+          }
+          if (ok) {
+            qk(tA, dQ1, s1);
+            tc_commit(a_full);
+            tc_commit(&empty[s1]);
           }
         }
-        tc_commit(&kv_empty[it % STAGES]);
+      }
+      for (int j = 0; ok && j < T; ++j) {
+        int sk = 0;
+        if (j + 1 < T) {
+          if (!acquire(sk)) break;
+          if (!waitc(b_free2, n_bfree2)) break;
+          qk(tB, dQ2, sk);
+          tc_commit(b_full);
+          if (!SHARED_K) tc_commit(&empty[sk]);
+        } else {
+          // Nobody waits for the last tile's release of B in sweep 2.
+          ++n_bfree2;
+        }
+        if (!waitc(p_ready, n_pready)) break;
+#pragma unroll
+        for (int part = 0; part < C::VF; ++part) {
+          int sv;
+          if (!acquire(sv)) {
+            ok = false;
+            break;
+          }
+          const uint64_t dv = dRingV + static_cast<uint64_t>((sv * C::SLOT) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < C::VKEYS / 16; ++kk) {
+            const int kg = part * (C::VKEYS / 16) + kk;  // global k-step: keys 16 kg .. 16 kg + 15
+            const uint32_t acol = 32u * (kg >> 1) + 8u * (kg & 1);
+            mma_ts(tO, tA + acol, dv + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_PV,
+                   (j > 0 || kg > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[sv]);
+        }
+        if (!ok) break;
+        if (j + 1 < T) {
+          if (!SHARED_K && !acquire(sk)) break;
+          qk(tA, dQ1, sk);
+          tc_commit(a_full);
+          tc_commit(&empty[sk]);
+        }
       }
       tc_commit(o_full);
       if (*ab.flag) mbar_wait_drain(o_full, 0, kWaitBudgetNs);
     }
   } else if (warp >= 4) {
     // =============================================================== softmax + epilogue
-    const int wg = (warp - 4) >> 2;
-    const int wq = warp & 3;
+    const int wg = (warp - 4) >> 2;  // 0..3
+    const int wq = warp & 3;         // TMEM lane quarter
     const int row = wq * 32 + lane;
     const int t = q0 + row;
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float sc = p.scale_log2;
     const int lim = p.causal ? min(t + 1, p.n) : p.n;  // keys j < lim are visible
 
-    // ---- sweep 1: running max / sum of map (wg + 1)
+    // ---- sweep 1: running max / sum of map (wg / 2) over key columns [64 (wg % 2), +64)
+    const int map = wg >> 1;
+    const int half = wg & 1;
     float m = -INFINITY, l = 0.f;
-    for (int it = 0; it < T; ++it) {
-      const int s = it & 1;
-      mbar_wait(&s_full[s], static_cast<uint32_t>(it >> 1) & 1u, ab);
-      __syncwarp();
-      tc_fence_after();
-      uint32_t r0[32], r1[32];
-      const uint32_t ta = tl + C::TM_S + 128u * s + 64u * wg;
-      tmem_ld32(ta, r0);
-      tmem_ld32(ta + 32, r1);
-      tmem_ld_wait2(r0, r1);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[s]);
-      __syncwarp();
-      const int nvis = lim - it * BN;
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        if (c >= nvis) r0[c] = __float_as_uint(-INFINITY);
-        if (c + 32 >= nvis) r1[c] = __float_as_uint(-INFINITY);
-        mx = fmaxf(mx, fmaxf(__uint_as_float(r0[c]), __uint_as_float(r1[c])));
+    {
+      uint64_t* fullb = map == 0 ? a_full : b_full;
+      uint64_t* freeb = map == 0 ? a_free1 : b_free1;
+      const uint32_t tbuf = tl + (map == 0 ? C::TM_A : C::TM_B) + 64u * half;
+      for (int j = 0; j < T; ++j) {
+        mbar_wait(fullb, static_cast<uint32_t>(j) & 1u, ab);
+        __syncwarp();
+        tc_fence_after();
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tbuf, r0);
+        tmem_ld32(tbuf + 32, r1);
+        tmem_ld_wait2(r0, r1);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(freeb);
+        __syncwarp();
+        row_stats64(r0, r1, lim - (j * BN + 64 * half), sc, m, l);
       }
-      const float m_new = fmaxf(m, mx * sc);
-      const float base = (m_new == -INFINITY) ? 0.f : m_new;
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        s0 += ex2(fmaf(__uint_as_float(r0[c]), sc, -base));
-        s1 += ex2(fmaf(__uint_as_float(r1[c]), sc, -base));
-      }
-      l = l * ex2(m - base) + (s0 + s1);
-      m = m_new;
     }
 
-    // ---- exchange the statistics of the two maps
-    stat_m[wg * 128 + row] = m;
-    stat_l[wg * 128 + row] = l;
+    // ---- exchange the four partial states through the (unused) O columns
+    tmem_st2(tl + C::TM_O + 2u * wg, __float_as_uint(m), __float_as_uint(l));
+    tmem_st_wait();
+    tc_fence_before();
     __syncwarp();
-    named_bar_sync(1, 256);
-    const float m1 = stat_m[row], l1 = stat_l[row];
-    const float m2 = stat_m[128 + row], l2 = stat_l[128 + row];
+    named_bar_sync(1, 128 * C::NSMWG);
+    tc_fence_after();
+    uint32_t ps[8];
+    tmem_ld8_wait(tl + C::TM_O, ps);
+    float m1 = __uint_as_float(ps[0]), l1 = __uint_as_float(ps[1]);
+    merge_state(m1, l1, __uint_as_float(ps[2]), __uint_as_float(ps[3]));
+    float m2 = __uint_as_float(ps[4]), l2 = __uint_as_float(ps[5]);
+    merge_state(m2, l2, __uint_as_float(ps[6]), __uint_as_float(ps[7]));
     float coef;
     if (EPI == kEpiRmsNorm) {
       coef = *p.lambda;
@@ -318,66 +457,90 @@ __global__ void __launch_bounds__(384, 1) twopass_fwd_kernel(const __grid_consta
     const float acoef = fabsf(coef);
     const float M2 = (acoef > 0.f) ? m2 + log2f(l2) - log2f(acoef) : INFINITY;
     const float neg2 = (coef >= 0.f) ? -1.f : 1.f;
+    const uint64_t sc2 = f2pack(sc, sc);
+    const uint64_t nM1 = f2pack(-M1, -M1), nM2 = f2pack(-M2, -M2), ng2 = f2pack(neg2, neg2);
 
-    // ---- sweep 2: signed combined weights -> TMEM (bf16) for the P.V MMA
-    for (int it = T; it < NI; ++it) {
-      const int s = it & 1;
-      const int j = it - T;
-      mbar_wait(&s_full[s], static_cast<uint32_t>(it >> 1) & 1u, ab);
+    // ---- sweep 2: signed combined weights of key columns [32 wg, +32) -> TMEM (bf16)
+    for (int j = 0; j < T; ++j) {
+      const uint32_t ph = static_cast<uint32_t>(T + j) & 1u;
+      mbar_wait(b_full, ph, ab);
       __syncwarp();
       tc_fence_after();
-      uint32_t a[32], c2[32];
-      const uint32_t ts = tl + C::TM_S + 128u * s;
-      tmem_ld32(ts + 32u * wg, a);
-      tmem_ld32(ts + 64u + 32u * wg, c2);
-      tmem_ld_wait2(a, c2);
+      uint32_t r[32];
+      tmem_ld32(tl + C::TM_B + 32u * wg, r);
+      tmem_ld_wait(r);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_free2);
+      __syncwarp();
+      uint64_t e2[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        float x0, x1;
+        f2unpack(fma2(f2pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), sc2, nM2), x0, x1);
+        e2[c] = f2pack(ex2(x0), ex2(x1));
+      }
+      mbar_wait(a_full, ph, ab);
+      __syncwarp();
+      tc_fence_after();
+      tmem_ld32(tl + C::TM_A + 32u * wg, r);
+      tmem_ld_wait(r);
       const int nvis = lim - (j * BN + 32 * wg);
       uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float p0 = fmaf(neg2, ex2(fmaf(__uint_as_float(c2[c]), sc, -M2)),
-                        ex2(fmaf(__uint_as_float(a[c]), sc, -M1)));
-        float p1 = fmaf(neg2, ex2(fmaf(__uint_as_float(c2[c + 1]), sc, -M2)),
-                        ex2(fmaf(__uint_as_float(a[c + 1]), sc, -M1)));
-        if (c >= nvis) p0 = 0.f;
-        if (c + 1 >= nvis) p1 = 0.f;
-        pk[c >> 1] = pack_bf16x2(p0, p1);
+      for (int c = 0; c < 16; ++c) {
+        float x0, x1;
+        f2unpack(fma2(f2pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), sc2, nM1), x0, x1);
+        float p0, p1;
+        f2unpack(fma2(e2[c], ng2, f2pack(ex2(x0), ex2(x1))), p0, p1);
+        if (2 * c >= nvis) p0 = 0.f;
+        if (2 * c + 1 >= nvis) p1 = 0.f;
+        pk[c] = pack_bf16x2(p0, p1);
       }
-      tmem_st16(ts + 32u * wg, pk);
+      tmem_st16(tl + C::TM_A + 32u * wg, pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[s]);
+      if (lane == 0) mbar_arrive(p_ready);
       __syncwarp();
     }
 
-    // ---- epilogue
+    // ---- epilogue: warpgroup wg owns output channels [wg * DV/4, +DV/4)
+    constexpr int QW = DV / 4;
     mbar_wait(o_full, 0, ab);
     __syncwarp();
     tc_fence_after();
-    constexpr int HALF = DV / 2;
-    const uint32_t to = tl + C::TM_O + wg * HALF;
-    __nv_bfloat16* orow =
-        p.out + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * DV + wg * HALF;
+    const uint32_t to = tl + C::TM_O + wg * QW;
     float rinv = 1.f;
     if (EPI == kEpiRmsNorm) {
-      float ss = 0.f;
+      float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
-      for (int ch = 0; ch < HALF / 32; ++ch) {
+      for (int ch = 0; ch < QW / 32; ++ch) {
         uint32_t r[32];
         tmem_ld32(to + 32 * ch, r);
         tmem_ld_wait(r);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) ss = fmaf(__uint_as_float(r[c]), __uint_as_float(r[c]), ss);
+        for (int c = 0; c < 32; c += 2) {
+          ss0 = fmaf(__uint_as_float(r[c]), __uint_as_float(r[c]), ss0);
+          ss1 = fmaf(__uint_as_float(r[c + 1]), __uint_as_float(r[c + 1]), ss1);
+        }
       }
-      stat_ss[wg * 128 + row] = ss;
+      // Every MMA has completed, so buffer A is free for the exchange.
+      tmem_st1(tl + C::TM_A + wg, __float_as_uint(ss0 + ss1));
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
-      named_bar_sync(1, 256);
-      const float tot = stat_ss[row] + stat_ss[128 + row];
+      named_bar_sync(1, 128 * C::NSMWG);
+      tc_fence_after();
+      uint32_t q4[4];
+      tmem_ld4_wait(tl + C::TM_A, q4);
+      const float tot = (__uint_as_float(q4[0]) + __uint_as_float(q4[1])) +
+                        (__uint_as_float(q4[2]) + __uint_as_float(q4[3]));
       rinv = p.norm_mult * rsqrtf(tot * (1.f / DV) + p.eps);
     }
+    __nv_bfloat16* orow = p.out + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * DV + wg * QW;
 #pragma unroll
-    for (int ch = 0; ch < HALF / 32; ++ch) {
+    for (int ch = 0; ch < QW / 32; ++ch) {
       uint32_t r[32];
       tmem_ld32(to + 32 * ch, r);
       tmem_ld_wait(r);
@@ -388,7 +551,7 @@ __global__ void __launch_bounds__(384, 1) twopass_fwd_kernel(const __grid_consta
           float y0 = __uint_as_float(r[c]) * rinv;
           float y1 = __uint_as_float(r[c + 1]) * rinv;
           if (EPI == kEpiRmsNorm && p.gamma != nullptr) {
-            const int col = wg * HALF + ch * 32 + c;
+            const int col = wg * QW + ch * 32 + c;
             y0 *= __ldg(p.gamma + col);
             y1 *= __ldg(p.gamma + col + 1);
           }
