@@ -191,7 +191,7 @@ diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d, 
   memset(&p, 0, sizeof(p));
   if ((st = make_map(&p.tm_q1, q1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
   if ((st = make_map(&p.tm_q2, q2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
-  // Query and key tiles are 128 rows; a value tile is split into two 64-row slots.
+  // Query and key tiles are 128 rows; a value tile is split into two 64-row ring slots.
   if ((st = make_map(&p.tm_k1, k1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
   if ((st = make_map(&p.tm_k2, k2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
   if ((st = make_map(&p.tm_v, v, B, n, H, dv, 64)) != DIFFATTN_OK) return st;
@@ -212,7 +212,9 @@ diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d, 
   p.status = status;
   const long long grid = static_cast<long long>(p.num_q_tiles) * B * H;
   if (grid > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "diffattn_forward: too many tiles");
-  cudaError_t e = (d == 64) ? da::launch_twopass_v1_d64(p, static_cast<int>(grid), s)
+  // d = 64 (value width 128): one sweep with two online-softmax states fits
+  // TMEM; d = 128 (value width 256) does not, and sweeps the keys twice.
+  cudaError_t e = (d == 64) ? da::launch_onepass_v1_d64(p, static_cast<int>(grid), s)
                             : da::launch_twopass_v1_d128(p, static_cast<int>(grid), s);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward (bf16) launch");
   g_launches.fetch_add(1);
@@ -297,7 +299,7 @@ diffattn_status diffattn_v2_forward(diffattn_dtype dt, int B, int Hq, int Hkv, i
   p.status = status;
   const long long grid = static_cast<long long>(p.num_q_tiles) * B * G;
   if (grid > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_forward: too many tiles");
-  cudaError_t e = da::launch_twopass_v2_d128(p, static_cast<int>(grid), s);
+  cudaError_t e = da::launch_onepass_v2_d128(p, static_cast<int>(grid), s);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_forward (bf16) launch");
   g_launches.fetch_add(1);
   return ok();

@@ -1,0 +1,447 @@
+// One-sweep differential-attention forward with two online-softmax states
+// (tcgen05 tensor cores, TMA, mbarriers; sm_103a).  Used where the value
+// width is 128: DIFF V1 with d = 64 (V = 2d = 128) and DIFF V2 with d = 128.
+//
+// What it computes (per (batch, unit, 128-query tile)):
+//   O_r = sum_j exp(S_r[:, j] - m_r) V_j,  l_r = sum_j exp(S_r[:, j] - m_r),   r in {1, 2}
+//   out = O_1 / l_1 - c * O_2 / l_2
+//   V1: c = lambda, then (1 - lambda_init) * gamma * out / sqrt(mean(out^2) + eps)
+//   V2: c = sigmoid(logit[b, t, pair]); Q_1/Q_2 are query heads 2g/2g+1 over one K/V head.
+// ("Differential Transformer" glossary page, "How differential attention
+// works"; DIFF V2 analysis page, DiffAttn operator, V2 code, GQA pairing;
+// news article section "差分注意力" for the per-head RMSNorm.)
+//
+// Each K/V tile is loaded once and serves both maps.  TMEM (512 columns):
+// O_1 [0, 128), O_2 [128, 256), A [256, 384) holds S_1 then P_1 (bf16
+// pairs), B [384, 512) holds S_2 then P_2.  MMA issue order per key tile j:
+//     PV1(j)  QK1(j+1)  PV2(j)  QK2(j+1)
+// so the softmax of one map overlaps the other map's MMAs, and S_r(j+1)
+// being complete implies PV_r(j) is complete (the tensor pipe runs in issue
+// order): a rescale of O_r never has to wait.
+//
+// Rescaling is conditional: a row keeps its reference maximum until the true
+// maximum exceeds it by more than 2^8 (P then stays below 256, exact enough in
+// bf16 and far from fp32 overflow); when any row of a warp must move, the warp
+// rescales its rows of O_r and l_r.  Both halves of a map see the same row
+// maximum (exchanged through shared memory), so they take the same decisions.
+//
+// Roles (576 threads, one CTA per SM):
+//   warp 0      TMA producer (Q once; then K_1, K_2 / K and V tiles into a ring
+//               of NSLOT equal slots, in the MMA thread's consumption order).
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer.
+//   warps 2-17  four softmax warpgroups; warpgroup w handles map w/2, key
+//               columns [64 (w%2), +64); thread = one query row (TMEM lane
+//               32 (warp % 4) + lane).  Epilogue: warpgroup w owns output
+//               channels [32 w, +32).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "params.h"
+#include "ptx.cuh"
+
+namespace da {
+
+template <int D, bool SHARED_K, int EPI, int NSLOT>
+struct OnePassCfg {
+  static constexpr int BM = 128;
+  static constexpr int BN = 128;
+  static constexpr int DV = 128;
+  static constexpr int NCTRL = 2;  // producer, MMA
+  static constexpr int NSMWG = 4;
+  static constexpr int NTHREADS = (NCTRL + 4 * NSMWG) * 32;
+  static constexpr int QB = D / 64;
+  static constexpr int VB = DV / 64;
+  static constexpr int Q_TILE = BM * D * 2;
+  static constexpr int K_TILE = BN * D * 2;
+  static constexpr int V_TILE = BN * DV * 2;
+  static constexpr int SLOT = K_TILE;
+  static constexpr int VF = V_TILE / SLOT;
+  static constexpr int VKEYS = BN / VF;
+  static constexpr int OFF_Q1 = 0;
+  static constexpr int OFF_Q2 = Q_TILE;
+  static constexpr int OFF_RING = 2 * Q_TILE;
+  static constexpr int OFF_BARS = OFF_RING + NSLOT * SLOT;
+  static constexpr int NBARS = 2 + 2 * NSLOT + 4;
+  static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
+  static constexpr int OFF_RED = (OFF_MISC + 16 + 15) / 16 * 16;  // float [2 parity][2 maps][2 halves][128]
+  static constexpr int OFF_LP = OFF_RED + 2 * 2 * 2 * 128 * 4;    // float [4][128]
+  static constexpr int OFF_SS = OFF_LP + 4 * 128 * 4;             // float [4][128]
+  static constexpr int SMEM_BYTES = OFF_SS + 4 * 128 * 4 + 1024;  // + 1 KB alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t TM_O1 = 0, TM_O2 = 128, TM_A = 256, TM_B = 384;
+  static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false, false);
+  static constexpr uint32_t IDESC_PV = idesc_bf16(BM, DV, false, true);
+  static constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units
+  static_assert(D == 64 || D == 128, "query/key width");
+  static_assert(V_TILE % SLOT == 0 && (VF == 1 || VF == 2), "value tile split");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(NSLOT >= 4, "ring depth");
+};
+
+template <int D, bool SHARED_K, int EPI, int NSLOT>
+__global__ void __launch_bounds__(576, 1) onepass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
+  using C = OnePassCfg<D, SHARED_K, EPI, NSLOT>;
+  constexpr int BM = C::BM, BN = C::BN, DV = C::DV;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
+  uint64_t* q_full = bars + 0;
+  uint64_t* o_full = bars + 1;
+  uint64_t* full = bars + 2;
+  uint64_t* empty = full + NSLOT;
+  uint64_t* s_full = empty + NSLOT;  // [2]: S_r of the current tile in its buffer
+  uint64_t* p_ready = s_full + 2;    // [2]: P_r of the current tile in its buffer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+  float* lpart = reinterpret_cast<float*>(smem + C::OFF_LP);
+  float* sspart = reinterpret_cast<float*>(smem + C::OFF_SS);
+
+  // ---- which tile this CTA owns
+  const int units = p.B * p.units_per_batch;
+  int unit, qt;
+  if (p.order == 0) {
+    unit = blockIdx.x / p.num_q_tiles;
+    qt = p.num_q_tiles - 1 - static_cast<int>(blockIdx.x % p.num_q_tiles);
+  } else {
+    qt = p.num_q_tiles - 1 - static_cast<int>(blockIdx.x / units);
+    unit = blockIdx.x % units;
+  }
+  const int b = unit / p.units_per_batch;
+  const int u = unit % p.units_per_batch;
+  int hq1, hq2, hk;
+  if (EPI == kEpiRmsNorm) {
+    hq1 = hq2 = hk = u;
+  } else {
+    hq1 = 2 * u;
+    hq2 = 2 * u + 1;
+    hk = hq1 / p.group;
+  }
+  const int q0 = qt * BM;
+  const int kv_end = p.causal ? min(p.n, q0 + BM) : p.n;
+  const int T = (kv_end + BN - 1) / BN;
+
+  // ---- set-up
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(o_full, 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(&s_full[r], 1);
+      mbar_init(&p_ready[r], 8);  // the 8 warps of the map's two warpgroups
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const AbortState ab{abort_flag, p.status};
+
+  if (warp == 0) {
+    // =============================================================== producer
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q1);
+      tma_prefetch_desc(&p.tm_q2);
+      tma_prefetch_desc(&p.tm_k1);
+      if (!SHARED_K) tma_prefetch_desc(&p.tm_k2);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_expect_tx(q_full, 2 * C::Q_TILE);
+      for (int bx = 0; bx < C::QB; ++bx) {
+        tma_load_4d(smem + C::OFF_Q1 + bx * BM * 128, &p.tm_q1, q_full, bx * 64, hq1, q0, b);
+        tma_load_4d(smem + C::OFF_Q2 + bx * BM * 128, &p.tm_q2, q_full, bx * 64, hq2, q0, b);
+      }
+      int fill = 0;
+      bool ok = true;
+      auto load = [&](const CUtensorMap* map, int key0, int rows, int nbox) {
+        if (!ok) return;
+        const int s = fill % NSLOT;
+        const uint32_t use = static_cast<uint32_t>(fill / NSLOT);
+        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, ab)) {
+          ok = false;
+          return;
+        }
+        uint8_t* dst = smem + C::OFF_RING + s * C::SLOT;
+        mbar_arrive_expect_tx(&full[s], C::SLOT);
+        for (int bx = 0; bx < nbox; ++bx) tma_load_4d(dst + bx * rows * 128, map, &full[s], bx * 64, hk, key0, b);
+        ++fill;
+      };
+      load(&p.tm_k1, 0, BN, C::QB);
+      if (!SHARED_K) load(&p.tm_k2, 0, BN, C::QB);
+      for (int j = 0; j < T; ++j) {
+        for (int part = 0; part < C::VF; ++part) load(&p.tm_v, j * BN + part * C::VKEYS, C::VKEYS, C::VB);
+        if (j + 1 < T) {
+          load(&p.tm_k1, (j + 1) * BN, BN, C::QB);
+          if (!SHARED_K) load(&p.tm_k2, (j + 1) * BN, BN, C::QB);
+        }
+      }
+      if (*ab.flag) {
+        mbar_wait_drain(q_full, 0, kWaitBudgetNs);
+        for (int f = (fill > NSLOT ? fill - NSLOT : 0); f < fill; ++f)
+          mbar_wait_drain(&full[f % NSLOT], static_cast<uint32_t>(f / NSLOT) & 1u, kWaitBudgetNs);
+      }
+    }
+  } else if (warp == 1) {
+    // =============================================================== MMA issuer
+    if (lane == 0) {
+      const uint64_t dQ1 = sdesc_sw128(smem_u32(smem + C::OFF_Q1), 16, 1024);
+      const uint64_t dQ2 = sdesc_sw128(smem_u32(smem + C::OFF_Q2), 16, 1024);
+      const uint64_t dRingK = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
+      const uint64_t dRingV = sdesc_sw128(smem_u32(smem + C::OFF_RING), C::VKEYS * 128, 1024);
+      const uint32_t tA = tmem + C::TM_A, tB = tmem + C::TM_B;
+      const uint32_t tO1 = tmem + C::TM_O1, tO2 = tmem + C::TM_O2;
+      int cons = 0;
+      bool ok = mbar_wait(q_full, 0, ab);
+      tc_fence_after();
+      auto acquire = [&](int& s) -> bool {
+        s = cons % NSLOT;
+        const uint32_t use = static_cast<uint32_t>(cons / NSLOT);
+        ++cons;
+        if (!mbar_wait(&full[s], use & 1u, ab)) return false;
+        tc_fence_after();
+        return true;
+      };
+      auto qk = [&](uint32_t dst, uint64_t dq, int s) {
+        const uint64_t dk = dRingK + static_cast<uint64_t>((s * C::SLOT) >> 4);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+          mma_ss(dst, dq + static_cast<uint64_t>((((k >> 2) * (BM * 128)) + (k & 3) * 32) >> 4),
+                 dk + static_cast<uint64_t>((((k >> 2) * (BN * 128)) + (k & 3) * 32) >> 4), C::IDESC_QK,
+                 k > 0 ? 1u : 0u);
+      };
+      int sv[2] = {0, 0};
+      auto pv = [&](uint32_t dO, uint32_t aP, int j) {
+#pragma unroll
+        for (int part = 0; part < C::VF; ++part) {
+          const uint64_t dv = dRingV + static_cast<uint64_t>((sv[part] * C::SLOT) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < C::VKEYS / 16; ++kk) {
+            const int kg = part * (C::VKEYS / 16) + kk;
+            mma_ts(dO, aP + 8u * kg, dv + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_PV,
+                   (j > 0 || kg > 0) ? 1u : 0u);
+          }
+        }
+      };
+      int sk = 0;
+      if (ok) ok = acquire(sk);
+      if (ok) {
+        qk(tA, dQ1, sk);
+        tc_commit(&s_full[0]);
+        if (!SHARED_K) {
+          tc_commit(&empty[sk]);
+          ok = acquire(sk);
+        }
+      }
+      if (ok) {
+        qk(tB, dQ2, sk);
+        tc_commit(&s_full[1]);
+        tc_commit(&empty[sk]);
+      }
+      for (int j = 0; ok && j < T; ++j) {
+        for (int part = 0; part < C::VF; ++part)
+          if (!acquire(sv[part])) ok = false;
+        if (!ok) break;
+        if (!mbar_wait(&p_ready[0], static_cast<uint32_t>(j) & 1u, ab)) break;
+        tc_fence_after();
+        pv(tO1, tA, j);
+        if (j + 1 < T) {
+          if (!acquire(sk)) break;
+          qk(tA, dQ1, sk);
+          tc_commit(&s_full[0]);
+          if (!SHARED_K) tc_commit(&empty[sk]);
+        }
+        if (!mbar_wait(&p_ready[1], static_cast<uint32_t>(j) & 1u, ab)) break;
+        tc_fence_after();
+        pv(tO2, tB, j);
+        for (int part = 0; part < C::VF; ++part) tc_commit(&empty[sv[part]]);
+        if (j + 1 < T) {
+          if (!SHARED_K && !acquire(sk)) break;
+          qk(tB, dQ2, sk);
+          tc_commit(&s_full[1]);
+          tc_commit(&empty[sk]);
+        }
+      }
+      tc_commit(o_full);
+      if (*ab.flag) mbar_wait_drain(o_full, 0, kWaitBudgetNs);
+    }
+  } else {
+    // =============================================================== softmax + epilogue
+    const int w = warp - C::NCTRL;
+    const int wg = w >> 2;  // 0..3
+    const int wq = warp & 3;  // TMEM lane quarter
+    const int row = wq * 32 + lane;
+    const int t = q0 + row;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const float sc = p.scale_log2;
+    const int lim = p.causal ? min(t + 1, p.n) : p.n;
+    const int map = wg >> 1, half = wg & 1;
+    const uint32_t tS = tl + (map ? C::TM_B : C::TM_A);
+    const uint32_t tOr = tl + (map ? C::TM_O2 : C::TM_O1) + 64u * half;
+    const uint64_t sc2 = f2pack(sc, sc);
+    float m_used = -INFINITY, l = 0.f;
+
+    for (int j = 0; j < T; ++j) {
+      mbar_wait(&s_full[map], static_cast<uint32_t>(j) & 1u, ab);
+      __syncwarp();
+      tc_fence_after();
+      uint32_t x0[32], x1[32];
+      tmem_ld32(tS + 64u * half, x0);
+      tmem_ld32(tS + 64u * half + 32u, x1);
+      tmem_ld_wait2(x0, x1);
+      const int nvis = lim - (j * BN + 64 * half);
+      if (nvis < 64) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if (c >= nvis) x0[c] = __float_as_uint(-INFINITY);
+          if (c + 32 >= nvis) x1[c] = __float_as_uint(-INFINITY);
+        }
+      }
+      float tm[11];
+#pragma unroll
+      for (int c = 0; c < 10; ++c)
+        tm[c] = max3(__uint_as_float(x0[3 * c]), __uint_as_float(x0[3 * c + 1]), __uint_as_float(x0[3 * c + 2]));
+      tm[10] = max3(__uint_as_float(x0[30]), __uint_as_float(x0[31]), __uint_as_float(x1[0]));
+      float tn[11];
+#pragma unroll
+      for (int c = 0; c < 10; ++c)
+        tn[c] = max3(__uint_as_float(x1[3 * c + 1]), __uint_as_float(x1[3 * c + 2]), __uint_as_float(x1[3 * c + 3]));
+      tn[10] = __uint_as_float(x1[31]);
+      const float pmax = max3(max3(max3(tm[0], tm[1], tm[2]), max3(tm[3], tm[4], tm[5]), max3(tm[6], tm[7], tm[8])),
+                              max3(tm[9], tm[10], tn[0]),
+                              max3(max3(tn[1], tn[2], tn[3]), max3(tn[4], tn[5], tn[6]), max3(tn[7], tn[8], fmaxf(tn[9], tn[10]))));
+      // Exchange the half-row maxima with the other warpgroup of this map.
+      float* rbuf = red + ((j & 1) * 2 + map) * 256;
+      rbuf[half * 128 + row] = pmax;
+      __syncwarp();
+      named_bar_sync(1 + map, 256);
+      const float mx = fmaxf(pmax, rbuf[(half ^ 1) * 128 + row]);
+      const float m_new = fmaxf(m_used, mx * sc);
+      const bool need = m_new > m_used + C::RESCALE_THRESHOLD;
+      const bool rescale = __any_sync(0xffffffffu, need);
+      float factor = 1.f;
+      if (rescale) {
+        factor = ex2(m_used - m_new);  // 0 on the first tile
+        l *= factor;
+        m_used = m_new;
+      }
+      const uint64_t nb2 = f2pack(-m_used, -m_used);
+      uint64_t acc0 = 0, acc1 = 0;
+      // P pairs are packed in place over score registers already consumed.
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        float a0, a1, b0, b1;
+        f2unpack(fma2(f2pack(__uint_as_float(x0[c]), __uint_as_float(x0[c + 1])), sc2, nb2), a0, a1);
+        f2unpack(fma2(f2pack(__uint_as_float(x1[c]), __uint_as_float(x1[c + 1])), sc2, nb2), b0, b1);
+        const float pa0 = ex2(a0), pa1 = ex2(a1), pb0 = ex2(b0), pb1 = ex2(b1);
+        acc0 = add2(acc0, f2pack(pa0, pa1));
+        acc1 = add2(acc1, f2pack(pb0, pb1));
+        x0[c >> 1] = pack_bf16x2(pa0, pa1);
+        x1[c >> 1] = pack_bf16x2(pb0, pb1);
+      }
+      float s0, s1;
+      f2unpack(add2(acc0, acc1), s0, s1);
+      l += s0 + s1;
+      // P of key columns [64 half, +64) -> buffer columns [32 half, +32).  The
+      // other half finished reading those S columns before the exchange above.
+      tmem_st16(tS + 32u * half, reinterpret_cast<const uint32_t(&)[16]>(x0));
+      tmem_st16(tS + 32u * half + 16u, reinterpret_cast<const uint32_t(&)[16]>(x1));
+      if (rescale && j > 0) {
+        // PV_r(j-1) has completed (it was issued before QK_r(j)), so O_r is quiescent.
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t o[32];
+          tmem_ld32(tOr + 32u * ch, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * factor);
+          tmem_st32(tOr + 32u * ch, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_ready[map]);
+      __syncwarp();
+    }
+
+    // ---- epilogue: out = O_1 / l_1 - c O_2 / l_2 over channels [32 wg, +32)
+    lpart[wg * 128 + row] = l;
+    mbar_wait(o_full, 0, ab);
+    __syncwarp();
+    tc_fence_after();
+    named_bar_sync(3, 128 * C::NSMWG);
+    const float l1 = lpart[row] + lpart[128 + row];
+    const float l2 = lpart[256 + row] + lpart[384 + row];
+    float coef;
+    if (EPI == kEpiRmsNorm) {
+      coef = *p.lambda;
+    } else {
+      const float lg = (t < p.n) ? p.lam_logits[b * p.sb + static_cast<long long>(t) * p.st + u] : 0.f;
+      coef = 1.f / (1.f + expf(-lg));
+    }
+    const float a1 = 1.f / l1, a2 = -coef / l2;
+    uint32_t o1[32], o2[32];
+    tmem_ld32(tl + C::TM_O1 + 32u * wg, o1);
+    tmem_ld32(tl + C::TM_O2 + 32u * wg, o2);
+    tmem_ld_wait2(o1, o2);
+    float y[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) y[c] = fmaf(__uint_as_float(o2[c]), a2, __uint_as_float(o1[c]) * a1);
+    float rinv = 1.f;
+    if (EPI == kEpiRmsNorm) {
+      float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        ss0 = fmaf(y[c], y[c], ss0);
+        ss1 = fmaf(y[c + 1], y[c + 1], ss1);
+      }
+      sspart[wg * 128 + row] = ss0 + ss1;
+      __syncwarp();
+      named_bar_sync(3, 128 * C::NSMWG);
+      const float tot = (sspart[row] + sspart[128 + row]) + (sspart[256 + row] + sspart[384 + row]);
+      rinv = p.norm_mult * rsqrtf(tot * (1.f / DV) + p.eps);
+    }
+    if (t < p.n) {
+      __nv_bfloat16* orow =
+          p.out + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * DV + 32 * wg;
+      uint32_t wv[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        float y0 = y[c] * rinv, y1 = y[c + 1] * rinv;
+        if (EPI == kEpiRmsNorm && p.gamma != nullptr) {
+          y0 *= __ldg(p.gamma + 32 * wg + c);
+          y1 *= __ldg(p.gamma + 32 * wg + c + 1);
+        }
+        wv[c >> 1] = pack_bf16x2(y0, y1);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) dst[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace da
