@@ -142,15 +142,22 @@ def time_device(w, x, da, steps, warmup, flush, dist=None):
     import torch
     lam_call, fwd_call, out = make_step(w, x, da)
     stream = torch.cuda.current_stream()
+    h0 = time.perf_counter()
     for _ in range(warmup):
+        flush.zero_()
         lam_call()
         fwd_call()
+    host_per_step = (time.perf_counter() - h0) / warmup
     da.device_status()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     c0 = da.launch_count()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    # Hold the stream in a device-side sleep (outside the events) long enough for
+    # the host to enqueue every timed step, so that the events see device time
+    # only, not gaps while Python marshals the next call.
+    torch.cuda._sleep(int(min(2e9, 3.0e9 * host_per_step * steps + 2e6)))
     t0 = time.perf_counter()
     for k in range(steps):
         flush.zero_()

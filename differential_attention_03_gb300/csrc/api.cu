@@ -151,7 +151,7 @@ diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d, 
   int* status = nullptr;
 
   if (dt == DIFFATTN_F32) {
-    if (d > da::kSimtMaxD) return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_forward: f32 needs d <= 256 (got %d)", d);
+    if (d > da::kSimtMaxD) return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_forward: f32 needs d <= 128 (got %d)", d);
     diffattn_status st = status_word(&status);
     if (st != DIFFATTN_OK) return st;
     da::SimtParams p{};
@@ -241,7 +241,7 @@ diffattn_status diffattn_v2_forward(diffattn_dtype dt, int B, int Hq, int Hkv, i
   const int G = Hq / 2;
 
   if (dt == DIFFATTN_F32) {
-    if (d > da::kSimtMaxD) return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_v2_forward: f32 needs d <= 256");
+    if (d > da::kSimtMaxD) return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_v2_forward: f32 needs d <= 128");
     da::SimtParams p{};
     p.q1 = p.q2 = static_cast<const float*>(q);
     p.k1 = p.k2 = static_cast<const float*>(k);

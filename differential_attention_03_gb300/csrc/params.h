@@ -47,8 +47,10 @@ struct SimtParams {
   long long rows_total;
 };
 
-constexpr int kSimtMaxD = 256;
-constexpr int kSimtMaxVPerLane = 16;  // value width <= 512
-constexpr int kSimtWarps = 4;
+constexpr int kSimtMaxD = 128;
+constexpr int kSimtMaxVPerLane = 8;  // value width <= 256
+constexpr int kSimtWarps = 8;
+constexpr int kSimtRows = 32;  // query rows per CTA
+constexpr int kSimtKeys = 32;  // keys per shared-memory tile
 
 }  // namespace da

@@ -3,17 +3,15 @@
 //
 // The fp32 workload needs 1e-4 agreement after the per-head RMSNorm, which
 // tf32 tensor-core operands (10-bit mantissa) cannot hold; this kernel keeps
-// every product and sum in fp32 FFMA.
+// every product and sum in fp32 FFMA and calls expf.
 //
-// One warp owns one (batch, unit, query) row:
-//   sweep 1  lanes split the visible keys; each lane computes full dot
-//            products q1.k1_j, q2.k2_j and keeps a running (max, sum) per map;
-//            the 32 partial states are merged with shuffles;
-//   sweep 2  each lane forms p_j = e1_j / l1 - c e2_j / l2 for its keys;
-//            the p_j are broadcast and every lane accumulates its value
-//            channels (lane + 32 i) of O = sum_j p_j v_j;
-//   epilogue V1: (1 - lambda_init) * gamma * O / sqrt(mean(O^2) + eps);
-//            V2: O.
+// One CTA owns 32 query rows of one (batch, unit); each warp owns 4 rows.  Key
+// tiles of 32 keys (K1, K2, V) are staged in shared memory (K rows padded to
+// d + 1 floats so that lane = key reads are conflict-free).  Per tile a lane
+// scores its key against the warp's rows for both maps, the two online
+// (max, sum) states are updated with warp shuffles, and every lane
+// accumulates its value channels (lane + 32 c) of O1 and O2.  Epilogue:
+// O1 / l1 - c O2 / l2, then the V1 per-head RMSNorm x (1 - lambda_init).
 #pragma once
 
 #include "params.h"
@@ -22,15 +20,27 @@
 namespace da {
 
 
+// Shared-memory floats the kernel needs for query/key width d and value width dv.
+__host__ __device__ constexpr int simt_smem_floats(int d, int dv) {
+  return 2 * kSimtRows * d + 2 * kSimtKeys * (d + 1) + kSimtKeys * dv;
+}
+
 __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const SimtParams p) {
-  __shared__ float qs[kSimtWarps][2][kSimtMaxD];
+  extern __shared__ float sm[];
+  constexpr int R = kSimtRows / kSimtWarps;  // query rows per warp
+  constexpr int NC = kSimtMaxVPerLane;       // value channels per lane (lane + 32 c)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long r = static_cast<long long>(blockIdx.x) * kSimtWarps + warp;
-  if (r >= p.rows_total) return;
-  const int t = static_cast<int>(r % p.n);
-  const long long bu = r / p.n;
-  const int u = static_cast<int>(bu % p.units_per_batch);
-  const int b = static_cast<int>(bu / p.units_per_batch);
+  const int d = p.d, dv = p.dv, dp = d + 1;
+  float* sq1 = sm;
+  float* sq2 = sq1 + kSimtRows * d;
+  float* sk1 = sq2 + kSimtRows * d;
+  float* sk2 = sk1 + kSimtKeys * dp;
+  float* sv = sk2 + kSimtKeys * dp;
+
+  const int nqb = (p.n + kSimtRows - 1) / kSimtRows;
+  const int unit = blockIdx.x / nqb;
+  const int qb = nqb - 1 - static_cast<int>(blockIdx.x % nqb);  // heaviest causal blocks first
+  const int u = unit % p.units_per_batch, b = unit / p.units_per_batch;
   int hq1, hq2, hk;
   if (p.v2) {
     hq1 = 2 * u;
@@ -39,112 +49,135 @@ __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const Sim
   } else {
     hq1 = hq2 = hk = u;
   }
-  const int d = p.d, dv = p.dv;
-  const float* q1 = p.q1 + ((static_cast<size_t>(b) * p.n + t) * p.heads_q + hq1) * d;
-  const float* q2 = p.q2 + ((static_cast<size_t>(b) * p.n + t) * p.heads_q + hq2) * d;
-  for (int c = lane; c < d; c += 32) {
-    qs[warp][0][c] = q1[c];
-    qs[warp][1][c] = q2[c];
-  }
-  __syncwarp();
-  const int kend = p.causal ? t + 1 : p.n;
-  const size_t kstride = static_cast<size_t>(p.heads_kv) * d;
-  const size_t vstride = static_cast<size_t>(p.heads_kv) * dv;
-  const float* k1 = p.k1 + (static_cast<size_t>(b) * p.n * p.heads_kv + hk) * d;
-  const float* k2 = p.k2 + (static_cast<size_t>(b) * p.n * p.heads_kv + hk) * d;
-  const float* vb = p.v + (static_cast<size_t>(b) * p.n * p.heads_kv + hk) * dv;
+  const int q0 = qb * kSimtRows;
+  const size_t qrow = static_cast<size_t>(p.heads_q) * d;
+  const size_t krow = static_cast<size_t>(p.heads_kv) * d;
+  const size_t vrow = static_cast<size_t>(p.heads_kv) * dv;
+  const float* gq1 = p.q1 + (static_cast<size_t>(b) * p.n) * qrow + static_cast<size_t>(hq1) * d;
+  const float* gq2 = p.q2 + (static_cast<size_t>(b) * p.n) * qrow + static_cast<size_t>(hq2) * d;
+  const float* gk1 = p.k1 + (static_cast<size_t>(b) * p.n) * krow + static_cast<size_t>(hk) * d;
+  const float* gk2 = p.k2 + (static_cast<size_t>(b) * p.n) * krow + static_cast<size_t>(hk) * d;
+  const float* gv = p.v + (static_cast<size_t>(b) * p.n) * vrow + static_cast<size_t>(hk) * dv;
 
-  // ---- sweep 1: per-lane running max / sum, then merged across the warp
-  float m1 = -INFINITY, l1 = 0.f, m2 = -INFINITY, l2 = 0.f;
-  for (int j = lane; j < kend; j += 32) {
-    const float* a = k1 + j * kstride;
-    const float* c = k2 + j * kstride;
-    float s1 = 0.f, s2 = 0.f;
-    for (int e = 0; e < d; ++e) {
-      s1 = fmaf(qs[warp][0][e], a[e], s1);
-      s2 = fmaf(qs[warp][1][e], c[e], s2);
-    }
-    s1 *= p.scale;
-    s2 *= p.scale;
-    float mn = fmaxf(m1, s1);
-    l1 = l1 * expf(m1 - mn) + expf(s1 - mn);
-    m1 = mn;
-    mn = fmaxf(m2, s2);
-    l2 = l2 * expf(m2 - mn) + expf(s2 - mn);
-    m2 = mn;
+  for (int i = threadIdx.x; i < kSimtRows * d; i += blockDim.x) {
+    const int r = i / d, c = i % d, t = q0 + r;
+    sq1[i] = t < p.n ? gq1[t * qrow + c] : 0.f;
+    sq2[i] = t < p.n ? gq2[t * qrow + c] : 0.f;
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float om1 = __shfl_xor_sync(0xffffffffu, m1, off), ol1 = __shfl_xor_sync(0xffffffffu, l1, off);
-    const float om2 = __shfl_xor_sync(0xffffffffu, m2, off), ol2 = __shfl_xor_sync(0xffffffffu, l2, off);
-    float mn = fmaxf(m1, om1);
-    if (mn != -INFINITY) {
-      l1 = l1 * expf(m1 - mn) + ol1 * expf(om1 - mn);
-      m1 = mn;
-    }
-    mn = fmaxf(m2, om2);
-    if (mn != -INFINITY) {
-      l2 = l2 * expf(m2 - mn) + ol2 * expf(om2 - mn);
-      m2 = mn;
-    }
-  }
-  float coef;
-  if (p.v2) {
-    const float lg = p.lam_logits[b * p.sb + static_cast<long long>(t) * p.st + u];
-    coef = 1.f / (1.f + expf(-lg));
-  } else {
-    coef = *p.lambda;
-  }
-  const float inv1 = 1.f / l1, c2 = coef / l2;
 
-  // ---- sweep 2: O = sum_j p_j v_j, channels lane + 32 i
-  float o[kSimtMaxVPerLane];
+  float m1[R], l1[R], m2[R], l2[R], o1[R][NC], o2[R][NC];
 #pragma unroll
-  for (int i = 0; i < kSimtMaxVPerLane; ++i) o[i] = 0.f;
-  for (int j0 = 0; j0 < kend; j0 += 32) {
-    const int j = j0 + lane;
-    float pj = 0.f;
-    if (j < kend) {
-      const float* a = k1 + j * kstride;
-      const float* c = k2 + j * kstride;
+  for (int r = 0; r < R; ++r) {
+    m1[r] = m2[r] = -INFINITY;
+    l1[r] = l2[r] = 0.f;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) o1[r][c] = o2[r][c] = 0.f;
+  }
+  const int kend = p.causal ? min(p.n, q0 + kSimtRows) : p.n;
+  for (int k0 = 0; k0 < kend; k0 += kSimtKeys) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < kSimtKeys * d; i += blockDim.x) {
+      const int r = i / d, c = i % d, j = k0 + r;
+      sk1[r * dp + c] = j < p.n ? gk1[j * krow + c] : 0.f;
+      sk2[r * dp + c] = j < p.n ? gk2[j * krow + c] : 0.f;
+    }
+    for (int i = threadIdx.x; i < kSimtKeys * dv; i += blockDim.x) {
+      const int r = i / dv, c = i % dv, j = k0 + r;
+      sv[i] = j < p.n ? gv[j * vrow + c] : 0.f;
+    }
+    __syncthreads();
+    const int key = k0 + lane;  // this lane's key in the tile
+    float pr1[R], pr2[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int row = warp * R + r, t = q0 + row;
       float s1 = 0.f, s2 = 0.f;
       for (int e = 0; e < d; ++e) {
-        s1 = fmaf(qs[warp][0][e], a[e], s1);
-        s2 = fmaf(qs[warp][1][e], c[e], s2);
+        s1 = fmaf(sq1[row * d + e], sk1[lane * dp + e], s1);
+        s2 = fmaf(sq2[row * d + e], sk2[lane * dp + e], s2);
       }
-      pj = expf(s1 * p.scale - m1) * inv1 - expf(s2 * p.scale - m2) * c2;
-    }
-    const int cnt = min(32, kend - j0);
-    for (int jj = 0; jj < cnt; ++jj) {
-      const float w = __shfl_sync(0xffffffffu, pj, jj);
-      const float* vr = vb + (j0 + jj) * vstride;
+      const bool vis = key < p.n && (!p.causal || key <= t);
+      s1 = vis ? s1 * p.scale : -INFINITY;
+      s2 = vis ? s2 * p.scale : -INFINITY;
+      float mx1 = s1, mx2 = s2;
 #pragma unroll
-      for (int i = 0; i < kSimtMaxVPerLane; ++i) {
-        const int c = lane + 32 * i;
-        if (c < dv) o[i] = fmaf(w, vr[c], o[i]);
+      for (int off = 16; off > 0; off >>= 1) {
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        mx2 = fmaxf(mx2, __shfl_xor_sync(0xffffffffu, mx2, off));
+      }
+      const float n1 = fmaxf(m1[r], mx1), n2 = fmaxf(m2[r], mx2);
+      // A row sees at least key 0 in the first tile, so n1, n2 are finite.
+      const float f1 = expf(m1[r] - n1), f2 = expf(m2[r] - n2);
+      pr1[r] = expf(s1 - n1);
+      pr2[r] = expf(s2 - n2);
+      float sum1 = pr1[r], sum2 = pr2[r];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        sum1 += __shfl_xor_sync(0xffffffffu, sum1, off);
+        sum2 += __shfl_xor_sync(0xffffffffu, sum2, off);
+      }
+      l1[r] = l1[r] * f1 + sum1;
+      l2[r] = l2[r] * f2 + sum2;
+      m1[r] = n1;
+      m2[r] = n2;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        o1[r][c] *= f1;
+        o2[r][c] *= f2;
+      }
+    }
+    const int cnt = min(kSimtKeys, kend - k0);
+    for (int kk = 0; kk < cnt; ++kk) {
+      float vv[NC];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) vv[c] = (lane + 32 * c < dv) ? sv[kk * dv + lane + 32 * c] : 0.f;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float w1 = __shfl_sync(0xffffffffu, pr1[r], kk);
+        const float w2 = __shfl_sync(0xffffffffu, pr2[r], kk);
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          o1[r][c] = fmaf(w1, vv[c], o1[r][c]);
+          o2[r][c] = fmaf(w2, vv[c], o2[r][c]);
+        }
       }
     }
   }
 
-  // ---- epilogue
-  float rinv = 1.f;
-  if (!p.v2) {
+  // ---- epilogue: out = O1 / l1 - c O2 / l2 (then the V1 norm)
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int t = q0 + warp * R + r;
+    if (t >= p.n) continue;  // warp-uniform
+    float coef;
+    if (p.v2) {
+      coef = 1.f / (1.f + expf(-p.lam_logits[b * p.sb + static_cast<long long>(t) * p.st + u]));
+    } else {
+      coef = *p.lambda;
+    }
+    const float a1 = 1.f / l1[r], a2 = coef / l2[r];
+    float y[NC];
     float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < kSimtMaxVPerLane; ++i)
-      if (lane + 32 * i < dv) ss = fmaf(o[i], o[i], ss);
+    for (int c = 0; c < NC; ++c) {
+      y[c] = o1[r][c] * a1 - o2[r][c] * a2;
+      if (lane + 32 * c < dv) ss = fmaf(y[c], y[c], ss);
+    }
+    float rinv = 1.f;
+    if (!p.v2) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    rinv = p.norm_mult * rsqrtf(ss / dv + p.eps);
-  }
-  float* orow = p.out + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * dv;
+      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      rinv = p.norm_mult * rsqrtf(ss / dv + p.eps);
+    }
+    float* orow = p.out + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * dv;
 #pragma unroll
-  for (int i = 0; i < kSimtMaxVPerLane; ++i) {
-    const int c = lane + 32 * i;
-    if (c < dv) {
-      float y = o[i] * rinv;
-      if (!p.v2 && p.gamma != nullptr) y *= p.gamma[c];
-      orow[c] = y;
+    for (int c = 0; c < NC; ++c) {
+      const int col = lane + 32 * c;
+      if (col < dv) {
+        float v = y[c] * rinv;
+        if (!p.v2 && p.gamma != nullptr) v *= p.gamma[col];
+        orow[col] = v;
+      }
     }
   }
 }

@@ -87,7 +87,7 @@ diffattn_status lambda_reparam(const float* lq1, const float* lk1, const float* 
  *   dt          : DIFFATTN_BF16 or DIFFATTN_F32; q*, k*, v and out share it.
  *   B, H, n, d  : batch, diff heads, tokens, per-map query/key width.  The
  *                 value width is 2d.  bf16 needs d in {64, 128}; f32 needs
- *                 d in [1, 256].  n = 0 or B = 0 or H = 0 is a no-op.
+ *                 d in [1, 128].  n = 0 or B = 0 or H = 0 is a no-op.
  *   q1, q2, k1, k2 : [B, n, H, d];  v, out : [B, n, H, 2d].
  *   lambda      : device fp32 scalar (e.g. written by lambda_reparam).
  *   lambda_init : host float, the fixed norm multiplier is (1 - lambda_init).
@@ -116,7 +116,7 @@ diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d,
  *
  *   q   : [B, n, Hq, d];  k, v : [B, n, Hkv, d];  out : [B, n, Hq/2, d].
  *   Hq even, Hq % Hkv == 0 and (Hq / Hkv) even (so a pair never straddles
- *   two KV heads).  bf16 needs d = 128; f32 needs d in [1, 256].
+ *   two KV heads).  bf16 needs d = 128; f32 needs d in [1, 128].
  *   lam_logits : device fp32; the logit of (b, t, g) is
  *                lam_logits[b*sb + t*st + g]  (sb = st = 0: one logit per pair).
  *   softmax_scale : <= 0 selects 1/sqrt(d).
