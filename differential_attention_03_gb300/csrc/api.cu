@@ -330,7 +330,9 @@ diffattn_status diffattn_debug_wait_timeout(long long budget_ns, void* stream) {
   int* status = nullptr;
   diffattn_status st = status_word(&status);
   if (st != DIFFATTN_OK) return st;
-  cudaError_t e = da::launch_wait_selftest(static_cast<unsigned long long>(budget_ns), status,
+  // The in-kernel budget counts SM cycles; 2 cycles per nanosecond (the
+  // clock is at most 2.07 GHz) makes the wait last at least about budget_ns.
+  cudaError_t e = da::launch_wait_selftest(static_cast<unsigned long long>(budget_ns) * 2ull, status,
                                            static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_debug_wait_timeout launch");
   g_launches.fetch_add(1);

@@ -15,8 +15,8 @@ cudaError_t launch_lambda_reparam(const float* lq1, const float* lk1, const floa
   lambda_reparam_kernel<<<1, 32, 0, s>>>(lq1, lk1, lq2, lk2, dim, lambda_init, out);
   return cudaGetLastError();
 }
-cudaError_t launch_wait_selftest(unsigned long long budget_ns, int* status, cudaStream_t s) {
-  wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(budget_ns, status);
+cudaError_t launch_wait_selftest(unsigned long long budget_cycles, int* status, cudaStream_t s) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(budget_cycles, status);
   return cudaGetLastError();
 }
 }  // namespace da

@@ -18,6 +18,6 @@ cudaError_t launch_onepass_v2_d128(const TwoPassParams& p, int grid, cudaStream_
 cudaError_t launch_simt_f32(const SimtParams& p, cudaStream_t s);
 cudaError_t launch_lambda_reparam(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
                                   int dim, float lambda_init, float* out, cudaStream_t s);
-cudaError_t launch_wait_selftest(unsigned long long budget_ns, int* status, cudaStream_t s);
+cudaError_t launch_wait_selftest(unsigned long long budget_cycles, int* status, cudaStream_t s);
 
 }  // namespace da

@@ -22,17 +22,21 @@
 // Rescaling is conditional: a row keeps its reference maximum until the true
 // maximum exceeds it by more than 2^8 (P then stays below 256, exact enough in
 // bf16 and far from fp32 overflow); when any row of a warp must move, the warp
-// rescales its rows of O_r and l_r.  Both halves of a map see the same row
-// maximum (exchanged through shared memory), so they take the same decisions.
+// rescales its rows of O_r and l_r.
 //
-// Roles (576 threads, one CTA per SM):
+// P placement (template flag PSM): in TMEM over S_r (the S_r buffer is busy
+// until PV_r completes, so QK_r(j+1) follows PV_r(j)), or in shared memory
+// (S_r is released as soon as it is loaded, QK_r(j+1) is issued before
+// PV_r(j), and a pv_done barrier guards the P buffer and O_r rescales).
+//
+// Roles (320 threads, one CTA per SM):
 //   warp 0      TMA producer (Q once; then K_1, K_2 / K and V tiles into a ring
 //               of NSLOT equal slots, in the MMA thread's consumption order).
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer.
-//   warps 2-17  four softmax warpgroups; warpgroup w handles map w/2, key
-//               columns [64 (w%2), +64); thread = one query row (TMEM lane
-//               32 (warp % 4) + lane).  Epilogue: warpgroup w owns output
-//               channels [32 w, +32).
+//   warps 2-9   two softmax warpgroups, one per map; thread = one query row
+//               (TMEM lane 32 (warp % 4) + lane) holding all 128 key columns
+//               of a tile, so no row statistic is exchanged between threads.
+//               Epilogue: warpgroup r owns output channels [64 r, +64).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -42,13 +46,13 @@
 
 namespace da {
 
-template <int D, bool SHARED_K, int EPI, int NSLOT>
+template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM>
 struct OnePassCfg {
   static constexpr int BM = 128;
   static constexpr int BN = 128;
   static constexpr int DV = 128;
   static constexpr int NCTRL = 2;  // producer, MMA
-  static constexpr int NSMWG = 4;
+  static constexpr int NSMWG = 2;  // one softmax warpgroup per map
   static constexpr int NTHREADS = (NCTRL + 4 * NSMWG) * 32;
   static constexpr int QB = D / 64;
   static constexpr int VB = DV / 64;
@@ -58,16 +62,17 @@ struct OnePassCfg {
   static constexpr int SLOT = K_TILE;
   static constexpr int VF = V_TILE / SLOT;
   static constexpr int VKEYS = BN / VF;
+  static constexpr int P_TILE = BM * BN * 2;  // one map's P (bf16) when it lives in shared memory
   static constexpr int OFF_Q1 = 0;
   static constexpr int OFF_Q2 = Q_TILE;
-  static constexpr int OFF_RING = 2 * Q_TILE;
+  static constexpr int OFF_P = 2 * Q_TILE;
+  static constexpr int OFF_RING = OFF_P + (PSM ? 2 * P_TILE : 0);
   static constexpr int OFF_BARS = OFF_RING + NSLOT * SLOT;
-  static constexpr int NBARS = 2 + 2 * NSLOT + 4;
+  static constexpr int NBARS = 2 + 2 * NSLOT + 8;
   static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
-  static constexpr int OFF_RED = (OFF_MISC + 16 + 15) / 16 * 16;  // float [2 parity][2 maps][2 halves][128]
-  static constexpr int OFF_LP = OFF_RED + 2 * 2 * 2 * 128 * 4;    // float [4][128]
-  static constexpr int OFF_SS = OFF_LP + 4 * 128 * 4;             // float [4][128]
-  static constexpr int SMEM_BYTES = OFF_SS + 4 * 128 * 4 + 1024;  // + 1 KB alignment slack
+  static constexpr int OFF_LP = (OFF_MISC + 16 + 15) / 16 * 16;  // float [2][128]
+  static constexpr int OFF_SS = OFF_LP + 2 * 128 * 4;             // float [2][128]
+  static constexpr int SMEM_BYTES = OFF_SS + 2 * 128 * 4 + 1024;  // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TM_O1 = 0, TM_O2 = 128, TM_A = 256, TM_B = 384;
   static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false, false);
@@ -79,9 +84,9 @@ struct OnePassCfg {
   static_assert(NSLOT >= 4, "ring depth");
 };
 
-template <int D, bool SHARED_K, int EPI, int NSLOT>
-__global__ void __launch_bounds__(576, 1) onepass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
-  using C = OnePassCfg<D, SHARED_K, EPI, NSLOT>;
+template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM>
+__global__ void __launch_bounds__(320, 1) onepass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
+  using C = OnePassCfg<D, SHARED_K, EPI, NSLOT, PSM>;
   constexpr int BM = C::BM, BN = C::BN, DV = C::DV;
 
   extern __shared__ uint8_t smem_raw[];
@@ -96,10 +101,11 @@ __global__ void __launch_bounds__(576, 1) onepass_fwd_kernel(const __grid_consta
   uint64_t* full = bars + 2;
   uint64_t* empty = full + NSLOT;
   uint64_t* s_full = empty + NSLOT;  // [2]: S_r of the current tile in its buffer
-  uint64_t* p_ready = s_full + 2;    // [2]: P_r of the current tile in its buffer
+  uint64_t* p_ready = s_full + 2;    // [2]: P_r of the current tile written
+  uint64_t* s_free = p_ready + 2;    // [2]: (P in shared memory) S_r loaded by the softmax warps
+  uint64_t* pv_done = s_free + 2;    // [2]: (P in shared memory) PV_r of the tile completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
-  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
   float* lpart = reinterpret_cast<float*>(smem + C::OFF_LP);
   float* sspart = reinterpret_cast<float*>(smem + C::OFF_SS);
 
@@ -137,7 +143,9 @@ __global__ void __launch_bounds__(576, 1) onepass_fwd_kernel(const __grid_consta
     }
     for (int r = 0; r < 2; ++r) {
       mbar_init(&s_full[r], 1);
-      mbar_init(&p_ready[r], 8);  // the 8 warps of the map's two warpgroups
+      mbar_init(&p_ready[r], 4);  // the map's 4 warps
+      mbar_init(&s_free[r], 4);
+      mbar_init(&pv_done[r], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -183,16 +191,20 @@ __global__ void __launch_bounds__(576, 1) onepass_fwd_kernel(const __grid_consta
       load(&p.tm_k1, 0, BN, C::QB);
       if (!SHARED_K) load(&p.tm_k2, 0, BN, C::QB);
       for (int j = 0; j < T; ++j) {
+        // Consumption order: with P in shared memory the next tile's QK^T is
+        // issued before this tile's PV, otherwise after it.
+        if (PSM && j + 1 < T) load(&p.tm_k1, (j + 1) * BN, BN, C::QB);
         for (int part = 0; part < C::VF; ++part) load(&p.tm_v, j * BN + part * C::VKEYS, C::VKEYS, C::VB);
-        if (j + 1 < T) {
+        if (PSM && j + 1 < T && !SHARED_K) load(&p.tm_k2, (j + 1) * BN, BN, C::QB);
+        if (!PSM && j + 1 < T) {
           load(&p.tm_k1, (j + 1) * BN, BN, C::QB);
           if (!SHARED_K) load(&p.tm_k2, (j + 1) * BN, BN, C::QB);
         }
       }
       if (*ab.flag) {
-        mbar_wait_drain(q_full, 0, kWaitBudgetNs);
+        mbar_wait_drain(q_full, 0, kWaitBudgetCycles);
         for (int f = (fill > NSLOT ? fill - NSLOT : 0); f < fill; ++f)
-          mbar_wait_drain(&full[f % NSLOT], static_cast<uint32_t>(f / NSLOT) & 1u, kWaitBudgetNs);
+          mbar_wait_drain(&full[f % NSLOT], static_cast<uint32_t>(f / NSLOT) & 1u, kWaitBudgetCycles);
       }
     }
   } else if (warp == 1) {
@@ -236,6 +248,21 @@ __global__ void __launch_bounds__(576, 1) onepass_fwd_kernel(const __grid_consta
           }
         }
       };
+      // PV with P from shared memory (K-major, 128-byte swizzle, two 64-key boxes).
+      const uint64_t dP1 = sdesc_sw128(smem_u32(smem + C::OFF_P), 16, 1024);
+      const uint64_t dP2 = sdesc_sw128(smem_u32(smem + C::OFF_P + C::P_TILE), 16, 1024);
+      auto pv_ss = [&](uint32_t dO, uint64_t dP, int j) {
+#pragma unroll
+        for (int part = 0; part < C::VF; ++part) {
+          const uint64_t dv = dRingV + static_cast<uint64_t>((sv[part] * C::SLOT) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < C::VKEYS / 16; ++kk) {
+            const int kg = part * (C::VKEYS / 16) + kk;
+            mma_ss(dO, dP + static_cast<uint64_t>((((kg >> 2) * (BM * 128)) + (kg & 3) * 32) >> 4),
+                   dv + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_PV, (j > 0 || kg > 0) ? 1u : 0u);
+          }
+        }
+      };
       int sk = 0;
       if (ok) ok = acquire(sk);
       if (ok) {
@@ -251,46 +278,82 @@ __global__ void __launch_bounds__(576, 1) onepass_fwd_kernel(const __grid_consta
         tc_commit(&s_full[1]);
         tc_commit(&empty[sk]);
       }
-      for (int j = 0; ok && j < T; ++j) {
-        for (int part = 0; part < C::VF; ++part)
-          if (!acquire(sv[part])) ok = false;
-        if (!ok) break;
-        if (!mbar_wait(&p_ready[0], static_cast<uint32_t>(j) & 1u, ab)) break;
-        tc_fence_after();
-        pv(tO1, tA, j);
-        if (j + 1 < T) {
-          if (!acquire(sk)) break;
-          qk(tA, dQ1, sk);
-          tc_commit(&s_full[0]);
-          if (!SHARED_K) tc_commit(&empty[sk]);
+      if constexpr (PSM) {
+        // Per tile: QK1(j+1) as soon as S1(j) is loaded, PV1(j), QK2(j+1) as
+        // soon as S2(j) is loaded, PV2(j).
+        for (int j = 0; ok && j < T; ++j) {
+          const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+          if (j + 1 < T) {
+            if (!acquire(sk)) break;
+            if (!mbar_wait(&s_free[0], ph, ab)) break;
+            tc_fence_after();
+            qk(tA, dQ1, sk);
+            tc_commit(&s_full[0]);
+            if (!SHARED_K) tc_commit(&empty[sk]);
+          }
+          for (int part = 0; part < C::VF; ++part)
+            if (!acquire(sv[part])) ok = false;
+          if (!ok) break;
+          if (!mbar_wait(&p_ready[0], ph, ab)) break;
+          tc_fence_after();
+          pv_ss(tO1, dP1, j);
+          tc_commit(&pv_done[0]);
+          if (j + 1 < T) {
+            if (!SHARED_K && !acquire(sk)) break;
+            if (!mbar_wait(&s_free[1], ph, ab)) break;
+            tc_fence_after();
+            qk(tB, dQ2, sk);
+            tc_commit(&s_full[1]);
+            tc_commit(&empty[sk]);
+          }
+          if (!mbar_wait(&p_ready[1], ph, ab)) break;
+          tc_fence_after();
+          pv_ss(tO2, dP2, j);
+          tc_commit(&pv_done[1]);
+          for (int part = 0; part < C::VF; ++part) tc_commit(&empty[sv[part]]);
         }
-        if (!mbar_wait(&p_ready[1], static_cast<uint32_t>(j) & 1u, ab)) break;
-        tc_fence_after();
-        pv(tO2, tB, j);
-        for (int part = 0; part < C::VF; ++part) tc_commit(&empty[sv[part]]);
-        if (j + 1 < T) {
-          if (!SHARED_K && !acquire(sk)) break;
-          qk(tB, dQ2, sk);
-          tc_commit(&s_full[1]);
-          tc_commit(&empty[sk]);
+      } else {
+      for (int j = 0; ok && j < T; ++j) {
+          for (int part = 0; part < C::VF; ++part)
+            if (!acquire(sv[part])) ok = false;
+          if (!ok) break;
+          if (!mbar_wait(&p_ready[0], static_cast<uint32_t>(j) & 1u, ab)) break;
+          tc_fence_after();
+          pv(tO1, tA, j);
+          if (j + 1 < T) {
+            if (!acquire(sk)) break;
+            qk(tA, dQ1, sk);
+            tc_commit(&s_full[0]);
+            if (!SHARED_K) tc_commit(&empty[sk]);
+          }
+          if (!mbar_wait(&p_ready[1], static_cast<uint32_t>(j) & 1u, ab)) break;
+          tc_fence_after();
+          pv(tO2, tB, j);
+          for (int part = 0; part < C::VF; ++part) tc_commit(&empty[sv[part]]);
+          if (j + 1 < T) {
+            if (!SHARED_K && !acquire(sk)) break;
+            qk(tB, dQ2, sk);
+            tc_commit(&s_full[1]);
+            tc_commit(&empty[sk]);
+          }
         }
       }
       tc_commit(o_full);
-      if (*ab.flag) mbar_wait_drain(o_full, 0, kWaitBudgetNs);
+      if (*ab.flag) mbar_wait_drain(o_full, 0, kWaitBudgetCycles);
     }
   } else {
     // =============================================================== softmax + epilogue
-    const int w = warp - C::NCTRL;
-    const int wg = w >> 2;  // 0..3
-    const int wq = warp & 3;  // TMEM lane quarter
+    // Warpgroup `map` owns map (map + 1); thread = one query row, all 128 key
+    // columns of each tile, so no row statistic is shared between threads.
+    const int map = (warp - C::NCTRL) >> 2;  // 0 or 1
+    const int wq = warp & 3;                  // TMEM lane quarter
     const int row = wq * 32 + lane;
     const int t = q0 + row;
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float sc = p.scale_log2;
     const int lim = p.causal ? min(t + 1, p.n) : p.n;
-    const int map = wg >> 1, half = wg & 1;
     const uint32_t tS = tl + (map ? C::TM_B : C::TM_A);
-    const uint32_t tOr = tl + (map ? C::TM_O2 : C::TM_O1) + 64u * half;
+    const uint32_t tOr = tl + (map ? C::TM_O2 : C::TM_O1);
     const uint64_t sc2 = f2pack(sc, sc);
     float m_used = -INFINITY, l = 0.f;
 
@@ -298,40 +361,39 @@ __global__ void __launch_bounds__(576, 1) onepass_fwd_kernel(const __grid_consta
       mbar_wait(&s_full[map], static_cast<uint32_t>(j) & 1u, ab);
       __syncwarp();
       tc_fence_after();
-      uint32_t x0[32], x1[32];
-      tmem_ld32(tS + 64u * half, x0);
-      tmem_ld32(tS + 64u * half + 32u, x1);
-      tmem_ld_wait2(x0, x1);
-      const int nvis = lim - (j * BN + 64 * half);
-      if (nvis < 64) {
+      uint32_t x[4][32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          if (c >= nvis) x0[c] = __float_as_uint(-INFINITY);
-          if (c + 32 >= nvis) x1[c] = __float_as_uint(-INFINITY);
-        }
+      for (int q = 0; q < 4; ++q) tmem_ld32(tS + 32u * q, x[q]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld_wait(x[q]);
+      if constexpr (PSM) {
+        // S_r is in registers: the next tile's QK^T may overwrite the buffer.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[map]);
+        __syncwarp();
       }
-      float tm[11];
+      const int nvis = lim - j * BN;
+      if (nvis < BN) {
 #pragma unroll
-      for (int c = 0; c < 10; ++c)
-        tm[c] = max3(__uint_as_float(x0[3 * c]), __uint_as_float(x0[3 * c + 1]), __uint_as_float(x0[3 * c + 2]));
-      tm[10] = max3(__uint_as_float(x0[30]), __uint_as_float(x0[31]), __uint_as_float(x1[0]));
-      float tn[11];
+        for (int q = 0; q < 4; ++q)
 #pragma unroll
-      for (int c = 0; c < 10; ++c)
-        tn[c] = max3(__uint_as_float(x1[3 * c + 1]), __uint_as_float(x1[3 * c + 2]), __uint_as_float(x1[3 * c + 3]));
-      tn[10] = __uint_as_float(x1[31]);
-      const float pmax = max3(max3(max3(tm[0], tm[1], tm[2]), max3(tm[3], tm[4], tm[5]), max3(tm[6], tm[7], tm[8])),
-                              max3(tm[9], tm[10], tn[0]),
-                              max3(max3(tn[1], tn[2], tn[3]), max3(tn[4], tn[5], tn[6]), max3(tn[7], tn[8], fmaxf(tn[9], tn[10]))));
-      // Exchange the half-row maxima with the other warpgroup of this map.
-      float* rbuf = red + ((j & 1) * 2 + map) * 256;
-      rbuf[half * 128 + row] = pmax;
-      __syncwarp();
-      named_bar_sync(1 + map, 256);
-      const float mx = fmaxf(pmax, rbuf[(half ^ 1) * 128 + row]);
+          for (int c = 0; c < 32; ++c)
+            if (32 * q + c >= nvis) x[q][c] = __float_as_uint(-INFINITY);
+      }
+      float mq[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float tm[11];
+#pragma unroll
+        for (int c = 0; c < 10; ++c)
+          tm[c] = max3(__uint_as_float(x[q][3 * c]), __uint_as_float(x[q][3 * c + 1]), __uint_as_float(x[q][3 * c + 2]));
+        tm[10] = fmaxf(__uint_as_float(x[q][30]), __uint_as_float(x[q][31]));
+        mq[q] = max3(max3(tm[0], tm[1], tm[2]), max3(tm[3], tm[4], tm[5]), max3(max3(tm[6], tm[7], tm[8]), tm[9], tm[10]));
+      }
+      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       const float m_new = fmaxf(m_used, mx * sc);
-      const bool need = m_new > m_used + C::RESCALE_THRESHOLD;
-      const bool rescale = __any_sync(0xffffffffu, need);
+      const bool rescale = __any_sync(0xffffffffu, m_new > m_used + C::RESCALE_THRESHOLD);
       float factor = 1.f;
       if (rescale) {
         factor = ex2(m_used - m_new);  // 0 on the first tile
@@ -339,36 +401,58 @@ __global__ void __launch_bounds__(576, 1) onepass_fwd_kernel(const __grid_consta
         m_used = m_new;
       }
       const uint64_t nb2 = f2pack(-m_used, -m_used);
-      uint64_t acc0 = 0, acc1 = 0;
-      // P pairs are packed in place over score registers already consumed.
+      uint64_t acc[4] = {0, 0, 0, 0};
+      // P pairs are packed in place over score registers already consumed:
+      // x[q][0..15] then hold key columns 32 q .. 32 q + 31 as bf16 pairs.
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float a0, a1, b0, b1;
-        f2unpack(fma2(f2pack(__uint_as_float(x0[c]), __uint_as_float(x0[c + 1])), sc2, nb2), a0, a1);
-        f2unpack(fma2(f2pack(__uint_as_float(x1[c]), __uint_as_float(x1[c + 1])), sc2, nb2), b0, b1);
-        const float pa0 = ex2(a0), pa1 = ex2(a1), pb0 = ex2(b0), pb1 = ex2(b1);
-        acc0 = add2(acc0, f2pack(pa0, pa1));
-        acc1 = add2(acc1, f2pack(pb0, pb1));
-        x0[c >> 1] = pack_bf16x2(pa0, pa1);
-        x1[c >> 1] = pack_bf16x2(pb0, pb1);
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float a0, a1;
+          f2unpack(fma2(f2pack(__uint_as_float(x[q][c]), __uint_as_float(x[q][c + 1])), sc2, nb2), a0, a1);
+          const float p0 = ex2(a0), p1 = ex2(a1);
+          acc[q] = add2(acc[q], f2pack(p0, p1));
+          x[q][c >> 1] = pack_bf16x2(p0, p1);
+        }
       }
-      float s0, s1;
-      f2unpack(add2(acc0, acc1), s0, s1);
-      l += s0 + s1;
-      // P of key columns [64 half, +64) -> buffer columns [32 half, +32).  The
-      // other half finished reading those S columns before the exchange above.
-      tmem_st16(tS + 32u * half, reinterpret_cast<const uint32_t(&)[16]>(x0));
-      tmem_st16(tS + 32u * half + 16u, reinterpret_cast<const uint32_t(&)[16]>(x1));
-      if (rescale && j > 0) {
-        // PV_r(j-1) has completed (it was issued before QK_r(j)), so O_r is quiescent.
+      float s0, s1, s2, s3;
+      f2unpack(add2(acc[0], acc[1]), s0, s1);
+      f2unpack(add2(acc[2], acc[3]), s2, s3);
+      l += (s0 + s1) + (s2 + s3);
+      if constexpr (PSM) {
+        // PV_r(j-1) must be complete before P_r is overwritten or O_r rescaled.
+        if (j > 0) {
+          mbar_wait(&pv_done[map], static_cast<uint32_t>(j - 1) & 1u, ab);
+          __syncwarp();
+          tc_fence_after();
+        }
+        // Row `row` of P_r: 64-key box q/2, 16-byte chunks 4 (q%2) .. 4 (q%2) + 3.
 #pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
+        for (int q = 0; q < 4; ++q) {
+          uint8_t* prow = smem + C::OFF_P + map * C::P_TILE + (q >> 1) * (BM * 128) + row * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(prow + (((4 * (q & 1) + c) ^ (row & 7)) << 4)) =
+                make_uint4(x[q][4 * c], x[q][4 * c + 1], x[q][4 * c + 2], x[q][4 * c + 3]);
+        }
+        fence_proxy_async_smem();
+      } else {
+        // P of key columns 32 q .. 32 q + 31 -> buffer columns 16 q .. 16 q + 15
+        // (this thread's own row; it has read all of its S columns).
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_st16(tS + 16u * q, reinterpret_cast<const uint32_t(&)[16]>(x[q]));
+      }
+      if (rescale && j > 0) {
+        // PSM: PV_r(j-1) completed (awaited above).  Otherwise it completed
+        // before S_r(j) did: it was issued before QK_r(j).
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
           uint32_t o[32];
-          tmem_ld32(tOr + 32u * ch, o);
+          tmem_ld32(tOr + 32u * q, o);
           tmem_ld_wait(o);
 #pragma unroll
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * factor);
-          tmem_st32(tOr + 32u * ch, o);
+          tmem_st32(tOr + 32u * q, o);
         }
       }
       tmem_st_wait();
@@ -378,14 +462,13 @@ __global__ void __launch_bounds__(576, 1) onepass_fwd_kernel(const __grid_consta
       __syncwarp();
     }
 
-    // ---- epilogue: out = O_1 / l_1 - c O_2 / l_2 over channels [32 wg, +32)
-    lpart[wg * 128 + row] = l;
+    // ---- epilogue: out = O_1 / l_1 - c O_2 / l_2; warpgroup `map` owns channels [64 map, +64)
+    lpart[map * 128 + row] = l;
     mbar_wait(o_full, 0, ab);
     __syncwarp();
     tc_fence_after();
-    named_bar_sync(3, 128 * C::NSMWG);
-    const float l1 = lpart[row] + lpart[128 + row];
-    const float l2 = lpart[256 + row] + lpart[384 + row];
+    named_bar_sync(1, 128 * C::NSMWG);
+    const float l1 = lpart[row], l2 = lpart[128 + row];
     float coef;
     if (EPI == kEpiRmsNorm) {
       coef = *p.lambda;
@@ -394,43 +477,48 @@ __global__ void __launch_bounds__(576, 1) onepass_fwd_kernel(const __grid_consta
       coef = 1.f / (1.f + expf(-lg));
     }
     const float a1 = 1.f / l1, a2 = -coef / l2;
-    uint32_t o1[32], o2[32];
-    tmem_ld32(tl + C::TM_O1 + 32u * wg, o1);
-    tmem_ld32(tl + C::TM_O2 + 32u * wg, o2);
-    tmem_ld_wait2(o1, o2);
-    float y[32];
+    float y[2][32];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) y[c] = fmaf(__uint_as_float(o2[c]), a2, __uint_as_float(o1[c]) * a1);
+    for (int h = 0; h < 2; ++h) {
+      uint32_t o1[32], o2[32];
+      tmem_ld32(tl + C::TM_O1 + 64u * map + 32u * h, o1);
+      tmem_ld32(tl + C::TM_O2 + 64u * map + 32u * h, o2);
+      tmem_ld_wait2(o1, o2);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) y[h][c] = fmaf(__uint_as_float(o2[c]), a2, __uint_as_float(o1[c]) * a1);
+    }
     float rinv = 1.f;
     if (EPI == kEpiRmsNorm) {
       float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        ss0 = fmaf(y[c], y[c], ss0);
-        ss1 = fmaf(y[c + 1], y[c + 1], ss1);
+      for (int c = 0; c < 32; ++c) {
+        ss0 = fmaf(y[0][c], y[0][c], ss0);
+        ss1 = fmaf(y[1][c], y[1][c], ss1);
       }
-      sspart[wg * 128 + row] = ss0 + ss1;
+      sspart[map * 128 + row] = ss0 + ss1;
       __syncwarp();
-      named_bar_sync(3, 128 * C::NSMWG);
-      const float tot = (sspart[row] + sspart[128 + row]) + (sspart[256 + row] + sspart[384 + row]);
-      rinv = p.norm_mult * rsqrtf(tot * (1.f / DV) + p.eps);
+      named_bar_sync(1, 128 * C::NSMWG);
+      rinv = p.norm_mult * rsqrtf((sspart[row] + sspart[128 + row]) * (1.f / DV) + p.eps);
     }
     if (t < p.n) {
       __nv_bfloat16* orow =
-          p.out + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * DV + 32 * wg;
-      uint32_t wv[16];
+          p.out + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * DV + 64 * map;
 #pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float y0 = y[c] * rinv, y1 = y[c + 1] * rinv;
-        if (EPI == kEpiRmsNorm && p.gamma != nullptr) {
-          y0 *= __ldg(p.gamma + 32 * wg + c);
-          y1 *= __ldg(p.gamma + 32 * wg + c + 1);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t wv[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float y0 = y[h][c] * rinv, y1 = y[h][c + 1] * rinv;
+          if (EPI == kEpiRmsNorm && p.gamma != nullptr) {
+            y0 *= __ldg(p.gamma + 64 * map + 32 * h + c);
+            y1 *= __ldg(p.gamma + 64 * map + 32 * h + c + 1);
+          }
+          wv[c >> 1] = pack_bf16x2(y0, y1);
         }
-        wv[c >> 1] = pack_bf16x2(y0, y1);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(orow);
+        uint4* dst = reinterpret_cast<uint4*>(orow + 32 * h);
 #pragma unroll
-      for (int v = 0; v < 4; ++v) dst[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+      }
     }
   }
 

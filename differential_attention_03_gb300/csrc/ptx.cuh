@@ -14,12 +14,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 // ----------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -59,18 +53,18 @@ struct AbortState {
 
 // Waits for the phase of `bar` with parity `parity` to complete.  Returns
 // false (and records DIFFATTN_ERR_TIMEOUT) if it has not completed within
-// kWaitBudgetNs, or if the CTA has already aborted.
+// kWaitBudgetCycles SM clocks, or if the CTA has already aborted.  The budget
+// is counted with clock64 (a cheap per-SM counter), checked every 64 polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const AbortState& ab,
-                                          uint64_t budget_ns = kWaitBudgetNs) {
+                                          uint64_t budget_cycles = kWaitBudgetCycles) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
-  if (*ab.flag) return false;
-  const uint64_t t0 = globaltimer_ns();
+  const uint64_t t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(a, parity)) return true;
-    if ((it & 31u) == 0) {
+    if ((it & 63u) == 0) {
       if (*ab.flag) return false;
-      if (globaltimer_ns() - t0 > budget_ns) {
+      if (static_cast<uint64_t>(clock64()) - t0 > budget_cycles) {
         *ab.flag = 1;
         atomicCAS(ab.status, 0, kStatusTimeout);
         return false;
@@ -81,13 +75,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 
 // Bounded wait used only while tearing down after an abort: ignores the abort
 // flag, so that copies and MMAs already in flight can land before exit.
-__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t budget_cycles) {
   const uint32_t a = smem_u32(bar);
-  const uint64_t t0 = globaltimer_ns();
+  const uint64_t t0 = clock64();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(a, parity)) return true;
-    if ((it & 31u) == 31u && globaltimer_ns() - t0 > budget_ns) return false;
+    if ((it & 63u) == 63u && static_cast<uint64_t>(clock64()) - t0 > budget_cycles) return false;
   }
+}
+
+// Makes this thread's generic-proxy shared-memory writes visible to the async
+// proxy (tcgen05.mma operand reads, TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ----------------------------------------------------------------- named barriers

@@ -200,7 +200,7 @@ __global__ void lambda_reparam_kernel(const float* lq1, const float* lk1, const 
 
 // Self-test of the bounded wait: one thread waits on an mbarrier that nothing
 // arrives on; the wait must run out and record the timeout status.
-__global__ void wait_timeout_selftest_kernel(unsigned long long budget_ns, int* status) {
+__global__ void wait_timeout_selftest_kernel(unsigned long long budget_cycles, int* status) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int flag;
   if (threadIdx.x == 0) {
@@ -211,7 +211,7 @@ __global__ void wait_timeout_selftest_kernel(unsigned long long budget_ns, int* 
   __syncthreads();
   if (threadIdx.x == 0) {
     const AbortState ab{&flag, status};
-    mbar_wait(&bar, 0, ab, budget_ns);
+    mbar_wait(&bar, 0, ab, budget_cycles);
   }
 }
 

@@ -8,9 +8,10 @@ namespace da {
 constexpr int kStatusOk = 0;
 constexpr int kStatusTimeout = 7;  // DIFFATTN_ERR_TIMEOUT
 
-// Budget of one in-kernel wait.  Every legitimate wait in these kernels lasts
-// microseconds; one second leaves room for time-slicing with other contexts
-// while still ending a wait on a phase that will never complete.
-constexpr uint64_t kWaitBudgetNs = 1000000000ull;
+// Budget of one in-kernel wait, in SM clock cycles (about one second at the
+// 2.07 GHz maximum clock, two at 1 GHz).  Every legitimate wait in these
+// kernels lasts microseconds; this leaves room for time-slicing with other
+// contexts while still ending a wait on a phase that will never complete.
+constexpr uint64_t kWaitBudgetCycles = 2000000000ull;
 
 }  // namespace da

@@ -267,9 +267,9 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
       }
       if (*ab.flag) {
         // Aborted: let the copies already issued land before the CTA exits.
-        mbar_wait_drain(q_full, 0, kWaitBudgetNs);
+        mbar_wait_drain(q_full, 0, kWaitBudgetCycles);
         for (int f = (fill > NSLOT ? fill - NSLOT : 0); f < fill; ++f)
-          mbar_wait_drain(&full[f % NSLOT], static_cast<uint32_t>(f / NSLOT) & 1u, kWaitBudgetNs);
+          mbar_wait_drain(&full[f % NSLOT], static_cast<uint32_t>(f / NSLOT) & 1u, kWaitBudgetCycles);
       }
     }
   } else if (warp == 1) {
@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
         }
       }
       tc_commit(o_full);
-      if (*ab.flag) mbar_wait_drain(o_full, 0, kWaitBudgetNs);
+      if (*ab.flag) mbar_wait_drain(o_full, 0, kWaitBudgetCycles);
     }
   } else if (warp >= 4) {
     // =============================================================== softmax + epilogue

@@ -22,9 +22,10 @@
  *  - Arguments are validated on the host before anything is launched; a bad
  *    argument returns a non-zero status and leaves all buffers untouched.
  *    diffattn_last_error() then returns a message (thread-local).
- *  - Kernels never trap.  Every wait inside a kernel is bounded; a wait that
- *    runs out records DIFFATTN_ERR_TIMEOUT in a device status word that
- *    diffattn_device_status() reads and clears.
+ *  - Kernels never trap.  Every wait inside a kernel is bounded (2e9 SM clock
+ *    cycles, about one second); a wait that runs out records
+ *    DIFFATTN_ERR_TIMEOUT in a device status word that diffattn_device_status()
+ *    reads and clears.
  */
 #ifndef DIFFATTN_H
 #define DIFFATTN_H
@@ -141,7 +142,8 @@ const char* diffattn_last_error(void);
 
 /*
  * Diagnostics: launches one CTA whose thread waits on an mbarrier that nothing
- * arrives on, with a budget of `budget_ns` nanoseconds (1 .. 1e9).  The wait
+ * arrives on, with a budget of about `budget_ns` nanoseconds (1 .. 1e9; the
+ * kernel counts 2 SM clock cycles per nanosecond).  The wait
  * must run out and record DIFFATTN_ERR_TIMEOUT in the status word; this is how
  * the bounded-wait path is exercised without hanging a GPU.  No copy is in
  * flight while it waits.
