@@ -50,7 +50,7 @@ struct SimtParams {
 constexpr int kSimtMaxD = 128;
 constexpr int kSimtMaxVPerLane = 8;  // value width <= 256
 constexpr int kSimtWarps = 8;
-constexpr int kSimtRows = 32;  // query rows per CTA
+constexpr int kSimtRows = 8;   // query rows per CTA (one per warp)
 constexpr int kSimtKeys = 32;  // keys per shared-memory tile
 
 }  // namespace da

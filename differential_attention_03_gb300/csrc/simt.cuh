@@ -5,7 +5,7 @@
 // tf32 tensor-core operands (10-bit mantissa) cannot hold; this kernel keeps
 // every product and sum in fp32 FFMA and calls expf.
 //
-// One CTA owns 32 query rows of one (batch, unit); each warp owns 4 rows.  Key
+// One CTA owns 8 query rows of one (batch, unit); each warp owns one row.  Key
 // tiles of 32 keys (K1, K2, V) are staged in shared memory (K rows padded to
 // d + 1 floats so that lane = key reads are conflict-free).  Per tile a lane
 // scores its key against the warp's rows for both maps, the two online
@@ -23,6 +23,61 @@ namespace da {
 // Shared-memory floats the kernel needs for query/key width d and value width dv.
 __host__ __device__ constexpr int simt_smem_floats(int d, int dv) {
   return 2 * kSimtRows * d + 2 * kSimtKeys * (d + 1) + kSimtKeys * dv;
+}
+
+// Copies rows [r0, r0 + nrows) x columns [0, width) of a strided global matrix
+// into shared memory (row pitch `pitch` floats), zero past `nvalid` rows.
+// With `vec` (width % 4 == 0, 16-byte aligned rows) it uses 16-byte loads.
+// All loads of the thread are issued before any store, so the copy costs one
+// memory round trip.
+__device__ __forceinline__ void stage_rows(float* dst, int pitch, const float* src, size_t stride, int r0,
+                                           int nvalid, int width, int nrows, bool vec) {
+  constexpr int kMaxPerThread = 8;  // 32 rows x 256 floats / 4 per load / 256 threads
+  if (vec) {
+    const int w4 = width >> 2, total = nrows * w4;
+    float4 buf[kMaxPerThread];
+#pragma unroll
+    for (int k = 0; k < kMaxPerThread; ++k) {
+      const int i = threadIdx.x + k * kSimtWarps * 32;
+      buf[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < total) {
+        const int r = i / w4, c = (i % w4) * 4;
+        if (r0 + r < nvalid) buf[k] = __ldg(reinterpret_cast<const float4*>(src + (r0 + r) * stride + c));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxPerThread; ++k) {
+      const int i = threadIdx.x + k * kSimtWarps * 32;
+      if (i < total) {
+        const int r = i / w4, c = (i % w4) * 4;
+        float* o = dst + r * pitch + c;
+        o[0] = buf[k].x;
+        o[1] = buf[k].y;
+        o[2] = buf[k].z;
+        o[3] = buf[k].w;
+      }
+    }
+  } else {
+    constexpr int kMaxScalar = 4 * kMaxPerThread;
+    const int total = nrows * width;
+    for (int base = 0; base < total; base += kMaxScalar * kSimtWarps * 32) {
+      float buf[kMaxScalar];
+#pragma unroll
+      for (int k = 0; k < kMaxScalar; ++k) {
+        const int i = base + threadIdx.x + k * kSimtWarps * 32;
+        buf[k] = 0.f;
+        if (i < total) {
+          const int r = i / width, c = i % width;
+          if (r0 + r < nvalid) buf[k] = __ldg(src + (r0 + r) * stride + c);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kMaxScalar; ++k) {
+        const int i = base + threadIdx.x + k * kSimtWarps * 32;
+        if (i < total) dst[(i / width) * pitch + i % width] = buf[k];
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const SimtParams p) {
@@ -59,11 +114,13 @@ __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const Sim
   const float* gk2 = p.k2 + (static_cast<size_t>(b) * p.n) * krow + static_cast<size_t>(hk) * d;
   const float* gv = p.v + (static_cast<size_t>(b) * p.n) * vrow + static_cast<size_t>(hk) * dv;
 
-  for (int i = threadIdx.x; i < kSimtRows * d; i += blockDim.x) {
-    const int r = i / d, c = i % d, t = q0 + r;
-    sq1[i] = t < p.n ? gq1[t * qrow + c] : 0.f;
-    sq2[i] = t < p.n ? gq2[t * qrow + c] : 0.f;
-  }
+  // Every load of a tile is issued before any of them is consumed, so a tile
+  // costs one memory round trip (16-byte loads when rows allow it).
+  const bool vec = ((d & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.q1) | reinterpret_cast<uintptr_t>(p.q2) |
+                                       reinterpret_cast<uintptr_t>(p.k1) | reinterpret_cast<uintptr_t>(p.k2) |
+                                       reinterpret_cast<uintptr_t>(p.v)) & 15u) == 0;
+  stage_rows(sq1, d, gq1, qrow, q0, p.n, d, kSimtRows, vec);
+  stage_rows(sq2, d, gq2, qrow, q0, p.n, d, kSimtRows, vec);
 
   float m1[R], l1[R], m2[R], l2[R], o1[R][NC], o2[R][NC];
 #pragma unroll
@@ -76,15 +133,9 @@ __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const Sim
   const int kend = p.causal ? min(p.n, q0 + kSimtRows) : p.n;
   for (int k0 = 0; k0 < kend; k0 += kSimtKeys) {
     __syncthreads();
-    for (int i = threadIdx.x; i < kSimtKeys * d; i += blockDim.x) {
-      const int r = i / d, c = i % d, j = k0 + r;
-      sk1[r * dp + c] = j < p.n ? gk1[j * krow + c] : 0.f;
-      sk2[r * dp + c] = j < p.n ? gk2[j * krow + c] : 0.f;
-    }
-    for (int i = threadIdx.x; i < kSimtKeys * dv; i += blockDim.x) {
-      const int r = i / dv, c = i % dv, j = k0 + r;
-      sv[i] = j < p.n ? gv[j * vrow + c] : 0.f;
-    }
+    stage_rows(sk1, dp, gk1, krow, k0, p.n, d, kSimtKeys, vec);
+    stage_rows(sk2, dp, gk2, krow, k0, p.n, d, kSimtKeys, vec);
+    stage_rows(sv, dv, gv, vrow, k0, p.n, dv, kSimtKeys, vec);
     __syncthreads();
     const int key = k0 + lane;  // this lane's key in the tile
     float pr1[R], pr2[R];

@@ -86,6 +86,7 @@ V1_SMALL = [
     ("f32", 1, 1, 128, 64, True, "ones"),
     ("f32", 2, 3, 77, 32, False, "uniform"),
     ("f32", 1, 2, 150, 128, True, "uniform"),
+    ("f32", 2, 1, 70, 30, True, "uniform"),  # d % 4 != 0: scalar staging path
 ]
 
 
