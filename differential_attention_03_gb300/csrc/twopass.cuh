@@ -24,28 +24,35 @@
 // Tiles are 128 queries x 128 keys: every QK^T MMA is M128 N128 K16, the
 // narrowest shape that runs at the full tensor rate on this part (N = 64 reads
 // the Q operand from shared memory twice as often per flop and runs at 2/3).
-// The two maps get separate TMEM buffers (A for S_1, B for S_2), so the QK^T
-// of one map runs while the softmax warps read the other.  Sweep-2 issue order
-//     QK2(j+1)  PV(j)  QK1(j+1)  QK2(j+2)  PV(j+1) ...
-// lets the softmax start the S_2 half of tile j+1 while PV(j) runs.
+//
+// Pipelining.  Each hand-off between the MMA thread and the softmax warps
+// costs several hundred cycles (commit -> mbarrier -> wake, and back), so no
+// MMA may wait on the softmax of the tile just before it:
+//   sweep 1  the O accumulator is not used yet, so all 512 TMEM columns form a
+//            ring of four 128-column S buffers (S_1(j) in buffer 2j % 4, S_2(j)
+//            in (2j+1) % 4); the MMA thread runs up to two tiles ahead.
+//   sweep 2  P goes to shared memory (128-byte swizzled, the A operand of an
+//            SS MMA), so S_1 / S_2 buffers are released as soon as the softmax
+//            has loaded them: per tile the MMA issues QK2(j+1), QK1(j+1), then
+//            PV(j), and the softmax of tile j+1 overlaps PV(j).
 //
 // Roles (640 threads, one CTA per SM):
 //   warp 0      TMA producer: Q_1, Q_2 once, then K_1 / K_2 / V tiles into a
 //               ring of NSLOT equal slots, in exactly the order warp 1
 //               consumes them; a slot is released by a tcgen05.commit after
 //               the last MMA reading it.
-//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer.
+//   warp 1      TMEM allocator and tcgen05.mma issuer (the whole warp runs the
+//               loop; one elected lane issues each MMA and commit).
 //   warps 4-19  four softmax warpgroups; thread = one query row (TMEM lane).
 //               Sweep 1: warpgroup w keeps running (max, sum) of map w/2 over
 //               key columns [64 (w%2), +64) of each tile.
 //               Sweep 2: warpgroup w owns key columns [32 w, +32) of both
-//               maps and writes its bf16 P over its own S_1 columns.
+//               maps and writes its bf16 P into shared memory.
 //               Epilogue: warpgroup w normalises/stores channels [w DV/4, +DV/4).
-// TMEM (512 columns x 128 lanes, fp32): O at [0, DV), A at [DV, DV+128),
-// B at [DV+128, DV+256).  P (bf16 pairs) of key columns 32 w .. 32 w + 31 sits
-// in A columns 32 w .. 32 w + 15.  Between the sweeps the per-warpgroup
-// statistics travel through the (still unused) O columns; the epilogue's sums
-// of squares through the A columns.
+// TMEM (512 columns x 128 lanes, fp32): sweep 1: four S buffers at 0, 128,
+// 256, 384; sweep 2: O at [0, DV), A (S_1) at [DV, DV+128), B (S_2) at
+// [DV+128, DV+256).  Between the sweeps the per-warpgroup statistics travel
+// through columns [0, 8); the epilogue's sums of squares through A.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -66,14 +73,16 @@ struct TwoPassCfg {
   static constexpr int Q_TILE = BM * D * 2;
   static constexpr int K_TILE = BN * D * 2;
   static constexpr int V_TILE = BN * DV * 2;
+  static constexpr int P_TILE = BM * BN * 2;  // bf16 P, two 64-key boxes
   static constexpr int SLOT = K_TILE;
   static constexpr int VF = V_TILE / SLOT;  // slots per V tile
   static constexpr int VKEYS = BN / VF;     // keys per V slot
   static constexpr int OFF_Q1 = 0;
   static constexpr int OFF_Q2 = Q_TILE;
-  static constexpr int OFF_RING = 2 * Q_TILE;
+  static constexpr int OFF_P = 2 * Q_TILE;
+  static constexpr int OFF_RING = OFF_P + P_TILE;
   static constexpr int OFF_BARS = OFF_RING + NSLOT * SLOT;
-  static constexpr int NBARS = 2 + 2 * NSLOT + 6;
+  static constexpr int NBARS = 2 * NSLOT + 16;
   static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
@@ -83,10 +92,10 @@ struct TwoPassCfg {
   static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(BM, DV, false, true);
   static_assert(D == 64 || D == 128, "query/key width");
-  static_assert(DV % 64 == 0 && DV <= 256, "value width");
+  static_assert(DV == 256, "sweep-1 buffer ring assumes O spans two 128-column buffers");
   static_assert(V_TILE % SLOT == 0 && (VF == 1 || VF == 2), "value tile split");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
-  static_assert(NSLOT >= 4, "ring depth");
+  static_assert(NSLOT >= VF + 2, "ring depth");
 };
 
 // Merge two partial softmax states (max in the scaled log2 domain, sum).
@@ -152,16 +161,18 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
   const int lane = threadIdx.x & 31;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
-  uint64_t* q_full = bars + 0;
-  uint64_t* o_full = bars + 1;
-  uint64_t* full = bars + 2;             // [NSLOT] slot loaded
-  uint64_t* empty = full + NSLOT;        // [NSLOT] slot released by the MMAs
-  uint64_t* a_full = empty + NSLOT;      // S_1 of the current tile in TMEM buffer A
-  uint64_t* b_full = a_full + 1;         // S_2 of the current tile in TMEM buffer B
-  uint64_t* a_free1 = b_full + 1;        // sweep 1: map-1 warps have read A
-  uint64_t* b_free1 = a_free1 + 1;       // sweep 1: map-2 warps have read B
-  uint64_t* b_free2 = b_free1 + 1;       // sweep 2: all softmax warps have read B
-  uint64_t* p_ready = b_free2 + 1;       // sweep 2: P of the tile is in buffer A
+  uint64_t* full = bars;              // [NSLOT] ring slot loaded
+  uint64_t* empty = full + NSLOT;     // [NSLOT] ring slot released by the MMAs
+  uint64_t* q_full = empty + NSLOT;
+  uint64_t* o_full = q_full + 1;
+  uint64_t* s1_full = o_full + 1;     // [4] sweep 1: S written into TMEM buffer b
+  uint64_t* s1_free = s1_full + 4;    // [4] sweep 1: the map's 8 warps have loaded buffer b
+  uint64_t* a2_full = s1_free + 4;    // sweep 2: S_1 of the tile in A
+  uint64_t* b2_full = a2_full + 1;    // sweep 2: S_2 of the tile in B
+  uint64_t* a2_free = b2_full + 1;    // sweep 2: every softmax warp has loaded A
+  uint64_t* b2_free = a2_free + 1;    // sweep 2: every softmax warp has loaded B
+  uint64_t* p_ready = b2_free + 1;    // sweep 2: P of the tile in shared memory
+  uint64_t* pv_done = p_ready + 1;    // sweep 2: PV of the tile completed (P buffer free)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -191,18 +202,22 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
 
   // ---- set-up
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(o_full, 1);
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(a_full, 1);
-    mbar_init(b_full, 1);
-    mbar_init(a_free1, 8);  // the 8 warps of warpgroups 0-1
-    mbar_init(b_free1, 8);  // the 8 warps of warpgroups 2-3
-    mbar_init(b_free2, 4 * C::NSMWG);
+    mbar_init(q_full, 1);
+    mbar_init(o_full, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&s1_full[i], 1);
+      mbar_init(&s1_free[i], 8);  // the 8 warps of the map that owns buffer i
+    }
+    mbar_init(a2_full, 1);
+    mbar_init(b2_full, 1);
+    mbar_init(a2_free, 4 * C::NSMWG);
+    mbar_init(b2_free, 4 * C::NSMWG);
     mbar_init(p_ready, 4 * C::NSMWG);
+    mbar_init(pv_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -247,9 +262,7 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
       };
       auto load_k1 = [&](int j) { load(&p.tm_k1, j * BN, BN, C::QB); };
       auto load_k2 = [&](int j) { load(&p.tm_k2, j * BN, BN, C::QB); };
-      auto load_v = [&](int j) {
-        for (int part = 0; part < C::VF; ++part) load(&p.tm_v, j * BN + part * C::VKEYS, C::VKEYS, C::VB);
-      };
+      // The fill order is exactly the MMA thread's consumption order.
       for (int j = 0; j < T; ++j) {  // sweep 1
         load_k1(j);
         if (!SHARED_K) load_k2(j);
@@ -261,9 +274,15 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
         load_k1(0);
       }
       for (int j = 0; j < T; ++j) {
-        if (j + 1 < T) SHARED_K ? load_k1(j + 1) : load_k2(j + 1);
-        load_v(j);
-        if (j + 1 < T && !SHARED_K) load_k1(j + 1);
+        if (j + 1 < T) {
+          if (SHARED_K) {
+            load_k1(j + 1);
+          } else {
+            load_k2(j + 1);
+            load_k1(j + 1);
+          }
+        }
+        for (int part = 0; part < C::VF; ++part) load(&p.tm_v, j * BN + part * C::VKEYS, C::VKEYS, C::VB);
       }
       if (*ab.flag) {
         // Aborted: let the copies already issued land before the CTA exits.
@@ -274,128 +293,137 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
     }
   } else if (warp == 1) {
     // =============================================================== MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop: warp-uniform control flow keeps the
+    // descriptors in uniform registers, and each MMA / commit is issued by one
+    // elected lane.  (Issued from a single divergent lane, an M128 N128 K16
+    // MMA took longer to issue than to execute.)
+    {
       // Descriptors are built once; a k-step or a ring slot only adds its
       // byte offset >> 4 to the start-address field (addresses stay below
       // 256 KB, so the 14-bit field never carries into the next one).
       const uint64_t dQ1 = sdesc_sw128(smem_u32(smem + C::OFF_Q1), 16, 1024);
       const uint64_t dQ2 = sdesc_sw128(smem_u32(smem + C::OFF_Q2), 16, 1024);
+      const uint64_t dP = sdesc_sw128(smem_u32(smem + C::OFF_P), 16, 1024);
       const uint64_t dRingK = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
       const uint64_t dRingV = sdesc_sw128(smem_u32(smem + C::OFF_RING), C::VKEYS * 128, 1024);
       const uint32_t tA = tmem + C::TM_A, tB = tmem + C::TM_B, tO = tmem + C::TM_O;
       int cons = 0;
-      uint32_t n_afree1 = 0, n_bfree1 = 0, n_bfree2 = 0, n_pready = 0;
-      bool ok = mbar_wait(q_full, 0, ab);
-      tc_fence_after();
+      // Every wait returns the same verdict in all lanes and leaves the warp converged.
+      auto waitp = [&](uint64_t* bar, uint32_t parity) -> bool {
+        const bool r = __all_sync(0xffffffffu, mbar_wait(bar, parity, ab));
+        tc_fence_after();
+        return r;
+      };
       auto acquire = [&](int& s) -> bool {
         s = cons % NSLOT;
         const uint32_t use = static_cast<uint32_t>(cons / NSLOT);
         ++cons;
-        if (!mbar_wait(&full[s], use & 1u, ab)) return false;
-        tc_fence_after();
-        return true;
-      };
-      auto waitc = [&](uint64_t* bar, uint32_t& n) -> bool {
-        const bool r = mbar_wait(bar, n & 1u, ab);
-        ++n;
-        tc_fence_after();
-        return r;
+        return waitp(&full[s], use & 1u);
       };
       auto qk = [&](uint32_t dst, uint64_t dq, int s) {
         const uint64_t dk = dRingK + static_cast<uint64_t>((s * C::SLOT) >> 4);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
-          mma_ss(dst, dq + static_cast<uint64_t>((((k >> 2) * (BM * 128)) + (k & 3) * 32) >> 4),
-                 dk + static_cast<uint64_t>((((k >> 2) * (BN * 128)) + (k & 3) * 32) >> 4), C::IDESC_QK,
-                 k > 0 ? 1u : 0u);
+          mma_ss_elect(dst, dq + static_cast<uint64_t>((((k >> 2) * (BM * 128)) + (k & 3) * 32) >> 4),
+                       dk + static_cast<uint64_t>((((k >> 2) * (BN * 128)) + (k & 3) * 32) >> 4), C::IDESC_QK,
+                       k > 0 ? 1u : 0u);
       };
-      // ---- sweep 1
+      bool ok = waitp(q_full, 0);
+      // ---- sweep 1: S index k = 2 j + map goes to TMEM buffer k % 4
+      uint32_t use[4] = {0, 0, 0, 0};
+      auto s1_claim = [&](int k) -> bool {  // buffer k % 4 must have been read since its last write
+        const int bb = k & 3;
+        if (use[bb] > 0 && !waitp(&s1_free[bb], (use[bb] - 1) & 1u)) return false;
+        ++use[bb];
+        return true;
+      };
       for (int j = 0; ok && j < T; ++j) {
         int s1, s2;
-        if (!acquire(s1)) break;
-        if (j > 0 && !waitc(a_free1, n_afree1)) break;
-        qk(tA, dQ1, s1);
-        tc_commit(a_full);
+        if (!acquire(s1) || !s1_claim(2 * j)) {
+          ok = false;
+          break;
+        }
+        qk(tmem + 128u * ((2 * j) & 3), dQ1, s1);
+        tc_commit_elect(&s1_full[(2 * j) & 3]);
         if (SHARED_K) {
           s2 = s1;
         } else {
-          tc_commit(&empty[s1]);
-          if (!acquire(s2)) break;
-        }
-        if (j > 0 && !waitc(b_free1, n_bfree1)) break;
-        qk(tB, dQ2, s2);
-        tc_commit(b_full);
-        tc_commit(&empty[s2]);
-      }
-      // ---- sweep 2
-      if (ok) ok = waitc(a_free1, n_afree1) && waitc(b_free1, n_bfree1);
-      if (ok) {
-        int s1, s2;
-        if (SHARED_K) {
-          ok = acquire(s2);
-          s1 = s2;
-          if (ok) {
-            qk(tB, dQ2, s2);
-            tc_commit(b_full);
-            qk(tA, dQ1, s1);
-            tc_commit(a_full);
-            tc_commit(&empty[s1]);
-          }
-        } else {
-          ok = acquire(s2);
-          if (ok) {
-            qk(tB, dQ2, s2);
-            tc_commit(b_full);
-            tc_commit(&empty[s2]);
-            ok = acquire(s1);
-          }
-          if (ok) {
-            qk(tA, dQ1, s1);
-            tc_commit(a_full);
-            tc_commit(&empty[s1]);
-          }
-        }
-      }
-      for (int j = 0; ok && j < T; ++j) {
-        int sk = 0;
-        if (j + 1 < T) {
-          if (!acquire(sk)) break;
-          if (!waitc(b_free2, n_bfree2)) break;
-          qk(tB, dQ2, sk);
-          tc_commit(b_full);
-          if (!SHARED_K) tc_commit(&empty[sk]);
-        } else {
-          // Nobody waits for the last tile's release of B in sweep 2.
-          ++n_bfree2;
-        }
-        if (!waitc(p_ready, n_pready)) break;
-#pragma unroll
-        for (int part = 0; part < C::VF; ++part) {
-          int sv;
-          if (!acquire(sv)) {
+          tc_commit_elect(&empty[s1]);
+          if (!acquire(s2)) {
             ok = false;
             break;
           }
-          const uint64_t dv = dRingV + static_cast<uint64_t>((sv * C::SLOT) >> 4);
+        }
+        if (!s1_claim(2 * j + 1)) {
+          ok = false;
+          break;
+        }
+        qk(tmem + 128u * ((2 * j + 1) & 3), dQ2, s2);
+        tc_commit_elect(&s1_full[(2 * j + 1) & 3]);
+        tc_commit_elect(&empty[s2]);
+      }
+      // ---- sweep 2 (A = buffer 2, B = buffer 3: wait for their last sweep-1 reads)
+      if (ok && use[3] > 0) ok = waitp(&s1_free[3], (use[3] - 1) & 1u);
+      if (ok && use[2] > 0) ok = waitp(&s1_free[2], (use[2] - 1) & 1u);
+      if (ok) {
+        int sa, sb;
+        ok = acquire(sb);
+        if (ok) {
+          qk(tB, dQ2, sb);
+          tc_commit_elect(b2_full);
+          if (SHARED_K) {
+            sa = sb;
+          } else {
+            tc_commit_elect(&empty[sb]);
+            ok = acquire(sa);
+          }
+        }
+        if (ok) {
+          qk(tA, dQ1, sa);
+          tc_commit_elect(a2_full);
+          tc_commit_elect(&empty[sa]);
+        }
+      }
+      for (int j = 0; ok && j < T; ++j) {
+        const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+        if (j + 1 < T) {
+          int sa, sb;
+          if (!acquire(sb) || !waitp(b2_free, ph)) break;
+          qk(tB, dQ2, sb);
+          tc_commit_elect(b2_full);
+          if (SHARED_K) {
+            sa = sb;
+          } else {
+            tc_commit_elect(&empty[sb]);
+            if (!acquire(sa)) break;
+          }
+          if (!waitp(a2_free, ph)) break;
+          qk(tA, dQ1, sa);
+          tc_commit_elect(a2_full);
+          tc_commit_elect(&empty[sa]);
+        }
+        int sv[C::VF];
+        bool got = true;
+#pragma unroll
+        for (int part = 0; part < C::VF; ++part) got = acquire(sv[part]) && got;
+        if (!got || !waitp(p_ready, ph)) break;
+#pragma unroll
+        for (int part = 0; part < C::VF; ++part) {
+          const uint64_t dv = dRingV + static_cast<uint64_t>((sv[part] * C::SLOT) >> 4);
 #pragma unroll
           for (int kk = 0; kk < C::VKEYS / 16; ++kk) {
             const int kg = part * (C::VKEYS / 16) + kk;  // global k-step: keys 16 kg .. 16 kg + 15
-            const uint32_t acol = 32u * (kg >> 1) + 8u * (kg & 1);
-            mma_ts(tO, tA + acol, dv + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_PV,
-                   (j > 0 || kg > 0) ? 1u : 0u);
+            mma_ss_elect(tO, dP + static_cast<uint64_t>((((kg >> 2) * (BM * 128)) + (kg & 3) * 32) >> 4),
+                         dv + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_PV, (j > 0 || kg > 0) ? 1u : 0u);
           }
-          tc_commit(&empty[sv]);
         }
-        if (!ok) break;
-        if (j + 1 < T) {
-          if (!SHARED_K && !acquire(sk)) break;
-          qk(tA, dQ1, sk);
-          tc_commit(a_full);
-          tc_commit(&empty[sk]);
-        }
+        tc_commit_elect(pv_done);
+#pragma unroll
+        for (int part = 0; part < C::VF; ++part) tc_commit_elect(&empty[sv[part]]);
       }
-      tc_commit(o_full);
+      tc_commit_elect(o_full);
       if (*ab.flag) mbar_wait_drain(o_full, 0, kWaitBudgetCycles);
+      __syncwarp();
     }
   } else if (warp >= 4) {
     // =============================================================== softmax + epilogue
@@ -411,35 +439,39 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
     const int map = wg >> 1;
     const int half = wg & 1;
     float m = -INFINITY, l = 0.f;
-    {
-      uint64_t* fullb = map == 0 ? a_full : b_full;
-      uint64_t* freeb = map == 0 ? a_free1 : b_free1;
-      const uint32_t tbuf = tl + (map == 0 ? C::TM_A : C::TM_B) + 64u * half;
-      for (int j = 0; j < T; ++j) {
-        mbar_wait(fullb, static_cast<uint32_t>(j) & 1u, ab);
-        __syncwarp();
-        tc_fence_after();
-        uint32_t r0[32], r1[32];
-        tmem_ld32(tbuf, r0);
-        tmem_ld32(tbuf + 32, r1);
-        tmem_ld_wait2(r0, r1);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(freeb);
-        __syncwarp();
-        row_stats64(r0, r1, lim - (j * BN + 64 * half), sc, m, l);
-      }
+    for (int j = 0; j < T; ++j) {
+      const int k = 2 * j + map;  // S index: buffer k % 4, its (k / 4)-th write
+      const int bb = k & 3;
+      mbar_wait(&s1_full[bb], static_cast<uint32_t>(k >> 2) & 1u, ab);
+      __syncwarp();
+      tc_fence_after();
+      uint32_t r0[32], r1[32];
+      const uint32_t tbuf = tl + 128u * bb + 64u * half;
+      tmem_ld32(tbuf, r0);
+      tmem_ld32(tbuf + 32, r1);
+      tmem_ld_wait2(r0, r1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s1_free[bb]);
+      __syncwarp();
+      row_stats64(r0, r1, lim - (j * BN + 64 * half), sc, m, l);
     }
 
-    // ---- exchange the four partial states through the (unused) O columns
-    tmem_st2(tl + C::TM_O + 2u * wg, __float_as_uint(m), __float_as_uint(l));
+    // ---- exchange the four partial states through TMEM columns [0, 8).
+    // The other map may still be reading buffer 0 for its last tile, so all
+    // sweep-1 reads finish first; sweep 2 writes buffer 0 only in PV, after
+    // every warp has read the exchange.
+    tc_fence_before();
+    named_bar_sync(1, 128 * C::NSMWG);
+    tc_fence_after();
+    tmem_st2(tl + 2u * wg, __float_as_uint(m), __float_as_uint(l));
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
     named_bar_sync(1, 128 * C::NSMWG);
     tc_fence_after();
     uint32_t ps[8];
-    tmem_ld8_wait(tl + C::TM_O, ps);
+    tmem_ld8_wait(tl, ps);
     float m1 = __uint_as_float(ps[0]), l1 = __uint_as_float(ps[1]);
     merge_state(m1, l1, __uint_as_float(ps[2]), __uint_as_float(ps[3]));
     float m2 = __uint_as_float(ps[4]), l2 = __uint_as_float(ps[5]);
@@ -459,11 +491,14 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
     const float neg2 = (coef >= 0.f) ? -1.f : 1.f;
     const uint64_t sc2 = f2pack(sc, sc);
     const uint64_t nM1 = f2pack(-M1, -M1), nM2 = f2pack(-M2, -M2), ng2 = f2pack(neg2, neg2);
+    // This thread's P chunks: row `row`, keys [32 wg, +32) = 64-key box wg / 2,
+    // 16-byte chunks 4 (wg % 2) .. 4 (wg % 2) + 3 of the 128-byte swizzled row.
+    uint8_t* prow = smem + C::OFF_P + (wg >> 1) * (BM * 128) + row * 128;
 
-    // ---- sweep 2: signed combined weights of key columns [32 wg, +32) -> TMEM (bf16)
+    // ---- sweep 2: signed combined weights of key columns [32 wg, +32) -> shared memory (bf16)
     for (int j = 0; j < T; ++j) {
-      const uint32_t ph = static_cast<uint32_t>(T + j) & 1u;
-      mbar_wait(b_full, ph, ab);
+      const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+      mbar_wait(b2_full, ph, ab);
       __syncwarp();
       tc_fence_after();
       uint32_t r[32];
@@ -471,7 +506,7 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
       tmem_ld_wait(r);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(b_free2);
+      if (lane == 0) mbar_arrive(b2_free);
       __syncwarp();
       uint64_t e2[16];
 #pragma unroll
@@ -480,11 +515,15 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
         f2unpack(fma2(f2pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), sc2, nM2), x0, x1);
         e2[c] = f2pack(ex2(x0), ex2(x1));
       }
-      mbar_wait(a_full, ph, ab);
+      mbar_wait(a2_full, ph, ab);
       __syncwarp();
       tc_fence_after();
       tmem_ld32(tl + C::TM_A + 32u * wg, r);
       tmem_ld_wait(r);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(a2_free);
+      __syncwarp();
       const int nvis = lim - (j * BN + 32 * wg);
       uint32_t pk[16];
 #pragma unroll
@@ -497,9 +536,13 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
         if (2 * c + 1 >= nvis) p1 = 0.f;
         pk[c] = pack_bf16x2(p0, p1);
       }
-      tmem_st16(tl + C::TM_A + 32u * wg, pk);
-      tmem_st_wait();
-      tc_fence_before();
+      // PV(j-1) must have completed before its P is overwritten.
+      if (j > 0) mbar_wait(pv_done, static_cast<uint32_t>(j - 1) & 1u, ab);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(prow + (((4 * (wg & 1) + c) ^ (row & 7)) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_ready);
       __syncwarp();
@@ -516,16 +559,16 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
       float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
       for (int ch = 0; ch < QW / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(to + 32 * ch, r);
-        tmem_ld_wait(r);
+        uint32_t rr[32];
+        tmem_ld32(to + 32 * ch, rr);
+        tmem_ld_wait(rr);
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          ss0 = fmaf(__uint_as_float(r[c]), __uint_as_float(r[c]), ss0);
-          ss1 = fmaf(__uint_as_float(r[c + 1]), __uint_as_float(r[c + 1]), ss1);
+          ss0 = fmaf(__uint_as_float(rr[c]), __uint_as_float(rr[c]), ss0);
+          ss1 = fmaf(__uint_as_float(rr[c + 1]), __uint_as_float(rr[c + 1]), ss1);
         }
       }
-      // Every MMA has completed, so buffer A is free for the exchange.
+      // Every MMA has completed and every read of A is done: A carries the exchange.
       tmem_st1(tl + C::TM_A + wg, __float_as_uint(ss0 + ss1));
       tmem_st_wait();
       tc_fence_before();
@@ -541,15 +584,15 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
     __nv_bfloat16* orow = p.out + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * DV + wg * QW;
 #pragma unroll
     for (int ch = 0; ch < QW / 32; ++ch) {
-      uint32_t r[32];
-      tmem_ld32(to + 32 * ch, r);
-      tmem_ld_wait(r);
+      uint32_t rr[32];
+      tmem_ld32(to + 32 * ch, rr);
+      tmem_ld_wait(rr);
       if (t < p.n) {
         uint32_t w[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          float y0 = __uint_as_float(r[c]) * rinv;
-          float y1 = __uint_as_float(r[c + 1]) * rinv;
+          float y0 = __uint_as_float(rr[c]) * rinv;
+          float y1 = __uint_as_float(rr[c + 1]) * rinv;
           if (EPI == kEpiRmsNorm && p.gamma != nullptr) {
             const int col = wg * QW + ch * 32 + c;
             y0 *= __ldg(p.gamma + col);
