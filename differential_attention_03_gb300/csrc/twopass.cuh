@@ -41,8 +41,9 @@
 //               ring of NSLOT equal slots, in exactly the order warp 1
 //               consumes them; a slot is released by a tcgen05.commit after
 //               the last MMA reading it.
-//   warp 1      TMEM allocator and tcgen05.mma issuer (the whole warp runs the
-//               loop; one elected lane issues each MMA and commit).
+//   warp 1      TMEM allocator; issues the map-1 MMAs (S_1) and P.V.
+//   warp 2      issues the map-2 MMAs (S_2).  (One warp cannot issue an MMA
+//               faster than every ~100 cycles; an N = 128 MMA runs in 64.)
 //   warps 4-19  four softmax warpgroups; thread = one query row (TMEM lane).
 //               Sweep 1: warpgroup w keeps running (max, sum) of map w/2 over
 //               key columns [64 (w%2), +64) of each tile.
@@ -82,7 +83,7 @@ struct TwoPassCfg {
   static constexpr int OFF_P = 2 * Q_TILE;
   static constexpr int OFF_RING = OFF_P + P_TILE;
   static constexpr int OFF_BARS = OFF_RING + NSLOT * SLOT;
-  static constexpr int NBARS = 2 * NSLOT + 16;
+  static constexpr int NBARS = 2 * NSLOT + 18;
   static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
@@ -96,6 +97,7 @@ struct TwoPassCfg {
   static_assert(V_TILE % SLOT == 0 && (VF == 1 || VF == 2), "value tile split");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(NSLOT >= VF + 2, "ring depth");
+  static_assert(!SHARED_K, "the two MMA warps consume separate K_1 / K_2 fills");
 };
 
 // Merge two partial softmax states (max in the scaled log2 domain, sum).
@@ -173,6 +175,7 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
   uint64_t* b2_free = a2_free + 1;    // sweep 2: every softmax warp has loaded B
   uint64_t* p_ready = b2_free + 1;    // sweep 2: P of the tile in shared memory
   uint64_t* pv_done = p_ready + 1;    // sweep 2: PV of the tile completed (P buffer free)
+  uint64_t* w2_done = pv_done + 1;    // every MMA of warp 2 completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -218,6 +221,7 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
     mbar_init(b2_free, 4 * C::NSMWG);
     mbar_init(p_ready, 4 * C::NSMWG);
     mbar_init(pv_done, 1);
+    mbar_init(w2_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -291,140 +295,119 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
           mbar_wait_drain(&full[f % NSLOT], static_cast<uint32_t>(f / NSLOT) & 1u, kWaitBudgetCycles);
       }
     }
-  } else if (warp == 1) {
-    // =============================================================== MMA issuer
-    // The whole warp runs this loop: warp-uniform control flow keeps the
-    // descriptors in uniform registers, and each MMA / commit is issued by one
-    // elected lane.  (Issued from a single divergent lane, an M128 N128 K16
-    // MMA took longer to issue than to execute.)
-    {
-      // Descriptors are built once; a k-step or a ring slot only adds its
-      // byte offset >> 4 to the start-address field (addresses stay below
-      // 256 KB, so the 14-bit field never carries into the next one).
-      const uint64_t dQ1 = sdesc_sw128(smem_u32(smem + C::OFF_Q1), 16, 1024);
-      const uint64_t dQ2 = sdesc_sw128(smem_u32(smem + C::OFF_Q2), 16, 1024);
-      const uint64_t dP = sdesc_sw128(smem_u32(smem + C::OFF_P), 16, 1024);
-      const uint64_t dRingK = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
-      const uint64_t dRingV = sdesc_sw128(smem_u32(smem + C::OFF_RING), C::VKEYS * 128, 1024);
-      const uint32_t tA = tmem + C::TM_A, tB = tmem + C::TM_B, tO = tmem + C::TM_O;
-      int cons = 0;
-      // Every wait returns the same verdict in all lanes and leaves the warp converged.
-      auto waitp = [&](uint64_t* bar, uint32_t parity) -> bool {
-        const bool r = __all_sync(0xffffffffu, mbar_wait(bar, parity, ab));
-        tc_fence_after();
-        return r;
-      };
-      auto acquire = [&](int& s) -> bool {
-        s = cons % NSLOT;
-        const uint32_t use = static_cast<uint32_t>(cons / NSLOT);
-        ++cons;
-        return waitp(&full[s], use & 1u);
-      };
-      auto qk = [&](uint32_t dst, uint64_t dq, int s) {
-        const uint64_t dk = dRingK + static_cast<uint64_t>((s * C::SLOT) >> 4);
+  } else if (warp == 1 || warp == 2) {
+    // =============================================================== MMA issuers
+    // One warp issues at most one tcgen05.mma every ~100 cycles, while an
+    // M128 N128 K16 MMA executes in 64: two issuing warps keep the tensor
+    // pipe full.  Warp 1 issues every map-1 MMA (S_1) and the P.V chain,
+    // warp 2 every map-2 MMA (S_2).  Each warp runs its loop warp-uniformly
+    // (descriptors stay in uniform registers) and issues from one elected
+    // lane; tcgen05.commit tracks the MMAs of the issuing thread, so every
+    // warp commits (and releases ring slots) for its own MMAs only.
+    const int mw = warp - 1;  // 0: map 1 + P.V, 1: map 2
+    // Descriptors are built once; a k-step or a ring slot only adds its byte
+    // offset >> 4 to the start-address field (addresses stay below 256 KB, so
+    // the 14-bit field never carries into the next one).
+    const uint64_t dQ = sdesc_sw128(smem_u32(smem + (mw == 0 ? C::OFF_Q1 : C::OFF_Q2)), 16, 1024);
+    const uint64_t dP = sdesc_sw128(smem_u32(smem + C::OFF_P), 16, 1024);
+    const uint64_t dRingK = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
+    const uint64_t dRingV = sdesc_sw128(smem_u32(smem + C::OFF_RING), C::VKEYS * 128, 1024);
+    const uint32_t tS2 = tmem + (mw == 0 ? C::TM_A : C::TM_B);  // this map's sweep-2 S buffer
+    uint64_t* s2_full = (mw == 0) ? a2_full : b2_full;
+    uint64_t* s2_free = (mw == 0) ? a2_free : b2_free;
+    // Every wait returns the same verdict in all lanes and leaves the warp converged.
+    auto waitp = [&](uint64_t* bar, uint32_t parity) -> bool {
+      const bool r = __all_sync(0xffffffffu, mbar_wait(bar, parity, ab));
+      tc_fence_after();
+      return r;
+    };
+    // Ring fill f sits in slot f % NSLOT, its (f / NSLOT)-th use.
+    auto acquire = [&](int f) -> bool { return waitp(&full[f % NSLOT], static_cast<uint32_t>(f / NSLOT) & 1u); };
+    auto qk = [&](uint32_t dst, int f) {
+      const uint64_t dk = dRingK + static_cast<uint64_t>(((f % NSLOT) * C::SLOT) >> 4);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_ss_elect(dst, dq + static_cast<uint64_t>((((k >> 2) * (BM * 128)) + (k & 3) * 32) >> 4),
-                       dk + static_cast<uint64_t>((((k >> 2) * (BN * 128)) + (k & 3) * 32) >> 4), C::IDESC_QK,
-                       k > 0 ? 1u : 0u);
-      };
-      bool ok = waitp(q_full, 0);
-      // ---- sweep 1: S index k = 2 j + map goes to TMEM buffer k % 4
-      uint32_t use[4] = {0, 0, 0, 0};
-      auto s1_claim = [&](int k) -> bool {  // buffer k % 4 must have been read since its last write
-        const int bb = k & 3;
-        if (use[bb] > 0 && !waitp(&s1_free[bb], (use[bb] - 1) & 1u)) return false;
-        ++use[bb];
-        return true;
-      };
-      for (int j = 0; ok && j < T; ++j) {
-        int s1, s2;
-        if (!acquire(s1) || !s1_claim(2 * j)) {
-          ok = false;
-          break;
-        }
-        qk(tmem + 128u * ((2 * j) & 3), dQ1, s1);
-        tc_commit_elect(&s1_full[(2 * j) & 3]);
-        if (SHARED_K) {
-          s2 = s1;
-        } else {
-          tc_commit_elect(&empty[s1]);
-          if (!acquire(s2)) {
-            ok = false;
-            break;
-          }
-        }
-        if (!s1_claim(2 * j + 1)) {
-          ok = false;
-          break;
-        }
-        qk(tmem + 128u * ((2 * j + 1) & 3), dQ2, s2);
-        tc_commit_elect(&s1_full[(2 * j + 1) & 3]);
-        tc_commit_elect(&empty[s2]);
+      for (int k = 0; k < D / 16; ++k)
+        mma_ss_elect(dst, dQ + static_cast<uint64_t>((((k >> 2) * (BM * 128)) + (k & 3) * 32) >> 4),
+                     dk + static_cast<uint64_t>((((k >> 2) * (BN * 128)) + (k & 3) * 32) >> 4), C::IDESC_QK,
+                     k > 0 ? 1u : 0u);
+    };
+    // Fill order of the producer: sweep 1 K1(j) = 2j, K2(j) = 2j + 1; sweep 2
+    // K2(0) = 2T, K1(0) = 2T + 1, then per tile j: K2(j+1), K1(j+1) (if
+    // j + 1 < T) and the VF parts of V(j).
+    const int F2 = 2 * T;
+    constexpr int PER_TILE = 2 + C::VF;
+    auto fill_k_next = [&](int j) { return F2 + 2 + PER_TILE * j + (mw == 0 ? 1 : 0); };  // K_map(j+1)
+    auto fill_v = [&](int j, int part) { return F2 + 2 + PER_TILE * j + (j + 1 < T ? 2 : 0) + part; };
+    bool ok = waitp(q_full, 0);
+    // ---- sweep 1: S_map(j) (S index k = 2 j + mw) goes to TMEM buffer k % 4
+    uint32_t use_lo = 0, use_hi = 0;  // writes so far of buffers mw and mw + 2
+    for (int j = 0; ok && j < T; ++j) {
+      const int k = 2 * j + mw;
+      const int bb = k & 3;
+      uint32_t& use = (bb & 2) ? use_hi : use_lo;
+      if (!acquire(k)) {
+        ok = false;
+        break;
       }
-      // ---- sweep 2 (A = buffer 2, B = buffer 3: wait for their last sweep-1 reads)
-      if (ok && use[3] > 0) ok = waitp(&s1_free[3], (use[3] - 1) & 1u);
-      if (ok && use[2] > 0) ok = waitp(&s1_free[2], (use[2] - 1) & 1u);
+      if (use > 0 && !waitp(&s1_free[bb], (use - 1) & 1u)) {  // read since its last write
+        ok = false;
+        break;
+      }
+      ++use;
+      qk(tmem + 128u * bb, k);
+      tc_commit_elect(&s1_full[bb]);
+      tc_commit_elect(&empty[k % NSLOT]);
+    }
+    // ---- sweep 2: this map's S buffer is sweep-1 buffer mw + 2 (A or B)
+    if (ok && use_hi > 0) ok = waitp(&s1_free[mw + 2], (use_hi - 1) & 1u);
+    if (ok) {
+      const int f = F2 + (mw == 0 ? 1 : 0);
+      ok = acquire(f);
       if (ok) {
-        int sa, sb;
-        ok = acquire(sb);
-        if (ok) {
-          qk(tB, dQ2, sb);
-          tc_commit_elect(b2_full);
-          if (SHARED_K) {
-            sa = sb;
-          } else {
-            tc_commit_elect(&empty[sb]);
-            ok = acquire(sa);
-          }
-        }
-        if (ok) {
-          qk(tA, dQ1, sa);
-          tc_commit_elect(a2_full);
-          tc_commit_elect(&empty[sa]);
-        }
+        qk(tS2, f);
+        tc_commit_elect(s2_full);
+        tc_commit_elect(&empty[f % NSLOT]);
       }
-      for (int j = 0; ok && j < T; ++j) {
-        const uint32_t ph = static_cast<uint32_t>(j) & 1u;
-        if (j + 1 < T) {
-          int sa, sb;
-          if (!acquire(sb) || !waitp(b2_free, ph)) break;
-          qk(tB, dQ2, sb);
-          tc_commit_elect(b2_full);
-          if (SHARED_K) {
-            sa = sb;
-          } else {
-            tc_commit_elect(&empty[sb]);
-            if (!acquire(sa)) break;
-          }
-          if (!waitp(a2_free, ph)) break;
-          qk(tA, dQ1, sa);
-          tc_commit_elect(a2_full);
-          tc_commit_elect(&empty[sa]);
+    }
+    for (int j = 0; ok && j < T; ++j) {
+      const uint32_t ph = static_cast<uint32_t>(j) & 1u;
+      if (j + 1 < T) {
+        const int f = fill_k_next(j);
+        if (!acquire(f) || !waitp(s2_free, ph)) {
+          ok = false;
+          break;
         }
-        int sv[C::VF];
+        qk(tS2, f);
+        tc_commit_elect(s2_full);
+        tc_commit_elect(&empty[f % NSLOT]);
+      }
+      if (mw == 0) {
         bool got = true;
 #pragma unroll
-        for (int part = 0; part < C::VF; ++part) got = acquire(sv[part]) && got;
-        if (!got || !waitp(p_ready, ph)) break;
+        for (int part = 0; part < C::VF; ++part) got = acquire(fill_v(j, part)) && got;
+        if (!got || !waitp(p_ready, ph)) {
+          ok = false;
+          break;
+        }
 #pragma unroll
         for (int part = 0; part < C::VF; ++part) {
-          const uint64_t dv = dRingV + static_cast<uint64_t>((sv[part] * C::SLOT) >> 4);
+          const uint64_t dv = dRingV + static_cast<uint64_t>(((fill_v(j, part) % NSLOT) * C::SLOT) >> 4);
 #pragma unroll
           for (int kk = 0; kk < C::VKEYS / 16; ++kk) {
             const int kg = part * (C::VKEYS / 16) + kk;  // global k-step: keys 16 kg .. 16 kg + 15
-            mma_ss_elect(tO, dP + static_cast<uint64_t>((((kg >> 2) * (BM * 128)) + (kg & 3) * 32) >> 4),
+            mma_ss_elect(tmem + C::TM_O, dP + static_cast<uint64_t>((((kg >> 2) * (BM * 128)) + (kg & 3) * 32) >> 4),
                          dv + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_PV, (j > 0 || kg > 0) ? 1u : 0u);
           }
         }
         tc_commit_elect(pv_done);
 #pragma unroll
-        for (int part = 0; part < C::VF; ++part) tc_commit_elect(&empty[sv[part]]);
+        for (int part = 0; part < C::VF; ++part) tc_commit_elect(&empty[fill_v(j, part) % NSLOT]);
       }
-      tc_commit_elect(o_full);
-      if (*ab.flag) mbar_wait_drain(o_full, 0, kWaitBudgetCycles);
-      __syncwarp();
     }
+    uint64_t* last = (mw == 0) ? o_full : w2_done;
+    tc_commit_elect(last);
+    if (*ab.flag) mbar_wait_drain(last, 0, kWaitBudgetCycles);
+    __syncwarp();
   } else if (warp >= 4) {
     // =============================================================== softmax + epilogue
     const int wg = (warp - 4) >> 2;  // 0..3
