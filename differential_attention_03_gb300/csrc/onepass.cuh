@@ -12,28 +12,36 @@
 // news article section "差分注意力" for the per-head RMSNorm.)
 //
 // Each K/V tile is loaded once and serves both maps.  TMEM (512 columns):
-// O_1 [0, 128), O_2 [128, 256), A [256, 384) holds S_1 then P_1 (bf16
-// pairs), B [384, 512) holds S_2 then P_2.  MMA issue order per key tile j:
-//     PV1(j)  QK1(j+1)  PV2(j)  QK2(j+1)
-// so the softmax of one map overlaps the other map's MMAs, and S_r(j+1)
-// being complete implies PV_r(j) is complete (the tensor pipe runs in issue
-// order): a rescale of O_r never has to wait.
+// O_1 [0, 128), O_2 [128, 256), A [256, 384) holds S_1, B [384, 512) S_2.
+// P placement (template flag PSM):
+//   PSM = false  P_r (bf16 pairs) overwrites S_r in TMEM and PV_r reads it
+//                from there (TS MMA); per map the MMAs run PV_r(j) then
+//                QK_r(j+1) into the buffer PV_r(j) has just read, so a map's
+//                softmax and its MMAs alternate.
+//   PSM = true   P_r goes to shared memory (128-byte swizzled, SS MMA), so
+//                S_r is released as soon as the softmax has loaded it:
+//                QK_r(j+1) runs during the softmax of tile j and only PV_r(j)
+//                waits for P_r(j); a pv_done barrier guards the P buffer and
+//                the rescale of O_r.
+// Either way S_r(j+1) (or pv_done) being complete implies PV_r(j) is
+// complete, so a rescale of O_r never races an MMA.
 //
 // Rescaling is conditional: a row keeps its reference maximum until the true
 // maximum exceeds it by more than 2^8 (P then stays below 256, exact enough in
 // bf16 and far from fp32 overflow); when any row of a warp must move, the warp
 // rescales its rows of O_r and l_r.
 //
-// P placement (template flag PSM): in TMEM over S_r (the S_r buffer is busy
-// until PV_r completes, so QK_r(j+1) follows PV_r(j)), or in shared memory
-// (S_r is released as soon as it is loaded, QK_r(j+1) is issued before
-// PV_r(j), and a pv_done barrier guards the P buffer and O_r rescales).
-//
-// Roles (320 threads, one CTA per SM):
+// Roles (352 threads, one CTA per SM):
 //   warp 0      TMA producer (Q once; then K_1, K_2 / K and V tiles into a ring
-//               of NSLOT equal slots, in the MMA thread's consumption order).
-//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer.
-//   warps 2-9   two softmax warpgroups, one per map; thread = one query row
+//               of NSLOT equal slots, in the order the MMA warps walk them).
+//   warps 1, 2  MMA issuers for map 1 and map 2 (warp 1 also allocates TMEM).
+//               One warp issues at most one tcgen05.mma about every 100
+//               cycles and an N = 128 MMA runs in 64, so each map gets its
+//               own issuer.  Both warps walk every ring fill, wait for it and
+//               commit its release once (empty barriers count two
+//               arrivals), also for the other map's K tiles, which they do
+//               not read.
+//   warps 3-10  two softmax warpgroups, one per map; thread = one query row
 //               (TMEM lane 32 (warp % 4) + lane) holding all 128 key columns
 //               of a tile, so no row statistic is exchanged between threads.
 //               Epilogue: warpgroup r owns output channels [64 r, +64).
@@ -51,7 +59,7 @@ struct OnePassCfg {
   static constexpr int BM = 128;
   static constexpr int BN = 128;
   static constexpr int DV = 128;
-  static constexpr int NCTRL = 2;  // producer, MMA
+  static constexpr int NCTRL = 3;  // producer, two MMA warps
   static constexpr int NSMWG = 2;  // one softmax warpgroup per map
   static constexpr int NTHREADS = (NCTRL + 4 * NSMWG) * 32;
   static constexpr int QB = D / 64;
@@ -62,9 +70,9 @@ struct OnePassCfg {
   static constexpr int SLOT = K_TILE;
   static constexpr int VF = V_TILE / SLOT;
   static constexpr int VKEYS = BN / VF;
-  static constexpr int P_TILE = BM * BN * 2;  // one map's P (bf16) when it lives in shared memory
   static constexpr int OFF_Q1 = 0;
   static constexpr int OFF_Q2 = Q_TILE;
+  static constexpr int P_TILE = BM * BN * 2;  // one map's P (bf16) when it lives in shared memory
   static constexpr int OFF_P = 2 * Q_TILE;
   static constexpr int OFF_RING = OFF_P + (PSM ? 2 * P_TILE : 0);
   static constexpr int OFF_BARS = OFF_RING + NSLOT * SLOT;
@@ -85,7 +93,7 @@ struct OnePassCfg {
 };
 
 template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM>
-__global__ void __launch_bounds__(320, 1) onepass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
+__global__ void __launch_bounds__(352, 1) onepass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
   using C = OnePassCfg<D, SHARED_K, EPI, NSLOT, PSM>;
   constexpr int BM = C::BM, BN = C::BN, DV = C::DV;
 
@@ -102,8 +110,8 @@ __global__ void __launch_bounds__(320, 1) onepass_fwd_kernel(const __grid_consta
   uint64_t* empty = full + NSLOT;
   uint64_t* s_full = empty + NSLOT;  // [2]: S_r of the current tile in its buffer
   uint64_t* p_ready = s_full + 2;    // [2]: P_r of the current tile written
-  uint64_t* s_free = p_ready + 2;    // [2]: (P in shared memory) S_r loaded by the softmax warps
-  uint64_t* pv_done = s_free + 2;    // [2]: (P in shared memory) PV_r of the tile completed
+  uint64_t* s_free = p_ready + 2;    // [2]: (PSM) S_r loaded by the map's softmax warps
+  uint64_t* pv_done = s_free + 2;    // [2]: (PSM) PV_r of the tile completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   float* lpart = reinterpret_cast<float*>(smem + C::OFF_LP);
@@ -136,10 +144,10 @@ __global__ void __launch_bounds__(320, 1) onepass_fwd_kernel(const __grid_consta
   // ---- set-up
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    mbar_init(o_full, 1);
+    mbar_init(o_full, 2);  // both MMA warps
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], 2);  // both MMA warps release every fill
     }
     for (int r = 0; r < 2; ++r) {
       mbar_init(&s_full[r], 1);
@@ -188,14 +196,17 @@ __global__ void __launch_bounds__(320, 1) onepass_fwd_kernel(const __grid_consta
         for (int bx = 0; bx < nbox; ++bx) tma_load_4d(dst + bx * rows * 128, map, &full[s], bx * 64, hk, key0, b);
         ++fill;
       };
+      // The fill order is the order in which both MMA warps walk the ring.
       load(&p.tm_k1, 0, BN, C::QB);
       if (!SHARED_K) load(&p.tm_k2, 0, BN, C::QB);
+      // PSM: the next tile's K before this tile's V (QK(j+1) is issued
+      // before PV(j)); otherwise after it.
       for (int j = 0; j < T; ++j) {
-        // Consumption order: with P in shared memory the next tile's QK^T is
-        // issued before this tile's PV, otherwise after it.
-        if (PSM && j + 1 < T) load(&p.tm_k1, (j + 1) * BN, BN, C::QB);
+        if (PSM && j + 1 < T) {
+          load(&p.tm_k1, (j + 1) * BN, BN, C::QB);
+          if (!SHARED_K) load(&p.tm_k2, (j + 1) * BN, BN, C::QB);
+        }
         for (int part = 0; part < C::VF; ++part) load(&p.tm_v, j * BN + part * C::VKEYS, C::VKEYS, C::VB);
-        if (PSM && j + 1 < T && !SHARED_K) load(&p.tm_k2, (j + 1) * BN, BN, C::QB);
         if (!PSM && j + 1 < T) {
           load(&p.tm_k1, (j + 1) * BN, BN, C::QB);
           if (!SHARED_K) load(&p.tm_k2, (j + 1) * BN, BN, C::QB);
@@ -207,140 +218,104 @@ __global__ void __launch_bounds__(320, 1) onepass_fwd_kernel(const __grid_consta
           mbar_wait_drain(&full[f % NSLOT], static_cast<uint32_t>(f / NSLOT) & 1u, kWaitBudgetCycles);
       }
     }
-  } else if (warp == 1) {
-    // =============================================================== MMA issuer
-    if (lane == 0) {
-      const uint64_t dQ1 = sdesc_sw128(smem_u32(smem + C::OFF_Q1), 16, 1024);
-      const uint64_t dQ2 = sdesc_sw128(smem_u32(smem + C::OFF_Q2), 16, 1024);
-      const uint64_t dRingK = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
-      const uint64_t dRingV = sdesc_sw128(smem_u32(smem + C::OFF_RING), C::VKEYS * 128, 1024);
-      const uint32_t tA = tmem + C::TM_A, tB = tmem + C::TM_B;
-      const uint32_t tO1 = tmem + C::TM_O1, tO2 = tmem + C::TM_O2;
-      int cons = 0;
-      bool ok = mbar_wait(q_full, 0, ab);
+  } else if (warp == 1 || warp == 2) {
+    // =============================================================== MMA issuers
+    // Warp 1 + r issues every MMA of map r + 1, warp-uniformly (descriptors
+    // stay in uniform registers), each from one elected lane.
+    const int r = warp - 1;
+    const uint64_t dQ = sdesc_sw128(smem_u32(smem + (r == 0 ? C::OFF_Q1 : C::OFF_Q2)), 16, 1024);
+    const uint64_t dRingK = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
+    const uint64_t dRingV = sdesc_sw128(smem_u32(smem + C::OFF_RING), C::VKEYS * 128, 1024);
+    const uint32_t tS = tmem + (r == 0 ? C::TM_A : C::TM_B);
+    const uint32_t tO = tmem + (r == 0 ? C::TM_O1 : C::TM_O2);
+    // Every wait returns the same verdict in all lanes and leaves the warp converged.
+    auto waitp = [&](uint64_t* bar, uint32_t parity) -> bool {
+      const bool v = __all_sync(0xffffffffu, mbar_wait(bar, parity, ab));
       tc_fence_after();
-      auto acquire = [&](int& s) -> bool {
-        s = cons % NSLOT;
-        const uint32_t use = static_cast<uint32_t>(cons / NSLOT);
-        ++cons;
-        if (!mbar_wait(&full[s], use & 1u, ab)) return false;
-        tc_fence_after();
-        return true;
-      };
-      auto qk = [&](uint32_t dst, uint64_t dq, int s) {
-        const uint64_t dk = dRingK + static_cast<uint64_t>((s * C::SLOT) >> 4);
+      return v;
+    };
+    int fill = 0;  // next ring fill: slot fill % NSLOT, its (fill / NSLOT)-th use
+    // Both warps wait on every fill in ring order, so each parity wait
+    // follows the completion of the slot's previous phase and is exact.
+    auto acquire_next = [&](int& s) -> bool {
+      s = fill % NSLOT;
+      const uint32_t use = static_cast<uint32_t>(fill / NSLOT);
+      ++fill;
+      return waitp(&full[s], use & 1u);
+    };
+    // A fill this map does not read is still awaited and then released: every
+    // arrival on a slot's empty barrier then follows the issue of that fill,
+    // so no warp can run ahead into the slot's next phase.
+    auto skip_next = [&]() -> bool {
+      int s;
+      const bool v = acquire_next(s);
+      tc_commit_elect(&empty[s]);
+      return v;
+    };
+    auto qk = [&](int s) {
+      const uint64_t dk = dRingK + static_cast<uint64_t>((s * C::SLOT) >> 4);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_ss(dst, dq + static_cast<uint64_t>((((k >> 2) * (BM * 128)) + (k & 3) * 32) >> 4),
-                 dk + static_cast<uint64_t>((((k >> 2) * (BN * 128)) + (k & 3) * 32) >> 4), C::IDESC_QK,
-                 k > 0 ? 1u : 0u);
-      };
-      int sv[2] = {0, 0};
-      auto pv = [&](uint32_t dO, uint32_t aP, int j) {
+      for (int k = 0; k < D / 16; ++k)
+        mma_ss_elect(tS, dQ + static_cast<uint64_t>((((k >> 2) * (BM * 128)) + (k & 3) * 32) >> 4),
+                     dk + static_cast<uint64_t>((((k >> 2) * (BN * 128)) + (k & 3) * 32) >> 4), C::IDESC_QK,
+                     k > 0 ? 1u : 0u);
+    };
+    // K fills of key tile jj: K (shared) or K_1 then K_2.  With P in shared
+    // memory QK_r(jj) only waits until the softmax has loaded S_r(jj-1).
+    auto k_tile = [&](int jj) -> bool {
+      if (!SHARED_K && r == 1 && !skip_next()) return false;
+      int s;
+      if (!acquire_next(s)) return false;
+      if (PSM && jj > 0 && !waitp(&s_free[r], static_cast<uint32_t>(jj - 1) & 1u)) return false;
+      qk(s);
+      tc_commit_elect(&s_full[r]);
+      tc_commit_elect(&empty[s]);
+      return SHARED_K || r == 1 || skip_next();
+    };
+    const uint64_t dP = sdesc_sw128(smem_u32(smem + C::OFF_P + r * C::P_TILE), 16, 1024);
+    bool ok = waitp(q_full, 0) && k_tile(0);
+    for (int j = 0; ok && j < T; ++j) {
+      if (PSM && j + 1 < T && !k_tile(j + 1)) {
+        ok = false;
+        break;
+      }
+      int sv[C::VF];
+      bool got = true;
 #pragma unroll
-        for (int part = 0; part < C::VF; ++part) {
-          const uint64_t dv = dRingV + static_cast<uint64_t>((sv[part] * C::SLOT) >> 4);
+      for (int part = 0; part < C::VF; ++part) got = acquire_next(sv[part]) && got;
+      if (!got || !waitp(&p_ready[r], static_cast<uint32_t>(j) & 1u)) {
+        ok = false;
+        break;
+      }
+      // PV_r(j): P_r from shared memory (k-step kg: keys 16 kg .. 16 kg + 15 =
+      // 64-key box kg / 4, 32-byte step kg % 4), or bf16 pairs in TMEM columns
+      // 8 kg .. 8 kg + 7 of the S_r buffer.
 #pragma unroll
-          for (int kk = 0; kk < C::VKEYS / 16; ++kk) {
-            const int kg = part * (C::VKEYS / 16) + kk;
-            mma_ts(dO, aP + 8u * kg, dv + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_PV,
-                   (j > 0 || kg > 0) ? 1u : 0u);
-          }
-        }
-      };
-      // PV with P from shared memory (K-major, 128-byte swizzle, two 64-key boxes).
-      const uint64_t dP1 = sdesc_sw128(smem_u32(smem + C::OFF_P), 16, 1024);
-      const uint64_t dP2 = sdesc_sw128(smem_u32(smem + C::OFF_P + C::P_TILE), 16, 1024);
-      auto pv_ss = [&](uint32_t dO, uint64_t dP, int j) {
+      for (int part = 0; part < C::VF; ++part) {
+        const uint64_t dv = dRingV + static_cast<uint64_t>((sv[part] * C::SLOT) >> 4);
 #pragma unroll
-        for (int part = 0; part < C::VF; ++part) {
-          const uint64_t dv = dRingV + static_cast<uint64_t>((sv[part] * C::SLOT) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < C::VKEYS / 16; ++kk) {
-            const int kg = part * (C::VKEYS / 16) + kk;
-            mma_ss(dO, dP + static_cast<uint64_t>((((kg >> 2) * (BM * 128)) + (kg & 3) * 32) >> 4),
-                   dv + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_PV, (j > 0 || kg > 0) ? 1u : 0u);
-          }
-        }
-      };
-      int sk = 0;
-      if (ok) ok = acquire(sk);
-      if (ok) {
-        qk(tA, dQ1, sk);
-        tc_commit(&s_full[0]);
-        if (!SHARED_K) {
-          tc_commit(&empty[sk]);
-          ok = acquire(sk);
+        for (int kk = 0; kk < C::VKEYS / 16; ++kk) {
+          const int kg = part * (C::VKEYS / 16) + kk;
+          const uint64_t dvk = dv + static_cast<uint64_t>(kk * (2048 >> 4));
+          const uint32_t acc = (j > 0 || kg > 0) ? 1u : 0u;
+          if (PSM)
+            mma_ss_elect(tO, dP + static_cast<uint64_t>((((kg >> 2) * (BM * 128)) + (kg & 3) * 32) >> 4), dvk,
+                         C::IDESC_PV, acc);
+          else
+            mma_ts_elect(tO, tS + 8u * kg, dvk, C::IDESC_PV, acc);
         }
       }
-      if (ok) {
-        qk(tB, dQ2, sk);
-        tc_commit(&s_full[1]);
-        tc_commit(&empty[sk]);
+      if (PSM) tc_commit_elect(&pv_done[r]);
+#pragma unroll
+      for (int part = 0; part < C::VF; ++part) tc_commit_elect(&empty[sv[part]]);
+      if (!PSM && j + 1 < T && !k_tile(j + 1)) {
+        ok = false;
+        break;
       }
-      if constexpr (PSM) {
-        // Per tile: QK1(j+1) as soon as S1(j) is loaded, PV1(j), QK2(j+1) as
-        // soon as S2(j) is loaded, PV2(j).
-        for (int j = 0; ok && j < T; ++j) {
-          const uint32_t ph = static_cast<uint32_t>(j) & 1u;
-          if (j + 1 < T) {
-            if (!acquire(sk)) break;
-            if (!mbar_wait(&s_free[0], ph, ab)) break;
-            tc_fence_after();
-            qk(tA, dQ1, sk);
-            tc_commit(&s_full[0]);
-            if (!SHARED_K) tc_commit(&empty[sk]);
-          }
-          for (int part = 0; part < C::VF; ++part)
-            if (!acquire(sv[part])) ok = false;
-          if (!ok) break;
-          if (!mbar_wait(&p_ready[0], ph, ab)) break;
-          tc_fence_after();
-          pv_ss(tO1, dP1, j);
-          tc_commit(&pv_done[0]);
-          if (j + 1 < T) {
-            if (!SHARED_K && !acquire(sk)) break;
-            if (!mbar_wait(&s_free[1], ph, ab)) break;
-            tc_fence_after();
-            qk(tB, dQ2, sk);
-            tc_commit(&s_full[1]);
-            tc_commit(&empty[sk]);
-          }
-          if (!mbar_wait(&p_ready[1], ph, ab)) break;
-          tc_fence_after();
-          pv_ss(tO2, dP2, j);
-          tc_commit(&pv_done[1]);
-          for (int part = 0; part < C::VF; ++part) tc_commit(&empty[sv[part]]);
-        }
-      } else {
-      for (int j = 0; ok && j < T; ++j) {
-          for (int part = 0; part < C::VF; ++part)
-            if (!acquire(sv[part])) ok = false;
-          if (!ok) break;
-          if (!mbar_wait(&p_ready[0], static_cast<uint32_t>(j) & 1u, ab)) break;
-          tc_fence_after();
-          pv(tO1, tA, j);
-          if (j + 1 < T) {
-            if (!acquire(sk)) break;
-            qk(tA, dQ1, sk);
-            tc_commit(&s_full[0]);
-            if (!SHARED_K) tc_commit(&empty[sk]);
-          }
-          if (!mbar_wait(&p_ready[1], static_cast<uint32_t>(j) & 1u, ab)) break;
-          tc_fence_after();
-          pv(tO2, tB, j);
-          for (int part = 0; part < C::VF; ++part) tc_commit(&empty[sv[part]]);
-          if (j + 1 < T) {
-            if (!SHARED_K && !acquire(sk)) break;
-            qk(tB, dQ2, sk);
-            tc_commit(&s_full[1]);
-            tc_commit(&empty[sk]);
-          }
-        }
-      }
-      tc_commit(o_full);
-      if (*ab.flag) mbar_wait_drain(o_full, 0, kWaitBudgetCycles);
     }
+    tc_commit_elect(o_full);
+    if (*ab.flag) mbar_wait_drain(o_full, 0, kWaitBudgetCycles);
+    __syncwarp();
   } else {
     // =============================================================== softmax + epilogue
     // Warpgroup `map` owns map (map + 1); thread = one query row, all 128 key
@@ -443,8 +418,8 @@ __global__ void __launch_bounds__(320, 1) onepass_fwd_kernel(const __grid_consta
         for (int q = 0; q < 4; ++q) tmem_st16(tS + 16u * q, reinterpret_cast<const uint32_t(&)[16]>(x[q]));
       }
       if (rescale && j > 0) {
-        // PSM: PV_r(j-1) completed (awaited above).  Otherwise it completed
-        // before S_r(j) did: it was issued before QK_r(j).
+        // PV_r(j-1) is complete: awaited above (PSM), or issued by the same
+        // warp before QK_r(j), whose commit of S_r(j) tracks all its MMAs.
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t o[32];

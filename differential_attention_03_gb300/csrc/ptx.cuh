@@ -73,6 +73,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+
 // Bounded wait used only while tearing down after an abort: ignores the abort
 // flag, so that copies and MMAs already in flight can land before exit.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t budget_cycles) {

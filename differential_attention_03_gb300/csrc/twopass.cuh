@@ -83,7 +83,7 @@ struct TwoPassCfg {
   static constexpr int OFF_P = 2 * Q_TILE;
   static constexpr int OFF_RING = OFF_P + P_TILE;
   static constexpr int OFF_BARS = OFF_RING + NSLOT * SLOT;
-  static constexpr int NBARS = 2 * NSLOT + 18;
+  static constexpr int NBARS = 3 * NSLOT + 18;
   static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
@@ -163,8 +163,8 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
   const int lane = threadIdx.x & 31;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
-  uint64_t* full = bars;              // [NSLOT] ring slot loaded
-  uint64_t* empty = full + NSLOT;     // [NSLOT] ring slot released by the MMAs
+  uint64_t* full = bars;              // [2][NSLOT] ring slot loaded, one barrier per consuming warp
+  uint64_t* empty = full + 2 * NSLOT; // [NSLOT] ring slot released by the MMAs
   uint64_t* q_full = empty + NSLOT;
   uint64_t* o_full = q_full + 1;
   uint64_t* s1_full = o_full + 1;     // [4] sweep 1: S written into TMEM buffer b
@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&full[s], 1);
+      mbar_init(&full[NSLOT + s], 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(q_full, 1);
@@ -250,8 +251,16 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
       }
       int fill = 0;
       bool ok = true;
+      // Each fill signals the `full` barrier of the warp that reads it (o = 0:
+      // warp 1, K_1 and V; o = 1: warp 2, K_2), so every warp sees only its
+      // own fills, in order, and its parity waits are exact.  For the abort
+      // drain, bit s of `last_o` is the owner of slot s's latest fill and bit
+      // (o NSLOT + s) of `par` the parity of owner o's latest fill in slot s
+      // (register bit masks: this bookkeeping sits on the producer's path).
+      static_assert(2 * NSLOT <= 32, "bit masks");
+      uint32_t last_o = 0, par = 0;
       // One slot fill: `nbox` boxes of [rows][64 columns] at key row `key0`.
-      auto load = [&](const CUtensorMap* map, int key0, int rows, int nbox) {
+      auto load = [&](const CUtensorMap* map, int key0, int rows, int nbox, int o) {
         if (!ok) return;
         const int s = fill % NSLOT;
         const uint32_t use = static_cast<uint32_t>(fill / NSLOT);
@@ -259,13 +268,16 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
           ok = false;
           return;
         }
+        uint64_t* bar = &full[o * NSLOT + s];
         uint8_t* dst = smem + C::OFF_RING + s * C::SLOT;
-        mbar_arrive_expect_tx(&full[s], C::SLOT);
-        for (int bx = 0; bx < nbox; ++bx) tma_load_4d(dst + bx * rows * 128, map, &full[s], bx * 64, hk, key0, b);
+        mbar_arrive_expect_tx(bar, C::SLOT);
+        for (int bx = 0; bx < nbox; ++bx) tma_load_4d(dst + bx * rows * 128, map, bar, bx * 64, hk, key0, b);
+        last_o = (last_o & ~(1u << s)) | (static_cast<uint32_t>(o) << s);
+        par ^= 1u << (o * NSLOT + s);  // now the parity after this fill; the fill's own is the flip of it
         ++fill;
       };
-      auto load_k1 = [&](int j) { load(&p.tm_k1, j * BN, BN, C::QB); };
-      auto load_k2 = [&](int j) { load(&p.tm_k2, j * BN, BN, C::QB); };
+      auto load_k1 = [&](int j) { load(&p.tm_k1, j * BN, BN, C::QB, 0); };
+      auto load_k2 = [&](int j) { load(&p.tm_k2, j * BN, BN, C::QB, 1); };
       // The fill order is exactly the MMA thread's consumption order.
       for (int j = 0; j < T; ++j) {  // sweep 1
         load_k1(j);
@@ -286,13 +298,15 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
             load_k1(j + 1);
           }
         }
-        for (int part = 0; part < C::VF; ++part) load(&p.tm_v, j * BN + part * C::VKEYS, C::VKEYS, C::VB);
+        for (int part = 0; part < C::VF; ++part) load(&p.tm_v, j * BN + part * C::VKEYS, C::VKEYS, C::VB, 0);
       }
       if (*ab.flag) {
         // Aborted: let the copies already issued land before the CTA exits.
         mbar_wait_drain(q_full, 0, kWaitBudgetCycles);
-        for (int f = (fill > NSLOT ? fill - NSLOT : 0); f < fill; ++f)
-          mbar_wait_drain(&full[f % NSLOT], static_cast<uint32_t>(f / NSLOT) & 1u, kWaitBudgetCycles);
+        for (int i = 0; i < NSLOT && i < fill; ++i) {
+          const int o = (last_o >> i) & 1;
+          mbar_wait_drain(&full[o * NSLOT + i], ((par >> (o * NSLOT + i)) & 1u) ^ 1u, kWaitBudgetCycles);
+        }
       }
     }
   } else if (warp == 1 || warp == 2) {
@@ -321,8 +335,17 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
       tc_fence_after();
       return r;
     };
-    // Ring fill f sits in slot f % NSLOT, its (f / NSLOT)-th use.
-    auto acquire = [&](int f) -> bool { return waitp(&full[f % NSLOT], static_cast<uint32_t>(f / NSLOT) & 1u); };
+    // Ring fill f sits in slot f % NSLOT and signals this warp's own `full`
+    // barrier of the slot; bit s of `ph` is the parity of this warp's next
+    // fill in slot s (each warp acquires its fills in increasing order).
+    uint32_t ph = 0;
+    uint64_t* my_full = full + mw * NSLOT;
+    auto acquire = [&](int f) -> bool {
+      const int s = f % NSLOT;
+      const uint32_t par = (ph >> s) & 1u;
+      ph ^= 1u << s;
+      return waitp(&my_full[s], par);
+    };
     auto qk = [&](uint32_t dst, int f) {
       const uint64_t dk = dRingK + static_cast<uint64_t>(((f % NSLOT) * C::SLOT) >> 4);
 #pragma unroll
