@@ -83,6 +83,8 @@ V1_SMALL = [
     ("bf16", 1, 2, 128, 64, True, "ones"),
     ("bf16", 1, 2, 129, 64, True, "ones"),
     ("bf16", 1, 1, 640, 128, True, "ones"),
+    ("bf16", 1, 2, 1100, 64, True, "uniform"),  # up to 9 key tiles: every ring / double-buffer phase recurs
+    ("bf16", 1, 1, 1100, 128, False, "uniform"),
     ("f32", 1, 1, 128, 64, True, "ones"),
     ("f32", 2, 3, 77, 32, False, "uniform"),
     ("f32", 1, 2, 150, 128, True, "uniform"),
@@ -130,6 +132,7 @@ V2_SMALL = [
     ("bf16", 1, 8, 2, 257, False, "pair"),
     ("bf16", 1, 4, 1, 128, True, "token"),
     ("bf16", 2, 4, 2, 1, True, "pair"),
+    ("bf16", 1, 4, 2, 1100, True, "token"),  # up to 9 key tiles
     ("f32", 1, 4, 2, 100, True, "pair"),
     ("f32", 2, 8, 2, 70, False, "token"),
 ]
