@@ -1,0 +1,366 @@
+"""Host model of the kernels' mbarrier protocols, run under random interleavings.
+
+The tcgen05 kernels hand data between a TMA producer warp, MMA-issuing warps
+and softmax warps through mbarriers that are waited on by phase parity.  A
+parity wait is only exact if the waiter has seen the barrier's previous
+phase complete; a waiter two phases behind, or one waiting for a phase whose
+predecessor is still pending, misreads the barrier.  Such slips show up on a
+GPU as a rare hang or as stale shared memory, so the protocols are modelled
+here on the host, step by step, with every agent advanced in random order:
+
+  * producer: fills ring slots in a fixed order, waiting on each slot's
+    `empty` barrier (all of the slot's releasers must have arrived);
+  * MMA warps: wait with the same parities the kernels use; their MMAs and
+    tcgen05.commit arrivals complete in issue order per warp, at random
+    later times;
+  * softmax warps: wait and arrive as the kernels do.
+
+Each ring slot, TMEM S buffer and shared-memory P buffer carries a tag of
+what was last written into it; a read that finds another tag (stale or
+overwritten data) is an error, and so is a state in which no agent can move
+(a deadlock).  The models follow the kernels in
+differential_attention_03_gb300/csrc (onepass.cuh, twopass.cuh).  Two
+variants that were wrong are kept as negative checks: the model must catch
+them.
+"""
+
+import random
+
+import pytest
+
+
+class Bar:
+    def __init__(self, count):
+        self.count = count
+        self.pending = count
+        self.phase = 0
+
+    def arrive(self):
+        self.pending -= 1
+        assert self.pending >= 0
+        if self.pending == 0:
+            self.phase += 1
+            self.pending = self.count
+
+    def done(self, parity):
+        # mbarrier.try_wait.parity: true once the phase of that parity has completed,
+        # i.e. when the current phase's parity differs.
+        return (self.phase & 1) != parity
+
+
+class World:
+    def __init__(self, seed):
+        self.rnd = random.Random(seed)
+        self.errors = []
+        self.pipes = {}     # MMA warp -> FIFO of ('mma', fn) / ('commit', bar)
+        self.tma = []       # (slot, tag, bar)
+        self.slot = {}      # ring slot -> tag of the fill it holds
+        self.tmem = {}      # TMEM buffer -> tag
+        self.pbuf = {}      # P buffer -> tag
+
+    def wait(self, bar, parity):
+        while not bar.done(parity):
+            yield
+
+    def mma(self, warp, fn):
+        self.pipes.setdefault(warp, []).append(("mma", fn))
+
+    def commit(self, warp, bar):
+        self.pipes.setdefault(warp, []).append(("commit", bar))
+
+    def expect(self, table, key, tag, what):
+        if table.get(key) != tag:
+            self.errors.append(f"{what}: {key} holds {table.get(key)}, wanted {tag}")
+
+    def run(self, agents, max_steps=400000):
+        live = dict(agents)
+        steps = 0
+        while live or self.tma or any(self.pipes.values()):
+            steps += 1
+            if steps > max_steps:  # every agent left is blocked on a wait that never completes
+                return "deadlock"
+            moves = list(live) + (["tma"] if self.tma else []) + [w for w, q in self.pipes.items() if q]
+            c = self.rnd.choice(moves)
+            if c == "tma":
+                i = 0 if self.rnd.random() < 0.6 else self.rnd.randrange(len(self.tma))
+                s, tag, bar = self.tma.pop(i)
+                self.slot[s] = tag
+                bar.arrive()
+            elif c in live:
+                try:
+                    next(live[c])
+                except StopIteration:
+                    del live[c]
+            else:
+                kind, x = self.pipes[c].pop(0)
+                if kind == "commit":
+                    x.arrive()
+                else:
+                    x()
+        return "ok" if not self.errors else self.errors[0]
+
+
+# --------------------------------------------------------------------------- one-pass kernel
+def onepass(T, seed, nslot, psm, shared_k, vf=2, npb=1, p_ready_per_buffer=True):
+    """onepass.cuh: one MMA warp per map, both walk every fill (empty counts 2)."""
+    W = World(seed)
+    full = [Bar(1) for _ in range(nslot)]
+    empty = [Bar(2) for _ in range(nslot)]
+    s_full = [Bar(1) for _ in range(2)]
+    s_free = [Bar(1) for _ in range(2)]
+    nbar = npb if p_ready_per_buffer else 1
+    p_ready = [[Bar(1) for _ in range(nbar)] for _ in range(2)]
+    pv_done = [[Bar(1) for _ in range(npb)] for _ in range(2)]
+    o_full = Bar(2)
+    fills = [("K1", 0)] + ([] if shared_k else [("K2", 0)])
+    for j in range(T):
+        if psm and j + 1 < T:
+            fills += [("K1", j + 1)] + ([] if shared_k else [("K2", j + 1)])
+        fills += [("V", j, p) for p in range(vf)]
+        if not psm and j + 1 < T:
+            fills += [("K1", j + 1)] + ([] if shared_k else [("K2", j + 1)])
+
+    def producer():
+        for f, tag in enumerate(fills):
+            s, use = f % nslot, f // nslot
+            if use:
+                yield from W.wait(empty[s], (use - 1) & 1)
+            W.tma.append((s, tag, full[s]))
+
+    def mma(r):
+        fill = 0
+        mine = "K1" if (r == 0 or shared_k) else "K2"
+
+        def acquire():
+            nonlocal fill
+            f = fill
+            fill += 1
+            s = f % nslot
+            yield from W.wait(full[s], (f // nslot) & 1)
+            W.expect(W.slot, s, fills[f], f"warp {r} acquire")
+            return s, fills[f]
+
+        def k_tile(jj):
+            while True:
+                s, tag = yield from acquire()
+                if tag[0] == mine:
+                    break
+                W.commit(r, empty[s])        # the other map's K: waited on, released
+            if psm and jj > 0:
+                yield from W.wait(s_free[r], (jj - 1) & 1)
+
+            def qk(s=s, tag=tag, jj=jj):
+                W.expect(W.slot, s, tag, f"QK{r + 1}({jj}) reads K")
+                W.tmem[("S", r)] = jj
+            W.mma(r, qk)
+            W.commit(r, s_full[r])
+            W.commit(r, empty[s])
+            if not shared_k and r == 0:
+                s2, _ = yield from acquire()  # K_2 of the same tile
+                W.commit(r, empty[s2])
+
+        yield from k_tile(0)
+        for j in range(T):
+            if psm and j + 1 < T:
+                yield from k_tile(j + 1)
+            sv = []
+            for _ in range(vf):
+                sv.append((yield from acquire()))
+            b = j % npb
+            yield from W.wait(p_ready[r][b if p_ready_per_buffer else 0],
+                              (j // npb if p_ready_per_buffer else j) & 1)
+
+            def pv(sv=sv, j=j, b=b):
+                for s, tag in sv:
+                    W.expect(W.slot, s, tag, f"PV{r + 1}({j}) reads V")
+                if psm:
+                    W.expect(W.pbuf, (r, b), j, f"PV{r + 1}({j}) reads P")
+                else:
+                    W.expect(W.tmem, ("P", r), j, f"PV{r + 1}({j}) reads P in TMEM")
+            W.mma(r, pv)
+            if psm:
+                W.commit(r, pv_done[r][b])
+            for s, _ in sv:
+                W.commit(r, empty[s])
+            if not psm and j + 1 < T:
+                yield from k_tile(j + 1)
+        W.commit(r, o_full)
+
+    def softmax(r):
+        for j in range(T):
+            yield from W.wait(s_full[r], j & 1)
+            W.expect(W.tmem, ("S", r), j, f"softmax {r + 1} reads S({j})")
+            if psm:
+                s_free[r].arrive()
+                b = j % npb
+                if j >= npb:
+                    yield from W.wait(pv_done[r][b], ((j - npb) // npb) & 1)
+                W.pbuf[(r, b)] = j
+            else:
+                W.tmem[("P", r)] = j      # P over S in TMEM
+            yield
+            p_ready[r][(j % npb) if p_ready_per_buffer else 0].arrive()
+        yield from W.wait(o_full, 0)
+
+    return W.run({"prod": producer(), "mma0": mma(0), "mma1": mma(1), "sm0": softmax(0), "sm1": softmax(1)})
+
+
+# --------------------------------------------------------------------------- two-sweep kernel
+def twopass(T, seed, nslot=4, vf=2, per_owner_full=True):
+    """twopass.cuh: warp 1 issues map-1 MMAs and P.V, warp 2 map-2 MMAs; each fill has one reader."""
+    W = World(seed)
+    nown = 2 if per_owner_full else 1
+    full = [[Bar(1) for _ in range(nslot)] for _ in range(nown)]
+    empty = [Bar(1) for _ in range(nslot)]
+    s1_full = [Bar(1) for _ in range(4)]
+    s1_free = [Bar(1) for _ in range(4)]
+    a2_full, b2_full, a2_free, b2_free = Bar(1), Bar(1), Bar(1), Bar(1)
+    p_ready, pv_done, o_full, w2_done = Bar(1), Bar(1), Bar(1), Bar(1)
+    xchg = Bar(2)
+    fills = []  # (tag, owner)
+    for j in range(T):
+        fills += [(("K1", j), 0), (("K2", j), 1)]
+    fills += [(("K2", 0), 1), (("K1", 0), 0)]
+    for j in range(T):
+        if j + 1 < T:
+            fills += [(("K2", j + 1), 1), (("K1", j + 1), 0)]
+        fills += [(("V", j, p), 0) for p in range(vf)]
+
+    def producer():
+        for f, (tag, o) in enumerate(fills):
+            s, use = f % nslot, f // nslot
+            if use:
+                yield from W.wait(empty[s], (use - 1) & 1)
+            W.tma.append((s, tag, full[o if per_owner_full else 0][s]))
+
+    def mma(mw):
+        ph = 0  # per-slot parity bits of this warp's own fills (per-owner barriers)
+        my = [f for f, (_, o) in enumerate(fills) if o == mw]
+        it = iter(my)
+
+        def acquire():
+            nonlocal ph
+            f = next(it)
+            s = f % nslot
+            if per_owner_full:
+                par = (ph >> s) & 1
+                ph ^= 1 << s
+                yield from W.wait(full[mw][s], par)
+            else:
+                yield from W.wait(full[0][s], (f // nslot) & 1)
+            W.expect(W.slot, s, fills[f][0], f"warp {mw + 1} acquire")
+            return s, fills[f][0]
+
+        def qk(buf, s, tag, what):
+            def go():
+                W.expect(W.slot, s, tag, what)
+                W.tmem[buf] = what
+            W.mma(mw, go)
+
+        use = {0: 0, 1: 0, 2: 0, 3: 0}
+        for j in range(T):
+            k = 2 * j + mw
+            bb = k & 3
+            s, tag = yield from acquire()
+            if use[bb]:
+                yield from W.wait(s1_free[bb], (use[bb] - 1) & 1)
+            use[bb] += 1
+            qk(("S1buf", bb), s, tag, ("sw1", k))
+            W.commit(mw, s1_full[bb])
+            W.commit(mw, empty[s])
+        if use[mw + 2]:
+            yield from W.wait(s1_free[mw + 2], (use[mw + 2] - 1) & 1)
+        sfull, sfree = (a2_full, a2_free) if mw == 0 else (b2_full, b2_free)
+        s, tag = yield from acquire()
+        qk(("S1buf", mw + 2), s, tag, ("sw2", mw, 0))
+        W.commit(mw, sfull)
+        W.commit(mw, empty[s])
+        for j in range(T):
+            if j + 1 < T:
+                s, tag = yield from acquire()
+                yield from W.wait(sfree, j & 1)
+                qk(("S1buf", mw + 2), s, tag, ("sw2", mw, j + 1))
+                W.commit(mw, sfull)
+                W.commit(mw, empty[s])
+            if mw == 0:
+                sv = []
+                for _ in range(vf):
+                    sv.append((yield from acquire()))
+                yield from W.wait(p_ready, j & 1)
+
+                def pv(sv=sv, j=j):
+                    for s_, tag_ in sv:
+                        W.expect(W.slot, s_, tag_, f"PV({j}) reads V")
+                    W.expect(W.pbuf, 0, j, f"PV({j}) reads P")
+                    W.tmem[("O",)] = j
+                W.mma(mw, pv)
+                W.commit(mw, pv_done)
+                for s_, _ in sv:
+                    W.commit(mw, empty[s_])
+        W.commit(mw, o_full if mw == 0 else w2_done)
+
+    def softmax(m):
+        for j in range(T):
+            k = 2 * j + m
+            bb = k & 3
+            yield from W.wait(s1_full[bb], (k >> 2) & 1)
+            W.expect(W.tmem, ("S1buf", bb), ("sw1", k), f"sweep-1 softmax {m} reads S")
+            s1_free[bb].arrive()
+        xchg.arrive()
+        yield from W.wait(xchg, 0)
+        if m == 1:
+            yield from W.wait(o_full, 0)
+            return
+        for j in range(T):
+            yield from W.wait(b2_full, j & 1)
+            W.expect(W.tmem, ("S1buf", 3), ("sw2", 1, j), "sweep-2 softmax reads S2")
+            b2_free.arrive()
+            yield from W.wait(a2_full, j & 1)
+            W.expect(W.tmem, ("S1buf", 2), ("sw2", 0, j), "sweep-2 softmax reads S1")
+            a2_free.arrive()
+            if j:
+                yield from W.wait(pv_done, (j - 1) & 1)
+            W.pbuf[0] = j
+            p_ready.arrive()
+        yield from W.wait(o_full, 0)
+
+    return W.run({"prod": producer(), "w1": mma(0), "w2": mma(1), "sm0": softmax(0), "sm1": softmax(1)})
+
+
+TS = [1, 2, 3, 5, 9]
+
+
+@pytest.mark.parametrize("T", TS)
+def test_onepass_p_in_smem(T):
+    for seed in range(25):
+        assert onepass(T, seed, nslot=7, psm=True, shared_k=False) == "ok", seed
+
+
+@pytest.mark.parametrize("T", TS)
+def test_onepass_p_in_tmem_shared_k(T):
+    for seed in range(25):
+        assert onepass(T, seed, nslot=4, psm=False, shared_k=True, vf=1) == "ok", seed
+
+
+@pytest.mark.parametrize("T", TS)
+def test_twopass_per_owner_full_barriers(T):
+    for seed in range(25):
+        assert twopass(T, seed) == "ok", seed
+
+
+def test_model_catches_double_buffered_p_with_one_ready_barrier():
+    # Two P buffers let a map's softmax finish tiles j and j+1 before its MMA
+    # warp waits for tile j: one p_ready barrier then completes two phases unseen.
+    bad = [onepass(T, seed, nslot=4, psm=True, shared_k=False, npb=2, p_ready_per_buffer=False)
+           for T in (3, 5, 9) for seed in range(25)]
+    assert any(r != "ok" for r in bad)
+    good = [onepass(T, seed, nslot=4, psm=True, shared_k=False, npb=2, p_ready_per_buffer=True)
+            for T in (3, 5, 9) for seed in range(25)]
+    assert all(r == "ok" for r in good)
+
+
+def test_model_catches_shared_full_barriers_with_partial_waiters():
+    # One full barrier per slot, but each warp waits only on its own fills: at the
+    # switch between the sweeps a warp can take an older phase for its fill.
+    bad = [twopass(T, seed, per_owner_full=False) for T in (2, 3, 5) for seed in range(60)]
+    assert any(r != "ok" for r in bad)
