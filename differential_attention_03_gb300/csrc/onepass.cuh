@@ -304,10 +304,11 @@ __global__ void __launch_bounds__(352, 1) onepass_fwd_kernel(const __grid_consta
           else
             mma_ts_elect(tO, tS + 8u * kg, dvk, C::IDESC_PV, acc);
         }
+        // Each V part is released as soon as its own MMAs are done.
+        if (part + 1 < C::VF) tc_commit_elect(&empty[sv[part]]);
       }
       if (PSM) tc_commit_elect(&pv_done[r]);
-#pragma unroll
-      for (int part = 0; part < C::VF; ++part) tc_commit_elect(&empty[sv[part]]);
+      tc_commit_elect(&empty[sv[C::VF - 1]]);
       if (!PSM && j + 1 < T && !k_tile(j + 1)) {
         ok = false;
         break;

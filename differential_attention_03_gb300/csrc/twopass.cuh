@@ -421,10 +421,12 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
             mma_ss_elect(tmem + C::TM_O, dP + static_cast<uint64_t>((((kg >> 2) * (BM * 128)) + (kg & 3) * 32) >> 4),
                          dv + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_PV, (j > 0 || kg > 0) ? 1u : 0u);
           }
+          // Each V part is released as soon as its own MMAs are done, so the
+          // next tile's first part starts loading half a P.V earlier.
+          if (part + 1 < C::VF) tc_commit_elect(&empty[fill_v(j, part) % NSLOT]);
         }
         tc_commit_elect(pv_done);
-#pragma unroll
-        for (int part = 0; part < C::VF; ++part) tc_commit_elect(&empty[fill_v(j, part) % NSLOT]);
+        tc_commit_elect(&empty[fill_v(j, C::VF - 1) % NSLOT]);
       }
     }
     uint64_t* last = (mw == 0) ? o_full : w2_done;

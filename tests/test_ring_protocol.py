@@ -170,18 +170,19 @@ def onepass(T, seed, nslot, psm, shared_k, vf=2, npb=1, p_ready_per_buffer=True)
             yield from W.wait(p_ready[r][b if p_ready_per_buffer else 0],
                               (j // npb if p_ready_per_buffer else j) & 1)
 
-            def pv(sv=sv, j=j, b=b):
-                for s, tag in sv:
+            for i, (s, tag) in enumerate(sv):  # the MMAs of one V part, then its release
+                def pv(s=s, tag=tag, j=j, b=b):
                     W.expect(W.slot, s, tag, f"PV{r + 1}({j}) reads V")
-                if psm:
-                    W.expect(W.pbuf, (r, b), j, f"PV{r + 1}({j}) reads P")
-                else:
-                    W.expect(W.tmem, ("P", r), j, f"PV{r + 1}({j}) reads P in TMEM")
-            W.mma(r, pv)
+                    if psm:
+                        W.expect(W.pbuf, (r, b), j, f"PV{r + 1}({j}) reads P")
+                    else:
+                        W.expect(W.tmem, ("P", r), j, f"PV{r + 1}({j}) reads P in TMEM")
+                W.mma(r, pv)
+                if i + 1 < len(sv):
+                    W.commit(r, empty[s])
             if psm:
                 W.commit(r, pv_done[r][b])
-            for s, _ in sv:
-                W.commit(r, empty[s])
+            W.commit(r, empty[sv[-1][0]])
             if not psm and j + 1 < T:
                 yield from k_tile(j + 1)
         W.commit(r, o_full)
@@ -288,15 +289,16 @@ def twopass(T, seed, nslot=4, vf=2, per_owner_full=True):
                     sv.append((yield from acquire()))
                 yield from W.wait(p_ready, j & 1)
 
-                def pv(sv=sv, j=j):
-                    for s_, tag_ in sv:
+                for i, (s_, tag_) in enumerate(sv):  # the MMAs of one V part, then its release
+                    def pv(s_=s_, tag_=tag_, j=j):
                         W.expect(W.slot, s_, tag_, f"PV({j}) reads V")
-                    W.expect(W.pbuf, 0, j, f"PV({j}) reads P")
-                    W.tmem[("O",)] = j
-                W.mma(mw, pv)
+                        W.expect(W.pbuf, 0, j, f"PV({j}) reads P")
+                        W.tmem[("O",)] = j
+                    W.mma(mw, pv)
+                    if i + 1 < len(sv):
+                        W.commit(mw, empty[s_])
                 W.commit(mw, pv_done)
-                for s_, _ in sv:
-                    W.commit(mw, empty[s_])
+                W.commit(mw, empty[sv[-1][0]])
         W.commit(mw, o_full if mw == 0 else w2_done)
 
     def softmax(m):
