@@ -31,7 +31,7 @@
 // bf16 and far from fp32 overflow); when any row of a warp must move, the warp
 // rescales its rows of O_r and l_r.
 //
-// Roles (352 threads, one CTA per SM):
+// Roles (608 threads, one CTA per SM):
 //   warp 0      TMA producer (Q once; then K_1, K_2 / K and V tiles into a ring
 //               of NSLOT equal slots, in the order the MMA warps walk them).
 //   warps 1, 2  MMA issuers for map 1 and map 2 (warp 1 also allocates TMEM).
@@ -41,10 +41,15 @@
 //               commit its release once (empty barriers count two
 //               arrivals), also for the other map's K tiles, which they do
 //               not read.
-//   warps 3-10  two softmax warpgroups, one per map; thread = one query row
-//               (TMEM lane 32 (warp % 4) + lane) holding all 128 key columns
-//               of a tile, so no row statistic is exchanged between threads.
-//               Epilogue: warpgroup r owns output channels [64 r, +64).
+//   warps 3-18  four softmax warpgroups, two per map: warpgroup (r, h) owns
+//               key columns [64 h, +64) of every tile of map r; thread = one
+//               query row (TMEM lane 32 (warp % 4) + lane).  The two halves of
+//               a row agree on the running maximum through shared memory (a
+//               named barrier per map and tile), so both scale P alike and
+//               take the same rescale decisions; their partial row sums are
+//               added in the epilogue, where warpgroup (r, h) owns output
+//               channels [32 (2 r + h), +32).  Two halves give four warps per
+//               SM sub-partition to hide the latency of loads and exp2.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -60,7 +65,7 @@ struct OnePassCfg {
   static constexpr int BN = 128;
   static constexpr int DV = 128;
   static constexpr int NCTRL = 3;  // producer, two MMA warps
-  static constexpr int NSMWG = 2;  // one softmax warpgroup per map
+  static constexpr int NSMWG = 4;  // two softmax warpgroups per map
   static constexpr int NTHREADS = (NCTRL + 4 * NSMWG) * 32;
   static constexpr int QB = D / 64;
   static constexpr int VB = DV / 64;
@@ -78,9 +83,10 @@ struct OnePassCfg {
   static constexpr int OFF_BARS = OFF_RING + NSLOT * SLOT;
   static constexpr int NBARS = 2 + 2 * NSLOT + 8;
   static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
-  static constexpr int OFF_LP = (OFF_MISC + 16 + 15) / 16 * 16;  // float [2][128]
-  static constexpr int OFF_SS = OFF_LP + 2 * 128 * 4;             // float [2][128]
-  static constexpr int SMEM_BYTES = OFF_SS + 2 * 128 * 4 + 1024;  // + 1 KB alignment slack
+  static constexpr int OFF_LP = (OFF_MISC + 16 + 15) / 16 * 16;  // float [4][128] partial row sums
+  static constexpr int OFF_SS = OFF_LP + 4 * 128 * 4;             // float [4][128] partial sums of squares
+  static constexpr int OFF_XM = OFF_SS + 4 * 128 * 4;             // float [2 tiles][2 maps][2 halves][128]
+  static constexpr int SMEM_BYTES = OFF_XM + 8 * 128 * 4 + 1024;  // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TM_O1 = 0, TM_O2 = 128, TM_A = 256, TM_B = 384;
   static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false, false);
@@ -93,7 +99,7 @@ struct OnePassCfg {
 };
 
 template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM>
-__global__ void __launch_bounds__(352, 1) onepass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
+__global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
   using C = OnePassCfg<D, SHARED_K, EPI, NSLOT, PSM>;
   constexpr int BM = C::BM, BN = C::BN, DV = C::DV;
 
@@ -116,6 +122,7 @@ __global__ void __launch_bounds__(352, 1) onepass_fwd_kernel(const __grid_consta
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   float* lpart = reinterpret_cast<float*>(smem + C::OFF_LP);
   float* sspart = reinterpret_cast<float*>(smem + C::OFF_SS);
+  float* xmax = reinterpret_cast<float*>(smem + C::OFF_XM);
 
   // ---- which tile this CTA owns
   const int units = p.B * p.units_per_batch;
@@ -151,8 +158,8 @@ __global__ void __launch_bounds__(352, 1) onepass_fwd_kernel(const __grid_consta
     }
     for (int r = 0; r < 2; ++r) {
       mbar_init(&s_full[r], 1);
-      mbar_init(&p_ready[r], 4);  // the map's 4 warps
-      mbar_init(&s_free[r], 4);
+      mbar_init(&p_ready[r], 8);  // the map's 8 softmax warps
+      mbar_init(&s_free[r], 8);
       mbar_init(&pv_done[r], 1);
     }
     *abort_flag = 0;
@@ -319,10 +326,10 @@ __global__ void __launch_bounds__(352, 1) onepass_fwd_kernel(const __grid_consta
     __syncwarp();
   } else {
     // =============================================================== softmax + epilogue
-    // Warpgroup `map` owns map (map + 1); thread = one query row, all 128 key
-    // columns of each tile, so no row statistic is shared between threads.
-    const int map = (warp - C::NCTRL) >> 2;  // 0 or 1
-    const int wq = warp & 3;                  // TMEM lane quarter
+    const int sw = warp - C::NCTRL;   // 0..15
+    const int map = sw >> 3;          // map (map + 1)
+    const int half = (sw >> 2) & 1;   // key columns [64 half, +64) of each tile
+    const int wq = warp & 3;          // TMEM lane quarter
     const int row = wq * 32 + lane;
     const int t = q0 + row;
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
@@ -337,11 +344,10 @@ __global__ void __launch_bounds__(352, 1) onepass_fwd_kernel(const __grid_consta
       mbar_wait(&s_full[map], static_cast<uint32_t>(j) & 1u, ab);
       __syncwarp();
       tc_fence_after();
-      uint32_t x[4][32];
+      uint32_t x[2][32];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_ld32(tS + 32u * q, x[q]);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_ld_wait(x[q]);
+      for (int q = 0; q < 2; ++q) tmem_ld32(tS + 64u * half + 32u * q, x[q]);
+      tmem_ld_wait2(x[0], x[1]);
       if constexpr (PSM) {
         // S_r is in registers: the next tile's QK^T may overwrite the buffer.
         tc_fence_before();
@@ -349,17 +355,17 @@ __global__ void __launch_bounds__(352, 1) onepass_fwd_kernel(const __grid_consta
         if (lane == 0) mbar_arrive(&s_free[map]);
         __syncwarp();
       }
-      const int nvis = lim - j * BN;
-      if (nvis < BN) {
+      const int nvis = lim - (j * BN + 64 * half);
+      if (nvis < 64) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
           for (int c = 0; c < 32; ++c)
             if (32 * q + c >= nvis) x[q][c] = __float_as_uint(-INFINITY);
       }
-      float mq[4];
+      float mq[2];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         float tm[11];
 #pragma unroll
         for (int c = 0; c < 10; ++c)
@@ -367,7 +373,14 @@ __global__ void __launch_bounds__(352, 1) onepass_fwd_kernel(const __grid_consta
         tm[10] = fmaxf(__uint_as_float(x[q][30]), __uint_as_float(x[q][31]));
         mq[q] = max3(max3(tm[0], tm[1], tm[2]), max3(tm[3], tm[4], tm[5]), max3(max3(tm[6], tm[7], tm[8]), tm[9], tm[10]));
       }
-      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      // Row maximum of the whole tile: exchange with the other half.  The
+      // buffer alternates with the tile, so a half one tile ahead never
+      // overwrites a value the other half has yet to read.
+      float* xm = xmax + ((j & 1) * 2 + map) * 256;
+      const float pm = fmaxf(mq[0], mq[1]);
+      xm[half * 128 + row] = pm;
+      named_bar_sync(2 + map, 256);
+      const float mx = fmaxf(pm, xm[(half ^ 1) * 128 + row]);
       const float m_new = fmaxf(m_used, mx * sc);
       const bool rescale = __any_sync(0xffffffffu, m_new > m_used + C::RESCALE_THRESHOLD);
       float factor = 1.f;
@@ -377,11 +390,11 @@ __global__ void __launch_bounds__(352, 1) onepass_fwd_kernel(const __grid_consta
         m_used = m_new;
       }
       const uint64_t nb2 = f2pack(-m_used, -m_used);
-      uint64_t acc[4] = {0, 0, 0, 0};
+      uint64_t acc[2] = {0, 0};
       // P pairs are packed in place over score registers already consumed:
-      // x[q][0..15] then hold key columns 32 q .. 32 q + 31 as bf16 pairs.
+      // x[q][0..15] then hold key columns 64 half + 32 q .. + 31 as bf16 pairs.
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           float a0, a1;
@@ -391,10 +404,9 @@ __global__ void __launch_bounds__(352, 1) onepass_fwd_kernel(const __grid_consta
           x[q][c >> 1] = pack_bf16x2(p0, p1);
         }
       }
-      float s0, s1, s2, s3;
+      float s0, s1;
       f2unpack(add2(acc[0], acc[1]), s0, s1);
-      f2unpack(add2(acc[2], acc[3]), s2, s3);
-      l += (s0 + s1) + (s2 + s3);
+      l += s0 + s1;
       if constexpr (PSM) {
         // PV_r(j-1) must be complete before P_r is overwritten or O_r rescaled.
         if (j > 0) {
@@ -402,33 +414,35 @@ __global__ void __launch_bounds__(352, 1) onepass_fwd_kernel(const __grid_consta
           __syncwarp();
           tc_fence_after();
         }
-        // Row `row` of P_r: 64-key box q/2, 16-byte chunks 4 (q%2) .. 4 (q%2) + 3.
+        // Row `row` of P_r, keys [64 half, +64) = 64-key box `half`: 16-byte
+        // chunk c holds keys 8c .. 8c + 7 of the box, at position c ^ (row % 8).
+        uint8_t* prow = smem + C::OFF_P + map * C::P_TILE + half * (BM * 128) + row * 128;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint8_t* prow = smem + C::OFF_P + map * C::P_TILE + (q >> 1) * (BM * 128) + row * 128;
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(prow + (((4 * (q & 1) + c) ^ (row & 7)) << 4)) =
-                make_uint4(x[q][4 * c], x[q][4 * c + 1], x[q][4 * c + 2], x[q][4 * c + 3]);
-        }
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
+              make_uint4(x[c >> 2][4 * (c & 3)], x[c >> 2][4 * (c & 3) + 1], x[c >> 2][4 * (c & 3) + 2],
+                         x[c >> 2][4 * (c & 3) + 3]);
         fence_proxy_async_smem();
       } else {
-        // P of key columns 32 q .. 32 q + 31 -> buffer columns 16 q .. 16 q + 15
-        // (this thread's own row; it has read all of its S columns).
+        // P of key columns 32 q' .. 32 q' + 31 (q' = 2 half + q) -> buffer
+        // columns 16 q' .. 16 q' + 15 (this thread's own row; the S columns it
+        // overwrites are its own and already loaded).
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_st16(tS + 16u * q, reinterpret_cast<const uint32_t(&)[16]>(x[q]));
+        for (int q = 0; q < 2; ++q)
+          tmem_st16(tS + 32u * half + 16u * q, reinterpret_cast<const uint32_t(&)[16]>(x[q]));
       }
       if (rescale && j > 0) {
         // PV_r(j-1) is complete: awaited above (PSM), or issued by the same
         // warp before QK_r(j), whose commit of S_r(j) tracks all its MMAs.
+        // This half rescales O_r columns [64 half, +64) of its rows.
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
           uint32_t o[32];
-          tmem_ld32(tOr + 32u * q, o);
+          tmem_ld32(tOr + 64u * half + 32u * q, o);
           tmem_ld_wait(o);
 #pragma unroll
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * factor);
-          tmem_st32(tOr + 32u * q, o);
+          tmem_st32(tOr + 64u * half + 32u * q, o);
         }
       }
       tmem_st_wait();
@@ -438,13 +452,15 @@ __global__ void __launch_bounds__(352, 1) onepass_fwd_kernel(const __grid_consta
       __syncwarp();
     }
 
-    // ---- epilogue: out = O_1 / l_1 - c O_2 / l_2; warpgroup `map` owns channels [64 map, +64)
-    lpart[map * 128 + row] = l;
+    // ---- epilogue: out = O_1 / l_1 - c O_2 / l_2; warpgroup (map, half) owns
+    // channels [32 cb, +32), cb = 2 map + half
+    const int cb = 2 * map + half;
+    lpart[cb * 128 + row] = l;
     mbar_wait(o_full, 0, ab);
     __syncwarp();
     tc_fence_after();
     named_bar_sync(1, 128 * C::NSMWG);
-    const float l1 = lpart[row], l2 = lpart[128 + row];
+    const float l1 = lpart[row] + lpart[128 + row], l2 = lpart[256 + row] + lpart[384 + row];
     float coef;
     if (EPI == kEpiRmsNorm) {
       coef = *p.lambda;
@@ -453,48 +469,45 @@ __global__ void __launch_bounds__(352, 1) onepass_fwd_kernel(const __grid_consta
       coef = 1.f / (1.f + expf(-lg));
     }
     const float a1 = 1.f / l1, a2 = -coef / l2;
-    float y[2][32];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    float y[32];
+    {
       uint32_t o1[32], o2[32];
-      tmem_ld32(tl + C::TM_O1 + 64u * map + 32u * h, o1);
-      tmem_ld32(tl + C::TM_O2 + 64u * map + 32u * h, o2);
+      tmem_ld32(tl + C::TM_O1 + 32u * cb, o1);
+      tmem_ld32(tl + C::TM_O2 + 32u * cb, o2);
       tmem_ld_wait2(o1, o2);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) y[h][c] = fmaf(__uint_as_float(o2[c]), a2, __uint_as_float(o1[c]) * a1);
+      for (int c = 0; c < 32; ++c) y[c] = fmaf(__uint_as_float(o2[c]), a2, __uint_as_float(o1[c]) * a1);
     }
     float rinv = 1.f;
     if (EPI == kEpiRmsNorm) {
       float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        ss0 = fmaf(y[0][c], y[0][c], ss0);
-        ss1 = fmaf(y[1][c], y[1][c], ss1);
+      for (int c = 0; c < 32; c += 2) {
+        ss0 = fmaf(y[c], y[c], ss0);
+        ss1 = fmaf(y[c + 1], y[c + 1], ss1);
       }
-      sspart[map * 128 + row] = ss0 + ss1;
+      sspart[cb * 128 + row] = ss0 + ss1;
       __syncwarp();
       named_bar_sync(1, 128 * C::NSMWG);
-      rinv = p.norm_mult * rsqrtf((sspart[row] + sspart[128 + row]) * (1.f / DV) + p.eps);
+      const float tot = (sspart[row] + sspart[128 + row]) + (sspart[256 + row] + sspart[384 + row]);
+      rinv = p.norm_mult * rsqrtf(tot * (1.f / DV) + p.eps);
     }
     if (t < p.n) {
       __nv_bfloat16* orow =
-          p.out + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * DV + 64 * map;
+          p.out + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * DV + 32 * cb;
+      uint32_t wv[16];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t wv[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float y0 = y[h][c] * rinv, y1 = y[h][c + 1] * rinv;
-          if (EPI == kEpiRmsNorm && p.gamma != nullptr) {
-            y0 *= __ldg(p.gamma + 64 * map + 32 * h + c);
-            y1 *= __ldg(p.gamma + 64 * map + 32 * h + c + 1);
-          }
-          wv[c >> 1] = pack_bf16x2(y0, y1);
+      for (int c = 0; c < 32; c += 2) {
+        float y0 = y[c] * rinv, y1 = y[c + 1] * rinv;
+        if (EPI == kEpiRmsNorm && p.gamma != nullptr) {
+          y0 *= __ldg(p.gamma + 32 * cb + c);
+          y1 *= __ldg(p.gamma + 32 * cb + c + 1);
         }
-        uint4* dst = reinterpret_cast<uint4*>(orow + 32 * h);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+        wv[c >> 1] = pack_bf16x2(y0, y1);
       }
+      uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) dst[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
     }
   }
 
