@@ -339,9 +339,10 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
     const uint32_t tOr = tl + (map ? C::TM_O2 : C::TM_O1);
     const uint64_t sc2 = f2pack(sc, sc);
     float m_used = -INFINITY, l = 0.f;
+    uint32_t ready = 0;  // (PSM) early test of this tile's barrier, made during the previous tile
 
     for (int j = 0; j < T; ++j) {
-      mbar_wait(&s_full[map], static_cast<uint32_t>(j) & 1u, ab);
+      if (!ready) mbar_wait(&s_full[map], static_cast<uint32_t>(j) & 1u, ab);
       __syncwarp();
       tc_fence_after();
       uint32_t x[2][32];
@@ -408,6 +409,9 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
       f2unpack(add2(acc[0], acc[1]), s0, s1);
       l += s0 + s1;
       if constexpr (PSM) {
+        // QK_r(j+1) was issued once S_r(j) was loaded: test its barrier now,
+        // off the critical path (phase j has been consumed: the test is exact).
+        ready = (j + 1 < T) ? mbar_test(&s_full[map], static_cast<uint32_t>(j + 1) & 1u) : 0u;
         // PV_r(j-1) must be complete before P_r is overwritten or O_r rescaled.
         if (j > 0) {
           mbar_wait(&pv_done[map], static_cast<uint32_t>(j - 1) & 1u, ab);

@@ -447,16 +447,20 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
     const int map = wg >> 1;
     const int half = wg & 1;
     float m = -INFINITY, l = 0.f;
+    uint32_t ready = 0;  // early test of this tile's barrier, made during the previous tile
     for (int j = 0; j < T; ++j) {
       const int k = 2 * j + map;  // S index: buffer k % 4, its (k / 4)-th write
       const int bb = k & 3;
-      mbar_wait(&s1_full[bb], static_cast<uint32_t>(k >> 2) & 1u, ab);
+      if (!ready) mbar_wait(&s1_full[bb], static_cast<uint32_t>(k >> 2) & 1u, ab);
       __syncwarp();
       tc_fence_after();
       uint32_t r0[32], r1[32];
       const uint32_t tbuf = tl + 128u * bb + 64u * half;
       tmem_ld32(tbuf, r0);
       tmem_ld32(tbuf + 32, r1);
+      // The MMA warps run ahead: test the next tile's buffer now (its previous
+      // phase, tile j - 1, has been consumed, so the test is exact).
+      ready = (j + 1 < T) ? mbar_test(&s1_full[(k + 2) & 3], static_cast<uint32_t>((k + 2) >> 2) & 1u) : 0u;
       tmem_ld_wait2(r0, r1);
       tc_fence_before();
       __syncwarp();
