@@ -63,6 +63,24 @@ diffattn_status status_word(int** out) {
   return DIFFATTN_OK;
 }
 
+// Number of SMs of the current device (cached per device); 0 if unknown.
+int sm_count() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int v = cache[dev].load();
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1) return 0;
+  cache[dev].store(v);
+  return v;
+}
+
+// Grid of a persistent kernel: one CTA per SM, never more CTAs than items.
+long long persistent_grid(long long items) {
+  const int sms = sm_count();
+  return (sms > 0 && items > sms) ? sms : items;
+}
+
 // ---------------------------------------------------------------- TMA maps
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -214,7 +232,9 @@ diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d, 
   if (grid > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "diffattn_forward: too many tiles");
   // d = 64 (value width 128): one sweep with two online-softmax states fits
   // TMEM; d = 128 (value width 256) does not, and sweeps the keys twice.
-  cudaError_t e = (d == 64) ? da::launch_onepass_v1_d64(p, static_cast<int>(grid), s)
+  // d = 64: many short items, so one persistent CTA per SM overlaps each
+  // item's start with the previous one's end; d = 128: one CTA per item.
+  cudaError_t e = (d == 64) ? da::launch_onepass_v1_d64(p, static_cast<int>(persistent_grid(grid)), s)
                             : da::launch_twopass_v1_d128(p, static_cast<int>(grid), s);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward (bf16) launch");
   g_launches.fetch_add(1);
@@ -299,6 +319,8 @@ diffattn_status diffattn_v2_forward(diffattn_dtype dt, int B, int Hq, int Hkv, i
   p.status = status;
   const long long grid = static_cast<long long>(p.num_q_tiles) * B * G;
   if (grid > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_forward: too many tiles");
+  // V2 items are long (up to n / 128 key tiles): one CTA per item, so the
+  // hardware's dynamic CTA scheduling balances them (measured faster here).
   cudaError_t e = da::launch_onepass_v2_d128(p, static_cast<int>(grid), s);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_forward (bf16) launch");
   g_launches.fetch_add(1);

@@ -1,6 +1,6 @@
 #include "onepass_inst.cuh"
 namespace da {
 cudaError_t launch_onepass_v1_d64(const TwoPassParams& p, int grid, cudaStream_t s) {
-  return launch_onepass<64, false, kEpiRmsNorm, 7, true>(p, grid, s);
+  return launch_onepass<64, false, kEpiRmsNorm, 7, true, true>(p, grid, s);
 }
 }  // namespace da

@@ -1,6 +1,6 @@
 #include "onepass_inst.cuh"
 namespace da {
 cudaError_t launch_onepass_v2_d128(const TwoPassParams& p, int grid, cudaStream_t s) {
-  return launch_onepass<128, true, kEpiV2, 4, false>(p, grid, s);
+  return launch_onepass<128, true, kEpiV2, 4, false, false>(p, grid, s);
 }
 }  // namespace da

@@ -31,6 +31,15 @@
 // bf16 and far from fp32 overflow); when any row of a warp must move, the warp
 // rescales its rows of O_r and l_r.
 //
+// Persistent (template flag PERSIST; else one CTA per item): one CTA per SM
+// walks a list of work items (batch, unit, query tile), heaviest first, dealt out in "snake" order (round k takes items
+// k G .. k G + G - 1, reversed on odd rounds), which balances the causal
+// triangle as well as a greedy scheduler without any shared counter.  The
+// ring, the per-tile barriers and their phases run on across items, so the
+// next item's Q and K tiles and its first QK^T overlap the epilogue of the
+// current one: q_free (both MMA warps' last QK^T of an item done) guards the
+// Q buffer, o_free (every softmax warp has read O) guards the accumulators.
+//
 // Roles (608 threads, one CTA per SM):
 //   warp 0      TMA producer (Q once; then K_1, K_2 / K and V tiles into a ring
 //               of NSLOT equal slots, in the order the MMA warps walk them).
@@ -59,7 +68,7 @@
 
 namespace da {
 
-template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM>
+template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST>
 struct OnePassCfg {
   static constexpr int BM = 128;
   static constexpr int BN = 128;
@@ -81,26 +90,29 @@ struct OnePassCfg {
   static constexpr int OFF_P = 2 * Q_TILE;
   static constexpr int OFF_RING = OFF_P + (PSM ? 2 * P_TILE : 0);
   static constexpr int OFF_BARS = OFF_RING + NSLOT * SLOT;
-  static constexpr int NBARS = 2 + 2 * NSLOT + 8;
+  static constexpr int NBARS = 6 + 2 * NSLOT + 8;
   static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
-  static constexpr int OFF_LP = (OFF_MISC + 16 + 15) / 16 * 16;  // float [4][128] partial row sums
-  static constexpr int OFF_SS = OFF_LP + 4 * 128 * 4;             // float [4][128] partial sums of squares
-  static constexpr int OFF_XM = OFF_SS + 4 * 128 * 4;             // float [2 tiles][2 maps][2 halves][128]
+  // Epilogue scratch alternates with the item parity: a map that runs ahead
+  // into the next item's epilogue never overwrites values still being read.
+  static constexpr int OFF_LP = (OFF_MISC + 16 + 15) / 16 * 16;  // float [2 items][4][128] partial row sums
+  static constexpr int OFF_SS = OFF_LP + 8 * 128 * 4;             // float [2 items][4][128] partial sums of squares
+  static constexpr int OFF_XM = OFF_SS + 8 * 128 * 4;             // float [2 tiles][2 maps][2 halves][128]
   static constexpr int SMEM_BYTES = OFF_XM + 8 * 128 * 4 + 1024;  // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TM_O1 = 0, TM_O2 = 128, TM_A = 256, TM_B = 384;
   static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(BM, DV, false, true);
   static constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units
+  static constexpr int MAX_ITEMS = PERSIST ? 0x7fffffff : 1;  // work items per CTA
   static_assert(D == 64 || D == 128, "query/key width");
   static_assert(V_TILE % SLOT == 0 && (VF == 1 || VF == 2), "value tile split");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(NSLOT >= 4, "ring depth");
 };
 
-template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM>
+template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST>
 __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
-  using C = OnePassCfg<D, SHARED_K, EPI, NSLOT, PSM>;
+  using C = OnePassCfg<D, SHARED_K, EPI, NSLOT, PSM, PERSIST>;
   constexpr int BM = C::BM, BN = C::BN, DV = C::DV;
 
   extern __shared__ uint8_t smem_raw[];
@@ -110,9 +122,12 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
   const int lane = threadIdx.x & 31;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
-  uint64_t* q_full = bars + 0;
-  uint64_t* o_full = bars + 1;
-  uint64_t* full = bars + 2;
+  uint64_t* q_full = bars + 0;       // Q of the item landed
+  uint64_t* o_full = bars + 1;       // every PV of the item completed (both MMA warps)
+  uint64_t* q_free = bars + 2;       // the item's last QK^T of both maps completed: Q may be replaced
+  uint64_t* o_free = bars + 3;       // every softmax warp has read the item's O
+  uint64_t* mma_done = bars + 4;     // [2] every MMA of an MMA warp completed (abort drain)
+  uint64_t* full = bars + 6;
   uint64_t* empty = full + NSLOT;
   uint64_t* s_full = empty + NSLOT;  // [2]: S_r of the current tile in its buffer
   uint64_t* p_ready = s_full + 2;    // [2]: P_r of the current tile written
@@ -124,34 +139,27 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
   float* sspart = reinterpret_cast<float*>(smem + C::OFF_SS);
   float* xmax = reinterpret_cast<float*>(smem + C::OFF_XM);
 
-  // ---- which tile this CTA owns
-  const int units = p.B * p.units_per_batch;
-  int unit, qt;
-  if (p.order == 0) {
-    unit = blockIdx.x / p.num_q_tiles;
-    qt = p.num_q_tiles - 1 - static_cast<int>(blockIdx.x % p.num_q_tiles);
-  } else {
-    qt = p.num_q_tiles - 1 - static_cast<int>(blockIdx.x / units);
-    unit = blockIdx.x % units;
-  }
-  const int b = unit / p.units_per_batch;
-  const int u = unit % p.units_per_batch;
-  int hq1, hq2, hk;
-  if (EPI == kEpiRmsNorm) {
-    hq1 = hq2 = hk = u;
-  } else {
-    hq1 = 2 * u;
-    hq2 = 2 * u + 1;
-    hk = hq1 / p.group;
-  }
-  const int q0 = qt * BM;
-  const int kv_end = p.causal ? min(p.n, q0 + BM) : p.n;
-  const int T = (kv_end + BN - 1) / BN;
+  // ---- this CTA's work items: round k takes item k G + blockIdx.x, or
+  // k G + G - 1 - blockIdx.x on odd rounds; the list ends at the first one
+  // past the last item (later rounds start further on).
+  const int nitems = p.num_q_tiles * p.B * p.units_per_batch;
+  const int G = static_cast<int>(gridDim.x);
+  auto item_of = [&](int k) -> int {
+    return k * G + ((k & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x));
+  };
+  auto tiles_of = [&](const TileCoord& c) -> int {
+    const int kv_end = p.causal ? min(p.n, c.q0 + BM) : p.n;
+    return (kv_end + BN - 1) / BN;
+  };
 
   // ---- set-up
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(o_full, 2);  // both MMA warps
+    mbar_init(q_free, 2);  // both MMA warps
+    mbar_init(o_free, 4 * C::NSMWG);
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 2);  // both MMA warps release every fill
@@ -183,44 +191,58 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
       tma_prefetch_desc(&p.tm_k1);
       if (!SHARED_K) tma_prefetch_desc(&p.tm_k2);
       tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(q_full, 2 * C::Q_TILE);
-      for (int bx = 0; bx < C::QB; ++bx) {
-        tma_load_4d(smem + C::OFF_Q1 + bx * BM * 128, &p.tm_q1, q_full, bx * 64, hq1, q0, b);
-        tma_load_4d(smem + C::OFF_Q2 + bx * BM * 128, &p.tm_q2, q_full, bx * 64, hq2, q0, b);
-      }
-      int fill = 0;
+      int fill = 0, qloads = 0;
       bool ok = true;
-      auto load = [&](const CUtensorMap* map, int key0, int rows, int nbox) {
-        if (!ok) return;
-        const int s = fill % NSLOT;
-        const uint32_t use = static_cast<uint32_t>(fill / NSLOT);
-        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, ab)) {
+      for (int k = 0; ok && k < C::MAX_ITEMS; ++k) {
+        const int idx = item_of(k);
+        if (idx >= nitems) break;
+        const TileCoord c = tile_coord<EPI>(p, idx);
+        const int T = tiles_of(c);
+        // Q of the previous item is read by its QK^T until q_free.
+        if (PERSIST && k > 0 && !mbar_wait(q_free, static_cast<uint32_t>(k - 1) & 1u, ab)) {
           ok = false;
-          return;
+          break;
         }
-        uint8_t* dst = smem + C::OFF_RING + s * C::SLOT;
-        mbar_arrive_expect_tx(&full[s], C::SLOT);
-        for (int bx = 0; bx < nbox; ++bx) tma_load_4d(dst + bx * rows * 128, map, &full[s], bx * 64, hk, key0, b);
-        ++fill;
-      };
-      // The fill order is the order in which both MMA warps walk the ring.
-      load(&p.tm_k1, 0, BN, C::QB);
-      if (!SHARED_K) load(&p.tm_k2, 0, BN, C::QB);
-      // PSM: the next tile's K before this tile's V (QK(j+1) is issued
-      // before PV(j)); otherwise after it.
-      for (int j = 0; j < T; ++j) {
-        if (PSM && j + 1 < T) {
-          load(&p.tm_k1, (j + 1) * BN, BN, C::QB);
-          if (!SHARED_K) load(&p.tm_k2, (j + 1) * BN, BN, C::QB);
+        mbar_arrive_expect_tx(q_full, 2 * C::Q_TILE);
+        for (int bx = 0; bx < C::QB; ++bx) {
+          tma_load_4d(smem + C::OFF_Q1 + bx * BM * 128, &p.tm_q1, q_full, bx * 64, c.hq1, c.q0, c.b);
+          tma_load_4d(smem + C::OFF_Q2 + bx * BM * 128, &p.tm_q2, q_full, bx * 64, c.hq2, c.q0, c.b);
         }
-        for (int part = 0; part < C::VF; ++part) load(&p.tm_v, j * BN + part * C::VKEYS, C::VKEYS, C::VB);
-        if (!PSM && j + 1 < T) {
-          load(&p.tm_k1, (j + 1) * BN, BN, C::QB);
-          if (!SHARED_K) load(&p.tm_k2, (j + 1) * BN, BN, C::QB);
+        ++qloads;
+        auto load = [&](const CUtensorMap* map, int key0, int rows, int nbox) {
+          if (!ok) return;
+          const int s = fill % NSLOT;
+          const uint32_t use = static_cast<uint32_t>(fill / NSLOT);
+          if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, ab)) {
+            ok = false;
+            return;
+          }
+          uint8_t* dst = smem + C::OFF_RING + s * C::SLOT;
+          mbar_arrive_expect_tx(&full[s], C::SLOT);
+          for (int bx = 0; bx < nbox; ++bx)
+            tma_load_4d(dst + bx * rows * 128, map, &full[s], bx * 64, c.hk, key0, c.b);
+          ++fill;
+        };
+        // The fill order is the order in which both MMA warps walk the ring.
+        load(&p.tm_k1, 0, BN, C::QB);
+        if (!SHARED_K) load(&p.tm_k2, 0, BN, C::QB);
+        // PSM: the next tile's K before this tile's V (QK(j+1) is issued
+        // before PV(j)); otherwise after it.
+        for (int j = 0; j < T; ++j) {
+          if (PSM && j + 1 < T) {
+            load(&p.tm_k1, (j + 1) * BN, BN, C::QB);
+            if (!SHARED_K) load(&p.tm_k2, (j + 1) * BN, BN, C::QB);
+          }
+          for (int part = 0; part < C::VF; ++part) load(&p.tm_v, j * BN + part * C::VKEYS, C::VKEYS, C::VB);
+          if (!PSM && j + 1 < T) {
+            load(&p.tm_k1, (j + 1) * BN, BN, C::QB);
+            if (!SHARED_K) load(&p.tm_k2, (j + 1) * BN, BN, C::QB);
+          }
         }
       }
       if (*ab.flag) {
-        mbar_wait_drain(q_full, 0, kWaitBudgetCycles);
+        // Aborted: let the copies already issued land before the CTA exits.
+        if (qloads > 0) mbar_wait_drain(q_full, static_cast<uint32_t>(qloads - 1) & 1u, kWaitBudgetCycles);
         for (int f = (fill > NSLOT ? fill - NSLOT : 0); f < fill; ++f)
           mbar_wait_drain(&full[f % NSLOT], static_cast<uint32_t>(f / NSLOT) & 1u, kWaitBudgetCycles);
       }
@@ -233,6 +255,7 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
     const uint64_t dQ = sdesc_sw128(smem_u32(smem + (r == 0 ? C::OFF_Q1 : C::OFF_Q2)), 16, 1024);
     const uint64_t dRingK = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
     const uint64_t dRingV = sdesc_sw128(smem_u32(smem + C::OFF_RING), C::VKEYS * 128, 1024);
+    const uint64_t dP = sdesc_sw128(smem_u32(smem + C::OFF_P + r * C::P_TILE), 16, 1024);
     const uint32_t tS = tmem + (r == 0 ? C::TM_A : C::TM_B);
     const uint32_t tO = tmem + (r == 0 ? C::TM_O1 : C::TM_O2);
     // Every wait returns the same verdict in all lanes and leaves the warp converged.
@@ -267,62 +290,84 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
                      dk + static_cast<uint64_t>((((k >> 2) * (BN * 128)) + (k & 3) * 32) >> 4), C::IDESC_QK,
                      k > 0 ? 1u : 0u);
     };
-    // K fills of key tile jj: K (shared) or K_1 then K_2.  With P in shared
-    // memory QK_r(jj) only waits until the softmax has loaded S_r(jj-1).
-    auto k_tile = [&](int jj) -> bool {
+    // K fills of the tile with global index g (tiles counted across items):
+    // K (shared) or K_1 then K_2.  With P in shared memory QK_r(g) only waits
+    // until the softmax has loaded S_r(g-1).  After an item's last QK^T both
+    // warps release the Q buffer.
+    auto k_tile = [&](uint32_t g, bool last_of_item) -> bool {
       if (!SHARED_K && r == 1 && !skip_next()) return false;
       int s;
       if (!acquire_next(s)) return false;
-      if (PSM && jj > 0 && !waitp(&s_free[r], static_cast<uint32_t>(jj - 1) & 1u)) return false;
+      if (PSM && g > 0 && !waitp(&s_free[r], (g - 1) & 1u)) return false;
       qk(s);
       tc_commit_elect(&s_full[r]);
       tc_commit_elect(&empty[s]);
+      if (PERSIST && last_of_item) tc_commit_elect(q_free);
       return SHARED_K || r == 1 || skip_next();
     };
-    const uint64_t dP = sdesc_sw128(smem_u32(smem + C::OFF_P + r * C::P_TILE), 16, 1024);
-    bool ok = waitp(q_full, 0) && k_tile(0);
-    for (int j = 0; ok && j < T; ++j) {
-      if (PSM && j + 1 < T && !k_tile(j + 1)) {
+    bool ok = true;
+    uint32_t gt = 0;  // tiles of earlier items
+    for (int k = 0; ok && k < C::MAX_ITEMS; ++k) {
+      const int idx = item_of(k);
+      if (idx >= nitems) break;
+      const int T = tiles_of(tile_coord<EPI>(p, idx));
+      if (!waitp(q_full, static_cast<uint32_t>(k) & 1u) || !k_tile(gt, T == 1)) {
         ok = false;
         break;
       }
-      int sv[C::VF];
-      bool got = true;
-#pragma unroll
-      for (int part = 0; part < C::VF; ++part) got = acquire_next(sv[part]) && got;
-      if (!got || !waitp(&p_ready[r], static_cast<uint32_t>(j) & 1u)) {
-        ok = false;
-        break;
-      }
-      // PV_r(j): P_r from shared memory (k-step kg: keys 16 kg .. 16 kg + 15 =
-      // 64-key box kg / 4, 32-byte step kg % 4), or bf16 pairs in TMEM columns
-      // 8 kg .. 8 kg + 7 of the S_r buffer.
-#pragma unroll
-      for (int part = 0; part < C::VF; ++part) {
-        const uint64_t dv = dRingV + static_cast<uint64_t>((sv[part] * C::SLOT) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < C::VKEYS / 16; ++kk) {
-          const int kg = part * (C::VKEYS / 16) + kk;
-          const uint64_t dvk = dv + static_cast<uint64_t>(kk * (2048 >> 4));
-          const uint32_t acc = (j > 0 || kg > 0) ? 1u : 0u;
-          if (PSM)
-            mma_ss_elect(tO, dP + static_cast<uint64_t>((((kg >> 2) * (BM * 128)) + (kg & 3) * 32) >> 4), dvk,
-                         C::IDESC_PV, acc);
-          else
-            mma_ts_elect(tO, tS + 8u * kg, dvk, C::IDESC_PV, acc);
+      for (int j = 0; ok && j < T; ++j) {
+        const uint32_t g = gt + static_cast<uint32_t>(j);
+        if (PSM && j + 1 < T && !k_tile(g + 1, j + 2 == T)) {
+          ok = false;
+          break;
         }
-        // Each V part is released as soon as its own MMAs are done.
-        if (part + 1 < C::VF) tc_commit_elect(&empty[sv[part]]);
+        int sv[C::VF];
+        bool got = true;
+#pragma unroll
+        for (int part = 0; part < C::VF; ++part) got = acquire_next(sv[part]) && got;
+        if (!got || !waitp(&p_ready[r], g & 1u)) {
+          ok = false;
+          break;
+        }
+        // The first PV of an item overwrites O_r: the previous item's
+        // epilogue must have read it.
+        if (PERSIST && j == 0 && k > 0 && !waitp(o_free, static_cast<uint32_t>(k - 1) & 1u)) {
+          ok = false;
+          break;
+        }
+        // PV_r(j): P_r from shared memory (k-step kg: keys 16 kg .. 16 kg + 15 =
+        // 64-key box kg / 4, 32-byte step kg % 4), or bf16 pairs in TMEM columns
+        // 8 kg .. 8 kg + 7 of the S_r buffer.
+#pragma unroll
+        for (int part = 0; part < C::VF; ++part) {
+          const uint64_t dv = dRingV + static_cast<uint64_t>((sv[part] * C::SLOT) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < C::VKEYS / 16; ++kk) {
+            const int kg = part * (C::VKEYS / 16) + kk;
+            const uint64_t dvk = dv + static_cast<uint64_t>(kk * (2048 >> 4));
+            const uint32_t acc = (j > 0 || kg > 0) ? 1u : 0u;
+            if (PSM)
+              mma_ss_elect(tO, dP + static_cast<uint64_t>((((kg >> 2) * (BM * 128)) + (kg & 3) * 32) >> 4), dvk,
+                           C::IDESC_PV, acc);
+            else
+              mma_ts_elect(tO, tS + 8u * kg, dvk, C::IDESC_PV, acc);
+          }
+          // Each V part is released as soon as its own MMAs are done.
+          if (part + 1 < C::VF) tc_commit_elect(&empty[sv[part]]);
+        }
+        if (PSM) tc_commit_elect(&pv_done[r]);
+        tc_commit_elect(&empty[sv[C::VF - 1]]);
+        if (!PSM && j + 1 < T && !k_tile(g + 1, j + 2 == T)) {
+          ok = false;
+          break;
+        }
       }
-      if (PSM) tc_commit_elect(&pv_done[r]);
-      tc_commit_elect(&empty[sv[C::VF - 1]]);
-      if (!PSM && j + 1 < T && !k_tile(j + 1)) {
-        ok = false;
-        break;
-      }
+      if (!ok) break;
+      tc_commit_elect(o_full);
+      gt += static_cast<uint32_t>(T);
     }
-    tc_commit_elect(o_full);
-    if (*ab.flag) mbar_wait_drain(o_full, 0, kWaitBudgetCycles);
+    tc_commit_elect(&mma_done[r]);
+    if (*ab.flag) mbar_wait_drain(&mma_done[r], 0, kWaitBudgetCycles);
     __syncwarp();
   } else {
     // =============================================================== softmax + epilogue
@@ -331,187 +376,209 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
     const int half = (sw >> 2) & 1;   // key columns [64 half, +64) of each tile
     const int wq = warp & 3;          // TMEM lane quarter
     const int row = wq * 32 + lane;
-    const int t = q0 + row;
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float sc = p.scale_log2;
-    const int lim = p.causal ? min(t + 1, p.n) : p.n;
     const uint32_t tS = tl + (map ? C::TM_B : C::TM_A);
     const uint32_t tOr = tl + (map ? C::TM_O2 : C::TM_O1);
     const uint64_t sc2 = f2pack(sc, sc);
-    float m_used = -INFINITY, l = 0.f;
-    uint32_t ready = 0;  // (PSM) early test of this tile's barrier, made during the previous tile
+    const int cb = 2 * map + half;  // epilogue: output channels [32 cb, +32)
+    uint32_t gt = 0;                // tiles of earlier items
 
-    for (int j = 0; j < T; ++j) {
-      if (!ready) mbar_wait(&s_full[map], static_cast<uint32_t>(j) & 1u, ab);
-      __syncwarp();
-      tc_fence_after();
-      uint32_t x[2][32];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) tmem_ld32(tS + 64u * half + 32u * q, x[q]);
-      tmem_ld_wait2(x[0], x[1]);
-      if constexpr (PSM) {
-        // S_r is in registers: the next tile's QK^T may overwrite the buffer.
-        tc_fence_before();
+    for (int k = 0; k < C::MAX_ITEMS; ++k) {
+      const int idx = item_of(k);
+      if (idx >= nitems) break;
+      const TileCoord c = tile_coord<EPI>(p, idx);
+      const int T = tiles_of(c);
+      const int t = c.q0 + row;
+      const int lim = p.causal ? min(t + 1, p.n) : p.n;
+      float m_used = -INFINITY, l = 0.f;
+      uint32_t ready = 0;  // (PSM) early test of this tile's barrier, made during the previous tile
+
+      for (int j = 0; j < T; ++j) {
+        const uint32_t g = gt + static_cast<uint32_t>(j);
+        if (!ready) mbar_wait(&s_full[map], g & 1u, ab);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[map]);
-        __syncwarp();
-      }
-      const int nvis = lim - (j * BN + 64 * half);
-      if (nvis < 64) {
+        tc_fence_after();
+        uint32_t x[2][32];
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (32 * q + c >= nvis) x[q][c] = __float_as_uint(-INFINITY);
-      }
-      float mq[2];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        float tm[11];
-#pragma unroll
-        for (int c = 0; c < 10; ++c)
-          tm[c] = max3(__uint_as_float(x[q][3 * c]), __uint_as_float(x[q][3 * c + 1]), __uint_as_float(x[q][3 * c + 2]));
-        tm[10] = fmaxf(__uint_as_float(x[q][30]), __uint_as_float(x[q][31]));
-        mq[q] = max3(max3(tm[0], tm[1], tm[2]), max3(tm[3], tm[4], tm[5]), max3(max3(tm[6], tm[7], tm[8]), tm[9], tm[10]));
-      }
-      // Row maximum of the whole tile: exchange with the other half.  The
-      // buffer alternates with the tile, so a half one tile ahead never
-      // overwrites a value the other half has yet to read.
-      float* xm = xmax + ((j & 1) * 2 + map) * 256;
-      const float pm = fmaxf(mq[0], mq[1]);
-      xm[half * 128 + row] = pm;
-      named_bar_sync(2 + map, 256);
-      const float mx = fmaxf(pm, xm[(half ^ 1) * 128 + row]);
-      const float m_new = fmaxf(m_used, mx * sc);
-      const bool rescale = __any_sync(0xffffffffu, m_new > m_used + C::RESCALE_THRESHOLD);
-      float factor = 1.f;
-      if (rescale) {
-        factor = ex2(m_used - m_new);  // 0 on the first tile
-        l *= factor;
-        m_used = m_new;
-      }
-      const uint64_t nb2 = f2pack(-m_used, -m_used);
-      uint64_t acc[2] = {0, 0};
-      // P pairs are packed in place over score registers already consumed:
-      // x[q][0..15] then hold key columns 64 half + 32 q .. + 31 as bf16 pairs.
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float a0, a1;
-          f2unpack(fma2(f2pack(__uint_as_float(x[q][c]), __uint_as_float(x[q][c + 1])), sc2, nb2), a0, a1);
-          const float p0 = ex2(a0), p1 = ex2(a1);
-          acc[q] = add2(acc[q], f2pack(p0, p1));
-          x[q][c >> 1] = pack_bf16x2(p0, p1);
-        }
-      }
-      float s0, s1;
-      f2unpack(add2(acc[0], acc[1]), s0, s1);
-      l += s0 + s1;
-      if constexpr (PSM) {
-        // QK_r(j+1) was issued once S_r(j) was loaded: test its barrier now,
-        // off the critical path (phase j has been consumed: the test is exact).
-        ready = (j + 1 < T) ? mbar_test(&s_full[map], static_cast<uint32_t>(j + 1) & 1u) : 0u;
-        // PV_r(j-1) must be complete before P_r is overwritten or O_r rescaled.
-        if (j > 0) {
-          mbar_wait(&pv_done[map], static_cast<uint32_t>(j - 1) & 1u, ab);
+        for (int q = 0; q < 2; ++q) tmem_ld32(tS + 64u * half + 32u * q, x[q]);
+        tmem_ld_wait2(x[0], x[1]);
+        if constexpr (PSM) {
+          // S_r is in registers: the next tile's QK^T may overwrite the buffer.
+          tc_fence_before();
           __syncwarp();
-          tc_fence_after();
+          if (lane == 0) mbar_arrive(&s_free[map]);
+          __syncwarp();
         }
-        // Row `row` of P_r, keys [64 half, +64) = 64-key box `half`: 16-byte
-        // chunk c holds keys 8c .. 8c + 7 of the box, at position c ^ (row % 8).
-        uint8_t* prow = smem + C::OFF_P + map * C::P_TILE + half * (BM * 128) + row * 128;
+        const int nvis = lim - (j * BN + 64 * half);
+        if (nvis < 64) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
-              make_uint4(x[c >> 2][4 * (c & 3)], x[c >> 2][4 * (c & 3) + 1], x[c >> 2][4 * (c & 3) + 2],
-                         x[c >> 2][4 * (c & 3) + 3]);
-        fence_proxy_async_smem();
-      } else {
-        // P of key columns 32 q' .. 32 q' + 31 (q' = 2 half + q) -> buffer
-        // columns 16 q' .. 16 q' + 15 (this thread's own row; the S columns it
-        // overwrites are its own and already loaded).
+          for (int q = 0; q < 2; ++q)
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
-          tmem_st16(tS + 32u * half + 16u * q, reinterpret_cast<const uint32_t(&)[16]>(x[q]));
-      }
-      if (rescale && j > 0) {
-        // PV_r(j-1) is complete: awaited above (PSM), or issued by the same
-        // warp before QK_r(j), whose commit of S_r(j) tracks all its MMAs.
-        // This half rescales O_r columns [64 half, +64) of its rows.
+            for (int cc = 0; cc < 32; ++cc)
+              if (32 * q + cc >= nvis) x[q][cc] = __float_as_uint(-INFINITY);
+        }
+        float mq[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          uint32_t o[32];
-          tmem_ld32(tOr + 64u * half + 32u * q, o);
-          tmem_ld_wait(o);
+          float tm[11];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * factor);
-          tmem_st32(tOr + 64u * half + 32u * q, o);
+          for (int cc = 0; cc < 10; ++cc)
+            tm[cc] = max3(__uint_as_float(x[q][3 * cc]), __uint_as_float(x[q][3 * cc + 1]),
+                          __uint_as_float(x[q][3 * cc + 2]));
+          tm[10] = fmaxf(__uint_as_float(x[q][30]), __uint_as_float(x[q][31]));
+          mq[q] = max3(max3(tm[0], tm[1], tm[2]), max3(tm[3], tm[4], tm[5]), max3(max3(tm[6], tm[7], tm[8]), tm[9], tm[10]));
         }
+        // Row maximum of the whole tile: exchange with the other half.  The
+        // buffer alternates with the (global) tile, so a half one tile ahead
+        // never overwrites a value the other half has yet to read.
+        float* xm = xmax + ((g & 1u) * 2 + map) * 256;
+        const float pm = fmaxf(mq[0], mq[1]);
+        xm[half * 128 + row] = pm;
+        named_bar_sync(2 + map, 256);
+        const float mx = fmaxf(pm, xm[(half ^ 1) * 128 + row]);
+        const float m_new = fmaxf(m_used, mx * sc);
+        const bool rescale = __any_sync(0xffffffffu, m_new > m_used + C::RESCALE_THRESHOLD);
+        float factor = 1.f;
+        if (rescale) {
+          factor = ex2(m_used - m_new);  // 0 on the first tile of an item
+          l *= factor;
+          m_used = m_new;
+        }
+        const uint64_t nb2 = f2pack(-m_used, -m_used);
+        uint64_t acc[2] = {0, 0};
+        // P pairs are packed in place over score registers already consumed:
+        // x[q][0..15] then hold key columns 64 half + 32 q .. + 31 as bf16 pairs.
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+#pragma unroll
+          for (int cc = 0; cc < 32; cc += 2) {
+            float a0, a1;
+            f2unpack(fma2(f2pack(__uint_as_float(x[q][cc]), __uint_as_float(x[q][cc + 1])), sc2, nb2), a0, a1);
+            const float p0 = ex2(a0), p1 = ex2(a1);
+            acc[q] = add2(acc[q], f2pack(p0, p1));
+            x[q][cc >> 1] = pack_bf16x2(p0, p1);
+          }
+        }
+        float s0, s1;
+        f2unpack(add2(acc[0], acc[1]), s0, s1);
+        l += s0 + s1;
+        if constexpr (PSM) {
+          // QK_r(g+1) was issued once S_r(g) was loaded: test its barrier now,
+          // off the critical path (phase g has been consumed: the test is exact).
+          ready = (j + 1 < T) ? mbar_test(&s_full[map], (g + 1) & 1u) : 0u;
+          // PV_r(g-1) must be complete before P_r is overwritten or O_r rescaled.
+          if (g > 0) {
+            mbar_wait(&pv_done[map], (g - 1) & 1u, ab);
+            __syncwarp();
+            tc_fence_after();
+          }
+          // Row `row` of P_r, keys [64 half, +64) = 64-key box `half`: 16-byte
+          // chunk cc holds keys 8cc .. 8cc + 7 of the box, at position cc ^ (row % 8).
+          uint8_t* prow = smem + C::OFF_P + map * C::P_TILE + half * (BM * 128) + row * 128;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc)
+            *reinterpret_cast<uint4*>(prow + ((cc ^ (row & 7)) << 4)) =
+                make_uint4(x[cc >> 2][4 * (cc & 3)], x[cc >> 2][4 * (cc & 3) + 1], x[cc >> 2][4 * (cc & 3) + 2],
+                           x[cc >> 2][4 * (cc & 3) + 3]);
+          fence_proxy_async_smem();
+        } else {
+          // P of key columns 32 q' .. 32 q' + 31 (q' = 2 half + q) -> buffer
+          // columns 16 q' .. 16 q' + 15 (this thread's own row; the S columns it
+          // overwrites are its own and already loaded).
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            tmem_st16(tS + 32u * half + 16u * q, reinterpret_cast<const uint32_t(&)[16]>(x[q]));
+        }
+        if (rescale && j > 0) {
+          // PV_r(j-1) is complete: awaited above (PSM), or issued by the same
+          // warp before QK_r(j), whose commit of S_r(j) tracks all its MMAs.
+          // This half rescales O_r columns [64 half, +64) of its rows.  (On an
+          // item's first tile O_r still holds the previous item: PV_r(0)
+          // overwrites it.)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            uint32_t o[32];
+            tmem_ld32(tOr + 64u * half + 32u * q, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) o[cc] = __float_as_uint(__uint_as_float(o[cc]) * factor);
+            tmem_st32(tOr + 64u * half + 32u * q, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_ready[map]);
+        __syncwarp();
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_ready[map]);
-      __syncwarp();
-    }
 
-    // ---- epilogue: out = O_1 / l_1 - c O_2 / l_2; warpgroup (map, half) owns
-    // channels [32 cb, +32), cb = 2 map + half
-    const int cb = 2 * map + half;
-    lpart[cb * 128 + row] = l;
-    mbar_wait(o_full, 0, ab);
-    __syncwarp();
-    tc_fence_after();
-    named_bar_sync(1, 128 * C::NSMWG);
-    const float l1 = lpart[row] + lpart[128 + row], l2 = lpart[256 + row] + lpart[384 + row];
-    float coef;
-    if (EPI == kEpiRmsNorm) {
-      coef = *p.lambda;
-    } else {
-      const float lg = (t < p.n) ? p.lam_logits[b * p.sb + static_cast<long long>(t) * p.st + u] : 0.f;
-      coef = 1.f / (1.f + expf(-lg));
-    }
-    const float a1 = 1.f / l1, a2 = -coef / l2;
-    float y[32];
-    {
-      uint32_t o1[32], o2[32];
-      tmem_ld32(tl + C::TM_O1 + 32u * cb, o1);
-      tmem_ld32(tl + C::TM_O2 + 32u * cb, o2);
-      tmem_ld_wait2(o1, o2);
-#pragma unroll
-      for (int c = 0; c < 32; ++c) y[c] = fmaf(__uint_as_float(o2[c]), a2, __uint_as_float(o1[c]) * a1);
-    }
-    float rinv = 1.f;
-    if (EPI == kEpiRmsNorm) {
-      float ss0 = 0.f, ss1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        ss0 = fmaf(y[c], y[c], ss0);
-        ss1 = fmaf(y[c + 1], y[c + 1], ss1);
-      }
-      sspart[cb * 128 + row] = ss0 + ss1;
+      // ---- epilogue: out = O_1 / l_1 - c O_2 / l_2; warpgroup (map, half)
+      // owns channels [32 cb, +32)
+      mbar_wait(o_full, static_cast<uint32_t>(k) & 1u, ab);
       __syncwarp();
-      named_bar_sync(1, 128 * C::NSMWG);
-      const float tot = (sspart[row] + sspart[128 + row]) + (sspart[256 + row] + sspart[384 + row]);
-      rinv = p.norm_mult * rsqrtf(tot * (1.f / DV) + p.eps);
-    }
-    if (t < p.n) {
-      __nv_bfloat16* orow =
-          p.out + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * DV + 32 * cb;
-      uint32_t wv[16];
-#pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float y0 = y[c] * rinv, y1 = y[c + 1] * rinv;
-        if (EPI == kEpiRmsNorm && p.gamma != nullptr) {
-          y0 *= __ldg(p.gamma + 32 * cb + c);
-          y1 *= __ldg(p.gamma + 32 * cb + c + 1);
+      tc_fence_after();
+      float y[32];
+      {
+        uint32_t o1[32], o2[32];
+        tmem_ld32(tl + C::TM_O1 + 32u * cb, o1);
+        tmem_ld32(tl + C::TM_O2 + 32u * cb, o2);
+        tmem_ld_wait2(o1, o2);
+        if constexpr (PERSIST) {
+          // O is in registers: the next item's first PV may overwrite it.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(o_free);
+          __syncwarp();
         }
-        wv[c >> 1] = pack_bf16x2(y0, y1);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(orow);
+        float* lp = lpart + (k & 1) * 512;
+        lp[cb * 128 + row] = l;
+        named_bar_sync(1, 128 * C::NSMWG);
+        const float l1 = lp[row] + lp[128 + row], l2 = lp[256 + row] + lp[384 + row];
+        float coef;
+        if (EPI == kEpiRmsNorm) {
+          coef = *p.lambda;
+        } else {
+          const float lg = (t < p.n) ? p.lam_logits[c.b * p.sb + static_cast<long long>(t) * p.st + c.u] : 0.f;
+          coef = 1.f / (1.f + expf(-lg));
+        }
+        const float a1 = 1.f / l1, a2 = -coef / l2;
 #pragma unroll
-      for (int v = 0; v < 4; ++v) dst[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+        for (int cc = 0; cc < 32; ++cc) y[cc] = fmaf(__uint_as_float(o2[cc]), a2, __uint_as_float(o1[cc]) * a1);
+      }
+      float rinv = 1.f;
+      if (EPI == kEpiRmsNorm) {
+        float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 32; cc += 2) {
+          ss0 = fmaf(y[cc], y[cc], ss0);
+          ss1 = fmaf(y[cc + 1], y[cc + 1], ss1);
+        }
+        float* sp = sspart + (k & 1) * 512;
+        sp[cb * 128 + row] = ss0 + ss1;
+        __syncwarp();
+        named_bar_sync(1, 128 * C::NSMWG);
+        const float tot = (sp[row] + sp[128 + row]) + (sp[256 + row] + sp[384 + row]);
+        rinv = p.norm_mult * rsqrtf(tot * (1.f / DV) + p.eps);
+      }
+      if (t < p.n) {
+        __nv_bfloat16* orow =
+            p.out + ((static_cast<size_t>(c.b) * p.n + t) * p.units_per_batch + c.u) * DV + 32 * cb;
+        uint32_t wv[16];
+#pragma unroll
+        for (int cc = 0; cc < 32; cc += 2) {
+          float y0 = y[cc] * rinv, y1 = y[cc + 1] * rinv;
+          if (EPI == kEpiRmsNorm && p.gamma != nullptr) {
+            y0 *= __ldg(p.gamma + 32 * cb + cc);
+            y1 *= __ldg(p.gamma + 32 * cb + cc + 1);
+          }
+          wv[cc >> 1] = pack_bf16x2(y0, y1);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+      }
+      gt += static_cast<uint32_t>(T);
     }
   }
 

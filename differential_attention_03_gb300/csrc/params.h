@@ -30,6 +30,41 @@ struct TwoPassParams {
   int* status;
 };
 
+// What work item `idx` of a tcgen05 launch computes: batch b, unit u (V1:
+// head; V2: query-head pair), its query heads and K/V head, query tile qt
+// (first row q0).  Items are ordered heaviest causal first: unit-major keeps
+// all query tiles of one unit together (its K/V stream shared in L2),
+// query-tile-major runs the heaviest tiles of every unit first.
+struct TileCoord {
+  int b, u, hq1, hq2, hk, qt, q0;
+};
+
+template <int EPI>
+__device__ __forceinline__ TileCoord tile_coord(const TwoPassParams& p, int idx) {
+  const int units = p.B * p.units_per_batch;
+  int unit, qt;
+  if (p.order == 0) {
+    unit = idx / p.num_q_tiles;
+    qt = p.num_q_tiles - 1 - idx % p.num_q_tiles;
+  } else {
+    qt = p.num_q_tiles - 1 - idx / units;
+    unit = idx % units;
+  }
+  TileCoord c;
+  c.b = unit / p.units_per_batch;
+  c.u = unit % p.units_per_batch;
+  if (EPI == kEpiRmsNorm) {
+    c.hq1 = c.hq2 = c.hk = c.u;
+  } else {
+    c.hq1 = 2 * c.u;
+    c.hq2 = 2 * c.u + 1;
+    c.hk = c.hq1 / p.group;
+  }
+  c.qt = qt;
+  c.q0 = qt * 128;
+  return c;
+}
+
 struct SimtParams {
   const float* q1;  // V1: [B, n, H, d]; V2: q [B, n, Hq, d] (q1 == q2)
   const float* q2;

@@ -84,7 +84,8 @@ class World:
             if c == "tma":
                 i = 0 if self.rnd.random() < 0.6 else self.rnd.randrange(len(self.tma))
                 s, tag, bar = self.tma.pop(i)
-                self.slot[s] = tag
+                if s != "Q":
+                    self.slot[s] = tag
                 bar.arrive()
             elif c in live:
                 try:
@@ -101,8 +102,14 @@ class World:
 
 
 # --------------------------------------------------------------------------- one-pass kernel
-def onepass(T, seed, nslot, psm, shared_k, vf=2, npb=1, p_ready_per_buffer=True):
-    """onepass.cuh: one MMA warp per map, both walk every fill (empty counts 2)."""
+def onepass(T, seed, nslot, psm, shared_k, vf=2, npb=1, p_ready_per_buffer=True, items=None):
+    """onepass.cuh: persistent; one MMA warp per map, both walk every fill (empty counts 2).
+
+    `items` lists the key-tile counts of the work items one CTA processes in
+    turn (default: one item of T tiles); ring, per-tile barriers and their
+    phases run on across items, q_free guards Q and o_free the accumulators.
+    """
+    items = [T] if items is None else items
     W = World(seed)
     full = [Bar(1) for _ in range(nslot)]
     empty = [Bar(2) for _ in range(nslot)]
@@ -111,21 +118,37 @@ def onepass(T, seed, nslot, psm, shared_k, vf=2, npb=1, p_ready_per_buffer=True)
     nbar = npb if p_ready_per_buffer else 1
     p_ready = [[Bar(1) for _ in range(nbar)] for _ in range(2)]
     pv_done = [[Bar(1) for _ in range(npb)] for _ in range(2)]
-    o_full = Bar(2)
-    fills = [("K1", 0)] + ([] if shared_k else [("K2", 0)])
-    for j in range(T):
-        if psm and j + 1 < T:
-            fills += [("K1", j + 1)] + ([] if shared_k else [("K2", j + 1)])
-        fills += [("V", j, p) for p in range(vf)]
-        if not psm and j + 1 < T:
-            fills += [("K1", j + 1)] + ([] if shared_k else [("K2", j + 1)])
+    q_full, o_full, q_free, o_free = Bar(1), Bar(2), Bar(2), Bar(2)
+    W.q = None
+    W.oread = {(a, r): -1 for a in range(2) for r in range(2)}  # (softmax agent, O_r) -> last item read
+    fills = []
+    for it, Ti in enumerate(items):
+        fills += [("K1", it, 0)] + ([] if shared_k else [("K2", it, 0)])
+        for j in range(Ti):
+            if psm and j + 1 < Ti:
+                fills += [("K1", it, j + 1)] + ([] if shared_k else [("K2", it, j + 1)])
+            fills += [("V", it, j, p) for p in range(vf)]
+            if not psm and j + 1 < Ti:
+                fills += [("K1", it, j + 1)] + ([] if shared_k else [("K2", it, j + 1)])
 
     def producer():
-        for f, tag in enumerate(fills):
-            s, use = f % nslot, f // nslot
-            if use:
-                yield from W.wait(empty[s], (use - 1) & 1)
-            W.tma.append((s, tag, full[s]))
+        f = 0
+        for it, Ti in enumerate(items):
+            if it:
+                yield from W.wait(q_free, (it - 1) & 1)
+
+            class QLoad:  # lands as a TMA copy: tags the Q buffer, then arrives q_full
+                def arrive(self, it=it):
+                    W.q = it
+                    q_full.arrive()
+            W.tma.append(("Q", it, QLoad()))
+            n_item = 1 + (0 if shared_k else 1) + Ti * vf + (Ti - 1) * (1 if shared_k else 2)
+            for _ in range(n_item):
+                s, use = f % nslot, f // nslot
+                if use:
+                    yield from W.wait(empty[s], (use - 1) & 1)
+                W.tma.append((s, fills[f], full[s]))
+                f += 1
 
     def mma(r):
         fill = 0
@@ -140,69 +163,93 @@ def onepass(T, seed, nslot, psm, shared_k, vf=2, npb=1, p_ready_per_buffer=True)
             W.expect(W.slot, s, fills[f], f"warp {r} acquire")
             return s, fills[f]
 
-        def k_tile(jj):
+        def k_tile(it, g, jj, last):
             while True:
                 s, tag = yield from acquire()
                 if tag[0] == mine:
                     break
                 W.commit(r, empty[s])        # the other map's K: waited on, released
-            if psm and jj > 0:
-                yield from W.wait(s_free[r], (jj - 1) & 1)
+            if psm and g > 0:
+                yield from W.wait(s_free[r], (g - 1) & 1)
 
-            def qk(s=s, tag=tag, jj=jj):
-                W.expect(W.slot, s, tag, f"QK{r + 1}({jj}) reads K")
-                W.tmem[("S", r)] = jj
+            def qk(s=s, tag=tag, g=g, it=it):
+                W.expect(W.slot, s, tag, f"QK{r + 1}({g}) reads K")
+                if W.q != it:
+                    W.errors.append(f"QK{r + 1}({g}) read Q of item {W.q}, wanted {it}")
+                W.tmem[("S", r)] = g
             W.mma(r, qk)
             W.commit(r, s_full[r])
             W.commit(r, empty[s])
+            if last:
+                W.commit(r, q_free)
             if not shared_k and r == 0:
                 s2, _ = yield from acquire()  # K_2 of the same tile
                 W.commit(r, empty[s2])
 
-        yield from k_tile(0)
-        for j in range(T):
-            if psm and j + 1 < T:
-                yield from k_tile(j + 1)
-            sv = []
-            for _ in range(vf):
-                sv.append((yield from acquire()))
-            b = j % npb
-            yield from W.wait(p_ready[r][b if p_ready_per_buffer else 0],
-                              (j // npb if p_ready_per_buffer else j) & 1)
-
-            for i, (s, tag) in enumerate(sv):  # the MMAs of one V part, then its release
-                def pv(s=s, tag=tag, j=j, b=b):
-                    W.expect(W.slot, s, tag, f"PV{r + 1}({j}) reads V")
-                    if psm:
-                        W.expect(W.pbuf, (r, b), j, f"PV{r + 1}({j}) reads P")
-                    else:
-                        W.expect(W.tmem, ("P", r), j, f"PV{r + 1}({j}) reads P in TMEM")
-                W.mma(r, pv)
-                if i + 1 < len(sv):
-                    W.commit(r, empty[s])
-            if psm:
-                W.commit(r, pv_done[r][b])
-            W.commit(r, empty[sv[-1][0]])
-            if not psm and j + 1 < T:
-                yield from k_tile(j + 1)
-        W.commit(r, o_full)
+        gt = 0
+        for it, Ti in enumerate(items):
+            yield from W.wait(q_full, it & 1)
+            yield from k_tile(it, gt, 0, Ti == 1)
+            for j in range(Ti):
+                g = gt + j
+                if psm and j + 1 < Ti:
+                    yield from k_tile(it, g + 1, j + 1, j + 2 == Ti)
+                sv = []
+                for _ in range(vf):
+                    sv.append((yield from acquire()))
+                b = g % npb
+                yield from W.wait(p_ready[r][b if p_ready_per_buffer else 0],
+                                  (g // npb if p_ready_per_buffer else g) & 1)
+                if j == 0 and it:
+                    yield from W.wait(o_free, (it - 1) & 1)
+                for i, (s, tag) in enumerate(sv):  # the MMAs of one V part, then its release
+                    def pv(s=s, tag=tag, g=g, b=b, it=it, j=j):
+                        W.expect(W.slot, s, tag, f"PV{r + 1}({g}) reads V")
+                        if psm:
+                            W.expect(W.pbuf, (r, b), g, f"PV{r + 1}({g}) reads P")
+                        else:
+                            W.expect(W.tmem, ("P", r), g, f"PV{r + 1}({g}) reads P in TMEM")
+                        if j == 0 and any(W.oread[(a, r)] != it - 1 for a in range(2)):
+                            W.errors.append(f"PV{r + 1} of item {it} overwrote O{r + 1} before every epilogue read it")
+                        W.tmem[("O", r)] = (it, j)
+                    W.mma(r, pv)
+                    if i + 1 < len(sv):
+                        W.commit(r, empty[s])
+                if psm:
+                    W.commit(r, pv_done[r][b])
+                W.commit(r, empty[sv[-1][0]])
+                if not psm and j + 1 < Ti:
+                    yield from k_tile(it, g + 1, j + 1, j + 2 == Ti)
+            W.commit(r, o_full)
+            gt += Ti
 
     def softmax(r):
-        for j in range(T):
-            yield from W.wait(s_full[r], j & 1)
-            W.expect(W.tmem, ("S", r), j, f"softmax {r + 1} reads S({j})")
-            if psm:
-                s_free[r].arrive()
-                b = j % npb
-                if j >= npb:
-                    yield from W.wait(pv_done[r][b], ((j - npb) // npb) & 1)
-                W.pbuf[(r, b)] = j
-            else:
-                W.tmem[("P", r)] = j      # P over S in TMEM
-            yield
-            p_ready[r][(j % npb) if p_ready_per_buffer else 0].arrive()
-        yield from W.wait(o_full, 0)
+        gt = 0
+        for it, Ti in enumerate(items):
+            for j in range(Ti):
+                g = gt + j
+                yield from W.wait(s_full[r], g & 1)
+                W.expect(W.tmem, ("S", r), g, f"softmax {r + 1} reads S({g})")
+                if psm:
+                    s_free[r].arrive()
+                    b = g % npb
+                    if g >= npb:
+                        yield from W.wait(pv_done[r][b], ((g - npb) // npb) & 1)
+                    W.pbuf[(r, b)] = g
+                else:
+                    W.tmem[("P", r)] = g      # P over S in TMEM
+                yield
+                p_ready[r][(g % npb) if p_ready_per_buffer else 0].arrive()
+            yield from W.wait(o_full, it & 1)
+            # Every epilogue warpgroup reads columns of both accumulators.
+            for rr in range(2):
+                W.expect(W.tmem, ("O", rr), (it, Ti - 1), f"epilogue {r + 1} reads O{rr + 1} of item {it}")
+                W.oread[(r, rr)] = it
+                yield
+            o_free.arrive()
+            gt += Ti
 
+    W.tma_kinds = True
     return W.run({"prod": producer(), "mma0": mma(0), "mma1": mma(1), "sm0": softmax(0), "sm1": softmax(1)})
 
 
@@ -344,6 +391,21 @@ def test_onepass_p_in_tmem_shared_k(T):
         assert onepass(T, seed, nslot=4, psm=False, shared_k=True, vf=1) == "ok", seed
 
 
+ITEM_LISTS = [[3, 1], [1, 1, 1], [2, 5, 1, 3], [4, 4]]
+
+
+@pytest.mark.parametrize("items", ITEM_LISTS)
+def test_onepass_persistent_p_in_smem(items):
+    for seed in range(20):
+        assert onepass(0, seed, nslot=7, psm=True, shared_k=False, items=items) == "ok", seed
+
+
+@pytest.mark.parametrize("items", ITEM_LISTS)
+def test_onepass_persistent_p_in_tmem_shared_k(items):
+    for seed in range(20):
+        assert onepass(0, seed, nslot=4, psm=False, shared_k=True, vf=1, items=items) == "ok", seed
+
+
 @pytest.mark.parametrize("T", TS)
 def test_twopass_per_owner_full_barriers(T):
     for seed in range(25):
@@ -359,6 +421,20 @@ def test_model_catches_double_buffered_p_with_one_ready_barrier():
     good = [onepass(T, seed, nslot=4, psm=True, shared_k=False, npb=2, p_ready_per_buffer=True)
             for T in (3, 5, 9) for seed in range(25)]
     assert all(r == "ok" for r in good)
+
+
+def test_model_catches_missing_q_free_and_o_free():
+    import inspect
+    src = inspect.getsource(onepass)
+    ns = {}
+    for cut, what in ((
+            """                if j == 0 and it:\n                    yield from W.wait(o_free, (it - 1) & 1)\n""", "o_free"),
+            ("""            if it:\n                yield from W.wait(q_free, (it - 1) & 1)\n""", "q_free")):
+        assert cut in src, what
+        exec(compile(src.replace(cut, ""), __file__, "exec"), globals(), ns)
+        bad = [ns["onepass"](0, seed, nslot=7, psm=True, shared_k=False, items=it)
+               for it in ([3, 1], [2, 5, 1, 3]) for seed in range(30)]
+        assert any(r != "ok" for r in bad), what
 
 
 def test_model_catches_shared_full_barriers_with_partial_waiters():
