@@ -97,7 +97,8 @@ struct OnePassCfg {
   static constexpr int OFF_LP = (OFF_MISC + 16 + 15) / 16 * 16;  // float [2 items][4][128] partial row sums
   static constexpr int OFF_SS = OFF_LP + 8 * 128 * 4;             // float [2 items][4][128] partial sums of squares
   static constexpr int OFF_XM = OFF_SS + 8 * 128 * 4;             // float [2 tiles][2 maps][2 halves][128]
-  static constexpr int SMEM_BYTES = OFF_XM + 8 * 128 * 4 + 1024;  // + 1 KB alignment slack
+  static constexpr int OFF_GAMMA = OFF_XM + 8 * 128 * 4;         // float [DV] RMSNorm weight (V1)
+  static constexpr int SMEM_BYTES = OFF_GAMMA + DV * 4 + 1024;    // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TM_O1 = 0, TM_O2 = 128, TM_A = 256, TM_B = 384;
   static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false, false);
@@ -138,6 +139,7 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
   float* lpart = reinterpret_cast<float*>(smem + C::OFF_LP);
   float* sspart = reinterpret_cast<float*>(smem + C::OFF_SS);
   float* xmax = reinterpret_cast<float*>(smem + C::OFF_XM);
+  float* sgamma = reinterpret_cast<float*>(smem + C::OFF_GAMMA);
 
   // ---- this CTA's work items: round k takes item k G + blockIdx.x, or
   // k G + G - 1 - blockIdx.x on odd rounds; the list ends at the first one
@@ -177,6 +179,9 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
+  // The epilogue's per-channel weight, staged once per CTA (a scalar global
+  // load per channel and item sat on the epilogue's critical path).
+  if (threadIdx.x < DV) sgamma[threadIdx.x] = (EPI == kEpiRmsNorm && p.gamma != nullptr) ? p.gamma[threadIdx.x] : 1.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -382,6 +387,7 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
     const uint32_t tOr = tl + (map ? C::TM_O2 : C::TM_O1);
     const uint64_t sc2 = f2pack(sc, sc);
     const int cb = 2 * map + half;  // epilogue: output channels [32 cb, +32)
+    const float lam = (EPI == kEpiRmsNorm) ? *p.lambda : 0.f;  // read once per CTA
     uint32_t gt = 0;                // tiles of earlier items
 
     for (int k = 0; k < C::MAX_ITEMS; ++k) {
@@ -535,10 +541,8 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
         lp[cb * 128 + row] = l;
         named_bar_sync(1, 128 * C::NSMWG);
         const float l1 = lp[row] + lp[128 + row], l2 = lp[256 + row] + lp[384 + row];
-        float coef;
-        if (EPI == kEpiRmsNorm) {
-          coef = *p.lambda;
-        } else {
+        float coef = lam;
+        if (EPI == kEpiV2) {
           const float lg = (t < p.n) ? p.lam_logits[c.b * p.sb + static_cast<long long>(t) * p.st + c.u] : 0.f;
           coef = 1.f / (1.f + expf(-lg));
         }
@@ -568,9 +572,9 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
 #pragma unroll
         for (int cc = 0; cc < 32; cc += 2) {
           float y0 = y[cc] * rinv, y1 = y[cc + 1] * rinv;
-          if (EPI == kEpiRmsNorm && p.gamma != nullptr) {
-            y0 *= __ldg(p.gamma + 32 * cb + cc);
-            y1 *= __ldg(p.gamma + 32 * cb + cc + 1);
+          if (EPI == kEpiRmsNorm) {
+            y0 *= sgamma[32 * cb + cc];
+            y1 *= sgamma[32 * cb + cc + 1];
           }
           wv[cc >> 1] = pack_bf16x2(y0, y1);
         }
