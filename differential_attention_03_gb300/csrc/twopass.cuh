@@ -85,7 +85,8 @@ struct TwoPassCfg {
   static constexpr int OFF_BARS = OFF_RING + NSLOT * SLOT;
   static constexpr int NBARS = 3 * NSLOT + 18;
   static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + 1 KB alignment slack
+  static constexpr int OFF_GAMMA = OFF_MISC + 16;            // float [DV] RMSNorm weight (V1)
+  static constexpr int SMEM_BYTES = OFF_GAMMA + DV * 4 + 1024;  // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TM_O = 0;
   static constexpr uint32_t TM_A = DV;
@@ -230,6 +231,11 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
+  // The epilogue's per-channel weight, staged once (a scalar global load per
+  // channel sat on the epilogue's critical path).
+  float* sgamma = reinterpret_cast<float*>(smem + C::OFF_GAMMA);
+  for (int i = threadIdx.x; i < DV; i += C::NTHREADS)
+    sgamma[i] = (EPI == kEpiRmsNorm && p.gamma != nullptr) ? p.gamma[i] : 1.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -607,8 +613,8 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
           float y1 = __uint_as_float(rr[c + 1]) * rinv;
           if (EPI == kEpiRmsNorm && p.gamma != nullptr) {
             const int col = wg * QW + ch * 32 + c;
-            y0 *= __ldg(p.gamma + col);
-            y1 *= __ldg(p.gamma + col + 1);
+            y0 *= sgamma[col];
+            y1 *= sgamma[col + 1];
           }
           w[c >> 1] = pack_bf16x2(y0, y1);
         }
