@@ -232,10 +232,13 @@ diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d, 
   if (grid > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "diffattn_forward: too many tiles");
   // d = 64 (value width 128): one sweep with two online-softmax states fits
   // TMEM; d = 128 (value width 256) does not, and sweeps the keys twice.
-  // d = 64: many short items, so one persistent CTA per SM overlaps each
-  // item's start with the previous one's end; d = 128: one CTA per item.
-  cudaError_t e = (d == 64) ? da::launch_onepass_v1_d64(p, static_cast<int>(persistent_grid(grid)), s)
-                            : da::launch_twopass_v1_d128(p, static_cast<int>(grid), s);
+  // Short items (up to 64 query tiles per head): one persistent CTA per SM,
+  // so each item's start overlaps the previous one's end.  Long items: one
+  // CTA per item (the fixed cost is small against them, and the hardware's
+  // dynamic CTA scheduling balances them; measured faster).
+  const bool persist = p.num_q_tiles <= 64;
+  const int g = static_cast<int>(persist ? persistent_grid(grid) : grid);
+  cudaError_t e = (d == 64) ? da::launch_onepass_v1_d64(p, g, persist, s) : da::launch_twopass_v1_d128(p, g, persist, s);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward (bf16) launch");
   g_launches.fetch_add(1);
   return ok();

@@ -1,6 +1,7 @@
 #include "onepass_inst.cuh"
 namespace da {
-cudaError_t launch_onepass_v1_d64(const TwoPassParams& p, int grid, cudaStream_t s) {
-  return launch_onepass<64, false, kEpiRmsNorm, 7, true, true>(p, grid, s);
+cudaError_t launch_onepass_v1_d64(const TwoPassParams& p, int grid, bool persistent, cudaStream_t s) {
+  return persistent ? launch_onepass<64, false, kEpiRmsNorm, 7, true, true>(p, grid, s)
+                    : launch_onepass<64, false, kEpiRmsNorm, 7, true, false>(p, grid, s);
 }
 }  // namespace da

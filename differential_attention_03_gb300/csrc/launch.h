@@ -9,9 +9,9 @@
 namespace da {
 
 // V1, d = 128, value width 256: two sweeps, one accumulator.
-cudaError_t launch_twopass_v1_d128(const TwoPassParams& p, int grid, cudaStream_t s);
+cudaError_t launch_twopass_v1_d128(const TwoPassParams& p, int grid, bool persistent, cudaStream_t s);
 // V1, d = 64, value width 128: one sweep, two online-softmax states.
-cudaError_t launch_onepass_v1_d64(const TwoPassParams& p, int grid, cudaStream_t s);
+cudaError_t launch_onepass_v1_d64(const TwoPassParams& p, int grid, bool persistent, cudaStream_t s);
 // V2, d = 128 (query/key/value width 128), one K/V head per query-head pair: one sweep.
 cudaError_t launch_onepass_v2_d128(const TwoPassParams& p, int grid, cudaStream_t s);
 

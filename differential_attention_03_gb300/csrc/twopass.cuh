@@ -36,6 +36,15 @@
 //            has loaded them: per tile the MMA issues QK2(j+1), QK1(j+1), then
 //            PV(j), and the softmax of tile j+1 overlaps PV(j).
 //
+// Persistent variant (template flag PERSIST; else one CTA per item): one CTA
+// per SM walks a list of work items, heaviest first, dealt out in "snake"
+// order over the CTAs (round k: items k G .. k G + G - 1, reversed on odd
+// rounds).  Ring fills, S-buffer uses and sweep-2 tile phases run on across
+// items, so the next item's Q and K tiles load during the current item's last
+// tiles and epilogue; q_free (both MMA warps' last QK^T of an item done)
+// guards the Q buffer, o_free (every softmax warp done with O and the S_1
+// buffer) guards the TMEM columns the next item's first MMAs write.
+//
 // Roles (640 threads, one CTA per SM):
 //   warp 0      TMA producer: Q_1, Q_2 once, then K_1 / K_2 / V tiles into a
 //               ring of NSLOT equal slots, in exactly the order warp 1
@@ -63,7 +72,7 @@
 
 namespace da {
 
-template <int D, int DV, bool SHARED_K, int EPI, int NSLOT>
+template <int D, int DV, bool SHARED_K, int EPI, int NSLOT, bool PERSIST>
 struct TwoPassCfg {
   static constexpr int BM = 128;   // queries per CTA (TMEM lanes)
   static constexpr int BN = 128;   // keys per tile
@@ -83,7 +92,7 @@ struct TwoPassCfg {
   static constexpr int OFF_P = 2 * Q_TILE;
   static constexpr int OFF_RING = OFF_P + P_TILE;
   static constexpr int OFF_BARS = OFF_RING + NSLOT * SLOT;
-  static constexpr int NBARS = 3 * NSLOT + 18;
+  static constexpr int NBARS = 3 * NSLOT + 22;
   static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
   static constexpr int OFF_GAMMA = OFF_MISC + 16;            // float [DV] RMSNorm weight (V1)
   static constexpr int SMEM_BYTES = OFF_GAMMA + DV * 4 + 1024;  // + 1 KB alignment slack
@@ -99,6 +108,8 @@ struct TwoPassCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(NSLOT >= VF + 2, "ring depth");
   static_assert(!SHARED_K, "the two MMA warps consume separate K_1 / K_2 fills");
+  static constexpr int MAX_ITEMS = PERSIST ? 0x7fffffff : 1;  // work items per CTA
+  static constexpr int FILLS_PER_TILE = 4 + VF;               // ring fills of an item with T key tiles: T * this
 };
 
 // Merge two partial softmax states (max in the scaled log2 domain, sum).
@@ -152,9 +163,9 @@ __device__ __forceinline__ void row_stats64(uint32_t (&r0)[32], uint32_t (&r1)[3
   m = m_new;
 }
 
-template <int D, int DV, bool SHARED_K, int EPI, int NSLOT>
+template <int D, int DV, bool SHARED_K, int EPI, int NSLOT, bool PERSIST>
 __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
-  using C = TwoPassCfg<D, DV, SHARED_K, EPI, NSLOT>;
+  using C = TwoPassCfg<D, DV, SHARED_K, EPI, NSLOT, PERSIST>;
   constexpr int BM = C::BM, BN = C::BN;
 
   extern __shared__ uint8_t smem_raw[];
@@ -166,8 +177,8 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
   uint64_t* full = bars;              // [2][NSLOT] ring slot loaded, one barrier per consuming warp
   uint64_t* empty = full + 2 * NSLOT; // [NSLOT] ring slot released by the MMAs
-  uint64_t* q_full = empty + NSLOT;
-  uint64_t* o_full = q_full + 1;
+  uint64_t* q_full = empty + NSLOT;   // Q of the item landed
+  uint64_t* o_full = q_full + 1;      // every PV of the item completed
   uint64_t* s1_full = o_full + 1;     // [4] sweep 1: S written into TMEM buffer b
   uint64_t* s1_free = s1_full + 4;    // [4] sweep 1: the map's 8 warps have loaded buffer b
   uint64_t* a2_full = s1_free + 4;    // sweep 2: S_1 of the tile in A
@@ -176,33 +187,24 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
   uint64_t* b2_free = a2_free + 1;    // sweep 2: every softmax warp has loaded B
   uint64_t* p_ready = b2_free + 1;    // sweep 2: P of the tile in shared memory
   uint64_t* pv_done = p_ready + 1;    // sweep 2: PV of the tile completed (P buffer free)
-  uint64_t* w2_done = pv_done + 1;    // every MMA of warp 2 completed
+  uint64_t* q_free = pv_done + 1;     // both maps' last QK^T of the item completed
+  uint64_t* o_free = q_free + 1;      // every softmax warp is done with O and the A buffer
+  uint64_t* mma_done = o_free + 1;    // [2] every MMA of warp 1 / warp 2 completed (abort drain)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
-  // ---- which tile this CTA owns
-  const int units = p.B * p.units_per_batch;
-  int unit, qt;
-  if (p.order == 0) {
-    unit = blockIdx.x / p.num_q_tiles;
-    qt = p.num_q_tiles - 1 - static_cast<int>(blockIdx.x % p.num_q_tiles);
-  } else {
-    qt = p.num_q_tiles - 1 - static_cast<int>(blockIdx.x / units);
-    unit = blockIdx.x % units;
-  }
-  const int b = unit / p.units_per_batch;
-  const int u = unit % p.units_per_batch;
-  int hq1, hq2, hk;
-  if (EPI == kEpiRmsNorm) {
-    hq1 = hq2 = hk = u;
-  } else {
-    hq1 = 2 * u;
-    hq2 = 2 * u + 1;
-    hk = hq1 / p.group;
-  }
-  const int q0 = qt * BM;
-  const int kv_end = p.causal ? min(p.n, q0 + BM) : p.n;
-  const int T = (kv_end + BN - 1) / BN;  // key tiles per sweep (>= 1)
+  // ---- this CTA's work items: round k takes item k G + blockIdx.x, or
+  // k G + G - 1 - blockIdx.x on odd rounds; the list ends at the first one
+  // past the last item (later rounds start further on).
+  const int nitems = p.num_q_tiles * p.B * p.units_per_batch;
+  const int G = static_cast<int>(gridDim.x);
+  auto item_of = [&](int k) -> int {
+    return k * G + ((k & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x));
+  };
+  auto tiles_of = [&](const TileCoord& c) -> int {
+    const int kv_end = p.causal ? min(p.n, c.q0 + BM) : p.n;
+    return (kv_end + BN - 1) / BN;  // key tiles per sweep (>= 1)
+  };
 
   // ---- set-up
   if (threadIdx.x == 0) {
@@ -223,7 +225,10 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
     mbar_init(b2_free, 4 * C::NSMWG);
     mbar_init(p_ready, 4 * C::NSMWG);
     mbar_init(pv_done, 1);
-    mbar_init(w2_done, 1);
+    mbar_init(q_free, 2);
+    mbar_init(o_free, 4 * C::NSMWG);
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -250,12 +255,7 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
       tma_prefetch_desc(&p.tm_k1);
       if (!SHARED_K) tma_prefetch_desc(&p.tm_k2);
       tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(q_full, 2 * C::Q_TILE);
-      for (int bx = 0; bx < C::QB; ++bx) {
-        tma_load_4d(smem + C::OFF_Q1 + bx * BM * 128, &p.tm_q1, q_full, bx * 64, hq1, q0, b);
-        tma_load_4d(smem + C::OFF_Q2 + bx * BM * 128, &p.tm_q2, q_full, bx * 64, hq2, q0, b);
-      }
-      int fill = 0;
+      int fill = 0, qloads = 0;
       bool ok = true;
       // Each fill signals the `full` barrier of the warp that reads it (o = 0:
       // warp 1, K_1 and V; o = 1: warp 2, K_2), so every warp sees only its
@@ -265,50 +265,59 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
       // (register bit masks: this bookkeeping sits on the producer's path).
       static_assert(2 * NSLOT <= 32, "bit masks");
       uint32_t last_o = 0, par = 0;
-      // One slot fill: `nbox` boxes of [rows][64 columns] at key row `key0`.
-      auto load = [&](const CUtensorMap* map, int key0, int rows, int nbox, int o) {
-        if (!ok) return;
-        const int s = fill % NSLOT;
-        const uint32_t use = static_cast<uint32_t>(fill / NSLOT);
-        if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, ab)) {
+      for (int k = 0; ok && k < C::MAX_ITEMS; ++k) {
+        const int idx = item_of(k);
+        if (idx >= nitems) break;
+        const TileCoord c = tile_coord<EPI>(p, idx);
+        const int T = tiles_of(c);
+        // Q of the previous item is read by its QK^T until q_free.
+        if (PERSIST && k > 0 && !mbar_wait(q_free, static_cast<uint32_t>(k - 1) & 1u, ab)) {
           ok = false;
-          return;
+          break;
         }
-        uint64_t* bar = &full[o * NSLOT + s];
-        uint8_t* dst = smem + C::OFF_RING + s * C::SLOT;
-        mbar_arrive_expect_tx(bar, C::SLOT);
-        for (int bx = 0; bx < nbox; ++bx) tma_load_4d(dst + bx * rows * 128, map, bar, bx * 64, hk, key0, b);
-        last_o = (last_o & ~(1u << s)) | (static_cast<uint32_t>(o) << s);
-        par ^= 1u << (o * NSLOT + s);  // now the parity after this fill; the fill's own is the flip of it
-        ++fill;
-      };
-      auto load_k1 = [&](int j) { load(&p.tm_k1, j * BN, BN, C::QB, 0); };
-      auto load_k2 = [&](int j) { load(&p.tm_k2, j * BN, BN, C::QB, 1); };
-      // The fill order is exactly the MMA thread's consumption order.
-      for (int j = 0; j < T; ++j) {  // sweep 1
-        load_k1(j);
-        if (!SHARED_K) load_k2(j);
-      }
-      if (SHARED_K) {  // sweep 2
+        mbar_arrive_expect_tx(q_full, 2 * C::Q_TILE);
+        for (int bx = 0; bx < C::QB; ++bx) {
+          tma_load_4d(smem + C::OFF_Q1 + bx * BM * 128, &p.tm_q1, q_full, bx * 64, c.hq1, c.q0, c.b);
+          tma_load_4d(smem + C::OFF_Q2 + bx * BM * 128, &p.tm_q2, q_full, bx * 64, c.hq2, c.q0, c.b);
+        }
+        ++qloads;
+        // One slot fill: `nbox` boxes of [rows][64 columns] at key row `key0`.
+        auto load = [&](const CUtensorMap* map, int key0, int rows, int nbox, int o) {
+          if (!ok) return;
+          const int s = fill % NSLOT;
+          const uint32_t use = static_cast<uint32_t>(fill / NSLOT);
+          if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, ab)) {
+            ok = false;
+            return;
+          }
+          uint64_t* bar = &full[o * NSLOT + s];
+          uint8_t* dst = smem + C::OFF_RING + s * C::SLOT;
+          mbar_arrive_expect_tx(bar, C::SLOT);
+          for (int bx = 0; bx < nbox; ++bx) tma_load_4d(dst + bx * rows * 128, map, bar, bx * 64, c.hk, key0, c.b);
+          last_o = (last_o & ~(1u << s)) | (static_cast<uint32_t>(o) << s);
+          par ^= 1u << (o * NSLOT + s);  // now the parity after this fill; the fill's own is the flip of it
+          ++fill;
+        };
+        auto load_k1 = [&](int j) { load(&p.tm_k1, j * BN, BN, C::QB, 0); };
+        auto load_k2 = [&](int j) { load(&p.tm_k2, j * BN, BN, C::QB, 1); };
+        // The fill order is exactly the MMA warps' consumption order.
+        for (int j = 0; j < T; ++j) {  // sweep 1
+          load_k1(j);
+          load_k2(j);
+        }
+        load_k2(0);  // sweep 2
         load_k1(0);
-      } else {
-        load_k2(0);
-        load_k1(0);
-      }
-      for (int j = 0; j < T; ++j) {
-        if (j + 1 < T) {
-          if (SHARED_K) {
-            load_k1(j + 1);
-          } else {
+        for (int j = 0; j < T; ++j) {
+          if (j + 1 < T) {
             load_k2(j + 1);
             load_k1(j + 1);
           }
+          for (int part = 0; part < C::VF; ++part) load(&p.tm_v, j * BN + part * C::VKEYS, C::VKEYS, C::VB, 0);
         }
-        for (int part = 0; part < C::VF; ++part) load(&p.tm_v, j * BN + part * C::VKEYS, C::VKEYS, C::VB, 0);
       }
       if (*ab.flag) {
         // Aborted: let the copies already issued land before the CTA exits.
-        mbar_wait_drain(q_full, 0, kWaitBudgetCycles);
+        if (qloads > 0) mbar_wait_drain(q_full, static_cast<uint32_t>(qloads - 1) & 1u, kWaitBudgetCycles);
         for (int i = 0; i < NSLOT && i < fill; ++i) {
           const int o = (last_o >> i) & 1;
           mbar_wait_drain(&full[o * NSLOT + i], ((par >> (o * NSLOT + i)) & 1u) ^ 1u, kWaitBudgetCycles);
@@ -360,268 +369,306 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
                      dk + static_cast<uint64_t>((((k >> 2) * (BN * 128)) + (k & 3) * 32) >> 4), C::IDESC_QK,
                      k > 0 ? 1u : 0u);
     };
-    // Fill order of the producer: sweep 1 K1(j) = 2j, K2(j) = 2j + 1; sweep 2
-    // K2(0) = 2T, K1(0) = 2T + 1, then per tile j: K2(j+1), K1(j+1) (if
-    // j + 1 < T) and the VF parts of V(j).
-    const int F2 = 2 * T;
     constexpr int PER_TILE = 2 + C::VF;
-    auto fill_k_next = [&](int j) { return F2 + 2 + PER_TILE * j + (mw == 0 ? 1 : 0); };  // K_map(j+1)
-    auto fill_v = [&](int j, int part) { return F2 + 2 + PER_TILE * j + (j + 1 < T ? 2 : 0) + part; };
-    bool ok = waitp(q_full, 0);
-    // ---- sweep 1: S_map(j) (S index k = 2 j + mw) goes to TMEM buffer k % 4
-    uint32_t use_lo = 0, use_hi = 0;  // writes so far of buffers mw and mw + 2
-    for (int j = 0; ok && j < T; ++j) {
-      const int k = 2 * j + mw;
-      const int bb = k & 3;
-      uint32_t& use = (bb & 2) ? use_hi : use_lo;
-      if (!acquire(k)) {
-        ok = false;
-        break;
+    uint32_t use_lo = 0, use_hi = 0;  // sweep-1 writes so far of buffers mw and mw + 2
+    int fbase = 0;                    // ring fills of earlier items
+    uint32_t g1 = 0;                  // key tiles of earlier items (each sweep)
+    bool ok = true;
+    for (int it = 0; ok && it < C::MAX_ITEMS; ++it) {
+      const int idx = item_of(it);
+      if (idx >= nitems) break;
+      const int T = tiles_of(tile_coord<EPI>(p, idx));
+      // Fill order of the producer within an item: sweep 1 K1(j) = 2j,
+      // K2(j) = 2j + 1; sweep 2 K2(0) = 2T, K1(0) = 2T + 1, then per tile j:
+      // K2(j+1), K1(j+1) (if j + 1 < T) and the VF parts of V(j).
+      const int F2 = fbase + 2 * T;
+      auto fill_k_next = [&](int j) { return F2 + 2 + PER_TILE * j + (mw == 0 ? 1 : 0); };  // K_map(j+1)
+      auto fill_v = [&](int j, int part) { return F2 + 2 + PER_TILE * j + (j + 1 < T ? 2 : 0) + part; };
+      ok = waitp(q_full, static_cast<uint32_t>(it) & 1u);
+      if (PERSIST && it > 0) {
+        // The previous item's epilogue reads O (buffers 0, 1) and A; o_free
+        // follows it, and so every sweep-2 read of the S buffers 2 and 3.
+        ok = ok && waitp(o_free, static_cast<uint32_t>(it - 1) & 1u);
       }
-      if (use > 0 && !waitp(&s1_free[bb], (use - 1) & 1u)) {  // read since its last write
-        ok = false;
-        break;
+      // ---- sweep 1: S_map(j) (S index k = 2 (g1 + j) + mw) goes to TMEM buffer k % 4
+      for (int j = 0; ok && j < T; ++j) {
+        const uint32_t k = 2u * (g1 + static_cast<uint32_t>(j)) + static_cast<uint32_t>(mw);
+        const int bb = static_cast<int>(k & 3u);
+        uint32_t& use = (bb & 2) ? use_hi : use_lo;
+        if (!acquire(fbase + 2 * j + mw)) {
+          ok = false;
+          break;
+        }
+        if (use > 0 && !waitp(&s1_free[bb], (use - 1) & 1u)) {  // read since its last write
+          ok = false;
+          break;
+        }
+        ++use;
+        qk(tmem + 128u * bb, fbase + 2 * j + mw);
+        tc_commit_elect(&s1_full[bb]);
+        tc_commit_elect(&empty[(fbase + 2 * j + mw) % NSLOT]);
       }
-      ++use;
-      qk(tmem + 128u * bb, k);
-      tc_commit_elect(&s1_full[bb]);
-      tc_commit_elect(&empty[k % NSLOT]);
-    }
-    // ---- sweep 2: this map's S buffer is sweep-1 buffer mw + 2 (A or B)
-    if (ok && use_hi > 0) ok = waitp(&s1_free[mw + 2], (use_hi - 1) & 1u);
-    if (ok) {
-      const int f = F2 + (mw == 0 ? 1 : 0);
-      ok = acquire(f);
+      // ---- sweep 2: this map's S buffer is sweep-1 buffer mw + 2 (A or B)
+      if (ok && use_hi > 0) ok = waitp(&s1_free[mw + 2], (use_hi - 1) & 1u);
       if (ok) {
-        qk(tS2, f);
-        tc_commit_elect(s2_full);
-        tc_commit_elect(&empty[f % NSLOT]);
-      }
-    }
-    for (int j = 0; ok && j < T; ++j) {
-      const uint32_t ph = static_cast<uint32_t>(j) & 1u;
-      if (j + 1 < T) {
-        const int f = fill_k_next(j);
-        if (!acquire(f) || !waitp(s2_free, ph)) {
-          ok = false;
-          break;
+        const int f = F2 + (mw == 0 ? 1 : 0);
+        ok = acquire(f);
+        if (ok) {
+          qk(tS2, f);
+          tc_commit_elect(s2_full);
+          tc_commit_elect(&empty[f % NSLOT]);
+          if (PERSIST && T == 1) tc_commit_elect(q_free);
         }
-        qk(tS2, f);
-        tc_commit_elect(s2_full);
-        tc_commit_elect(&empty[f % NSLOT]);
       }
-      if (mw == 0) {
-        bool got = true;
-#pragma unroll
-        for (int part = 0; part < C::VF; ++part) got = acquire(fill_v(j, part)) && got;
-        if (!got || !waitp(p_ready, ph)) {
-          ok = false;
-          break;
-        }
-#pragma unroll
-        for (int part = 0; part < C::VF; ++part) {
-          const uint64_t dv = dRingV + static_cast<uint64_t>(((fill_v(j, part) % NSLOT) * C::SLOT) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < C::VKEYS / 16; ++kk) {
-            const int kg = part * (C::VKEYS / 16) + kk;  // global k-step: keys 16 kg .. 16 kg + 15
-            mma_ss_elect(tmem + C::TM_O, dP + static_cast<uint64_t>((((kg >> 2) * (BM * 128)) + (kg & 3) * 32) >> 4),
-                         dv + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_PV, (j > 0 || kg > 0) ? 1u : 0u);
+      for (int j = 0; ok && j < T; ++j) {
+        const uint32_t ph2 = (g1 + static_cast<uint32_t>(j)) & 1u;
+        if (j + 1 < T) {
+          const int f = fill_k_next(j);
+          if (!acquire(f) || !waitp(s2_free, ph2)) {
+            ok = false;
+            break;
           }
-          // Each V part is released as soon as its own MMAs are done, so the
-          // next tile's first part starts loading half a P.V earlier.
-          if (part + 1 < C::VF) tc_commit_elect(&empty[fill_v(j, part) % NSLOT]);
+          qk(tS2, f);
+          tc_commit_elect(s2_full);
+          tc_commit_elect(&empty[f % NSLOT]);
+          if (PERSIST && j + 2 == T) tc_commit_elect(q_free);  // the item's last QK^T of this map
         }
-        tc_commit_elect(pv_done);
-        tc_commit_elect(&empty[fill_v(j, C::VF - 1) % NSLOT]);
+        if (mw == 0) {
+          bool got = true;
+#pragma unroll
+          for (int part = 0; part < C::VF; ++part) got = acquire(fill_v(j, part)) && got;
+          if (!got || !waitp(p_ready, ph2)) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int part = 0; part < C::VF; ++part) {
+            const uint64_t dv = dRingV + static_cast<uint64_t>(((fill_v(j, part) % NSLOT) * C::SLOT) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < C::VKEYS / 16; ++kk) {
+              const int kg = part * (C::VKEYS / 16) + kk;  // global k-step: keys 16 kg .. 16 kg + 15
+              mma_ss_elect(tmem + C::TM_O,
+                           dP + static_cast<uint64_t>((((kg >> 2) * (BM * 128)) + (kg & 3) * 32) >> 4),
+                           dv + static_cast<uint64_t>(kk * (2048 >> 4)), C::IDESC_PV, (j > 0 || kg > 0) ? 1u : 0u);
+            }
+            // Each V part is released as soon as its own MMAs are done, so the
+            // next tile's first part starts loading half a P.V earlier.
+            if (part + 1 < C::VF) tc_commit_elect(&empty[fill_v(j, part) % NSLOT]);
+          }
+          tc_commit_elect(pv_done);
+          tc_commit_elect(&empty[fill_v(j, C::VF - 1) % NSLOT]);
+        }
       }
+      if (!ok) break;
+      if (mw == 0) tc_commit_elect(o_full);
+      fbase += C::FILLS_PER_TILE * T;
+      g1 += static_cast<uint32_t>(T);
     }
-    uint64_t* last = (mw == 0) ? o_full : w2_done;
-    tc_commit_elect(last);
-    if (*ab.flag) mbar_wait_drain(last, 0, kWaitBudgetCycles);
+    tc_commit_elect(&mma_done[mw]);
+    if (*ab.flag) mbar_wait_drain(&mma_done[mw], 0, kWaitBudgetCycles);
     __syncwarp();
   } else if (warp >= 4) {
     // =============================================================== softmax + epilogue
     const int wg = (warp - 4) >> 2;  // 0..3
     const int wq = warp & 3;         // TMEM lane quarter
     const int row = wq * 32 + lane;
-    const int t = q0 + row;
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float sc = p.scale_log2;
-    const int lim = p.causal ? min(t + 1, p.n) : p.n;  // keys j < lim are visible
-
-    // ---- sweep 1: running max / sum of map (wg / 2) over key columns [64 (wg % 2), +64)
     const int map = wg >> 1;
     const int half = wg & 1;
-    float m = -INFINITY, l = 0.f;
-    uint32_t ready = 0;  // early test of this tile's barrier, made during the previous tile
-    for (int j = 0; j < T; ++j) {
-      const int k = 2 * j + map;  // S index: buffer k % 4, its (k / 4)-th write
-      const int bb = k & 3;
-      if (!ready) mbar_wait(&s1_full[bb], static_cast<uint32_t>(k >> 2) & 1u, ab);
-      __syncwarp();
-      tc_fence_after();
-      uint32_t r0[32], r1[32];
-      const uint32_t tbuf = tl + 128u * bb + 64u * half;
-      tmem_ld32(tbuf, r0);
-      tmem_ld32(tbuf + 32, r1);
-      // The MMA warps run ahead: test the next tile's buffer now (its previous
-      // phase, tile j - 1, has been consumed, so the test is exact).
-      ready = (j + 1 < T) ? mbar_test(&s1_full[(k + 2) & 3], static_cast<uint32_t>((k + 2) >> 2) & 1u) : 0u;
-      tmem_ld_wait2(r0, r1);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s1_free[bb]);
-      __syncwarp();
-      row_stats64(r0, r1, lim - (j * BN + 64 * half), sc, m, l);
-    }
+    const float lam = (EPI == kEpiRmsNorm) ? *p.lambda : 0.f;  // read once per CTA
+    uint32_t g1 = 0;  // key tiles of earlier items (each sweep)
 
-    // ---- exchange the four partial states through TMEM columns [0, 8).
-    // The other map may still be reading buffer 0 for its last tile, so all
-    // sweep-1 reads finish first; sweep 2 writes buffer 0 only in PV, after
-    // every warp has read the exchange.
-    tc_fence_before();
-    named_bar_sync(1, 128 * C::NSMWG);
-    tc_fence_after();
-    tmem_st2(tl + 2u * wg, __float_as_uint(m), __float_as_uint(l));
-    tmem_st_wait();
-    tc_fence_before();
-    __syncwarp();
-    named_bar_sync(1, 128 * C::NSMWG);
-    tc_fence_after();
-    uint32_t ps[8];
-    tmem_ld8_wait(tl, ps);
-    float m1 = __uint_as_float(ps[0]), l1 = __uint_as_float(ps[1]);
-    merge_state(m1, l1, __uint_as_float(ps[2]), __uint_as_float(ps[3]));
-    float m2 = __uint_as_float(ps[4]), l2 = __uint_as_float(ps[5]);
-    merge_state(m2, l2, __uint_as_float(ps[6]), __uint_as_float(ps[7]));
-    float coef;
-    if (EPI == kEpiRmsNorm) {
-      coef = *p.lambda;
-    } else {
-      const float lg = (t < p.n) ? p.lam_logits[b * p.sb + static_cast<long long>(t) * p.st + u] : 0.f;
-      coef = 1.f / (1.f + expf(-lg));
-    }
-    // P = 2^(s1*sc - M1) + neg2 * 2^(s2*sc - M2),  M1 = m1 + log2 l1,
-    // M2 = m2 + log2 l2 - log2 |coef|,  neg2 = -sign(coef).
-    const float M1 = m1 + log2f(l1);
-    const float acoef = fabsf(coef);
-    const float M2 = (acoef > 0.f) ? m2 + log2f(l2) - log2f(acoef) : INFINITY;
-    const float neg2 = (coef >= 0.f) ? -1.f : 1.f;
-    const uint64_t sc2 = f2pack(sc, sc);
-    const uint64_t nM1 = f2pack(-M1, -M1), nM2 = f2pack(-M2, -M2), ng2 = f2pack(neg2, neg2);
-    // This thread's P chunks: row `row`, keys [32 wg, +32) = 64-key box wg / 2,
-    // 16-byte chunks 4 (wg % 2) .. 4 (wg % 2) + 3 of the 128-byte swizzled row.
-    uint8_t* prow = smem + C::OFF_P + (wg >> 1) * (BM * 128) + row * 128;
+    for (int it = 0; it < C::MAX_ITEMS; ++it) {
+      const int idx = item_of(it);
+      if (idx >= nitems) break;
+      const TileCoord c = tile_coord<EPI>(p, idx);
+      const int T = tiles_of(c);
+      const int t = c.q0 + row;
+      const int lim = p.causal ? min(t + 1, p.n) : p.n;  // keys j < lim are visible
 
-    // ---- sweep 2: signed combined weights of key columns [32 wg, +32) -> shared memory (bf16)
-    for (int j = 0; j < T; ++j) {
-      const uint32_t ph = static_cast<uint32_t>(j) & 1u;
-      mbar_wait(b2_full, ph, ab);
-      __syncwarp();
-      tc_fence_after();
-      uint32_t r[32];
-      tmem_ld32(tl + C::TM_B + 32u * wg, r);
-      tmem_ld_wait(r);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b2_free);
-      __syncwarp();
-      uint64_t e2[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        float x0, x1;
-        f2unpack(fma2(f2pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), sc2, nM2), x0, x1);
-        e2[c] = f2pack(ex2(x0), ex2(x1));
+      // ---- sweep 1: running max / sum of map (wg / 2) over key columns [64 (wg % 2), +64)
+      float m = -INFINITY, l = 0.f;
+      uint32_t ready = 0;  // early test of this tile's barrier, made during the previous tile
+      for (int j = 0; j < T; ++j) {
+        const uint32_t k = 2u * (g1 + static_cast<uint32_t>(j)) + static_cast<uint32_t>(map);  // buffer k % 4, its (k / 4)-th write
+        const int bb = static_cast<int>(k & 3u);
+        if (!ready) mbar_wait(&s1_full[bb], (k >> 2) & 1u, ab);
+        __syncwarp();
+        tc_fence_after();
+        uint32_t r0[32], r1[32];
+        const uint32_t tbuf = tl + 128u * bb + 64u * half;
+        tmem_ld32(tbuf, r0);
+        tmem_ld32(tbuf + 32, r1);
+        // The MMA warps run ahead: test the next tile's buffer now (its previous
+        // phase, tile j - 1, has been consumed, so the test is exact).
+        ready = (j + 1 < T) ? mbar_test(&s1_full[(k + 2) & 3u], ((k + 2) >> 2) & 1u) : 0u;
+        tmem_ld_wait2(r0, r1);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s1_free[bb]);
+        __syncwarp();
+        row_stats64(r0, r1, lim - (j * BN + 64 * half), sc, m, l);
       }
-      mbar_wait(a2_full, ph, ab);
-      __syncwarp();
+
+      // ---- exchange the four partial states through TMEM columns [0, 8).
+      // The other map may still be reading buffer 0 for its last tile, so all
+      // sweep-1 reads finish first; the next writes to buffer 0 are this
+      // item's PV (after every warp has read the exchange) and, after o_free,
+      // the next item's S.
+      tc_fence_before();
+      named_bar_sync(1, 128 * C::NSMWG);
       tc_fence_after();
-      tmem_ld32(tl + C::TM_A + 32u * wg, r);
-      tmem_ld_wait(r);
+      tmem_st2(tl + 2u * wg, __float_as_uint(m), __float_as_uint(l));
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(a2_free);
-      __syncwarp();
-      const int nvis = lim - (j * BN + 32 * wg);
-      uint32_t pk[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        float x0, x1;
-        f2unpack(fma2(f2pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), sc2, nM1), x0, x1);
-        float p0, p1;
-        f2unpack(fma2(e2[c], ng2, f2pack(ex2(x0), ex2(x1))), p0, p1);
-        if (2 * c >= nvis) p0 = 0.f;
-        if (2 * c + 1 >= nvis) p1 = 0.f;
-        pk[c] = pack_bf16x2(p0, p1);
+      named_bar_sync(1, 128 * C::NSMWG);
+      tc_fence_after();
+      uint32_t ps[8];
+      tmem_ld8_wait(tl, ps);
+      float m1 = __uint_as_float(ps[0]), l1 = __uint_as_float(ps[1]);
+      merge_state(m1, l1, __uint_as_float(ps[2]), __uint_as_float(ps[3]));
+      float m2 = __uint_as_float(ps[4]), l2 = __uint_as_float(ps[5]);
+      merge_state(m2, l2, __uint_as_float(ps[6]), __uint_as_float(ps[7]));
+      float coef = lam;
+      if (EPI == kEpiV2) {
+        const float lg = (t < p.n) ? p.lam_logits[c.b * p.sb + static_cast<long long>(t) * p.st + c.u] : 0.f;
+        coef = 1.f / (1.f + expf(-lg));
       }
-      // PV(j-1) must have completed before its P is overwritten.
-      if (j > 0) mbar_wait(pv_done, static_cast<uint32_t>(j - 1) & 1u, ab);
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(prow + (((4 * (wg & 1) + c) ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_ready);
-      __syncwarp();
-    }
+      // P = 2^(s1*sc - M1) + neg2 * 2^(s2*sc - M2),  M1 = m1 + log2 l1,
+      // M2 = m2 + log2 l2 - log2 |coef|,  neg2 = -sign(coef).
+      const float M1 = m1 + log2f(l1);
+      const float acoef = fabsf(coef);
+      const float M2 = (acoef > 0.f) ? m2 + log2f(l2) - log2f(acoef) : INFINITY;
+      const float neg2 = (coef >= 0.f) ? -1.f : 1.f;
+      const uint64_t sc2 = f2pack(sc, sc);
+      const uint64_t nM1 = f2pack(-M1, -M1), nM2 = f2pack(-M2, -M2), ng2 = f2pack(neg2, neg2);
+      // This thread's P chunks: row `row`, keys [32 wg, +32) = 64-key box wg / 2,
+      // 16-byte chunks 4 (wg % 2) .. 4 (wg % 2) + 3 of the 128-byte swizzled row.
+      uint8_t* prow = smem + C::OFF_P + (wg >> 1) * (BM * 128) + row * 128;
 
-    // ---- epilogue: warpgroup wg owns output channels [wg * DV/4, +DV/4)
-    constexpr int QW = DV / 4;
-    mbar_wait(o_full, 0, ab);
-    __syncwarp();
-    tc_fence_after();
-    const uint32_t to = tl + C::TM_O + wg * QW;
-    float rinv = 1.f;
-    if (EPI == kEpiRmsNorm) {
-      float ss0 = 0.f, ss1 = 0.f;
+      // ---- sweep 2: signed combined weights of key columns [32 wg, +32) -> shared memory (bf16)
+      for (int j = 0; j < T; ++j) {
+        const uint32_t g = g1 + static_cast<uint32_t>(j);  // sweep-2 tile, counted across items
+        mbar_wait(b2_full, g & 1u, ab);
+        __syncwarp();
+        tc_fence_after();
+        uint32_t r[32];
+        tmem_ld32(tl + C::TM_B + 32u * wg, r);
+        tmem_ld_wait(r);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b2_free);
+        __syncwarp();
+        uint64_t e2[16];
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          float x0, x1;
+          f2unpack(fma2(f2pack(__uint_as_float(r[2 * cc]), __uint_as_float(r[2 * cc + 1])), sc2, nM2), x0, x1);
+          e2[cc] = f2pack(ex2(x0), ex2(x1));
+        }
+        mbar_wait(a2_full, g & 1u, ab);
+        __syncwarp();
+        tc_fence_after();
+        tmem_ld32(tl + C::TM_A + 32u * wg, r);
+        tmem_ld_wait(r);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(a2_free);
+        __syncwarp();
+        const int nvis = lim - (j * BN + 32 * wg);
+        uint32_t pk[16];
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) {
+          float x0, x1;
+          f2unpack(fma2(f2pack(__uint_as_float(r[2 * cc]), __uint_as_float(r[2 * cc + 1])), sc2, nM1), x0, x1);
+          float p0, p1;
+          f2unpack(fma2(e2[cc], ng2, f2pack(ex2(x0), ex2(x1))), p0, p1);
+          if (2 * cc >= nvis) p0 = 0.f;
+          if (2 * cc + 1 >= nvis) p1 = 0.f;
+          pk[cc] = pack_bf16x2(p0, p1);
+        }
+        // PV of the previous tile (possibly of the previous item) must have
+        // completed before its P is overwritten.
+        if (g > 0) mbar_wait(pv_done, (g - 1) & 1u, ab);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          *reinterpret_cast<uint4*>(prow + (((4 * (wg & 1) + cc) ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_ready);
+        __syncwarp();
+      }
+
+      // ---- epilogue: warpgroup wg owns output channels [wg * DV/4, +DV/4)
+      constexpr int QW = DV / 4;
+      mbar_wait(o_full, static_cast<uint32_t>(it) & 1u, ab);
+      __syncwarp();
+      tc_fence_after();
+      const uint32_t to = tl + C::TM_O + wg * QW;
+      float rinv = 1.f;
+      if (EPI == kEpiRmsNorm) {
+        float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < QW / 32; ++ch) {
+          uint32_t rr[32];
+          tmem_ld32(to + 32 * ch, rr);
+          tmem_ld_wait(rr);
+#pragma unroll
+          for (int cc = 0; cc < 32; cc += 2) {
+            ss0 = fmaf(__uint_as_float(rr[cc]), __uint_as_float(rr[cc]), ss0);
+            ss1 = fmaf(__uint_as_float(rr[cc + 1]), __uint_as_float(rr[cc + 1]), ss1);
+          }
+        }
+        // Every MMA of the item has completed and every read of A is done: A
+        // carries the exchange (the next item writes it only after o_free).
+        tmem_st1(tl + C::TM_A + wg, __float_as_uint(ss0 + ss1));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        named_bar_sync(1, 128 * C::NSMWG);
+        tc_fence_after();
+        uint32_t q4[4];
+        tmem_ld4_wait(tl + C::TM_A, q4);
+        const float tot = (__uint_as_float(q4[0]) + __uint_as_float(q4[1])) +
+                          (__uint_as_float(q4[2]) + __uint_as_float(q4[3]));
+        rinv = p.norm_mult * rsqrtf(tot * (1.f / DV) + p.eps);
+      }
+      __nv_bfloat16* orow =
+          p.out + ((static_cast<size_t>(c.b) * p.n + t) * p.units_per_batch + c.u) * DV + wg * QW;
+      uint32_t w[QW / 2];
 #pragma unroll
       for (int ch = 0; ch < QW / 32; ++ch) {
         uint32_t rr[32];
         tmem_ld32(to + 32 * ch, rr);
         tmem_ld_wait(rr);
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          ss0 = fmaf(__uint_as_float(rr[c]), __uint_as_float(rr[c]), ss0);
-          ss1 = fmaf(__uint_as_float(rr[c + 1]), __uint_as_float(rr[c + 1]), ss1);
-        }
-      }
-      // Every MMA has completed and every read of A is done: A carries the exchange.
-      tmem_st1(tl + C::TM_A + wg, __float_as_uint(ss0 + ss1));
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      named_bar_sync(1, 128 * C::NSMWG);
-      tc_fence_after();
-      uint32_t q4[4];
-      tmem_ld4_wait(tl + C::TM_A, q4);
-      const float tot = (__uint_as_float(q4[0]) + __uint_as_float(q4[1])) +
-                        (__uint_as_float(q4[2]) + __uint_as_float(q4[3]));
-      rinv = p.norm_mult * rsqrtf(tot * (1.f / DV) + p.eps);
-    }
-    __nv_bfloat16* orow = p.out + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * DV + wg * QW;
-#pragma unroll
-    for (int ch = 0; ch < QW / 32; ++ch) {
-      uint32_t rr[32];
-      tmem_ld32(to + 32 * ch, rr);
-      tmem_ld_wait(rr);
-      if (t < p.n) {
-        uint32_t w[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float y0 = __uint_as_float(rr[c]) * rinv;
-          float y1 = __uint_as_float(rr[c + 1]) * rinv;
-          if (EPI == kEpiRmsNorm && p.gamma != nullptr) {
-            const int col = wg * QW + ch * 32 + c;
+        for (int cc = 0; cc < 32; cc += 2) {
+          float y0 = __uint_as_float(rr[cc]) * rinv;
+          float y1 = __uint_as_float(rr[cc + 1]) * rinv;
+          if (EPI == kEpiRmsNorm) {
+            const int col = wg * QW + ch * 32 + cc;
             y0 *= sgamma[col];
             y1 *= sgamma[col + 1];
           }
-          w[c >> 1] = pack_bf16x2(y0, y1);
+          w[ch * 16 + (cc >> 1)] = pack_bf16x2(y0, y1);
         }
-        uint4* dst = reinterpret_cast<uint4*>(orow + ch * 32);
-#pragma unroll
-        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
       }
+      if constexpr (PERSIST) {
+        // O and A are no longer read: the next item's first MMAs may write them.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free);
+        __syncwarp();
+      }
+      if (t < p.n) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int v = 0; v < QW / 8; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+      }
+      g1 += static_cast<uint32_t>(T);
     }
   }
 

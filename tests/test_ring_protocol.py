@@ -254,41 +254,76 @@ def onepass(T, seed, nslot, psm, shared_k, vf=2, npb=1, p_ready_per_buffer=True,
 
 
 # --------------------------------------------------------------------------- two-sweep kernel
-def twopass(T, seed, nslot=4, vf=2, per_owner_full=True):
-    """twopass.cuh: warp 1 issues map-1 MMAs and P.V, warp 2 map-2 MMAs; each fill has one reader."""
+def twopass(T, seed, nslot=4, vf=2, per_owner_full=True, items=None, wait_o_free=True):
+    """twopass.cuh: warp 1 issues map-1 MMAs and P.V, warp 2 map-2 MMAs; each fill has one reader.
+
+    Persistent when `items` lists several items: fills, S-buffer uses and
+    sweep-2 tile phases run on across items.  TMEM is modelled by buffer:
+    sweep 1 cycles S through buffers 0-3 (O lives in 0 and 1, so an S write
+    there clobbers O and the between-sweeps exchange kept in buffer 0), sweep
+    2 keeps S_1 in buffer 2 (also the epilogue's exchange) and S_2 in 3.
+    """
+    items = [T] if items is None else items
     W = World(seed)
     nown = 2 if per_owner_full else 1
     full = [[Bar(1) for _ in range(nslot)] for _ in range(nown)]
     empty = [Bar(1) for _ in range(nslot)]
     s1_full = [Bar(1) for _ in range(4)]
     s1_free = [Bar(1) for _ in range(4)]
-    a2_full, b2_full, a2_free, b2_free = Bar(1), Bar(1), Bar(1), Bar(1)
-    p_ready, pv_done, o_full, w2_done = Bar(1), Bar(1), Bar(1), Bar(1)
-    xchg = Bar(2)
+    # sweep 2: both softmax agents (all warpgroups in the kernel) load S_1 / S_2
+    # and write their part of P: free and ready barriers count both
+    a2_full, b2_full, a2_free, b2_free = Bar(1), Bar(1), Bar(2), Bar(2)
+    p_ready, pv_done, o_full = Bar(2), Bar(1), Bar(1)
+    q_full, q_free, o_free = Bar(1), Bar(2), Bar(2)
+    xchg = Bar(2)   # the softmax agents' rendezvous (named barrier)
+    W.q = None
+    W.tmem = {}
+
+    def tm_write(buf, tag):
+        W.tmem[buf] = tag
+        if buf in (0, 1):            # O and the exchange columns live in buffers 0 and 1
+            W.tmem["O"] = ("clobbered", tag)
+            if buf == 0:
+                W.tmem["X"] = ("clobbered", tag)
+        if buf == 2:
+            W.tmem["AX"] = ("clobbered", tag)
+
     fills = []  # (tag, owner)
-    for j in range(T):
-        fills += [(("K1", j), 0), (("K2", j), 1)]
-    fills += [(("K2", 0), 1), (("K1", 0), 0)]
-    for j in range(T):
-        if j + 1 < T:
-            fills += [(("K2", j + 1), 1), (("K1", j + 1), 0)]
-        fills += [(("V", j, p), 0) for p in range(vf)]
+    for it, Ti in enumerate(items):
+        for j in range(Ti):
+            fills += [(("K1", it, j), 0), (("K2", it, j), 1)]
+        fills += [(("K2", it, 0), 1), (("K1", it, 0), 0)]
+        for j in range(Ti):
+            if j + 1 < Ti:
+                fills += [(("K2", it, j + 1), 1), (("K1", it, j + 1), 0)]
+            fills += [(("V", it, j, p), 0) for p in range(vf)]
 
     def producer():
-        for f, (tag, o) in enumerate(fills):
-            s, use = f % nslot, f // nslot
-            if use:
-                yield from W.wait(empty[s], (use - 1) & 1)
-            W.tma.append((s, tag, full[o if per_owner_full else 0][s]))
+        f = 0
+        for it, Ti in enumerate(items):
+            if it:
+                yield from W.wait(q_free, (it - 1) & 1)
+
+            class QLoad:
+                def arrive(self, it=it):
+                    W.q = it
+                    q_full.arrive()
+            W.tma.append(("Q", it, QLoad()))
+            for _ in range(Ti * (4 + vf)):
+                tag, o = fills[f]
+                s, use = f % nslot, f // nslot
+                if use:
+                    yield from W.wait(empty[s], (use - 1) & 1)
+                W.tma.append((s, tag, full[o if per_owner_full else 0][s]))
+                f += 1
 
     def mma(mw):
         ph = 0  # per-slot parity bits of this warp's own fills (per-owner barriers)
-        my = [f for f, (_, o) in enumerate(fills) if o == mw]
-        it = iter(my)
+        it_f = iter([f for f, (_, o) in enumerate(fills) if o == mw])
 
         def acquire():
             nonlocal ph
-            f = next(it)
+            f = next(it_f)
             s = f % nslot
             if per_owner_full:
                 par = (ph >> s) & 1
@@ -299,79 +334,112 @@ def twopass(T, seed, nslot=4, vf=2, per_owner_full=True):
             W.expect(W.slot, s, fills[f][0], f"warp {mw + 1} acquire")
             return s, fills[f][0]
 
-        def qk(buf, s, tag, what):
+        def qk(buf, s, tag, what, it):
             def go():
                 W.expect(W.slot, s, tag, what)
-                W.tmem[buf] = what
+                if W.q != it:
+                    W.errors.append(f"{what} read Q of item {W.q}, wanted {it}")
+                tm_write(buf, what)
             W.mma(mw, go)
 
         use = {0: 0, 1: 0, 2: 0, 3: 0}
-        for j in range(T):
-            k = 2 * j + mw
-            bb = k & 3
-            s, tag = yield from acquire()
-            if use[bb]:
-                yield from W.wait(s1_free[bb], (use[bb] - 1) & 1)
-            use[bb] += 1
-            qk(("S1buf", bb), s, tag, ("sw1", k))
-            W.commit(mw, s1_full[bb])
-            W.commit(mw, empty[s])
-        if use[mw + 2]:
-            yield from W.wait(s1_free[mw + 2], (use[mw + 2] - 1) & 1)
         sfull, sfree = (a2_full, a2_free) if mw == 0 else (b2_full, b2_free)
-        s, tag = yield from acquire()
-        qk(("S1buf", mw + 2), s, tag, ("sw2", mw, 0))
-        W.commit(mw, sfull)
-        W.commit(mw, empty[s])
-        for j in range(T):
-            if j + 1 < T:
+        g1 = 0
+        for it, Ti in enumerate(items):
+            yield from W.wait(q_full, it & 1)
+            if it and wait_o_free:  # (o_free also follows every sweep-2 read of buffers 2, 3)
+                yield from W.wait(o_free, (it - 1) & 1)
+            for j in range(Ti):
+                k = 2 * (g1 + j) + mw
+                bb = k & 3
                 s, tag = yield from acquire()
-                yield from W.wait(sfree, j & 1)
-                qk(("S1buf", mw + 2), s, tag, ("sw2", mw, j + 1))
-                W.commit(mw, sfull)
+                if use[bb]:
+                    yield from W.wait(s1_free[bb], (use[bb] - 1) & 1)
+                use[bb] += 1
+                qk(bb, s, tag, ("sw1", k), it)
+                W.commit(mw, s1_full[bb])
                 W.commit(mw, empty[s])
+            if use[mw + 2]:
+                yield from W.wait(s1_free[mw + 2], (use[mw + 2] - 1) & 1)
+            s, tag = yield from acquire()
+            qk(mw + 2, s, tag, ("sw2", mw, g1), it)
+            W.commit(mw, sfull)
+            W.commit(mw, empty[s])
+            if Ti == 1:
+                W.commit(mw, q_free)
+            for j in range(Ti):
+                g = g1 + j
+                if j + 1 < Ti:
+                    s, tag = yield from acquire()
+                    yield from W.wait(sfree, g & 1)
+                    qk(mw + 2, s, tag, ("sw2", mw, g + 1), it)
+                    W.commit(mw, sfull)
+                    W.commit(mw, empty[s])
+                    if j + 2 == Ti:
+                        W.commit(mw, q_free)
+                if mw == 0:
+                    sv = []
+                    for _ in range(vf):
+                        sv.append((yield from acquire()))
+                    yield from W.wait(p_ready, g & 1)
+                    for i, (s_, tag_) in enumerate(sv):  # the MMAs of one V part, then its release
+                        def pv(s_=s_, tag_=tag_, g=g, it=it, j=j):
+                            W.expect(W.slot, s_, tag_, f"PV({g}) reads V")
+                            W.expect(W.pbuf, 0, g, f"PV({g}) reads P of agent 0")
+                            W.expect(W.pbuf, 1, g, f"PV({g}) reads P of agent 1")
+                            W.tmem[0] = W.tmem[1] = ("O", it, j)
+                            W.tmem["O"] = (it, j)
+                            W.tmem["X"] = ("clobbered by PV", it)
+                        W.mma(mw, pv)
+                        if i + 1 < len(sv):
+                            W.commit(mw, empty[s_])
+                    W.commit(mw, pv_done)
+                    W.commit(mw, empty[sv[-1][0]])
             if mw == 0:
-                sv = []
-                for _ in range(vf):
-                    sv.append((yield from acquire()))
-                yield from W.wait(p_ready, j & 1)
-
-                for i, (s_, tag_) in enumerate(sv):  # the MMAs of one V part, then its release
-                    def pv(s_=s_, tag_=tag_, j=j):
-                        W.expect(W.slot, s_, tag_, f"PV({j}) reads V")
-                        W.expect(W.pbuf, 0, j, f"PV({j}) reads P")
-                        W.tmem[("O",)] = j
-                    W.mma(mw, pv)
-                    if i + 1 < len(sv):
-                        W.commit(mw, empty[s_])
-                W.commit(mw, pv_done)
-                W.commit(mw, empty[sv[-1][0]])
-        W.commit(mw, o_full if mw == 0 else w2_done)
+                W.commit(mw, o_full)
+            g1 += Ti
 
     def softmax(m):
-        for j in range(T):
-            k = 2 * j + m
-            bb = k & 3
-            yield from W.wait(s1_full[bb], (k >> 2) & 1)
-            W.expect(W.tmem, ("S1buf", bb), ("sw1", k), f"sweep-1 softmax {m} reads S")
-            s1_free[bb].arrive()
-        xchg.arrive()
-        yield from W.wait(xchg, 0)
-        if m == 1:
-            yield from W.wait(o_full, 0)
-            return
-        for j in range(T):
-            yield from W.wait(b2_full, j & 1)
-            W.expect(W.tmem, ("S1buf", 3), ("sw2", 1, j), "sweep-2 softmax reads S2")
-            b2_free.arrive()
-            yield from W.wait(a2_full, j & 1)
-            W.expect(W.tmem, ("S1buf", 2), ("sw2", 0, j), "sweep-2 softmax reads S1")
-            a2_free.arrive()
-            if j:
-                yield from W.wait(pv_done, (j - 1) & 1)
-            W.pbuf[0] = j
-            p_ready.arrive()
-        yield from W.wait(o_full, 0)
+        g1 = 0
+        nx = 0  # rendezvous uses so far
+        for it, Ti in enumerate(items):
+            for j in range(Ti):
+                k = 2 * (g1 + j) + m
+                bb = k & 3
+                yield from W.wait(s1_full[bb], (k >> 2) & 1)
+                W.expect(W.tmem, bb, ("sw1", k), f"sweep-1 softmax {m} reads S")
+                s1_free[bb].arrive()
+            # exchange through buffer 0's first columns, between two rendezvous
+            xchg.arrive()
+            yield from W.wait(xchg, nx & 1)
+            nx += 1
+            W.tmem["X"] = ("x", it)
+            xchg.arrive()
+            yield from W.wait(xchg, nx & 1)
+            nx += 1
+            W.expect(W.tmem, "X", ("x", it), f"softmax {m} reads the exchange")
+            for j in range(Ti):
+                g = g1 + j
+                yield from W.wait(b2_full, g & 1)
+                W.expect(W.tmem, 3, ("sw2", 1, g), f"sweep-2 softmax {m} reads S2")
+                b2_free.arrive()
+                yield from W.wait(a2_full, g & 1)
+                W.expect(W.tmem, 2, ("sw2", 0, g), f"sweep-2 softmax {m} reads S1")
+                a2_free.arrive()
+                if g:
+                    yield from W.wait(pv_done, (g - 1) & 1)
+                W.pbuf[m] = g
+                p_ready.arrive()
+            yield from W.wait(o_full, it & 1)
+            W.expect(W.tmem, "O", (it, Ti - 1), f"epilogue {m} reads O of item {it}")
+            W.tmem["AX"] = ("ss", it)         # the sums of squares through buffer 2
+            xchg.arrive()
+            yield from W.wait(xchg, nx & 1)
+            nx += 1
+            W.expect(W.tmem, "AX", ("ss", it), f"epilogue {m} reads the exchange in A")
+            W.expect(W.tmem, "O", (it, Ti - 1), f"epilogue {m} reads O of item {it} again")
+            o_free.arrive()
+            g1 += Ti
 
     return W.run({"prod": producer(), "w1": mma(0), "w2": mma(1), "sm0": softmax(0), "sm1": softmax(1)})
 
@@ -435,6 +503,17 @@ def test_model_catches_missing_q_free_and_o_free():
         bad = [ns["onepass"](0, seed, nslot=7, psm=True, shared_k=False, items=it)
                for it in ([3, 1], [2, 5, 1, 3]) for seed in range(30)]
         assert any(r != "ok" for r in bad), what
+
+
+@pytest.mark.parametrize("items", ITEM_LISTS)
+def test_twopass_persistent(items):
+    for seed in range(20):
+        assert twopass(0, seed, items=items) == "ok", seed
+
+
+def test_model_catches_missing_twopass_o_free():
+    bad = [twopass(0, seed, items=it, wait_o_free=False) for it in ([3, 1], [1, 2, 1], [2, 5, 1]) for seed in range(40)]
+    assert any(r != "ok" for r in bad)
 
 
 def test_model_catches_shared_full_barriers_with_partial_waiters():
