@@ -85,6 +85,10 @@ V1_SMALL = [
     ("bf16", 1, 1, 640, 128, True, "ones"),
     ("bf16", 1, 2, 1100, 64, True, "uniform"),  # up to 9 key tiles: every ring / double-buffer phase recurs
     ("bf16", 1, 1, 1100, 128, False, "uniform"),
+    # more work items than SMs: persistent CTAs walk several items each
+    ("bf16", 2, 128, 300, 64, True, "uniform"),
+    ("bf16", 2, 64, 300, 128, True, "uniform"),
+    ("bf16", 1, 24, 1100, 64, True, "ones"),
     ("f32", 1, 1, 128, 64, True, "ones"),
     ("f32", 2, 3, 77, 32, False, "uniform"),
     ("f32", 1, 2, 150, 128, True, "uniform"),
