@@ -520,10 +520,28 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
       }
 
       // ---- epilogue: out = O_1 / l_1 - c O_2 / l_2; warpgroup (map, half)
-      // owns channels [32 cb, +32)
+      // owns channels [32 cb, +32).  The row sums are final after the last
+      // tile; the persistent form exchanges them while the last PVs still
+      // run (one CTA per item measured better with the exchange after o_full).
+      float* lp = lpart + (k & 1) * 512;
+      float l1 = 0.f, l2 = 0.f;
+      auto exchange_l = [&]() {
+        lp[cb * 128 + row] = l;
+        named_bar_sync(1, 128 * C::NSMWG);
+        l1 = lp[row] + lp[128 + row];
+        l2 = lp[256 + row] + lp[384 + row];
+      };
+      if constexpr (PERSIST) exchange_l();
       mbar_wait(o_full, static_cast<uint32_t>(k) & 1u, ab);
       __syncwarp();
       tc_fence_after();
+      if constexpr (!PERSIST) exchange_l();
+      float coef = lam;
+      if (EPI == kEpiV2) {
+        const float lg = (t < p.n) ? p.lam_logits[c.b * p.sb + static_cast<long long>(t) * p.st + c.u] : 0.f;
+        coef = 1.f / (1.f + expf(-lg));
+      }
+      const float a1 = 1.f / l1, a2 = -coef / l2;
       float y[32];
       {
         uint32_t o1[32], o2[32];
@@ -537,16 +555,6 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
           if (lane == 0) mbar_arrive(o_free);
           __syncwarp();
         }
-        float* lp = lpart + (k & 1) * 512;
-        lp[cb * 128 + row] = l;
-        named_bar_sync(1, 128 * C::NSMWG);
-        const float l1 = lp[row] + lp[128 + row], l2 = lp[256 + row] + lp[384 + row];
-        float coef = lam;
-        if (EPI == kEpiV2) {
-          const float lg = (t < p.n) ? p.lam_logits[c.b * p.sb + static_cast<long long>(t) * p.st + c.u] : 0.f;
-          coef = 1.f / (1.f + expf(-lg));
-        }
-        const float a1 = 1.f / l1, a2 = -coef / l2;
 #pragma unroll
         for (int cc = 0; cc < 32; ++cc) y[cc] = fmaf(__uint_as_float(o2[cc]), a2, __uint_as_float(o1[cc]) * a1);
       }
