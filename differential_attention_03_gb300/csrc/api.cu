@@ -102,9 +102,10 @@ diffattn_status get_encoder(EncodeTiledFn* fn) {
   return DIFFATTN_OK;
 }
 
-// 4-D map over a BSHD bf16 tensor [B, n, heads, W]; box = 64 columns x 1 head
-// x `rows` tokens x 1 batch, 128-byte swizzle; reads past n return zeros.
-diffattn_status make_map(CUtensorMap* m, const void* base, int B, int n, int heads, int W, int rows) {
+// 4-D map over a BSHD bf16 tensor [B, n, heads, W]; box = `cols` columns x 1
+// head x `rows` tokens x 1 batch, the swizzle as wide as a box row (64 or 128
+// bytes); loads past n return zeros, stores past n are dropped.
+diffattn_status make_map_box(CUtensorMap* m, const void* base, int B, int n, int heads, int W, int cols, int rows) {
   EncodeTiledFn enc;
   diffattn_status s = get_encoder(&enc);
   if (s != DIFFATTN_OK) return s;
@@ -112,13 +113,19 @@ diffattn_status make_map(CUtensorMap* m, const void* base, int B, int n, int hea
                               static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(W) * 2, static_cast<cuuint64_t>(W) * heads * 2,
                                  static_cast<cuuint64_t>(W) * heads * n * 2};
-  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(rows), 1};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(cols), 1, static_cast<cuuint32_t>(rows), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle sw = (cols * 2 == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(DIFFATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
   return DIFFATTN_OK;
+}
+
+// Load maps: 64-column boxes (128-byte rows, 128-byte swizzle).
+diffattn_status make_map(CUtensorMap* m, const void* base, int B, int n, int heads, int W, int rows) {
+  return make_map_box(m, base, B, n, heads, W, 64, rows);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -213,6 +220,8 @@ diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d, 
   if ((st = make_map(&p.tm_k1, k1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
   if ((st = make_map(&p.tm_k2, k2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
   if ((st = make_map(&p.tm_v, v, B, n, H, dv, 64)) != DIFFATTN_OK) return st;
+  // Output stores: one box per softmax warpgroup (a quarter of the channels).
+  if ((st = make_map_box(&p.tm_out, out, B, n, H, dv, dv / 4, 128)) != DIFFATTN_OK) return st;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lambda = lambda;
   p.gamma = gamma;
@@ -304,6 +313,7 @@ diffattn_status diffattn_v2_forward(diffattn_dtype dt, int B, int Hq, int Hkv, i
   if ((st = make_map(&p.tm_k1, k, B, n, Hkv, d, 128)) != DIFFATTN_OK) return st;
   p.tm_k2 = p.tm_k1;
   if ((st = make_map(&p.tm_v, v, B, n, Hkv, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_box(&p.tm_out, out, B, n, G, d, d / 4, 128)) != DIFFATTN_OK) return st;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lam_logits = lam_logits;
   p.sb = sb;

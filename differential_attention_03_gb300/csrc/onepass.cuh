@@ -109,7 +109,26 @@ struct OnePassCfg {
   static_assert(V_TILE % SLOT == 0 && (VF == 1 || VF == 2), "value tile split");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(NSLOT >= 4, "ring depth");
+  // Output staging of the one-item form (128 rows x 32 channels, 64-byte
+  // rows, 64-byte swizzle) for warpgroup (r, h): the first half of its P box
+  // when P is in shared memory, else a quarter of the Q buffers.
+  static constexpr int STG_BYTES = BM * 64;
+  static_assert(PSM || 2 * Q_TILE >= 4 * STG_BYTES, "output staging in the Q buffers");
 };
+
+// 32 output channels of one row: y * rinv (* gamma), rounded to bf16 pairs.
+template <bool GAMMA>
+__device__ __forceinline__ void pack_out_row(const float (&y)[32], float rinv, const float* g, uint32_t (&wv)[16]) {
+#pragma unroll
+  for (int cc = 0; cc < 32; cc += 2) {
+    float y0 = y[cc] * rinv, y1 = y[cc + 1] * rinv;
+    if (GAMMA) {
+      y0 *= g[cc];
+      y1 *= g[cc + 1];
+    }
+    wv[cc >> 1] = pack_bf16x2(y0, y1);
+  }
+}
 
 template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST>
 __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
@@ -573,28 +592,48 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
         const float tot = (sp[row] + sp[128 + row]) + (sp[256 + row] + sp[384 + row]);
         rinv = p.norm_mult * rsqrtf(tot * (1.f / DV) + p.eps);
       }
-      if (t < p.n) {
-        __nv_bfloat16* orow =
-            p.out + ((static_cast<size_t>(c.b) * p.n + t) * p.units_per_batch + c.u) * DV + 32 * cb;
-        uint32_t wv[16];
+      if constexpr (PERSIST) {
+        // Row stores straight from registers: they drain while the next
+        // item starts (staging them for a TMA store put a warpgroup barrier
+        // and a proxy fence on the item transition, measured slower).
+        if (t < p.n) {
+          __nv_bfloat16* orow =
+              p.out + ((static_cast<size_t>(c.b) * p.n + t) * p.units_per_batch + c.u) * DV + 32 * cb;
+          uint32_t wv[16];
+          pack_out_row<EPI == kEpiRmsNorm>(y, rinv, sgamma + 32 * cb, wv);
+          uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-        for (int cc = 0; cc < 32; cc += 2) {
-          float y0 = y[cc] * rinv, y1 = y[cc + 1] * rinv;
-          if (EPI == kEpiRmsNorm) {
-            y0 *= sgamma[32 * cb + cc];
-            y1 *= sgamma[32 * cb + cc + 1];
-          }
-          wv[cc >> 1] = pack_bf16x2(y0, y1);
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
         }
-        uint4* dst = reinterpret_cast<uint4*>(orow);
+      } else {
+        // One item per CTA: the warpgroup's 128 x 32 block goes through
+        // shared memory (16-byte chunk v of row `row` at v ^ ((row / 2) % 4):
+        // the 64-byte swizzle) and one TMA store, which drops rows past n
+        // (row stores, one row per thread and 4 KB apart, queue up in the
+        // load/store unit at the end of the CTA).  The staging is free: the
+        // item's MMAs have completed (o_full) and no other item follows.
+        uint32_t wv[16];
+        pack_out_row<EPI == kEpiRmsNorm>(y, rinv, sgamma + 32 * cb, wv);
+        uint8_t* const stg =
+            smem + (PSM ? C::OFF_P + map * C::P_TILE + half * (BM * 128) : C::OFF_Q1 + cb * C::STG_BYTES);
+        uint8_t* srow = stg + row * 64;
 #pragma unroll
-        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+        for (int v = 0; v < 4; ++v)
+          *reinterpret_cast<uint4*>(srow + ((v ^ ((row >> 1) & 3)) << 4)) =
+              make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+        fence_proxy_async_smem();
+        named_bar_sync(4 + cb, 128);
+        if ((threadIdx.x & 127) == 96) {  // lane 0 of the warpgroup's first warp
+          tma_store_4d(&p.tm_out, stg, 32 * cb, c.u, c.q0, c.b);
+          bulk_commit_group();
+        }
       }
       gt += static_cast<uint32_t>(T);
     }
   }
 
   // ---- teardown
+  if (!PERSIST && warp >= C::NCTRL && (threadIdx.x & 127) == 96) bulk_wait_all();  // output store
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

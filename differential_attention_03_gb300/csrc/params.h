@@ -28,6 +28,7 @@ struct TwoPassParams {
   int num_q_tiles;
   int order;  // 0: unit-major tile order, 1: query-tile-major
   int* status;
+  CUtensorMap tm_out;  // output [B, n, units_per_batch, DV] for TMA stores
 };
 
 // What work item `idx` of a tcgen05 launch computes: batch b, unit u (V1:

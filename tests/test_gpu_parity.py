@@ -192,6 +192,59 @@ def test_v1_full_size_sampled(wid):
         assert err <= TOL[w.dtype], f"workload {wid} batch {b}: max abs error {err}"
 
 
+def _spread_scores(x, names, n, seed):
+    # Per-row query scales from 0.1 to 12 and a block of keys scaled by 8 late in
+    # the sequence: row maxima differ by hundreds (exp2 units) and jump within
+    # a row, so a reference maximum taken over the wrong values overflows or
+    # underflows the exponentials.
+    g = torch.Generator().manual_seed(seed)
+    rs = (torch.rand(n, generator=g) * 11.9 + 0.1).to(x[names[0]].device)
+    for k in names:
+        x[k] = (x[k].float() * rs.view(1, -1, 1, 1)).to(x[k].dtype)
+    return x
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_v1_wide_score_range(d):
+    w = shrink(WORKLOADS[2], B=1, H=2, n=700, d=d, causal=True, gamma="uniform", layer=3, seed=41)
+    x = _spread_scores(make_v1(w, "cuda"), ("q1", "q2"), w.n, 41)
+    for k in ("k1", "k2"):
+        x[k][:, 520:540] = (x[k][:, 520:540].float() * 8).to(x[k].dtype)
+    out, _ = _v1_gpu(x, w)
+    ref = _v1_oracle(x, w)
+    err = _err(_np(out), ref)
+    # Near one-hot rows put outputs up to a few units, where the bf16 output
+    # rounding alone is ~1e-2: the bound scales with the output's magnitude.
+    scale = max(1.0, float(np.max(np.abs(ref))))
+    assert err <= TOL["bf16"] * scale, f"max abs error {err} (output scale {scale})"
+
+
+def test_v2_wide_score_range():
+    w = shrink(WORKLOADS[5], B=1, Hq=4, Hkv=2, n=700, causal=True, seed=43)
+    x = _spread_scores(make_v2(w, "cuda"), ("q",), w.n, 43)
+    x["k"][:, 520:540] = (x["k"][:, 520:540].float() * 8).to(x["k"].dtype)
+    out = da.diffattn_v2_forward(x["q"], x["k"], x["v"], x["lam_logits"], causal=True)
+    da.device_status()
+    lg_host = np.broadcast_to(x["lam_logits"].cpu().double().numpy(), (w.B, w.n, w.Hq // 2))
+    ref = oracle.diff_attn_v2(x["q"], x["k"], x["v"], lg_host, True)
+    err = _err(_np(out), ref)
+    scale = max(1.0, float(np.max(np.abs(ref))))
+    assert err <= TOL["bf16"] * scale, f"max abs error {err} (output scale {scale})"
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_v1_d64_long_items_sampled(causal):
+    # More than 64 query tiles per head: the d = 64 kernel runs one CTA per
+    # work item instead of the persistent schedule (ragged tail: n % 128 = 108).
+    w = shrink(WORKLOADS[2], B=1, H=2, n=8300, causal=causal, layer=3, seed=31)
+    x = make_v1(w, "cuda")
+    out, _ = _v1_gpu(x, w)
+    rows = _sample_rows(w.n, 24, 31)
+    ref = _v1_oracle(x, w, rows=rows)
+    err = _err(_np(out[:, rows]), ref)
+    assert err <= TOL["bf16"], f"max abs error {err}"
+
+
 def test_v2_full_size_sampled():
     w = WORKLOADS[5]
     x = make_v2(w, "cuda")
