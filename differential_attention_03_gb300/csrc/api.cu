@@ -220,8 +220,8 @@ diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d, 
   if ((st = make_map(&p.tm_k1, k1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
   if ((st = make_map(&p.tm_k2, k2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
   if ((st = make_map(&p.tm_v, v, B, n, H, dv, 64)) != DIFFATTN_OK) return st;
-  // Output stores: one box per softmax warpgroup (a quarter of the channels).
-  if ((st = make_map_box(&p.tm_out, out, B, n, H, dv, dv / 4, 128)) != DIFFATTN_OK) return st;
+  // Output stores: boxes of 128 tokens x 32 channels.
+  if ((st = make_map_box(&p.tm_out, out, B, n, H, dv, 32, 128)) != DIFFATTN_OK) return st;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lambda = lambda;
   p.gamma = gamma;
@@ -313,7 +313,7 @@ diffattn_status diffattn_v2_forward(diffattn_dtype dt, int B, int Hq, int Hkv, i
   if ((st = make_map(&p.tm_k1, k, B, n, Hkv, d, 128)) != DIFFATTN_OK) return st;
   p.tm_k2 = p.tm_k1;
   if ((st = make_map(&p.tm_v, v, B, n, Hkv, d, 128)) != DIFFATTN_OK) return st;
-  if ((st = make_map_box(&p.tm_out, out, B, n, G, d, d / 4, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_box(&p.tm_out, out, B, n, G, d, 32, 128)) != DIFFATTN_OK) return st;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lam_logits = lam_logits;
   p.sb = sb;

@@ -108,6 +108,10 @@ struct TwoPassCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(NSLOT >= VF + 2, "ring depth");
   static_assert(!SHARED_K, "the two MMA warps consume separate K_1 / K_2 fills");
+  // Output staging per softmax warpgroup: 128 rows x 32 channels (64-byte
+  // rows) in a quarter of the P buffer.
+  static constexpr int STG_BYTES = BM * 64;
+  static_assert(4 * STG_BYTES <= P_TILE && (DV / 4) % 32 == 0, "output staging");
   static constexpr int MAX_ITEMS = PERSIST ? 0x7fffffff : 1;  // work items per CTA
   static constexpr int FILLS_PER_TILE = 4 + VF;               // ring fills of an item with T key tiles: T * this
 };
@@ -516,6 +520,10 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
       // sweep-1 reads finish first; the next writes to buffer 0 are this
       // item's PV (after every warp has read the exchange) and, after o_free,
       // the next item's S.
+      // The previous item's output stores staged in P: their issuing threads
+      // (lane 0 of each warpgroup's first warp) wait for the reads before
+      // this barrier, which every sweep-2 write of P follows.
+      if ((threadIdx.x & 127) == 0) bulk_wait_read_all();
       tc_fence_before();
       named_bar_sync(1, 128 * C::NSMWG);
       tc_fence_after();
@@ -636,8 +644,6 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
                           (__uint_as_float(q4[2]) + __uint_as_float(q4[3]));
         rinv = p.norm_mult * rsqrtf(tot * (1.f / DV) + p.eps);
       }
-      __nv_bfloat16* orow =
-          p.out + ((static_cast<size_t>(c.b) * p.n + t) * p.units_per_batch + c.u) * DV + wg * QW;
       uint32_t w[QW / 2];
 #pragma unroll
       for (int ch = 0; ch < QW / 32; ++ch) {
@@ -663,16 +669,38 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
         if (lane == 0) mbar_arrive(o_free);
         __syncwarp();
       }
-      if (t < p.n) {
-        uint4* dst = reinterpret_cast<uint4*>(orow);
+      // The warpgroup's 128 x QW block goes out in 128 x 32 rounds through its
+      // quarter of the P buffer (free from the item's last PV until the next
+      // item's sweep 2; 64-byte rows, 64-byte swizzle: 16-byte chunk v of row
+      // `row` at v ^ ((row / 2) % 4)), each round one TMA store, which drops
+      // rows past n.  (Row stores from registers, one row per thread and rows
+      // DV * units * 2 bytes apart, took ~7k cycles per item.)
+      {
+        uint8_t* const srow = smem + C::OFF_P + wg * C::STG_BYTES + row * 64;
 #pragma unroll
-        for (int v = 0; v < QW / 8; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        for (int rd = 0; rd < QW / 32; ++rd) {
+          if (rd > 0) {
+            if ((threadIdx.x & 127) == 0) bulk_wait_read_all();  // the previous round has read the staging
+            named_bar_sync(2 + wg, 128);
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            *reinterpret_cast<uint4*>(srow + ((v ^ ((row >> 1) & 3)) << 4)) =
+                make_uint4(w[16 * rd + 4 * v], w[16 * rd + 4 * v + 1], w[16 * rd + 4 * v + 2], w[16 * rd + 4 * v + 3]);
+          fence_proxy_async_smem();
+          named_bar_sync(2 + wg, 128);
+          if ((threadIdx.x & 127) == 0) {
+            tma_store_4d(&p.tm_out, smem + C::OFF_P + wg * C::STG_BYTES, wg * QW + 32 * rd, c.u, c.q0, c.b);
+            bulk_commit_group();
+          }
+        }
       }
       g1 += static_cast<uint32_t>(T);
     }
   }
 
   // ---- teardown
+  if (warp >= 4 && (warp & 3) == 0 && lane == 0) bulk_wait_all();  // output stores
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
