@@ -115,10 +115,11 @@ class ClockSampler:
                 out = subprocess.run(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
                                       "--format=csv,noheader,nounits"], capture_output=True, text=True,
                                      timeout=10).stdout
+                stamp = time.perf_counter()
                 for line in out.splitlines():
                     parts = [x.strip() for x in line.split(",")]
                     if len(parts) >= 7:
-                        self.rows.append(parts)
+                        self.rows.append((stamp, parts))
             except Exception as e:  # noqa: BLE001
                 self.error = str(e)
                 return
@@ -127,11 +128,19 @@ class ClockSampler:
     def start(self):
         self.thread.start()
 
-    def stop(self):
+    def stop(self, window=None):
+        """Summary of the samples taken inside `window` = (t0, t1) (perf_counter seconds), the
+        timed region; of every sample if none fell inside it."""
         self.stop_evt.set()
         self.thread.join(timeout=15)
+        rows = self.rows
+        scope = "whole run"
+        if window is not None:
+            inside = [r for r in rows if window[0] <= r[0] <= window[1]]
+            if inside:
+                rows, scope = inside, "timed region"
         sm, mx, reasons = [], [], set()
-        for parts in self.rows:
+        for _, parts in rows:
             try:
                 sm.append(float(parts[0]))
                 mx.append(float(parts[1]))
@@ -144,7 +153,7 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [self.error or "no samples"], "samples": 0}
         loaded = [x for x in sm if x > 0.5 * max(sm)] or sm
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "scope": scope}
 
 
 # --------------------------------------------------------------------------- our path
@@ -191,7 +200,7 @@ def time_device(w, x, da, steps, warmup, flush, dist=None):
     # the host to enqueue every timed step, so that the events see device time
     # only, not gaps while Python marshals the next call.
     torch.cuda._sleep(int(min(2e9, 3.0e9 * host_per_step * steps + 2e6)))
-    t0 = time.perf_counter()
+    t0 = time.perf_counter()  # the device sleep above belongs to the timed region's clock window
     for k in range(steps):
         flush.zero_()
         ev[k][0].record(stream)
@@ -208,7 +217,8 @@ def time_device(w, x, da, steps, warmup, flush, dist=None):
     step_ms = [a.elapsed_time(c) for a, b, c in ev]
     kern_ms = [b.elapsed_time(c) for a, b, c in ev]
     return {"step_ms": sum(step_ms) / steps, "kernel_ms": sum(kern_ms) / steps,
-            "kernel_ms_median": statistics.median(kern_ms), "wall_s": wall, "launches": launches, "out": out}
+            "kernel_ms_median": statistics.median(kern_ms), "wall_s": wall, "launches": launches, "out": out,
+            "window": (t0, t0 + wall)}
 
 
 def time_e2e(w, x, da, steps):
@@ -325,7 +335,7 @@ def run_ours(args):
     sampler.start()  # polls from before the warm-up to the end of the timed steps
     x = inputs(w)
     res = time_device(w, x, da, args.steps, args.warmup, flush, dist)
-    clocks = sampler.stop()
+    clocks = sampler.stop(res["window"])
     step_ms = torch.tensor([res["step_ms"], res["kernel_ms"]], device="cuda", dtype=torch.float64)
     if dist is not None:
         dist.all_reduce(step_ms, op=tdist.ReduceOp.MAX)
@@ -431,7 +441,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
