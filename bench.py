@@ -222,22 +222,45 @@ def time_device(w, x, da, steps, warmup, flush, dist=None):
 
 
 def time_e2e(w, x, da, steps):
-    """End-to-end through the public API: pinned host inputs -> device -> forward -> host output."""
-    import torch
-    host = {k: t.cpu().pin_memory() for k, t in x.items()}
-    dev = {k: torch.empty_like(t) for k, t in x.items()}
-    lam_call, fwd_call, out = make_step(w, dev, da)
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out.numel() * out.element_size()
-    stream = torch.cuda.current_stream()
+    """End to end through the C ABI with host buffers.
 
-    def one():
-        for k in host:
-            dev[k].copy_(host[k], non_blocking=True)
-        lam_call()
-        fwd_call()
-        out_host.copy_(out, non_blocking=True)
+    V1: diffattn_forward_host takes the step's inputs in page-locked host
+    memory and returns the output there (copies in, forward and copies out
+    pipelined over batch chunks inside the library); lambda and gamma are
+    layer parameters resident on the device.  V2: the inputs are copied in
+    and the output back around diffattn_v2_forward.  Every step includes the
+    copies of its inputs and output.
+    """
+    import torch
+    stream = torch.cuda.current_stream()
+    if w.kind == "v1":
+        names = ("q1", "q2", "k1", "k2", "v")
+        host = {k: x[k].cpu().pin_memory() for k in names}
+        lam = torch.empty(1, device=x["q1"].device, dtype=torch.float32)
+        lin = da.lambda_init(w.layer)
+        out_host = torch.empty(x["v"].shape, dtype=x["v"].dtype).pin_memory()
+        ws = torch.empty(da.forward_host_workspace_bytes(x["q1"].dtype, w.B, w.H, w.n, w.d), dtype=torch.uint8,
+                         device=x["q1"].device)
+
+        def one():
+            da.lambda_reparam(x["lq1"], x["lk1"], x["lq2"], x["lk2"], lin, out=lam)
+            da.diffattn_forward_host(host["q1"], host["q2"], host["k1"], host["k2"], host["v"], lam, lin,
+                                     gamma=x["gamma"], causal=w.causal, out=out_host, workspace=ws)
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+    else:
+        host = {k: t.cpu().pin_memory() for k, t in x.items()}
+        dev = {k: torch.empty_like(t) for k, t in x.items()}
+        _, fwd_call, out = make_step(w, dev, da)
+        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+        def one():
+            for k in host:
+                dev[k].copy_(host[k], non_blocking=True)
+            fwd_call()
+            out_host.copy_(out, non_blocking=True)
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out.numel() * out.element_size()
 
     for _ in range(2):
         one()

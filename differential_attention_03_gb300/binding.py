@@ -52,6 +52,11 @@ def lib() -> ctypes.CDLL:
             L.lambda_reparam.restype = i
             L.diffattn_forward.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, f, vp, f, i, vp, vp]
             L.diffattn_forward.restype = i
+            L.diffattn_forward_host_workspace.argtypes = [i, i, i, i, i]
+            L.diffattn_forward_host_workspace.restype = ctypes.c_size_t
+            L.diffattn_forward_host.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, f, vp, f, i, vp, vp,
+                                                ctypes.c_size_t, vp]
+            L.diffattn_forward_host.restype = i
             L.diffattn_v2_forward.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, ll, ll, f, i, vp, vp]
             L.diffattn_v2_forward.restype = i
             L.diffattn_device_status.argtypes = [vp]
@@ -137,6 +142,56 @@ def diffattn_forward(q1, q2, k1, k2, v, lam, lambda_init_value: float, gamma=Non
     _check(lib().diffattn_forward(_dt(q1), B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v),
                                   _ptr(lam), float(lambda_init_value), _ptr(gamma), float(eps),
                                   1 if causal else 0, _ptr(out), _stream(stream)))
+    return out
+
+
+def _need_host(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def forward_host_workspace_bytes(dtype, B: int, H: int, n: int, d: int) -> int:
+    """Device workspace (bytes) that diffattn_forward_host needs for these sizes."""
+    return int(lib().diffattn_forward_host_workspace(BF16 if dtype == torch.bfloat16 else F32, B, H, n, d))
+
+
+def diffattn_forward_host(q1, q2, k1, k2, v, lam, lambda_init_value: float, gamma=None, eps: float = 1e-5,
+                          causal: bool = True, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """diffattn_forward on HOST tensors (page-locked for asynchronous copies).
+
+    The library copies the inputs in, runs the forward and copies the output
+    back, pipelined over chunks of the batch.  lam / gamma are device tensors
+    (layer parameters); workspace is a device uint8 tensor of at least
+    forward_host_workspace_bytes(...) bytes (allocated here if None).  The host
+    output is complete once `stream` (default: the current stream) has
+    reached this call.
+    """
+    B, n, H, d = q1.shape
+    dt = q1.dtype
+    for name, t in (("q1", q1), ("q2", q2), ("k1", k1), ("k2", k2)):
+        _need_host(t, name, dt, (B, n, H, d))
+    _need_host(v, "v", dt, (B, n, H, 2 * d))
+    _need(lam, "lambda", torch.float32, (1,))
+    if gamma is not None:
+        _need(gamma, "gamma", torch.float32, (2 * d,))
+    if out is None:
+        out = torch.empty((B, n, H, 2 * d), dtype=dt).pin_memory()
+    _need_host(out, "out", dt, (B, n, H, 2 * d))
+    need = forward_host_workspace_bytes(dt, B, H, n, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=lam.device)
+    if not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
+    _check(lib().diffattn_forward_host(_dt(q1), B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v),
+                                       _ptr(lam), float(lambda_init_value), _ptr(gamma), float(eps),
+                                       1 if causal else 0, _ptr(out), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
 
 

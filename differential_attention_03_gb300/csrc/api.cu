@@ -253,6 +253,139 @@ diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d, 
   return ok();
 }
 
+// ---------------------------------------------------------------- host-buffer forward
+namespace {
+
+constexpr int kMaxChunks = 8;
+
+// Copy streams and events of the host-buffer forward, created once per device
+// and reused by every call (enqueueing a call holds the mutex, so calls from
+// several host threads do not interleave their event records).
+struct HostPipe {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, last_out = nullptr;
+  cudaEvent_t in_done[kMaxChunks] = {}, fwd_done[kMaxChunks] = {};
+};
+
+diffattn_status host_pipe(HostPipe** out) {
+  static HostPipe pipes[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DIFFATTN_ERR_CUDA, "device index %d out of range", dev);
+  *out = &pipes[dev];
+  return DIFFATTN_OK;
+}
+
+diffattn_status host_pipe_init(HostPipe& hp) {
+  if (hp.ready) return DIFFATTN_OK;
+  cudaError_t e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.last_out, cudaEventDisableTiming);
+  for (int c = 0; e == cudaSuccess && c < kMaxChunks; ++c) {
+    e = cudaEventCreateWithFlags(&hp.in_done[c], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.fwd_done[c], cudaEventDisableTiming);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward_host: stream/event creation");
+  hp.ready = true;
+  return DIFFATTN_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+
+size_t diffattn_forward_host_workspace(diffattn_dtype dt, int B, int H, int n, int d) {
+  if ((dt != DIFFATTN_F32 && dt != DIFFATTN_BF16) || B < 0 || H < 0 || n < 0 || d < 1) return 0;
+  const size_t es = dt == DIFFATTN_BF16 ? 2 : 4;
+  const size_t qk = static_cast<size_t>(B) * n * H * d * es;  // one of q1, q2, k1, k2
+  const size_t vo = 2 * qk;                                   // v or out
+  return 4 * round256(qk) + 2 * round256(vo);
+}
+
+diffattn_status diffattn_forward_host(diffattn_dtype dt, int B, int H, int n, int d, const void* q1,
+                                      const void* q2, const void* k1, const void* k2, const void* v,
+                                      const float* lambda, float lambda_init, const float* gamma, float eps,
+                                      int causal, void* out, void* workspace, size_t workspace_bytes,
+                                      void* stream) {
+  if (dt != DIFFATTN_F32 && dt != DIFFATTN_BF16)
+    return fail(DIFFATTN_ERR_DTYPE, "diffattn_forward_host: bad dtype %d", (int)dt);
+  if (B < 0 || H < 0 || n < 0 || d < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_forward_host: bad sizes B=%d H=%d n=%d d=%d", B, H, n, d);
+  if (B == 0 || H == 0 || n == 0) return ok();
+  if (!q1 || !q2 || !k1 || !k2 || !v || !lambda || !out || !workspace)
+    return fail(DIFFATTN_ERR_NULL, "diffattn_forward_host: NULL pointer");
+  const size_t need = diffattn_forward_host_workspace(dt, B, H, n, d);
+  if (workspace_bytes < need)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_forward_host: workspace of %zu bytes, %zu needed", workspace_bytes,
+                need);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_forward_host: workspace not 256-byte aligned");
+  HostPipe* hp = nullptr;
+  diffattn_status st = host_pipe(&hp);
+  if (st != DIFFATTN_OK) return st;
+  std::lock_guard<std::mutex> lk(hp->mu);
+  if ((st = host_pipe_init(*hp)) != DIFFATTN_OK) return st;
+
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t es = dt == DIFFATTN_BF16 ? 2 : 4;
+  const size_t qk_b = static_cast<size_t>(n) * H * d * es;  // bytes of one batch of q1 (q2, k1, k2)
+  const size_t vo_b = 2 * qk_b;                             // bytes of one batch of v (out)
+  const size_t qk = round256(qk_b * B), vo = round256(vo_b * B);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* const dq1 = ws;
+  uint8_t* const dq2 = dq1 + qk;
+  uint8_t* const dk1 = dq2 + qk;
+  uint8_t* const dk2 = dk1 + qk;
+  uint8_t* const dv = dk2 + qk;
+  uint8_t* const dout = dv + vo;
+
+  // The copies in wait for the caller's earlier work on `stream` (which
+  // includes the copy out of the previous call on this workspace).
+  cudaError_t e = cudaEventRecord(hp->start, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->in, hp->start, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward_host: stream ordering");
+  const int nchunk = B < kMaxChunks ? B : kMaxChunks;
+  for (int c = 0; c < nchunk; ++c) {
+    const int b0 = static_cast<int>(static_cast<long long>(B) * c / nchunk);
+    const int b1 = static_cast<int>(static_cast<long long>(B) * (c + 1) / nchunk);
+    const size_t oq = qk_b * b0, ov = vo_b * b0;
+    const size_t nq = qk_b * (b1 - b0), nv = vo_b * (b1 - b0);
+    const uint8_t* hq1 = static_cast<const uint8_t*>(q1);
+    const uint8_t* hq2 = static_cast<const uint8_t*>(q2);
+    const uint8_t* hk1 = static_cast<const uint8_t*>(k1);
+    const uint8_t* hk2 = static_cast<const uint8_t*>(k2);
+    const uint8_t* hv = static_cast<const uint8_t*>(v);
+    // One cudaMemcpyAsync per tensor of the chunk, on the copy-in stream.
+    e = cudaMemcpyAsync(dq1 + oq, hq1 + oq, nq, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dq2 + oq, hq2 + oq, nq, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dk1 + oq, hk1 + oq, nq, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dk2 + oq, hk2 + oq, nq, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dv + ov, hv + ov, nv, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->in_done[c], hp->in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->in_done[c], 0);
+    if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward_host: copy in");
+    // The forward of the chunk on the caller's stream.
+    st = diffattn_forward(dt, b1 - b0, H, n, d, dq1 + oq, dq2 + oq, dk1 + oq, dk2 + oq, dv + ov, lambda, lambda_init,
+                          gamma, eps, causal, dout + ov, stream);
+    if (st != DIFFATTN_OK) return st;
+    // Its output back on the copy-out stream.
+    e = cudaEventRecord(hp->fwd_done[c], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->fwd_done[c], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<uint8_t*>(out) + ov, dout + ov, nv, cudaMemcpyDeviceToHost, hp->out);
+    if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward_host: copy out");
+  }
+  // The caller's stream resumes once every output byte is back in host memory.
+  e = cudaEventRecord(hp->last_out, hp->out);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->last_out, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward_host: stream ordering");
+  return ok();
+}
+
 diffattn_status diffattn_v2_forward(diffattn_dtype dt, int B, int Hq, int Hkv, int n, int d, const void* q,
                                     const void* k, const void* v, const float* lam_logits, long long sb,
                                     long long st_, float softmax_scale, int causal, void* out, void* stream) {

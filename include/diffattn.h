@@ -30,6 +30,8 @@
 #ifndef DIFFATTN_H
 #define DIFFATTN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -105,6 +107,36 @@ diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d,
                                  const void* k2, const void* v, const float* lambda,
                                  float lambda_init, const float* gamma, float eps,
                                  int causal, void* out, void* stream);
+
+/*
+ * diffattn_forward on inputs and output in HOST memory: the call copies the
+ * inputs in, runs the forward and copies the output back, pipelined over
+ * chunks of the batch (the copy of chunk c + 1 in, the forward of chunk c
+ * and the copy of chunk c - 1 out overlap on internal copy streams).  Same
+ * operation, layouts, arguments and errors as diffattn_forward, except:
+ *   q1, q2, k1, k2, v (in), out : host memory, [B, n, H, d] / [B, n, H, 2d];
+ *                 page-locked (cudaHostAlloc / cudaHostRegister) for the
+ *                 copies to be asynchronous; pageable memory still works
+ *                 but each copy then blocks the host.
+ *   lambda, gamma : device memory as for diffattn_forward (parameters of the
+ *                 layer, resident on the device).
+ *   workspace   : device memory the caller owns, at least
+ *                 diffattn_forward_host_workspace(dt, B, H, n, d) bytes,
+ *                 256-byte aligned; it holds the device copies of the inputs
+ *                 and of the output (the library allocates nothing per call).
+ * Asynchronous on `stream`: the output in host memory is complete when the
+ * stream's work up to this call is; the workspace and the host buffers must
+ * not be touched before that.  A smaller workspace -> ERR_SHAPE; an
+ * unaligned workspace -> ERR_ALIGN.
+ */
+size_t diffattn_forward_host_workspace(diffattn_dtype dt, int B, int H, int n, int d);
+
+diffattn_status diffattn_forward_host(diffattn_dtype dt, int B, int H, int n, int d,
+                                      const void* q1, const void* q2, const void* k1,
+                                      const void* k2, const void* v, const float* lambda,
+                                      float lambda_init, const float* gamma, float eps,
+                                      int causal, void* out, void* workspace,
+                                      size_t workspace_bytes, void* stream);
 
 /*
  * DIFF V2 forward (DIFF V2 analysis page, sections "2. 커스텀 커널 제거",

@@ -32,7 +32,8 @@ def _declared():
 def test_header_declares_the_entry_points():
     names = _declared()
     for want in ("diffattn_forward", "diffattn_v2_forward", "lambda_reparam", "diffattn_lambda_init",
-                 "diffattn_device_status", "diffattn_last_error"):
+                 "diffattn_device_status", "diffattn_last_error", "diffattn_forward_host",
+                 "diffattn_forward_host_workspace"):
         assert want in names
 
 
@@ -77,6 +78,36 @@ def test_forward_host_validation(L):
     assert _fwd(L, ptrs=[A, A, MIS, A, A]) == da.ERR_ALIGN
     assert _fwd(L, out=MIS) == da.ERR_ALIGN
     assert b"16-byte" in L.diffattn_last_error()
+
+
+def test_forward_host_workspace_size(L):
+    def r256(x):
+        return (x + 255) // 256 * 256
+    for dt, es in ((1, 2), (0, 4)):
+        for B, H, n, d in ((4, 16, 2048, 64), (1, 1, 1, 1), (3, 2, 129, 128)):
+            qk = B * n * H * d * es
+            assert L.diffattn_forward_host_workspace(dt, B, H, n, d) == 4 * r256(qk) + 2 * r256(2 * qk)
+    assert L.diffattn_forward_host_workspace(7, 1, 1, 8, 64) == 0
+    assert L.diffattn_forward_host_workspace(1, -1, 1, 8, 64) == 0
+
+
+def test_forward_host_buffer_validation(L):
+    """The host-buffer entry point rejects bad arguments before any CUDA call."""
+    W = P(0x100000)  # 256-byte aligned fake device workspace (never dereferenced)
+    need = L.diffattn_forward_host_workspace(1, 1, 1, 8, 64)
+
+    def call(dt=1, B=1, n=8, d=64, q1=A, out=A, ws=W, nbytes=need):
+        return L.diffattn_forward_host(dt, B, 1, n, d, q1, A, A, A, A, A, ctypes.c_float(0.2), None,
+                                       ctypes.c_float(1e-5), 1, out, ws, nbytes, None)
+    assert call(dt=7) == da.ERR_DTYPE
+    assert call(n=-1) == da.ERR_SHAPE
+    assert call(n=0) == da.OK
+    assert call(q1=None) == da.ERR_NULL
+    assert call(out=None) == da.ERR_NULL
+    assert call(ws=None) == da.ERR_NULL
+    assert call(nbytes=need - 1) == da.ERR_SHAPE
+    assert b"workspace" in L.diffattn_last_error()
+    assert call(ws=P(0x100010)) == da.ERR_ALIGN
 
 
 def test_v2_host_validation(L):

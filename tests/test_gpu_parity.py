@@ -232,6 +232,24 @@ def test_v2_wide_score_range():
     assert err <= TOL["bf16"] * scale, f"max abs error {err} (output scale {scale})"
 
 
+@pytest.mark.parametrize("B,H,n,d", [(5, 2, 300, 64), (3, 1, 260, 128), (9, 1, 130, 64), (1, 3, 129, 64)])
+def test_v1_host_buffers_match_device_path(B, H, n, d):
+    # Inputs and output in page-locked host memory, copied and computed in
+    # batch chunks: every (batch, head, query tile) is computed by the same
+    # kernel as on the device path, so the outputs are identical.
+    w = shrink(WORKLOADS[2], B=B, H=H, n=n, d=d, causal=True, gamma="uniform", layer=2, seed=60 + B)
+    x = make_v1(w, "cuda")
+    ref, lam = _v1_gpu(x, w)
+    host = {k: x[k].cpu().pin_memory() for k in ("q1", "q2", "k1", "k2", "v")}
+    out = da.diffattn_forward_host(host["q1"], host["q2"], host["k1"], host["k2"], host["v"], lam,
+                                   da.lambda_init(w.layer), gamma=x["gamma"], causal=True)
+    da.device_status()
+    assert torch.equal(out, ref.cpu())
+    if B * H * n <= 1500:
+        err = _err(_np(out), _v1_oracle(x, w))
+        assert err <= TOL["bf16"], f"max abs error {err}"
+
+
 @pytest.mark.parametrize("causal", [True, False])
 def test_v1_d64_long_items_sampled(causal):
     # More than 64 query tiles per head: the d = 64 kernel runs one CTA per
