@@ -24,7 +24,7 @@ Sources (web pages on the Differential Transformer; cited by title and section):
               lambda re-parameterisation, lambda_init schedule, multi-head,
               per-head RMSNorm with the fixed (1 - lambda_init) multiplier).
 
-Readings where the pages are silent or garbled (each also listed in the design doc):
+Readings where the pages are silent or garbled:
   * scale 1/sqrt(d) with d the per-map query/key width ([GLOSSARY] code; the
     [V2] and [SUMMARY] formulas omit it, the [NEWS] equation was stripped);
   * causal mask: key j visible to query i iff j <= i (decoder-only, [NEWS]);
