@@ -10,6 +10,7 @@ from .diffattn_oracle import (  # noqa: F401
     attention_map,
     diff_attn_head,
     diff_attn_v1,
+    diff_attn_v1_decode,
     diff_attn_v2,
     difference_map,
     head_rmsnorm,

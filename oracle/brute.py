@@ -94,3 +94,34 @@ def brute_v2(q, k, v, lam_logits, causal=True, scale=None):
             ob.append(oi)
         out.append(ob)
     return out
+
+
+def brute_v1_decode(q1, q2, k1, k2, v, lam, lam_init, gamma=None, eps=1e-5, lens=None):
+    """DIFF V1 decode: q[b][h][c] over the cache k[b][j][h][c], v[b][j][h][c], keys j < lens[b].
+
+    Returns nested lists y[b][h][c] (all zeros where no key is visible).
+    """
+    B, n, H = len(k1), len(k1[0]), len(k1[0][0])
+    d = len(k1[0][0][0])
+    dv = len(v[0][0][0])
+    scale = 1.0 / math.sqrt(d)
+    y = []
+    for b in range(B):
+        L = n if lens is None else int(lens[b])
+        yb = []
+        for h in range(H):
+            if L == 0:
+                yb.append([0.0] * dv)
+                continue
+            q1r = [_get(q1, b, h, c) for c in range(d)]
+            q2r = [_get(q2, b, h, c) for c in range(d)]
+            k1r = [[_get(k1, b, j, h, c) for c in range(d)] for j in range(L)]
+            k2r = [[_get(k2, b, j, h, c) for c in range(d)] for j in range(L)]
+            w1 = _softmax_weights(q1r, k1r, scale, lambda j: True)
+            w2 = _softmax_weights(q2r, k2r, scale, lambda j: True)
+            o = [sum((w1[j] - lam * w2[j]) * _get(v, b, j, h, c) for j in range(L)) for c in range(dv)]
+            ms = sum(x * x for x in o) / dv
+            g = [1.0] * dv if gamma is None else [float(x) for x in gamma]
+            yb.append([(1.0 - lam_init) * g[c] * o[c] / math.sqrt(ms + eps) for c in range(dv)])
+        y.append(yb)
+    return y

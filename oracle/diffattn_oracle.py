@@ -189,6 +189,38 @@ def diff_attn_v1(q1, q2, k1, k2, v, lam: float, lam_init: float, gamma=None,
     return y
 
 
+def diff_attn_v1_decode(q1, q2, k1, k2, v, lam: float, lam_init: float, gamma=None,
+                        eps: float = DEFAULT_EPS, lens=None) -> np.ndarray:
+    """DIFF V1 for one new token per sequence over a key/value cache (decode).
+
+    q1, q2: [B, H, d], the new token's queries; k1, k2: [B, n, H, d] and v:
+    [B, n, H, 2d], the cache (the new token's own keys included); lens: [B]
+    keys visible to sequence b (keys j < lens[b]), default n.  The output of a
+    head is the same operator as one row of diff_attn_v1: the difference of
+    two softmax maps over the visible keys times V, then the per-head RMSNorm
+    with the fixed (1 - lambda_init).  Reading where the pages are silent: a
+    sequence with no visible key (lens[b] = 0) gets an all-zero output.
+    Returns [B, H, 2d] (fp64).
+    """
+    q1, q2, k1, k2, v = (_f64(a) for a in (q1, q2, k1, k2, v))
+    B, n, H, d = k1.shape
+    if q1.shape != (B, H, d) or q2.shape != (B, H, d) or v.shape != (B, n, H, 2 * d):
+        raise ValueError("need q [B, H, d], k [B, n, H, d], v [B, n, H, 2d]")
+    lens = np.full(B, n, dtype=np.int64) if lens is None else np.asarray(lens, dtype=np.int64).reshape(-1)
+    if lens.shape != (B,) or lens.min(initial=0) < 0 or lens.max(initial=0) > n:
+        raise ValueError("lens must be [B] with 0 <= len <= n")
+    y = np.zeros((B, H, 2 * d), dtype=np.float64)
+    for b in range(B):
+        L = int(lens[b])
+        if L == 0:
+            continue
+        for h in range(H):
+            o = diff_attn_head(q1[b, None, h], q2[b, None, h], k1[b, :L, h], k2[b, :L, h], v[b, :L, h],
+                               lam, causal=False)
+            y[b, h] = head_rmsnorm(o, gamma, eps, lam_init)[0]
+    return y
+
+
 def diff_attn_v2(q, k, v, lam_logits, causal: bool = True, scale=None, rows=None,
                  pairing: str = "adjacent") -> np.ndarray:
     """DIFF V2 forward: out_g = attn[2g] - sigmoid(lambda_g) * attn[2g+1].

@@ -82,3 +82,25 @@ def test_v2_pin_catches_halves_pairing(monkeypatch):
     monkeypatch.setattr(pins.oracle, "diff_attn_v2", halves)
     with pytest.raises(AssertionError):
         pins.test_v2_against_sdpa(True)
+
+
+def test_decode_pins_catch_an_ignored_length(monkeypatch):
+    real = om.diff_attn_v1_decode
+
+    def all_keys(q1, q2, k1, k2, v, lam, lam_init, gamma=None, eps=om.DEFAULT_EPS, lens=None):
+        return real(q1, q2, k1, k2, v, lam, lam_init, gamma, eps, None)  # attends past the sequence's length
+
+    monkeypatch.setattr(pins.oracle, "diff_attn_v1_decode", all_keys)
+    with pytest.raises(AssertionError):
+        pins.test_decode_matches_brute_force_with_lengths()
+
+
+def test_decode_pins_catch_a_swapped_map(monkeypatch):
+    real = om.diff_attn_v1_decode
+
+    def swapped(q1, q2, k1, k2, v, lam, lam_init, gamma=None, eps=om.DEFAULT_EPS, lens=None):
+        return real(q2, q1, k1, k2, v, lam, lam_init, gamma, eps, lens)  # q1 against K2 and q2 against K1
+
+    monkeypatch.setattr(pins.oracle, "diff_attn_v1_decode", swapped)
+    with pytest.raises(AssertionError):
+        pins.test_decode_is_the_last_row_of_causal_attention()

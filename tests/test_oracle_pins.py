@@ -293,3 +293,54 @@ def test_v2_rejects_pairs_that_straddle_groups():
     k = np.zeros((1, 4, 2, 2))
     with pytest.raises(ValueError):
         oracle.diff_attn_v2(q, k, k, np.zeros((1, 4, 3)))
+
+
+# ---------------------------------------------------------------- decode (one query per sequence)
+def _decode_case(seed, B=3, n=9, H=2, d=4):
+    r = _rng(seed)
+    q1, q2 = (r.normal(size=(B, H, d)) for _ in range(2))
+    k1, k2 = (r.normal(size=(B, n, H, d)) for _ in range(2))
+    v = r.normal(size=(B, n, H, 2 * d))
+    return q1, q2, k1, k2, v, r.uniform(0.9, 1.1, 2 * d)
+
+
+def test_decode_is_the_last_row_of_causal_attention():
+    # The new token's query over the cache (its own key included) is the last
+    # row of the causal forward over the sequence with that query appended.
+    q1, q2, k1, k2, v, g = _decode_case(30)
+    B, n, H, d = k1.shape
+    r = _rng(31)
+    Q1, Q2 = (r.normal(size=(B, n, H, d)) for _ in range(2))
+    Q1[:, -1], Q2[:, -1] = q1, q2
+    lam, lin = 0.41, 0.2
+    full = oracle.diff_attn_v1(Q1, Q2, k1, k2, v, lam, lin, g, 1e-5, True, rows=[n - 1])[:, 0]
+    np.testing.assert_allclose(oracle.diff_attn_v1_decode(q1, q2, k1, k2, v, lam, lin, g), full, atol=1e-12)
+
+
+def test_decode_matches_brute_force_with_lengths():
+    q1, q2, k1, k2, v, g = _decode_case(32)
+    lens = [9, 1, 5]
+    lam, lin = 0.7, 0.5560582041556406
+    y = oracle.diff_attn_v1_decode(q1, q2, k1, k2, v, lam, lin, g, 1e-5, lens)
+    yb = np.array(brute.brute_v1_decode(q1, q2, k1, k2, v, lam, lin, g, 1e-5, lens))
+    np.testing.assert_allclose(y, yb, atol=1e-12)
+
+
+def test_decode_closed_forms():
+    q1, q2, k1, k2, v, _ = _decode_case(33)
+    B, n, H, d = k1.shape
+    lam, lin, eps = 0.3, 0.2, 1e-5
+    # Zero queries: both maps are uniform over the visible keys, O = (1 - lambda) mean(V).
+    z = np.zeros_like(q1)
+    lens = np.array([9, 4, 1])
+    y = oracle.diff_attn_v1_decode(z, z, k1, k2, v, lam, lin, None, eps, lens)
+    for b in range(B):
+        o = (1 - lam) * v[b, :lens[b]].mean(axis=0)  # [H, 2d]
+        want = (1 - lin) * o / np.sqrt((o * o).mean(axis=-1, keepdims=True) + eps)
+        np.testing.assert_allclose(y[b], want, atol=1e-12)
+    # One visible key: both maps put weight 1 on it, O = (1 - lambda) V[0].
+    y1 = oracle.diff_attn_v1_decode(q1, q2, k1, k2, v, lam, lin, None, eps, [1, 1, 1])
+    o = (1 - lam) * v[:, 0]
+    np.testing.assert_allclose(y1, (1 - lin) * o / np.sqrt((o * o).mean(axis=-1, keepdims=True) + eps), atol=1e-12)
+    # No visible key: zeros (the reading for an empty cache).
+    assert not np.any(oracle.diff_attn_v1_decode(q1, q2, k1, k2, v, lam, lin, None, eps, [0, 9, 0])[[0, 2]])
