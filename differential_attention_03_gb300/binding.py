@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
             L.diffattn_forward_host.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, f, vp, f, i, vp, vp,
                                                 ctypes.c_size_t, vp]
             L.diffattn_forward_host.restype = i
+            L.diffattn_decode.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, f, vp, f, vp, vp]
+            L.diffattn_decode.restype = i
             L.diffattn_v2_forward.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, ll, ll, f, i, vp, vp]
             L.diffattn_v2_forward.restype = i
             L.diffattn_device_status.argtypes = [vp]
@@ -192,6 +194,35 @@ def diffattn_forward_host(q1, q2, k1, k2, v, lam, lambda_init_value: float, gamm
                                        _ptr(lam), float(lambda_init_value), _ptr(gamma), float(eps),
                                        1 if causal else 0, _ptr(out), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def diffattn_decode(q1, q2, k1, k2, v, lam, lambda_init_value: float, gamma=None, eps: float = 1e-5,
+                    lens=None, out=None, stream=None) -> torch.Tensor:
+    """DIFF V1 decode: one new token per sequence over a key/value cache.
+
+    q1, q2: [B, H, d]; k1, k2: [B, n, H, d]; v: [B, n, H, 2d] (bf16, d in
+    {64, 128}); lens: int32 [B] visible keys per sequence or None (all n).
+    Returns out [B, H, 2d].
+    """
+    B, n, H, d = k1.shape
+    dt = k1.dtype
+    _need(q1, "q1", dt, (B, H, d))
+    _need(q2, "q2", dt, (B, H, d))
+    _need(k1, "k1", dt, (B, n, H, d))
+    _need(k2, "k2", dt, (B, n, H, d))
+    _need(v, "v", dt, (B, n, H, 2 * d))
+    _need(lam, "lambda", torch.float32, (1,))
+    if gamma is not None:
+        _need(gamma, "gamma", torch.float32, (2 * d,))
+    if lens is not None:
+        _need(lens, "lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, H, 2 * d), device=k1.device, dtype=dt)
+    _need(out, "out", dt, (B, H, 2 * d))
+    _check(lib().diffattn_decode(_dt(k1), B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v),
+                                 _ptr(lens), _ptr(lam), float(lambda_init_value), _ptr(gamma), float(eps),
+                                 _ptr(out), _stream(stream)))
     return out
 
 

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -11,6 +12,7 @@
 #include <mutex>
 #include <string>
 
+#include "decode.cuh"
 #include "diffattn.h"
 #include "launch.h"
 
@@ -383,6 +385,61 @@ diffattn_status diffattn_forward_host(diffattn_dtype dt, int B, int H, int n, in
   e = cudaEventRecord(hp->last_out, hp->out);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->last_out, 0);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward_host: stream ordering");
+  return ok();
+}
+
+diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, const void* q1, const void* q2,
+                                const void* k1, const void* k2, const void* v, const int* lens,
+                                const float* lambda, float lambda_init, const float* gamma, float eps, void* out,
+                                void* stream) {
+  if (dt != DIFFATTN_F32 && dt != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "diffattn_decode: bad dtype %d", (int)dt);
+  if (B < 0 || H < 0 || n < 0 || d < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode: bad sizes B=%d H=%d n=%d d=%d", B, H, n, d);
+  if (B == 0 || H == 0) return ok();
+  if (!q1 || !q2 || !k1 || !k2 || !v || !lambda || !out) return fail(DIFFATTN_ERR_NULL, "diffattn_decode: NULL pointer");
+  if (dt != DIFFATTN_BF16 || (d != 64 && d != 128))
+    return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_decode: bf16 with d in {64, 128} only (got dtype %d, d=%d)", (int)dt,
+                d);
+  if (!std::isfinite(lambda_init)) return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode: lambda_init not finite");
+  if (!aligned16(q1) || !aligned16(q2) || !aligned16(k1) || !aligned16(k2) || !aligned16(v) || !aligned16(out))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_decode: bf16 tensors must be 16-byte aligned");
+  const long long units = static_cast<long long>(B) * H;
+  if (units * da::DecodeCfg<64>::MAX_CS > 0x7fffffffll)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode: too many (batch, head) pairs");
+  if (eps <= 0.f) eps = 1e-5f;
+  int* status = nullptr;
+  diffattn_status st = status_word(&status);
+  if (st != DIFFATTN_OK) return st;
+  da::DecodeParams p;
+  memset(&p, 0, sizeof(p));
+  const int bk = (d == 64) ? da::DecodeCfg<64>::BK : da::DecodeCfg<128>::BK;
+  const int nn = n > 0 ? n : 1;  // an empty cache still needs a valid map (no key is read)
+  if ((st = make_map(&p.tm_k1, k1, B, nn, H, d, bk)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&p.tm_k2, k2, B, nn, H, d, bk)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&p.tm_v, v, B, nn, H, 2 * d, bk)) != DIFFATTN_OK) return st;
+  p.q1 = static_cast<const __nv_bfloat16*>(q1);
+  p.q2 = static_cast<const __nv_bfloat16*>(q2);
+  p.lens = lens;
+  p.lambda = lambda;
+  p.gamma = gamma;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  p.norm_mult = 1.f - lambda_init;
+  p.eps = eps;
+  p.B = B;
+  p.H = H;
+  p.n = n;
+  p.status = status;
+  // CTAs per (b, h): the smallest power of two that gives at least two waves
+  // of two CTAs per SM, at most 8 and at most one CTA per four stages of keys.
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  const long long want = 4ll * sms;
+  const int max_by_keys = std::max(1, n / (4 * bk));
+  int cs = 1;
+  while (cs < da::DecodeCfg<64>::MAX_CS && units * cs < want && cs * 2 <= max_by_keys) cs *= 2;
+  cudaError_t e = da::launch_decode_v1(p, d, static_cast<int>(units), cs, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_decode launch");
+  g_launches.fetch_add(1);
   return ok();
 }
 

@@ -1,0 +1,408 @@
+// One-token differential-attention decode over a key/value cache (CUDA
+// cores, TMA, thread-block clusters with distributed shared memory; sm_103a).
+//
+// What it computes, per (batch b, head h), with L = lens[b] visible keys:
+//   O_r = sum_{j < L} softmax_j(q_r . k_r[j] / sqrt d) v[j]          r = 1, 2
+//   out = (1 - lambda_init) gamma (O_1 - lambda O_2) / sqrt(mean_c (O_1 - lambda O_2)^2 + eps)
+// i.e. the DIFF V1 operator for the newest token of a causal sequence, whose
+// keys and values sit in the cache ("Differential Transformer" glossary page,
+// "How differential attention works"; news article section "差分注意力" for
+// the per-head RMSNorm with the fixed (1 - lambda_init)).  L = 0 gives zeros.
+//
+// The step is bound by HBM: every visible key's k_1, k_2 and v are read
+// exactly once (V once for both maps), 8 d bytes per key, against ~12 d
+// flops.  So no tensor cores: the work is spread so that enough bytes are in
+// flight on every SM.
+//   * A cluster of CS CTAs per (b, h) (CS from 1 to 8, chosen by the host so
+//     that the grid fills the GPU); CTA c streams keys [c C, c C + C) of
+//     the cache (C a multiple of the stage size) through a ring of NST
+//     stages filled by TMA (K_1, K_2 and V tiles of BK keys, 128-byte
+//     swizzled rows; 32 KB a stage).
+//   * Four warps per CTA, BK / 4 keys each per stage; PARTS lanes share a key
+//     (32 products of q . k each, combined by shuffles), so a warp scores its
+//     keys in one pass; every warp keeps its own online-softmax state per map
+//     (running maximum, per-lane partial sums, 2d / 32 output channels per
+//     lane for each map), rescaled only when the maximum grows.
+//   * The CTA merges its warps' states in shared memory; the cluster's CTAs
+//     then merge theirs through distributed shared memory in CTA rank 0,
+//     which applies the combine and the per-head RMSNorm and stores the row.
+//     No global scratch.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "params.h"
+#include "ptx.cuh"
+
+namespace da {
+
+struct DecodeParams {
+  CUtensorMap tm_k1;  // [B, n, H, d] key caches, boxes of 64 columns x BK keys
+  CUtensorMap tm_k2;
+  CUtensorMap tm_v;   // [B, n, H, 2d]
+  const __nv_bfloat16* q1;  // [B, H, d]
+  const __nv_bfloat16* q2;
+  const int* lens;          // [B] visible keys, or nullptr: n for every sequence
+  const float* lambda;      // device scalar
+  const float* gamma;       // [2d] or nullptr
+  __nv_bfloat16* out;       // [B, H, 2d]
+  float scale_log2;         // log2(e) / sqrt(d)
+  float norm_mult;          // 1 - lambda_init
+  float eps;
+  int B, H, n;
+  int* status;
+};
+
+template <int D>
+struct DecodeCfg {
+  static constexpr int MAX_CS = 8;  // CTAs per (b, h) cluster: chosen at launch, at most this (16-CTA
+                                    // clusters measured slower: 5.5 vs 6.2 TB/s at B8 H8 n32768 d128)
+  static constexpr int NWARP = 4;
+  static constexpr int NTHREADS = NWARP * 32;
+  static constexpr int DV = 2 * D;
+  static constexpr int BK = D == 64 ? 64 : 32;  // keys per stage
+  static constexpr int KW = BK / NWARP;         // keys per warp per stage
+  static constexpr int PARTS = 32 / KW;         // lanes per key
+  static constexpr int PE = D / PARTS;          // q . k products per lane (32)
+  static constexpr int QB = D / 64, VB = DV / 64;
+  static constexpr int K_BYTES = QB * BK * 128, V_BYTES = VB * BK * 128;
+  static constexpr int STAGE = 2 * K_BYTES + V_BYTES;
+  static constexpr int NST = 3;
+  static constexpr int CH = DV / 32;  // output channels per lane and map
+  static constexpr int PART_FLOATS = 2 * (DV + 2);  // per map: max, sum, DV channels
+  static constexpr int OFF_BARS = NST * STAGE;
+  static constexpr int OFF_FLAG = OFF_BARS + 2 * NST * 8;
+  static constexpr int OFF_WARP = (OFF_FLAG + 16 + 15) / 16 * 16;  // float [NWARP][PART_FLOATS]
+  static constexpr int OFF_PART = OFF_WARP + NWARP * PART_FLOATS * 4;  // float [PART_FLOATS]: the CTA's state
+  static constexpr int OFF_RED = OFF_PART + PART_FLOATS * 4;           // float [NWARP]
+  static constexpr int SMEM_BYTES = OFF_RED + NWARP * 4 + 1024;        // + 1 KB alignment slack
+  static_assert(D == 64 || D == 128, "query/key width");
+  static_assert(PE == 32 && PARTS * KW == 32, "lane split");
+  static_assert(STAGE == 32768, "stage size");
+};
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Float at shared-memory address `a` of CTA `rank` of this cluster.
+__device__ __forceinline__ float ld_cluster_f32(uint32_t a, uint32_t rank) {
+  uint32_t ra;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <int D>
+__global__ void __launch_bounds__(128) decode_v1_kernel(const __grid_constant__ DecodeParams p) {
+  using C = DecodeCfg<D>;
+  constexpr int BK = C::BK, KW = C::KW, PARTS = C::PARTS, DV = C::DV, CH = C::CH, NST = C::NST;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
+  uint64_t* empty = full + NST;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
+  float* wpart = reinterpret_cast<float*>(smem + C::OFF_WARP);
+  float* part = reinterpret_cast<float*>(smem + C::OFF_PART);
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t cs = cluster_nctarank();
+  const int unit = blockIdx.x / cs;  // (b, h)
+  const uint32_t rank = cluster_ctarank();
+  const int b = unit / p.H, h = unit % p.H;
+  int L = p.lens ? p.lens[b] : p.n;
+  L = max(0, min(L, p.n));
+  // This CTA's keys: [k_begin, k_end), a multiple of BK long except at L.
+  const int chunk = ((L + static_cast<int>(cs) * BK - 1) / (static_cast<int>(cs) * BK)) * BK;
+  const int k_begin = min(L, static_cast<int>(rank) * chunk);
+  const int k_end = min(L, k_begin + chunk);
+  const int nblk = (k_end - k_begin + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C::NWARP);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const AbortState ab{abort_flag, p.status};
+
+  auto issue = [&](int i) {  // block i of this CTA into stage i % NST
+    uint8_t* st = smem + (i % NST) * C::STAGE;
+    const int key0 = k_begin + i * BK;
+    mbar_arrive_expect_tx(&full[i % NST], C::STAGE);
+    for (int bx = 0; bx < C::QB; ++bx) {
+      tma_load_4d(st + bx * BK * 128, &p.tm_k1, &full[i % NST], bx * 64, h, key0, b);
+      tma_load_4d(st + C::K_BYTES + bx * BK * 128, &p.tm_k2, &full[i % NST], bx * 64, h, key0, b);
+    }
+    for (int bx = 0; bx < C::VB; ++bx)
+      tma_load_4d(st + 2 * C::K_BYTES + bx * BK * 128, &p.tm_v, &full[i % NST], bx * 64, h, key0, b);
+  };
+  int issued = 0;
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&p.tm_k1);
+    tma_prefetch_desc(&p.tm_k2);
+    tma_prefetch_desc(&p.tm_v);
+    for (; issued < NST && issued < nblk; ++issued) issue(issued);
+  }
+
+  // This lane's 32 query products (pre-scaled into the log2 domain).
+  const int kk = lane / PARTS, prt = lane % PARTS;
+  float q1r[32], q2r[32];
+  {
+    const __nv_bfloat16* q1p = p.q1 + (static_cast<size_t>(b) * p.H + h) * D + prt * 32;
+    const __nv_bfloat16* q2p = p.q2 + (static_cast<size_t>(b) * p.H + h) * D + prt * 32;
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+      const uint4 a = *reinterpret_cast<const uint4*>(q1p + i);
+      const uint4 c = *reinterpret_cast<const uint4*>(q2p + i);
+      const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wc[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        q1r[i + 2 * e] = bf16_lo(wa[e]) * p.scale_log2;
+        q1r[i + 2 * e + 1] = bf16_hi(wa[e]) * p.scale_log2;
+        q2r[i + 2 * e] = bf16_lo(wc[e]) * p.scale_log2;
+        q2r[i + 2 * e + 1] = bf16_hi(wc[e]) * p.scale_log2;
+      }
+    }
+  }
+
+  float m1 = -INFINITY, m2 = -INFINITY, ls1 = 0.f, ls2 = 0.f;
+  float o1[CH], o2[CH];
+#pragma unroll
+  for (int c = 0; c < CH; ++c) o1[c] = o2[c] = 0.f;
+  // Byte offsets inside a stage that do not change: this lane's 32 key
+  // columns (box, first 16-byte chunk) and its CH value channels.
+  const int kbox = (prt * 32) / 64, kchunk0 = ((prt * 32) % 64) / 8;
+  const int vc0 = lane * CH, vbox = vc0 / 64, vbyte = (vc0 % 64) * 2;
+
+  for (int i = 0; i < nblk; ++i) {
+    const int s = i % NST;
+    if (!mbar_wait(&full[s], static_cast<uint32_t>(i / NST) & 1u, ab)) break;
+    const uint8_t* st = smem + s * C::STAGE;
+    const int row = warp * KW + kk;  // this lane's key within the stage
+    // ---- scores: 32 products per lane, PARTS lanes per key
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int off = kbox * BK * 128 + row * 128 + (((kchunk0 + c) ^ (row & 7)) << 4);
+      const uint4 a = *reinterpret_cast<const uint4*>(st + off);
+      const uint4 e = *reinterpret_cast<const uint4*>(st + C::K_BYTES + off);
+      const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, we[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        s1 = fmaf(q1r[8 * c + 2 * t], bf16_lo(wa[t]), s1);
+        s1 = fmaf(q1r[8 * c + 2 * t + 1], bf16_hi(wa[t]), s1);
+        s2 = fmaf(q2r[8 * c + 2 * t], bf16_lo(we[t]), s2);
+        s2 = fmaf(q2r[8 * c + 2 * t + 1], bf16_hi(we[t]), s2);
+      }
+    }
+#pragma unroll
+    for (int x = 1; x < PARTS; x <<= 1) {
+      s1 += __shfl_xor_sync(0xffffffffu, s1, x);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, x);
+    }
+    if (k_begin + i * BK + row >= k_end) s1 = s2 = -INFINITY;  // past this CTA's keys or the length
+    // ---- online softmax of this warp's keys
+    float x1 = s1, x2 = s2;
+#pragma unroll
+    for (int x = PARTS; x < 32; x <<= 1) {
+      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, x));
+      x2 = fmaxf(x2, __shfl_xor_sync(0xffffffffu, x2, x));
+    }
+    if (x1 > m1) {
+      const float f = (m1 == -INFINITY) ? 0.f : ex2(m1 - x1);
+      m1 = x1;
+      ls1 *= f;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) o1[c] *= f;
+    }
+    if (x2 > m2) {
+      const float f = (m2 == -INFINITY) ? 0.f : ex2(m2 - x2);
+      m2 = x2;
+      ls2 *= f;
+#pragma unroll
+      for (int c = 0; c < CH; ++c) o2[c] *= f;
+    }
+    const float p1 = (s1 == -INFINITY) ? 0.f : ex2(s1 - m1);
+    const float p2 = (s2 == -INFINITY) ? 0.f : ex2(s2 - m2);
+    if (prt == 0) {
+      ls1 += p1;
+      ls2 += p2;
+    }
+    // ---- P.V: every lane accumulates its CH channels over the warp's keys
+    const uint8_t* vb = st + 2 * C::K_BYTES + vbox * BK * 128;
+#pragma unroll
+    for (int k2 = 0; k2 < KW; ++k2) {
+      const float w1 = __shfl_sync(0xffffffffu, p1, k2 * PARTS);
+      const float w2 = __shfl_sync(0xffffffffu, p2, k2 * PARTS);
+      const int r = warp * KW + k2;
+      const uint8_t* vr = vb + r * 128 + ((((vbyte >> 4)) ^ (r & 7)) << 4) + (vbyte & 15);
+      uint32_t vw[CH / 2];
+      if constexpr (CH == 4) {
+        const uint2 t = *reinterpret_cast<const uint2*>(vr);
+        vw[0] = t.x;
+        vw[1] = t.y;
+      } else {
+        const uint4 t = *reinterpret_cast<const uint4*>(vr);
+        vw[0] = t.x;
+        vw[1] = t.y;
+        vw[2] = t.z;
+        vw[3] = t.w;
+      }
+#pragma unroll
+      for (int c = 0; c < CH / 2; ++c) {
+        const float va = bf16_lo(vw[c]), vc = bf16_hi(vw[c]);
+        o1[2 * c] = fmaf(w1, va, o1[2 * c]);
+        o1[2 * c + 1] = fmaf(w1, vc, o1[2 * c + 1]);
+        o2[2 * c] = fmaf(w2, va, o2[2 * c]);
+        o2[2 * c + 1] = fmaf(w2, vc, o2[2 * c + 1]);
+      }
+    }
+    // ---- release the stage; thread 0 refills it once all four warps have
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (threadIdx.x == 0 && issued < nblk) {
+      if (!mbar_wait(&empty[s], static_cast<uint32_t>(i / NST) & 1u, ab)) break;
+      issue(issued);
+      ++issued;
+    }
+  }
+  if (threadIdx.x == 0 && *ab.flag) {
+    // Aborted: let the copies already issued land before the CTA exits.
+    for (int f = (issued > NST ? issued - NST : 0); f < issued; ++f)
+      mbar_wait_drain(&full[f % NST], static_cast<uint32_t>(f / NST) & 1u, kWaitBudgetCycles);
+  }
+
+  // ---- merge the warps' states (shared memory), then the cluster's (rank 0)
+#pragma unroll
+  for (int x = 1; x < 32; x <<= 1) {
+    ls1 += __shfl_xor_sync(0xffffffffu, ls1, x);
+    ls2 += __shfl_xor_sync(0xffffffffu, ls2, x);
+  }
+  float* wp = wpart + warp * C::PART_FLOATS;  // [m1, l1, m2, l2, o1[DV], o2[DV]]
+  if (lane == 0) {
+    wp[0] = m1;
+    wp[1] = ls1;
+    wp[2] = m2;
+    wp[3] = ls2;
+  }
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    wp[4 + vc0 + c] = o1[c];
+    wp[4 + DV + vc0 + c] = o2[c];
+  }
+  __syncthreads();
+  {
+    float M1 = -INFINITY, M2 = -INFINITY;
+    float fa[C::NWARP], fb[C::NWARP];
+#pragma unroll
+    for (int w = 0; w < C::NWARP; ++w) {
+      M1 = fmaxf(M1, wpart[w * C::PART_FLOATS]);
+      M2 = fmaxf(M2, wpart[w * C::PART_FLOATS + 2]);
+    }
+#pragma unroll
+    for (int w = 0; w < C::NWARP; ++w) {
+      const float mw1 = wpart[w * C::PART_FLOATS], mw2 = wpart[w * C::PART_FLOATS + 2];
+      fa[w] = (mw1 == -INFINITY) ? 0.f : ex2(mw1 - M1);
+      fb[w] = (mw2 == -INFINITY) ? 0.f : ex2(mw2 - M2);
+    }
+    for (int c = threadIdx.x; c < DV; c += C::NTHREADS) {
+      float a = 0.f, e = 0.f;
+#pragma unroll
+      for (int w = 0; w < C::NWARP; ++w) {
+        a = fmaf(wpart[w * C::PART_FLOATS + 4 + c], fa[w], a);
+        e = fmaf(wpart[w * C::PART_FLOATS + 4 + DV + c], fb[w], e);
+      }
+      part[4 + c] = a;
+      part[4 + DV + c] = e;
+    }
+    if (threadIdx.x == 0) {
+      float l1 = 0.f, l2 = 0.f;
+#pragma unroll
+      for (int w = 0; w < C::NWARP; ++w) {
+        l1 = fmaf(wpart[w * C::PART_FLOATS + 1], fa[w], l1);
+        l2 = fmaf(wpart[w * C::PART_FLOATS + 3], fb[w], l2);
+      }
+      part[0] = M1;
+      part[1] = l1;
+      part[2] = M2;
+      part[3] = l2;
+    }
+  }
+  cluster_sync_all();  // every CTA's state is written (release / acquire across the cluster)
+
+  if (rank == 0) {
+    const uint32_t pa = smem_u32(part);
+    float M1 = -INFINITY, M2 = -INFINITY;
+    for (uint32_t r = 0; r < cs; ++r) {
+      M1 = fmaxf(M1, ld_cluster_f32(pa, r));
+      M2 = fmaxf(M2, ld_cluster_f32(pa + 8, r));
+    }
+    float l1 = 0.f, l2 = 0.f;
+    constexpr int CPT = DV / C::NTHREADS;  // channels per thread: 1 or 2
+    float y1[CPT], y2[CPT];
+#pragma unroll
+    for (int t = 0; t < CPT; ++t) y1[t] = y2[t] = 0.f;
+    for (uint32_t r = 0; r < cs; ++r) {
+      const float mr1 = ld_cluster_f32(pa, r), mr2 = ld_cluster_f32(pa + 8, r);
+      const float f1 = (mr1 == -INFINITY) ? 0.f : ex2(mr1 - M1);
+      const float f2 = (mr2 == -INFINITY) ? 0.f : ex2(mr2 - M2);
+      l1 = fmaf(ld_cluster_f32(pa + 4, r), f1, l1);
+      l2 = fmaf(ld_cluster_f32(pa + 12, r), f2, l2);
+#pragma unroll
+      for (int t = 0; t < CPT; ++t) {
+        const int c = threadIdx.x + t * C::NTHREADS;
+        y1[t] = fmaf(ld_cluster_f32(pa + 4 * (4 + c), r), f1, y1[t]);
+        y2[t] = fmaf(ld_cluster_f32(pa + 4 * (4 + DV + c), r), f2, y2[t]);
+      }
+    }
+    const float lam = *p.lambda;
+    const float a1 = (l1 > 0.f) ? 1.f / l1 : 0.f;
+    const float a2 = (l2 > 0.f) ? -lam / l2 : 0.f;
+    float y[CPT], ss = 0.f;
+#pragma unroll
+    for (int t = 0; t < CPT; ++t) {
+      y[t] = fmaf(y2[t], a2, y1[t] * a1);
+      ss = fmaf(y[t], y[t], ss);
+    }
+#pragma unroll
+    for (int x = 1; x < 32; x <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, x);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < C::NWARP; ++w) tot += red[w];
+    const float rinv = p.norm_mult * rsqrtf(tot * (1.f / DV) + p.eps);
+    __nv_bfloat16* orow = p.out + (static_cast<size_t>(b) * p.H + h) * DV;
+#pragma unroll
+    for (int t = 0; t < CPT; ++t) {
+      const int c = threadIdx.x + t * C::NTHREADS;
+      const float g = p.gamma ? p.gamma[c] : 1.f;
+      orow[c] = __float2bfloat16_rn(y[t] * rinv * g);
+    }
+  }
+  cluster_sync_all();  // rank 0 has read every CTA's state: they may exit
+}
+
+}  // namespace da

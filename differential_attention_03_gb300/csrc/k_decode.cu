@@ -1,0 +1,34 @@
+// Launchers of the decode kernel (clusters of `cs` CTAs per (batch, head)).
+#include "decode.cuh"
+#include "launch.h"
+
+namespace da {
+
+template <int D>
+static cudaError_t launch_decode(const DecodeParams& p, int units, int cs, cudaStream_t s) {
+  using C = DecodeCfg<D>;
+  auto kern = decode_v1_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units) * static_cast<unsigned>(cs), 1, 1);
+  cfg.blockDim = dim3(C::NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_v1(const DecodeParams& p, int d, int units, int cs, cudaStream_t s) {
+  return d == 64 ? launch_decode<64>(p, units, cs, s) : launch_decode<128>(p, units, cs, s);
+}
+
+}  // namespace da

@@ -139,6 +139,32 @@ diffattn_status diffattn_forward_host(diffattn_dtype dt, int B, int H, int n, in
                                       size_t workspace_bytes, void* stream);
 
 /*
+ * DIFF V1 decode step: one new token per sequence over a key/value cache
+ * ("Differential Transformer" glossary page, "How differential attention
+ * works"; news article section "差分注意力" for the per-head RMSNorm):
+ *
+ *   O   = (softmax(q1 K1^T / sqrt d) - lambda softmax(q2 K2^T / sqrt d)) V   per (b, h), keys j < lens[b]
+ *   out = (1 - lambda_init) * gamma * O / sqrt(mean_c O^2 + eps)
+ *
+ * i.e. diffattn_forward's last row of a causal sequence whose keys and
+ * values (the new token's included) are already in the cache.
+ *   dt          : DIFFATTN_BF16 (d in {64, 128}); other types -> ERR_UNSUPPORTED.
+ *   q1, q2      : [B, H, d] device, the new token's queries.
+ *   k1, k2      : [B, n, H, d] device key caches; v : [B, n, H, 2d] value cache.
+ *   lens        : device int32 [B], keys visible to each sequence, clamped to
+ *                 [0, n]; NULL: n for every sequence.  A sequence with no
+ *                 visible key gets an all-zero output.
+ *   lambda, lambda_init, gamma, eps : as for diffattn_forward.
+ *   out         : [B, H, 2d] device.
+ * Memory-bound: K1, K2 and V are read once (V for both maps).  No scratch
+ * memory; asynchronous on `stream`.  Errors as for diffattn_forward.
+ */
+diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, const void* q1,
+                                const void* q2, const void* k1, const void* k2, const void* v,
+                                const int* lens, const float* lambda, float lambda_init,
+                                const float* gamma, float eps, void* out, void* stream);
+
+/*
  * DIFF V2 forward (DIFF V2 analysis page, sections "2. 커스텀 커널 제거",
  * "5. 간소화된 λ 매개변수화" and "GQA와의 호환성"): 2h query heads over h KV
  * heads, grouped-query attention, each even/odd pair of query heads inside

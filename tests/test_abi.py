@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
     names = _declared()
     for want in ("diffattn_forward", "diffattn_v2_forward", "lambda_reparam", "diffattn_lambda_init",
                  "diffattn_device_status", "diffattn_last_error", "diffattn_forward_host",
-                 "diffattn_forward_host_workspace"):
+                 "diffattn_forward_host_workspace", "diffattn_decode"):
         assert want in names
 
 
@@ -108,6 +108,20 @@ def test_forward_host_buffer_validation(L):
     assert call(nbytes=need - 1) == da.ERR_SHAPE
     assert b"workspace" in L.diffattn_last_error()
     assert call(ws=P(0x100010)) == da.ERR_ALIGN
+
+
+def test_decode_host_validation(L):
+    def call(dt=1, B=1, n=8, d=64, q1=A, out=A, k1=A):
+        return L.diffattn_decode(dt, B, 2, n, d, q1, A, k1, A, A, None, A, ctypes.c_float(0.2), None,
+                                 ctypes.c_float(1e-5), out, None)
+    assert call(dt=7) == da.ERR_DTYPE
+    assert call(n=-1) == da.ERR_SHAPE
+    assert call(B=0) == da.OK
+    assert call(q1=None) == da.ERR_NULL
+    assert call(out=None) == da.ERR_NULL
+    assert call(dt=0) == da.ERR_UNSUPPORTED   # fp32 decode is not provided
+    assert call(d=96) == da.ERR_UNSUPPORTED
+    assert call(k1=MIS) == da.ERR_ALIGN
 
 
 def test_v2_host_validation(L):

@@ -250,6 +250,40 @@ def test_v1_host_buffers_match_device_path(B, H, n, d):
         assert err <= TOL["bf16"], f"max abs error {err}"
 
 
+# --------------------------------------------------------------------------- decode
+DECODE = [  # B, H, n, d, lens
+    (2, 2, 300, 64, None),
+    (3, 2, 1000, 128, [1000, 37, 0]),      # ragged lengths, an empty cache
+    (1, 3, 1, 64, None),                    # a single key
+    (4, 1, 777, 64, [1, 64, 65, 777]),      # stage and cluster-chunk boundaries
+    (2, 4, 5000, 128, [5000, 4097]),
+    (1, 2, 40000, 64, None),                # long cache: every CTA of the cluster streams many stages
+]
+
+
+@pytest.mark.parametrize("B,H,n,d,lens", DECODE)
+def test_v1_decode(B, H, n, d, lens):
+    w = shrink(WORKLOADS[2], B=B, H=H, n=n, d=d, gamma="uniform", layer=3, seed=90 + n)
+    x = make_v1(w, "cuda")
+    g = torch.Generator(device="cuda").manual_seed(91 + n)
+    q1 = torch.randn((B, H, d), generator=g, device="cuda").to(torch.bfloat16)
+    q2 = torch.randn((B, H, d), generator=g, device="cuda").to(torch.bfloat16)
+    lin = da.lambda_init(w.layer)
+    lam = da.lambda_reparam(x["lq1"], x["lk1"], x["lq2"], x["lk2"], lin)
+    lens_t = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = da.diffattn_decode(q1, q2, x["k1"], x["k2"], x["v"], lam, lin, gamma=x["gamma"], lens=lens_t)
+    da.device_status()
+    ref = oracle.diff_attn_v1_decode(q1, q2, x["k1"], x["k2"], x["v"], float(lam.item()), lin,
+                                     x["gamma"].cpu(), 1e-5, lens)
+    assert out.shape == (B, H, 2 * d)
+    err = _err(_np(out), ref)
+    assert err <= TOL["bf16"], f"max abs error {err}"
+    if lens is not None:
+        for b, L in enumerate(lens):
+            if L == 0:
+                assert not bool(out[b].float().abs().max() > 0)
+
+
 @pytest.mark.parametrize("causal", [True, False])
 def test_v1_d64_long_items_sampled(causal):
     # More than 64 query tiles per head: the d = 64 kernel runs one CTA per
