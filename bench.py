@@ -276,6 +276,47 @@ def time_e2e(w, x, da, steps):
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
+DECODE_WORKLOADS = [  # (name, B, H, n, d): one new token per sequence over a key/value cache of n tokens
+    ("v1-decode-bf16-B8H16-n32768-d64", 8, 16, 32768, 64),
+    ("v1-decode-bf16-B8H8-n32768-d128", 8, 8, 32768, 128),
+]
+
+
+def time_decode(da, flush, B, H, n, d, runs=20):
+    """DIFF V1 decode step over a key/value cache: median CUDA-event time (L2 flushed), HBM GB/s."""
+    import torch
+    g = torch.Generator(device="cuda").manual_seed(1000 + n + d)
+
+    def rnd(*shape):
+        return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    q1, q2 = rnd(B, H, d), rnd(B, H, d)
+    k1, k2, v = rnd(B, n, H, d), rnd(B, n, H, d), rnd(B, n, H, 2 * d)
+    lam = torch.tensor([0.3], device="cuda")
+    gamma = torch.ones(2 * d, device="cuda")
+    out = torch.empty((B, H, 2 * d), device="cuda", dtype=torch.bfloat16)
+
+    def call():
+        da.diffattn_decode(q1, q2, k1, k2, v, lam, 0.2, gamma=gamma, out=out)
+    for _ in range(3):
+        call()
+    da.device_status()
+    ts = []
+    for _ in range(runs):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    da.device_status()
+    ms = statistics.median(ts)
+    nbytes = B * H * n * 4 * d * 2 + B * H * 4 * d * 2  # K1, K2, V read once; q in, out
+    del q1, q2, k1, k2, v
+    torch.cuda.empty_cache()
+    return ms, nbytes
+
+
 def cpu_baseline(w, x, budget_s=12.0):
     """The fp64 oracle as it stands, on a bounded sample of the same workload.
 
@@ -402,6 +443,10 @@ def run_ours(args):
                 del xc
             torch.cuda.empty_cache()
 
+    decode = {}
+    if rank == 0 and world == 1 and not args.no_all_configs:
+        decode = decode_results(da, flush, peaks)
+
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 5), "higher_is_better": True, "scaling": "weak",
@@ -420,6 +465,8 @@ def run_ours(args):
     }
     if configs:
         line["configs"] = configs
+    if decode:
+        line["decode"] = decode
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(w, x)
         cb.pop("seconds", None)
@@ -463,6 +510,26 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def decode_results(da, flush, peaks):
+    out = {}
+    for name, B, H, n, d in DECODE_WORKLOADS:
+        ms, nb = time_decode(da, flush, B, H, n, d)
+        gbs = nb / (ms * 1e-3) / 1e9
+        out[name] = {"us": round(ms * 1e3, 1), "hbm_gbs": round(gbs, 1), "bound": "hbm",
+                     "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_gbs": peaks["hbm_gbs"],
+                     "algorithmic_bytes": nb, "tokens_per_s": round(B / (ms * 1e-3), 1)}
+    return out
+
+
+def run_decode_only():
+    import torch
+    from differential_attention_03_gb300 import binding as da, build
+    build.build()
+    da.lib()
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
+    print(json.dumps({"decode": decode_results(da, flush, read_peaks())}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -472,11 +539,15 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-all-configs", action="store_true")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time only the decode workloads (one JSON line with the 'decode' object)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.decode_only:
+        run_decode_only()
     else:
         run_ours(args)
 

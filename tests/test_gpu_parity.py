@@ -284,6 +284,24 @@ def test_v1_decode(B, H, n, d, lens):
                 assert not bool(out[b].float().abs().max() > 0)
 
 
+@pytest.mark.parametrize("B,H,n,d", [(8, 16, 32768, 64), (8, 8, 32768, 128)])
+def test_v1_decode_bench_sizes(B, H, n, d):
+    # The decode workloads bench.py times, in the same launch configuration,
+    # every output row against the oracle.
+    g = torch.Generator(device="cuda").manual_seed(1000 + n + d)
+
+    def rnd(*shape):
+        return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    q1, q2 = rnd(B, H, d), rnd(B, H, d)
+    k1, k2, v = rnd(B, n, H, d), rnd(B, n, H, 2 * d)[..., :d].contiguous(), rnd(B, n, H, 2 * d)
+    lam = torch.tensor([0.3], device="cuda")
+    out = da.diffattn_decode(q1, q2, k1, k2, v, lam, 0.2)
+    da.device_status()
+    ref = oracle.diff_attn_v1_decode(q1, q2, k1, k2, v, 0.3, 0.2, None, 1e-5)
+    err = _err(_np(out), ref)
+    assert err <= TOL["bf16"], f"max abs error {err}"
+
+
 @pytest.mark.parametrize("causal", [True, False])
 def test_v1_d64_long_items_sampled(causal):
     # More than 64 query tiles per head: the d = 64 kernel runs one CTA per
