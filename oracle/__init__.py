@@ -12,6 +12,7 @@ from .diffattn_oracle import (  # noqa: F401
     diff_attn_v1,
     diff_attn_v1_decode,
     diff_attn_v2,
+    diff_attn_v2_decode,
     difference_map,
     head_rmsnorm,
     lambda_init,

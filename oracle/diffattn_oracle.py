@@ -263,3 +263,44 @@ def diff_attn_v2(q, k, v, lam_logits, causal: bool = True, scale=None, rows=None
                 oo = attention_map(q[b, :, ho], k[b, :, ko], scale, causal, blk) @ v[b, :, ko]
                 out[b, s:s + blk.size, g] = oe - sig[s:s + blk.size] * oo
     return out
+
+
+def diff_attn_v2_decode(q, k, v, lam_logits, lens=None, scale=None) -> np.ndarray:
+    """DIFF V2 for one new token per sequence over a key/value cache (decode).
+
+    q: [B, Hq, d], the new token's query heads; k, v: [B, n, Hkv, d], the cache
+    (the new token's own keys included); lam_logits: [B, Hq/2], the new
+    token's logit per head pair; lens: [B] visible keys (keys j < lens[b]),
+    default n.  out_g = A_{2g} - sigmoid(logit_g) A_{2g+1} over the visible
+    keys, A_j reading KV head j // (Hq/Hkv): the same operator as one row of
+    diff_attn_v2.  A sequence with no visible key gets zeros.
+    Returns [B, Hq/2, d] (fp64).
+    """
+    q, k, v = (_f64(a) for a in (q, k, v))
+    B, n, Hkv, d = k.shape
+    Hq = q.shape[1]
+    if q.shape != (B, Hq, d) or v.shape != (B, n, Hkv, d):
+        raise ValueError("need q [B, Hq, d], k and v [B, n, Hkv, d]")
+    if Hq % 2 or Hq % Hkv or (Hq // Hkv) % 2:
+        raise ValueError("need Hq even and Hq/Hkv even so each pair shares a KV head")
+    lam_logits = _f64(lam_logits)
+    if lam_logits.shape != (B, Hq // 2):
+        raise ValueError("lam_logits must be [B, Hq/2]")
+    lens = np.full(B, n, dtype=np.int64) if lens is None else np.asarray(lens, dtype=np.int64).reshape(-1)
+    if lens.shape != (B,) or lens.min(initial=0) < 0 or lens.max(initial=0) > n:
+        raise ValueError("lens must be [B] with 0 <= len <= n")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    group = Hq // Hkv
+    out = np.zeros((B, Hq // 2, d), dtype=np.float64)
+    for b in range(B):
+        L = int(lens[b])
+        if L == 0:
+            continue
+        for g in range(Hq // 2):
+            he, ho = 2 * g, 2 * g + 1
+            kv = he // group
+            ae = attention_map(q[b, None, he], k[b, :L, kv], scale, False)
+            ao = attention_map(q[b, None, ho], k[b, :L, kv], scale, False)
+            out[b, g] = ((ae - sigmoid(lam_logits[b, g]) * ao) @ v[b, :L, kv])[0]
+    return out

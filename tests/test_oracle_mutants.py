@@ -104,3 +104,16 @@ def test_decode_pins_catch_a_swapped_map(monkeypatch):
     monkeypatch.setattr(pins.oracle, "diff_attn_v1_decode", swapped)
     with pytest.raises(AssertionError):
         pins.test_decode_is_the_last_row_of_causal_attention()
+
+
+def test_v2_decode_pin_catches_swapped_pair(monkeypatch):
+    real = om.diff_attn_v2_decode
+
+    def swapped(q, k, v, lam_logits, lens=None, scale=None):
+        q = om._f64(q).copy()
+        q[:, 0::2], q[:, 1::2] = q[:, 1::2].copy(), q[:, 0::2].copy()  # odd head first
+        return real(q, k, v, lam_logits, lens, scale)
+
+    monkeypatch.setattr(pins.oracle, "diff_attn_v2_decode", swapped)
+    with pytest.raises(AssertionError):
+        pins.test_v2_decode_is_the_last_row_of_causal_v2()

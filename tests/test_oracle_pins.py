@@ -344,3 +344,41 @@ def test_decode_closed_forms():
     np.testing.assert_allclose(y1, (1 - lin) * o / np.sqrt((o * o).mean(axis=-1, keepdims=True) + eps), atol=1e-12)
     # No visible key: zeros (the reading for an empty cache).
     assert not np.any(oracle.diff_attn_v1_decode(q1, q2, k1, k2, v, lam, lin, None, eps, [0, 9, 0])[[0, 2]])
+
+
+def test_v2_decode_is_the_last_row_of_causal_v2():
+    r = _rng(40)
+    B, n, Hq, Hkv, d = 2, 7, 8, 2, 4
+    Q = r.normal(size=(B, n, Hq, d))
+    k, v = r.normal(size=(B, n, Hkv, d)), r.normal(size=(B, n, Hkv, d))
+    lg = r.normal(size=(B, n, Hq // 2))
+    full = oracle.diff_attn_v2(Q, k, v, lg, True, rows=[n - 1])[:, 0]
+    y = oracle.diff_attn_v2_decode(Q[:, -1], k, v, lg[:, -1])
+    np.testing.assert_allclose(y, full, atol=1e-12)
+
+
+def test_v2_decode_lengths_and_closed_forms():
+    r = _rng(41)
+    B, n, Hq, Hkv, d = 3, 6, 4, 1, 4
+    q = r.normal(size=(B, Hq, d))
+    k, v = r.normal(size=(B, n, Hkv, d)), r.normal(size=(B, n, Hkv, d))
+    lg = r.normal(size=(B, Hq // 2))
+    lens = [6, 2, 0]
+    y = oracle.diff_attn_v2_decode(q, k, v, lg, lens)
+    # Against the full-sequence oracle on the truncated cache, row by row.
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert not np.any(y[b])
+            continue
+        Q = np.zeros((1, L, Hq, d))
+        Q[0, -1] = q[b]
+        lgs = np.zeros((1, L, Hq // 2))
+        lgs[0, -1] = lg[b]
+        np.testing.assert_allclose(y[b], oracle.diff_attn_v2(Q, k[b:b + 1, :L], v[b:b + 1, :L], lgs, True,
+                                                             rows=[L - 1])[0, 0], atol=1e-12)
+    # Zero queries: uniform maps, out = (1 - sigmoid(logit)) mean(V) of the pair's KV head.
+    z = oracle.diff_attn_v2_decode(np.zeros_like(q), k, v, lg, [6, 3, 1])
+    for b, L in enumerate([6, 3, 1]):
+        for g in range(Hq // 2):
+            want = (1 - 1 / (1 + math.exp(-lg[b, g]))) * v[b, :L, 0].mean(axis=0)
+            np.testing.assert_allclose(z[b, g], want, atol=1e-12)
