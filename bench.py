@@ -276,9 +276,10 @@ def time_e2e(w, x, da, steps):
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
-DECODE_WORKLOADS = [  # (name, B, H, n, d): one new token per sequence over a key/value cache of n tokens
+DECODE_WORKLOADS = [  # (name, B, H or (Hq, Hkv), n, d): one new token per sequence over a cache of n tokens
     ("v1-decode-bf16-B8H16-n32768-d64", 8, 16, 32768, 64),
     ("v1-decode-bf16-B8H8-n32768-d128", 8, 8, 32768, 128),
+    ("v2-decode-bf16-B8Hq32Hkv16-n32768-d128", 8, (32, 16), 32768, 128),
 ]
 
 
@@ -289,14 +290,25 @@ def time_decode(da, flush, B, H, n, d, runs=20):
 
     def rnd(*shape):
         return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
-    q1, q2 = rnd(B, H, d), rnd(B, H, d)
-    k1, k2, v = rnd(B, n, H, d), rnd(B, n, H, d), rnd(B, n, H, 2 * d)
-    lam = torch.tensor([0.3], device="cuda")
-    gamma = torch.ones(2 * d, device="cuda")
-    out = torch.empty((B, H, 2 * d), device="cuda", dtype=torch.bfloat16)
+    if isinstance(H, tuple):  # DIFF V2: (Hq, Hkv)
+        Hq, Hkv = H
+        q, k, v = rnd(B, Hq, d), rnd(B, n, Hkv, d), rnd(B, n, Hkv, d)
+        lg = torch.randn((B, Hq // 2), generator=g, device="cuda")
+        out = torch.empty((B, Hq // 2, d), device="cuda", dtype=torch.bfloat16)
+        nbytes_kv = B * n * Hkv * 2 * d * 2 + B * (Hq + Hq // 2) * d * 2  # K and V once; q in, out
 
-    def call():
-        da.diffattn_decode(q1, q2, k1, k2, v, lam, 0.2, gamma=gamma, out=out)
+        def call():
+            da.diffattn_v2_decode(q, k, v, lg, out=out)
+    else:
+        q1, q2 = rnd(B, H, d), rnd(B, H, d)
+        k1, k2, v = rnd(B, n, H, d), rnd(B, n, H, d), rnd(B, n, H, 2 * d)
+        lam = torch.tensor([0.3], device="cuda")
+        gamma = torch.ones(2 * d, device="cuda")
+        out = torch.empty((B, H, 2 * d), device="cuda", dtype=torch.bfloat16)
+        nbytes_kv = B * H * n * 4 * d * 2 + B * H * 4 * d * 2  # K1, K2, V read once; q in, out
+
+        def call():
+            da.diffattn_decode(q1, q2, k1, k2, v, lam, 0.2, gamma=gamma, out=out)
     for _ in range(3):
         call()
     da.device_status()
@@ -311,10 +323,8 @@ def time_decode(da, flush, B, H, n, d, runs=20):
         ts.append(e0.elapsed_time(e1))
     da.device_status()
     ms = statistics.median(ts)
-    nbytes = B * H * n * 4 * d * 2 + B * H * 4 * d * 2  # K1, K2, V read once; q in, out
-    del q1, q2, k1, k2, v
     torch.cuda.empty_cache()
-    return ms, nbytes
+    return ms, nbytes_kv
 
 
 def cpu_baseline(w, x, budget_s=12.0):

@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
             L.diffattn_forward_host.restype = i
             L.diffattn_decode.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, f, vp, f, vp, vp]
             L.diffattn_decode.restype = i
+            L.diffattn_v2_decode.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, ll, f, vp, vp]
+            L.diffattn_v2_decode.restype = i
             L.diffattn_v2_forward.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, ll, ll, f, i, vp, vp]
             L.diffattn_v2_forward.restype = i
             L.diffattn_device_status.argtypes = [vp]
@@ -223,6 +225,36 @@ def diffattn_decode(q1, q2, k1, k2, v, lam, lambda_init_value: float, gamma=None
     _check(lib().diffattn_decode(_dt(k1), B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v),
                                  _ptr(lens), _ptr(lam), float(lambda_init_value), _ptr(gamma), float(eps),
                                  _ptr(out), _stream(stream)))
+    return out
+
+
+def diffattn_v2_decode(q, k, v, lam_logits, lens=None, softmax_scale: float = 0.0, out=None,
+                       stream=None) -> torch.Tensor:
+    """DIFF V2 decode: one new token per sequence over a key/value cache.
+
+    q: [B, Hq, d]; k, v: [B, n, Hkv, d] (bf16, d = 128); lam_logits: fp32
+    [B, Hq/2] (one logit per pair of each sequence) or [Hq/2] (shared by all
+    sequences); lens: int32 [B] or None.  Returns out [B, Hq/2, d].
+    """
+    B, n, Hkv, d = k.shape
+    Hq = q.shape[1]
+    dt = k.dtype
+    _need(q, "q", dt, (B, Hq, d))
+    _need(k, "k", dt, (B, n, Hkv, d))
+    _need(v, "v", dt, (B, n, Hkv, d))
+    if lam_logits.dim() == 1:
+        _need(lam_logits, "lam_logits", torch.float32, (Hq // 2,))
+        sb = 0
+    else:
+        _need(lam_logits, "lam_logits", torch.float32, (B, Hq // 2))
+        sb = Hq // 2
+    if lens is not None:
+        _need(lens, "lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, Hq // 2, d), device=k.device, dtype=dt)
+    _need(out, "out", dt, (B, Hq // 2, d))
+    _check(lib().diffattn_v2_decode(_dt(k), B, Hq, Hkv, n, d, _ptr(q), _ptr(k), _ptr(v), _ptr(lens),
+                                    _ptr(lam_logits), sb, float(softmax_scale), _ptr(out), _stream(stream)))
     return out
 
 

@@ -388,6 +388,18 @@ diffattn_status diffattn_forward_host(diffattn_dtype dt, int B, int H, int n, in
   return ok();
 }
 
+// CTAs per (batch, head) cluster of the decode kernels: the smallest power of
+// two that gives at least two waves of two CTAs per SM, at most 8 and at most
+// one CTA per four stages of keys.
+static int decode_cluster_size(long long units, int n, int bk) {
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  const long long want = 4ll * sms;
+  const int max_by_keys = std::max(1, n / (4 * bk));
+  int cs = 1;
+  while (cs < da::DecodeCfg<64>::MAX_CS && units * cs < want && cs * 2 <= max_by_keys) cs *= 2;
+  return cs;
+}
+
 diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, const void* q1, const void* q2,
                                 const void* k1, const void* k2, const void* v, const int* lens,
                                 const float* lambda, float lambda_init, const float* gamma, float eps, void* out,
@@ -430,15 +442,62 @@ diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, c
   p.H = H;
   p.n = n;
   p.status = status;
-  // CTAs per (b, h): the smallest power of two that gives at least two waves
-  // of two CTAs per SM, at most 8 and at most one CTA per four stages of keys.
-  const int sms = sm_count() > 0 ? sm_count() : 148;
-  const long long want = 4ll * sms;
-  const int max_by_keys = std::max(1, n / (4 * bk));
-  int cs = 1;
-  while (cs < da::DecodeCfg<64>::MAX_CS && units * cs < want && cs * 2 <= max_by_keys) cs *= 2;
+  const int cs = decode_cluster_size(units, n, bk);
   cudaError_t e = da::launch_decode_v1(p, d, static_cast<int>(units), cs, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_decode launch");
+  g_launches.fetch_add(1);
+  return ok();
+}
+
+diffattn_status diffattn_v2_decode(diffattn_dtype dt, int B, int Hq, int Hkv, int n, int d, const void* q,
+                                   const void* k, const void* v, const int* lens, const float* lam_logits,
+                                   long long sb, float softmax_scale, void* out, void* stream) {
+  if (dt != DIFFATTN_F32 && dt != DIFFATTN_BF16)
+    return fail(DIFFATTN_ERR_DTYPE, "diffattn_v2_decode: bad dtype %d", (int)dt);
+  if (B < 0 || Hq < 0 || Hkv < 1 || n < 0 || d < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_decode: bad sizes B=%d Hq=%d Hkv=%d n=%d d=%d", B, Hq, Hkv, n, d);
+  if (Hq % 2 != 0 || Hq % Hkv != 0 || (Hq / Hkv) % 2 != 0)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_decode: need Hq even, Hq %% Hkv == 0 and Hq/Hkv even (Hq=%d Hkv=%d)",
+                Hq, Hkv);
+  if (sb < 0) return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_decode: negative logit stride");
+  if (B == 0 || Hq == 0) return ok();
+  if (!q || !k || !v || !lam_logits || !out) return fail(DIFFATTN_ERR_NULL, "diffattn_v2_decode: NULL pointer");
+  if (dt != DIFFATTN_BF16 || d != 128)
+    return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_v2_decode: bf16 with d = 128 only (got dtype %d, d=%d)", (int)dt,
+                d);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_v2_decode: bf16 tensors must be 16-byte aligned");
+  const int G = Hq / 2;
+  const long long units = static_cast<long long>(B) * G;
+  if (units * da::DecodeCfg<128, true>::MAX_CS > 0x7fffffffll)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_decode: too many (batch, pair) units");
+  int* status = nullptr;
+  diffattn_status st = status_word(&status);
+  if (st != DIFFATTN_OK) return st;
+  da::DecodeParams p;
+  memset(&p, 0, sizeof(p));
+  constexpr int bk = da::DecodeCfg<128, true>::BK;
+  const int nn = n > 0 ? n : 1;  // an empty cache still needs a valid map (no key is read)
+  if ((st = make_map(&p.tm_k1, k, B, nn, Hkv, d, bk)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&p.tm_v, v, B, nn, Hkv, d, bk)) != DIFFATTN_OK) return st;
+  p.tm_k2 = p.tm_k1;
+  p.q1 = static_cast<const __nv_bfloat16*>(q);
+  p.q2 = p.q1;
+  p.lens = lens;
+  p.lam_logits = lam_logits;
+  p.sb = sb;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.f / std::sqrt(static_cast<float>(d));
+  p.scale_log2 = static_cast<float>(1.4426950408889634 * scale);
+  p.norm_mult = 1.f;
+  p.B = B;
+  p.H = G;
+  p.n = n;
+  p.group = Hq / Hkv;
+  p.status = status;
+  const int cs = decode_cluster_size(units, n, bk);
+  cudaError_t e = da::launch_decode_v2_d128(p, static_cast<int>(units), cs, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_decode launch");
   g_launches.fetch_add(1);
   return ok();
 }

@@ -8,6 +8,10 @@
 // keys and values sit in the cache ("Differential Transformer" glossary page,
 // "How differential attention works"; news article section "差分注意力" for
 // the per-head RMSNorm with the fixed (1 - lambda_init)).  L = 0 gives zeros.
+// DIFF V2 (template flag V2; DIFF V2 analysis page, "2. 커스텀 커널 제거" and
+// "GQA와의 호환성"): per (b, head pair g), query heads 2g and 2g + 1 over their
+// shared KV head, out = O_1 - sigmoid(logit[b, g]) O_2, no norm; the key tile
+// is then read once for both queries and V is d wide.
 //
 // The step is bound by HBM: every visible key's k_1, k_2 and v are read
 // exactly once (V once for both maps), 8 d bytes per key, against ~12 d
@@ -37,37 +41,41 @@
 namespace da {
 
 struct DecodeParams {
-  CUtensorMap tm_k1;  // [B, n, H, d] key caches, boxes of 64 columns x BK keys
-  CUtensorMap tm_k2;
-  CUtensorMap tm_v;   // [B, n, H, 2d]
-  const __nv_bfloat16* q1;  // [B, H, d]
-  const __nv_bfloat16* q2;
+  CUtensorMap tm_k1;  // V1: [B, n, H, d] key caches; V2: [B, n, Hkv, d]; boxes of 64 columns x BK keys
+  CUtensorMap tm_k2;  // (V1 only)
+  CUtensorMap tm_v;   // V1: [B, n, H, 2d]; V2: [B, n, Hkv, d]
+  const __nv_bfloat16* q1;  // V1: [B, H, d]; V2: q [B, Hq, d]
+  const __nv_bfloat16* q2;  // V1: [B, H, d]; V2: unused
   const int* lens;          // [B] visible keys, or nullptr: n for every sequence
-  const float* lambda;      // device scalar
-  const float* gamma;       // [2d] or nullptr
-  __nv_bfloat16* out;       // [B, H, 2d]
-  float scale_log2;         // log2(e) / sqrt(d)
-  float norm_mult;          // 1 - lambda_init
+  const float* lambda;      // V1: device scalar
+  const float* gamma;       // V1: [2d] or nullptr
+  const float* lam_logits;  // V2: logit of pair g of sequence b at b * sb + g
+  long long sb;
+  __nv_bfloat16* out;       // V1: [B, H, 2d]; V2: [B, Hq / 2, d]
+  float scale_log2;         // softmax scale * log2(e)
+  float norm_mult;          // V1: 1 - lambda_init
   float eps;
-  int B, H, n;
+  int B, H, n;  // H: V1 heads; V2 head pairs per sequence (Hq / 2)
+  int group;    // V2: query heads per KV head
   int* status;
 };
 
-template <int D>
+template <int D, bool V2 = false>
 struct DecodeCfg {
   static constexpr int MAX_CS = 8;  // CTAs per (b, h) cluster: chosen at launch, at most this (16-CTA
                                     // clusters measured slower: 5.5 vs 6.2 TB/s at B8 H8 n32768 d128)
-  static constexpr int NWARP = 4;
+  static constexpr int NWARP = V2 ? 8 : 4;  // V2: eight warps, so that a stage is 64 keys (32 KB)
   static constexpr int NTHREADS = NWARP * 32;
-  static constexpr int DV = 2 * D;
-  static constexpr int BK = D == 64 ? 64 : 32;  // keys per stage
+  static constexpr int DV = V2 ? D : 2 * D;     // value width
+  static constexpr int NKT = V2 ? 1 : 2;         // key tiles a stage holds (V2: one K for both queries)
+  static constexpr int BK = (V2 || D == 64) ? 64 : 32;  // keys per stage
   static constexpr int KW = BK / NWARP;         // keys per warp per stage
   static constexpr int PARTS = 32 / KW;         // lanes per key
   static constexpr int PE = D / PARTS;          // q . k products per lane (32)
   static constexpr int QB = D / 64, VB = DV / 64;
   static constexpr int K_BYTES = QB * BK * 128, V_BYTES = VB * BK * 128;
-  static constexpr int STAGE = 2 * K_BYTES + V_BYTES;
-  static constexpr int NST = 3;
+  static constexpr int STAGE = NKT * K_BYTES + V_BYTES;
+  static constexpr int NST = 3;  // 96 KB of stages in flight
   static constexpr int CH = DV / 32;  // output channels per lane and map
   static constexpr int PART_FLOATS = 2 * (DV + 2);  // per map: max, sum, DV channels
   static constexpr int OFF_BARS = NST * STAGE;
@@ -78,7 +86,8 @@ struct DecodeCfg {
   static constexpr int SMEM_BYTES = OFF_RED + NWARP * 4 + 1024;        // + 1 KB alignment slack
   static_assert(D == 64 || D == 128, "query/key width");
   static_assert(PE == 32 && PARTS * KW == 32, "lane split");
-  static_assert(STAGE == 32768, "stage size");
+  static_assert(NST * STAGE == 98304, "stage ring");
+  static_assert(!V2 || D == 128, "V2 decode: d = 128");
 };
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -110,9 +119,9 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t a, uint32_t rank) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-template <int D>
-__global__ void __launch_bounds__(128) decode_v1_kernel(const __grid_constant__ DecodeParams p) {
-  using C = DecodeCfg<D>;
+template <int D, bool V2>
+__global__ void __launch_bounds__(DecodeCfg<D, V2>::NTHREADS, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
+  using C = DecodeCfg<D, V2>;
   constexpr int BK = C::BK, KW = C::KW, PARTS = C::PARTS, DV = C::DV, CH = C::CH, NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -125,9 +134,13 @@ __global__ void __launch_bounds__(128) decode_v1_kernel(const __grid_constant__ 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t cs = cluster_nctarank();
-  const int unit = blockIdx.x / cs;  // (b, h)
+  const int unit = blockIdx.x / cs;  // (b, h), V2: (b, pair)
   const uint32_t rank = cluster_ctarank();
   const int b = unit / p.H, h = unit % p.H;
+  // Heads: V1 head h for everything; V2 query heads 2h, 2h + 1 over KV head 2h / group.
+  const int hk = V2 ? (2 * h) / p.group : h;
+  const size_t q1_off = V2 ? (static_cast<size_t>(b) * 2 * p.H + 2 * h) * D : (static_cast<size_t>(b) * p.H + h) * D;
+  const size_t q2_off = V2 ? q1_off + D : q1_off;
   int L = p.lens ? p.lens[b] : p.n;
   L = max(0, min(L, p.n));
   // This CTA's keys: [k_begin, k_end), a multiple of BK long except at L.
@@ -152,11 +165,11 @@ __global__ void __launch_bounds__(128) decode_v1_kernel(const __grid_constant__ 
     const int key0 = k_begin + i * BK;
     mbar_arrive_expect_tx(&full[i % NST], C::STAGE);
     for (int bx = 0; bx < C::QB; ++bx) {
-      tma_load_4d(st + bx * BK * 128, &p.tm_k1, &full[i % NST], bx * 64, h, key0, b);
-      tma_load_4d(st + C::K_BYTES + bx * BK * 128, &p.tm_k2, &full[i % NST], bx * 64, h, key0, b);
+      tma_load_4d(st + bx * BK * 128, &p.tm_k1, &full[i % NST], bx * 64, hk, key0, b);
+      if (!V2) tma_load_4d(st + C::K_BYTES + bx * BK * 128, &p.tm_k2, &full[i % NST], bx * 64, hk, key0, b);
     }
     for (int bx = 0; bx < C::VB; ++bx)
-      tma_load_4d(st + 2 * C::K_BYTES + bx * BK * 128, &p.tm_v, &full[i % NST], bx * 64, h, key0, b);
+      tma_load_4d(st + C::NKT * C::K_BYTES + bx * BK * 128, &p.tm_v, &full[i % NST], bx * 64, hk, key0, b);
   };
   int issued = 0;
   if (threadIdx.x == 0) {
@@ -170,8 +183,8 @@ __global__ void __launch_bounds__(128) decode_v1_kernel(const __grid_constant__ 
   const int kk = lane / PARTS, prt = lane % PARTS;
   float q1r[32], q2r[32];
   {
-    const __nv_bfloat16* q1p = p.q1 + (static_cast<size_t>(b) * p.H + h) * D + prt * 32;
-    const __nv_bfloat16* q2p = p.q2 + (static_cast<size_t>(b) * p.H + h) * D + prt * 32;
+    const __nv_bfloat16* q1p = p.q1 + q1_off + prt * 32;
+    const __nv_bfloat16* q2p = (V2 ? p.q1 : p.q2) + q2_off + prt * 32;
 #pragma unroll
     for (int i = 0; i < 32; i += 8) {
       const uint4 a = *reinterpret_cast<const uint4*>(q1p + i);
@@ -207,7 +220,7 @@ __global__ void __launch_bounds__(128) decode_v1_kernel(const __grid_constant__ 
     for (int c = 0; c < 4; ++c) {
       const int off = kbox * BK * 128 + row * 128 + (((kchunk0 + c) ^ (row & 7)) << 4);
       const uint4 a = *reinterpret_cast<const uint4*>(st + off);
-      const uint4 e = *reinterpret_cast<const uint4*>(st + C::K_BYTES + off);
+      const uint4 e = V2 ? a : *reinterpret_cast<const uint4*>(st + C::K_BYTES + off);  // V2: one key tile
       const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, we[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -251,7 +264,7 @@ __global__ void __launch_bounds__(128) decode_v1_kernel(const __grid_constant__ 
       ls2 += p2;
     }
     // ---- P.V: every lane accumulates its CH channels over the warp's keys
-    const uint8_t* vb = st + 2 * C::K_BYTES + vbox * BK * 128;
+    const uint8_t* vb = st + C::NKT * C::K_BYTES + vbox * BK * 128;
 #pragma unroll
     for (int k2 = 0; k2 < KW; ++k2) {
       const float w1 = __shfl_sync(0xffffffffu, p1, k2 * PARTS);
@@ -360,7 +373,8 @@ __global__ void __launch_bounds__(128) decode_v1_kernel(const __grid_constant__ 
       M2 = fmaxf(M2, ld_cluster_f32(pa + 8, r));
     }
     float l1 = 0.f, l2 = 0.f;
-    constexpr int CPT = DV / C::NTHREADS;  // channels per thread: 1 or 2
+    constexpr int CPT = DV > C::NTHREADS ? DV / C::NTHREADS : 1;  // channels per thread: 1 or 2
+    const bool has_ch = threadIdx.x < DV;                           // (V2: 128 channels, 256 threads)
     float y1[CPT], y2[CPT];
 #pragma unroll
     for (int t = 0; t < CPT; ++t) y1[t] = y2[t] = 0.f;
@@ -373,32 +387,38 @@ __global__ void __launch_bounds__(128) decode_v1_kernel(const __grid_constant__ 
 #pragma unroll
       for (int t = 0; t < CPT; ++t) {
         const int c = threadIdx.x + t * C::NTHREADS;
+        if (!has_ch) break;
         y1[t] = fmaf(ld_cluster_f32(pa + 4 * (4 + c), r), f1, y1[t]);
         y2[t] = fmaf(ld_cluster_f32(pa + 4 * (4 + DV + c), r), f2, y2[t]);
       }
     }
-    const float lam = *p.lambda;
+    // V1: c = lambda, then the per-head RMSNorm; V2: c = sigmoid(logit), no norm.
+    const float coef = V2 ? 1.f / (1.f + expf(-p.lam_logits[b * p.sb + h])) : *p.lambda;
     const float a1 = (l1 > 0.f) ? 1.f / l1 : 0.f;
-    const float a2 = (l2 > 0.f) ? -lam / l2 : 0.f;
+    const float a2 = (l2 > 0.f) ? -coef / l2 : 0.f;
     float y[CPT], ss = 0.f;
 #pragma unroll
     for (int t = 0; t < CPT; ++t) {
       y[t] = fmaf(y2[t], a2, y1[t] * a1);
       ss = fmaf(y[t], y[t], ss);
     }
+    float rinv = 1.f;
+    if (!V2) {
 #pragma unroll
-    for (int x = 1; x < 32; x <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, x);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    float tot = 0.f;
+      for (int x = 1; x < 32; x <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, x);
+      if (lane == 0) red[warp] = ss;
+      __syncthreads();
+      float tot = 0.f;
 #pragma unroll
-    for (int w = 0; w < C::NWARP; ++w) tot += red[w];
-    const float rinv = p.norm_mult * rsqrtf(tot * (1.f / DV) + p.eps);
+      for (int w = 0; w < C::NWARP; ++w) tot += red[w];
+      rinv = p.norm_mult * rsqrtf(tot * (1.f / DV) + p.eps);
+    }
     __nv_bfloat16* orow = p.out + (static_cast<size_t>(b) * p.H + h) * DV;
 #pragma unroll
     for (int t = 0; t < CPT; ++t) {
       const int c = threadIdx.x + t * C::NTHREADS;
-      const float g = p.gamma ? p.gamma[c] : 1.f;
+      if (!has_ch) break;
+      const float g = (!V2 && p.gamma) ? p.gamma[c] : 1.f;
       orow[c] = __float2bfloat16_rn(y[t] * rinv * g);
     }
   }

@@ -4,10 +4,10 @@
 
 namespace da {
 
-template <int D>
+template <int D, bool V2>
 static cudaError_t launch_decode(const DecodeParams& p, int units, int cs, cudaStream_t s) {
-  using C = DecodeCfg<D>;
-  auto kern = decode_v1_kernel<D>;
+  using C = DecodeCfg<D, V2>;
+  auto kern = decode_kernel<D, V2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -28,7 +28,11 @@ static cudaError_t launch_decode(const DecodeParams& p, int units, int cs, cudaS
 }
 
 cudaError_t launch_decode_v1(const DecodeParams& p, int d, int units, int cs, cudaStream_t s) {
-  return d == 64 ? launch_decode<64>(p, units, cs, s) : launch_decode<128>(p, units, cs, s);
+  return d == 64 ? launch_decode<64, false>(p, units, cs, s) : launch_decode<128, false>(p, units, cs, s);
+}
+
+cudaError_t launch_decode_v2_d128(const DecodeParams& p, int units, int cs, cudaStream_t s) {
+  return launch_decode<128, true>(p, units, cs, s);
 }
 
 }  // namespace da

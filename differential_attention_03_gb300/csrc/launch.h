@@ -23,6 +23,8 @@ cudaError_t launch_simt_f32(const SimtParams& p, cudaStream_t s);
 // V1 decode (one query per sequence over a key/value cache), d in {64, 128}:
 // a cluster of `cs` CTAs (1..8) over the keys of each of the `units` (batch, head) pairs.
 cudaError_t launch_decode_v1(const DecodeParams& p, int d, int units, int cs, cudaStream_t s);
+// V2 decode, d = 128: head pairs over their shared KV head (one key tile for both queries).
+cudaError_t launch_decode_v2_d128(const DecodeParams& p, int units, int cs, cudaStream_t s);
 cudaError_t launch_lambda_reparam(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
                                   int dim, float lambda_init, float* out, cudaStream_t s);
 cudaError_t launch_wait_selftest(unsigned long long budget_cycles, int* status, cudaStream_t s);

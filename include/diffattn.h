@@ -165,6 +165,33 @@ diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, c
                                 const float* gamma, float eps, void* out, void* stream);
 
 /*
+ * DIFF V2 decode step: one new token per sequence over a key/value cache
+ * (DIFF V2 analysis page, sections "2. 커스텀 커널 제거", "5. 간소화된 λ
+ * 매개변수화" and "GQA와의 호환성"): per head pair g of sequence b,
+ *
+ *   out_g = softmax(q_{2g} K_kv^T * scale) V_kv - sigmoid(logit[b*sb + g]) softmax(q_{2g+1} K_kv^T * scale) V_kv
+ *
+ * over the keys j < lens[b], kv = 2g / (Hq / Hkv); no norm.  The last row of
+ * diffattn_v2_forward for a causal sequence whose keys and values (the new
+ * token's included) are in the cache; each K/V tile is read once for both
+ * query heads of a pair.
+ *   dt          : DIFFATTN_BF16 with d = 128; other types / widths -> ERR_UNSUPPORTED.
+ *   q           : [B, Hq, d] device; k, v : [B, n, Hkv, d] device caches.
+ *   Hq even, Hq % Hkv == 0, (Hq / Hkv) even.
+ *   lens        : device int32 [B] (clamped to [0, n]) or NULL (n); a
+ *                 sequence with no visible key gets zeros.
+ *   lam_logits  : device fp32, the logit of pair g of sequence b at
+ *                 lam_logits[b*sb + g] (sb = 0: one logit per pair).
+ *   softmax_scale : <= 0 selects 1/sqrt(d).
+ *   out         : [B, Hq/2, d] device.
+ * No scratch memory; asynchronous on `stream`.  Errors as for diffattn_forward.
+ */
+diffattn_status diffattn_v2_decode(diffattn_dtype dt, int B, int Hq, int Hkv, int n, int d,
+                                   const void* q, const void* k, const void* v, const int* lens,
+                                   const float* lam_logits, long long sb, float softmax_scale,
+                                   void* out, void* stream);
+
+/*
  * DIFF V2 forward (DIFF V2 analysis page, sections "2. 커스텀 커널 제거",
  * "5. 간소화된 λ 매개변수화" and "GQA와의 호환성"): 2h query heads over h KV
  * heads, grouped-query attention, each even/odd pair of query heads inside

@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
     names = _declared()
     for want in ("diffattn_forward", "diffattn_v2_forward", "lambda_reparam", "diffattn_lambda_init",
                  "diffattn_device_status", "diffattn_last_error", "diffattn_forward_host",
-                 "diffattn_forward_host_workspace", "diffattn_decode"):
+                 "diffattn_forward_host_workspace", "diffattn_decode", "diffattn_v2_decode"):
         assert want in names
 
 
@@ -122,6 +122,18 @@ def test_decode_host_validation(L):
     assert call(dt=0) == da.ERR_UNSUPPORTED   # fp32 decode is not provided
     assert call(d=96) == da.ERR_UNSUPPORTED
     assert call(k1=MIS) == da.ERR_ALIGN
+
+
+def test_v2_decode_host_validation(L):
+    def call(dt=1, Hq=4, Hkv=2, n=8, d=128, q=A, sb=0):
+        return L.diffattn_v2_decode(dt, 1, Hq, Hkv, n, d, q, A, A, None, A, sb, ctypes.c_float(0.0), A, None)
+    assert call(Hq=3, Hkv=1) == da.ERR_SHAPE
+    assert call(Hq=6, Hkv=2) == da.ERR_SHAPE
+    assert call(sb=-1) == da.ERR_SHAPE
+    assert call(q=None) == da.ERR_NULL
+    assert call(d=64) == da.ERR_UNSUPPORTED
+    assert call(dt=0) == da.ERR_UNSUPPORTED
+    assert call(q=MIS) == da.ERR_ALIGN
 
 
 def test_v2_host_validation(L):

@@ -284,6 +284,48 @@ def test_v1_decode(B, H, n, d, lens):
                 assert not bool(out[b].float().abs().max() > 0)
 
 
+V2_DECODE = [  # B, Hq, Hkv, n, lens, per-sequence logits
+    (2, 4, 2, 300, None, True),
+    (3, 8, 2, 1000, [1000, 31, 0], False),   # group 4: two pairs per KV head; ragged, empty
+    (1, 2, 1, 1, None, True),
+    (2, 4, 1, 5000, [5000, 4097], True),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,n,lens,per_seq", V2_DECODE)
+def test_v2_decode(B, Hq, Hkv, n, lens, per_seq):
+    d = 128
+    g = torch.Generator(device="cuda").manual_seed(700 + n)
+
+    def rnd(*shape):
+        return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    q, k, v = rnd(B, Hq, d), rnd(B, n, Hkv, d), rnd(B, n, Hkv, d)
+    lg = torch.randn((B, Hq // 2) if per_seq else (Hq // 2,), generator=g, device="cuda")
+    lens_t = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = da.diffattn_v2_decode(q, k, v, lg, lens=lens_t)
+    da.device_status()
+    lg_host = lg.cpu().double().numpy() if per_seq else np.broadcast_to(lg.cpu().double().numpy(), (B, Hq // 2))
+    ref = oracle.diff_attn_v2_decode(q, k, v, lg_host, lens)
+    assert out.shape == (B, Hq // 2, d)
+    err = _err(_np(out), ref)
+    assert err <= TOL["bf16"], f"max abs error {err}"
+
+
+def test_v2_decode_bench_size():
+    B, Hq, Hkv, n, d = 8, 32, 16, 32768, 128
+    g = torch.Generator(device="cuda").manual_seed(1000 + n)
+
+    def rnd(*shape):
+        return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    q, k, v = rnd(B, Hq, d), rnd(B, n, Hkv, d), rnd(B, n, Hkv, d)
+    lg = torch.randn((B, Hq // 2), generator=g, device="cuda")
+    out = da.diffattn_v2_decode(q, k, v, lg)
+    da.device_status()
+    ref = oracle.diff_attn_v2_decode(q, k, v, lg.cpu().double().numpy())
+    err = _err(_np(out), ref)
+    assert err <= TOL["bf16"], f"max abs error {err}"
+
+
 @pytest.mark.parametrize("B,H,n,d", [(8, 16, 32768, 64), (8, 8, 32768, 128)])
 def test_v1_decode_bench_sizes(B, H, n, d):
     # The decode workloads bench.py times, in the same launch configuration,
