@@ -52,36 +52,37 @@ def hbm_bytes(w) -> float:
 # DRAM traffic of the dominant kernel per launch (dram__bytes_read.sum +
 # dram__bytes_write.sum) from one ncu --set full capture of each workload
 # (cold-cache replay; summaries under profiles/).  A figure holds only for the
-# kernel sources it was taken from: the bench reports it while the hash of
-# the kernel sources still matches, and null otherwise.
-NCU_TRAFFIC = {
-    "sources_sha256_16": "99a2a5f875d1ae3c",
-    "bytes_per_launch": {
-        "v1-bf16-B4H16-n2048-d64": 136.099840e6 + 14.131200e6,
-        "v1-bf16-B2H12-n4096-d128": 329.992448e6 + 29.970432e6,
-        "v2-bf16-B8Hq32Hkv16-n8192-d128": 1074.024e6 + 255.850240e6,
-    },
+# kernel it was taken from: it is keyed to the hash of that kernel's source
+# files and reported while the hash still matches, null otherwise.
+KERNEL_FILES = {
+    "v1-bf16-B4H16-n2048-d64": ['onepass.cuh', 'onepass_inst.cuh', 'k_onepass_v1_d64.cu', 'params.h', 'ptx.cuh', 'status.cuh'],
+    "v1-bf16-B2H12-n4096-d128": ['twopass.cuh', 'twopass_inst.cuh', 'k_twopass_v1_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh'],
+    "v2-bf16-B8Hq32Hkv16-n8192-d128": ['onepass.cuh', 'onepass_inst.cuh', 'k_onepass_v2_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh'],
+}
+NCU_TRAFFIC = {  # workload: (source hash of its kernel, bytes per launch)
+    "v1-bf16-B4H16-n2048-d64": ("413f0242e5ff72fd", 136.099840e6 + 14.131200e6),
+    "v1-bf16-B2H12-n4096-d128": ("292777c78dab3bb4", 329.992448e6 + 29.970432e6),
+    "v2-bf16-B8Hq32Hkv16-n8192-d128": ("bdd09c4f5ca33d5a", 1074.024e6 + 255.850240e6),
 }
 
 
-def kernel_sources_hash() -> str:
-    """Hash of the device-code sources (every csrc file but api.cu, the host side: argument checks,
-    descriptor encoding, launch selection and the host-buffer pipeline)."""
+def kernel_sources_hash(workload: str) -> str:
+    """Hash of the source files of the kernel that runs `workload`."""
     import hashlib
     d = os.path.join(ROOT, "differential_attention_03_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")) and f != "api.cu":
-            h.update(f.encode())
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+    for f in sorted(KERNEL_FILES.get(workload, [])):
+        h.update(f.encode())
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(workload: str):
-    if kernel_sources_hash() != NCU_TRAFFIC["sources_sha256_16"]:
+    if workload not in NCU_TRAFFIC:
         return None
-    return NCU_TRAFFIC["bytes_per_launch"].get(workload)
+    digest, nbytes = NCU_TRAFFIC[workload]
+    return nbytes if kernel_sources_hash(workload) == digest else None
 
 
 def read_peaks():
