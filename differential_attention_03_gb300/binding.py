@@ -57,9 +57,15 @@ def lib() -> ctypes.CDLL:
             L.diffattn_forward_host.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, f, vp, f, i, vp, vp,
                                                 ctypes.c_size_t, vp]
             L.diffattn_forward_host.restype = i
-            L.diffattn_decode.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, f, vp, f, vp, vp]
+            L.diffattn_decode_workspace.argtypes = [i, i, i]
+            L.diffattn_decode_workspace.restype = ctypes.c_size_t
+            L.diffattn_v2_decode_workspace.argtypes = [i, i, i]
+            L.diffattn_v2_decode_workspace.restype = ctypes.c_size_t
+            L.diffattn_decode.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, f, vp, f, vp, vp,
+                                          ctypes.c_size_t, vp]
             L.diffattn_decode.restype = i
-            L.diffattn_v2_decode.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, ll, f, vp, vp]
+            L.diffattn_v2_decode.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, ll, f, vp, vp, ctypes.c_size_t,
+                                             vp]
             L.diffattn_v2_decode.restype = i
             L.diffattn_v2_forward.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, ll, ll, f, i, vp, vp]
             L.diffattn_v2_forward.restype = i
@@ -199,13 +205,32 @@ def diffattn_forward_host(q1, q2, k1, k2, v, lam, lambda_init_value: float, gamm
     return out
 
 
+def _ws_args(workspace, need):
+    if workspace is None:
+        return None, 0
+    nbytes = workspace.numel() * workspace.element_size()
+    if not workspace.is_cuda or nbytes < need:
+        raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
+    return _ptr(workspace), nbytes
+
+
+def decode_workspace_bytes(B: int, H: int, d: int) -> int:
+    """Device workspace that lets diffattn_decode split a (b, h) pair over several clusters."""
+    return int(lib().diffattn_decode_workspace(B, H, d))
+
+
+def v2_decode_workspace_bytes(B: int, Hq: int, d: int) -> int:
+    return int(lib().diffattn_v2_decode_workspace(B, Hq, d))
+
+
 def diffattn_decode(q1, q2, k1, k2, v, lam, lambda_init_value: float, gamma=None, eps: float = 1e-5,
-                    lens=None, out=None, stream=None) -> torch.Tensor:
+                    lens=None, out=None, workspace=None, stream=None) -> torch.Tensor:
     """DIFF V1 decode: one new token per sequence over a key/value cache.
 
     q1, q2: [B, H, d]; k1, k2: [B, n, H, d]; v: [B, n, H, 2d] (bf16, d in
     {64, 128}); lens: int32 [B] visible keys per sequence or None (all n).
-    Returns out [B, H, 2d].
+    workspace: None or a device tensor of decode_workspace_bytes(B, H, d)
+    bytes (lets few (b, h) pairs use the whole GPU).  Returns out [B, H, 2d].
     """
     B, n, H, d = k1.shape
     dt = k1.dtype
@@ -222,14 +247,15 @@ def diffattn_decode(q1, q2, k1, k2, v, lam, lambda_init_value: float, gamma=None
     if out is None:
         out = torch.empty((B, H, 2 * d), device=k1.device, dtype=dt)
     _need(out, "out", dt, (B, H, 2 * d))
+    wp, wn = _ws_args(workspace, decode_workspace_bytes(B, H, d))
     _check(lib().diffattn_decode(_dt(k1), B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v),
                                  _ptr(lens), _ptr(lam), float(lambda_init_value), _ptr(gamma), float(eps),
-                                 _ptr(out), _stream(stream)))
+                                 _ptr(out), wp, wn, _stream(stream)))
     return out
 
 
 def diffattn_v2_decode(q, k, v, lam_logits, lens=None, softmax_scale: float = 0.0, out=None,
-                       stream=None) -> torch.Tensor:
+                       workspace=None, stream=None) -> torch.Tensor:
     """DIFF V2 decode: one new token per sequence over a key/value cache.
 
     q: [B, Hq, d]; k, v: [B, n, Hkv, d] (bf16, d = 128); lam_logits: fp32
@@ -253,8 +279,10 @@ def diffattn_v2_decode(q, k, v, lam_logits, lens=None, softmax_scale: float = 0.
     if out is None:
         out = torch.empty((B, Hq // 2, d), device=k.device, dtype=dt)
     _need(out, "out", dt, (B, Hq // 2, d))
+    wp, wn = _ws_args(workspace, v2_decode_workspace_bytes(B, Hq, d))
     _check(lib().diffattn_v2_decode(_dt(k), B, Hq, Hkv, n, d, _ptr(q), _ptr(k), _ptr(v), _ptr(lens),
-                                    _ptr(lam_logits), sb, float(softmax_scale), _ptr(out), _stream(stream)))
+                                    _ptr(lam_logits), sb, float(softmax_scale), _ptr(out), wp, wn,
+                                    _stream(stream)))
     return out
 
 

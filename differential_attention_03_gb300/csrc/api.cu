@@ -400,10 +400,35 @@ static int decode_cluster_size(long long units, int n, int bk) {
   return cs;
 }
 
+// Clusters per (batch, head) when a workspace is given: as many as keep the
+// grid within one wave of two CTAs per SM (so that pairs too few to fill the
+// GPU with one cluster each still do), at most kMaxSplit, each CTA keeping at
+// least four stages of keys.
+constexpr int kMaxSplit = 8;
+static int decode_split(long long units, int cs, int n, int bk) {
+  const int sms = sm_count() > 0 ? sm_count() : 148;
+  int ns = static_cast<int>(std::min<long long>(kMaxSplit, (2ll * sms) / std::max<long long>(1, units * cs)));
+  ns = std::max(1, std::min(ns, n / (4 * bk * cs)));
+  return ns;
+}
+
+// Partial-state floats of one cluster: two maps x (maximum, sum, dv channels).
+static size_t decode_part_floats(int dv) { return 2 * (static_cast<size_t>(dv) + 2); }
+
+size_t diffattn_decode_workspace(int B, int H, int d) {
+  if (B < 0 || H < 0 || d < 1) return 0;
+  return static_cast<size_t>(B) * H * kMaxSplit * decode_part_floats(2 * d) * sizeof(float);
+}
+
+size_t diffattn_v2_decode_workspace(int B, int Hq, int d) {
+  if (B < 0 || Hq < 0 || d < 1) return 0;
+  return static_cast<size_t>(B) * (Hq / 2) * kMaxSplit * decode_part_floats(d) * sizeof(float);
+}
+
 diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, const void* q1, const void* q2,
                                 const void* k1, const void* k2, const void* v, const int* lens,
                                 const float* lambda, float lambda_init, const float* gamma, float eps, void* out,
-                                void* stream) {
+                                void* workspace, size_t workspace_bytes, void* stream) {
   if (dt != DIFFATTN_F32 && dt != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "diffattn_decode: bad dtype %d", (int)dt);
   if (B < 0 || H < 0 || n < 0 || d < 1)
     return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode: bad sizes B=%d H=%d n=%d d=%d", B, H, n, d);
@@ -416,7 +441,7 @@ diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, c
   if (!aligned16(q1) || !aligned16(q2) || !aligned16(k1) || !aligned16(k2) || !aligned16(v) || !aligned16(out))
     return fail(DIFFATTN_ERR_ALIGN, "diffattn_decode: bf16 tensors must be 16-byte aligned");
   const long long units = static_cast<long long>(B) * H;
-  if (units * da::DecodeCfg<64>::MAX_CS > 0x7fffffffll)
+  if (units * da::DecodeCfg<64>::MAX_CS * kMaxSplit > 0x7fffffffll)
     return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode: too many (batch, head) pairs");
   if (eps <= 0.f) eps = 1e-5f;
   int* status = nullptr;
@@ -443,6 +468,11 @@ diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, c
   p.n = n;
   p.status = status;
   const int cs = decode_cluster_size(units, n, bk);
+  p.nsplit = 1;
+  if (workspace != nullptr && workspace_bytes >= diffattn_decode_workspace(B, H, d)) {
+    p.nsplit = decode_split(units, cs, n, bk);
+    p.ws = static_cast<float*>(workspace);
+  }
   cudaError_t e = da::launch_decode_v1(p, d, static_cast<int>(units), cs, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_decode launch");
   g_launches.fetch_add(1);
@@ -451,7 +481,8 @@ diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, c
 
 diffattn_status diffattn_v2_decode(diffattn_dtype dt, int B, int Hq, int Hkv, int n, int d, const void* q,
                                    const void* k, const void* v, const int* lens, const float* lam_logits,
-                                   long long sb, float softmax_scale, void* out, void* stream) {
+                                   long long sb, float softmax_scale, void* out, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
   if (dt != DIFFATTN_F32 && dt != DIFFATTN_BF16)
     return fail(DIFFATTN_ERR_DTYPE, "diffattn_v2_decode: bad dtype %d", (int)dt);
   if (B < 0 || Hq < 0 || Hkv < 1 || n < 0 || d < 1)
@@ -469,7 +500,7 @@ diffattn_status diffattn_v2_decode(diffattn_dtype dt, int B, int Hq, int Hkv, in
     return fail(DIFFATTN_ERR_ALIGN, "diffattn_v2_decode: bf16 tensors must be 16-byte aligned");
   const int G = Hq / 2;
   const long long units = static_cast<long long>(B) * G;
-  if (units * da::DecodeCfg<128, true>::MAX_CS > 0x7fffffffll)
+  if (units * da::DecodeCfg<128, true>::MAX_CS * kMaxSplit > 0x7fffffffll)
     return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_decode: too many (batch, pair) units");
   int* status = nullptr;
   diffattn_status st = status_word(&status);
@@ -496,6 +527,11 @@ diffattn_status diffattn_v2_decode(diffattn_dtype dt, int B, int Hq, int Hkv, in
   p.group = Hq / Hkv;
   p.status = status;
   const int cs = decode_cluster_size(units, n, bk);
+  p.nsplit = 1;
+  if (workspace != nullptr && workspace_bytes >= diffattn_v2_decode_workspace(B, Hq, d)) {
+    p.nsplit = decode_split(units, cs, n, bk);
+    p.ws = static_cast<float*>(workspace);
+  }
   cudaError_t e = da::launch_decode_v2_d128(p, static_cast<int>(units), cs, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_decode launch");
   g_launches.fetch_add(1);

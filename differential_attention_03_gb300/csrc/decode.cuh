@@ -30,7 +30,10 @@
 //   * The CTA merges its warps' states in shared memory; the cluster's CTAs
 //     then merge theirs through distributed shared memory in CTA rank 0,
 //     which applies the combine and the per-head RMSNorm and stores the row.
-//     No global scratch.
+//     No global scratch.  With few (b, h) pairs the caller may pass a
+//     workspace: then nsplit clusters share a pair's keys, rank 0 of each
+//     writes the cluster's state there, and decode_combine_kernel merges the
+//     nsplit states of a pair and finishes the row.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -57,6 +60,8 @@ struct DecodeParams {
   float eps;
   int B, H, n;  // H: V1 heads; V2 head pairs per sequence (Hq / 2)
   int group;    // V2: query heads per KV head
+  int nsplit;   // clusters per (b, h); > 1: each writes its state to ws and a combine kernel finishes
+  float* ws;    // [B * H][nsplit][2 (DV + 2)] partial states (nsplit > 1)
   int* status;
 };
 
@@ -119,6 +124,82 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t a, uint32_t rank) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Finishes row (b, h) from its merged state (sums l1, l2; unnormalised
+// outputs y1, y2 of this thread's channels threadIdx.x + t NTHREADS): the
+// combine (V1: lambda, V2: sigmoid(logit)), V1's per-head RMSNorm, the store.
+// Every thread of the CTA calls it (it holds a CTA barrier for V1).
+template <int D, bool V2, int NTHREADS, int CPT>
+__device__ __forceinline__ void decode_finish(const DecodeParams& p, int b, int h, float l1, float l2,
+                                              const float (&y1)[CPT], const float (&y2)[CPT], float* red) {
+  constexpr int DV = V2 ? D : 2 * D;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool has_ch = threadIdx.x < DV;
+  const float coef = V2 ? 1.f / (1.f + expf(-p.lam_logits[b * p.sb + h])) : *p.lambda;
+  const float a1 = (l1 > 0.f) ? 1.f / l1 : 0.f;
+  const float a2 = (l2 > 0.f) ? -coef / l2 : 0.f;
+  float y[CPT], ss = 0.f;
+#pragma unroll
+  for (int t = 0; t < CPT; ++t) {
+    y[t] = has_ch ? fmaf(y2[t], a2, y1[t] * a1) : 0.f;
+    ss = fmaf(y[t], y[t], ss);
+  }
+  float rinv = 1.f;
+  if (!V2) {
+#pragma unroll
+    for (int x = 1; x < 32; x <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, x);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < NTHREADS / 32; ++w) tot += red[w];
+    rinv = p.norm_mult * rsqrtf(tot * (1.f / DV) + p.eps);
+  }
+  __nv_bfloat16* orow = p.out + (static_cast<size_t>(b) * p.H + h) * DV;
+#pragma unroll
+  for (int t = 0; t < CPT; ++t) {
+    const int c = threadIdx.x + t * NTHREADS;
+    if (!has_ch) break;
+    const float g = (!V2 && p.gamma) ? p.gamma[c] : 1.f;
+    orow[c] = __float2bfloat16_rn(y[t] * rinv * g);
+  }
+}
+
+// Merges the nsplit cluster states of each (b, h) pair (one CTA per pair)
+// written by decode_kernel into p.ws, and finishes the row.
+template <int D, bool V2>
+__global__ void __launch_bounds__(DecodeCfg<D, V2>::NTHREADS) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
+  using C = DecodeCfg<D, V2>;
+  constexpr int DV = C::DV;
+  constexpr int CPT = DV > C::NTHREADS ? DV / C::NTHREADS : 1;
+  __shared__ float red[C::NWARP];
+  const int unit = blockIdx.x;
+  const int b = unit / p.H, h = unit % p.H;
+  const float* src = p.ws + static_cast<size_t>(unit) * p.nsplit * C::PART_FLOATS;
+  float M1 = -INFINITY, M2 = -INFINITY;
+  for (int r = 0; r < p.nsplit; ++r) {
+    M1 = fmaxf(M1, src[r * C::PART_FLOATS]);
+    M2 = fmaxf(M2, src[r * C::PART_FLOATS + 2]);
+  }
+  float l1 = 0.f, l2 = 0.f, y1[CPT], y2[CPT];
+#pragma unroll
+  for (int t = 0; t < CPT; ++t) y1[t] = y2[t] = 0.f;
+  for (int r = 0; r < p.nsplit; ++r) {
+    const float* sr = src + r * C::PART_FLOATS;
+    const float f1 = (sr[0] == -INFINITY) ? 0.f : ex2(sr[0] - M1);
+    const float f2 = (sr[2] == -INFINITY) ? 0.f : ex2(sr[2] - M2);
+    l1 = fmaf(sr[1], f1, l1);
+    l2 = fmaf(sr[3], f2, l2);
+#pragma unroll
+    for (int t = 0; t < CPT; ++t) {
+      const int c = threadIdx.x + t * C::NTHREADS;
+      if (c >= DV) break;
+      y1[t] = fmaf(sr[4 + c], f1, y1[t]);
+      y2[t] = fmaf(sr[4 + DV + c], f2, y2[t]);
+    }
+  }
+  decode_finish<D, V2, C::NTHREADS, CPT>(p, b, h, l1, l2, y1, y2, red);
+}
+
 template <int D, bool V2>
 __global__ void __launch_bounds__(DecodeCfg<D, V2>::NTHREADS, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
   using C = DecodeCfg<D, V2>;
@@ -134,7 +215,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2>::NTHREADS, 2) decode_kernel(c
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t cs = cluster_nctarank();
-  const int unit = blockIdx.x / cs;  // (b, h), V2: (b, pair)
+  const int cluster = static_cast<int>(blockIdx.x / cs);
+  const int unit = cluster / p.nsplit;  // (b, h), V2: (b, pair)
+  const int split = cluster % p.nsplit;  // which share of the pair's keys this cluster takes
   const uint32_t rank = cluster_ctarank();
   const int b = unit / p.H, h = unit % p.H;
   // Heads: V1 head h for everything; V2 query heads 2h, 2h + 1 over KV head 2h / group.
@@ -144,8 +227,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2>::NTHREADS, 2) decode_kernel(c
   int L = p.lens ? p.lens[b] : p.n;
   L = max(0, min(L, p.n));
   // This CTA's keys: [k_begin, k_end), a multiple of BK long except at L.
-  const int chunk = ((L + static_cast<int>(cs) * BK - 1) / (static_cast<int>(cs) * BK)) * BK;
-  const int k_begin = min(L, static_cast<int>(rank) * chunk);
+  const int nct = static_cast<int>(cs) * p.nsplit;  // CTAs sharing the pair's keys
+  const int chunk = ((L + nct * BK - 1) / (nct * BK)) * BK;
+  const int k_begin = min(L, (split * static_cast<int>(cs) + static_cast<int>(rank)) * chunk);
   const int k_end = min(L, k_begin + chunk);
   const int nblk = (k_end - k_begin + BK - 1) / BK;
 
@@ -392,34 +476,24 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2>::NTHREADS, 2) decode_kernel(c
         y2[t] = fmaf(ld_cluster_f32(pa + 4 * (4 + DV + c), r), f2, y2[t]);
       }
     }
-    // V1: c = lambda, then the per-head RMSNorm; V2: c = sigmoid(logit), no norm.
-    const float coef = V2 ? 1.f / (1.f + expf(-p.lam_logits[b * p.sb + h])) : *p.lambda;
-    const float a1 = (l1 > 0.f) ? 1.f / l1 : 0.f;
-    const float a2 = (l2 > 0.f) ? -coef / l2 : 0.f;
-    float y[CPT], ss = 0.f;
+    if (p.nsplit > 1) {
+      // This cluster's state of the pair: the combine kernel finishes the row.
+      float* dst = p.ws + (static_cast<size_t>(unit) * p.nsplit + split) * C::PART_FLOATS;
+      if (threadIdx.x == 0) {
+        dst[0] = M1;
+        dst[1] = l1;
+        dst[2] = M2;
+        dst[3] = l2;
+      }
 #pragma unroll
-    for (int t = 0; t < CPT; ++t) {
-      y[t] = fmaf(y2[t], a2, y1[t] * a1);
-      ss = fmaf(y[t], y[t], ss);
-    }
-    float rinv = 1.f;
-    if (!V2) {
-#pragma unroll
-      for (int x = 1; x < 32; x <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, x);
-      if (lane == 0) red[warp] = ss;
-      __syncthreads();
-      float tot = 0.f;
-#pragma unroll
-      for (int w = 0; w < C::NWARP; ++w) tot += red[w];
-      rinv = p.norm_mult * rsqrtf(tot * (1.f / DV) + p.eps);
-    }
-    __nv_bfloat16* orow = p.out + (static_cast<size_t>(b) * p.H + h) * DV;
-#pragma unroll
-    for (int t = 0; t < CPT; ++t) {
-      const int c = threadIdx.x + t * C::NTHREADS;
-      if (!has_ch) break;
-      const float g = (!V2 && p.gamma) ? p.gamma[c] : 1.f;
-      orow[c] = __float2bfloat16_rn(y[t] * rinv * g);
+      for (int t = 0; t < CPT; ++t) {
+        const int c = threadIdx.x + t * C::NTHREADS;
+        if (!has_ch) break;
+        dst[4 + c] = y1[t];
+        dst[4 + DV + c] = y2[t];
+      }
+    } else {
+      decode_finish<D, V2, C::NTHREADS, CPT>(p, b, h, l1, l2, y1, y2, red);
     }
   }
   cluster_sync_all();  // rank 0 has read every CTA's state: they may exit

@@ -1,4 +1,5 @@
-// Launchers of the decode kernel (clusters of `cs` CTAs per (batch, head)).
+// Launchers of the decode kernel (p.nsplit clusters of `cs` CTAs per (batch, head), then the
+// combine kernel when p.nsplit > 1).
 #include "decode.cuh"
 #include "launch.h"
 
@@ -11,7 +12,7 @@ static cudaError_t launch_decode(const DecodeParams& p, int units, int cs, cudaS
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(units) * static_cast<unsigned>(cs), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(units) * static_cast<unsigned>(p.nsplit) * static_cast<unsigned>(cs), 1, 1);
   cfg.blockDim = dim3(C::NTHREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = s;
@@ -24,6 +25,9 @@ static cudaError_t launch_decode(const DecodeParams& p, int units, int cs, cudaS
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return e;
+  if (p.nsplit > 1) {  // merge the clusters' states of every (b, h) and finish the rows
+    decode_combine_kernel<D, V2><<<units, C::NTHREADS, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -156,13 +156,22 @@ diffattn_status diffattn_forward_host(diffattn_dtype dt, int B, int H, int n, in
  *                 visible key gets an all-zero output.
  *   lambda, lambda_init, gamma, eps : as for diffattn_forward.
  *   out         : [B, H, 2d] device.
- * Memory-bound: K1, K2 and V are read once (V for both maps).  No scratch
- * memory; asynchronous on `stream`.  Errors as for diffattn_forward.
+ *   workspace   : NULL, or device memory the caller owns of at least
+ *                 diffattn_decode_workspace(B, H, d) bytes (4-byte aligned).
+ *                 With it, when there are too few (b, h) pairs to fill the GPU,
+ *                 several thread-block clusters share a pair's keys and a second
+ *                 small kernel merges their states; results are the same up
+ *                 to fp32 rounding order.  Without it nothing is allocated.
+ * Memory-bound: K1, K2 and V are read once (V for both maps); asynchronous
+ * on `stream`.  Errors as for diffattn_forward.
  */
+size_t diffattn_decode_workspace(int B, int H, int d);
+
 diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, const void* q1,
                                 const void* q2, const void* k1, const void* k2, const void* v,
                                 const int* lens, const float* lambda, float lambda_init,
-                                const float* gamma, float eps, void* out, void* stream);
+                                const float* gamma, float eps, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream);
 
 /*
  * DIFF V2 decode step: one new token per sequence over a key/value cache
@@ -184,12 +193,17 @@ diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, c
  *                 lam_logits[b*sb + g] (sb = 0: one logit per pair).
  *   softmax_scale : <= 0 selects 1/sqrt(d).
  *   out         : [B, Hq/2, d] device.
- * No scratch memory; asynchronous on `stream`.  Errors as for diffattn_forward.
+ *   workspace   : NULL, or at least diffattn_v2_decode_workspace(B, Hq, d)
+ *                 bytes of device memory, as for diffattn_decode.
+ * Asynchronous on `stream`.  Errors as for diffattn_forward.
  */
+size_t diffattn_v2_decode_workspace(int B, int Hq, int d);
+
 diffattn_status diffattn_v2_decode(diffattn_dtype dt, int B, int Hq, int Hkv, int n, int d,
                                    const void* q, const void* k, const void* v, const int* lens,
                                    const float* lam_logits, long long sb, float softmax_scale,
-                                   void* out, void* stream);
+                                   void* out, void* workspace, size_t workspace_bytes,
+                                   void* stream);
 
 /*
  * DIFF V2 forward (DIFF V2 analysis page, sections "2. 커스텀 커널 제거",

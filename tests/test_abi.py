@@ -33,7 +33,8 @@ def test_header_declares_the_entry_points():
     names = _declared()
     for want in ("diffattn_forward", "diffattn_v2_forward", "lambda_reparam", "diffattn_lambda_init",
                  "diffattn_device_status", "diffattn_last_error", "diffattn_forward_host",
-                 "diffattn_forward_host_workspace", "diffattn_decode", "diffattn_v2_decode"):
+                 "diffattn_forward_host_workspace", "diffattn_decode", "diffattn_v2_decode",
+                 "diffattn_decode_workspace", "diffattn_v2_decode_workspace"):
         assert want in names
 
 
@@ -113,7 +114,7 @@ def test_forward_host_buffer_validation(L):
 def test_decode_host_validation(L):
     def call(dt=1, B=1, n=8, d=64, q1=A, out=A, k1=A):
         return L.diffattn_decode(dt, B, 2, n, d, q1, A, k1, A, A, None, A, ctypes.c_float(0.2), None,
-                                 ctypes.c_float(1e-5), out, None)
+                                 ctypes.c_float(1e-5), out, None, 0, None)
     assert call(dt=7) == da.ERR_DTYPE
     assert call(n=-1) == da.ERR_SHAPE
     assert call(B=0) == da.OK
@@ -124,9 +125,17 @@ def test_decode_host_validation(L):
     assert call(k1=MIS) == da.ERR_ALIGN
 
 
+def test_decode_workspace_sizes(L):
+    # Eight cluster states per (b, h) at most, each two maps x (maximum, sum, value-width channels), fp32.
+    assert L.diffattn_decode_workspace(8, 16, 64) == 8 * 16 * 8 * 2 * (128 + 2) * 4
+    assert L.diffattn_v2_decode_workspace(8, 32, 128) == 8 * 16 * 8 * 2 * (128 + 2) * 4
+    assert L.diffattn_decode_workspace(-1, 16, 64) == 0
+
+
 def test_v2_decode_host_validation(L):
     def call(dt=1, Hq=4, Hkv=2, n=8, d=128, q=A, sb=0):
-        return L.diffattn_v2_decode(dt, 1, Hq, Hkv, n, d, q, A, A, None, A, sb, ctypes.c_float(0.0), A, None)
+        return L.diffattn_v2_decode(dt, 1, Hq, Hkv, n, d, q, A, A, None, A, sb, ctypes.c_float(0.0), A, None, 0,
+                                    None)
     assert call(Hq=3, Hkv=1) == da.ERR_SHAPE
     assert call(Hq=6, Hkv=2) == da.ERR_SHAPE
     assert call(sb=-1) == da.ERR_SHAPE

@@ -261,6 +261,44 @@ DECODE = [  # B, H, n, d, lens
 ]
 
 
+@pytest.mark.parametrize("B,H,n,d,lens", [(1, 2, 40000, 64, None), (2, 3, 9000, 128, [9000, 2500]),
+                                             (1, 4, 3000, 64, [1])])
+def test_v1_decode_split_over_clusters(B, H, n, d, lens):
+    # With a workspace, the few (b, h) pairs spread over several clusters each; the
+    # combine kernel merges their states.  Same operator, fp32 rounding order only.
+    w = shrink(WORKLOADS[2], B=B, H=H, n=n, d=d, gamma="uniform", layer=4, seed=95 + n)
+    x = make_v1(w, "cuda")
+    g = torch.Generator(device="cuda").manual_seed(96 + n)
+    q1 = torch.randn((B, H, d), generator=g, device="cuda").to(torch.bfloat16)
+    q2 = torch.randn((B, H, d), generator=g, device="cuda").to(torch.bfloat16)
+    lin = da.lambda_init(w.layer)
+    lam = da.lambda_reparam(x["lq1"], x["lk1"], x["lq2"], x["lk2"], lin)
+    lens_t = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
+    ws = torch.empty(da.decode_workspace_bytes(B, H, d), dtype=torch.uint8, device="cuda")
+    out = da.diffattn_decode(q1, q2, x["k1"], x["k2"], x["v"], lam, lin, gamma=x["gamma"], lens=lens_t, workspace=ws)
+    one = da.diffattn_decode(q1, q2, x["k1"], x["k2"], x["v"], lam, lin, gamma=x["gamma"], lens=lens_t)
+    da.device_status()
+    ref = oracle.diff_attn_v1_decode(q1, q2, x["k1"], x["k2"], x["v"], float(lam.item()), lin,
+                                     x["gamma"].cpu(), 1e-5, lens)
+    assert _err(_np(out), ref) <= TOL["bf16"]
+    assert _err(_np(out), _np(one)) <= 1.6e-2  # a bf16 ulp or two where rounding orders differ
+
+
+def test_v2_decode_split_over_clusters():
+    B, Hq, Hkv, n, d = 1, 4, 2, 30000, 128
+    g = torch.Generator(device="cuda").manual_seed(77)
+
+    def rnd(*shape):
+        return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    q, k, v = rnd(B, Hq, d), rnd(B, n, Hkv, d), rnd(B, n, Hkv, d)
+    lg = torch.randn((B, Hq // 2), generator=g, device="cuda")
+    ws = torch.empty(da.v2_decode_workspace_bytes(B, Hq, d), dtype=torch.uint8, device="cuda")
+    out = da.diffattn_v2_decode(q, k, v, lg, workspace=ws)
+    da.device_status()
+    ref = oracle.diff_attn_v2_decode(q, k, v, lg.cpu().double().numpy())
+    assert _err(_np(out), ref) <= TOL["bf16"]
+
+
 @pytest.mark.parametrize("B,H,n,d,lens", DECODE)
 def test_v1_decode(B, H, n, d, lens):
     w = shrink(WORKLOADS[2], B=B, H=H, n=n, d=d, gamma="uniform", layer=3, seed=90 + n)
