@@ -281,6 +281,8 @@ DECODE_WORKLOADS = [  # (name, B, H or (Hq, Hkv), n, d): one new token per seque
     ("v1-decode-bf16-B8H16-n32768-d64", 8, 16, 32768, 64),
     ("v1-decode-bf16-B8H8-n32768-d128", 8, 8, 32768, 128),
     ("v2-decode-bf16-B8Hq32Hkv16-n32768-d128", 8, (32, 16), 32768, 128),
+    # one sequence, long cache: the pairs are split over clusters through the workspace
+    ("v1-decode-bf16-B1H16-n131072-d64-workspace", 1, 16, 131072, 64),
 ]
 
 
@@ -298,8 +300,10 @@ def time_decode(da, flush, B, H, n, d, runs=20):
         out = torch.empty((B, Hq // 2, d), device="cuda", dtype=torch.bfloat16)
         nbytes_kv = B * n * Hkv * 2 * d * 2 + B * (Hq + Hq // 2) * d * 2  # K and V once; q in, out
 
+        ws = torch.empty(da.v2_decode_workspace_bytes(B, Hq, d), dtype=torch.uint8, device="cuda")
+
         def call():
-            da.diffattn_v2_decode(q, k, v, lg, out=out)
+            da.diffattn_v2_decode(q, k, v, lg, out=out, workspace=ws)
     else:
         q1, q2 = rnd(B, H, d), rnd(B, H, d)
         k1, k2, v = rnd(B, n, H, d), rnd(B, n, H, d), rnd(B, n, H, 2 * d)
@@ -308,8 +312,10 @@ def time_decode(da, flush, B, H, n, d, runs=20):
         out = torch.empty((B, H, 2 * d), device="cuda", dtype=torch.bfloat16)
         nbytes_kv = B * H * n * 4 * d * 2 + B * H * 4 * d * 2  # K1, K2, V read once; q in, out
 
+        ws = torch.empty(da.decode_workspace_bytes(B, H, d), dtype=torch.uint8, device="cuda")
+
         def call():
-            da.diffattn_decode(q1, q2, k1, k2, v, lam, 0.2, gamma=gamma, out=out)
+            da.diffattn_decode(q1, q2, k1, k2, v, lam, 0.2, gamma=gamma, out=out, workspace=ws)
     for _ in range(3):
         call()
     da.device_status()
