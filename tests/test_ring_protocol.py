@@ -19,7 +19,7 @@ Each ring slot, TMEM S buffer and shared-memory P buffer carries a tag of
 what was last written into it; a read that finds another tag (stale or
 overwritten data) is an error, and so is a state in which no agent can move
 (a deadlock).  The models follow the kernels in
-differential_attention_03_gb300/csrc (onepass.cuh, twopass.cuh).  Two
+differential_attention_03_gb300/csrc (onepass.cuh, twopass.cuh, decode.cuh).  Two
 variants that were wrong are kept as negative checks: the model must catch
 them.
 """
@@ -520,4 +520,47 @@ def test_model_catches_shared_full_barriers_with_partial_waiters():
     # One full barrier per slot, but each warp waits only on its own fills: at the
     # switch between the sweeps a warp can take an older phase for its fill.
     bad = [twopass(T, seed, per_owner_full=False) for T in (2, 3, 5) for seed in range(60)]
+    assert any(r != "ok" for r in bad)
+
+
+# --------------------------------------------------------------------------- decode kernel
+def decode(nblk, seed, nst=3, nwarp=4, refill_waits_empty=True):
+    """decode.cuh: thread 0 issues the first NST stages, then refills stage s once all
+    warps have released it (empty, count = warps); every warp waits on every fill in
+    order (full, count 1 + the copy's bytes) and reads the stage's keys."""
+    W = World(seed)
+    full = [Bar(1) for _ in range(nst)]
+    empty = [Bar(nwarp) for _ in range(nst)]
+    W.stage = {}
+
+    def warp(wi):
+        issued = 0
+        if wi == 0:  # thread 0 of warp 0 also produces
+            while issued < min(nst, nblk):
+                W.tma.append((issued % nst, issued, full[issued % nst]))
+                issued += 1
+        for i in range(nblk):
+            s = i % nst
+            yield from W.wait(full[s], (i // nst) & 1)
+            W.expect(W.slot, s, i, f"warp {wi} reads block {i}")
+            yield
+            empty[s].arrive()
+            if wi == 0 and issued < nblk:
+                if refill_waits_empty:
+                    yield from W.wait(empty[s], (i // nst) & 1)
+                W.tma.append((s, issued, full[s]))
+                issued += 1
+
+    return W.run({f"w{w}": warp(w) for w in range(nwarp)})
+
+
+@pytest.mark.parametrize("nblk", [0, 1, 2, 3, 4, 7, 16])
+def test_decode_ring(nblk):
+    for seed in range(30):
+        assert decode(nblk, seed) == "ok", seed
+        assert decode(nblk, seed, nwarp=8) == "ok", seed
+
+
+def test_model_catches_decode_refill_without_empty_wait():
+    bad = [decode(nblk, seed, refill_waits_empty=False) for nblk in (5, 9, 16) for seed in range(40)]
     assert any(r != "ok" for r in bad)
