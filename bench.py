@@ -277,17 +277,23 @@ def time_e2e(w, x, da, steps):
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
-DECODE_WORKLOADS = [  # (name, B, H or (Hq, Hkv), n, d): one new token per sequence over a cache of n tokens
-    ("v1-decode-bf16-B8H16-n32768-d64", 8, 16, 32768, 64),
-    ("v1-decode-bf16-B8H8-n32768-d128", 8, 8, 32768, 128),
-    ("v2-decode-bf16-B8Hq32Hkv16-n32768-d128", 8, (32, 16), 32768, 128),
+DECODE_WORKLOADS = [  # (name, B, H or (Hq, Hkv), n, d, key cache): one new token per sequence over n cached tokens
+    ("v1-decode-bf16-B8H16-n32768-d64", 8, 16, 32768, 64, "bf16"),
+    ("v1-decode-bf16-B8H8-n32768-d128", 8, 8, 32768, 128, "bf16"),
+    ("v2-decode-bf16-B8Hq32Hkv16-n32768-d128", 8, (32, 16), 32768, 128, "bf16"),
     # one sequence, long cache: the pairs are split over clusters through the workspace
-    ("v1-decode-bf16-B1H16-n131072-d64-workspace", 1, 16, 131072, 64),
+    ("v1-decode-bf16-B1H16-n131072-d64-workspace", 1, 16, 131072, 64, "bf16"),
+    # FP8 (e4m3) key caches, bf16 values
+    ("v1-decode-fp8k-B8H16-n32768-d64", 8, 16, 32768, 64, "e4m3"),
+    ("v2-decode-fp8k-B8Hq32Hkv16-n32768-d128", 8, (32, 16), 32768, 128, "e4m3"),
 ]
 
 
-def time_decode(da, flush, B, H, n, d, runs=20):
-    """DIFF V1 decode step over a key/value cache: median CUDA-event time (L2 flushed), HBM GB/s."""
+def time_decode(da, flush, B, H, n, d, keys="bf16", runs=20):
+    """DIFF decode step over a key/value cache: median CUDA-event time (L2 flushed), HBM GB/s.
+
+    keys "e4m3": the key caches hold FP8 codes (1 byte an element) with one scale per tensor.
+    """
     import torch
     g = torch.Generator(device="cuda").manual_seed(1000 + n + d)
 
@@ -298,24 +304,39 @@ def time_decode(da, flush, B, H, n, d, runs=20):
         q, k, v = rnd(B, Hq, d), rnd(B, n, Hkv, d), rnd(B, n, Hkv, d)
         lg = torch.randn((B, Hq // 2), generator=g, device="cuda")
         out = torch.empty((B, Hq // 2, d), device="cuda", dtype=torch.bfloat16)
-        nbytes_kv = B * n * Hkv * 2 * d * 2 + B * (Hq + Hq // 2) * d * 2  # K and V once; q in, out
+        kb = 1 if keys == "e4m3" else 2  # bytes of a key element
+        nbytes_kv = B * n * Hkv * d * (kb + 2) + B * (Hq + Hq // 2) * d * 2  # K and V once; q in, out
 
         ws = torch.empty(da.v2_decode_workspace_bytes(B, Hq, d), dtype=torch.uint8, device="cuda")
+        if keys == "e4m3":
+            k8 = (k.float() * (448.0 / 6.0)).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+            del k
 
-        def call():
-            da.diffattn_v2_decode(q, k, v, lg, out=out, workspace=ws)
+            def call():
+                da.diffattn_v2_decode_fp8k(q, k8, 6.0 / 448.0, v, lg, out=out, workspace=ws)
+        else:
+            def call():
+                da.diffattn_v2_decode(q, k, v, lg, out=out, workspace=ws)
     else:
         q1, q2 = rnd(B, H, d), rnd(B, H, d)
         k1, k2, v = rnd(B, n, H, d), rnd(B, n, H, d), rnd(B, n, H, 2 * d)
         lam = torch.tensor([0.3], device="cuda")
         gamma = torch.ones(2 * d, device="cuda")
         out = torch.empty((B, H, 2 * d), device="cuda", dtype=torch.bfloat16)
-        nbytes_kv = B * H * n * 4 * d * 2 + B * H * 4 * d * 2  # K1, K2, V read once; q in, out
+        kb = 1 if keys == "e4m3" else 2  # bytes of a key element
+        nbytes_kv = B * H * n * d * (2 * kb + 4) + B * H * 4 * d * 2  # K1, K2, V read once; q in, out
 
         ws = torch.empty(da.decode_workspace_bytes(B, H, d), dtype=torch.uint8, device="cuda")
+        if keys == "e4m3":
+            k1, k2 = ((t.float() * (448.0 / 6.0)).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+                      for t in (k1, k2))
 
-        def call():
-            da.diffattn_decode(q1, q2, k1, k2, v, lam, 0.2, gamma=gamma, out=out, workspace=ws)
+            def call():
+                da.diffattn_decode_fp8k(q1, q2, k1, k2, 6.0 / 448.0, 6.0 / 448.0, v, lam, 0.2, gamma=gamma,
+                                        out=out, workspace=ws)
+        else:
+            def call():
+                da.diffattn_decode(q1, q2, k1, k2, v, lam, 0.2, gamma=gamma, out=out, workspace=ws)
     for _ in range(3):
         call()
     da.device_status()
@@ -529,8 +550,8 @@ def run_reference(args):
 
 def decode_results(da, flush, peaks):
     out = {}
-    for name, B, H, n, d in DECODE_WORKLOADS:
-        ms, nb = time_decode(da, flush, B, H, n, d)
+    for name, B, H, n, d, keys in DECODE_WORKLOADS:
+        ms, nb = time_decode(da, flush, B, H, n, d, keys)
         gbs = nb / (ms * 1e-3) / 1e9
         out[name] = {"us": round(ms * 1e3, 1), "hbm_gbs": round(gbs, 1), "bound": "hbm",
                      "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_gbs": peaks["hbm_gbs"],

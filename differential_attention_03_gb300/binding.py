@@ -67,6 +67,12 @@ def lib() -> ctypes.CDLL:
             L.diffattn_v2_decode.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, ll, f, vp, vp, ctypes.c_size_t,
                                              vp]
             L.diffattn_v2_decode.restype = i
+            L.diffattn_decode_fp8k.argtypes = [i, i, i, i, vp, vp, vp, vp, f, f, vp, vp, vp, f, vp, f, vp, vp,
+                                               ctypes.c_size_t, vp]
+            L.diffattn_decode_fp8k.restype = i
+            L.diffattn_v2_decode_fp8k.argtypes = [i, i, i, i, i, vp, vp, f, vp, vp, vp, ll, f, vp, vp,
+                                                  ctypes.c_size_t, vp]
+            L.diffattn_v2_decode_fp8k.restype = i
             L.diffattn_v2_forward.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, ll, ll, f, i, vp, vp]
             L.diffattn_v2_forward.restype = i
             L.diffattn_device_status.argtypes = [vp]
@@ -283,6 +289,74 @@ def diffattn_v2_decode(q, k, v, lam_logits, lens=None, softmax_scale: float = 0.
     _check(lib().diffattn_v2_decode(_dt(k), B, Hq, Hkv, n, d, _ptr(q), _ptr(k), _ptr(v), _ptr(lens),
                                     _ptr(lam_logits), sb, float(softmax_scale), _ptr(out), wp, wn,
                                     _stream(stream)))
+    return out
+
+
+def _need_fp8(t: torch.Tensor, name: str, shape):
+    if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise ValueError(f"{name} must hold e4m3 bytes (torch.float8_e4m3fn or torch.uint8), got {t.dtype}")
+    _need(t, name, None, shape)
+
+
+def diffattn_decode_fp8k(q1, q2, k1, k2, k1_scale: float, k2_scale: float, v, lam, lambda_init_value: float,
+                         gamma=None, eps: float = 1e-5, lens=None, out=None, workspace=None,
+                         stream=None) -> torch.Tensor:
+    """DIFF V1 decode over an FP8 key cache.
+
+    k1, k2: [B, n, H, d] e4m3 codes (torch.float8_e4m3fn or their bytes as
+    torch.uint8) of K_r / k_scale_r; the result is diffattn_decode's for the
+    keys k_scale_r * k_r.  q1, q2, v, lam, gamma, lens, workspace: as for
+    diffattn_decode (bf16, d in {64, 128}).  Returns out [B, H, 2d] (bf16).
+    """
+    B, n, H, d = k1.shape
+    _need(q1, "q1", torch.bfloat16, (B, H, d))
+    _need(q2, "q2", torch.bfloat16, (B, H, d))
+    _need_fp8(k1, "k1", (B, n, H, d))
+    _need_fp8(k2, "k2", (B, n, H, d))
+    _need(v, "v", torch.bfloat16, (B, n, H, 2 * d))
+    _need(lam, "lambda", torch.float32, (1,))
+    if gamma is not None:
+        _need(gamma, "gamma", torch.float32, (2 * d,))
+    if lens is not None:
+        _need(lens, "lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, H, 2 * d), device=v.device, dtype=torch.bfloat16)
+    _need(out, "out", torch.bfloat16, (B, H, 2 * d))
+    wp, wn = _ws_args(workspace, decode_workspace_bytes(B, H, d))
+    _check(lib().diffattn_decode_fp8k(B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), float(k1_scale),
+                                      float(k2_scale), _ptr(v), _ptr(lens), _ptr(lam), float(lambda_init_value),
+                                      _ptr(gamma), float(eps), _ptr(out), wp, wn, _stream(stream)))
+    return out
+
+
+def diffattn_v2_decode_fp8k(q, k, k_scale: float, v, lam_logits, lens=None, softmax_scale: float = 0.0,
+                            out=None, workspace=None, stream=None) -> torch.Tensor:
+    """DIFF V2 decode over an FP8 key cache.
+
+    k: [B, n, Hkv, d] e4m3 codes of K / k_scale (torch.float8_e4m3fn or
+    torch.uint8); everything else as for diffattn_v2_decode (bf16, d = 128).
+    Returns out [B, Hq/2, d] (bf16).
+    """
+    B, n, Hkv, d = k.shape
+    Hq = q.shape[1]
+    _need(q, "q", torch.bfloat16, (B, Hq, d))
+    _need_fp8(k, "k", (B, n, Hkv, d))
+    _need(v, "v", torch.bfloat16, (B, n, Hkv, d))
+    if lam_logits.dim() == 1:
+        _need(lam_logits, "lam_logits", torch.float32, (Hq // 2,))
+        sb = 0
+    else:
+        _need(lam_logits, "lam_logits", torch.float32, (B, Hq // 2))
+        sb = Hq // 2
+    if lens is not None:
+        _need(lens, "lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, Hq // 2, d), device=v.device, dtype=torch.bfloat16)
+    _need(out, "out", torch.bfloat16, (B, Hq // 2, d))
+    wp, wn = _ws_args(workspace, v2_decode_workspace_bytes(B, Hq, d))
+    _check(lib().diffattn_v2_decode_fp8k(B, Hq, Hkv, n, d, _ptr(q), _ptr(k), float(k_scale), _ptr(v), _ptr(lens),
+                                         _ptr(lam_logits), sb, float(softmax_scale), _ptr(out), wp, wn,
+                                         _stream(stream)))
     return out
 
 

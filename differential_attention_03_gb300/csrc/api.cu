@@ -130,6 +130,26 @@ diffattn_status make_map(CUtensorMap* m, const void* base, int B, int n, int hea
   return make_map_box(m, base, B, n, heads, W, 64, rows);
 }
 
+// 4-D map over a BSHD byte tensor (e4m3 key cache) [B, n, heads, W], W of 64
+// or 128: box = one full row of W bytes x `rows` tokens, swizzle W bytes wide.
+diffattn_status make_map_u8(CUtensorMap* m, const void* base, int B, int n, int heads, int W, int rows) {
+  EncodeTiledFn enc;
+  diffattn_status s = get_encoder(&enc);
+  if (s != DIFFATTN_OK) return s;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(W) * heads,
+                                 static_cast<cuuint64_t>(W) * heads * n};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(W), 1, static_cast<cuuint32_t>(rows), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle sw = (W == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DIFFATTN_ERR_CUDA, "cuTensorMapEncodeTiled (u8) failed (CUresult %d)", (int)r);
+  return DIFFATTN_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Tile order: unit-major keeps all query tiles of one head together so that its
@@ -425,34 +445,45 @@ size_t diffattn_v2_decode_workspace(int B, int Hq, int d) {
   return static_cast<size_t>(B) * (Hq / 2) * kMaxSplit * decode_part_floats(d) * sizeof(float);
 }
 
-diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, const void* q1, const void* q2,
-                                const void* k1, const void* k2, const void* v, const int* lens,
-                                const float* lambda, float lambda_init, const float* gamma, float eps, void* out,
-                                void* workspace, size_t workspace_bytes, void* stream) {
-  if (dt != DIFFATTN_F32 && dt != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "diffattn_decode: bad dtype %d", (int)dt);
+// V1 decode with bf16 (k8 false) or e4m3 (k8 true, scales k1_scale, k2_scale) key caches.
+static diffattn_status decode_v1(const char* fn, diffattn_dtype dt, int B, int H, int n, int d, const void* q1,
+                                 const void* q2, const void* k1, const void* k2, bool k8, float k1_scale,
+                                 float k2_scale, const void* v, const int* lens, const float* lambda,
+                                 float lambda_init, const float* gamma, float eps, void* out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (dt != DIFFATTN_F32 && dt != DIFFATTN_BF16) return fail(DIFFATTN_ERR_DTYPE, "%s: bad dtype %d", fn, (int)dt);
   if (B < 0 || H < 0 || n < 0 || d < 1)
-    return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode: bad sizes B=%d H=%d n=%d d=%d", B, H, n, d);
+    return fail(DIFFATTN_ERR_SHAPE, "%s: bad sizes B=%d H=%d n=%d d=%d", fn, B, H, n, d);
   if (B == 0 || H == 0) return ok();
-  if (!q1 || !q2 || !k1 || !k2 || !v || !lambda || !out) return fail(DIFFATTN_ERR_NULL, "diffattn_decode: NULL pointer");
+  if (!q1 || !q2 || !k1 || !k2 || !v || !lambda || !out) return fail(DIFFATTN_ERR_NULL, "%s: NULL pointer", fn);
   if (dt != DIFFATTN_BF16 || (d != 64 && d != 128))
-    return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_decode: bf16 with d in {64, 128} only (got dtype %d, d=%d)", (int)dt,
+    return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: bf16 with d in {64, 128} only (got dtype %d, d=%d)", fn, (int)dt,
                 d);
-  if (!std::isfinite(lambda_init)) return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode: lambda_init not finite");
+  if (!std::isfinite(lambda_init)) return fail(DIFFATTN_ERR_SHAPE, "%s: lambda_init not finite", fn);
+  if (k8 && !(std::isfinite(k1_scale) && std::isfinite(k2_scale) && k1_scale > 0.f && k2_scale > 0.f))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: key scales must be finite and positive", fn);
   if (!aligned16(q1) || !aligned16(q2) || !aligned16(k1) || !aligned16(k2) || !aligned16(v) || !aligned16(out))
-    return fail(DIFFATTN_ERR_ALIGN, "diffattn_decode: bf16 tensors must be 16-byte aligned");
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
   const long long units = static_cast<long long>(B) * H;
   if (units * da::DecodeCfg<64>::MAX_CS * kMaxSplit > 0x7fffffffll)
-    return fail(DIFFATTN_ERR_SHAPE, "diffattn_decode: too many (batch, head) pairs");
+    return fail(DIFFATTN_ERR_SHAPE, "%s: too many (batch, head) pairs", fn);
   if (eps <= 0.f) eps = 1e-5f;
   int* status = nullptr;
   diffattn_status st = status_word(&status);
   if (st != DIFFATTN_OK) return st;
   da::DecodeParams p;
   memset(&p, 0, sizeof(p));
-  const int bk = (d == 64) ? da::DecodeCfg<64>::BK : da::DecodeCfg<128>::BK;
+  const int bk = (d == 64) ? da::DecodeCfg<64>::BK : da::DecodeCfg<128>::BK;  // (the same with K8)
   const int nn = n > 0 ? n : 1;  // an empty cache still needs a valid map (no key is read)
-  if ((st = make_map(&p.tm_k1, k1, B, nn, H, d, bk)) != DIFFATTN_OK) return st;
-  if ((st = make_map(&p.tm_k2, k2, B, nn, H, d, bk)) != DIFFATTN_OK) return st;
+  if (k8) {
+    if ((st = make_map_u8(&p.tm_k1, k1, B, nn, H, d, bk)) != DIFFATTN_OK) return st;
+    if ((st = make_map_u8(&p.tm_k2, k2, B, nn, H, d, bk)) != DIFFATTN_OK) return st;
+  } else {
+    if ((st = make_map(&p.tm_k1, k1, B, nn, H, d, bk)) != DIFFATTN_OK) return st;
+    if ((st = make_map(&p.tm_k2, k2, B, nn, H, d, bk)) != DIFFATTN_OK) return st;
+  }
+  p.k1_scale = k1_scale;
+  p.k2_scale = k2_scale;
   if ((st = make_map(&p.tm_v, v, B, nn, H, 2 * d, bk)) != DIFFATTN_OK) return st;
   p.q1 = static_cast<const __nv_bfloat16*>(q1);
   p.q2 = static_cast<const __nv_bfloat16*>(q2);
@@ -473,35 +504,54 @@ diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, c
     p.nsplit = decode_split(units, cs, n, bk);
     p.ws = static_cast<float*>(workspace);
   }
-  cudaError_t e = da::launch_decode_v1(p, d, static_cast<int>(units), cs, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "diffattn_decode launch");
+  cudaError_t e = da::launch_decode_v1(p, d, k8, static_cast<int>(units), cs, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
   g_launches.fetch_add(1);
   return ok();
 }
 
-diffattn_status diffattn_v2_decode(diffattn_dtype dt, int B, int Hq, int Hkv, int n, int d, const void* q,
-                                   const void* k, const void* v, const int* lens, const float* lam_logits,
-                                   long long sb, float softmax_scale, void* out, void* workspace,
-                                   size_t workspace_bytes, void* stream) {
+diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, const void* q1, const void* q2,
+                                const void* k1, const void* k2, const void* v, const int* lens,
+                                const float* lambda, float lambda_init, const float* gamma, float eps, void* out,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_v1("diffattn_decode", dt, B, H, n, d, q1, q2, k1, k2, false, 1.f, 1.f, v, lens, lambda, lambda_init,
+                   gamma, eps, out, workspace, workspace_bytes, stream);
+}
+
+diffattn_status diffattn_decode_fp8k(int B, int H, int n, int d, const void* q1, const void* q2, const void* k1,
+                                     const void* k2, float k1_scale, float k2_scale, const void* v,
+                                     const int* lens, const float* lambda, float lambda_init, const float* gamma,
+                                     float eps, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_v1("diffattn_decode_fp8k", DIFFATTN_BF16, B, H, n, d, q1, q2, k1, k2, true, k1_scale, k2_scale, v,
+                   lens, lambda, lambda_init, gamma, eps, out, workspace, workspace_bytes, stream);
+}
+
+// V2 decode with a bf16 (k8 false) or e4m3 (k8 true, scale k_scale) key cache.
+static diffattn_status decode_v2(const char* fn, diffattn_dtype dt, int B, int Hq, int Hkv, int n, int d,
+                                 const void* q, const void* k, bool k8, float k_scale, const void* v,
+                                 const int* lens, const float* lam_logits, long long sb, float softmax_scale,
+                                 void* out, void* workspace, size_t workspace_bytes, void* stream) {
   if (dt != DIFFATTN_F32 && dt != DIFFATTN_BF16)
-    return fail(DIFFATTN_ERR_DTYPE, "diffattn_v2_decode: bad dtype %d", (int)dt);
+    return fail(DIFFATTN_ERR_DTYPE, "%s: bad dtype %d", fn, (int)dt);
   if (B < 0 || Hq < 0 || Hkv < 1 || n < 0 || d < 1)
-    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_decode: bad sizes B=%d Hq=%d Hkv=%d n=%d d=%d", B, Hq, Hkv, n, d);
+    return fail(DIFFATTN_ERR_SHAPE, "%s: bad sizes B=%d Hq=%d Hkv=%d n=%d d=%d", fn, B, Hq, Hkv, n, d);
   if (Hq % 2 != 0 || Hq % Hkv != 0 || (Hq / Hkv) % 2 != 0)
-    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_decode: need Hq even, Hq %% Hkv == 0 and Hq/Hkv even (Hq=%d Hkv=%d)",
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need Hq even, Hq %% Hkv == 0 and Hq/Hkv even (Hq=%d Hkv=%d)", fn,
                 Hq, Hkv);
-  if (sb < 0) return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_decode: negative logit stride");
+  if (sb < 0) return fail(DIFFATTN_ERR_SHAPE, "%s: negative logit stride", fn);
   if (B == 0 || Hq == 0) return ok();
-  if (!q || !k || !v || !lam_logits || !out) return fail(DIFFATTN_ERR_NULL, "diffattn_v2_decode: NULL pointer");
+  if (k8 && !(std::isfinite(k_scale) && k_scale > 0.f))
+    return fail(DIFFATTN_ERR_SHAPE, "%s: key scale must be finite and positive", fn);
+  if (!q || !k || !v || !lam_logits || !out) return fail(DIFFATTN_ERR_NULL, "%s: NULL pointer", fn);
   if (dt != DIFFATTN_BF16 || d != 128)
-    return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_v2_decode: bf16 with d = 128 only (got dtype %d, d=%d)", (int)dt,
+    return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: bf16 with d = 128 only (got dtype %d, d=%d)", fn, (int)dt,
                 d);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
-    return fail(DIFFATTN_ERR_ALIGN, "diffattn_v2_decode: bf16 tensors must be 16-byte aligned");
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
   const int G = Hq / 2;
   const long long units = static_cast<long long>(B) * G;
   if (units * da::DecodeCfg<128, true>::MAX_CS * kMaxSplit > 0x7fffffffll)
-    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_decode: too many (batch, pair) units");
+    return fail(DIFFATTN_ERR_SHAPE, "%s: too many (batch, pair) units", fn);
   int* status = nullptr;
   diffattn_status st = status_word(&status);
   if (st != DIFFATTN_OK) return st;
@@ -509,7 +559,10 @@ diffattn_status diffattn_v2_decode(diffattn_dtype dt, int B, int Hq, int Hkv, in
   memset(&p, 0, sizeof(p));
   constexpr int bk = da::DecodeCfg<128, true>::BK;
   const int nn = n > 0 ? n : 1;  // an empty cache still needs a valid map (no key is read)
-  if ((st = make_map(&p.tm_k1, k, B, nn, Hkv, d, bk)) != DIFFATTN_OK) return st;
+  if ((st = k8 ? make_map_u8(&p.tm_k1, k, B, nn, Hkv, d, bk) : make_map(&p.tm_k1, k, B, nn, Hkv, d, bk)) !=
+      DIFFATTN_OK)
+    return st;
+  p.k1_scale = p.k2_scale = k_scale;
   if ((st = make_map(&p.tm_v, v, B, nn, Hkv, d, bk)) != DIFFATTN_OK) return st;
   p.tm_k2 = p.tm_k1;
   p.q1 = static_cast<const __nv_bfloat16*>(q);
@@ -532,10 +585,26 @@ diffattn_status diffattn_v2_decode(diffattn_dtype dt, int B, int Hq, int Hkv, in
     p.nsplit = decode_split(units, cs, n, bk);
     p.ws = static_cast<float*>(workspace);
   }
-  cudaError_t e = da::launch_decode_v2_d128(p, static_cast<int>(units), cs, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_decode launch");
+  cudaError_t e = da::launch_decode_v2_d128(p, k8, static_cast<int>(units), cs, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
   g_launches.fetch_add(1);
   return ok();
+}
+
+diffattn_status diffattn_v2_decode(diffattn_dtype dt, int B, int Hq, int Hkv, int n, int d, const void* q,
+                                   const void* k, const void* v, const int* lens, const float* lam_logits,
+                                   long long sb, float softmax_scale, void* out, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  return decode_v2("diffattn_v2_decode", dt, B, Hq, Hkv, n, d, q, k, false, 1.f, v, lens, lam_logits, sb,
+                   softmax_scale, out, workspace, workspace_bytes, stream);
+}
+
+diffattn_status diffattn_v2_decode_fp8k(int B, int Hq, int Hkv, int n, int d, const void* q, const void* k,
+                                        float k_scale, const void* v, const int* lens, const float* lam_logits,
+                                        long long sb, float softmax_scale, void* out, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  return decode_v2("diffattn_v2_decode_fp8k", DIFFATTN_BF16, B, Hq, Hkv, n, d, q, k, true, k_scale, v, lens,
+                   lam_logits, sb, softmax_scale, out, workspace, workspace_bytes, stream);
 }
 
 diffattn_status diffattn_v2_forward(diffattn_dtype dt, int B, int Hq, int Hkv, int n, int d, const void* q,

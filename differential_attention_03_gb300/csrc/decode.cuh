@@ -12,6 +12,11 @@
 // "GQA와의 호환성"): per (b, head pair g), query heads 2g and 2g + 1 over their
 // shared KV head, out = O_1 - sigmoid(logit[b, g]) O_2, no norm; the key tile
 // is then read once for both queries and V is d wide.
+// Template flag K8: the key caches in FP8 (e4m3, one dequantisation scale per
+// tensor, folded into the query), the values in bf16; 6 d bytes a key (V1)
+// instead of 8 d.  The low-bit attention the glossary page's remark on
+// smaller activation outliers points to, applied where the step is bound by
+// the bytes it reads.
 //
 // The step is bound by HBM: every visible key's k_1, k_2 and v are read
 // exactly once (V once for both maps), 8 d bytes per key, against ~12 d
@@ -37,6 +42,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "params.h"
 #include "ptx.cuh"
@@ -44,7 +50,7 @@
 namespace da {
 
 struct DecodeParams {
-  CUtensorMap tm_k1;  // V1: [B, n, H, d] key caches; V2: [B, n, Hkv, d]; boxes of 64 columns x BK keys
+  CUtensorMap tm_k1;  // V1: [B, n, H, d] key caches; V2: [B, n, Hkv, d]; boxes of 64 columns (K8: d bytes) x BK keys
   CUtensorMap tm_k2;  // (V1 only)
   CUtensorMap tm_v;   // V1: [B, n, H, 2d]; V2: [B, n, Hkv, d]
   const __nv_bfloat16* q1;  // V1: [B, H, d]; V2: q [B, Hq, d]
@@ -56,6 +62,7 @@ struct DecodeParams {
   long long sb;
   __nv_bfloat16* out;       // V1: [B, H, 2d]; V2: [B, Hq / 2, d]
   float scale_log2;         // softmax scale * log2(e)
+  float k1_scale, k2_scale; // K8: dequantisation scales of the e4m3 key caches (V2: k1_scale)
   float norm_mult;          // V1: 1 - lambda_init
   float eps;
   int B, H, n;  // H: V1 heads; V2 head pairs per sequence (Hq / 2)
@@ -65,7 +72,7 @@ struct DecodeParams {
   int* status;
 };
 
-template <int D, bool V2 = false>
+template <int D, bool V2 = false, bool K8 = false>
 struct DecodeCfg {
   static constexpr int MAX_CS = 8;  // CTAs per (b, h) cluster: chosen at launch, at most this (16-CTA
                                     // clusters measured slower: 5.5 vs 6.2 TB/s at B8 H8 n32768 d128)
@@ -77,10 +84,12 @@ struct DecodeCfg {
   static constexpr int KW = BK / NWARP;         // keys per warp per stage
   static constexpr int PARTS = 32 / KW;         // lanes per key
   static constexpr int PE = D / PARTS;          // q . k products per lane (32)
-  static constexpr int QB = D / 64, VB = DV / 64;
-  static constexpr int K_BYTES = QB * BK * 128, V_BYTES = VB * BK * 128;
-  static constexpr int STAGE = NKT * K_BYTES + V_BYTES;
-  static constexpr int NST = 3;  // 96 KB of stages in flight
+  static constexpr int KROW = K8 ? D : 128;  // bytes of a key row in one TMA box (bf16: 64 columns)
+  static constexpr int QB = K8 ? 1 : D / 64;  // key boxes per row
+  static constexpr int VB = DV / 64;
+  static constexpr int K_BYTES = QB * BK * KROW, V_BYTES = VB * BK * 128;
+  static constexpr int STAGE = NKT * K_BYTES + V_BYTES;  // 32 KB (K8: 24 KB)
+  static constexpr int NST = 98304 / STAGE;              // 96 KB of stages in flight
   static constexpr int CH = DV / 32;  // output channels per lane and map
   static constexpr int PART_FLOATS = 2 * (DV + 2);  // per map: max, sum, DV channels
   static constexpr int OFF_BARS = NST * STAGE;
@@ -92,6 +101,7 @@ struct DecodeCfg {
   static_assert(D == 64 || D == 128, "query/key width");
   static_assert(PE == 32 && PARTS * KW == 32, "lane split");
   static_assert(NST * STAGE == 98304, "stage ring");
+  static_assert(STAGE % 1024 == 0 && K_BYTES % 1024 == 0, "swizzled boxes start on 1 KB");
   static_assert(!V2 || D == 128, "V2 decode: d = 128");
 };
 
@@ -119,6 +129,22 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t a, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
   return v;
+}
+
+// Four e4m3 values (bytes 0..3 of w, byte 0 first) to floats; exact (every
+// e4m3 value is an f16 value).
+__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float (&f)[4]) {
+  uint32_t h01, h23;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+      : "=r"(h01), "=r"(h23)
+      : "r"(w));
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+  const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+  f[0] = a.x;
+  f[1] = a.y;
+  f[2] = c.x;
+  f[3] = c.y;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -168,7 +194,7 @@ __device__ __forceinline__ void decode_finish(const DecodeParams& p, int b, int 
 // written by decode_kernel into p.ws, and finishes the row.
 template <int D, bool V2>
 __global__ void __launch_bounds__(DecodeCfg<D, V2>::NTHREADS) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
-  using C = DecodeCfg<D, V2>;
+  using C = DecodeCfg<D, V2>;  // (the key type does not change the state layout)
   constexpr int DV = C::DV;
   constexpr int CPT = DV > C::NTHREADS ? DV / C::NTHREADS : 1;
   __shared__ float red[C::NWARP];
@@ -200,9 +226,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2>::NTHREADS) decode_combine_ker
   decode_finish<D, V2, C::NTHREADS, CPT>(p, b, h, l1, l2, y1, y2, red);
 }
 
-template <int D, bool V2>
-__global__ void __launch_bounds__(DecodeCfg<D, V2>::NTHREADS, 2) decode_kernel(const __grid_constant__ DecodeParams p) {
-  using C = DecodeCfg<D, V2>;
+template <int D, bool V2, bool K8>
+__global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
+    decode_kernel(const __grid_constant__ DecodeParams p) {
+  using C = DecodeCfg<D, V2, K8>;
   constexpr int BK = C::BK, KW = C::KW, PARTS = C::PARTS, DV = C::DV, CH = C::CH, NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -248,9 +275,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2>::NTHREADS, 2) decode_kernel(c
     uint8_t* st = smem + (i % NST) * C::STAGE;
     const int key0 = k_begin + i * BK;
     mbar_arrive_expect_tx(&full[i % NST], C::STAGE);
-    for (int bx = 0; bx < C::QB; ++bx) {
-      tma_load_4d(st + bx * BK * 128, &p.tm_k1, &full[i % NST], bx * 64, hk, key0, b);
-      if (!V2) tma_load_4d(st + C::K_BYTES + bx * BK * 128, &p.tm_k2, &full[i % NST], bx * 64, hk, key0, b);
+    for (int bx = 0; bx < C::QB; ++bx) {  // (K8: one box of D bytes a row)
+      tma_load_4d(st + bx * BK * C::KROW, &p.tm_k1, &full[i % NST], bx * 64, hk, key0, b);
+      if (!V2) tma_load_4d(st + C::K_BYTES + bx * BK * C::KROW, &p.tm_k2, &full[i % NST], bx * 64, hk, key0, b);
     }
     for (int bx = 0; bx < C::VB; ++bx)
       tma_load_4d(st + C::NKT * C::K_BYTES + bx * BK * 128, &p.tm_v, &full[i % NST], bx * 64, hk, key0, b);
@@ -263,8 +290,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2>::NTHREADS, 2) decode_kernel(c
     for (; issued < NST && issued < nblk; ++issued) issue(issued);
   }
 
-  // This lane's 32 query products (pre-scaled into the log2 domain).
+  // This lane's 32 query products (pre-scaled into the log2 domain, and by
+  // the key scale of an e4m3 key cache).
   const int kk = lane / PARTS, prt = lane % PARTS;
+  const float qs1 = K8 ? p.scale_log2 * p.k1_scale : p.scale_log2;
+  const float qs2 = K8 ? p.scale_log2 * (V2 ? p.k1_scale : p.k2_scale) : p.scale_log2;
   float q1r[32], q2r[32];
   {
     const __nv_bfloat16* q1p = p.q1 + q1_off + prt * 32;
@@ -276,10 +306,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2>::NTHREADS, 2) decode_kernel(c
       const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wc[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        q1r[i + 2 * e] = bf16_lo(wa[e]) * p.scale_log2;
-        q1r[i + 2 * e + 1] = bf16_hi(wa[e]) * p.scale_log2;
-        q2r[i + 2 * e] = bf16_lo(wc[e]) * p.scale_log2;
-        q2r[i + 2 * e + 1] = bf16_hi(wc[e]) * p.scale_log2;
+        q1r[i + 2 * e] = bf16_lo(wa[e]) * qs1;
+        q1r[i + 2 * e + 1] = bf16_hi(wa[e]) * qs1;
+        q2r[i + 2 * e] = bf16_lo(wc[e]) * qs2;
+        q2r[i + 2 * e + 1] = bf16_hi(wc[e]) * qs2;
       }
     }
   }
@@ -300,18 +330,44 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2>::NTHREADS, 2) decode_kernel(c
     const int row = warp * KW + kk;  // this lane's key within the stage
     // ---- scores: 32 products per lane, PARTS lanes per key
     float s1 = 0.f, s2 = 0.f;
+    if constexpr (K8) {
+      // 32 e4m3 key values: 16-byte chunks 2 prt and 2 prt + 1 of the row
+      // (128-byte rows: 128-byte swizzle, chunk ^ (row % 8); 64-byte rows:
+      // 64-byte swizzle, chunk ^ ((row / 2) % 4)).
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int off = kbox * BK * 128 + row * 128 + (((kchunk0 + c) ^ (row & 7)) << 4);
-      const uint4 a = *reinterpret_cast<const uint4*>(st + off);
-      const uint4 e = V2 ? a : *reinterpret_cast<const uint4*>(st + C::K_BYTES + off);  // V2: one key tile
-      const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, we[4] = {e.x, e.y, e.z, e.w};
+      for (int c = 0; c < 2; ++c) {
+        const int ch = 2 * prt + c;
+        const int pch = (C::KROW == 128) ? (ch ^ (row & 7)) : (ch ^ ((row >> 1) & 3));
+        const int off = row * C::KROW + (pch << 4);
+        const uint4 a = *reinterpret_cast<const uint4*>(st + off);
+        const uint4 e = V2 ? a : *reinterpret_cast<const uint4*>(st + C::K_BYTES + off);  // V2: one key tile
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, we[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        s1 = fmaf(q1r[8 * c + 2 * t], bf16_lo(wa[t]), s1);
-        s1 = fmaf(q1r[8 * c + 2 * t + 1], bf16_hi(wa[t]), s1);
-        s2 = fmaf(q2r[8 * c + 2 * t], bf16_lo(we[t]), s2);
-        s2 = fmaf(q2r[8 * c + 2 * t + 1], bf16_hi(we[t]), s2);
+        for (int t = 0; t < 4; ++t) {
+          float fa[4], fe[4];
+          e4m3x4_to_f32(wa[t], fa);
+          e4m3x4_to_f32(we[t], fe);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            s1 = fmaf(q1r[16 * c + 4 * t + u], fa[u], s1);
+            s2 = fmaf(q2r[16 * c + 4 * t + u], fe[u], s2);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int off = kbox * BK * 128 + row * 128 + (((kchunk0 + c) ^ (row & 7)) << 4);
+        const uint4 a = *reinterpret_cast<const uint4*>(st + off);
+        const uint4 e = V2 ? a : *reinterpret_cast<const uint4*>(st + C::K_BYTES + off);  // V2: one key tile
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, we[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          s1 = fmaf(q1r[8 * c + 2 * t], bf16_lo(wa[t]), s1);
+          s1 = fmaf(q1r[8 * c + 2 * t + 1], bf16_hi(wa[t]), s1);
+          s2 = fmaf(q2r[8 * c + 2 * t], bf16_lo(we[t]), s2);
+          s2 = fmaf(q2r[8 * c + 2 * t + 1], bf16_hi(we[t]), s2);
+        }
       }
     }
 #pragma unroll

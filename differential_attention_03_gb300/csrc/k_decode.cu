@@ -5,10 +5,10 @@
 
 namespace da {
 
-template <int D, bool V2>
+template <int D, bool V2, bool K8>
 static cudaError_t launch_decode(const DecodeParams& p, int units, int cs, cudaStream_t s) {
-  using C = DecodeCfg<D, V2>;
-  auto kern = decode_kernel<D, V2>;
+  using C = DecodeCfg<D, V2, K8>;
+  auto kern = decode_kernel<D, V2, K8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -31,12 +31,13 @@ static cudaError_t launch_decode(const DecodeParams& p, int units, int cs, cudaS
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_v1(const DecodeParams& p, int d, int units, int cs, cudaStream_t s) {
-  return d == 64 ? launch_decode<64, false>(p, units, cs, s) : launch_decode<128, false>(p, units, cs, s);
+cudaError_t launch_decode_v1(const DecodeParams& p, int d, bool k8, int units, int cs, cudaStream_t s) {
+  if (k8) return d == 64 ? launch_decode<64, false, true>(p, units, cs, s) : launch_decode<128, false, true>(p, units, cs, s);
+  return d == 64 ? launch_decode<64, false, false>(p, units, cs, s) : launch_decode<128, false, false>(p, units, cs, s);
 }
 
-cudaError_t launch_decode_v2_d128(const DecodeParams& p, int units, int cs, cudaStream_t s) {
-  return launch_decode<128, true>(p, units, cs, s);
+cudaError_t launch_decode_v2_d128(const DecodeParams& p, bool k8, int units, int cs, cudaStream_t s) {
+  return k8 ? launch_decode<128, true, true>(p, units, cs, s) : launch_decode<128, true, false>(p, units, cs, s);
 }
 
 }  // namespace da

@@ -22,10 +22,10 @@ cudaError_t launch_onepass_v2_d128(const TwoPassParams& p, int grid, cudaStream_
 cudaError_t launch_simt_f32(const SimtParams& p, cudaStream_t s);
 // V1 decode (one query per sequence over a key/value cache), d in {64, 128}:
 // p.nsplit clusters of `cs` CTAs (1..8) over the keys of each of the `units` (batch, head)
-// pairs (with p.nsplit > 1 the states go through p.ws to a combine kernel).
-cudaError_t launch_decode_v1(const DecodeParams& p, int d, int units, int cs, cudaStream_t s);
+// pairs (with p.nsplit > 1 the states go through p.ws to a combine kernel).  k8: e4m3 key caches.
+cudaError_t launch_decode_v1(const DecodeParams& p, int d, bool k8, int units, int cs, cudaStream_t s);
 // V2 decode, d = 128: head pairs over their shared KV head (one key tile for both queries).
-cudaError_t launch_decode_v2_d128(const DecodeParams& p, int units, int cs, cudaStream_t s);
+cudaError_t launch_decode_v2_d128(const DecodeParams& p, bool k8, int units, int cs, cudaStream_t s);
 cudaError_t launch_lambda_reparam(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
                                   int dim, float lambda_init, float* out, cudaStream_t s);
 cudaError_t launch_wait_selftest(unsigned long long budget_cycles, int* status, cudaStream_t s);

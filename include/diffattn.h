@@ -174,6 +174,25 @@ diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, c
                                 size_t workspace_bytes, void* stream);
 
 /*
+ * diffattn_decode with the key caches in FP8 (the low-bit attention that the
+ * "Differential Transformer" glossary page motivates by DIFF's smaller
+ * activation outliers): k1, k2 are [B, n, H, d] device arrays of e4m3 bytes
+ * (OCP FP8 E4M3, "fn": no infinities, 0x7f / 0xff are NaN) holding
+ * K_r / k_scale_r, one scale per tensor; the kernel computes exactly what
+ * diffattn_decode computes for the bf16 caches K_r = k_scale_r * e4m3(k_r)
+ * (fp32 arithmetic; each e4m3 value is converted exactly).  q1, q2, v, out,
+ * lens, lambda, gamma, workspace: as for diffattn_decode (bf16, d in {64, 128};
+ * workspace size diffattn_decode_workspace).  k1_scale, k2_scale: finite and
+ * positive, else ERR_SHAPE.  6 d bytes read a key instead of 8 d.
+ */
+diffattn_status diffattn_decode_fp8k(int B, int H, int n, int d, const void* q1, const void* q2,
+                                     const void* k1, const void* k2, float k1_scale,
+                                     float k2_scale, const void* v, const int* lens,
+                                     const float* lambda, float lambda_init, const float* gamma,
+                                     float eps, void* out, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/*
  * DIFF V2 decode step: one new token per sequence over a key/value cache
  * (DIFF V2 analysis page, sections "2. 커스텀 커널 제거", "5. 간소화된 λ
  * 매개변수화" and "GQA와의 호환성"): per head pair g of sequence b,
@@ -204,6 +223,19 @@ diffattn_status diffattn_v2_decode(diffattn_dtype dt, int B, int Hq, int Hkv, in
                                    const float* lam_logits, long long sb, float softmax_scale,
                                    void* out, void* workspace, size_t workspace_bytes,
                                    void* stream);
+
+/*
+ * diffattn_v2_decode with the key cache in FP8: k is a [B, n, Hkv, d] device
+ * array of e4m3 bytes holding K / k_scale (k_scale finite and positive, else
+ * ERR_SHAPE); the result is diffattn_v2_decode's for K = k_scale * e4m3(k).
+ * Everything else as for diffattn_v2_decode (bf16, d = 128; workspace size
+ * diffattn_v2_decode_workspace).  3 d bytes read a key instead of 4 d.
+ */
+diffattn_status diffattn_v2_decode_fp8k(int B, int Hq, int Hkv, int n, int d, const void* q,
+                                        const void* k, float k_scale, const void* v,
+                                        const int* lens, const float* lam_logits, long long sb,
+                                        float softmax_scale, void* out, void* workspace,
+                                        size_t workspace_bytes, void* stream);
 
 /*
  * DIFF V2 forward (DIFF V2 analysis page, sections "2. 커스텀 커널 제거",

@@ -14,6 +14,8 @@ from .diffattn_oracle import (  # noqa: F401
     diff_attn_v2,
     diff_attn_v2_decode,
     difference_map,
+    dequant_e4m3,
+    e4m3_decode,
     head_rmsnorm,
     lambda_init,
     lambda_reparam,

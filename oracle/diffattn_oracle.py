@@ -23,6 +23,9 @@ Sources (web pages on the Differential Transformer; cited by title and section):
   [NEWS]      esgcw.com.cn news article, section "差分注意力" (projections,
               lambda re-parameterisation, lambda_init schedule, multi-head,
               per-head RMSNorm with the fixed (1 - lambda_init) multiplier).
+  [FP8]       The OCP 8-bit floating point specification (E4M3): the byte
+              format of an FP8 key cache; the [GLOSSARY] page only motivates
+              low-bit attention by DIFF's smaller activation outliers.
 
 Readings where the pages are silent or garbled:
   * scale 1/sqrt(d) with d the per-map query/key width ([GLOSSARY] code; the
@@ -304,3 +307,38 @@ def diff_attn_v2_decode(q, k, v, lam_logits, lens=None, scale=None) -> np.ndarra
             ao = attention_map(q[b, None, ho], k[b, :L, kv], scale, False)
             out[b, g] = ((ae - sigmoid(lam_logits[b, g]) * ao) @ v[b, :L, kv])[0]
     return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Values of FP8 E4M3 codes ([FP8], the "fn" variant), fp64, same shape.
+
+    Bit 7 is the sign, bits 6..3 the exponent with bias 7, bits 2..0 the
+    mantissa.  Exponent 0 is subnormal: (m / 8) * 2^-6.  Otherwise
+    (1 + m / 8) * 2^(e - 7), the all-ones exponent included, except that
+    exponent 15 with mantissa 7 is NaN (the format has no infinities), so the
+    largest finite value is 1.75 * 2^8 = 448.  ``codes``: bytes as a uint8
+    array, or a torch uint8 / float8_e4m3fn tensor (its bytes are read).
+    """
+    x = codes
+    if hasattr(x, "detach"):  # a torch tensor: read its bytes
+        import torch
+
+        x = x.detach().to("cpu")
+        if x.dtype != torch.uint8:
+            x = x.view(torch.uint8)
+        x = x.numpy()
+    c = np.asarray(x)
+    if c.dtype != np.uint8:
+        raise ValueError("e4m3 codes must be bytes (uint8)")
+    c = c.astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64)))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def dequant_e4m3(codes, scale: float) -> np.ndarray:
+    """A key cache stored as e4m3 codes with one scale per tensor: scale * value ([FP8])."""
+    return float(scale) * e4m3_decode(codes)

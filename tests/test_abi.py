@@ -34,7 +34,8 @@ def test_header_declares_the_entry_points():
     for want in ("diffattn_forward", "diffattn_v2_forward", "lambda_reparam", "diffattn_lambda_init",
                  "diffattn_device_status", "diffattn_last_error", "diffattn_forward_host",
                  "diffattn_forward_host_workspace", "diffattn_decode", "diffattn_v2_decode",
-                 "diffattn_decode_workspace", "diffattn_v2_decode_workspace"):
+                 "diffattn_decode_workspace", "diffattn_v2_decode_workspace", "diffattn_decode_fp8k",
+                 "diffattn_v2_decode_fp8k"):
         assert want in names
 
 
@@ -143,6 +144,30 @@ def test_v2_decode_host_validation(L):
     assert call(d=64) == da.ERR_UNSUPPORTED
     assert call(dt=0) == da.ERR_UNSUPPORTED
     assert call(q=MIS) == da.ERR_ALIGN
+
+
+def test_fp8k_decode_host_validation(L):
+    def v1(B=1, n=8, d=64, k1=A, s1=1.0, s2=1.0, out=A):
+        return L.diffattn_decode_fp8k(B, 2, n, d, A, A, k1, A, ctypes.c_float(s1), ctypes.c_float(s2), A, None, A,
+                                      ctypes.c_float(0.2), None, ctypes.c_float(1e-5), out, None, 0, None)
+    assert v1(n=-1) == da.ERR_SHAPE
+    assert v1(B=0) == da.OK
+    assert v1(k1=None) == da.ERR_NULL
+    assert v1(d=96) == da.ERR_UNSUPPORTED
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        assert v1(s1=bad) == da.ERR_SHAPE
+        assert v1(s2=bad) == da.ERR_SHAPE
+    assert b"scale" in L.diffattn_last_error()
+    assert v1(k1=MIS) == da.ERR_ALIGN
+
+    def v2(Hq=4, Hkv=2, d=128, k=A, s=1.0):
+        return L.diffattn_v2_decode_fp8k(1, Hq, Hkv, 8, d, A, k, ctypes.c_float(s), A, None, A, 0,
+                                         ctypes.c_float(0.0), A, None, 0, None)
+    assert v2(Hq=6, Hkv=2) == da.ERR_SHAPE
+    assert v2(k=None) == da.ERR_NULL
+    assert v2(d=64) == da.ERR_UNSUPPORTED
+    assert v2(s=0.0) == da.ERR_SHAPE
+    assert v2(k=MIS) == da.ERR_ALIGN
 
 
 def test_v2_host_validation(L):

@@ -438,3 +438,108 @@ def test_launch_count_counts_kernels():
     c0 = da.launch_count()
     _v1_gpu(x, w)
     assert da.launch_count() - c0 == 2  # lambda_reparam + forward
+
+
+# --------------------------------------------------------------------------- decode over FP8 (e4m3) key caches
+def _quant_e4m3(k):
+    """Input preparation: one fp32 scale per tensor (amax / 448) and the e4m3 codes of k / scale."""
+    scale = float(k.float().abs().max()) / 448.0
+    return (k.float() / scale).to(torch.float8_e4m3fn), scale
+
+
+DECODE_FP8 = [  # B, H, n, d, lens, workspace
+    (2, 2, 300, 64, None, False),
+    (3, 2, 1000, 128, [1000, 37, 0], False),  # ragged lengths, an empty cache
+    (1, 3, 1, 64, None, False),               # a single key
+    (4, 1, 777, 64, [1, 64, 65, 777], False),  # stage and cluster-chunk boundaries
+    (2, 4, 5000, 128, [5000, 4097], False),
+    (1, 2, 40000, 64, None, True),            # few pairs: split over clusters, combine kernel
+    (2, 3, 9000, 128, [9000, 2500], True),
+]
+
+
+@pytest.mark.parametrize("B,H,n,d,lens,use_ws", DECODE_FP8)
+def test_v1_decode_fp8_keys(B, H, n, d, lens, use_ws):
+    # The CUDA path reads e4m3 key codes; the oracle gets the keys they stand
+    # for (decoded from the format's definition, times the scale) in fp64.
+    g = torch.Generator(device="cuda").manual_seed(1300 + n + d)
+
+    def rnd(*shape):
+        return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    q1, q2 = rnd(B, H, d), rnd(B, H, d)
+    k1, s1 = _quant_e4m3(rnd(B, n, H, d))
+    k2, s2 = _quant_e4m3(rnd(B, n, H, d) * 2)
+    v = rnd(B, n, H, 2 * d)
+    gamma = 0.9 + 0.2 * torch.rand(2 * d, generator=g, device="cuda")
+    lin = da.lambda_init(5)
+    lam = torch.tensor([0.45], device="cuda")
+    lens_t = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
+    ws = torch.empty(da.decode_workspace_bytes(B, H, d), dtype=torch.uint8, device="cuda") if use_ws else None
+    out = da.diffattn_decode_fp8k(q1, q2, k1, k2, s1, s2, v, lam, lin, gamma=gamma, lens=lens_t, workspace=ws)
+    da.device_status()
+    ref = oracle.diff_attn_v1_decode(q1, q2, oracle.dequant_e4m3(k1, s1), oracle.dequant_e4m3(k2, s2), v, 0.45,
+                                     lin, gamma.cpu(), 1e-5, lens)
+    assert out.shape == (B, H, 2 * d)
+    err = _err(_np(out), ref)
+    assert err <= TOL["bf16"], f"max abs error {err}"
+    # The same codes handed over as plain bytes give the same result.
+    out_u8 = da.diffattn_decode_fp8k(q1, q2, k1.view(torch.uint8), k2.view(torch.uint8), s1, s2, v, lam, lin,
+                                     gamma=gamma, lens=lens_t, workspace=ws)
+    assert torch.equal(out, out_u8)
+
+
+V2_DECODE_FP8 = [  # B, Hq, Hkv, n, lens, per-sequence logits, workspace
+    (2, 4, 2, 300, None, True, False),
+    (3, 8, 2, 1000, [1000, 31, 0], False, False),
+    (1, 2, 1, 1, None, True, False),
+    (2, 4, 1, 5000, [5000, 4097], True, False),
+    (1, 4, 2, 30000, None, True, True),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,n,lens,per_seq,use_ws", V2_DECODE_FP8)
+def test_v2_decode_fp8_keys(B, Hq, Hkv, n, lens, per_seq, use_ws):
+    d = 128
+    g = torch.Generator(device="cuda").manual_seed(1700 + n)
+
+    def rnd(*shape):
+        return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    q, v = rnd(B, Hq, d), rnd(B, n, Hkv, d)
+    k, ks = _quant_e4m3(rnd(B, n, Hkv, d))
+    lg = torch.randn((B, Hq // 2) if per_seq else (Hq // 2,), generator=g, device="cuda")
+    lens_t = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
+    ws = torch.empty(da.v2_decode_workspace_bytes(B, Hq, d), dtype=torch.uint8, device="cuda") if use_ws else None
+    out = da.diffattn_v2_decode_fp8k(q, k, ks, v, lg, lens=lens_t, workspace=ws)
+    da.device_status()
+    lg_host = lg.cpu().double().numpy() if per_seq else np.broadcast_to(lg.cpu().double().numpy(), (B, Hq // 2))
+    ref = oracle.diff_attn_v2_decode(q, oracle.dequant_e4m3(k, ks), v, lg_host, lens)
+    err = _err(_np(out), ref)
+    assert err <= TOL["bf16"], f"max abs error {err}"
+
+
+def test_decode_fp8_keys_bench_sizes():
+    # The FP8-key decode workloads bench.py times, in its launch configuration.
+    g = torch.Generator(device="cuda").manual_seed(1900)
+
+    def rnd(*shape):
+        return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    B, H, n, d = 8, 16, 32768, 64
+    q1, q2 = rnd(B, H, d), rnd(B, H, d)
+    k1, s1 = _quant_e4m3(rnd(B, n, H, d))
+    k2, s2 = _quant_e4m3(rnd(B, n, H, d))
+    v = rnd(B, n, H, 2 * d)
+    lam = torch.tensor([0.3], device="cuda")
+    out = da.diffattn_decode_fp8k(q1, q2, k1, k2, s1, s2, v, lam, 0.2)
+    da.device_status()
+    ref = oracle.diff_attn_v1_decode(q1, q2, oracle.dequant_e4m3(k1, s1), oracle.dequant_e4m3(k2, s2), v, 0.3, 0.2,
+                                     None, 1e-5)
+    assert _err(_np(out), ref) <= TOL["bf16"]
+    del k1, k2, v
+    B, Hq, Hkv, d = 8, 32, 16, 128
+    q, v = rnd(B, Hq, d), rnd(B, n, Hkv, d)
+    k, ks = _quant_e4m3(rnd(B, n, Hkv, d))
+    lg = torch.randn((B, Hq // 2), generator=g, device="cuda")
+    out = da.diffattn_v2_decode_fp8k(q, k, ks, v, lg)
+    da.device_status()
+    ref = oracle.diff_attn_v2_decode(q, oracle.dequant_e4m3(k, ks), v, lg.cpu().double().numpy())
+    assert _err(_np(out), ref) <= TOL["bf16"]

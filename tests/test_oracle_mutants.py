@@ -117,3 +117,28 @@ def test_v2_decode_pin_catches_swapped_pair(monkeypatch):
     monkeypatch.setattr(pins.oracle, "diff_attn_v2_decode", swapped)
     with pytest.raises(AssertionError):
         pins.test_v2_decode_is_the_last_row_of_causal_v2()
+
+
+def _e4m3_bias8(codes):
+    c = np.asarray(codes).astype(np.int64)
+    e, m = (c >> 3) & 0xF, (c & 7) / 8.0
+    mag = np.where(e == 0, m * 2.0 ** -7, (1 + m) * np.exp2(e - 8.0))  # exponent bias 8 instead of 7
+    return np.where(c & 0x80, -mag, mag)
+
+
+def _e4m3_no_subnormals(codes):
+    c = np.asarray(codes).astype(np.int64)
+    e, m = (c >> 3) & 0xF, (c & 7) / 8.0
+    mag = (1 + m) * np.exp2(e - 7.0)  # treats exponent 0 as normal
+    mag = np.where(c & 0x7F, mag, 0.0)
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return np.where(c & 0x80, -mag, mag)
+
+
+@pytest.mark.parametrize("mutant", [_e4m3_bias8, _e4m3_no_subnormals])
+def test_e4m3_pins_catch_mutants(monkeypatch, mutant):
+    monkeypatch.setattr(pins.oracle, "e4m3_decode", mutant)
+    with pytest.raises(AssertionError):
+        pins.test_e4m3_decode_closed_forms()
+    with pytest.raises(AssertionError):
+        pins.test_e4m3_decode_matches_torch_float8()

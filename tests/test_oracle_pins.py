@@ -382,3 +382,31 @@ def test_v2_decode_lengths_and_closed_forms():
         for g in range(Hq // 2):
             want = (1 - 1 / (1 + math.exp(-lg[b, g]))) * v[b, :L, 0].mean(axis=0)
             np.testing.assert_allclose(z[b, g], want, atol=1e-12)
+
+
+# ---------------------------------------------------------------- FP8 (e4m3) key-cache codes
+def test_e4m3_decode_closed_forms():
+    # Values the E4M3 format fixes: zero and negative zero, one, the largest
+    # finite value, the smallest normal and subnormal values, NaN, sign symmetry.
+    v = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    assert v[0x00] == 0.0 and v[0x80] == 0.0 and math.copysign(1.0, v[0x80]) == -1.0
+    assert v[0x38] == 1.0 and v[0xB8] == -1.0
+    assert v[0x30] == 0.5 and v[0x40] == 2.0 and v[0x3C] == 1.5
+    assert v[0x7E] == 448.0 and v[0xFE] == -448.0
+    assert v[0x08] == 2.0 ** -6 and v[0x01] == 2.0 ** -9 and v[0x07] == 7 * 2.0 ** -9
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF]) and np.isnan(v).sum() == 2
+    np.testing.assert_array_equal(v[0x80:0xFF], -v[0x00:0x7F])
+    assert np.all(np.diff(v[0x00:0x7F]) > 0)  # finite positive codes increase with the code
+
+
+def test_e4m3_decode_matches_torch_float8():
+    # Every code against PyTorch's own float8_e4m3fn conversion (a library routine).
+    c = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    want = c.view(torch.float8_e4m3fn).double().numpy()
+    got = oracle.e4m3_decode(c.numpy())
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    np.testing.assert_array_equal(got[ok], want[ok])
+    # A float8 tensor is read through its bytes; dequantisation multiplies by the scale.
+    x = torch.tensor([[0.75, -3.5], [448.0, 2.0 ** -9]]).to(torch.float8_e4m3fn)
+    np.testing.assert_array_equal(oracle.dequant_e4m3(x, 0.25), 0.25 * np.array([[0.75, -3.5], [448.0, 2.0 ** -9]]))

@@ -559,6 +559,9 @@ def test_decode_ring(nblk):
     for seed in range(30):
         assert decode(nblk, seed) == "ok", seed
         assert decode(nblk, seed, nwarp=8) == "ok", seed
+        # e4m3 key caches: four stages of 24 KB
+        assert decode(nblk, seed, nst=4) == "ok", seed
+        assert decode(nblk, seed, nst=4, nwarp=8) == "ok", seed
 
 
 def test_model_catches_decode_refill_without_empty_wait():
