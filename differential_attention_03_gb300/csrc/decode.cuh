@@ -31,7 +31,9 @@
 //     (32 products of q . k each, combined by shuffles), so a warp scores its
 //     keys in one pass; every warp keeps its own online-softmax state per map
 //     (running maximum, per-lane partial sums, 2d / 32 output channels per
-//     lane for each map), rescaled only when the maximum grows.
+//     lane for each map), rescaled only when the maximum grows.  Products
+//     and value accumulations run as packed f32x2 FMAs (two lanes of fp32
+//     arithmetic per instruction), which halves the instructions a key costs.
 //   * The CTA merges its warps' states in shared memory; the cluster's CTAs
 //     then merge theirs through distributed shared memory in CTA rank 0,
 //     which applies the combine and the per-head RMSNorm and stores the row.
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
   const int kk = lane / PARTS, prt = lane % PARTS;
   const float qs1 = K8 ? p.scale_log2 * p.k1_scale : p.scale_log2;
   const float qs2 = K8 ? p.scale_log2 * (V2 ? p.k1_scale : p.k2_scale) : p.scale_log2;
-  float q1r[32], q2r[32];
+  uint64_t q1r[16], q2r[16];  // pairs of query products
   {
     const __nv_bfloat16* q1p = p.q1 + q1_off + prt * 32;
     const __nv_bfloat16* q2p = (V2 ? p.q1 : p.q2) + q2_off + prt * 32;
@@ -306,18 +308,16 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
       const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wc[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        q1r[i + 2 * e] = bf16_lo(wa[e]) * qs1;
-        q1r[i + 2 * e + 1] = bf16_hi(wa[e]) * qs1;
-        q2r[i + 2 * e] = bf16_lo(wc[e]) * qs2;
-        q2r[i + 2 * e + 1] = bf16_hi(wc[e]) * qs2;
+        q1r[i / 2 + e] = f2pack(bf16_lo(wa[e]) * qs1, bf16_hi(wa[e]) * qs1);
+        q2r[i / 2 + e] = f2pack(bf16_lo(wc[e]) * qs2, bf16_hi(wc[e]) * qs2);
       }
     }
   }
 
   float m1 = -INFINITY, m2 = -INFINITY, ls1 = 0.f, ls2 = 0.f;
-  float o1[CH], o2[CH];
+  uint64_t o1p[CH / 2], o2p[CH / 2];
 #pragma unroll
-  for (int c = 0; c < CH; ++c) o1[c] = o2[c] = 0.f;
+  for (int c = 0; c < CH / 2; ++c) o1p[c] = o2p[c] = 0ull;
   // Byte offsets inside a stage that do not change: this lane's 32 key
   // columns (box, first 16-byte chunk) and its CH value channels.
   const int kbox = (prt * 32) / 64, kchunk0 = ((prt * 32) % 64) / 8;
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
     const uint8_t* st = smem + s * C::STAGE;
     const int row = warp * KW + kk;  // this lane's key within the stage
     // ---- scores: 32 products per lane, PARTS lanes per key
-    float s1 = 0.f, s2 = 0.f;
+    uint64_t a1 = 0ull, a2 = 0ull, b1 = 0ull, b2 = 0ull;
     if constexpr (K8) {
       // 32 e4m3 key values: 16-byte chunks 2 prt and 2 prt + 1 of the row
       // (128-byte rows: 128-byte swizzle, chunk ^ (row % 8); 64-byte rows:
@@ -347,11 +347,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
           float fa[4], fe[4];
           e4m3x4_to_f32(wa[t], fa);
           e4m3x4_to_f32(we[t], fe);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            s1 = fmaf(q1r[16 * c + 4 * t + u], fa[u], s1);
-            s2 = fmaf(q2r[16 * c + 4 * t + u], fe[u], s2);
-          }
+          a1 = fma2(q1r[8 * c + 2 * t], f2pack(fa[0], fa[1]), a1);
+          b1 = fma2(q1r[8 * c + 2 * t + 1], f2pack(fa[2], fa[3]), b1);
+          a2 = fma2(q2r[8 * c + 2 * t], f2pack(fe[0], fe[1]), a2);
+          b2 = fma2(q2r[8 * c + 2 * t + 1], f2pack(fe[2], fe[3]), b2);
         }
       }
     } else {
@@ -363,12 +362,24 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
         const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, we[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          s1 = fmaf(q1r[8 * c + 2 * t], bf16_lo(wa[t]), s1);
-          s1 = fmaf(q1r[8 * c + 2 * t + 1], bf16_hi(wa[t]), s1);
-          s2 = fmaf(q2r[8 * c + 2 * t], bf16_lo(we[t]), s2);
-          s2 = fmaf(q2r[8 * c + 2 * t + 1], bf16_hi(we[t]), s2);
+          if (t & 1) {
+            b1 = fma2(q1r[4 * c + t], f2pack(bf16_lo(wa[t]), bf16_hi(wa[t])), b1);
+            b2 = fma2(q2r[4 * c + t], f2pack(bf16_lo(we[t]), bf16_hi(we[t])), b2);
+          } else {
+            a1 = fma2(q1r[4 * c + t], f2pack(bf16_lo(wa[t]), bf16_hi(wa[t])), a1);
+            a2 = fma2(q2r[4 * c + t], f2pack(bf16_lo(we[t]), bf16_hi(we[t])), a2);
+          }
         }
       }
+    }
+    float s1, s2;
+    {
+      const uint64_t t1 = add2(a1, b1), t2 = add2(a2, b2);
+      float l, h;
+      f2unpack(t1, l, h);
+      s1 = l + h;
+      f2unpack(t2, l, h);
+      s2 = l + h;
     }
 #pragma unroll
     for (int x = 1; x < PARTS; x <<= 1) {
@@ -388,14 +399,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
       m1 = x1;
       ls1 *= f;
 #pragma unroll
-      for (int c = 0; c < CH; ++c) o1[c] *= f;
+      for (int c = 0; c < CH / 2; ++c) o1p[c] = fma2(o1p[c], f2pack(f, f), 0ull);
     }
     if (x2 > m2) {
       const float f = (m2 == -INFINITY) ? 0.f : ex2(m2 - x2);
       m2 = x2;
       ls2 *= f;
 #pragma unroll
-      for (int c = 0; c < CH; ++c) o2[c] *= f;
+      for (int c = 0; c < CH / 2; ++c) o2p[c] = fma2(o2p[c], f2pack(f, f), 0ull);
     }
     const float p1 = (s1 == -INFINITY) ? 0.f : ex2(s1 - m1);
     const float p2 = (s2 == -INFINITY) ? 0.f : ex2(s2 - m2);
@@ -425,11 +436,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
       }
 #pragma unroll
       for (int c = 0; c < CH / 2; ++c) {
-        const float va = bf16_lo(vw[c]), vc = bf16_hi(vw[c]);
-        o1[2 * c] = fmaf(w1, va, o1[2 * c]);
-        o1[2 * c + 1] = fmaf(w1, vc, o1[2 * c + 1]);
-        o2[2 * c] = fmaf(w2, va, o2[2 * c]);
-        o2[2 * c + 1] = fmaf(w2, vc, o2[2 * c + 1]);
+        const uint64_t vp = f2pack(bf16_lo(vw[c]), bf16_hi(vw[c]));
+        o1p[c] = fma2(f2pack(w1, w1), vp, o1p[c]);
+        o2p[c] = fma2(f2pack(w2, w2), vp, o2p[c]);
       }
     }
     // ---- release the stage; thread 0 refills it once all four warps have
@@ -461,9 +470,14 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
     wp[3] = ls2;
   }
 #pragma unroll
-  for (int c = 0; c < CH; ++c) {
-    wp[4 + vc0 + c] = o1[c];
-    wp[4 + DV + vc0 + c] = o2[c];
+  for (int c = 0; c < CH / 2; ++c) {
+    float l, h;
+    f2unpack(o1p[c], l, h);
+    wp[4 + vc0 + 2 * c] = l;
+    wp[4 + vc0 + 2 * c + 1] = h;
+    f2unpack(o2p[c], l, h);
+    wp[4 + DV + vc0 + 2 * c] = l;
+    wp[4 + DV + vc0 + 2 * c + 1] = h;
   }
   __syncthreads();
   {
