@@ -481,9 +481,10 @@ def run_ours(args):
                 del xc
             torch.cuda.empty_cache()
 
-    decode = {}
+    decode, backward = {}, {}
     if rank == 0 and world == 1 and not args.no_all_configs:
         decode = decode_results(da, flush, peaks)
+        backward = backward_results(da, flush, (clocks or {}).get("sm_mhz") or 2070)
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -505,6 +506,8 @@ def run_ours(args):
         line["configs"] = configs
     if decode:
         line["decode"] = decode
+    if backward:
+        line["backward"] = backward
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(w, x)
         cb.pop("seconds", None)
@@ -548,6 +551,67 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+BACKWARD_WORKLOADS = [  # (name, B, H, n, d): fp32 DIFF V1 backward, causal
+    ("v1-bwd-f32-B4H16-n2048-d64", 4, 16, 2048, 64),
+    ("v1-bwd-f32-B1H1-n128-d64", 1, 1, 128, 64),
+]
+# fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 flops x the SM clock (MHz).
+FP32_LANES = 152 * 128
+
+
+def backward_flops(B, H, n, d):
+    """Algorithmic FLOPs of the backward: per visible (query, key) pair 20 d.
+
+    2 d each for the two score recomputations, 4 d for dO . v (value width 2d),
+    4 d for dV, 2 d each for dQ_1, dQ_2, dK_1, dK_2; causal: n (n + 1) / 2 pairs.
+    """
+    return B * H * (n * (n + 1) // 2) * 20 * d
+
+
+def time_backward(da, flush, B, H, n, d, runs=10):
+    """fp32 DIFF V1 backward (4 kernels): median CUDA-event time, L2 flushed."""
+    import torch
+    g = torch.Generator(device="cuda").manual_seed(3000 + n + d)
+
+    def rnd(*shape):
+        return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32)
+    q1, q2, k1, k2 = (rnd(B, n, H, d) for _ in range(4))
+    v, dy = rnd(B, n, H, 2 * d), rnd(B, n, H, 2 * d)
+    gamma = torch.ones(2 * d, device="cuda")
+    lam = torch.tensor([0.3], device="cuda")
+    ws = torch.empty(da.backward_workspace_bytes(B, H, n, d), dtype=torch.uint8, device="cuda")
+
+    def call():
+        da.diffattn_backward(q1, q2, k1, k2, v, lam, 0.2, dy, gamma=gamma, workspace=ws)
+    for _ in range(3):
+        call()
+    da.device_status()
+    ts = []
+    for _ in range(runs):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    da.device_status()
+    torch.cuda.empty_cache()
+    return statistics.median(ts)
+
+
+def backward_results(da, flush, sm_mhz):
+    out = {}
+    peak = 2 * FP32_LANES * sm_mhz * 1e6 / 1e12
+    for name, B, H, n, d in BACKWARD_WORKLOADS:
+        ms = time_backward(da, flush, B, H, n, d)
+        tf = backward_flops(B, H, n, d) / (ms * 1e-3) / 1e12
+        out[name] = {"ms": round(ms, 4), "tflops": round(tf, 3), "bound": "alu",
+                     "peak_tflops": round(peak, 1), "peak": f"fp32 FMA: {FP32_LANES} lanes x 2 x {sm_mhz} MHz",
+                     "frac": round(tf / peak, 4), "tokens_per_s": round(B * n / (ms * 1e-3), 1)}
+    return out
+
+
 def decode_results(da, flush, peaks):
     out = {}
     for name, B, H, n, d, keys in DECODE_WORKLOADS:
@@ -557,6 +621,15 @@ def decode_results(da, flush, peaks):
                      "frac": round(gbs / peaks["hbm_gbs"], 4), "peak_gbs": peaks["hbm_gbs"],
                      "algorithmic_bytes": nb, "tokens_per_s": round(B / (ms * 1e-3), 1)}
     return out
+
+
+def run_backward_only():
+    import torch
+    from differential_attention_03_gb300 import binding as da, build
+    build.build()
+    da.lib()
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
+    print(json.dumps({"backward": backward_results(da, flush, 2070)}), flush=True)
 
 
 def run_decode_only():
@@ -579,6 +652,8 @@ def main(argv=None):
     ap.add_argument("--no-all-configs", action="store_true")
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the decode workloads (one JSON line with the 'decode' object)")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time only the fp32 backward workloads (one JSON line with the 'backward' object)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -586,6 +661,8 @@ def main(argv=None):
         run_reference(args)
     elif args.decode_only:
         run_decode_only()
+    elif args.backward_only:
+        run_backward_only()
     else:
         run_ours(args)
 

@@ -73,6 +73,13 @@ def lib() -> ctypes.CDLL:
             L.diffattn_v2_decode_fp8k.argtypes = [i, i, i, i, i, vp, vp, f, vp, vp, vp, ll, f, vp, vp,
                                                   ctypes.c_size_t, vp]
             L.diffattn_v2_decode_fp8k.restype = i
+            L.diffattn_backward_workspace.argtypes = [i, i, i, i]
+            L.diffattn_backward_workspace.restype = ctypes.c_size_t
+            L.diffattn_backward.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, f, vp, f, i, vp, vp, vp, vp, vp,
+                                            vp, vp, vp, vp, ctypes.c_size_t, vp]
+            L.diffattn_backward.restype = i
+            L.lambda_reparam_backward.argtypes = [vp, vp, vp, vp, i, vp, vp, vp, vp, vp, vp]
+            L.lambda_reparam_backward.restype = i
             L.diffattn_v2_forward.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, ll, ll, f, i, vp, vp]
             L.diffattn_v2_forward.restype = i
             L.diffattn_device_status.argtypes = [vp]
@@ -358,6 +365,53 @@ def diffattn_v2_decode_fp8k(q, k, k_scale: float, v, lam_logits, lens=None, soft
                                          _ptr(lam_logits), sb, float(softmax_scale), _ptr(out), wp, wn,
                                          _stream(stream)))
     return out
+
+
+def backward_workspace_bytes(B: int, H: int, n: int, d: int) -> int:
+    """Device workspace diffattn_backward needs (per-row statistics, dO, dgamma shares)."""
+    return int(lib().diffattn_backward_workspace(B, H, n, d))
+
+
+def diffattn_backward(q1, q2, k1, k2, v, lam, lambda_init_value: float, dy, gamma=None, eps: float = 1e-5,
+                      causal: bool = True, workspace=None, stream=None) -> dict:
+    """DIFF V1 backward (fp32): gradients of diffattn_forward's output given dy.
+
+    Shapes as for diffattn_forward (fp32, d <= 128); dy: [B, n, H, 2d].
+    Returns a dict: dq1, dq2, dk1, dk2, dv (like their inputs), dlam [1],
+    dgamma [2d].  workspace: None (allocated here with torch) or a device
+    tensor of backward_workspace_bytes(B, H, n, d) bytes.
+    """
+    B, n, H, d = q1.shape
+    dt = torch.float32
+    for name, t, shp in (("q1", q1, (B, n, H, d)), ("q2", q2, (B, n, H, d)), ("k1", k1, (B, n, H, d)),
+                         ("k2", k2, (B, n, H, d)), ("v", v, (B, n, H, 2 * d)), ("dy", dy, (B, n, H, 2 * d))):
+        _need(t, name, dt, shp)
+    _need(lam, "lambda", torch.float32, (1,))
+    if gamma is not None:
+        _need(gamma, "gamma", torch.float32, (2 * d,))
+    need = backward_workspace_bytes(B, H, n, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q1.device)
+    wp, wn = _ws_args(workspace, need)
+    g = {k: torch.empty_like(t) for k, t in (("dq1", q1), ("dq2", q2), ("dk1", k1), ("dk2", k2), ("dv", v))}
+    g["dlam"] = torch.empty(1, device=q1.device, dtype=torch.float32)
+    g["dgamma"] = torch.empty(2 * d, device=q1.device, dtype=torch.float32)
+    _check(lib().diffattn_backward(F32, B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v), _ptr(lam),
+                                   float(lambda_init_value), _ptr(gamma), float(eps), 1 if causal else 0, _ptr(dy),
+                                   _ptr(g["dq1"]), _ptr(g["dq2"]), _ptr(g["dk1"]), _ptr(g["dk2"]), _ptr(g["dv"]),
+                                   _ptr(g["dlam"]), _ptr(g["dgamma"]), wp, wn, _stream(stream)))
+    return g
+
+
+def lambda_reparam_backward(lq1, lk1, lq2, lk2, dlam, stream=None):
+    """Gradients of lambda_reparam's lambda with respect to lq1, lk1, lq2, lk2, given dlam [1] (device)."""
+    for name, t in (("lq1", lq1), ("lk1", lk1), ("lq2", lq2), ("lk2", lk2)):
+        _need(t, name, torch.float32, (lq1.numel(),))
+    _need(dlam, "dlam", torch.float32, (1,))
+    outs = [torch.empty_like(t) for t in (lq1, lk1, lq2, lk2)]
+    _check(lib().lambda_reparam_backward(_ptr(lq1), _ptr(lk1), _ptr(lq2), _ptr(lk2), lq1.numel(), _ptr(dlam),
+                                         *(_ptr(o) for o in outs), _stream(stream)))
+    return tuple(outs)
 
 
 def diffattn_v2_forward(q, k, v, lam_logits, causal: bool = True, softmax_scale: float = 0.0, out=None,

@@ -694,6 +694,127 @@ diffattn_status diffattn_v2_forward(diffattn_dtype dt, int B, int Hq, int Hkv, i
   return ok();
 }
 
+// ---- backward (fp32, V1)
+static size_t bwd_rows(int B, int H, int n) { return static_cast<size_t>(B) * H * n; }
+static size_t bwd_row_ctas(int B, int H, int n) {
+  return static_cast<size_t>(B) * H * ((static_cast<size_t>(n) + da::kSimtRows - 1) / da::kSimtRows);
+}
+
+size_t diffattn_backward_workspace(int B, int H, int n, int d) {
+  if (B < 0 || H < 0 || n < 0 || d < 1) return 0;
+  const size_t R = bwd_rows(B, H, n), dv = 2 * static_cast<size_t>(d);
+  return round256(R * dv * 4) + round256(5 * R * 4) + round256(bwd_row_ctas(B, H, n) * dv * 4);
+}
+
+diffattn_status diffattn_backward(diffattn_dtype dt, int B, int H, int n, int d, const void* q1, const void* q2,
+                                  const void* k1, const void* k2, const void* v, const float* lambda,
+                                  float lambda_init, const float* gamma, float eps, int causal, const void* dy,
+                                  void* dq1, void* dq2, void* dk1, void* dk2, void* dv, float* dlambda,
+                                  float* dgamma, void* workspace, size_t workspace_bytes, void* stream) {
+  if (dt != DIFFATTN_F32 && dt != DIFFATTN_BF16)
+    return fail(DIFFATTN_ERR_DTYPE, "diffattn_backward: bad dtype %d", (int)dt);
+  if (B < 0 || H < 0 || n < 0 || d < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_backward: bad sizes B=%d H=%d n=%d d=%d", B, H, n, d);
+  if (dt != DIFFATTN_F32 || d > da::kSimtMaxD)
+    return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_backward: f32 with d <= 128 only (got dtype %d, d=%d)", (int)dt,
+                d);
+  if (!dlambda) return fail(DIFFATTN_ERR_NULL, "diffattn_backward: NULL dlambda");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int dvw = 2 * d;
+  if (B == 0 || H == 0 || n == 0) {  // no rows: dlambda = 0, dgamma = 0
+    cudaError_t e = cudaMemsetAsync(dlambda, 0, sizeof(float), s);
+    if (e == cudaSuccess && dgamma) e = cudaMemsetAsync(dgamma, 0, dvw * sizeof(float), s);
+    if (e != cudaSuccess) return cuda_fail(e, "diffattn_backward: clearing dlambda / dgamma");
+    return ok();
+  }
+  if (!q1 || !q2 || !k1 || !k2 || !v || !lambda || !dy || !dq1 || !dq2 || !dk1 || !dk2 || !dv || !workspace)
+    return fail(DIFFATTN_ERR_NULL, "diffattn_backward: NULL pointer");
+  if (!std::isfinite(lambda_init)) return fail(DIFFATTN_ERR_SHAPE, "diffattn_backward: lambda_init not finite");
+  const size_t need = diffattn_backward_workspace(B, H, n, d);
+  if (workspace_bytes < need)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_backward: workspace of %zu bytes, need %zu", workspace_bytes, need);
+  if (!aligned16(workspace)) return fail(DIFFATTN_ERR_ALIGN, "diffattn_backward: workspace must be 16-byte aligned");
+  const long long nqb8 = (static_cast<long long>(n) + da::kSimtRows - 1) / da::kSimtRows;
+  if (static_cast<long long>(B) * H * nqb8 > 0x7fffffffll)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_backward: too many (batch, head, row block) units");
+  if (eps <= 0.f) eps = 1e-5f;
+  const size_t R = bwd_rows(B, H, n);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* ws_do = reinterpret_cast<float*>(ws);
+  float* ws_row = reinterpret_cast<float*>(ws + round256(R * dvw * 4));
+  float* ws_dg = reinterpret_cast<float*>(ws + round256(R * dvw * 4) + round256(5 * R * 4));
+
+  da::SimtParams rp{};
+  rp.q1 = static_cast<const float*>(q1);
+  rp.q2 = static_cast<const float*>(q2);
+  rp.k1 = static_cast<const float*>(k1);
+  rp.k2 = static_cast<const float*>(k2);
+  rp.v = static_cast<const float*>(v);
+  rp.lambda = lambda;
+  rp.gamma = gamma;
+  rp.scale = 1.f / std::sqrt(static_cast<float>(d));
+  rp.norm_mult = 1.f - lambda_init;
+  rp.eps = eps;
+  rp.B = B;
+  rp.n = n;
+  rp.d = d;
+  rp.dv = dvw;
+  rp.causal = causal ? 1 : 0;
+  rp.v2 = 0;
+  rp.heads_q = rp.heads_kv = rp.units_per_batch = H;
+  rp.group = 1;
+  rp.rows_total = static_cast<long long>(R);
+  rp.dy = static_cast<const float*>(dy);
+  rp.ws_do = ws_do;
+  rp.ws_row = ws_row;
+  rp.ws_dgamma = ws_dg;
+
+  da::BwdParams p{};
+  p.q1 = rp.q1;
+  p.q2 = rp.q2;
+  p.k1 = rp.k1;
+  p.k2 = rp.k2;
+  p.v = rp.v;
+  p.dO = ws_do;
+  p.row = ws_row;
+  p.dgp = ws_dg;
+  p.lambda = lambda;
+  p.dq1 = static_cast<float*>(dq1);
+  p.dq2 = static_cast<float*>(dq2);
+  p.dk1 = static_cast<float*>(dk1);
+  p.dk2 = static_cast<float*>(dk2);
+  p.dv = static_cast<float*>(dv);
+  p.dlambda = dlambda;
+  p.dgamma = dgamma;
+  p.scale = rp.scale;
+  p.B = B;
+  p.H = H;
+  p.n = n;
+  p.d = d;
+  p.dvw = dvw;
+  p.causal = rp.causal;
+  p.rows = static_cast<long long>(R);
+  p.n_row_ctas = static_cast<int>(bwd_row_ctas(B, H, n));
+  cudaError_t e = da::launch_simt_bwd_rows(rp, s);
+  if (e == cudaSuccess) e = da::launch_backward_f32(p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_backward launch");
+  g_launches.fetch_add(4);
+  return ok();
+}
+
+diffattn_status lambda_reparam_backward(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
+                                        int dim, const float* dlambda, float* dlq1, float* dlk1, float* dlq2,
+                                        float* dlk2, void* stream) {
+  if (!lq1 || !lk1 || !lq2 || !lk2 || !dlambda || !dlq1 || !dlk1 || !dlq2 || !dlk2)
+    return fail(DIFFATTN_ERR_NULL, "lambda_reparam_backward: NULL pointer");
+  if (dim < 1) return fail(DIFFATTN_ERR_SHAPE, "lambda_reparam_backward: dim must be >= 1 (got %d)", dim);
+  cudaError_t e = da::launch_lambda_reparam_bwd(lq1, lk1, lq2, lk2, dim, dlambda, dlq1, dlk1, dlq2, dlk2,
+                                                static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "lambda_reparam_backward launch");
+  g_launches.fetch_add(1);
+  return ok();
+}
+
 diffattn_status diffattn_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

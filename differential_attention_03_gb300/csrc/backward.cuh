@@ -1,0 +1,287 @@
+// fp32 backward pass of the multi-head DIFF V1 forward on CUDA cores.
+//
+// The forward (per batch b, head h; c = 1/sqrt d; causal or not):
+//   A_r = softmax(c Q_r K_r^T),  O = (A_1 - lambda A_2) V,
+//   y = (1 - lambda_init) gamma O / rms(O)
+// ("Differential Transformer" glossary page, "How differential attention
+// works"; news article section "差分注意力" for the lambda re-parameterisation
+// and the per-head RMSNorm).  The pages give no backward; it is the chain rule
+// of that forward:
+//   dO from dy through the RMSNorm (row pass: simt_fwd_f32_kernel<true>),
+//   dV = A_1^T dO - lambda A_2^T dO,
+//   dS_1 = A_1 (dO V^T - D_1),  dS_2 = A_2 (-lambda dO V^T - D_2),
+//   dQ_r = c dS_r K_r,  dK_r = c dS_r^T Q_r,
+//   dlambda = -sum dO . A_2 V,  dgamma = sum (1 - lambda_init) (O / rms(O)) dy,
+// with D_r = rowsum(A_r dA_r) from the row pass.  The maps are recomputed
+// from the row pass's log-sum-exps, a 32 x 32 block at a time, never stored.
+//
+//   bwd_dkdv_kernel: one CTA per (b, h, 32 keys); sweeps the query blocks that
+//     see those keys; dV, dK_1, dK_2 of its keys in registers.
+//   bwd_dq_kernel:   one CTA per (b, h, 32 queries); sweeps the key blocks the
+//     queries see; dQ_1, dQ_2 in registers.
+//   bwd_reduce_kernel: dlambda and dgamma from the row pass's shares, in a
+//     fixed order (deterministic).
+// Both sweeps use the same 32 x 32 block step: warp w takes query rows
+// 4w .. 4w + 3 of the block and lane j its key j (scores and dO . v_j as
+// dot products over shared-memory rows padded to an odd pitch), writes
+// P = A_1 - lambda A_2, dS_1 and dS_2 to shared memory; then every thread
+// accumulates its outputs from them.
+#pragma once
+
+#include "params.h"
+#include "stage.cuh"
+
+namespace da {
+
+constexpr int kBwdBlk = 32;  // queries and keys per block step
+constexpr int kBwdThreads = 256;
+constexpr int kBwdMaxCV = 32;  // value channels a thread accumulates (dv <= 256)
+constexpr int kBwdMaxCK = 16;  // key/query channels a thread accumulates (d <= 128)
+
+// Shared-memory floats of both sweeps: K_1, K_2, V, Q_1, Q_2, dO tiles, three
+// 32 x 33 blocks (P, dS_1, dS_2) and the four row statistics.
+__host__ __device__ constexpr int bwd_smem_floats(int d, int dv) {
+  return 4 * kBwdBlk * (d + 1) + 2 * kBwdBlk * (dv + 1) + 3 * kBwdBlk * (kBwdBlk + 1) + 4 * kBwdBlk;
+}
+
+struct BwdSmem {
+  float *k1, *k2, *v, *q1, *q2, *dO, *P, *S1, *S2, *st;
+  __device__ BwdSmem(float* sm, int d, int dv) {
+    const int dp = d + 1, dvp = dv + 1;
+    k1 = sm;
+    k2 = k1 + kBwdBlk * dp;
+    v = k2 + kBwdBlk * dp;
+    q1 = v + kBwdBlk * dvp;
+    q2 = q1 + kBwdBlk * dp;
+    dO = q2 + kBwdBlk * dp;
+    P = dO + kBwdBlk * dvp;
+    S1 = P + kBwdBlk * (kBwdBlk + 1);
+    S2 = S1 + kBwdBlk * (kBwdBlk + 1);
+    st = S2 + kBwdBlk * (kBwdBlk + 1);  // [4][32]: lse_1, lse_2, D_1, D_2 of the query block
+  }
+};
+
+// Stages the query block [q0, q0 + 32) of unit (b, h): Q_1, Q_2, dO rows and statistics.
+__device__ __forceinline__ void bwd_stage_queries(const BwdParams& p, const BwdSmem& s, int b, int h, int q0,
+                                                  bool vec) {
+  const int d = p.d, dv = p.dvw;
+  const size_t qrow = static_cast<size_t>(p.H) * d;
+  const long long unit_row0 = (static_cast<long long>(b) * p.H + h) * p.n;
+  stage_rows(s.q1, d + 1, p.q1 + static_cast<size_t>(b) * p.n * qrow + static_cast<size_t>(h) * d, qrow, q0, p.n,
+             d, kBwdBlk, vec);
+  stage_rows(s.q2, d + 1, p.q2 + static_cast<size_t>(b) * p.n * qrow + static_cast<size_t>(h) * d, qrow, q0, p.n,
+             d, kBwdBlk, vec);
+  stage_rows(s.dO, dv + 1, p.dO + unit_row0 * dv, dv, q0, p.n, dv, kBwdBlk, (dv & 3) == 0);
+  if (threadIdx.x < 4 * kBwdBlk) {
+    const int k = threadIdx.x / kBwdBlk, i = threadIdx.x % kBwdBlk;
+    s.st[threadIdx.x] = (q0 + i < p.n) ? p.row[k * p.rows + unit_row0 + q0 + i] : 0.f;
+  }
+}
+
+// Stages the key block [k0, k0 + 32) of unit (b, h): K_1, K_2, V rows.
+__device__ __forceinline__ void bwd_stage_keys(const BwdParams& p, const BwdSmem& s, int b, int h, int k0, bool vec) {
+  const int d = p.d, dv = p.dvw;
+  const size_t krow = static_cast<size_t>(p.H) * d, vrow = static_cast<size_t>(p.H) * dv;
+  stage_rows(s.k1, d + 1, p.k1 + static_cast<size_t>(b) * p.n * krow + static_cast<size_t>(h) * d, krow, k0, p.n,
+             d, kBwdBlk, vec);
+  stage_rows(s.k2, d + 1, p.k2 + static_cast<size_t>(b) * p.n * krow + static_cast<size_t>(h) * d, krow, k0, p.n,
+             d, kBwdBlk, vec);
+  stage_rows(s.v, dv + 1, p.v + static_cast<size_t>(b) * p.n * vrow + static_cast<size_t>(h) * dv, vrow, k0, p.n,
+             dv, kBwdBlk, vec);
+}
+
+// The 32 x 32 block step: P = A_1 - lambda A_2, dS_1, dS_2 for queries
+// [q0, q0 + 32) and keys [k0, k0 + 32) into shared memory (0 where masked).
+__device__ __forceinline__ void bwd_block_step(const BwdParams& p, const BwdSmem& s, int q0, int k0, float lam) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int d = p.d, dv = p.dvw, dp = d + 1, dvp = dv + 1;
+  const int key = k0 + lane;
+#pragma unroll
+  for (int r = 0; r < kBwdBlk / (kBwdThreads / 32); ++r) {
+    const int i = warp * (kBwdBlk / (kBwdThreads / 32)) + r, t = q0 + i;
+    const bool valid = t < p.n && key < p.n && (!p.causal || key <= t);
+    float s1 = 0.f, s2 = 0.f, dpv = 0.f;
+    for (int e = 0; e < d; ++e) {
+      s1 = fmaf(s.q1[i * dp + e], s.k1[lane * dp + e], s1);
+      s2 = fmaf(s.q2[i * dp + e], s.k2[lane * dp + e], s2);
+    }
+    for (int c = 0; c < dv; ++c) dpv = fmaf(s.dO[i * dvp + c], s.v[lane * dvp + c], dpv);
+    const float p1 = valid ? expf(s1 * p.scale - s.st[i]) : 0.f;
+    const float p2 = valid ? expf(s2 * p.scale - s.st[kBwdBlk + i]) : 0.f;
+    s.P[i * (kBwdBlk + 1) + lane] = p1 - lam * p2;
+    s.S1[i * (kBwdBlk + 1) + lane] = p1 * (dpv - s.st[2 * kBwdBlk + i]);
+    s.S2[i * (kBwdBlk + 1) + lane] = p2 * (-lam * dpv - s.st[3 * kBwdBlk + i]);
+  }
+}
+
+__device__ __forceinline__ bool bwd_vec(const BwdParams& p) {
+  return ((p.d & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.q1) | reinterpret_cast<uintptr_t>(p.q2) |
+                               reinterpret_cast<uintptr_t>(p.k1) | reinterpret_cast<uintptr_t>(p.k2) |
+                               reinterpret_cast<uintptr_t>(p.v)) & 15u) == 0;
+}
+
+// dV, dK_1, dK_2 of 32 keys: thread (warp w, lane j) owns key k0 + j and the
+// channel slices w * cv .. w * cv + cv - 1 (value) and w * ck .. (key).
+__global__ void __launch_bounds__(kBwdThreads) bwd_dkdv_kernel(const BwdParams p) {
+  extern __shared__ float sm[];
+  const BwdSmem s(sm, p.d, p.dvw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nblk = (p.n + kBwdBlk - 1) / kBwdBlk;
+  const int kb = blockIdx.x % nblk, unit = blockIdx.x / nblk;
+  const int b = unit / p.H, h = unit % p.H, k0 = kb * kBwdBlk;
+  const int d = p.d, dv = p.dvw, dp = d + 1, dvp = dv + 1;
+  const int cv = (dv + 7) / 8, ck = (d + 7) / 8;
+  const bool vec = bwd_vec(p);
+  const float lam = *p.lambda;
+  bwd_stage_keys(p, s, b, h, k0, vec);
+  float av[kBwdMaxCV], a1[kBwdMaxCK], a2[kBwdMaxCK];
+#pragma unroll
+  for (int k = 0; k < kBwdMaxCV; ++k) av[k] = 0.f;
+#pragma unroll
+  for (int k = 0; k < kBwdMaxCK; ++k) a1[k] = a2[k] = 0.f;
+  for (int qb = p.causal ? kb : 0; qb < nblk; ++qb) {
+    const int q0 = qb * kBwdBlk;
+    __syncthreads();  // the previous block's reads are done
+    bwd_stage_queries(p, s, b, h, q0, vec);
+    __syncthreads();
+    bwd_block_step(p, s, q0, k0, lam);
+    __syncthreads();
+    for (int i = 0; i < kBwdBlk; ++i) {
+      const float w = s.P[i * (kBwdBlk + 1) + lane];
+      const float g1 = s.S1[i * (kBwdBlk + 1) + lane];
+      const float g2 = s.S2[i * (kBwdBlk + 1) + lane];
+#pragma unroll
+      for (int k = 0; k < kBwdMaxCV; ++k) {
+        const int c = warp * cv + k;
+        if (k < cv && c < dv) av[k] = fmaf(w, s.dO[i * dvp + c], av[k]);
+      }
+#pragma unroll
+      for (int k = 0; k < kBwdMaxCK; ++k) {
+        const int c = warp * ck + k;
+        if (k < ck && c < d) {
+          a1[k] = fmaf(g1, s.q1[i * dp + c], a1[k]);
+          a2[k] = fmaf(g2, s.q2[i * dp + c], a2[k]);
+        }
+      }
+    }
+  }
+  const int key = k0 + lane;
+  if (key < p.n) {
+    const size_t kr = (static_cast<size_t>(b) * p.n + key) * p.H + h;
+#pragma unroll
+    for (int k = 0; k < kBwdMaxCV; ++k) {
+      const int c = warp * cv + k;
+      if (k < cv && c < dv) p.dv[kr * dv + c] = av[k];
+    }
+#pragma unroll
+    for (int k = 0; k < kBwdMaxCK; ++k) {
+      const int c = warp * ck + k;
+      if (k < ck && c < d) {
+        p.dk1[kr * d + c] = p.scale * a1[k];
+        p.dk2[kr * d + c] = p.scale * a2[k];
+      }
+    }
+  }
+}
+
+// dQ_1, dQ_2 of 32 queries: thread (warp w, lane i) owns query q0 + i and the
+// channel slice w * ck .. w * ck + ck - 1.
+__global__ void __launch_bounds__(kBwdThreads) bwd_dq_kernel(const BwdParams p) {
+  extern __shared__ float sm[];
+  const BwdSmem s(sm, p.d, p.dvw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nblk = (p.n + kBwdBlk - 1) / kBwdBlk;
+  const int qb = nblk - 1 - blockIdx.x % nblk;  // heaviest causal blocks first
+  const int unit = blockIdx.x / nblk;
+  const int b = unit / p.H, h = unit % p.H, q0 = qb * kBwdBlk;
+  const int d = p.d, dp = d + 1;
+  const int ck = (d + 7) / 8;
+  const bool vec = bwd_vec(p);
+  const float lam = *p.lambda;
+  bwd_stage_queries(p, s, b, h, q0, vec);
+  float a1[kBwdMaxCK], a2[kBwdMaxCK];
+#pragma unroll
+  for (int k = 0; k < kBwdMaxCK; ++k) a1[k] = a2[k] = 0.f;
+  const int kb_end = p.causal ? qb : nblk - 1;
+  for (int kb = 0; kb <= kb_end; ++kb) {
+    const int k0 = kb * kBwdBlk;
+    __syncthreads();  // the previous block's reads are done
+    bwd_stage_keys(p, s, b, h, k0, vec);
+    __syncthreads();
+    bwd_block_step(p, s, q0, k0, lam);
+    __syncthreads();
+    for (int j = 0; j < kBwdBlk; ++j) {
+      const float g1 = s.S1[lane * (kBwdBlk + 1) + j];
+      const float g2 = s.S2[lane * (kBwdBlk + 1) + j];
+#pragma unroll
+      for (int k = 0; k < kBwdMaxCK; ++k) {
+        const int c = warp * ck + k;
+        if (k < ck && c < d) {
+          a1[k] = fmaf(g1, s.k1[j * dp + c], a1[k]);
+          a2[k] = fmaf(g2, s.k2[j * dp + c], a2[k]);
+        }
+      }
+    }
+  }
+  const int t = q0 + lane;
+  if (t < p.n) {
+    const size_t qr = (static_cast<size_t>(b) * p.n + t) * p.H + h;
+#pragma unroll
+    for (int k = 0; k < kBwdMaxCK; ++k) {
+      const int c = warp * ck + k;
+      if (k < ck && c < d) {
+        p.dq1[qr * d + c] = p.scale * a1[k];
+        p.dq2[qr * d + c] = p.scale * a2[k];
+      }
+    }
+  }
+}
+
+// dlambda = sum of the rows' shares, dgamma[c] = sum of the CTAs' shares, one
+// CTA, fixed summation order.
+__global__ void __launch_bounds__(kBwdThreads) bwd_reduce_kernel(const BwdParams p) {
+  __shared__ float red[kBwdThreads];
+  float a = 0.f;
+  const float* share = p.row + 4 * p.rows;
+  for (long long r = threadIdx.x; r < p.rows; r += kBwdThreads) a += share[r];
+  red[threadIdx.x] = a;
+  __syncthreads();
+  for (int w = kBwdThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *p.dlambda = red[0];
+  if (p.dgamma != nullptr) {
+    for (int c = threadIdx.x; c < p.dvw; c += kBwdThreads) {
+      float g = 0.f;
+      for (int k = 0; k < p.n_row_ctas; ++k) g += p.dgp[static_cast<size_t>(k) * p.dvw + c];
+      p.dgamma[c] = g;
+    }
+  }
+}
+
+// Gradients of lambda = exp(<lq1, lk1>) - exp(<lq2, lk2>) + lambda_init with
+// respect to the four vectors, given dlambda (device scalar); one warp.
+__global__ void lambda_reparam_bwd_kernel(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
+                                          int dim, const float* dlambda, float* dlq1, float* dlk1, float* dlq2,
+                                          float* dlk2) {
+  float a = 0.f, c = 0.f;
+  for (int i = threadIdx.x; i < dim; i += 32) {
+    a = fmaf(lq1[i], lk1[i], a);
+    c = fmaf(lq2[i], lk2[i], c);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, off);
+    c += __shfl_xor_sync(0xffffffffu, c, off);
+  }
+  const float g = *dlambda, e1 = g * expf(a), e2 = g * expf(c);
+  for (int i = threadIdx.x; i < dim; i += 32) {
+    dlq1[i] = e1 * lk1[i];
+    dlk1[i] = e1 * lq1[i];
+    dlq2[i] = -e2 * lk2[i];
+    dlk2[i] = -e2 * lq2[i];
+  }
+}
+
+}  // namespace da

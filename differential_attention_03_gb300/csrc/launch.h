@@ -8,6 +8,7 @@
 
 namespace da {
 struct DecodeParams;
+struct BwdParams;
 }
 
 namespace da {
@@ -26,6 +27,13 @@ cudaError_t launch_simt_f32(const SimtParams& p, cudaStream_t s);
 cudaError_t launch_decode_v1(const DecodeParams& p, int d, bool k8, int units, int cs, cudaStream_t s);
 // V2 decode, d = 128: head pairs over their shared KV head (one key tile for both queries).
 cudaError_t launch_decode_v2_d128(const DecodeParams& p, bool k8, int units, int cs, cudaStream_t s);
+// fp32 V1 backward: the row pass (per-row statistics, dO, dgamma shares), then the
+// dK/dV and dQ sweeps and the dlambda/dgamma reduction (3 kernels).
+cudaError_t launch_simt_bwd_rows(const SimtParams& p, cudaStream_t s);
+cudaError_t launch_backward_f32(const BwdParams& p, cudaStream_t s);
+cudaError_t launch_lambda_reparam_bwd(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
+                                      int dim, const float* dlambda, float* dlq1, float* dlk1, float* dlq2,
+                                      float* dlk2, cudaStream_t s);
 cudaError_t launch_lambda_reparam(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
                                   int dim, float lambda_init, float* out, cudaStream_t s);
 cudaError_t launch_wait_selftest(unsigned long long budget_cycles, int* status, cudaStream_t s);

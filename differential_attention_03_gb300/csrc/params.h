@@ -81,6 +81,35 @@ struct SimtParams {
   int B, n, d, dv, causal, v2;
   int heads_q, heads_kv, units_per_batch, group;
   long long rows_total;
+  // Backward row pass (V1) only: dy [B, n, H, dv]; outputs in the backward workspace.
+  const float* dy;
+  float* ws_do;      // [B * H * n][dv]: dO, the gradient of the pre-norm output
+  float* ws_row;     // [5][B * H * n]: log-sum-exp 1, 2; D_1; D_2; the row's share of dlambda
+  float* ws_dgamma;  // [CTAs][dv]: each CTA's share of dgamma
+};
+
+// fp32 V1 backward (backward.cuh): inputs, the row pass's workspace, outputs.
+struct BwdParams {
+  const float* q1;  // [B, n, H, d]
+  const float* q2;
+  const float* k1;
+  const float* k2;
+  const float* v;       // [B, n, H, dv]
+  const float* dO;      // [B * H * n][dv] (row pass)
+  const float* row;     // [5][B * H * n]: lse_1, lse_2, D_1, D_2, dlambda share (row pass)
+  const float* dgp;     // [n_row_ctas][dv]: dgamma shares (row pass)
+  const float* lambda;  // device scalar
+  float* dq1;           // [B, n, H, d]
+  float* dq2;
+  float* dk1;
+  float* dk2;
+  float* dv;       // [B, n, H, dv]
+  float* dlambda;  // device scalar
+  float* dgamma;   // [dv] or nullptr
+  float scale;
+  int B, H, n, d, dvw, causal;
+  long long rows;  // B * H * n
+  int n_row_ctas;
 };
 
 constexpr int kSimtMaxD = 128;

@@ -12,10 +12,17 @@
 // (max, sum) states are updated with warp shuffles, and every lane
 // accumulates its value channels (lane + 32 c) of O1 and O2.  Epilogue:
 // O1 / l1 - c O2 / l2, then the V1 per-head RMSNorm x (1 - lambda_init).
+//
+// With BWD (V1 only) the same sweep is the backward pass's row pass: the
+// epilogue writes, per query row, the maps' log-sum-exps, dO (the gradient
+// of the pre-norm output, through the RMSNorm), D_r = rowsum(A_r * dA_r) and
+// the row's share of dlambda, and per CTA its share of dgamma (the dK/dV and
+// dQ sweeps are in backward.cuh).
 #pragma once
 
 #include "params.h"
 #include "ptx.cuh"
+#include "stage.cuh"
 
 namespace da {
 
@@ -25,61 +32,7 @@ __host__ __device__ constexpr int simt_smem_floats(int d, int dv) {
   return 2 * kSimtRows * d + 2 * kSimtKeys * (d + 1) + kSimtKeys * dv;
 }
 
-// Copies rows [r0, r0 + nrows) x columns [0, width) of a strided global matrix
-// into shared memory (row pitch `pitch` floats), zero past `nvalid` rows.
-// With `vec` (width % 4 == 0, 16-byte aligned rows) it uses 16-byte loads.
-// All loads of the thread are issued before any store, so the copy costs one
-// memory round trip.
-__device__ __forceinline__ void stage_rows(float* dst, int pitch, const float* src, size_t stride, int r0,
-                                           int nvalid, int width, int nrows, bool vec) {
-  constexpr int kMaxPerThread = 8;  // 32 rows x 256 floats / 4 per load / 256 threads
-  if (vec) {
-    const int w4 = width >> 2, total = nrows * w4;
-    float4 buf[kMaxPerThread];
-#pragma unroll
-    for (int k = 0; k < kMaxPerThread; ++k) {
-      const int i = threadIdx.x + k * kSimtWarps * 32;
-      buf[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (i < total) {
-        const int r = i / w4, c = (i % w4) * 4;
-        if (r0 + r < nvalid) buf[k] = __ldg(reinterpret_cast<const float4*>(src + (r0 + r) * stride + c));
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kMaxPerThread; ++k) {
-      const int i = threadIdx.x + k * kSimtWarps * 32;
-      if (i < total) {
-        const int r = i / w4, c = (i % w4) * 4;
-        float* o = dst + r * pitch + c;
-        o[0] = buf[k].x;
-        o[1] = buf[k].y;
-        o[2] = buf[k].z;
-        o[3] = buf[k].w;
-      }
-    }
-  } else {
-    constexpr int kMaxScalar = 4 * kMaxPerThread;
-    const int total = nrows * width;
-    for (int base = 0; base < total; base += kMaxScalar * kSimtWarps * 32) {
-      float buf[kMaxScalar];
-#pragma unroll
-      for (int k = 0; k < kMaxScalar; ++k) {
-        const int i = base + threadIdx.x + k * kSimtWarps * 32;
-        buf[k] = 0.f;
-        if (i < total) {
-          const int r = i / width, c = i % width;
-          if (r0 + r < nvalid) buf[k] = __ldg(src + (r0 + r) * stride + c);
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < kMaxScalar; ++k) {
-        const int i = base + threadIdx.x + k * kSimtWarps * 32;
-        if (i < total) dst[(i / width) * pitch + i % width] = buf[k];
-      }
-    }
-  }
-}
-
+template <bool BWD>
 __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const SimtParams p) {
   extern __shared__ float sm[];
   constexpr int R = kSimtRows / kSimtWarps;  // query rows per warp
@@ -195,6 +148,83 @@ __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const Sim
     }
   }
 
+  if constexpr (BWD) {
+    static_assert(R == 1, "one query row per warp");
+    // Backward row pass, with m = 1 - lambda_init, O_r = A_r V, O = O_1 - lambda O_2,
+    // Oh = O / rms(O), g = m gamma dy:
+    //   dO = (g - Oh mean(g Oh)) / rms(O);  D_1 = dO . O_1;  D_2 = -lambda dO . O_2;
+    //   dlambda_row = -dO . O_2;  dgamma += m Oh dy.
+    __syncthreads();  // every warp is done with the key tiles: sk1 now stages dgamma rows
+    float* sdg = sk1;  // [kSimtWarps][dv] (32 (d + 1) >= 8 dv floats)
+    const int t = q0 + warp;
+    const long long R_rows = p.rows_total;
+    if (t < p.n) {  // warp-uniform
+      const float lam = *p.lambda;
+      const float a1 = 1.f / l1[0], a2 = 1.f / l2[0];
+      float o1n[NC], o2n[NC], y[NC], ss = 0.f;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        o1n[c] = o1[0][c] * a1;
+        o2n[c] = o2[0][c] * a2;
+        y[c] = o1n[c] - lam * o2n[c];
+        if (lane + 32 * c < dv) ss = fmaf(y[c], y[c], ss);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      const float rinv = rsqrtf(ss / dv + p.eps);
+      const long long ri = (static_cast<long long>(b) * p.units_per_batch + u) * p.n + t;
+      const float* dyrow = p.dy + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * dv;
+      float g[NC], oh[NC], gs = 0.f;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        const int col = lane + 32 * c;
+        g[c] = oh[c] = 0.f;
+        if (col < dv) {
+          const float dyc = dyrow[col];
+          g[c] = p.norm_mult * (p.gamma != nullptr ? p.gamma[col] : 1.f) * dyc;
+          oh[c] = y[c] * rinv;
+          gs = fmaf(g[c], oh[c], gs);
+          sdg[warp * dv + col] = p.norm_mult * oh[c] * dyc;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, off);
+      const float gmean = gs / dv;
+      float dd1 = 0.f, dd2 = 0.f;
+      float* dorow = p.ws_do + ri * dv;
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        const int col = lane + 32 * c;
+        if (col < dv) {
+          const float dO = (g[c] - oh[c] * gmean) * rinv;
+          dorow[col] = dO;
+          dd1 = fmaf(dO, o1n[c], dd1);
+          dd2 = fmaf(dO, o2n[c], dd2);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        dd1 += __shfl_xor_sync(0xffffffffu, dd1, off);
+        dd2 += __shfl_xor_sync(0xffffffffu, dd2, off);
+      }
+      if (lane == 0) {
+        p.ws_row[ri] = m1[0] + logf(l1[0]);
+        p.ws_row[R_rows + ri] = m2[0] + logf(l2[0]);
+        p.ws_row[2 * R_rows + ri] = dd1;
+        p.ws_row[3 * R_rows + ri] = -lam * dd2;
+        p.ws_row[4 * R_rows + ri] = -dd2;
+      }
+    } else {
+      for (int col = lane; col < dv; col += 32) sdg[warp * dv + col] = 0.f;
+    }
+    __syncthreads();
+    for (int col = threadIdx.x; col < dv; col += kSimtWarps * 32) {
+      float a = 0.f;
+#pragma unroll
+      for (int w = 0; w < kSimtWarps; ++w) a += sdg[w * dv + col];
+      p.ws_dgamma[static_cast<size_t>(blockIdx.x) * dv + col] = a;
+    }
+  } else {
   // ---- epilogue: out = O1 / l1 - c O2 / l2 (then the V1 norm)
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -231,6 +261,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const Sim
       }
     }
   }
+  }  // !BWD
 }
 
 // lambda = exp(<lq1, lk1>) - exp(<lq2, lk2>) + lambda_init, one warp.

@@ -261,6 +261,49 @@ diffattn_status diffattn_v2_forward(diffattn_dtype dt, int B, int Hq, int Hkv, i
                                     void* stream);
 
 /*
+ * Backward pass of diffattn_forward (DIFF V1), fp32 on CUDA cores.  The pages
+ * ("Differential Transformer" glossary page, "How differential attention
+ * works"; news article section "差分注意力") define the forward and report
+ * trained models; the gradients are the chain rule of that forward:
+ *
+ *   A_r = softmax(Q_r K_r^T / sqrt d),  O = (A_1 - lambda A_2) V,
+ *   y = (1 - lambda_init) gamma O / sqrt(mean_c O^2 + eps)
+ *
+ * Given dy = dL/dy it writes dL/dq1, dq2, dk1, dk2, dv, dL/dlambda and
+ * dL/dgamma; the maps are recomputed, never stored.
+ *   dt          : DIFFATTN_F32 (d in [1, 128]); DIFFATTN_BF16 -> ERR_UNSUPPORTED.
+ *   q1, q2, k1, k2, dq1, dq2, dk1, dk2 : [B, n, H, d] device; v, dy, dv : [B, n, H, 2d].
+ *   lambda      : device scalar (as for the forward); lambda_init, eps, causal, gamma
+ *                 (device [2d] or NULL for ones): as for diffattn_forward.
+ *   dlambda     : device scalar (required); dgamma : device [2d] or NULL (not written).
+ *   workspace   : device memory of at least diffattn_backward_workspace(B, H, n, d)
+ *                 bytes, 16-byte aligned (per-row statistics, dO, dgamma shares);
+ *                 smaller -> ERR_SHAPE.  The library allocates nothing.
+ * Sums for dlambda and dgamma run in a fixed order (same inputs, same bits).
+ * Asynchronous on `stream` (four kernels).  Errors as for diffattn_forward.
+ */
+size_t diffattn_backward_workspace(int B, int H, int n, int d);
+
+diffattn_status diffattn_backward(diffattn_dtype dt, int B, int H, int n, int d, const void* q1,
+                                  const void* q2, const void* k1, const void* k2, const void* v,
+                                  const float* lambda, float lambda_init, const float* gamma,
+                                  float eps, int causal, const void* dy, void* dq1, void* dq2,
+                                  void* dk1, void* dk2, void* dv, float* dlambda, float* dgamma,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Gradients of lambda = exp(<lq1, lk1>) - exp(<lq2, lk2>) + lambda_init
+ * (news article section "差分注意力") with respect to the four vectors of
+ * length dim, given the device scalar dlambda: dlq1 = dlambda exp(<lq1, lk1>) lk1,
+ * dlk1 = dlambda exp(<lq1, lk1>) lq1, and the second pair with the opposite
+ * sign.  All pointers are device fp32.  One warp, asynchronous on `stream`.
+ */
+diffattn_status lambda_reparam_backward(const float* lq1, const float* lk1, const float* lq2,
+                                        const float* lk2, int dim, const float* dlambda,
+                                        float* dlq1, float* dlk1, float* dlq2, float* dlk2,
+                                        void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device status
  * word on the current device.  Returns DIFFATTN_OK, DIFFATTN_ERR_TIMEOUT if a
  * bounded in-kernel wait ran out since the last call, or DIFFATTN_ERR_CUDA if

@@ -35,7 +35,8 @@ def test_header_declares_the_entry_points():
                  "diffattn_device_status", "diffattn_last_error", "diffattn_forward_host",
                  "diffattn_forward_host_workspace", "diffattn_decode", "diffattn_v2_decode",
                  "diffattn_decode_workspace", "diffattn_v2_decode_workspace", "diffattn_decode_fp8k",
-                 "diffattn_v2_decode_fp8k"):
+                 "diffattn_v2_decode_fp8k", "diffattn_backward", "diffattn_backward_workspace",
+                 "lambda_reparam_backward"):
         assert want in names
 
 
@@ -168,6 +169,31 @@ def test_fp8k_decode_host_validation(L):
     assert v2(d=64) == da.ERR_UNSUPPORTED
     assert v2(s=0.0) == da.ERR_SHAPE
     assert v2(k=MIS) == da.ERR_ALIGN
+
+
+def test_backward_host_validation(L):
+    need = L.diffattn_backward_workspace(2, 3, 100, 64)
+    R = 2 * 3 * 100
+    ctas = 2 * 3 * 13  # 8-row blocks of the row pass
+    r256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert need == r256(R * 128 * 4) + r256(5 * R * 4) + r256(ctas * 128 * 4)
+    W = P(0x100000)
+
+    def call(dt=0, B=2, n=100, d=64, q1=A, dlam=A, ws=W, nbytes=need):
+        return L.diffattn_backward(dt, B, 3, n, d, q1, A, A, A, A, A, ctypes.c_float(0.2), None,
+                                   ctypes.c_float(1e-5), 1, A, A, A, A, A, A, dlam, None, ws, nbytes, None)
+    assert call(dt=7) == da.ERR_DTYPE
+    assert call(dt=1) == da.ERR_UNSUPPORTED  # bf16 backward is not provided
+    assert call(d=129) == da.ERR_UNSUPPORTED
+    assert call(n=-1) == da.ERR_SHAPE
+    assert call(dlam=None) == da.ERR_NULL
+    assert call(q1=None) == da.ERR_NULL
+    assert call(ws=None) == da.ERR_NULL
+    assert call(nbytes=need - 1) == da.ERR_SHAPE
+    assert b"workspace" in L.diffattn_last_error()
+    assert call(ws=P(0x100008)) == da.ERR_ALIGN
+    assert L.lambda_reparam_backward(A, A, A, A, 8, None, A, A, A, A, None) == da.ERR_NULL
+    assert L.lambda_reparam_backward(A, A, A, A, 0, A, A, A, A, A, None) == da.ERR_SHAPE
 
 
 def test_v2_host_validation(L):

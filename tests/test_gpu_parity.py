@@ -543,3 +543,83 @@ def test_decode_fp8_keys_bench_sizes():
     da.device_status()
     ref = oracle.diff_attn_v2_decode(q, oracle.dequant_e4m3(k, ks), v, lg.cpu().double().numpy())
     assert _err(_np(out), ref) <= TOL["bf16"]
+
+
+# --------------------------------------------------------------------------- backward (fp32)
+BWD = [  # B, H, n, d, causal, lambda, gamma
+    (1, 1, 1, 8, True, 0.35, True),        # one token
+    (2, 2, 40, 16, True, 0.35, True),      # one ragged 32-block plus a tail
+    (1, 2, 100, 64, True, -0.3, False),    # lambda < 0, no gamma
+    (2, 1, 77, 32, False, 1.2, True),      # non-causal, lambda > 1
+    (1, 1, 130, 128, True, 0.6, True),     # d = 128: value width 256
+    (1, 2, 65, 30, True, 0.5, True),       # d % 4 != 0: scalar staging
+]
+
+
+def _bwd_inputs(B, H, n, d, gamma, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+
+    def rnd(*shape):
+        return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32)
+    x = {k: rnd(B, n, H, d) for k in ("q1", "q2", "k1", "k2")}
+    x["v"], x["dy"] = rnd(B, n, H, 2 * d), rnd(B, n, H, 2 * d)
+    x["gamma"] = (0.9 + 0.2 * torch.rand(2 * d, generator=g, device="cuda")) if gamma else None
+    return x
+
+
+@pytest.mark.parametrize("B,H,n,d,causal,lam,gamma", BWD)
+def test_v1_backward_f32(B, H, n, d, causal, lam, gamma):
+    x = _bwd_inputs(B, H, n, d, gamma, 2000 + n + d)
+    lin = da.lambda_init(3)
+    lam_t = torch.tensor([lam], device="cuda")
+    got = da.diffattn_backward(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], lam_t, lin, x["dy"], gamma=x["gamma"],
+                               causal=causal)
+    da.device_status()
+    ref = oracle.diff_attn_v1_backward(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], lam, lin,
+                                       None if x["gamma"] is None else x["gamma"].cpu(), 1e-5, causal, x["dy"])
+    for k in ("dq1", "dq2", "dk1", "dk2", "dv", "dgamma"):
+        r = np.asarray(ref[k])
+        scale = max(1.0, float(np.max(np.abs(r))))
+        err = _err(_np(got[k]), r)
+        assert err <= TOL["f32"] * scale, f"{k}: max abs error {err} (scale {scale})"
+    assert abs(float(got["dlam"].item()) - ref["dlam"]) <= TOL["f32"] * max(1.0, abs(ref["dlam"]))
+
+
+def test_v1_backward_is_deterministic_and_chains_to_lambda_vectors():
+    B, H, n, d = 2, 3, 200, 64
+    x = _bwd_inputs(B, H, n, d, True, 77)
+    g = torch.Generator(device="cuda").manual_seed(78)
+    lv = [0.1 * torch.randn(d, generator=g, device="cuda") for _ in range(4)]
+    lin = da.lambda_init(2)
+    lam = da.lambda_reparam(*lv, lin)
+    a = da.diffattn_backward(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], lam, lin, x["dy"], gamma=x["gamma"])
+    b = da.diffattn_backward(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], lam, lin, x["dy"], gamma=x["gamma"])
+    da.device_status()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k  # fixed summation orders: same bits
+    grads = da.lambda_reparam_backward(*lv, a["dlam"])
+    da.device_status()
+    want = oracle.lambda_reparam_backward(*(t.cpu() for t in lv), float(a["dlam"].item()))
+    for gk, wk in zip(grads, want):
+        assert _err(_np(gk), wk) <= 1e-5 * max(1.0, float(np.max(np.abs(wk))))
+
+
+def test_v1_backward_bench_size_sampled():
+    # The workload bench.py times the backward on (B4 H16 n2048 d64, fp32, causal):
+    # dV, dK, dQ of sampled heads against the oracle on those heads.
+    B, H, n, d = 4, 16, 2048, 64
+    x = _bwd_inputs(B, H, n, d, True, 5)
+    lin = da.lambda_init(1)
+    lam = torch.tensor([0.25], device="cuda")
+    got = da.diffattn_backward(x["q1"], x["q2"], x["k1"], x["k2"], x["v"], lam, lin, x["dy"], gamma=x["gamma"])
+    da.device_status()
+    for b, h in ((0, 0), (B - 1, H - 1)):
+        sel = {k: x[k][b:b + 1, :, h:h + 1] for k in ("q1", "q2", "k1", "k2", "v", "dy")}
+        ref = oracle.diff_attn_v1_backward(sel["q1"], sel["q2"], sel["k1"], sel["k2"], sel["v"], 0.25, lin,
+                                           x["gamma"].cpu(), 1e-5, True, sel["dy"])
+        for k in ("dq1", "dq2", "dk1", "dk2", "dv"):
+            r = np.asarray(ref[k])
+            err = _err(_np(got[k][b:b + 1, :, h:h + 1]), r)
+            assert err <= TOL["f32"] * max(1.0, float(np.max(np.abs(r)))), f"({b},{h}) {k}: {err}"
+    for k in ("dq1", "dq2", "dk1", "dk2", "dv", "dgamma", "dlam"):
+        assert bool(torch.isfinite(got[k]).all()), k
