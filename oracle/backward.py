@@ -1,4 +1,4 @@
-"""Plain fp64 CPU oracle for the DIFF V1 backward pass (test infrastructure only).
+"""Plain fp64 CPU oracle for the DIFF V1 and V2 backward passes (test infrastructure only).
 
 TEST INFRASTRUCTURE ONLY, like the rest of ``oracle/``: imported by ``tests/``,
 ``__graft_entry__.smoke()`` and ``bench.py``'s CPU legs, never by the product.
@@ -104,4 +104,55 @@ def lambda_reparam_backward(lq1, lk1, lq2, lk2, dlam: float):
     return dlam * e1 * lk1, dlam * e1 * lq1, -dlam * e2 * lk2, -dlam * e2 * lq2
 
 
-__all__ = ["diff_attn_v1_backward", "lambda_reparam_backward", "DEFAULT_EPS"]
+
+
+def diff_attn_v2_backward(q, k, v, lam_logits, causal: bool, dy, scale=None) -> dict:
+    """Gradients of the DIFF V2 forward (oracle.diff_attn_v2) with respect to q, k, v and the logits.
+
+    q: [B, n, Hq, d]; k, v: [B, n, Hkv, d]; lam_logits, and the returned
+    dlogits: [B, n, Hq/2] (one logit per token and pair); dy: [B, n, Hq/2, d].
+    Per pair g of query heads 2g, 2g + 1 over KV head kv = 2g / (Hq/Hkv), with
+    s = sigmoid(logit) per row, A_e, A_o the two heads' maps:
+
+        out   = A_e V - s * A_o V          (no norm)
+        dV   += A_e^T dy - A_o^T (s * dy)
+        dA_e  = dy V^T,  dA_o = -s * dy V^T
+        dlogit = -s (1 - s) rowsum(dy * A_o V)
+        dS    = A * (dA - rowsum(A * dA)),  dq = c dS K,  dK += c dS^T q
+
+    dK and dV sum over every query head that reads the KV head.  Returns a dict
+    of fp64 arrays dq, dk, dv, dlogits.
+    """
+    q, k, v, dy = (_f64(a) for a in (q, k, v, dy))
+    lg = _f64(lam_logits)
+    B, n, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if Hq % 2 or Hq % Hkv or (Hq // Hkv) % 2:
+        raise ValueError("need Hq even and Hq/Hkv even so each pair shares a KV head")
+    G, group = Hq // 2, Hq // Hkv
+    if lg.shape != (B, n, G) or dy.shape != (B, n, G, d):
+        raise ValueError("need lam_logits [B, n, Hq/2] and dy [B, n, Hq/2, d]")
+    c = 1.0 / math.sqrt(d) if scale is None else scale
+    out = {"dq": np.zeros_like(q), "dk": np.zeros_like(k), "dv": np.zeros_like(v), "dlogits": np.zeros_like(lg)}
+    for b in range(B):
+        for g in range(G):
+            he, ho = 2 * g, 2 * g + 1
+            kv = he // group
+            K, V, dY = k[b, :, kv], v[b, :, kv], dy[b, :, g]
+            s = 1.0 / (1.0 + np.exp(-lg[b, :, g]))[:, None]  # [n, 1]
+            Ae = attention_map(q[b, :, he], K, c, causal)
+            Ao = attention_map(q[b, :, ho], K, c, causal)
+            Oo = Ao @ V
+            out["dv"][b, :, kv] += Ae.T @ dY - Ao.T @ (s * dY)
+            dAe = dY @ V.T
+            dAo = -s * (dY @ V.T)
+            out["dlogits"][b, :, g] = -(s * (1.0 - s))[:, 0] * np.sum(dY * Oo, axis=-1)
+            dSe = Ae * (dAe - np.sum(Ae * dAe, axis=-1, keepdims=True))
+            dSo = Ao * (dAo - np.sum(Ao * dAo, axis=-1, keepdims=True))
+            out["dq"][b, :, he] = c * (dSe @ K)
+            out["dq"][b, :, ho] = c * (dSo @ K)
+            out["dk"][b, :, kv] += c * (dSe.T @ q[b, :, he] + dSo.T @ q[b, :, ho])
+    return out
+
+
+__all__ = ["diff_attn_v1_backward", "diff_attn_v2_backward", "lambda_reparam_backward", "DEFAULT_EPS"]

@@ -170,3 +170,72 @@ def test_mutant_harness_is_faithful(monkeypatch):
     _mutant(monkeypatch, "none")
     for case in CASES:
         test_backward_matches_autograd_of_library_routines(*case)
+
+
+# ------------------------------------------------------------------ DIFF V2
+def _v2_autograd(x, causal):
+    """V2 composed from library routines (SDPA per query head over its KV head), autograd in fp64."""
+    q = torch.tensor(x["q"], requires_grad=True)
+    k = torch.tensor(x["k"], requires_grad=True)
+    v = torch.tensor(x["v"], requires_grad=True)
+    lg = torch.tensor(x["lg"], requires_grad=True)
+    B, n, Hq, d = q.shape
+    group = Hq // k.shape[2]
+    kk = k.repeat_interleave(group, dim=2)  # query head j reads KV head j // group
+    vv = v.repeat_interleave(group, dim=2)
+    a = F.scaled_dot_product_attention(q.permute(0, 2, 1, 3), kk.permute(0, 2, 1, 3), vv.permute(0, 2, 1, 3),
+                                       is_causal=causal).permute(0, 2, 1, 3)
+    y = a[:, :, 0::2] - torch.sigmoid(lg)[..., None] * a[:, :, 1::2]
+    (y * torch.tensor(x["dy"])).sum().backward()
+    return {"dq": q.grad.numpy(), "dk": k.grad.numpy(), "dv": v.grad.numpy(), "dlogits": lg.grad.numpy()}
+
+
+def _v2_case(seed, B=2, n=6, Hq=4, Hkv=2, d=4):
+    r = np.random.default_rng(seed)
+    return {"q": r.normal(size=(B, n, Hq, d)), "k": r.normal(size=(B, n, Hkv, d)), "v": r.normal(size=(B, n, Hkv, d)),
+            "lg": r.normal(size=(B, n, Hq // 2)), "dy": r.normal(size=(B, n, Hq // 2, d))}
+
+
+@pytest.mark.parametrize("Hq,Hkv,causal", [(4, 2, True), (8, 2, True), (4, 1, False), (2, 1, True)])
+def test_v2_backward_matches_autograd(Hq, Hkv, causal):
+    x = _v2_case(20 + Hq + Hkv, Hq=Hq, Hkv=Hkv)
+    got = oracle.diff_attn_v2_backward(x["q"], x["k"], x["v"], x["lg"], causal, x["dy"])
+    want = _v2_autograd(x, causal)
+    for key in ("dq", "dk", "dv", "dlogits"):
+        np.testing.assert_allclose(got[key], want[key], rtol=1e-9, atol=1e-11, err_msg=key)
+
+
+def test_v2_backward_matches_finite_differences():
+    x = _v2_case(31, B=1, n=4, Hq=4, Hkv=1, d=2)
+    got = oracle.diff_attn_v2_backward(x["q"], x["k"], x["v"], x["lg"], True, x["dy"])
+
+    def loss(z):
+        return float(np.sum(oracle.diff_attn_v2(z["q"], z["k"], z["v"], z["lg"], True) * x["dy"]))
+    h = 1e-6
+    for name, gname in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("lg", "dlogits")):
+        fd = np.zeros_like(x[name])
+        for idx in np.ndindex(x[name].shape):
+            zp = {kk: x[kk].copy() for kk in ("q", "k", "v", "lg")}
+            zm = {kk: x[kk].copy() for kk in ("q", "k", "v", "lg")}
+            zp[name][idx] += h
+            zm[name][idx] -= h
+            fd[idx] = (loss(zp) - loss(zm)) / (2 * h)
+        np.testing.assert_allclose(got[gname], fd, rtol=1e-5, atol=1e-7, err_msg=name)
+
+
+def test_v2_backward_pin_catches_unsummed_kv_gradient(monkeypatch):
+    # A plausible mistake: dK / dV of a KV head taken from its last pair only (not summed over the group).
+    real = ob.diff_attn_v2_backward
+
+    def last_pair_only(q, k, v, lam_logits, causal, dy, scale=None):
+        out = real(q, k, v, lam_logits, causal, dy, scale)
+        G, Hkv = np.asarray(lam_logits).shape[2], np.asarray(k).shape[2]
+        if G > Hkv:  # several pairs per KV head: keep one pair's share
+            q1 = np.asarray(q).copy()
+            q1[:, :, :-2] = 0.0
+            one = real(q1, k, v, lam_logits, causal, dy, scale)
+            out["dk"] = one["dk"]
+        return out
+    monkeypatch.setattr(oracle, "diff_attn_v2_backward", last_pair_only)
+    with pytest.raises(AssertionError):
+        test_v2_backward_matches_autograd(8, 2, True)
