@@ -551,38 +551,53 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-BACKWARD_WORKLOADS = [  # (name, B, H, n, d): fp32 DIFF V1 backward, causal
+BACKWARD_WORKLOADS = [  # (name, B, H or (Hq, Hkv), n, d): fp32 DIFF V1 / V2 backward, causal
     ("v1-bwd-f32-B4H16-n2048-d64", 4, 16, 2048, 64),
     ("v1-bwd-f32-B1H1-n128-d64", 1, 1, 128, 64),
+    ("v2-bwd-f32-B2Hq32Hkv16-n2048-d128", 2, (32, 16), 2048, 128),
 ]
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 flops x the SM clock (MHz).
 FP32_LANES = 152 * 128
 
 
 def backward_flops(B, H, n, d):
-    """Algorithmic FLOPs of the backward: per visible (query, key) pair 20 d.
+    """Algorithmic FLOPs of the backward per visible (query, key) pair, causal: n (n + 1) / 2 pairs.
 
-    2 d each for the two score recomputations, 4 d for dO . v (value width 2d),
-    4 d for dV, 2 d each for dQ_1, dQ_2, dK_1, dK_2; causal: n (n + 1) / 2 pairs.
+    V1 (H heads): 20 d a pair: 2 d each for the two score recomputations, 4 d for
+    dO . v (value width 2d), 4 d for dV, 2 d each for dQ_1, dQ_2, dK_1, dK_2.
+    V2 (H = (Hq, Hkv), Hq / 2 head pairs): 16 d a pair and head pair: the same
+    terms with a value width of d.
     """
-    return B * H * (n * (n + 1) // 2) * 20 * d
+    pairs = n * (n + 1) // 2
+    if isinstance(H, tuple):
+        return B * (H[0] // 2) * pairs * 16 * d
+    return B * H * pairs * 20 * d
 
 
 def time_backward(da, flush, B, H, n, d, runs=10):
-    """fp32 DIFF V1 backward (4 kernels): median CUDA-event time, L2 flushed."""
+    """fp32 DIFF V1 / V2 backward (4 kernels): median CUDA-event time, L2 flushed."""
     import torch
     g = torch.Generator(device="cuda").manual_seed(3000 + n + d)
 
     def rnd(*shape):
         return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32)
-    q1, q2, k1, k2 = (rnd(B, n, H, d) for _ in range(4))
-    v, dy = rnd(B, n, H, 2 * d), rnd(B, n, H, 2 * d)
-    gamma = torch.ones(2 * d, device="cuda")
-    lam = torch.tensor([0.3], device="cuda")
-    ws = torch.empty(da.backward_workspace_bytes(B, H, n, d), dtype=torch.uint8, device="cuda")
+    if isinstance(H, tuple):  # DIFF V2: (Hq, Hkv), one logit per pair
+        Hq, Hkv = H
+        q, k, v, dy = rnd(B, n, Hq, d), rnd(B, n, Hkv, d), rnd(B, n, Hkv, d), rnd(B, n, Hq // 2, d)
+        lg = rnd(Hq // 2)
+        ws = torch.empty(da.v2_backward_workspace_bytes(B, Hq, n, d), dtype=torch.uint8, device="cuda")
 
-    def call():
-        da.diffattn_backward(q1, q2, k1, k2, v, lam, 0.2, dy, gamma=gamma, workspace=ws)
+        def call():
+            da.diffattn_v2_backward(q, k, v, lg, dy, workspace=ws)
+    else:
+        q1, q2, k1, k2 = (rnd(B, n, H, d) for _ in range(4))
+        v, dy = rnd(B, n, H, 2 * d), rnd(B, n, H, 2 * d)
+        gamma = torch.ones(2 * d, device="cuda")
+        lam = torch.tensor([0.3], device="cuda")
+        ws = torch.empty(da.backward_workspace_bytes(B, H, n, d), dtype=torch.uint8, device="cuda")
+
+        def call():
+            da.diffattn_backward(q1, q2, k1, k2, v, lam, 0.2, dy, gamma=gamma, workspace=ws)
     for _ in range(3):
         call()
     da.device_status()

@@ -78,6 +78,11 @@ def lib() -> ctypes.CDLL:
             L.diffattn_backward.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, f, vp, f, i, vp, vp, vp, vp, vp,
                                             vp, vp, vp, vp, ctypes.c_size_t, vp]
             L.diffattn_backward.restype = i
+            L.diffattn_v2_backward_workspace.argtypes = [i, i, i, i]
+            L.diffattn_v2_backward_workspace.restype = ctypes.c_size_t
+            L.diffattn_v2_backward.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, ll, ll, f, i, vp, vp, vp, vp, vp,
+                                               vp, ctypes.c_size_t, vp]
+            L.diffattn_v2_backward.restype = i
             L.lambda_reparam_backward.argtypes = [vp, vp, vp, vp, i, vp, vp, vp, vp, vp, vp]
             L.lambda_reparam_backward.restype = i
             L.diffattn_v2_forward.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, ll, ll, f, i, vp, vp]
@@ -400,6 +405,47 @@ def diffattn_backward(q1, q2, k1, k2, v, lam, lambda_init_value: float, dy, gamm
                                    float(lambda_init_value), _ptr(gamma), float(eps), 1 if causal else 0, _ptr(dy),
                                    _ptr(g["dq1"]), _ptr(g["dq2"]), _ptr(g["dk1"]), _ptr(g["dk2"]), _ptr(g["dv"]),
                                    _ptr(g["dlam"]), _ptr(g["dgamma"]), wp, wn, _stream(stream)))
+    return g
+
+
+def v2_backward_workspace_bytes(B: int, Hq: int, n: int, d: int) -> int:
+    return int(lib().diffattn_v2_backward_workspace(B, Hq, n, d))
+
+
+def diffattn_v2_backward(q, k, v, lam_logits, dy, causal: bool = True, softmax_scale: float = 0.0,
+                         workspace=None, stream=None) -> dict:
+    """DIFF V2 backward (fp32): gradients of diffattn_v2_forward's output given dy.
+
+    q: [B, n, Hq, d]; k, v: [B, n, Hkv, d]; dy: [B, n, Hq/2, d]; lam_logits:
+    fp32 [B, n, Hq/2] (per token), [B, Hq/2] (per sequence) or [Hq/2] (per
+    pair).  Returns a dict: dq, dk, dv and dlogits (shaped like lam_logits).
+    """
+    B, n, Hq, d = q.shape
+    Hkv = k.shape[2]
+    dt = torch.float32
+    _need(q, "q", dt, (B, n, Hq, d))
+    _need(k, "k", dt, (B, n, Hkv, d))
+    _need(v, "v", dt, (B, n, Hkv, d))
+    _need(dy, "dy", dt, (B, n, Hq // 2, d))
+    G = Hq // 2
+    if lam_logits.dim() == 3:
+        _need(lam_logits, "lam_logits", dt, (B, n, G))
+        sb, st = n * G, G
+    elif lam_logits.dim() == 2:
+        _need(lam_logits, "lam_logits", dt, (B, G))
+        sb, st = G, 0
+    else:
+        _need(lam_logits, "lam_logits", dt, (G,))
+        sb, st = 0, 0
+    need = v2_backward_workspace_bytes(B, Hq, n, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    wp, wn = _ws_args(workspace, need)
+    g = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+         "dlogits": torch.empty_like(lam_logits)}
+    _check(lib().diffattn_v2_backward(F32, B, Hq, Hkv, n, d, _ptr(q), _ptr(k), _ptr(v), _ptr(lam_logits), sb, st,
+                                      float(softmax_scale), 1 if causal else 0, _ptr(dy), _ptr(g["dq"]),
+                                      _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dlogits"]), wp, wn, _stream(stream)))
     return g
 
 

@@ -696,6 +696,7 @@ diffattn_status diffattn_v2_forward(diffattn_dtype dt, int B, int Hq, int Hkv, i
 
 // ---- backward (fp32, V1)
 static size_t bwd_rows(int B, int H, int n) { return static_cast<size_t>(B) * H * n; }
+constexpr size_t kBwdRowSlots = 6;  // per row: lse_1, lse_2, D_1, D_2, dlambda / dlogit share, coefficient
 static size_t bwd_row_ctas(int B, int H, int n) {
   return static_cast<size_t>(B) * H * ((static_cast<size_t>(n) + da::kSimtRows - 1) / da::kSimtRows);
 }
@@ -703,7 +704,7 @@ static size_t bwd_row_ctas(int B, int H, int n) {
 size_t diffattn_backward_workspace(int B, int H, int n, int d) {
   if (B < 0 || H < 0 || n < 0 || d < 1) return 0;
   const size_t R = bwd_rows(B, H, n), dv = 2 * static_cast<size_t>(d);
-  return round256(R * dv * 4) + round256(5 * R * 4) + round256(bwd_row_ctas(B, H, n) * dv * 4);
+  return round256(R * dv * 4) + round256(kBwdRowSlots * R * 4) + round256(bwd_row_ctas(B, H, n) * dv * 4);
 }
 
 diffattn_status diffattn_backward(diffattn_dtype dt, int B, int H, int n, int d, const void* q1, const void* q2,
@@ -742,7 +743,7 @@ diffattn_status diffattn_backward(diffattn_dtype dt, int B, int H, int n, int d,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* ws_do = reinterpret_cast<float*>(ws);
   float* ws_row = reinterpret_cast<float*>(ws + round256(R * dvw * 4));
-  float* ws_dg = reinterpret_cast<float*>(ws + round256(R * dvw * 4) + round256(5 * R * 4));
+  float* ws_dg = reinterpret_cast<float*>(ws + round256(R * dvw * 4) + round256(kBwdRowSlots * R * 4));
 
   da::SimtParams rp{};
   rp.q1 = static_cast<const float*>(q1);
@@ -788,17 +789,121 @@ diffattn_status diffattn_backward(diffattn_dtype dt, int B, int H, int n, int d,
   p.dgamma = dgamma;
   p.scale = rp.scale;
   p.B = B;
-  p.H = H;
   p.n = n;
   p.d = d;
   p.dvw = dvw;
   p.causal = rp.causal;
+  p.v2 = 0;
+  p.heads_q = p.heads_kv = p.units = H;
+  p.group = 1;
   p.rows = static_cast<long long>(R);
   p.n_row_ctas = static_cast<int>(bwd_row_ctas(B, H, n));
   cudaError_t e = da::launch_simt_bwd_rows(rp, s);
   if (e == cudaSuccess) e = da::launch_backward_f32(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_backward launch");
   g_launches.fetch_add(4);
+  return ok();
+}
+
+size_t diffattn_v2_backward_workspace(int B, int Hq, int n, int d) {
+  if (B < 0 || Hq < 0 || n < 0 || d < 1) return 0;
+  const size_t R = bwd_rows(B, Hq / 2, n);
+  return round256(R * static_cast<size_t>(d) * 4) + round256(kBwdRowSlots * R * 4);
+}
+
+diffattn_status diffattn_v2_backward(diffattn_dtype dt, int B, int Hq, int Hkv, int n, int d, const void* q,
+                                     const void* k, const void* v, const float* lam_logits, long long sb,
+                                     long long st, float softmax_scale, int causal, const void* dy, void* dq,
+                                     void* dk, void* dv, float* dlogits, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  if (dt != DIFFATTN_F32 && dt != DIFFATTN_BF16)
+    return fail(DIFFATTN_ERR_DTYPE, "diffattn_v2_backward: bad dtype %d", (int)dt);
+  if (B < 0 || Hq < 0 || Hkv < 1 || n < 0 || d < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_backward: bad sizes B=%d Hq=%d Hkv=%d n=%d d=%d", B, Hq, Hkv, n, d);
+  if (Hq % 2 != 0 || Hq % Hkv != 0 || (Hq / Hkv) % 2 != 0)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_backward: need Hq even, Hq %% Hkv == 0 and Hq/Hkv even");
+  if (sb < 0 || st < 0) return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_backward: negative logit stride");
+  if (dt != DIFFATTN_F32 || d > da::kSimtMaxD)
+    return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_v2_backward: f32 with d <= 128 only (got dtype %d, d=%d)",
+                (int)dt, d);
+  const int G = Hq / 2;
+  const bool dense = st == G && sb == static_cast<long long>(n) * G;  // one logit per token and pair
+  if (!dense && !(st == 0 && (sb == 0 || sb == G)))
+    return fail(DIFFATTN_ERR_UNSUPPORTED,
+                "diffattn_v2_backward: logit strides (sb, st) must be (n*Hq/2, Hq/2), (Hq/2, 0) or (0, 0)");
+  if (B == 0 || Hq == 0 || n == 0) return ok();
+  if (!q || !k || !v || !lam_logits || !dy || !dq || !dk || !dv || !dlogits || !workspace)
+    return fail(DIFFATTN_ERR_NULL, "diffattn_v2_backward: NULL pointer");
+  const size_t need = diffattn_v2_backward_workspace(B, Hq, n, d);
+  if (workspace_bytes < need)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_backward: workspace of %zu bytes, need %zu", workspace_bytes,
+                need);
+  if (!aligned16(workspace))
+    return fail(DIFFATTN_ERR_ALIGN, "diffattn_v2_backward: workspace must be 16-byte aligned");
+  const long long nqb8 = (static_cast<long long>(n) + da::kSimtRows - 1) / da::kSimtRows;
+  if (static_cast<long long>(B) * G * nqb8 > 0x7fffffffll)
+    return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_backward: too many (batch, pair, row block) units");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t R = bwd_rows(B, G, n);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* ws_do = reinterpret_cast<float*>(ws);
+  float* ws_row = reinterpret_cast<float*>(ws + round256(R * d * 4));
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.f / std::sqrt(static_cast<float>(d));
+
+  da::SimtParams rp{};
+  rp.q1 = rp.q2 = static_cast<const float*>(q);
+  rp.k1 = rp.k2 = static_cast<const float*>(k);
+  rp.v = static_cast<const float*>(v);
+  rp.lam_logits = lam_logits;
+  rp.sb = sb;
+  rp.st = st;
+  rp.scale = scale;
+  rp.norm_mult = 1.f;
+  rp.eps = 1e-5f;
+  rp.B = B;
+  rp.n = n;
+  rp.d = d;
+  rp.dv = d;
+  rp.causal = causal ? 1 : 0;
+  rp.v2 = 1;
+  rp.heads_q = Hq;
+  rp.heads_kv = Hkv;
+  rp.units_per_batch = G;
+  rp.group = Hq / Hkv;
+  rp.rows_total = static_cast<long long>(R);
+  rp.dy = static_cast<const float*>(dy);
+  rp.ws_do = ws_do;
+  rp.ws_row = ws_row;
+  rp.dlogits_dense = dense ? dlogits : nullptr;
+
+  da::BwdParams p{};
+  p.q1 = p.q2 = rp.q1;
+  p.k1 = p.k2 = rp.k1;
+  p.v = rp.v;
+  p.dO = ws_do;
+  p.row = ws_row;
+  p.dq1 = p.dq2 = static_cast<float*>(dq);
+  p.dk1 = p.dk2 = static_cast<float*>(dk);
+  p.dv = static_cast<float*>(dv);
+  p.dlogits = dlogits;
+  p.sb = sb;
+  p.scale = scale;
+  p.B = B;
+  p.n = n;
+  p.d = d;
+  p.dvw = d;
+  p.causal = rp.causal;
+  p.v2 = 1;
+  p.heads_q = Hq;
+  p.heads_kv = Hkv;
+  p.units = G;
+  p.group = Hq / Hkv;
+  p.rows = static_cast<long long>(R);
+  p.n_logit_outs = dense ? 0 : (sb == 0 ? G : B * G);
+  cudaError_t e = da::launch_simt_bwd_rows(rp, s);
+  if (e == cudaSuccess) e = da::launch_backward_f32(p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_backward launch");
+  g_launches.fetch_add(dense ? 3 : 4);
   return ok();
 }
 

@@ -1,4 +1,4 @@
-// fp32 backward pass of the multi-head DIFF V1 forward on CUDA cores.
+// fp32 backward passes of the multi-head DIFF V1 and V2 forwards on CUDA cores.
 //
 // The forward (per batch b, head h; c = 1/sqrt d; causal or not):
 //   A_r = softmax(c Q_r K_r^T),  O = (A_1 - lambda A_2) V,
@@ -14,6 +14,11 @@
 //   dlambda = -sum dO . A_2 V,  dgamma = sum (1 - lambda_init) (O / rms(O)) dy,
 // with D_r = rowsum(A_r dA_r) from the row pass.  The maps are recomputed
 // from the row pass's log-sum-exps, a 32 x 32 block at a time, never stored.
+// DIFF V2 (DIFF V2 analysis page, "2. 커스텀 커널 제거" and "GQA와의 호환성"):
+// map 1 / map 2 are query heads 2g / 2g + 1 over their shared KV head, the
+// coefficient is the row's s = sigmoid(logit) instead of lambda, there is no
+// norm (dO = dy), dK and dV sum over every pair of the KV head's group, and
+// dlogit = -s (1 - s) dO . A_2 V.
 //
 //   bwd_dkdv_kernel: one CTA per (b, h, 32 keys); sweeps the query blocks that
 //     see those keys; dV, dK_1, dK_2 of its keys in registers.
@@ -39,9 +44,9 @@ constexpr int kBwdMaxCV = 32;  // value channels a thread accumulates (dv <= 256
 constexpr int kBwdMaxCK = 16;  // key/query channels a thread accumulates (d <= 128)
 
 // Shared-memory floats of both sweeps: K_1, K_2, V, Q_1, Q_2, dO tiles, three
-// 32 x 33 blocks (P, dS_1, dS_2) and the four row statistics.
+// 32 x 33 blocks (P, dS_1, dS_2) and five row statistics.
 __host__ __device__ constexpr int bwd_smem_floats(int d, int dv) {
-  return 4 * kBwdBlk * (d + 1) + 2 * kBwdBlk * (dv + 1) + 3 * kBwdBlk * (kBwdBlk + 1) + 4 * kBwdBlk;
+  return 4 * kBwdBlk * (d + 1) + 2 * kBwdBlk * (dv + 1) + 3 * kBwdBlk * (kBwdBlk + 1) + 5 * kBwdBlk;
 }
 
 struct BwdSmem {
@@ -57,60 +62,67 @@ struct BwdSmem {
     P = dO + kBwdBlk * dvp;
     S1 = P + kBwdBlk * (kBwdBlk + 1);
     S2 = S1 + kBwdBlk * (kBwdBlk + 1);
-    st = S2 + kBwdBlk * (kBwdBlk + 1);  // [4][32]: lse_1, lse_2, D_1, D_2 of the query block
+    st = S2 + kBwdBlk * (kBwdBlk + 1);  // [5][32]: lse_1, lse_2, D_1, D_2, coefficient of the query block
   }
 };
 
-// Stages the query block [q0, q0 + 32) of unit (b, h): Q_1, Q_2, dO rows and statistics.
-__device__ __forceinline__ void bwd_stage_queries(const BwdParams& p, const BwdSmem& s, int b, int h, int q0,
-                                                  bool vec) {
+// Stages the query block [q0, q0 + 32) of row unit `unit` (V1: (b, h); V2: (b, pair)):
+// Q_1 (head hq1), Q_2 (head hq2), dO rows and the statistics.
+__device__ __forceinline__ void bwd_stage_queries(const BwdParams& p, const BwdSmem& s, int b, int hq1, int hq2,
+                                                  long long unit, int q0, bool vec) {
   const int d = p.d, dv = p.dvw;
-  const size_t qrow = static_cast<size_t>(p.H) * d;
-  const long long unit_row0 = (static_cast<long long>(b) * p.H + h) * p.n;
-  stage_rows(s.q1, d + 1, p.q1 + static_cast<size_t>(b) * p.n * qrow + static_cast<size_t>(h) * d, qrow, q0, p.n,
-             d, kBwdBlk, vec);
-  stage_rows(s.q2, d + 1, p.q2 + static_cast<size_t>(b) * p.n * qrow + static_cast<size_t>(h) * d, qrow, q0, p.n,
-             d, kBwdBlk, vec);
+  const size_t qrow = static_cast<size_t>(p.heads_q) * d;
+  const float* qb = p.q1 + static_cast<size_t>(b) * p.n * qrow;
+  const long long unit_row0 = unit * p.n;
+  stage_rows(s.q1, d + 1, qb + static_cast<size_t>(hq1) * d, qrow, q0, p.n, d, kBwdBlk, vec);
+  stage_rows(s.q2, d + 1, (p.q2 + static_cast<size_t>(b) * p.n * qrow) + static_cast<size_t>(hq2) * d, qrow, q0,
+             p.n, d, kBwdBlk, vec);
   stage_rows(s.dO, dv + 1, p.dO + unit_row0 * dv, dv, q0, p.n, dv, kBwdBlk, (dv & 3) == 0);
-  if (threadIdx.x < 4 * kBwdBlk) {
+  if (threadIdx.x < 5 * kBwdBlk) {
     const int k = threadIdx.x / kBwdBlk, i = threadIdx.x % kBwdBlk;
-    s.st[threadIdx.x] = (q0 + i < p.n) ? p.row[k * p.rows + unit_row0 + q0 + i] : 0.f;
+    const int slot = k < 4 ? k : 5;  // lse_1, lse_2, D_1, D_2, coefficient
+    s.st[threadIdx.x] = (q0 + i < p.n) ? p.row[slot * p.rows + unit_row0 + q0 + i] : 0.f;
   }
 }
 
-// Stages the key block [k0, k0 + 32) of unit (b, h): K_1, K_2, V rows.
-__device__ __forceinline__ void bwd_stage_keys(const BwdParams& p, const BwdSmem& s, int b, int h, int k0, bool vec) {
+// Stages the key block [k0, k0 + 32) of KV head hk: K_1, K_2 (V1 only; V2 reads K_1 twice), V rows.
+__device__ __forceinline__ void bwd_stage_keys(const BwdParams& p, const BwdSmem& s, int b, int hk, int k0,
+                                               bool vec) {
   const int d = p.d, dv = p.dvw;
-  const size_t krow = static_cast<size_t>(p.H) * d, vrow = static_cast<size_t>(p.H) * dv;
-  stage_rows(s.k1, d + 1, p.k1 + static_cast<size_t>(b) * p.n * krow + static_cast<size_t>(h) * d, krow, k0, p.n,
+  const size_t krow = static_cast<size_t>(p.heads_kv) * d, vrow = static_cast<size_t>(p.heads_kv) * dv;
+  stage_rows(s.k1, d + 1, p.k1 + static_cast<size_t>(b) * p.n * krow + static_cast<size_t>(hk) * d, krow, k0, p.n,
              d, kBwdBlk, vec);
-  stage_rows(s.k2, d + 1, p.k2 + static_cast<size_t>(b) * p.n * krow + static_cast<size_t>(h) * d, krow, k0, p.n,
-             d, kBwdBlk, vec);
-  stage_rows(s.v, dv + 1, p.v + static_cast<size_t>(b) * p.n * vrow + static_cast<size_t>(h) * dv, vrow, k0, p.n,
+  if (!p.v2)
+    stage_rows(s.k2, d + 1, p.k2 + static_cast<size_t>(b) * p.n * krow + static_cast<size_t>(hk) * d, krow, k0,
+               p.n, d, kBwdBlk, vec);
+  stage_rows(s.v, dv + 1, p.v + static_cast<size_t>(b) * p.n * vrow + static_cast<size_t>(hk) * dv, vrow, k0, p.n,
              dv, kBwdBlk, vec);
 }
 
-// The 32 x 32 block step: P = A_1 - lambda A_2, dS_1, dS_2 for queries
+// The 32 x 32 block step: P = A_1 - coef A_2, dS_1, dS_2 for queries
 // [q0, q0 + 32) and keys [k0, k0 + 32) into shared memory (0 where masked).
+// coef is lambda (V1) or the row's sigmoid(logit) (V2).
 __device__ __forceinline__ void bwd_block_step(const BwdParams& p, const BwdSmem& s, int q0, int k0, float lam) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = p.d, dv = p.dvw, dp = d + 1, dvp = dv + 1;
   const int key = k0 + lane;
+  const float* k2s = p.v2 ? s.k1 : s.k2;
 #pragma unroll
   for (int r = 0; r < kBwdBlk / (kBwdThreads / 32); ++r) {
     const int i = warp * (kBwdBlk / (kBwdThreads / 32)) + r, t = q0 + i;
     const bool valid = t < p.n && key < p.n && (!p.causal || key <= t);
+    const float coef = p.v2 ? s.st[4 * kBwdBlk + i] : lam;
     float s1 = 0.f, s2 = 0.f, dpv = 0.f;
     for (int e = 0; e < d; ++e) {
       s1 = fmaf(s.q1[i * dp + e], s.k1[lane * dp + e], s1);
-      s2 = fmaf(s.q2[i * dp + e], s.k2[lane * dp + e], s2);
+      s2 = fmaf(s.q2[i * dp + e], k2s[lane * dp + e], s2);
     }
     for (int c = 0; c < dv; ++c) dpv = fmaf(s.dO[i * dvp + c], s.v[lane * dvp + c], dpv);
     const float p1 = valid ? expf(s1 * p.scale - s.st[i]) : 0.f;
     const float p2 = valid ? expf(s2 * p.scale - s.st[kBwdBlk + i]) : 0.f;
-    s.P[i * (kBwdBlk + 1) + lane] = p1 - lam * p2;
+    s.P[i * (kBwdBlk + 1) + lane] = p1 - coef * p2;
     s.S1[i * (kBwdBlk + 1) + lane] = p1 * (dpv - s.st[2 * kBwdBlk + i]);
-    s.S2[i * (kBwdBlk + 1) + lane] = p2 * (-lam * dpv - s.st[3 * kBwdBlk + i]);
+    s.S2[i * (kBwdBlk + 1) + lane] = p2 * (-coef * dpv - s.st[3 * kBwdBlk + i]);
   }
 }
 
@@ -120,54 +132,62 @@ __device__ __forceinline__ bool bwd_vec(const BwdParams& p) {
                                reinterpret_cast<uintptr_t>(p.v)) & 15u) == 0;
 }
 
-// dV, dK_1, dK_2 of 32 keys: thread (warp w, lane j) owns key k0 + j and the
-// channel slices w * cv .. w * cv + cv - 1 (value) and w * ck .. (key).
+// dV, dK_1, dK_2 of 32 keys of one KV head (V1: head h; V2: KV head, over
+// every head pair of its group): thread (warp w, lane j) owns key k0 + j and
+// the channel slices w * cv .. w * cv + cv - 1 (value) and w * ck .. (key).
 __global__ void __launch_bounds__(kBwdThreads) bwd_dkdv_kernel(const BwdParams p) {
   extern __shared__ float sm[];
   const BwdSmem s(sm, p.d, p.dvw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nblk = (p.n + kBwdBlk - 1) / kBwdBlk;
-  const int kb = blockIdx.x % nblk, unit = blockIdx.x / nblk;
-  const int b = unit / p.H, h = unit % p.H, k0 = kb * kBwdBlk;
+  const int kb = blockIdx.x % nblk, kvu = blockIdx.x / nblk;
+  const int b = kvu / p.heads_kv, hk = kvu % p.heads_kv, k0 = kb * kBwdBlk;
   const int d = p.d, dv = p.dvw, dp = d + 1, dvp = dv + 1;
   const int cv = (dv + 7) / 8, ck = (d + 7) / 8;
   const bool vec = bwd_vec(p);
-  const float lam = *p.lambda;
-  bwd_stage_keys(p, s, b, h, k0, vec);
+  const float lam = p.v2 ? 0.f : *p.lambda;
+  // Query-head pairs reading this KV head: V1 the head itself; V2 pairs
+  // hk * group / 2 .. (hk + 1) * group / 2 - 1.
+  const int g0 = p.v2 ? hk * (p.group / 2) : hk, g1 = p.v2 ? g0 + p.group / 2 : hk + 1;
+  bwd_stage_keys(p, s, b, hk, k0, vec);
   float av[kBwdMaxCV], a1[kBwdMaxCK], a2[kBwdMaxCK];
 #pragma unroll
   for (int k = 0; k < kBwdMaxCV; ++k) av[k] = 0.f;
 #pragma unroll
   for (int k = 0; k < kBwdMaxCK; ++k) a1[k] = a2[k] = 0.f;
-  for (int qb = p.causal ? kb : 0; qb < nblk; ++qb) {
-    const int q0 = qb * kBwdBlk;
-    __syncthreads();  // the previous block's reads are done
-    bwd_stage_queries(p, s, b, h, q0, vec);
-    __syncthreads();
-    bwd_block_step(p, s, q0, k0, lam);
-    __syncthreads();
-    for (int i = 0; i < kBwdBlk; ++i) {
-      const float w = s.P[i * (kBwdBlk + 1) + lane];
-      const float g1 = s.S1[i * (kBwdBlk + 1) + lane];
-      const float g2 = s.S2[i * (kBwdBlk + 1) + lane];
+  for (int g = g0; g < g1; ++g) {
+    const int hq1 = p.v2 ? 2 * g : g, hq2 = p.v2 ? 2 * g + 1 : g;
+    const long long unit = static_cast<long long>(b) * p.units + g;
+    for (int qb = p.causal ? kb : 0; qb < nblk; ++qb) {
+      const int q0 = qb * kBwdBlk;
+      __syncthreads();  // the previous block's reads are done
+      bwd_stage_queries(p, s, b, hq1, hq2, unit, q0, vec);
+      __syncthreads();
+      bwd_block_step(p, s, q0, k0, lam);
+      __syncthreads();
+      for (int i = 0; i < kBwdBlk; ++i) {
+        const float w = s.P[i * (kBwdBlk + 1) + lane];
+        const float e1 = s.S1[i * (kBwdBlk + 1) + lane];
+        const float e2 = s.S2[i * (kBwdBlk + 1) + lane];
 #pragma unroll
-      for (int k = 0; k < kBwdMaxCV; ++k) {
-        const int c = warp * cv + k;
-        if (k < cv && c < dv) av[k] = fmaf(w, s.dO[i * dvp + c], av[k]);
-      }
+        for (int k = 0; k < kBwdMaxCV; ++k) {
+          const int c = warp * cv + k;
+          if (k < cv && c < dv) av[k] = fmaf(w, s.dO[i * dvp + c], av[k]);
+        }
 #pragma unroll
-      for (int k = 0; k < kBwdMaxCK; ++k) {
-        const int c = warp * ck + k;
-        if (k < ck && c < d) {
-          a1[k] = fmaf(g1, s.q1[i * dp + c], a1[k]);
-          a2[k] = fmaf(g2, s.q2[i * dp + c], a2[k]);
+        for (int k = 0; k < kBwdMaxCK; ++k) {
+          const int c = warp * ck + k;
+          if (k < ck && c < d) {
+            a1[k] = fmaf(e1, s.q1[i * dp + c], a1[k]);
+            a2[k] = fmaf(e2, s.q2[i * dp + c], a2[k]);
+          }
         }
       }
     }
   }
   const int key = k0 + lane;
   if (key < p.n) {
-    const size_t kr = (static_cast<size_t>(b) * p.n + key) * p.H + h;
+    const size_t kr = (static_cast<size_t>(b) * p.n + key) * p.heads_kv + hk;
 #pragma unroll
     for (int k = 0; k < kBwdMaxCV; ++k) {
       const int c = warp * cv + k;
@@ -177,15 +197,20 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dkdv_kernel(const BwdParams p
     for (int k = 0; k < kBwdMaxCK; ++k) {
       const int c = warp * ck + k;
       if (k < ck && c < d) {
-        p.dk1[kr * d + c] = p.scale * a1[k];
-        p.dk2[kr * d + c] = p.scale * a2[k];
+        if (p.v2) {
+          p.dk1[kr * d + c] = p.scale * (a1[k] + a2[k]);  // both query heads read this key
+        } else {
+          p.dk1[kr * d + c] = p.scale * a1[k];
+          p.dk2[kr * d + c] = p.scale * a2[k];
+        }
       }
     }
   }
 }
 
-// dQ_1, dQ_2 of 32 queries: thread (warp w, lane i) owns query q0 + i and the
-// channel slice w * ck .. w * ck + ck - 1.
+// dQ_1, dQ_2 of 32 queries of one row unit (V1: head h; V2: the pair's two
+// query heads): thread (warp w, lane i) owns query q0 + i and the channel
+// slice w * ck .. w * ck + ck - 1.
 __global__ void __launch_bounds__(kBwdThreads) bwd_dq_kernel(const BwdParams p) {
   extern __shared__ float sm[];
   const BwdSmem s(sm, p.d, p.dvw);
@@ -193,12 +218,15 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dq_kernel(const BwdParams p) 
   const int nblk = (p.n + kBwdBlk - 1) / kBwdBlk;
   const int qb = nblk - 1 - blockIdx.x % nblk;  // heaviest causal blocks first
   const int unit = blockIdx.x / nblk;
-  const int b = unit / p.H, h = unit % p.H, q0 = qb * kBwdBlk;
+  const int b = unit / p.units, g = unit % p.units, q0 = qb * kBwdBlk;
+  const int hq1 = p.v2 ? 2 * g : g, hq2 = p.v2 ? 2 * g + 1 : g;
+  const int hk = p.v2 ? (2 * g) / p.group : g;
   const int d = p.d, dp = d + 1;
   const int ck = (d + 7) / 8;
   const bool vec = bwd_vec(p);
-  const float lam = *p.lambda;
-  bwd_stage_queries(p, s, b, h, q0, vec);
+  const float lam = p.v2 ? 0.f : *p.lambda;
+  const float* k2s = p.v2 ? s.k1 : s.k2;
+  bwd_stage_queries(p, s, b, hq1, hq2, unit, q0, vec);
   float a1[kBwdMaxCK], a2[kBwdMaxCK];
 #pragma unroll
   for (int k = 0; k < kBwdMaxCK; ++k) a1[k] = a2[k] = 0.f;
@@ -206,56 +234,73 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dq_kernel(const BwdParams p) 
   for (int kb = 0; kb <= kb_end; ++kb) {
     const int k0 = kb * kBwdBlk;
     __syncthreads();  // the previous block's reads are done
-    bwd_stage_keys(p, s, b, h, k0, vec);
+    bwd_stage_keys(p, s, b, hk, k0, vec);
     __syncthreads();
     bwd_block_step(p, s, q0, k0, lam);
     __syncthreads();
     for (int j = 0; j < kBwdBlk; ++j) {
-      const float g1 = s.S1[lane * (kBwdBlk + 1) + j];
-      const float g2 = s.S2[lane * (kBwdBlk + 1) + j];
+      const float e1 = s.S1[lane * (kBwdBlk + 1) + j];
+      const float e2 = s.S2[lane * (kBwdBlk + 1) + j];
 #pragma unroll
       for (int k = 0; k < kBwdMaxCK; ++k) {
         const int c = warp * ck + k;
         if (k < ck && c < d) {
-          a1[k] = fmaf(g1, s.k1[j * dp + c], a1[k]);
-          a2[k] = fmaf(g2, s.k2[j * dp + c], a2[k]);
+          a1[k] = fmaf(e1, s.k1[j * dp + c], a1[k]);
+          a2[k] = fmaf(e2, k2s[j * dp + c], a2[k]);
         }
       }
     }
   }
   const int t = q0 + lane;
   if (t < p.n) {
-    const size_t qr = (static_cast<size_t>(b) * p.n + t) * p.H + h;
+    const size_t qr = (static_cast<size_t>(b) * p.n + t) * p.heads_q;
 #pragma unroll
     for (int k = 0; k < kBwdMaxCK; ++k) {
       const int c = warp * ck + k;
       if (k < ck && c < d) {
-        p.dq1[qr * d + c] = p.scale * a1[k];
-        p.dq2[qr * d + c] = p.scale * a2[k];
+        p.dq1[(qr + hq1) * d + c] = p.scale * a1[k];
+        p.dq2[(qr + hq2) * d + c] = p.scale * a2[k];
       }
     }
   }
 }
 
-// dlambda = sum of the rows' shares, dgamma[c] = sum of the CTAs' shares, one
-// CTA, fixed summation order.
+// Fixed-order reductions of the row pass's shares.  V1 (one CTA): dlambda =
+// sum of every row's share, dgamma[c] = sum of the CTAs' shares.  V2 (one CTA
+// per output, logits shared by a sequence's tokens): dlogit of (b, pair) =
+// sum over the tokens (and over the sequences when sb = 0) of the rows' shares.
 __global__ void __launch_bounds__(kBwdThreads) bwd_reduce_kernel(const BwdParams p) {
   __shared__ float red[kBwdThreads];
-  float a = 0.f;
   const float* share = p.row + 4 * p.rows;
-  for (long long r = threadIdx.x; r < p.rows; r += kBwdThreads) a += share[r];
+  float a = 0.f;
+  int g = 0, b0 = 0, b1 = 0;
+  if (p.v2) {
+    g = p.sb == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) % p.units;
+    b0 = p.sb == 0 ? 0 : static_cast<int>(blockIdx.x) / p.units;
+    b1 = p.sb == 0 ? p.B : b0 + 1;
+    for (int b = b0; b < b1; ++b) {
+      const float* sr = share + (static_cast<long long>(b) * p.units + g) * p.n;
+      for (int t = threadIdx.x; t < p.n; t += kBwdThreads) a += sr[t];
+    }
+  } else {
+    for (long long r = threadIdx.x; r < p.rows; r += kBwdThreads) a += share[r];
+  }
   red[threadIdx.x] = a;
   __syncthreads();
   for (int w = kBwdThreads / 2; w > 0; w >>= 1) {
     if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
     __syncthreads();
   }
+  if (p.v2) {
+    if (threadIdx.x == 0) p.dlogits[static_cast<long long>(b0) * p.sb + g] = red[0];
+    return;
+  }
   if (threadIdx.x == 0) *p.dlambda = red[0];
   if (p.dgamma != nullptr) {
     for (int c = threadIdx.x; c < p.dvw; c += kBwdThreads) {
-      float g = 0.f;
-      for (int k = 0; k < p.n_row_ctas; ++k) g += p.dgp[static_cast<size_t>(k) * p.dvw + c];
-      p.dgamma[c] = g;
+      float s2 = 0.f;
+      for (int k = 0; k < p.n_row_ctas; ++k) s2 += p.dgp[static_cast<size_t>(k) * p.dvw + c];
+      p.dgamma[c] = s2;
     }
   }
 }

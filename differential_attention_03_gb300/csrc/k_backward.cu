@@ -10,15 +10,16 @@ static_assert(kBwdThreads == kSimtWarps * 32, "stage_rows assumes the SIMT CTA s
 cudaError_t launch_backward_f32(const BwdParams& p, cudaStream_t s) {
   cudaError_t e;
   const long long nblk = (p.n + kBwdBlk - 1) / kBwdBlk;
-  const unsigned grid = static_cast<unsigned>(nblk * p.B * p.H);
+  const unsigned grid = static_cast<unsigned>(nblk * p.B * p.units);
   const int smem = bwd_smem_floats(p.d, p.dvw) * 4;
   e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  bwd_dkdv_kernel<<<grid, kBwdThreads, smem, s>>>(p);
+  bwd_dkdv_kernel<<<static_cast<unsigned>(nblk * p.B * p.heads_kv), kBwdThreads, smem, s>>>(p);
   bwd_dq_kernel<<<grid, kBwdThreads, smem, s>>>(p);
-  bwd_reduce_kernel<<<1, kBwdThreads, 0, s>>>(p);
+  const int nred = p.v2 ? p.n_logit_outs : 1;
+  if (nred > 0) bwd_reduce_kernel<<<nred, kBwdThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -150,56 +150,67 @@ __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const Sim
 
   if constexpr (BWD) {
     static_assert(R == 1, "one query row per warp");
-    // Backward row pass, with m = 1 - lambda_init, O_r = A_r V, O = O_1 - lambda O_2,
+    // Backward row pass.  V1, with m = 1 - lambda_init, O_r = A_r V, O = O_1 - lambda O_2,
     // Oh = O / rms(O), g = m gamma dy:
     //   dO = (g - Oh mean(g Oh)) / rms(O);  D_1 = dO . O_1;  D_2 = -lambda dO . O_2;
     //   dlambda_row = -dO . O_2;  dgamma += m Oh dy.
+    // V2 (no norm, s = sigmoid(logit) of the row): dO = dy;  D_1 = dO . O_1;
+    //   D_2 = -s dO . O_2;  dlogit_row = -s (1 - s) dO . O_2.
+    // Row slots: lse_1, lse_2, D_1, D_2, dlambda / dlogit share, coefficient (lambda or s).
     __syncthreads();  // every warp is done with the key tiles: sk1 now stages dgamma rows
     float* sdg = sk1;  // [kSimtWarps][dv] (32 (d + 1) >= 8 dv floats)
     const int t = q0 + warp;
     const long long R_rows = p.rows_total;
     if (t < p.n) {  // warp-uniform
-      const float lam = *p.lambda;
+      const float coef =
+          p.v2 ? 1.f / (1.f + expf(-p.lam_logits[b * p.sb + static_cast<long long>(t) * p.st + u])) : *p.lambda;
       const float a1 = 1.f / l1[0], a2 = 1.f / l2[0];
       float o1n[NC], o2n[NC], y[NC], ss = 0.f;
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         o1n[c] = o1[0][c] * a1;
         o2n[c] = o2[0][c] * a2;
-        y[c] = o1n[c] - lam * o2n[c];
+        y[c] = o1n[c] - coef * o2n[c];
         if (lane + 32 * c < dv) ss = fmaf(y[c], y[c], ss);
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-      const float rinv = rsqrtf(ss / dv + p.eps);
       const long long ri = (static_cast<long long>(b) * p.units_per_batch + u) * p.n + t;
       const float* dyrow = p.dy + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * dv;
-      float g[NC], oh[NC], gs = 0.f;
+      float dOv[NC];
+      if (p.v2) {
 #pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        const int col = lane + 32 * c;
-        g[c] = oh[c] = 0.f;
-        if (col < dv) {
-          const float dyc = dyrow[col];
-          g[c] = p.norm_mult * (p.gamma != nullptr ? p.gamma[col] : 1.f) * dyc;
-          oh[c] = y[c] * rinv;
-          gs = fmaf(g[c], oh[c], gs);
-          sdg[warp * dv + col] = p.norm_mult * oh[c] * dyc;
+        for (int c = 0; c < NC; ++c) dOv[c] = (lane + 32 * c < dv) ? dyrow[lane + 32 * c] : 0.f;
+      } else {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float rinv = rsqrtf(ss / dv + p.eps);
+        float g[NC], oh[NC], gs = 0.f;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          const int col = lane + 32 * c;
+          g[c] = oh[c] = 0.f;
+          if (col < dv) {
+            const float dyc = dyrow[col];
+            g[c] = p.norm_mult * (p.gamma != nullptr ? p.gamma[col] : 1.f) * dyc;
+            oh[c] = y[c] * rinv;
+            gs = fmaf(g[c], oh[c], gs);
+            sdg[warp * dv + col] = p.norm_mult * oh[c] * dyc;
+          }
         }
-      }
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, off);
-      const float gmean = gs / dv;
+        for (int off = 16; off > 0; off >>= 1) gs += __shfl_xor_sync(0xffffffffu, gs, off);
+        const float gmean = gs / dv;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) dOv[c] = (g[c] - oh[c] * gmean) * rinv;
+      }
       float dd1 = 0.f, dd2 = 0.f;
       float* dorow = p.ws_do + ri * dv;
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         const int col = lane + 32 * c;
         if (col < dv) {
-          const float dO = (g[c] - oh[c] * gmean) * rinv;
-          dorow[col] = dO;
-          dd1 = fmaf(dO, o1n[c], dd1);
-          dd2 = fmaf(dO, o2n[c], dd2);
+          dorow[col] = dOv[c];
+          dd1 = fmaf(dOv[c], o1n[c], dd1);
+          dd2 = fmaf(dOv[c], o2n[c], dd2);
         }
       }
 #pragma unroll
@@ -208,21 +219,27 @@ __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const Sim
         dd2 += __shfl_xor_sync(0xffffffffu, dd2, off);
       }
       if (lane == 0) {
+        const float share = p.v2 ? -coef * (1.f - coef) * dd2 : -dd2;
         p.ws_row[ri] = m1[0] + logf(l1[0]);
         p.ws_row[R_rows + ri] = m2[0] + logf(l2[0]);
         p.ws_row[2 * R_rows + ri] = dd1;
-        p.ws_row[3 * R_rows + ri] = -lam * dd2;
-        p.ws_row[4 * R_rows + ri] = -dd2;
+        p.ws_row[3 * R_rows + ri] = -coef * dd2;
+        p.ws_row[4 * R_rows + ri] = share;
+        p.ws_row[5 * R_rows + ri] = coef;
+        if (p.dlogits_dense != nullptr)  // V2 with one logit per token: its gradient directly
+          p.dlogits_dense[b * p.sb + static_cast<long long>(t) * p.st + u] = share;
       }
-    } else {
+    } else if (!p.v2) {
       for (int col = lane; col < dv; col += 32) sdg[warp * dv + col] = 0.f;
     }
     __syncthreads();
-    for (int col = threadIdx.x; col < dv; col += kSimtWarps * 32) {
-      float a = 0.f;
+    if (!p.v2) {
+      for (int col = threadIdx.x; col < dv; col += kSimtWarps * 32) {
+        float a = 0.f;
 #pragma unroll
-      for (int w = 0; w < kSimtWarps; ++w) a += sdg[w * dv + col];
-      p.ws_dgamma[static_cast<size_t>(blockIdx.x) * dv + col] = a;
+        for (int w = 0; w < kSimtWarps; ++w) a += sdg[w * dv + col];
+        p.ws_dgamma[static_cast<size_t>(blockIdx.x) * dv + col] = a;
+      }
     }
   } else {
   // ---- epilogue: out = O1 / l1 - c O2 / l2 (then the V1 norm)

@@ -292,6 +292,33 @@ diffattn_status diffattn_backward(diffattn_dtype dt, int B, int H, int n, int d,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Backward pass of diffattn_v2_forward (DIFF V2), fp32 on CUDA cores: per head
+ * pair g of query heads 2g, 2g + 1 over KV head kv = 2g / (Hq / Hkv), with
+ * s = sigmoid(logit) of the row, out = A_2g V - s A_2g+1 V (DIFF V2 analysis
+ * page, "2. 커스텀 커널 제거", "5. 간소화된 λ 매개변수화", "GQA와의 호환성").
+ * Given dy [B, n, Hq/2, d] it writes dq [B, n, Hq, d], dk and dv [B, n, Hkv, d]
+ * (summed over every query head that reads the KV head) and dlogits, laid out
+ * like lam_logits: strides (sb, st) = (n*Hq/2, Hq/2) (one logit per token and
+ * pair), (Hq/2, 0) (per sequence and pair) or (0, 0) (per pair), the
+ * gradient summed over the tokens (and sequences) that share a logit; other
+ * strides -> ERR_UNSUPPORTED.
+ *   dt : DIFFATTN_F32 (d in [1, 128]); DIFFATTN_BF16 -> ERR_UNSUPPORTED.
+ *   softmax_scale, causal, Hq / Hkv rules: as for diffattn_v2_forward.
+ *   workspace : at least diffattn_v2_backward_workspace(B, Hq, n, d) bytes of
+ *               device memory, 16-byte aligned; the library allocates nothing.
+ * Fixed summation orders (same inputs, same bits).  Asynchronous on `stream`.
+ * Errors as for diffattn_forward.
+ */
+size_t diffattn_v2_backward_workspace(int B, int Hq, int n, int d);
+
+diffattn_status diffattn_v2_backward(diffattn_dtype dt, int B, int Hq, int Hkv, int n, int d,
+                                     const void* q, const void* k, const void* v,
+                                     const float* lam_logits, long long sb, long long st,
+                                     float softmax_scale, int causal, const void* dy, void* dq,
+                                     void* dk, void* dv, float* dlogits, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/*
  * Gradients of lambda = exp(<lq1, lk1>) - exp(<lq2, lk2>) + lambda_init
  * (news article section "差分注意力") with respect to the four vectors of
  * length dim, given the device scalar dlambda: dlq1 = dlambda exp(<lq1, lk1>) lk1,

@@ -36,7 +36,7 @@ def test_header_declares_the_entry_points():
                  "diffattn_forward_host_workspace", "diffattn_decode", "diffattn_v2_decode",
                  "diffattn_decode_workspace", "diffattn_v2_decode_workspace", "diffattn_decode_fp8k",
                  "diffattn_v2_decode_fp8k", "diffattn_backward", "diffattn_backward_workspace",
-                 "lambda_reparam_backward"):
+                 "lambda_reparam_backward", "diffattn_v2_backward", "diffattn_v2_backward_workspace"):
         assert want in names
 
 
@@ -176,7 +176,7 @@ def test_backward_host_validation(L):
     R = 2 * 3 * 100
     ctas = 2 * 3 * 13  # 8-row blocks of the row pass
     r256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    assert need == r256(R * 128 * 4) + r256(5 * R * 4) + r256(ctas * 128 * 4)
+    assert need == r256(R * 128 * 4) + r256(6 * R * 4) + r256(ctas * 128 * 4)
     W = P(0x100000)
 
     def call(dt=0, B=2, n=100, d=64, q1=A, dlam=A, ws=W, nbytes=need):
@@ -194,6 +194,28 @@ def test_backward_host_validation(L):
     assert call(ws=P(0x100008)) == da.ERR_ALIGN
     assert L.lambda_reparam_backward(A, A, A, A, 8, None, A, A, A, A, None) == da.ERR_NULL
     assert L.lambda_reparam_backward(A, A, A, A, 0, A, A, A, A, A, None) == da.ERR_SHAPE
+
+
+def test_v2_backward_host_validation(L):
+    R = 2 * 2 * 50
+    r256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    need = L.diffattn_v2_backward_workspace(2, 4, 50, 32)
+    assert need == r256(R * 32 * 4) + r256(6 * R * 4)
+    W = P(0x100000)
+
+    def call(dt=0, Hq=4, Hkv=2, n=50, d=32, sb=0, st=0, q=A, dlog=A, ws=W, nbytes=need):
+        return L.diffattn_v2_backward(dt, 2, Hq, Hkv, n, d, q, A, A, A, sb, st, ctypes.c_float(0.0), 1, A, A, A,
+                                      A, dlog, ws, nbytes, None)
+    assert call(dt=7) == da.ERR_DTYPE
+    assert call(dt=1) == da.ERR_UNSUPPORTED
+    assert call(Hq=6, Hkv=2) == da.ERR_SHAPE
+    assert call(sb=-1) == da.ERR_SHAPE
+    assert call(sb=3, st=0) == da.ERR_UNSUPPORTED        # neither per pair, per sequence nor per token
+    assert call(sb=2, st=0, q=None) == da.ERR_NULL       # per sequence (Hq/2, 0): past the stride check
+    assert call(sb=100, st=2, q=None) == da.ERR_NULL     # per token (n * Hq/2, Hq/2)
+    assert call(dlog=None) == da.ERR_NULL
+    assert call(nbytes=need - 1) == da.ERR_SHAPE
+    assert call(ws=P(0x100008)) == da.ERR_ALIGN
 
 
 def test_v2_host_validation(L):

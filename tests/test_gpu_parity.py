@@ -623,3 +623,37 @@ def test_v1_backward_bench_size_sampled():
             assert err <= TOL["f32"] * max(1.0, float(np.max(np.abs(r)))), f"({b},{h}) {k}: {err}"
     for k in ("dq1", "dq2", "dk1", "dk2", "dv", "dgamma", "dlam"):
         assert bool(torch.isfinite(got[k]).all()), k
+
+
+BWD_V2 = [  # B, Hq, Hkv, n, d, causal, logit granularity
+    (2, 4, 2, 40, 16, True, "token"),
+    (1, 8, 2, 100, 64, True, "pair"),     # group 4: two pairs per KV head, dK / dV summed over both
+    (2, 4, 1, 77, 32, False, "seq"),
+    (1, 2, 1, 130, 128, True, "token"),   # d = 128
+    (1, 4, 2, 1, 8, True, "pair"),        # one token
+    (2, 4, 2, 65, 30, True, "seq"),       # d % 4 != 0
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,n,d,causal,gran", BWD_V2)
+def test_v2_backward_f32(B, Hq, Hkv, n, d, causal, gran):
+    g = torch.Generator(device="cuda").manual_seed(2500 + n + d + Hq)
+
+    def rnd(*shape):
+        return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32)
+    G = Hq // 2
+    q, k, v, dy = rnd(B, n, Hq, d), rnd(B, n, Hkv, d), rnd(B, n, Hkv, d), rnd(B, n, G, d)
+    lg = {"token": rnd(B, n, G), "seq": rnd(B, G), "pair": rnd(G)}[gran]
+    got = da.diffattn_v2_backward(q, k, v, lg, dy, causal=causal)
+    da.device_status()
+    lg_np = lg.cpu().double().numpy()
+    dense = {"token": lg_np, "seq": np.broadcast_to(lg_np[:, None, :], (B, n, G)),
+             "pair": np.broadcast_to(lg_np, (B, n, G))}[gran]
+    ref = oracle.diff_attn_v2_backward(q, k, v, np.ascontiguousarray(dense), causal, dy)
+    ref["dlogits"] = {"token": ref["dlogits"], "seq": ref["dlogits"].sum(axis=1),
+                      "pair": ref["dlogits"].sum(axis=(0, 1))}[gran]
+    for key in ("dq", "dk", "dv", "dlogits"):
+        r = np.asarray(ref[key])
+        scale = max(1.0, float(np.max(np.abs(r))))
+        err = _err(_np(got[key]), r)
+        assert err <= TOL["f32"] * scale, f"{key}: max abs error {err} (scale {scale})"
