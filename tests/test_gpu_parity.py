@@ -635,6 +635,24 @@ BWD_V2 = [  # B, Hq, Hkv, n, d, causal, logit granularity
 ]
 
 
+def _v2_bwd_reference(q, k, v, lg, dy, causal, gran):
+    """The oracle's gradients; a logit shared by tokens (and sequences) gets their summed gradient."""
+    B, n, G = q.shape[0], q.shape[1], q.shape[2] // 2
+    lg_np = lg.cpu().double().numpy()
+    if gran == "token":
+        dense = lg_np
+    elif gran == "seq":
+        dense = np.broadcast_to(lg_np[:, None, :], (B, n, G))
+    else:
+        dense = np.broadcast_to(lg_np, (B, n, G))
+    ref = oracle.diff_attn_v2_backward(q, k, v, np.ascontiguousarray(dense), causal, dy)
+    if gran == "seq":
+        ref["dlogits"] = ref["dlogits"].sum(axis=1)
+    elif gran == "pair":
+        ref["dlogits"] = ref["dlogits"].sum(axis=(0, 1))
+    return ref
+
+
 @pytest.mark.parametrize("B,Hq,Hkv,n,d,causal,gran", BWD_V2)
 def test_v2_backward_f32(B, Hq, Hkv, n, d, causal, gran):
     g = torch.Generator(device="cuda").manual_seed(2500 + n + d + Hq)
@@ -646,12 +664,7 @@ def test_v2_backward_f32(B, Hq, Hkv, n, d, causal, gran):
     lg = {"token": rnd(B, n, G), "seq": rnd(B, G), "pair": rnd(G)}[gran]
     got = da.diffattn_v2_backward(q, k, v, lg, dy, causal=causal)
     da.device_status()
-    lg_np = lg.cpu().double().numpy()
-    dense = {"token": lg_np, "seq": np.broadcast_to(lg_np[:, None, :], (B, n, G)),
-             "pair": np.broadcast_to(lg_np, (B, n, G))}[gran]
-    ref = oracle.diff_attn_v2_backward(q, k, v, np.ascontiguousarray(dense), causal, dy)
-    ref["dlogits"] = {"token": ref["dlogits"], "seq": ref["dlogits"].sum(axis=1),
-                      "pair": ref["dlogits"].sum(axis=(0, 1))}[gran]
+    ref = _v2_bwd_reference(q, k, v, lg, dy, causal, gran)
     for key in ("dq", "dk", "dv", "dlogits"):
         r = np.asarray(ref[key])
         scale = max(1.0, float(np.max(np.abs(r))))
