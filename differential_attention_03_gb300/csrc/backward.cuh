@@ -28,9 +28,11 @@
 //     fixed order (deterministic).
 // Both sweeps use the same 32 x 32 block step: warp w takes query rows
 // 4w .. 4w + 3 of the block and lane j its key j (scores and dO . v_j as
-// dot products over shared-memory rows padded to an odd pitch), writes
-// P = A_1 - lambda A_2, dS_1 and dS_2 to shared memory; then every thread
-// accumulates its outputs from them.
+// dot products over shared-memory rows; with d % 32 == 0 as float4 reads,
+// each of the lane's key-row reads serving the warp's four query rows),
+// writes P = A_1 - lambda A_2, dS_1 and dS_2 to shared memory; then every
+// thread accumulates its outputs from them (float4 reads of its channel
+// slice when d % 32 == 0).
 #pragma once
 
 #include "params.h"
@@ -43,16 +45,26 @@ constexpr int kBwdThreads = 256;
 constexpr int kBwdMaxCV = 32;  // value channels a thread accumulates (dv <= 256)
 constexpr int kBwdMaxCK = 16;  // key/query channels a thread accumulates (d <= 128)
 
+// Row pitches of the shared-memory tiles.  d % 32 == 0 ("fast"): d + 4, so
+// that rows start on 16 bytes and the float4 reads of eight consecutive lanes
+// (rows j .. j + 7) fall on 32 different banks; else d + 1 (odd: a lane per
+// row reads scalars without conflicts).
+__host__ __device__ constexpr bool bwd_fast(int d) { return d % 32 == 0; }
+__host__ __device__ constexpr int bwd_pitch(int w, bool fast) { return fast ? w + 4 : w + 1; }
+
 // Shared-memory floats of both sweeps: K_1, K_2, V, Q_1, Q_2, dO tiles, three
 // 32 x 33 blocks (P, dS_1, dS_2) and five row statistics.
 __host__ __device__ constexpr int bwd_smem_floats(int d, int dv) {
-  return 4 * kBwdBlk * (d + 1) + 2 * kBwdBlk * (dv + 1) + 3 * kBwdBlk * (kBwdBlk + 1) + 5 * kBwdBlk;
+  return 4 * kBwdBlk * bwd_pitch(d, bwd_fast(d)) + 2 * kBwdBlk * bwd_pitch(dv, bwd_fast(d)) +
+         3 * kBwdBlk * (kBwdBlk + 1) + 5 * kBwdBlk;
 }
 
 struct BwdSmem {
   float *k1, *k2, *v, *q1, *q2, *dO, *P, *S1, *S2, *st;
+  int dp, dvp;  // row pitches (floats)
   __device__ BwdSmem(float* sm, int d, int dv) {
-    const int dp = d + 1, dvp = dv + 1;
+    dp = bwd_pitch(d, bwd_fast(d));
+    dvp = bwd_pitch(dv, bwd_fast(d));
     k1 = sm;
     k2 = k1 + kBwdBlk * dp;
     v = k2 + kBwdBlk * dp;
@@ -74,10 +86,10 @@ __device__ __forceinline__ void bwd_stage_queries(const BwdParams& p, const BwdS
   const size_t qrow = static_cast<size_t>(p.heads_q) * d;
   const float* qb = p.q1 + static_cast<size_t>(b) * p.n * qrow;
   const long long unit_row0 = unit * p.n;
-  stage_rows(s.q1, d + 1, qb + static_cast<size_t>(hq1) * d, qrow, q0, p.n, d, kBwdBlk, vec);
-  stage_rows(s.q2, d + 1, (p.q2 + static_cast<size_t>(b) * p.n * qrow) + static_cast<size_t>(hq2) * d, qrow, q0,
+  stage_rows(s.q1, s.dp, qb + static_cast<size_t>(hq1) * d, qrow, q0, p.n, d, kBwdBlk, vec);
+  stage_rows(s.q2, s.dp, (p.q2 + static_cast<size_t>(b) * p.n * qrow) + static_cast<size_t>(hq2) * d, qrow, q0,
              p.n, d, kBwdBlk, vec);
-  stage_rows(s.dO, dv + 1, p.dO + unit_row0 * dv, dv, q0, p.n, dv, kBwdBlk, (dv & 3) == 0);
+  stage_rows(s.dO, s.dvp, p.dO + unit_row0 * dv, dv, q0, p.n, dv, kBwdBlk, (dv & 3) == 0);
   if (threadIdx.x < 5 * kBwdBlk) {
     const int k = threadIdx.x / kBwdBlk, i = threadIdx.x % kBwdBlk;
     const int slot = k < 4 ? k : 5;  // lse_1, lse_2, D_1, D_2, coefficient
@@ -90,34 +102,70 @@ __device__ __forceinline__ void bwd_stage_keys(const BwdParams& p, const BwdSmem
                                                bool vec) {
   const int d = p.d, dv = p.dvw;
   const size_t krow = static_cast<size_t>(p.heads_kv) * d, vrow = static_cast<size_t>(p.heads_kv) * dv;
-  stage_rows(s.k1, d + 1, p.k1 + static_cast<size_t>(b) * p.n * krow + static_cast<size_t>(hk) * d, krow, k0, p.n,
+  stage_rows(s.k1, s.dp, p.k1 + static_cast<size_t>(b) * p.n * krow + static_cast<size_t>(hk) * d, krow, k0, p.n,
              d, kBwdBlk, vec);
   if (!p.v2)
-    stage_rows(s.k2, d + 1, p.k2 + static_cast<size_t>(b) * p.n * krow + static_cast<size_t>(hk) * d, krow, k0,
+    stage_rows(s.k2, s.dp, p.k2 + static_cast<size_t>(b) * p.n * krow + static_cast<size_t>(hk) * d, krow, k0,
                p.n, d, kBwdBlk, vec);
-  stage_rows(s.v, dv + 1, p.v + static_cast<size_t>(b) * p.n * vrow + static_cast<size_t>(hk) * dv, vrow, k0, p.n,
+  stage_rows(s.v, s.dvp, p.v + static_cast<size_t>(b) * p.n * vrow + static_cast<size_t>(hk) * dv, vrow, k0, p.n,
              dv, kBwdBlk, vec);
 }
 
 // The 32 x 32 block step: P = A_1 - coef A_2, dS_1, dS_2 for queries
 // [q0, q0 + 32) and keys [k0, k0 + 32) into shared memory (0 where masked).
 // coef is lambda (V1) or the row's sigmoid(logit) (V2).
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+  acc = fmaf(a.x, b.x, acc);
+  acc = fmaf(a.y, b.y, acc);
+  acc = fmaf(a.z, b.z, acc);
+  return fmaf(a.w, b.w, acc);
+}
+
+__device__ __forceinline__ float4 ld4(const float* a) { return *reinterpret_cast<const float4*>(a); }
+
 __device__ __forceinline__ void bwd_block_step(const BwdParams& p, const BwdSmem& s, int q0, int k0, float lam) {
+  constexpr int RW = kBwdBlk / (kBwdThreads / 32);  // query rows per warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int d = p.d, dv = p.dvw, dp = d + 1, dvp = dv + 1;
+  const int d = p.d, dv = p.dvw, dp = s.dp, dvp = s.dvp;
   const int key = k0 + lane;
   const float* k2s = p.v2 ? s.k1 : s.k2;
+  float s1v[RW], s2v[RW], dpvv[RW];
 #pragma unroll
-  for (int r = 0; r < kBwdBlk / (kBwdThreads / 32); ++r) {
-    const int i = warp * (kBwdBlk / (kBwdThreads / 32)) + r, t = q0 + i;
+  for (int r = 0; r < RW; ++r) s1v[r] = s2v[r] = dpvv[r] = 0.f;
+  if (bwd_fast(d)) {
+    // Each float4 of this lane's key (and value) row is read once and used
+    // for the warp's four query rows (broadcast float4 reads).
+    for (int e = 0; e < d; e += 4) {
+      const float4 ka = ld4(s.k1 + lane * dp + e), kb = ld4(k2s + lane * dp + e);
+#pragma unroll
+      for (int r = 0; r < RW; ++r) {
+        const int i = warp * RW + r;
+        s1v[r] = dot4(ld4(s.q1 + i * dp + e), ka, s1v[r]);
+        s2v[r] = dot4(ld4(s.q2 + i * dp + e), kb, s2v[r]);
+      }
+    }
+    for (int c = 0; c < dv; c += 4) {
+      const float4 vv = ld4(s.v + lane * dvp + c);
+#pragma unroll
+      for (int r = 0; r < RW; ++r) dpvv[r] = dot4(ld4(s.dO + (warp * RW + r) * dvp + c), vv, dpvv[r]);
+    }
+  } else {
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+      const int i = warp * RW + r;
+      for (int e = 0; e < d; ++e) {
+        s1v[r] = fmaf(s.q1[i * dp + e], s.k1[lane * dp + e], s1v[r]);
+        s2v[r] = fmaf(s.q2[i * dp + e], k2s[lane * dp + e], s2v[r]);
+      }
+      for (int c = 0; c < dv; ++c) dpvv[r] = fmaf(s.dO[i * dvp + c], s.v[lane * dvp + c], dpvv[r]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < RW; ++r) {
+    const int i = warp * RW + r, t = q0 + i;
     const bool valid = t < p.n && key < p.n && (!p.causal || key <= t);
     const float coef = p.v2 ? s.st[4 * kBwdBlk + i] : lam;
-    float s1 = 0.f, s2 = 0.f, dpv = 0.f;
-    for (int e = 0; e < d; ++e) {
-      s1 = fmaf(s.q1[i * dp + e], s.k1[lane * dp + e], s1);
-      s2 = fmaf(s.q2[i * dp + e], k2s[lane * dp + e], s2);
-    }
-    for (int c = 0; c < dv; ++c) dpv = fmaf(s.dO[i * dvp + c], s.v[lane * dvp + c], dpv);
+    const float s1 = s1v[r], s2 = s2v[r], dpv = dpvv[r];
     const float p1 = valid ? expf(s1 * p.scale - s.st[i]) : 0.f;
     const float p2 = valid ? expf(s2 * p.scale - s.st[kBwdBlk + i]) : 0.f;
     s.P[i * (kBwdBlk + 1) + lane] = p1 - coef * p2;
@@ -142,9 +190,9 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dkdv_kernel(const BwdParams p
   const int nblk = (p.n + kBwdBlk - 1) / kBwdBlk;
   const int kb = blockIdx.x % nblk, kvu = blockIdx.x / nblk;
   const int b = kvu / p.heads_kv, hk = kvu % p.heads_kv, k0 = kb * kBwdBlk;
-  const int d = p.d, dv = p.dvw, dp = d + 1, dvp = dv + 1;
+  const int d = p.d, dv = p.dvw, dp = s.dp, dvp = s.dvp;
   const int cv = (dv + 7) / 8, ck = (d + 7) / 8;
-  const bool vec = bwd_vec(p);
+  const bool vec = bwd_vec(p), fast = bwd_fast(d);
   const float lam = p.v2 ? 0.f : *p.lambda;
   // Query-head pairs reading this KV head: V1 the head itself; V2 pairs
   // hk * group / 2 .. (hk + 1) * group / 2 - 1.
@@ -169,6 +217,33 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dkdv_kernel(const BwdParams p
         const float w = s.P[i * (kBwdBlk + 1) + lane];
         const float e1 = s.S1[i * (kBwdBlk + 1) + lane];
         const float e2 = s.S2[i * (kBwdBlk + 1) + lane];
+        if (fast) {  // cv, ck multiples of 4: float4 broadcast reads of the warp's channel slices
+#pragma unroll
+          for (int k = 0; k < kBwdMaxCV; k += 4) {
+            if (k < cv) {
+              const float4 o = ld4(s.dO + i * dvp + warp * cv + k);
+              av[k] = fmaf(w, o.x, av[k]);
+              av[k + 1] = fmaf(w, o.y, av[k + 1]);
+              av[k + 2] = fmaf(w, o.z, av[k + 2]);
+              av[k + 3] = fmaf(w, o.w, av[k + 3]);
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < kBwdMaxCK; k += 4) {
+            if (k < ck) {
+              const float4 qa = ld4(s.q1 + i * dp + warp * ck + k), qb = ld4(s.q2 + i * dp + warp * ck + k);
+              a1[k] = fmaf(e1, qa.x, a1[k]);
+              a1[k + 1] = fmaf(e1, qa.y, a1[k + 1]);
+              a1[k + 2] = fmaf(e1, qa.z, a1[k + 2]);
+              a1[k + 3] = fmaf(e1, qa.w, a1[k + 3]);
+              a2[k] = fmaf(e2, qb.x, a2[k]);
+              a2[k + 1] = fmaf(e2, qb.y, a2[k + 1]);
+              a2[k + 2] = fmaf(e2, qb.z, a2[k + 2]);
+              a2[k + 3] = fmaf(e2, qb.w, a2[k + 3]);
+            }
+          }
+          continue;
+        }
 #pragma unroll
         for (int k = 0; k < kBwdMaxCV; ++k) {
           const int c = warp * cv + k;
@@ -221,9 +296,9 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dq_kernel(const BwdParams p) 
   const int b = unit / p.units, g = unit % p.units, q0 = qb * kBwdBlk;
   const int hq1 = p.v2 ? 2 * g : g, hq2 = p.v2 ? 2 * g + 1 : g;
   const int hk = p.v2 ? (2 * g) / p.group : g;
-  const int d = p.d, dp = d + 1;
+  const int d = p.d, dp = s.dp;
   const int ck = (d + 7) / 8;
-  const bool vec = bwd_vec(p);
+  const bool vec = bwd_vec(p), fast = bwd_fast(d);
   const float lam = p.v2 ? 0.f : *p.lambda;
   const float* k2s = p.v2 ? s.k1 : s.k2;
   bwd_stage_queries(p, s, b, hq1, hq2, unit, q0, vec);
@@ -241,6 +316,23 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dq_kernel(const BwdParams p) 
     for (int j = 0; j < kBwdBlk; ++j) {
       const float e1 = s.S1[lane * (kBwdBlk + 1) + j];
       const float e2 = s.S2[lane * (kBwdBlk + 1) + j];
+      if (fast) {  // ck a multiple of 4: float4 broadcast reads of the key rows' channel slice
+#pragma unroll
+        for (int k = 0; k < kBwdMaxCK; k += 4) {
+          if (k < ck) {
+            const float4 ka = ld4(s.k1 + j * dp + warp * ck + k), kb = ld4(k2s + j * dp + warp * ck + k);
+            a1[k] = fmaf(e1, ka.x, a1[k]);
+            a1[k + 1] = fmaf(e1, ka.y, a1[k + 1]);
+            a1[k + 2] = fmaf(e1, ka.z, a1[k + 2]);
+            a1[k + 3] = fmaf(e1, ka.w, a1[k + 3]);
+            a2[k] = fmaf(e2, kb.x, a2[k]);
+            a2[k + 1] = fmaf(e2, kb.y, a2[k + 1]);
+            a2[k + 2] = fmaf(e2, kb.z, a2[k + 2]);
+            a2[k + 3] = fmaf(e2, kb.w, a2[k + 3]);
+          }
+        }
+        continue;
+      }
 #pragma unroll
       for (int k = 0; k < kBwdMaxCK; ++k) {
         const int c = warp * ck + k;
