@@ -357,16 +357,21 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dq_kernel(const BwdParams p) 
   }
 }
 
-// Fixed-order reductions of the row pass's shares.  V1 (one CTA): dlambda =
-// sum of every row's share, dgamma[c] = sum of the CTAs' shares.  V2 (one CTA
-// per output, logits shared by a sequence's tokens): dlogit of (b, pair) =
-// sum over the tokens (and over the sequences when sb = 0) of the rows' shares.
+// Fixed-order reductions of the row pass's shares, one CTA per output.  V1:
+// CTA 0 dlambda = sum of every row's share; CTA 1 + c dgamma[c] = sum of the
+// row-pass CTAs' shares.  V2 (logits shared by a sequence's tokens): dlogit of
+// (b, pair) = sum over the tokens (and the sequences when sb = 0) of the
+// rows' shares.
 __global__ void __launch_bounds__(kBwdThreads) bwd_reduce_kernel(const BwdParams p) {
   __shared__ float red[kBwdThreads];
   const float* share = p.row + 4 * p.rows;
   float a = 0.f;
   int g = 0, b0 = 0, b1 = 0;
-  if (p.v2) {
+  const bool dgamma_cta = !p.v2 && blockIdx.x > 0;
+  if (dgamma_cta) {
+    const int c = static_cast<int>(blockIdx.x) - 1;
+    for (int k = threadIdx.x; k < p.n_row_ctas; k += kBwdThreads) a += p.dgp[static_cast<size_t>(k) * p.dvw + c];
+  } else if (p.v2) {
     g = p.sb == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) % p.units;
     b0 = p.sb == 0 ? 0 : static_cast<int>(blockIdx.x) / p.units;
     b1 = p.sb == 0 ? p.B : b0 + 1;
@@ -383,18 +388,13 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_reduce_kernel(const BwdParams
     if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
     __syncthreads();
   }
-  if (p.v2) {
-    if (threadIdx.x == 0) p.dlogits[static_cast<long long>(b0) * p.sb + g] = red[0];
-    return;
-  }
-  if (threadIdx.x == 0) *p.dlambda = red[0];
-  if (p.dgamma != nullptr) {
-    for (int c = threadIdx.x; c < p.dvw; c += kBwdThreads) {
-      float s2 = 0.f;
-      for (int k = 0; k < p.n_row_ctas; ++k) s2 += p.dgp[static_cast<size_t>(k) * p.dvw + c];
-      p.dgamma[c] = s2;
-    }
-  }
+  if (threadIdx.x != 0) return;
+  if (p.v2)
+    p.dlogits[static_cast<long long>(b0) * p.sb + g] = red[0];
+  else if (dgamma_cta)
+    p.dgamma[blockIdx.x - 1] = red[0];
+  else
+    *p.dlambda = red[0];
 }
 
 // Gradients of lambda = exp(<lq1, lk1>) - exp(<lq2, lk2>) + lambda_init with

@@ -18,7 +18,7 @@ cudaError_t launch_backward_f32(const BwdParams& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   bwd_dkdv_kernel<<<static_cast<unsigned>(nblk * p.B * p.heads_kv), kBwdThreads, smem, s>>>(p);
   bwd_dq_kernel<<<grid, kBwdThreads, smem, s>>>(p);
-  const int nred = p.v2 ? p.n_logit_outs : 1;
+  const int nred = p.v2 ? p.n_logit_outs : 1 + (p.dgamma != nullptr ? p.dvw : 0);
   if (nred > 0) bwd_reduce_kernel<<<nred, kBwdThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
