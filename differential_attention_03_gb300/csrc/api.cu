@@ -12,6 +12,7 @@
 #include <mutex>
 #include <string>
 
+#include "bwd_params.h"
 #include "decode.cuh"
 #include "diffattn.h"
 #include "launch.h"
@@ -765,10 +766,11 @@ diffattn_status diffattn_backward(diffattn_dtype dt, int B, int H, int n, int d,
   rp.heads_q = rp.heads_kv = rp.units_per_batch = H;
   rp.group = 1;
   rp.rows_total = static_cast<long long>(R);
-  rp.dy = static_cast<const float*>(dy);
-  rp.ws_do = ws_do;
-  rp.ws_row = ws_row;
-  rp.ws_dgamma = ws_dg;
+  da::SimtBwdExtra rx{};
+  rx.dy = static_cast<const float*>(dy);
+  rx.ws_do = ws_do;
+  rx.ws_row = ws_row;
+  rx.ws_dgamma = ws_dg;
 
   da::BwdParams p{};
   p.q1 = rp.q1;
@@ -798,7 +800,7 @@ diffattn_status diffattn_backward(diffattn_dtype dt, int B, int H, int n, int d,
   p.group = 1;
   p.rows = static_cast<long long>(R);
   p.n_row_ctas = static_cast<int>(bwd_row_ctas(B, H, n));
-  cudaError_t e = da::launch_simt_bwd_rows(rp, s);
+  cudaError_t e = da::launch_simt_bwd_rows(rp, rx, s);
   if (e == cudaSuccess) e = da::launch_backward_f32(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_backward launch");
   g_launches.fetch_add(4);
@@ -871,10 +873,11 @@ diffattn_status diffattn_v2_backward(diffattn_dtype dt, int B, int Hq, int Hkv, 
   rp.units_per_batch = G;
   rp.group = Hq / Hkv;
   rp.rows_total = static_cast<long long>(R);
-  rp.dy = static_cast<const float*>(dy);
-  rp.ws_do = ws_do;
-  rp.ws_row = ws_row;
-  rp.dlogits_dense = dense ? dlogits : nullptr;
+  da::SimtBwdExtra rx{};
+  rx.dy = static_cast<const float*>(dy);
+  rx.ws_do = ws_do;
+  rx.ws_row = ws_row;
+  rx.dlogits_dense = dense ? dlogits : nullptr;
 
   da::BwdParams p{};
   p.q1 = p.q2 = rp.q1;
@@ -900,7 +903,7 @@ diffattn_status diffattn_v2_backward(diffattn_dtype dt, int B, int Hq, int Hkv, 
   p.group = Hq / Hkv;
   p.rows = static_cast<long long>(R);
   p.n_logit_outs = dense ? 0 : (sb == 0 ? G : B * G);
-  cudaError_t e = da::launch_simt_bwd_rows(rp, s);
+  cudaError_t e = da::launch_simt_bwd_rows(rp, rx, s);
   if (e == cudaSuccess) e = da::launch_backward_f32(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_backward launch");
   g_launches.fetch_add(dense ? 3 : 4);

@@ -35,7 +35,7 @@
 // slice when d % 32 == 0).
 #pragma once
 
-#include "params.h"
+#include "bwd_params.h"
 #include "stage.cuh"
 
 namespace da {

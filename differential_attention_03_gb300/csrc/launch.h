@@ -9,6 +9,7 @@
 namespace da {
 struct DecodeParams;
 struct BwdParams;
+struct SimtBwdExtra;
 }
 
 namespace da {
@@ -29,7 +30,7 @@ cudaError_t launch_decode_v1(const DecodeParams& p, int d, bool k8, int units, i
 cudaError_t launch_decode_v2_d128(const DecodeParams& p, bool k8, int units, int cs, cudaStream_t s);
 // fp32 V1 backward: the row pass (per-row statistics, dO, dgamma shares), then the
 // dK/dV and dQ sweeps and the dlambda/dgamma reduction (3 kernels).
-cudaError_t launch_simt_bwd_rows(const SimtParams& p, cudaStream_t s);
+cudaError_t launch_simt_bwd_rows(const SimtParams& p, const SimtBwdExtra& x, cudaStream_t s);
 cudaError_t launch_backward_f32(const BwdParams& p, cudaStream_t s);
 cudaError_t launch_lambda_reparam_bwd(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
                                       int dim, const float* dlambda, float* dlq1, float* dlk1, float* dlq2,

@@ -81,40 +81,6 @@ struct SimtParams {
   int B, n, d, dv, causal, v2;
   int heads_q, heads_kv, units_per_batch, group;
   long long rows_total;
-  // Backward row pass (V1) only: dy [B, n, H, dv]; outputs in the backward workspace.
-  const float* dy;
-  float* ws_do;      // [B * H * n][dv]: dO, the gradient of the pre-norm output
-  float* ws_row;     // [5][B * H * n]: log-sum-exp 1, 2; D_1; D_2; the row's share of dlambda
-  float* ws_dgamma;  // [CTAs][dv]: each CTA's share of dgamma (V1)
-  float* dlogits_dense;  // V2 with a per-token logit stride: dlogit of (b, t, pair) at b sb + t st + pair
-};
-
-// fp32 V1 backward (backward.cuh): inputs, the row pass's workspace, outputs.
-struct BwdParams {
-  const float* q1;  // V1: [B, n, H, d]; V2: q [B, n, Hq, d] (q1 == q2)
-  const float* q2;
-  const float* k1;  // V1: [B, n, H, d]; V2: k [B, n, Hkv, d] (k1 == k2)
-  const float* k2;
-  const float* v;       // V1: [B, n, H, dv]; V2: [B, n, Hkv, d]
-  const float* dO;      // [B * units * n][dv] (row pass)
-  const float* row;     // [6][B * units * n]: lse_1, lse_2, D_1, D_2, dlambda / dlogit share, coefficient
-  const float* dgp;     // [n_row_ctas][dv]: dgamma shares (V1 row pass)
-  const float* lambda;  // V1 device scalar
-  float* dq1;           // V1: [B, n, H, d]; V2: dq [B, n, Hq, d] (dq1 == dq2)
-  float* dq2;
-  float* dk1;  // V1: [B, n, H, d]; V2: dk [B, n, Hkv, d] (dK_1 + dK_2 of every pair of the group)
-  float* dk2;
-  float* dv;       // like v
-  float* dlambda;  // V1 device scalar
-  float* dgamma;   // V1 [dv] or nullptr
-  float* dlogits;  // V2, logit shared by a sequence's tokens: dlogit of (b, pair) at b sb + pair
-  long long sb;    // (sb = 0: one logit per pair for every sequence)
-  float scale;
-  int B, n, d, dvw, causal, v2;
-  int heads_q, heads_kv, units, group;  // units: V1 heads, V2 head pairs per sequence; group = Hq / Hkv
-  long long rows;                       // B * units * n
-  int n_row_ctas;
-  int n_logit_outs;  // V2: dlogits entries the reduction writes (0: none)
 };
 
 constexpr int kSimtMaxD = 128;

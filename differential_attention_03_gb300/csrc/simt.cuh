@@ -20,6 +20,7 @@
 // dQ sweeps are in backward.cuh).
 #pragma once
 
+#include "bwd_params.h"
 #include "params.h"
 #include "ptx.cuh"
 #include "stage.cuh"
@@ -38,7 +39,7 @@ __host__ __device__ constexpr int simt_smem_floats(int d, int dv) {
 }
 
 template <bool BWD>
-__global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const SimtParams p) {
+__global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const SimtParams p, const SimtBwdExtra x) {
   extern __shared__ float sm[];
   constexpr int R = kSimtRows / kSimtWarps;  // query rows per warp
   constexpr int NC = kSimtMaxVPerLane;       // value channels per lane (lane + 32 c)
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const Sim
         if (lane + 32 * c < dv) ss = fmaf(y[c], y[c], ss);
       }
       const long long ri = (static_cast<long long>(b) * p.units_per_batch + u) * p.n + t;
-      const float* dyrow = p.dy + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * dv;
+      const float* dyrow = x.dy + ((static_cast<size_t>(b) * p.n + t) * p.units_per_batch + u) * dv;
       float dOv[NC];
       if (p.v2) {
 #pragma unroll
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const Sim
         for (int c = 0; c < NC; ++c) dOv[c] = (g[c] - oh[c] * gmean) * rinv;
       }
       float dd1 = 0.f, dd2 = 0.f;
-      float* dorow = p.ws_do + ri * dv;
+      float* dorow = x.ws_do + ri * dv;
 #pragma unroll
       for (int c = 0; c < NC; ++c) {
         const int col = lane + 32 * c;
@@ -236,14 +237,14 @@ __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const Sim
       }
       if (lane == 0) {
         const float share = p.v2 ? -coef * (1.f - coef) * dd2 : -dd2;
-        p.ws_row[ri] = m1[0] + logf(l1[0]);
-        p.ws_row[R_rows + ri] = m2[0] + logf(l2[0]);
-        p.ws_row[2 * R_rows + ri] = dd1;
-        p.ws_row[3 * R_rows + ri] = -coef * dd2;
-        p.ws_row[4 * R_rows + ri] = share;
-        p.ws_row[5 * R_rows + ri] = coef;
-        if (p.dlogits_dense != nullptr)  // V2 with one logit per token: its gradient directly
-          p.dlogits_dense[b * p.sb + static_cast<long long>(t) * p.st + u] = share;
+        x.ws_row[ri] = m1[0] + logf(l1[0]);
+        x.ws_row[R_rows + ri] = m2[0] + logf(l2[0]);
+        x.ws_row[2 * R_rows + ri] = dd1;
+        x.ws_row[3 * R_rows + ri] = -coef * dd2;
+        x.ws_row[4 * R_rows + ri] = share;
+        x.ws_row[5 * R_rows + ri] = coef;
+        if (x.dlogits_dense != nullptr)  // V2 with one logit per token: its gradient directly
+          x.dlogits_dense[b * p.sb + static_cast<long long>(t) * p.st + u] = share;
       }
     } else if (!p.v2) {
       for (int col = lane; col < dv; col += 32) sdg[warp * dv + col] = 0.f;
@@ -254,7 +255,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const Sim
         float a = 0.f;
 #pragma unroll
         for (int w = 0; w < kSimtWarps; ++w) a += sdg[w * dv + col];
-        p.ws_dgamma[static_cast<size_t>(blockIdx.x) * dv + col] = a;
+        x.ws_dgamma[static_cast<size_t>(blockIdx.x) * dv + col] = a;
       }
     }
   } else {
