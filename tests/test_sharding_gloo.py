@@ -62,3 +62,57 @@ def test_batch_slice_edges():
     assert batch_slice(1, 2, 1) == (1, 1)
     with pytest.raises(ValueError):
         batch_slice(4, 2, 2)
+
+
+def _bwd_worker(rank, world, port, out):
+    # Every rank draws the same global batch, takes its slice, computes the
+    # backward of its entries (the oracle stands in for the kernels on the
+    # CPU) and sums the shared parameters' gradients over the ranks.
+    import numpy as np
+
+    import oracle
+    from differential_attention_03_gb300.sharding import allreduce_shared_grads
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    r = np.random.default_rng(5)
+    B, n, H, d = 5, 6, 2, 4
+    x = {k: r.normal(size=(B, n, H, d)) for k in ("q1", "q2", "k1", "k2")}
+    x["v"], x["dy"] = r.normal(size=(B, n, H, 2 * d)), r.normal(size=(B, n, H, 2 * d))
+    gamma = r.uniform(0.5, 1.5, size=2 * d)
+    start, stop = batch_slice(B, world, rank)
+    mine = oracle.diff_attn_v1_backward(*(x[k][start:stop] for k in ("q1", "q2", "k1", "k2", "v")), 0.4, 0.3,
+                                        gamma, 1e-5, True, x["dy"][start:stop])
+    shared = [torch.tensor([mine["dlam"]], dtype=torch.float64), torch.tensor(mine["dgamma"])]
+    allreduce_shared_grads(shared)
+    full = oracle.diff_attn_v1_backward(*(x[k] for k in ("q1", "q2", "k1", "k2", "v")), 0.4, 0.3, gamma, 1e-5,
+                                        True, x["dy"])
+    ok_shared = (abs(float(shared[0]) - full["dlam"]) < 1e-10
+                 and float(np.max(np.abs(shared[1].numpy() - full["dgamma"]))) < 1e-10)
+    ok_local = all(float(np.max(np.abs(mine[k] - full[k][start:stop]))) < 1e-12 for k in ("dq1", "dk2", "dv"))
+    flags = torch.tensor([int(ok_shared), int(ok_local)])
+    dist.all_reduce(flags, op=dist.ReduceOp.MIN)
+    if rank == 0:
+        out.put(flags.tolist())
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_sum_the_shared_gradients():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_bwd_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    flags = q.get(timeout=180)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert flags == [1, 1]  # shared gradients summed to the full batch's; per-entry gradients need no exchange
+
+
+def test_allreduce_shared_grads_rejects_mixed_dtypes():
+    from differential_attention_03_gb300.sharding import allreduce_shared_grads
+    with pytest.raises(ValueError):
+        allreduce_shared_grads([torch.zeros(1, dtype=torch.float32), torch.zeros(2, dtype=torch.float64)])
