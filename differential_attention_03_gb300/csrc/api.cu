@@ -833,7 +833,14 @@ diffattn_status diffattn_v2_backward(diffattn_dtype dt, int B, int Hq, int Hkv, 
   if (!dense && !(st == 0 && (sb == 0 || sb == G)))
     return fail(DIFFATTN_ERR_UNSUPPORTED,
                 "diffattn_v2_backward: logit strides (sb, st) must be (n*Hq/2, Hq/2), (Hq/2, 0) or (0, 0)");
-  if (B == 0 || Hq == 0 || n == 0) return ok();
+  if (B == 0 || Hq == 0 || n == 0) {  // no rows: a logit shared by tokens gets a zero gradient
+    const size_t shared = dense ? 0 : (sb == 0 ? static_cast<size_t>(G) : static_cast<size_t>(B) * G);
+    if (shared > 0 && dlogits != nullptr) {
+      cudaError_t e = cudaMemsetAsync(dlogits, 0, shared * sizeof(float), static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_backward: clearing dlogits");
+    }
+    return ok();
+  }
   if (!q || !k || !v || !lam_logits || !dy || !dq || !dk || !dv || !dlogits || !workspace)
     return fail(DIFFATTN_ERR_NULL, "diffattn_v2_backward: NULL pointer");
   const size_t need = diffattn_v2_backward_workspace(B, Hq, n, d);
