@@ -24,3 +24,4 @@ from .diffattn_oracle import (  # noqa: F401
 )
 from .brute import brute_v1, brute_v2  # noqa: F401
 from .backward import diff_attn_v1_backward, diff_attn_v2_backward, lambda_reparam_backward  # noqa: F401
+from .projections import diff_v1_layer, diff_v2_layer  # noqa: F401
