@@ -142,3 +142,22 @@ def test_e4m3_pins_catch_mutants(monkeypatch, mutant):
         pins.test_e4m3_decode_closed_forms()
     with pytest.raises(AssertionError):
         pins.test_e4m3_decode_matches_torch_float8()
+
+
+def _lambda_init_rate(rate):
+    def f(layer_index):
+        return 0.8 - 0.6 * math.exp(-rate * (layer_index - 1))  # the rate 0.3 replaced
+    return f
+
+
+def _lambda_init_no_offset(layer_index):
+    return 0.8 - 0.6 * math.exp(-0.3 * layer_index)  # l in place of (l - 1)
+
+
+@pytest.mark.parametrize("mutant", [_lambda_init_rate(0.2), _lambda_init_rate(0.5), _lambda_init_no_offset],
+                         ids=["rate0.2", "rate0.5", "no_offset"])
+def test_lambda_init_pin_catches_mutants(monkeypatch, mutant):
+    pins.test_lambda_init_closed_forms()  # passes on the real oracle
+    monkeypatch.setattr(pins.oracle, "lambda_init", mutant)
+    with pytest.raises(AssertionError):
+        pins.test_lambda_init_closed_forms()

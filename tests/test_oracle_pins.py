@@ -70,6 +70,29 @@ def test_lambda_init_properties():
         oracle.lambda_init(0)
 
 
+# lambda_init at the layers of the measured workloads, evaluated from the schedule
+# the news article prints (section "差分注意力": 0.8 - 0.6 exp(-0.3 (l - 1)),
+# l in [1, L]) and the glossary's prose after its worked example (the same
+# schedule, deeper layers starting nearer 0.8).  Written out as literals so that
+# a wrong rate or a wrong layer offset in the oracle cannot reproduce them.
+LAMBDA_INIT_CLOSED_FORMS = {
+    1: 0.2,
+    4: 0.5560582041556406,    # 0.8 - 0.6 e^-0.9
+    12: 0.777870099559256,    # 0.8 - 0.6 e^-3.3
+    20: 0.7979924207255172,   # 0.8 - 0.6 e^-5.7
+}
+# The gap 0.8 - lambda_init shrinks by e^-0.3 per layer.
+LAMBDA_INIT_GAP_RATIO = 0.7408182206817179
+
+
+def test_lambda_init_closed_forms():
+    """The rate 0.3 and the offset (l - 1) of the schedule, pinned by its values at l = 1, 4, 12, 20."""
+    for l, want in LAMBDA_INIT_CLOSED_FORMS.items():
+        assert abs(oracle.lambda_init(l) - want) <= 1e-15, l
+    g1, g2 = 0.8 - oracle.lambda_init(7), 0.8 - oracle.lambda_init(8)
+    assert abs(g2 / g1 - LAMBDA_INIT_GAP_RATIO) <= 1e-13
+
+
 def test_lambda_reparam_closed_forms():
     lin = 0.5560582041556406
     z = np.zeros(64)
