@@ -468,6 +468,14 @@ static diffattn_status decode_v1(const char* fn, diffattn_dtype dt, int B, int H
   const long long units = static_cast<long long>(B) * H;
   if (units * da::DecodeCfg<64>::MAX_CS * kMaxSplit > 0x7fffffffll)
     return fail(DIFFATTN_ERR_SHAPE, "%s: too many (batch, head) pairs", fn);
+  if (workspace != nullptr) {
+    const size_t need = diffattn_decode_workspace(B, H, d);
+    if (workspace_bytes < need)
+      return fail(DIFFATTN_ERR_SHAPE, "%s: workspace of %zu bytes, %zu needed (or pass NULL)", fn, workspace_bytes,
+                  need);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)
+      return fail(DIFFATTN_ERR_ALIGN, "%s: workspace must be 4-byte aligned", fn);
+  }
   if (eps <= 0.f) eps = 1e-5f;
   int* status = nullptr;
   diffattn_status st = status_word(&status);
@@ -501,7 +509,7 @@ static diffattn_status decode_v1(const char* fn, diffattn_dtype dt, int B, int H
   p.status = status;
   const int cs = decode_cluster_size(units, n, bk);
   p.nsplit = 1;
-  if (workspace != nullptr && workspace_bytes >= diffattn_decode_workspace(B, H, d)) {
+  if (workspace != nullptr) {
     p.nsplit = decode_split(units, cs, n, bk);
     p.ws = static_cast<float*>(workspace);
   }
@@ -553,6 +561,14 @@ static diffattn_status decode_v2(const char* fn, diffattn_dtype dt, int B, int H
   const long long units = static_cast<long long>(B) * G;
   if (units * da::DecodeCfg<128, true>::MAX_CS * kMaxSplit > 0x7fffffffll)
     return fail(DIFFATTN_ERR_SHAPE, "%s: too many (batch, pair) units", fn);
+  if (workspace != nullptr) {
+    const size_t need = diffattn_v2_decode_workspace(B, Hq, d);
+    if (workspace_bytes < need)
+      return fail(DIFFATTN_ERR_SHAPE, "%s: workspace of %zu bytes, %zu needed (or pass NULL)", fn, workspace_bytes,
+                  need);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 3u) != 0)
+      return fail(DIFFATTN_ERR_ALIGN, "%s: workspace must be 4-byte aligned", fn);
+  }
   int* status = nullptr;
   diffattn_status st = status_word(&status);
   if (st != DIFFATTN_OK) return st;
@@ -582,7 +598,7 @@ static diffattn_status decode_v2(const char* fn, diffattn_dtype dt, int B, int H
   p.status = status;
   const int cs = decode_cluster_size(units, n, bk);
   p.nsplit = 1;
-  if (workspace != nullptr && workspace_bytes >= diffattn_v2_decode_workspace(B, Hq, d)) {
+  if (workspace != nullptr) {
     p.nsplit = decode_split(units, cs, n, bk);
     p.ws = static_cast<float*>(workspace);
   }

@@ -162,6 +162,8 @@ diffattn_status diffattn_forward_host(diffattn_dtype dt, int B, int H, int n, in
  *                 several thread-block clusters share a pair's keys and a second
  *                 small kernel merges their states; results are the same up
  *                 to fp32 rounding order.  Without it nothing is allocated.
+ *                 A non-NULL workspace smaller than that -> ERR_SHAPE; one
+ *                 not 4-byte aligned -> ERR_ALIGN.
  * Memory-bound: K1, K2 and V are read once (V for both maps); asynchronous
  * on `stream`.  Errors as for diffattn_forward.
  */
@@ -213,7 +215,8 @@ diffattn_status diffattn_decode_fp8k(int B, int H, int n, int d, const void* q1,
  *   softmax_scale : <= 0 selects 1/sqrt(d).
  *   out         : [B, Hq/2, d] device.
  *   workspace   : NULL, or at least diffattn_v2_decode_workspace(B, Hq, d)
- *                 bytes of device memory, as for diffattn_decode.
+ *                 bytes of device memory, as for diffattn_decode (smaller ->
+ *                 ERR_SHAPE, not 4-byte aligned -> ERR_ALIGN).
  * Asynchronous on `stream`.  Errors as for diffattn_forward.
  */
 size_t diffattn_v2_decode_workspace(int B, int Hq, int d);

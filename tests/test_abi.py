@@ -127,6 +127,29 @@ def test_decode_host_validation(L):
     assert call(k1=MIS) == da.ERR_ALIGN
 
 
+def test_decode_workspace_validation(L):
+    """A workspace that is given must be large enough and 4-byte aligned (NULL is always fine)."""
+    W = P(0x100000)
+    need1 = L.diffattn_decode_workspace(1, 2, 64)
+    need2 = L.diffattn_v2_decode_workspace(1, 4, 128)
+
+    def v1(ws=W, nbytes=need1):
+        return L.diffattn_decode(1, 1, 2, 8, 64, A, A, A, A, A, None, A, ctypes.c_float(0.2), None,
+                                 ctypes.c_float(1e-5), A, ws, nbytes, None)
+
+    def v2(ws=W, nbytes=need2):
+        return L.diffattn_v2_decode(1, 1, 4, 2, 8, 128, A, A, A, None, A, 0, ctypes.c_float(0.0), A, ws, nbytes,
+                                    None)
+
+    def v1_fp8(ws=W, nbytes=need1):
+        return L.diffattn_decode_fp8k(1, 2, 8, 64, A, A, A, A, ctypes.c_float(1.0), ctypes.c_float(1.0), A, None, A,
+                                      ctypes.c_float(0.2), None, ctypes.c_float(1e-5), A, ws, nbytes, None)
+    for call, need in ((v1, need1), (v2, need2), (v1_fp8, need1)):
+        assert call(nbytes=need - 1) == da.ERR_SHAPE
+        assert b"workspace" in L.diffattn_last_error()
+        assert call(ws=P(0x100002)) == da.ERR_ALIGN
+
+
 def test_decode_workspace_sizes(L):
     # Eight cluster states per (b, h) at most, each two maps x (maximum, sum, value-width channels), fp32.
     assert L.diffattn_decode_workspace(8, 16, 64) == 8 * 16 * 8 * 2 * (128 + 2) * 4
