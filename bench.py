@@ -4,10 +4,10 @@ A step is one DIFF V1 layer forward of the selected workload: lambda_init and
 the lambda re-parameterisation (one warp), then the fused forward (two
 softmax maps, their lambda-weighted difference times V, the per-head RMSNorm
 with (1 - lambda_init)) on inputs already resident in HBM.  For the DIFF V2
-workload a step is the V2 forward.  The default workload is the one the
-metric is normally quoted on (B4 H16 n2048 d64); ``--config`` selects
-another, and the line's ``configs`` object reports every workload measured in
-the same run.
+workload a step is the V2 forward.  The default workload is the largest one
+that fits one GPU (B1 H12 n65536 d128, causal: 4.0e13 FLOP a step);
+``--config`` selects another, and the line's ``configs`` object reports every
+workload measured in the same run.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config C]
        python bench.py --impl reference ...   (the fp64 CPU oracle, timed on
@@ -28,7 +28,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "diff-attn fwd TFLOP/s (bf16) and % of GB300 dense tensor peak; tokens/s"
-DEFAULT_CONFIG = 2
+DEFAULT_CONFIG = 4
 FLUSH_BYTES = 512 << 20  # > 129 MB L2
 
 
@@ -57,6 +57,7 @@ def hbm_bytes(w) -> float:
 KERNEL_FILES = {
     "v1-bf16-B4H16-n2048-d64": ['onepass.cuh', 'onepass_inst.cuh', 'k_onepass_v1_d64.cu', 'params.h', 'ptx.cuh', 'status.cuh'],
     "v1-bf16-B2H12-n4096-d128": ['twopass.cuh', 'twopass_inst.cuh', 'k_twopass_v1_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh'],
+    "v1-bf16-B1H12-n65536-d128": ['twopass.cuh', 'twopass_inst.cuh', 'k_twopass_v1_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh'],
     "v2-bf16-B8Hq32Hkv16-n8192-d128": ['onepass.cuh', 'onepass_inst.cuh', 'k_onepass_v2_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh'],
 }
 NCU_TRAFFIC = {  # workload: (source hash of its kernel, bytes per launch)
@@ -435,6 +436,18 @@ def run_ours(args):
         return make_v1(w, "cuda") if w.kind == "v1" else make_v2(w, "cuda")
 
     w = WORKLOADS[args.config]
+    if args.kernel_only:
+        # The forward of the workload alone (for profilers): warm-up and timed
+        # steps, nothing else launched; one short JSON line.
+        x = inputs(w)
+        res = time_device(w, x, da, args.steps, args.warmup, flush, dist)
+        if rank == 0:
+            print(json.dumps({"workload": w.name, "kernel_ms": round(res["kernel_ms"], 4),
+                              "tflops": round(flops(w) / (res["kernel_ms"] * 1e-3) / 1e12, 2),
+                              "steps": args.steps, "warmup": args.warmup}), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     sampler = ClockSampler(local)
     sampler.start()  # polls from before the warm-up to the end of the timed steps
     x = inputs(w)
@@ -456,6 +469,8 @@ def run_ours(args):
     if w.dtype == "bf16":
         roof = {"bound": "tensor", "achieved": round(kernel_tflops, 2), "peak": peaks["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(kernel_tflops / peaks["bf16_tflops"], 4),
+                "frac_of_sustained": (round(kernel_tflops / peaks["bf16_tflops_sustained"], 4)
+                                      if peaks.get("bf16_tflops_sustained") else None),
                 "traffic": ncu_traffic(w.name), "traffic_unit": "bytes per launch (ncu, cold-cache replay)",
                 "algorithmic_bytes": hbm_bytes(w), "peak_source": peaks["source"] + " (burst bf16 dense)"}
     else:
@@ -538,8 +553,13 @@ def run_reference(args):
         secs.append(last["seconds"])
     v = statistics.mean(vals)
     f_step = flops(w)
+    # A whole step of the workload would take the oracle far longer than the
+    # run: each timed step is a bounded sample, and ms_per_step is the time a
+    # full step would take at the sample's rate (extrapolated, not measured).
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": f_step / (v * 1e12) * 1e3,
+            "ms_per_step_kind": "extrapolated (full-workload FLOPs / the sampled rate)",
+            "ms_per_sampled_step": round(1e3 * statistics.mean(secs), 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1) inputs, shapes of the workload)",
             "config": {"workload": w.name, "global_batch": w.B, "seq_len": w.n, "heads": w.H or w.Hq,
@@ -659,12 +679,15 @@ def run_decode_only():
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-all-configs", action="store_true")
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="time only the workload's forward (warm-up + timed steps) and print a short line; "
+                         "the command the ncu captures run")
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the decode workloads (one JSON line with the 'decode' object)")
     ap.add_argument("--backward-only", action="store_true",
@@ -672,6 +695,14 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != world:
+        # One process per GPU: N > 1 needs a launcher (torch.distributed.run) that
+        # starts N ranks; timing one GPU under --gpus N would misreport the job.
+        sys.stderr.write(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch one process per GPU, "
+                         f"e.g. python -m torch.distributed.run --nproc-per-node {args.gpus} "
+                         f"--master-addr 127.0.0.1 bench.py --gpus {args.gpus}\n")
+        return 2
     if args.impl == "reference":
         run_reference(args)
     elif args.decode_only:
@@ -683,4 +714,4 @@ def main(argv=None):
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())
