@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
             L.diffattn_decode.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, f, vp, f, vp, vp,
                                           ctypes.c_size_t, vp]
             L.diffattn_decode.restype = i
+            L.diffattn_decode_noalloc.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, f, vp, f, vp, vp]
+            L.diffattn_decode_noalloc.restype = i
             L.diffattn_v2_decode.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, vp, ll, f, vp, vp, ctypes.c_size_t,
                                              vp]
             L.diffattn_v2_decode.restype = i
@@ -269,6 +271,37 @@ def diffattn_decode(q1, q2, k1, k2, v, lam, lambda_init_value: float, gamma=None
     _check(lib().diffattn_decode(_dt(k1), B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v),
                                  _ptr(lens), _ptr(lam), float(lambda_init_value), _ptr(gamma), float(eps),
                                  _ptr(out), wp, wn, _stream(stream)))
+    return out
+
+
+def diffattn_decode_noalloc(q1, q2, k1, k2, v, lam, lambda_init_value: float, gamma=None, eps: float = 1e-5,
+                            lens=None, out=None, stream=None) -> torch.Tensor:
+    """diffattn_decode for callers that cannot allocate device memory.
+
+    Same arguments and result as diffattn_decode with a workspace, but the
+    split states live in a fixed 4 MiB scratch inside the library (B*H at
+    most 504 pairs at d = 64, 254 at d = 128).  Calls that can overlap on the
+    GPU share that scratch and must be serialised on one stream.  ``out`` is
+    allocated here with torch when None; pass it to allocate nothing.
+    """
+    B, n, H, d = k1.shape
+    dt = k1.dtype
+    _need(q1, "q1", dt, (B, H, d))
+    _need(q2, "q2", dt, (B, H, d))
+    _need(k1, "k1", dt, (B, n, H, d))
+    _need(k2, "k2", dt, (B, n, H, d))
+    _need(v, "v", dt, (B, n, H, 2 * d))
+    _need(lam, "lambda", torch.float32, (1,))
+    if gamma is not None:
+        _need(gamma, "gamma", torch.float32, (2 * d,))
+    if lens is not None:
+        _need(lens, "lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, H, 2 * d), device=k1.device, dtype=dt)
+    _need(out, "out", dt, (B, H, 2 * d))
+    _check(lib().diffattn_decode_noalloc(_dt(k1), B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v),
+                                         _ptr(lens), _ptr(lam), float(lambda_init_value), _ptr(gamma), float(eps),
+                                         _ptr(out), _stream(stream)))
     return out
 
 

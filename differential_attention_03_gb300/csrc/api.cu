@@ -527,6 +527,68 @@ diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, c
                    gamma, eps, out, workspace, workspace_bytes, stream);
 }
 
+// ---------------------------------------------------------------- decode with no allocation
+}  // extern "C"
+
+// Scratch of diffattn_decode_noalloc: the partial softmax states of the
+// clusters that share a (batch, head) pair's keys, the same data a caller's
+// workspace holds for diffattn_decode.  A fixed array in the library's device
+// image: every GPU that loads the library keeps these 4 MiB until the process
+// exits.  Host code may not use the name as an address (it is a host-side
+// stand-in); decode_noalloc_scratch() looks the device address up.
+constexpr size_t kDecodeScratchBytes = size_t(4) << 20;
+static __device__ __align__(256) float g_decode_noalloc_scratch[kDecodeScratchBytes / sizeof(float)];
+
+namespace {
+
+// Device address of the scratch on the current device, looked up once per
+// device (the first call on a device does it, with that device current).
+diffattn_status decode_noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* ptrs[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DIFFATTN_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(mu);
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
+    ptrs[dev] = p;
+  }
+  *out = ptrs[dev];
+  return DIFFATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+diffattn_status diffattn_decode_noalloc(diffattn_dtype dt, int B, int H, int n, int d, const void* q1,
+                                        const void* q2, const void* k1, const void* k2, const void* v,
+                                        const int* lens, const float* lambda, float lambda_init,
+                                        const float* gamma, float eps, void* out, void* stream) {
+  const char* fn = "diffattn_decode_noalloc";
+  // Only calls that reach a launch need the scratch; every other call gets
+  // diffattn_decode's own answer (an argument error, or nothing to do).
+  void* scratch = nullptr;
+  if (dt == DIFFATTN_BF16 && B > 0 && H > 0 && n >= 0 && (d == 64 || d == 128)) {
+    const size_t need = diffattn_decode_workspace(B, H, d);
+    if (need > kDecodeScratchBytes)
+      return fail(DIFFATTN_ERR_SHAPE,
+                  "%s: B*H = %lld (batch, head) pairs need %zu bytes of scratch, more than the %zu it has "
+                  "(at most %zu pairs at d = %d); call diffattn_decode with a NULL workspace instead (it "
+                  "allocates nothing, and that many pairs fill the GPU without splitting)",
+                  fn, static_cast<long long>(B) * H, need, kDecodeScratchBytes,
+                  kDecodeScratchBytes / diffattn_decode_workspace(1, 1, d), d);
+    diffattn_status st = decode_noalloc_scratch(&scratch);
+    if (st != DIFFATTN_OK) return st;
+  }
+  return decode_v1(fn, dt, B, H, n, d, q1, q2, k1, k2, false, 1.f, 1.f, v, lens, lambda, lambda_init, gamma, eps,
+                   out, scratch, scratch ? kDecodeScratchBytes : 0, stream);
+}
+
 diffattn_status diffattn_decode_fp8k(int B, int H, int n, int d, const void* q1, const void* q2, const void* k1,
                                      const void* k2, float k1_scale, float k2_scale, const void* v,
                                      const int* lens, const float* lambda, float lambda_init, const float* gamma,

@@ -176,6 +176,49 @@ diffattn_status diffattn_decode(diffattn_dtype dt, int B, int H, int n, int d, c
                                 size_t workspace_bytes, void* stream);
 
 /*
+ * diffattn_decode for callers that cannot allocate device memory.  The paper
+ * has no counterpart: this is a deployment variant of the decode step above.
+ *
+ * Who needs it: the split form of diffattn_decode (several clusters share
+ * the keys of one (batch, head) pair when there are too few pairs to fill
+ * the GPU) keeps partial softmax states in a workspace that the caller
+ * allocates.  Some callers cannot: a plugin inside a host framework that
+ * owns every byte of device memory, a plain C caller with no device
+ * allocator at hand, or a serving loop that forbids cudaMalloc after
+ * start-up because it can synchronise the device and take milliseconds.
+ * This call takes no workspace; it uses a fixed scratch array compiled
+ * into the library instead, and calls no cudaMalloc, cudaFree or any
+ * other allocating routine.
+ *
+ * Same operation, arguments, layouts and errors as diffattn_decode with a
+ * workspace (bf16, d in {64, 128}), and the same result: the pairs are split
+ * over clusters exactly as diffattn_decode splits them when given one.
+ *
+ * Limits and sharing:
+ *  - the scratch holds 4 MiB (4194304 bytes) on every GPU that loads the
+ *    library, until the process exits;
+ *  - a call needs diffattn_decode_workspace(B, H, d) <= 4194304, i.e.
+ *    B*H <= 504 pairs at d = 64 and B*H <= 254 at d = 128; a larger batch is
+ *    rejected with ERR_SHAPE before anything is launched (such a batch fills
+ *    the GPU without splitting: call diffattn_decode with a NULL workspace,
+ *    which also allocates nothing);
+ *  - the first call on a device looks up the scratch's device address (once
+ *    per device, with that device current); make that first call before any
+ *    stream capture;
+ *  - every call on a device uses the same scratch, and each call writes
+ *    every value it later reads (nothing needs clearing between calls).
+ *    Calls whose kernels can overlap on the GPU (other streams, other host
+ *    threads) race on the scratch and corrupt each other's results:
+ *    serialise them on one stream.
+ */
+diffattn_status diffattn_decode_noalloc(diffattn_dtype dt, int B, int H, int n, int d,
+                                        const void* q1, const void* q2, const void* k1,
+                                        const void* k2, const void* v, const int* lens,
+                                        const float* lambda, float lambda_init,
+                                        const float* gamma, float eps, void* out,
+                                        void* stream);
+
+/*
  * diffattn_decode with the key caches in FP8 (the low-bit attention that the
  * "Differential Transformer" glossary page motivates by DIFF's smaller
  * activation outliers): k1, k2 are [B, n, H, d] device arrays of e4m3 bytes

@@ -35,7 +35,8 @@ def test_header_declares_the_entry_points():
                  "diffattn_device_status", "diffattn_last_error", "diffattn_forward_host",
                  "diffattn_forward_host_workspace", "diffattn_decode", "diffattn_v2_decode",
                  "diffattn_decode_workspace", "diffattn_v2_decode_workspace", "diffattn_decode_fp8k",
-                 "diffattn_v2_decode_fp8k", "diffattn_backward", "diffattn_backward_workspace",
+                 "diffattn_v2_decode_fp8k", "diffattn_decode_noalloc", "diffattn_backward",
+                 "diffattn_backward_workspace",
                  "lambda_reparam_backward", "diffattn_v2_backward", "diffattn_v2_backward_workspace"):
         assert want in names
 
@@ -148,6 +149,21 @@ def test_decode_workspace_validation(L):
         assert call(nbytes=need - 1) == da.ERR_SHAPE
         assert b"workspace" in L.diffattn_last_error()
         assert call(ws=P(0x100002)) == da.ERR_ALIGN
+
+
+def test_decode_noalloc_host_validation(L):
+    """The no-allocation decode rejects batches beyond its fixed scratch before any CUDA call."""
+    def call(dt=1, B=1, H=2, n=8, d=64):
+        return L.diffattn_decode_noalloc(dt, B, H, n, d, A, A, A, A, A, None, A, ctypes.c_float(0.2), None,
+                                         ctypes.c_float(1e-5), A, None)
+    assert call(B=255, H=1, d=128) == da.ERR_SHAPE      # 255 pairs x 16512 bytes > 4 MiB
+    assert b"scratch" in L.diffattn_last_error()
+    assert call(B=1, H=505, d=64) == da.ERR_SHAPE       # 505 pairs x 8320 bytes > 4 MiB
+    assert call(B=0) == da.OK
+    assert call(dt=7) == da.ERR_DTYPE
+    assert call(dt=0) == da.ERR_UNSUPPORTED
+    assert call(d=96) == da.ERR_UNSUPPORTED
+    assert call(n=-1) == da.ERR_SHAPE
 
 
 def test_decode_workspace_sizes(L):
