@@ -496,10 +496,12 @@ def run_ours(args):
                 del xc
             torch.cuda.empty_cache()
 
-    decode, backward = {}, {}
+    decode, backward, layer, fp8 = {}, {}, {}, {}
     if rank == 0 and world == 1 and not args.no_all_configs:
         decode = decode_results(da, flush, peaks)
-        backward = backward_results(da, flush, (clocks or {}).get("sm_mhz") or 2070)
+        backward = backward_results(da, flush, (clocks or {}).get("sm_mhz") or 2070, peaks)
+        layer = layer_results(da, flush, peaks)
+        fp8 = fp8_results(da, flush, peaks, inputs)
 
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -523,6 +525,10 @@ def run_ours(args):
         line["decode"] = decode
     if backward:
         line["backward"] = backward
+    if layer:
+        line["layer"] = layer
+    if fp8:
+        line["fp8"] = fp8
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(w, x)
         cb.pop("seconds", None)
@@ -571,10 +577,12 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-BACKWARD_WORKLOADS = [  # (name, B, H or (Hq, Hkv), n, d): fp32 DIFF V1 / V2 backward, causal
-    ("v1-bwd-f32-B4H16-n2048-d64", 4, 16, 2048, 64),
-    ("v1-bwd-f32-B1H1-n128-d64", 1, 1, 128, 64),
-    ("v2-bwd-f32-B2Hq32Hkv16-n2048-d128", 2, (32, 16), 2048, 128),
+BACKWARD_WORKLOADS = [  # (name, B, H or (Hq, Hkv), n, d, dtype): DIFF V1 / V2 backward, causal
+    ("v1-bwd-bf16-B4H16-n2048-d64", 4, 16, 2048, 64, "bf16"),
+    ("v2-bwd-bf16-B2Hq32Hkv16-n2048-d128", 2, (32, 16), 2048, 128, "bf16"),
+    ("v1-bwd-f32-B4H16-n2048-d64", 4, 16, 2048, 64, "f32"),
+    ("v1-bwd-f32-B1H1-n128-d64", 1, 1, 128, 64, "f32"),
+    ("v2-bwd-f32-B2Hq32Hkv16-n2048-d128", 2, (32, 16), 2048, 128, "f32"),
 ]
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 flops x the SM clock (MHz).
 FP32_LANES = 152 * 128
@@ -594,17 +602,19 @@ def backward_flops(B, H, n, d):
     return B * H * pairs * 20 * d
 
 
-def time_backward(da, flush, B, H, n, d, runs=10):
-    """fp32 DIFF V1 / V2 backward (4 kernels): median CUDA-event time, L2 flushed."""
+def time_backward(da, flush, B, H, n, d, dtype="f32", runs=10):
+    """DIFF V1 / V2 backward: median CUDA-event time, L2 flushed.  fp32 inputs run on the CUDA cores,
+    bf16 inputs on the tensor cores (statistics pass, dK/dV/dQ kernel, reductions; fp32 gradients)."""
     import torch
     g = torch.Generator(device="cuda").manual_seed(3000 + n + d)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
 
     def rnd(*shape):
-        return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32)
+        return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(tdt)
     if isinstance(H, tuple):  # DIFF V2: (Hq, Hkv), one logit per pair
         Hq, Hkv = H
         q, k, v, dy = rnd(B, n, Hq, d), rnd(B, n, Hkv, d), rnd(B, n, Hkv, d), rnd(B, n, Hq // 2, d)
-        lg = rnd(Hq // 2)
+        lg = torch.randn(Hq // 2, generator=g, device="cuda")
         ws = torch.empty(da.v2_backward_workspace_bytes(B, Hq, n, d), dtype=torch.uint8, device="cuda")
 
         def call():
@@ -635,15 +645,138 @@ def time_backward(da, flush, B, H, n, d, runs=10):
     return statistics.median(ts)
 
 
-def backward_results(da, flush, sm_mhz):
+def backward_results(da, flush, sm_mhz, peaks=None):
     out = {}
-    peak = 2 * FP32_LANES * sm_mhz * 1e6 / 1e12
-    for name, B, H, n, d in BACKWARD_WORKLOADS:
-        ms = time_backward(da, flush, B, H, n, d)
+    peaks = peaks or read_peaks()
+    peak32 = 2 * FP32_LANES * sm_mhz * 1e6 / 1e12
+    for name, B, H, n, d, dtype in BACKWARD_WORKLOADS:
+        ms = time_backward(da, flush, B, H, n, d, dtype)
         tf = backward_flops(B, H, n, d) / (ms * 1e-3) / 1e12
-        out[name] = {"ms": round(ms, 4), "tflops": round(tf, 3), "bound": "alu",
-                     "peak_tflops": round(peak, 1), "peak": f"fp32 FMA: {FP32_LANES} lanes x 2 x {sm_mhz} MHz",
-                     "frac": round(tf / peak, 4), "tokens_per_s": round(B * n / (ms * 1e-3), 1)}
+        if dtype == "bf16":
+            out[name] = {"ms": round(ms, 4), "tflops": round(tf, 2), "bound": "tensor",
+                         "peak_tflops": peaks["bf16_tflops"], "peak": "measured burst bf16 dense",
+                         "frac": round(tf / peaks["bf16_tflops"], 4), "tokens_per_s": round(B * n / (ms * 1e-3), 1)}
+        else:
+            out[name] = {"ms": round(ms, 4), "tflops": round(tf, 3), "bound": "alu",
+                         "peak_tflops": round(peak32, 1), "peak": f"fp32 FMA: {FP32_LANES} lanes x 2 x {sm_mhz} MHz",
+                         "frac": round(tf / peak32, 4), "tokens_per_s": round(B * n / (ms * 1e-3), 1)}
+    return out
+
+
+LAYER_WORKLOADS = [  # (name, kind, B, n, D, H or (Hq, Hkv), d): attention layers around the operator, causal
+    ("v1-layer-bf16-B2-n4096-D3072-H12-d128", "v1", 2, 4096, 3072, 12, 128),
+    ("v2-layer-bf16-B2-n8192-D2048-Hq32Hkv16-d128", "v2", 2, 8192, 2048, (32, 16), 128),
+]
+PROJECTION_WORKLOADS = [  # (name, M, N, K): c = a w^T alone
+    ("projection-bf16-8192x8192x8192", 8192, 8192, 8192),
+    ("projection-bf16-8192x9216x3072", 8192, 9216, 3072),
+]
+
+
+def fp8_results(da, flush, peaks, inputs):
+    """The V1 forward with e4m3 queries and keys (one scale per tensor, amax / 448) on the d = 128
+    workloads: TFLOP/s (the same algorithmic FLOPs as bf16) against the measured burst bf16 peak."""
+    import torch
+    from differential_attention_03_gb300.inputs import WORKLOADS
+    out = {}
+    for wid in (3, 4):
+        w = WORKLOADS[wid]
+        x = inputs(w)
+        codes, scales = [], []
+        for k in ("q1", "q2", "k1", "k2"):
+            sc = float(x[k].float().abs().max()) / 448.0
+            codes.append((x[k].float() / sc).to(torch.float8_e4m3fn))
+            scales.append(sc)
+            del x[k]
+        lin = da.lambda_init(w.layer)
+        lam = da.lambda_reparam(x["lq1"], x["lk1"], x["lq2"], x["lk2"], lin)
+        y = torch.empty(x["v"].shape, device="cuda", dtype=torch.bfloat16)
+
+        def call():
+            da.diffattn_forward_fp8qk(*codes, scales, x["v"], lam, lin, gamma=x["gamma"], causal=w.causal, out=y)
+        ms = _median_ms(call, flush, runs=5 if wid == 4 else 10)
+        da.device_status()
+        tf = flops(w) / (ms * 1e-3) / 1e12
+        out["fp8qk-" + w.name] = {"ms": round(ms, 4), "tflops": round(tf, 2),
+                                  "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                                  "tokens_per_s": round(w.B * w.n / (ms * 1e-3), 1)}
+        del codes, x, y
+        torch.cuda.empty_cache()
+    return out
+
+
+def layer_flops(kind, B, n, D, H, d):
+    """Algorithmic FLOPs of one layer forward: the two projections (2 M K N each) plus the operator
+    (V1 12 n^2 d per (b, h), V2 4 n^2 d per query head; halved for causal)."""
+    M = B * n
+    if kind == "v1":
+        return 2.0 * M * D * 6 * H * d + 6.0 * n * n * d * B * H + 2.0 * M * 2 * H * d * D
+    Hq, Hkv = H
+    G = Hq // 2
+    return 2.0 * M * D * ((Hq + 2 * Hkv) * d + G) + 2.0 * n * n * d * B * Hq + 2.0 * M * G * d * D
+
+
+def _median_ms(call, flush, runs=10):
+    import torch
+    for _ in range(3):
+        call()
+    ts = []
+    for _ in range(runs):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def layer_results(da, flush, peaks):
+    """Attention layers (projections, operator, W^O) and the projection GEMM alone: TFLOP/s against the
+    measured burst bf16 peak."""
+    import torch
+    out = {}
+    g = torch.Generator(device="cuda").manual_seed(4242)
+
+    def rnd(*shape, scale=1.0):
+        return (scale * torch.randn(shape, generator=g, device="cuda")).to(torch.bfloat16)
+    for name, kind, B, n, D, H, d in LAYER_WORKLOADS:
+        x = rnd(B, n, D)
+        if kind == "v1":
+            w_qkv, w_o = rnd(6 * H * d, D, scale=D ** -0.5), rnd(D, 2 * H * d, scale=(2 * H * d) ** -0.5)
+            lv = [0.1 * torch.randn(d, generator=g, device="cuda") for _ in range(4)]
+            ws = torch.empty(da.layer_workspace_bytes(B, n, H, d), dtype=torch.uint8, device="cuda")
+            y = torch.empty((B, n, D), device="cuda", dtype=torch.bfloat16)
+
+            def call():
+                da.layer_forward(x, w_qkv, w_o, *lv, 0.7, H, out=y, workspace=ws)
+        else:
+            Hq, Hkv = H
+            w = rnd((Hq + 2 * Hkv) * d + Hq // 2, D, scale=D ** -0.5)
+            w_o = rnd(D, Hq // 2 * d, scale=(Hq // 2 * d) ** -0.5)
+            ws = torch.empty(da.v2_layer_workspace_bytes(B, n, Hq, Hkv, d), dtype=torch.uint8, device="cuda")
+            y = torch.empty((B, n, D), device="cuda", dtype=torch.bfloat16)
+
+            def call():
+                da.v2_layer_forward(x, w, w_o, Hq, Hkv, out=y, workspace=ws)
+        ms = _median_ms(call, flush)
+        da.device_status()
+        tf = layer_flops(kind, B, n, D, H, d) / (ms * 1e-3) / 1e12
+        out[name] = {"ms": round(ms, 4), "tflops": round(tf, 2), "frac": round(tf / peaks["bf16_tflops"], 4),
+                     "tokens_per_s": round(B * n / (ms * 1e-3), 1), "bound": "tensor"}
+        del x, ws, y
+        torch.cuda.empty_cache()
+    for name, M, N, K in PROJECTION_WORKLOADS:
+        a, w = rnd(M, K), rnd(N, K)
+        c = torch.empty((M, N), device="cuda", dtype=torch.bfloat16)
+        ms = _median_ms(lambda: da.projection(a, w, out=c), flush)
+        da.device_status()
+        tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        out[name] = {"ms": round(ms, 4), "tflops": round(tf, 2), "frac": round(tf / peaks["bf16_tflops"], 4),
+                     "bound": "tensor"}
+        del a, w, c
+        torch.cuda.empty_cache()
     return out
 
 
@@ -665,6 +798,18 @@ def run_backward_only():
     da.lib()
     flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
     print(json.dumps({"backward": backward_results(da, flush, 2070)}), flush=True)
+
+
+def run_layer_only():
+    import torch
+    from differential_attention_03_gb300 import binding as da, build
+    build.build()
+    da.lib()
+    flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
+    from differential_attention_03_gb300.inputs import make_v1
+    peaks = read_peaks()
+    print(json.dumps({"layer": layer_results(da, flush, peaks),
+                      "fp8": fp8_results(da, flush, peaks, lambda w: make_v1(w, "cuda"))}), flush=True)
 
 
 def run_decode_only():
@@ -690,6 +835,8 @@ def main(argv=None):
                          "the command the ncu captures run")
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the decode workloads (one JSON line with the 'decode' object)")
+    ap.add_argument("--layer-only", action="store_true",
+                    help="time only the attention layers, the projection GEMM and the FP8 forward (one JSON line)")
     ap.add_argument("--backward-only", action="store_true",
                     help="time only the fp32 backward workloads (one JSON line with the 'backward' object)")
     args = ap.parse_args(argv)
@@ -709,6 +856,8 @@ def main(argv=None):
         run_decode_only()
     elif args.backward_only:
         run_backward_only()
+    elif args.layer_only:
+        run_layer_only()
     else:
         run_ours(args)
 

@@ -89,6 +89,19 @@ def lib() -> ctypes.CDLL:
             L.lambda_reparam_backward.restype = i
             L.diffattn_v2_forward.argtypes = [i, i, i, i, i, i, vp, vp, vp, vp, ll, ll, f, i, vp, vp]
             L.diffattn_v2_forward.restype = i
+            L.diffattn_forward_fp8qk.argtypes = [i, i, i, i, vp, vp, vp, vp, f, f, f, f, vp, vp, f, vp, f, i, vp, vp]
+            L.diffattn_forward_fp8qk.restype = i
+            L.diffattn_projection.argtypes = [i, i, i, vp, vp, vp, vp]
+            L.diffattn_projection.restype = i
+            L.diffattn_layer_workspace.argtypes = [i, i, i, i]
+            L.diffattn_layer_workspace.restype = ctypes.c_size_t
+            L.diffattn_layer_forward.argtypes = [i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, f, vp, f, i, vp, vp,
+                                                 ctypes.c_size_t, vp]
+            L.diffattn_layer_forward.restype = i
+            L.diffattn_v2_layer_workspace.argtypes = [i, i, i, i, i]
+            L.diffattn_v2_layer_workspace.restype = ctypes.c_size_t
+            L.diffattn_v2_layer_forward.argtypes = [i, i, i, i, i, i, vp, vp, vp, i, vp, vp, ctypes.c_size_t, vp]
+            L.diffattn_v2_layer_forward.restype = i
             L.diffattn_device_status.argtypes = [vp]
             L.diffattn_device_status.restype = i
             L.diffattn_last_error.argtypes = []
@@ -172,6 +185,32 @@ def diffattn_forward(q1, q2, k1, k2, v, lam, lambda_init_value: float, gamma=Non
     _check(lib().diffattn_forward(_dt(q1), B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v),
                                   _ptr(lam), float(lambda_init_value), _ptr(gamma), float(eps),
                                   1 if causal else 0, _ptr(out), _stream(stream)))
+    return out
+
+
+def diffattn_forward_fp8qk(q1, q2, k1, k2, scales, v, lam, lambda_init_value: float, gamma=None, eps: float = 1e-5,
+                           causal: bool = True, out=None, stream=None) -> torch.Tensor:
+    """DIFF V1 forward with e4m3 queries and keys (QK^T on the FP8 tensor-core path).
+
+    q1, q2, k1, k2: [B, n, H, 128] e4m3 codes (torch.float8_e4m3fn or their bytes as uint8) of
+    Q_r / q_scale_r and K_r / k_scale_r; scales = (q1_scale, q2_scale, k1_scale, k2_scale).  The
+    result is diffattn_forward's for Q_r = q_scale_r e4m3(q_r), K_r = k_scale_r e4m3(k_r); v bf16
+    [B, n, H, 256].  Returns out [B, n, H, 256] bf16.
+    """
+    B, n, H, d = q1.shape
+    for name, t in (("q1", q1), ("q2", q2), ("k1", k1), ("k2", k2)):
+        _need_fp8(t, name, (B, n, H, d))
+    _need(v, "v", torch.bfloat16, (B, n, H, 2 * d))
+    _need(lam, "lambda", torch.float32, (1,))
+    if gamma is not None:
+        _need(gamma, "gamma", torch.float32, (2 * d,))
+    if out is None:
+        out = torch.empty((B, n, H, 2 * d), device=v.device, dtype=torch.bfloat16)
+    _need(out, "out", torch.bfloat16, (B, n, H, 2 * d))
+    s1, s2, s3, s4 = (float(x) for x in scales)
+    _check(lib().diffattn_forward_fp8qk(B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), s1, s2, s3, s4, _ptr(v),
+                                        _ptr(lam), float(lambda_init_value), _ptr(gamma), float(eps),
+                                        1 if causal else 0, _ptr(out), _stream(stream)))
     return out
 
 
@@ -412,15 +451,16 @@ def backward_workspace_bytes(B: int, H: int, n: int, d: int) -> int:
 
 def diffattn_backward(q1, q2, k1, k2, v, lam, lambda_init_value: float, dy, gamma=None, eps: float = 1e-5,
                       causal: bool = True, workspace=None, stream=None) -> dict:
-    """DIFF V1 backward (fp32): gradients of diffattn_forward's output given dy.
+    """DIFF V1 backward: gradients of diffattn_forward's output given dy.
 
-    Shapes as for diffattn_forward (fp32, d <= 128); dy: [B, n, H, 2d].
-    Returns a dict: dq1, dq2, dk1, dk2, dv (like their inputs), dlam [1],
-    dgamma [2d].  workspace: None (allocated here with torch) or a device
-    tensor of backward_workspace_bytes(B, H, n, d) bytes.
+    Shapes as for diffattn_forward; fp32 inputs (d <= 128, CUDA cores) or bf16
+    inputs (d = 64, tensor cores); dy: [B, n, H, 2d] in the inputs' dtype.
+    Returns a dict of fp32 gradients: dq1, dq2, dk1, dk2, dv (shaped like
+    their inputs), dlam [1], dgamma [2d].  workspace: None (allocated here
+    with torch) or a device tensor of backward_workspace_bytes(B, H, n, d) bytes.
     """
     B, n, H, d = q1.shape
-    dt = torch.float32
+    dt = q1.dtype
     for name, t, shp in (("q1", q1, (B, n, H, d)), ("q2", q2, (B, n, H, d)), ("k1", k1, (B, n, H, d)),
                          ("k2", k2, (B, n, H, d)), ("v", v, (B, n, H, 2 * d)), ("dy", dy, (B, n, H, 2 * d))):
         _need(t, name, dt, shp)
@@ -431,10 +471,11 @@ def diffattn_backward(q1, q2, k1, k2, v, lam, lambda_init_value: float, dy, gamm
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q1.device)
     wp, wn = _ws_args(workspace, need)
-    g = {k: torch.empty_like(t) for k, t in (("dq1", q1), ("dq2", q2), ("dk1", k1), ("dk2", k2), ("dv", v))}
+    g = {k: torch.empty(t.shape, device=t.device, dtype=torch.float32)
+         for k, t in (("dq1", q1), ("dq2", q2), ("dk1", k1), ("dk2", k2), ("dv", v))}
     g["dlam"] = torch.empty(1, device=q1.device, dtype=torch.float32)
     g["dgamma"] = torch.empty(2 * d, device=q1.device, dtype=torch.float32)
-    _check(lib().diffattn_backward(F32, B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v), _ptr(lam),
+    _check(lib().diffattn_backward(_dt(q1), B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v), _ptr(lam),
                                    float(lambda_init_value), _ptr(gamma), float(eps), 1 if causal else 0, _ptr(dy),
                                    _ptr(g["dq1"]), _ptr(g["dq2"]), _ptr(g["dk1"]), _ptr(g["dk2"]), _ptr(g["dv"]),
                                    _ptr(g["dlam"]), _ptr(g["dgamma"]), wp, wn, _stream(stream)))
@@ -447,36 +488,39 @@ def v2_backward_workspace_bytes(B: int, Hq: int, n: int, d: int) -> int:
 
 def diffattn_v2_backward(q, k, v, lam_logits, dy, causal: bool = True, softmax_scale: float = 0.0,
                          workspace=None, stream=None) -> dict:
-    """DIFF V2 backward (fp32): gradients of diffattn_v2_forward's output given dy.
+    """DIFF V2 backward: gradients of diffattn_v2_forward's output given dy.
 
-    q: [B, n, Hq, d]; k, v: [B, n, Hkv, d]; dy: [B, n, Hq/2, d]; lam_logits:
+    q: [B, n, Hq, d]; k, v: [B, n, Hkv, d]; dy: [B, n, Hq/2, d], all fp32
+    (d <= 128, CUDA cores) or all bf16 (d = 128, tensor cores); lam_logits:
     fp32 [B, n, Hq/2] (per token), [B, Hq/2] (per sequence) or [Hq/2] (per
-    pair).  Returns a dict: dq, dk, dv and dlogits (shaped like lam_logits).
+    pair).  Returns a dict of fp32 gradients: dq, dk, dv and dlogits (shaped
+    like lam_logits).
     """
     B, n, Hq, d = q.shape
     Hkv = k.shape[2]
-    dt = torch.float32
+    dt = q.dtype
     _need(q, "q", dt, (B, n, Hq, d))
     _need(k, "k", dt, (B, n, Hkv, d))
     _need(v, "v", dt, (B, n, Hkv, d))
     _need(dy, "dy", dt, (B, n, Hq // 2, d))
     G = Hq // 2
+    f32 = torch.float32
     if lam_logits.dim() == 3:
-        _need(lam_logits, "lam_logits", dt, (B, n, G))
+        _need(lam_logits, "lam_logits", f32, (B, n, G))
         sb, st = n * G, G
     elif lam_logits.dim() == 2:
-        _need(lam_logits, "lam_logits", dt, (B, G))
+        _need(lam_logits, "lam_logits", f32, (B, G))
         sb, st = G, 0
     else:
-        _need(lam_logits, "lam_logits", dt, (G,))
+        _need(lam_logits, "lam_logits", f32, (G,))
         sb, st = 0, 0
     need = v2_backward_workspace_bytes(B, Hq, n, d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     wp, wn = _ws_args(workspace, need)
-    g = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
-         "dlogits": torch.empty_like(lam_logits)}
-    _check(lib().diffattn_v2_backward(F32, B, Hq, Hkv, n, d, _ptr(q), _ptr(k), _ptr(v), _ptr(lam_logits), sb, st,
+    g = {"dq": torch.empty(q.shape, device=q.device, dtype=f32), "dk": torch.empty(k.shape, device=q.device, dtype=f32),
+         "dv": torch.empty(v.shape, device=q.device, dtype=f32), "dlogits": torch.empty_like(lam_logits)}
+    _check(lib().diffattn_v2_backward(_dt(q), B, Hq, Hkv, n, d, _ptr(q), _ptr(k), _ptr(v), _ptr(lam_logits), sb, st,
                                       float(softmax_scale), 1 if causal else 0, _ptr(dy), _ptr(g["dq"]),
                                       _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dlogits"]), wp, wn, _stream(stream)))
     return g
@@ -522,6 +566,83 @@ def diffattn_v2_forward(q, k, v, lam_logits, causal: bool = True, softmax_scale:
     _check(lib().diffattn_v2_forward(_dt(q), B, Hq, Hkv, n, d, _ptr(q), _ptr(k), _ptr(v), _ptr(lam_logits),
                                      sb, st, float(softmax_scale), 1 if causal else 0, _ptr(out),
                                      _stream(stream)))
+    return out
+
+
+def projection(a, w, out=None, stream=None) -> torch.Tensor:
+    """out = a w^T on the tensor cores: a [M, K], w [N, K] (bf16; K, N multiples of 8) -> [M, N] bf16."""
+    M, K = a.shape
+    N = w.shape[0]
+    _need(a, "a", torch.bfloat16, (M, K))
+    _need(w, "w", torch.bfloat16, (N, K))
+    if out is None:
+        out = torch.empty((M, N), device=a.device, dtype=torch.bfloat16)
+    _need(out, "out", torch.bfloat16, (M, N))
+    _check(lib().diffattn_projection(M, N, K, _ptr(a), _ptr(w), _ptr(out), _stream(stream)))
+    return out
+
+
+def layer_workspace_bytes(B: int, n: int, H: int, d: int) -> int:
+    return int(lib().diffattn_layer_workspace(B, n, H, d))
+
+
+def layer_forward(x, w_qkv, w_o, lq1, lk1, lq2, lk2, lambda_init_value: float, H: int, gamma=None,
+                  eps: float = 1e-5, causal: bool = True, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """DIFF V1 attention layer: X [W^Q | W^K | W^V], the operator with the per-head norm, W^O.
+
+    x: [B, n, D] bf16; w_qkv: [3 H 2d, D] bf16 (rows: W^Q's columns, then W^K's, then W^V's; head i's
+    2d columns of W^Q hold Q_1 then Q_2); w_o: [D, H 2d] bf16; lq1..lk2: fp32 [d]; gamma: fp32 [2d] or
+    None.  workspace: a device tensor of layer_workspace_bytes(B, n, H, d) bytes (allocated here if
+    None).  Returns out [B, n, D] bf16.
+    """
+    B, n, D = x.shape
+    d = w_qkv.shape[0] // (6 * H)
+    _need(x, "x", torch.bfloat16, (B, n, D))
+    _need(w_qkv, "w_qkv", torch.bfloat16, (6 * H * d, D))
+    _need(w_o, "w_o", torch.bfloat16, (D, 2 * H * d))
+    for name, t in (("lq1", lq1), ("lk1", lk1), ("lq2", lq2), ("lk2", lk2)):
+        _need(t, name, torch.float32, (d,))
+    if gamma is not None:
+        _need(gamma, "gamma", torch.float32, (2 * d,))
+    if out is None:
+        out = torch.empty((B, n, D), device=x.device, dtype=torch.bfloat16)
+    _need(out, "out", torch.bfloat16, (B, n, D))
+    need = layer_workspace_bytes(B, n, H, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    wp, wn = _ws_args(workspace, need)
+    _check(lib().diffattn_layer_forward(B, n, D, H, d, _ptr(x), _ptr(w_qkv), _ptr(w_o), _ptr(lq1), _ptr(lk1),
+                                        _ptr(lq2), _ptr(lk2), float(lambda_init_value), _ptr(gamma), float(eps),
+                                        1 if causal else 0, _ptr(out), wp, wn, _stream(stream)))
+    return out
+
+
+def v2_layer_workspace_bytes(B: int, n: int, Hq: int, Hkv: int, d: int) -> int:
+    return int(lib().diffattn_v2_layer_workspace(B, n, Hq, Hkv, d))
+
+
+def v2_layer_forward(x, w_qkvl, w_o, Hq: int, Hkv: int, causal: bool = True, out=None, workspace=None,
+                     stream=None) -> torch.Tensor:
+    """DIFF V2 attention layer: X [W^Q | W^K | W^V | W^lambda], the V2 operator, W^O.
+
+    x: [B, n, D] bf16; w_qkvl: [(Hq + 2 Hkv) d + Hq/2, D] bf16 (rows: W^Q's columns, W^K's, W^V's,
+    then the Hq/2 pair-logit columns of W^lambda); w_o: [D, Hq/2 d] bf16.  Returns out [B, n, D].
+    """
+    B, n, D = x.shape
+    G = Hq // 2
+    d = (w_qkvl.shape[0] - G) // (Hq + 2 * Hkv)
+    _need(x, "x", torch.bfloat16, (B, n, D))
+    _need(w_qkvl, "w_qkvl", torch.bfloat16, ((Hq + 2 * Hkv) * d + G, D))
+    _need(w_o, "w_o", torch.bfloat16, (D, G * d))
+    if out is None:
+        out = torch.empty((B, n, D), device=x.device, dtype=torch.bfloat16)
+    _need(out, "out", torch.bfloat16, (B, n, D))
+    need = v2_layer_workspace_bytes(B, n, Hq, Hkv, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    wp, wn = _ws_args(workspace, need)
+    _check(lib().diffattn_v2_layer_forward(B, n, D, Hq, Hkv, d, _ptr(x), _ptr(w_qkvl), _ptr(w_o),
+                                           1 if causal else 0, _ptr(out), wp, wn, _stream(stream)))
     return out
 
 

@@ -13,7 +13,9 @@
 #include <string>
 
 #include "bwd_params.h"
+#include "bwd_tc_params.h"
 #include "decode.cuh"
+#include "gemm_params.h"
 #include "diffattn.h"
 #include "launch.h"
 
@@ -105,17 +107,21 @@ diffattn_status get_encoder(EncodeTiledFn* fn) {
   return DIFFATTN_OK;
 }
 
-// 4-D map over a BSHD bf16 tensor [B, n, heads, W]; box = `cols` columns x 1
-// head x `rows` tokens x 1 batch, the swizzle as wide as a box row (64 or 128
-// bytes); loads past n return zeros, stores past n are dropped.
-diffattn_status make_map_box(CUtensorMap* m, const void* base, int B, int n, int heads, int W, int cols, int rows) {
+// 4-D map over a BSHD bf16 view [B, n, heads, W]: W columns of each head,
+// heads `head_stride` elements apart, tokens `token_stride` elements apart
+// (e.g. the query map of one attention head inside a fused projection
+// output); box = `cols` columns x 1 head x `rows` tokens x 1 batch, the
+// swizzle as wide as a box row (64 or 128 bytes); loads past n return zeros,
+// stores past n are dropped.
+diffattn_status make_map_view(CUtensorMap* m, const void* base, int B, int n, int heads, int W, long long head_stride,
+                              long long token_stride, int cols, int rows) {
   EncodeTiledFn enc;
   diffattn_status s = get_encoder(&enc);
   if (s != DIFFATTN_OK) return s;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(heads),
                               static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(B)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(W) * 2, static_cast<cuuint64_t>(W) * heads * 2,
-                                 static_cast<cuuint64_t>(W) * heads * n * 2};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(head_stride) * 2, static_cast<cuuint64_t>(token_stride) * 2,
+                                 static_cast<cuuint64_t>(token_stride) * n * 2};
   const cuuint32_t box[4] = {static_cast<cuuint32_t>(cols), 1, static_cast<cuuint32_t>(rows), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapSwizzle sw = (cols * 2 == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
@@ -123,6 +129,32 @@ diffattn_status make_map_box(CUtensorMap* m, const void* base, int B, int n, int
                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(DIFFATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  return DIFFATTN_OK;
+}
+
+// 4-D map over a contiguous BSHD bf16 tensor [B, n, heads, W]; box = `cols`
+// columns x 1 head x `rows` tokens x 1 batch, the swizzle as wide as a box row
+// (64 or 128 bytes); loads past n return zeros, stores past n are dropped.
+diffattn_status make_map_box(CUtensorMap* m, const void* base, int B, int n, int heads, int W, int cols, int rows) {
+  return make_map_view(m, base, B, n, heads, W, W, static_cast<long long>(W) * heads, cols, rows);
+}
+
+// 2-D map over a row-major bf16 matrix [rows, cols] with row stride `ld`
+// elements: box = 64 columns (128 bytes, 128-byte swizzle) x `box_rows` rows;
+// loads past either edge return zeros.
+diffattn_status make_map_2d(CUtensorMap* m, const void* base, long long rows, long long cols, long long ld,
+                            int box_rows) {
+  EncodeTiledFn enc;
+  diffattn_status s = get_encoder(&enc);
+  if (s != DIFFATTN_OK) return s;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DIFFATTN_ERR_CUDA, "cuTensorMapEncodeTiled (2-D) failed (CUresult %d)", (int)r);
   return DIFFATTN_OK;
 }
 
@@ -160,6 +192,126 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int pick_order(long long units, long long n, int kv_row_bytes) {
   const long long total = units * n * kv_row_bytes;
   return total > (96ll << 20) ? 0 : 1;
+}
+
+// Where the inputs of one bf16 forward live: BSHD views, each a base pointer
+// with head and token strides in elements (contiguous tensors, or the
+// columns of one head inside a fused projection output).
+struct QKVViews {
+  const void* q1;
+  const void* q2;
+  const void* k1;
+  const void* k2;
+  const void* v;
+  long long q_head, q_tok;  // strides of q1, q2
+  long long k_head, k_tok;  // strides of k1, k2
+  long long v_head, v_tok;  // strides of v
+};
+
+// Fills a V1 tcgen05 launch around its input maps (already in p) and
+// launches it: sc1 / sc2 are the two maps' softmax scales x log2(e); f8
+// selects the kernel that reads e4m3 queries and keys.  `out` is a
+// contiguous [B, n, H, 2d] tensor.
+diffattn_status launch_v1_tc(const char* fn, da::TwoPassParams& p, bool f8, int B, int H, int n, int d, float sc1,
+                             float sc2, const float* lambda, float lambda_init, const float* gamma, float eps,
+                             int causal, void* out, int* status, cudaStream_t s) {
+  const int dv = 2 * d;
+  diffattn_status st;
+  // Output stores: boxes of 128 tokens x 32 channels.
+  if ((st = make_map_box(&p.tm_out, out, B, n, H, dv, 32, 128)) != DIFFATTN_OK) return st;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lambda = lambda;
+  p.gamma = gamma;
+  p.lam_logits = nullptr;
+  p.scale_log2 = sc1;
+  p.scale2_log2 = sc2;
+  p.norm_mult = 1.f - lambda_init;
+  p.eps = eps;
+  p.B = B;
+  p.n = n;
+  p.causal = causal ? 1 : 0;
+  p.units_per_batch = H;
+  p.group = 1;
+  p.num_q_tiles = (n + 127) / 128;
+  p.order = pick_order(static_cast<long long>(B) * H, n, (2 * d + dv) * 2);
+  p.status = status;
+  const long long grid = static_cast<long long>(p.num_q_tiles) * B * H;
+  if (grid > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "%s: too many tiles", fn);
+  // d = 64 (value width 128): one sweep with two online-softmax states fits
+  // TMEM; d = 128 (value width 256) does not, and sweeps the keys twice.
+  // Short items (up to 64 query tiles per head): one persistent CTA per SM,
+  // so each item's start overlaps the previous one's end.  Long items: one
+  // CTA per item (the fixed cost is small against them, and the hardware's
+  // dynamic CTA scheduling balances them; measured faster).
+  const bool persist = p.num_q_tiles <= 64;
+  const int g = static_cast<int>(persist ? persistent_grid(grid) : grid);
+  cudaError_t e = f8 ? da::launch_twopass_v1_d128_f8(p, g, persist, s)
+                     : (d == 64) ? da::launch_onepass_v1_d64(p, g, persist, s)
+                                 : da::launch_twopass_v1_d128(p, g, persist, s);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  g_launches.fetch_add(1);
+  return DIFFATTN_OK;
+}
+
+// DIFF V1 bf16 forward (tcgen05 kernels) on already validated views; `out`
+// is a contiguous [B, n, H, 2d] tensor.
+diffattn_status forward_v1_bf16(const char* fn, const QKVViews& x, int B, int H, int n, int d, const float* lambda,
+                                float lambda_init, const float* gamma, float eps, int causal, void* out, int* status,
+                                cudaStream_t s) {
+  const int dv = 2 * d;
+  da::TwoPassParams p;
+  memset(&p, 0, sizeof(p));
+  diffattn_status st;
+  // Query and key tiles are 128 rows; a value tile is split into two 64-row ring slots.
+  if ((st = make_map_view(&p.tm_q1, x.q1, B, n, H, d, x.q_head, x.q_tok, 64, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_view(&p.tm_q2, x.q2, B, n, H, d, x.q_head, x.q_tok, 64, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_view(&p.tm_k1, x.k1, B, n, H, d, x.k_head, x.k_tok, 64, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_view(&p.tm_k2, x.k2, B, n, H, d, x.k_head, x.k_tok, 64, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_view(&p.tm_v, x.v, B, n, H, dv, x.v_head, x.v_tok, 64, 64)) != DIFFATTN_OK) return st;
+  const float sc = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  return launch_v1_tc(fn, p, false, B, H, n, d, sc, sc, lambda, lambda_init, gamma, eps, causal, out, status, s);
+}
+
+// DIFF V2 bf16 forward (d = 128) on already validated views of q (Hq heads)
+// and k, v (Hkv heads); `out` is a contiguous [B, n, Hq / 2, d] tensor.
+diffattn_status forward_v2_bf16(const char* fn, const QKVViews& x, int B, int Hq, int Hkv, int n, int d,
+                                const float* lam_logits, long long sb, long long st_, float scale, int causal,
+                                void* out, int* status, cudaStream_t s) {
+  const int G = Hq / 2;
+  da::TwoPassParams p;
+  memset(&p, 0, sizeof(p));
+  diffattn_status st;
+  if ((st = make_map_view(&p.tm_q1, x.q1, B, n, Hq, d, x.q_head, x.q_tok, 64, 128)) != DIFFATTN_OK) return st;
+  p.tm_q2 = p.tm_q1;
+  // Key and value tiles are 128 rows (one ring slot each).
+  if ((st = make_map_view(&p.tm_k1, x.k1, B, n, Hkv, d, x.k_head, x.k_tok, 64, 128)) != DIFFATTN_OK) return st;
+  p.tm_k2 = p.tm_k1;
+  if ((st = make_map_view(&p.tm_v, x.v, B, n, Hkv, d, x.v_head, x.v_tok, 64, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_box(&p.tm_out, out, B, n, G, d, 32, 128)) != DIFFATTN_OK) return st;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lam_logits = lam_logits;
+  p.sb = sb;
+  p.st = st_;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 * scale);
+  p.norm_mult = 1.f;
+  p.eps = 0.f;
+  p.B = B;
+  p.n = n;
+  p.causal = causal ? 1 : 0;
+  p.units_per_batch = G;
+  p.group = Hq / Hkv;
+  p.num_q_tiles = (n + 127) / 128;
+  // K/V bytes per pair: the pairs of one KV head share its stream.
+  p.order = pick_order(static_cast<long long>(B) * Hkv, n, 2 * d * 2);
+  p.status = status;
+  const long long grid = static_cast<long long>(p.num_q_tiles) * B * G;
+  if (grid > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "%s: too many tiles", fn);
+  // V2 items are long (up to n / 128 key tiles): one CTA per item, so the
+  // hardware's dynamic CTA scheduling balances them (measured faster here).
+  cudaError_t e = da::launch_onepass_v2_d128(p, static_cast<int>(grid), s);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  g_launches.fetch_add(1);
+  return DIFFATTN_OK;
 }
 
 }  // namespace
@@ -235,44 +387,49 @@ diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d, 
     return fail(DIFFATTN_ERR_ALIGN, "diffattn_forward: bf16 tensors must be 16-byte aligned");
   diffattn_status st = status_word(&status);
   if (st != DIFFATTN_OK) return st;
+  const long long Hd = static_cast<long long>(H) * d;
+  const QKVViews x{q1, q2, k1, k2, v, d, Hd, d, Hd, dv, 2 * Hd};
+  if ((st = forward_v1_bf16("diffattn_forward (bf16)", x, B, H, n, d, lambda, lambda_init, gamma, eps, causal, out,
+                            status, s)) != DIFFATTN_OK)
+    return st;
+  return ok();
+}
+
+// ---------------------------------------------------------------- forward with e4m3 queries and keys
+diffattn_status diffattn_forward_fp8qk(int B, int H, int n, int d, const void* q1, const void* q2, const void* k1,
+                                       const void* k2, float q1_scale, float q2_scale, float k1_scale,
+                                       float k2_scale, const void* v, const float* lambda, float lambda_init,
+                                       const float* gamma, float eps, int causal, void* out, void* stream) {
+  const char* fn = "diffattn_forward_fp8qk";
+  if (B < 0 || H < 0 || n < 0 || d < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: bad sizes B=%d H=%d n=%d d=%d", fn, B, H, n, d);
+  if (d != 128) return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: d = 128 only (got %d)", fn, d);
+  if (B == 0 || H == 0 || n == 0) return ok();
+  if (!q1 || !q2 || !k1 || !k2 || !v || !lambda || !out) return fail(DIFFATTN_ERR_NULL, "%s: NULL pointer", fn);
+  if (!std::isfinite(lambda_init)) return fail(DIFFATTN_ERR_SHAPE, "%s: lambda_init not finite", fn);
+  for (float sc : {q1_scale, q2_scale, k1_scale, k2_scale})
+    if (!(std::isfinite(sc) && sc > 0.f)) return fail(DIFFATTN_ERR_SHAPE, "%s: scales must be finite and positive", fn);
+  if (!aligned16(q1) || !aligned16(q2) || !aligned16(k1) || !aligned16(k2) || !aligned16(v) || !aligned16(out))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  if (eps <= 0.f) eps = 1e-5f;
+  int* status = nullptr;
+  diffattn_status st = status_word(&status);
+  if (st != DIFFATTN_OK) return st;
+  const int dv = 2 * d;
   da::TwoPassParams p;
   memset(&p, 0, sizeof(p));
-  if ((st = make_map(&p.tm_q1, q1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
-  if ((st = make_map(&p.tm_q2, q2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
-  // Query and key tiles are 128 rows; a value tile is split into two 64-row ring slots.
-  if ((st = make_map(&p.tm_k1, k1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
-  if ((st = make_map(&p.tm_k2, k2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
-  if ((st = make_map(&p.tm_v, v, B, n, H, dv, 64)) != DIFFATTN_OK) return st;
-  // Output stores: boxes of 128 tokens x 32 channels.
-  if ((st = make_map_box(&p.tm_out, out, B, n, H, dv, 32, 128)) != DIFFATTN_OK) return st;
-  p.out = static_cast<__nv_bfloat16*>(out);
-  p.lambda = lambda;
-  p.gamma = gamma;
-  p.lam_logits = nullptr;
-  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
-  p.norm_mult = 1.f - lambda_init;
-  p.eps = eps;
-  p.B = B;
-  p.n = n;
-  p.causal = causal ? 1 : 0;
-  p.units_per_batch = H;
-  p.group = 1;
-  p.num_q_tiles = (n + 127) / 128;
-  p.order = pick_order(static_cast<long long>(B) * H, n, (2 * d + dv) * 2);
-  p.status = status;
-  const long long grid = static_cast<long long>(p.num_q_tiles) * B * H;
-  if (grid > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "diffattn_forward: too many tiles");
-  // d = 64 (value width 128): one sweep with two online-softmax states fits
-  // TMEM; d = 128 (value width 256) does not, and sweeps the keys twice.
-  // Short items (up to 64 query tiles per head): one persistent CTA per SM,
-  // so each item's start overlaps the previous one's end.  Long items: one
-  // CTA per item (the fixed cost is small against them, and the hardware's
-  // dynamic CTA scheduling balances them; measured faster).
-  const bool persist = p.num_q_tiles <= 64;
-  const int g = static_cast<int>(persist ? persistent_grid(grid) : grid);
-  cudaError_t e = (d == 64) ? da::launch_onepass_v1_d64(p, g, persist, s) : da::launch_twopass_v1_d128(p, g, persist, s);
-  if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward (bf16) launch");
-  g_launches.fetch_add(1);
+  // Query and key rows are 128 bytes: one box (128-byte swizzle) of 128 rows a tile.
+  if ((st = make_map_u8(&p.tm_q1, q1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_u8(&p.tm_q2, q2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_u8(&p.tm_k1, k1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_u8(&p.tm_k2, k2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_box(&p.tm_v, v, B, n, H, dv, 64, 64)) != DIFFATTN_OK) return st;
+  // S_r = (q_scale_r k_scale_r) e4m3(q_r) e4m3(k_r)^T / sqrt(d): the scales fold into each map's exponent.
+  const double c = 1.4426950408889634 / std::sqrt(static_cast<double>(d));
+  const float sc1 = static_cast<float>(c * q1_scale * k1_scale), sc2 = static_cast<float>(c * q2_scale * k2_scale);
+  if ((st = launch_v1_tc(fn, p, true, B, H, n, d, sc1, sc2, lambda, lambda_init, gamma, eps, causal, out, status,
+                         static_cast<cudaStream_t>(stream))) != DIFFATTN_OK)
+    return st;
   return ok();
 }
 
@@ -738,40 +895,385 @@ diffattn_status diffattn_v2_forward(diffattn_dtype dt, int B, int Hq, int Hkv, i
   if (d != 128) return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_v2_forward: bf16 needs d = 128 (got %d)", d);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return fail(DIFFATTN_ERR_ALIGN, "diffattn_v2_forward: bf16 tensors must be 16-byte aligned");
+  const long long Hqd = static_cast<long long>(Hq) * d, Hkvd = static_cast<long long>(Hkv) * d;
+  const QKVViews x{q, q, k, k, v, d, Hqd, d, Hkvd, d, Hkvd};
+  if ((st = forward_v2_bf16("diffattn_v2_forward (bf16)", x, B, Hq, Hkv, n, d, lam_logits, sb, st_, scale, causal,
+                            out, status, s)) != DIFFATTN_OK)
+    return st;
+  return ok();
+}
+
+// ---------------------------------------------------------------- projections and the attention layer
+}  // extern "C"
+
+namespace {
+
+constexpr int kGemmGroupM = 16;  // row blocks per group of the persistent tile walk
+
+// C = A B^T on the tensor cores.  A [M, K] (row stride lda), B [N, K] (row
+// stride ldb) bf16; columns [0, n_main) of C go to `c` in bf16 (row stride
+// ldc), columns [n_main, N) to `c2` in fp32 (row stride ldc2).  Arguments
+// validated by the caller (K >= 1, strides and pointers 16-byte aligned).
+diffattn_status gemm_bf16(const char* fn, const void* a, long long lda, const void* b, long long ldb, int M, int N,
+                          int K, void* c, long long ldc, int n_main, float* c2, long long ldc2, int* status,
+                          cudaStream_t s) {
+  da::GemmParams p;
+  memset(&p, 0, sizeof(p));
+  diffattn_status st;
+  if ((st = make_map_2d(&p.tm_a, a, M, K, lda, da::kGemmBM)) != DIFFATTN_OK) return st;
+  if ((st = make_map_2d(&p.tm_b, b, N, K, ldb, da::kGemmBN)) != DIFFATTN_OK) return st;
+  p.c = static_cast<__nv_bfloat16*>(c);
+  p.c2 = c2;
+  p.ldc = ldc;
+  p.ldc2 = ldc2;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.n_main = n_main;
+  p.tiles_m = (M + da::kGemmBM - 1) / da::kGemmBM;
+  p.tiles_n = (N + da::kGemmBN - 1) / da::kGemmBN;
+  p.group_m = kGemmGroupM;
+  p.status = status;
+  const long long tiles = static_cast<long long>(p.tiles_m) * p.tiles_n;
+  if (tiles > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "%s: too many output tiles", fn);
+  cudaError_t e = da::launch_gemm_bf16(p, static_cast<int>(persistent_grid(tiles)), s);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  g_launches.fetch_add(1);
+  return DIFFATTN_OK;
+}
+
+// Byte offset of element `elems` of a bf16 buffer.
+const void* bf16_at(const void* base, long long elems) { return static_cast<const uint8_t*>(base) + 2 * elems; }
+
+}  // namespace
+
+extern "C" {
+
+diffattn_status diffattn_projection(int M, int N, int K, const void* a, const void* w, void* c, void* stream) {
+  const char* fn = "diffattn_projection";
+  if (M < 0 || N < 0 || K < 1) return fail(DIFFATTN_ERR_SHAPE, "%s: bad sizes M=%d N=%d K=%d", fn, M, N, K);
+  if (M == 0 || N == 0) return ok();
+  if (!a || !w || !c) return fail(DIFFATTN_ERR_NULL, "%s: NULL pointer", fn);
+  if (K % 8 != 0 || N % 8 != 0)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: K and N must be multiples of 8 (16-byte rows; got K=%d N=%d)", fn, K, N);
+  if (!aligned16(a) || !aligned16(w) || !aligned16(c)) return fail(DIFFATTN_ERR_ALIGN, "%s: 16-byte alignment", fn);
+  int* status = nullptr;
+  diffattn_status st = status_word(&status);
+  if (st != DIFFATTN_OK) return st;
+  if ((st = gemm_bf16(fn, a, K, w, K, M, N, K, c, N, N, nullptr, 0, status, static_cast<cudaStream_t>(stream))) !=
+      DIFFATTN_OK)
+    return st;
+  return ok();
+}
+
+size_t diffattn_layer_workspace(int B, int n, int H, int d) {
+  if (B < 0 || n < 0 || H < 0 || d < 1) return 0;
+  const size_t M = static_cast<size_t>(B) * n, Hd = static_cast<size_t>(H) * d;
+  return round256(M * 6 * Hd * 2) + round256(M * 2 * Hd * 2) + 256;
+}
+
+diffattn_status diffattn_layer_forward(int B, int n, int D, int H, int d, const void* x, const void* w_qkv,
+                                       const void* w_o, const float* lq1, const float* lk1, const float* lq2,
+                                       const float* lk2, float lambda_init, const float* gamma, float eps,
+                                       int causal, void* out, void* workspace, size_t workspace_bytes,
+                                       void* stream) {
+  const char* fn = "diffattn_layer_forward";
+  if (B < 0 || n < 0 || D < 1 || H < 1 || d < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: bad sizes B=%d n=%d D=%d H=%d d=%d", fn, B, n, D, H, d);
+  if (d != 64 && d != 128) return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: d must be 64 or 128 (got %d)", fn, d);
+  if (D % 8 != 0) return fail(DIFFATTN_ERR_SHAPE, "%s: D must be a multiple of 8 (got %d)", fn, D);
+  if (B == 0 || n == 0) return ok();
+  if (!x || !w_qkv || !w_o || !lq1 || !lk1 || !lq2 || !lk2 || !out || !workspace)
+    return fail(DIFFATTN_ERR_NULL, "%s: NULL pointer", fn);
+  if (!std::isfinite(lambda_init)) return fail(DIFFATTN_ERR_SHAPE, "%s: lambda_init not finite", fn);
+  if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(w_o) || !aligned16(out))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: x, w_qkv, w_o and out must be 16-byte aligned", fn);
+  const size_t need = diffattn_layer_workspace(B, n, H, d);
+  if (workspace_bytes < need)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: workspace of %zu bytes, %zu needed", fn, workspace_bytes, need);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DIFFATTN_ERR_ALIGN, "%s: workspace not 256-byte aligned", fn);
+  const long long M = static_cast<long long>(B) * n, Hd = static_cast<long long>(H) * d;
+  if (M > 0x7fffffffll || 6 * Hd > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "%s: too large", fn);
+  if (eps <= 0.f) eps = 1e-5f;
+  int* status = nullptr;
+  diffattn_status st = status_word(&status);
+  if (st != DIFFATTN_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* qkv = ws;                                                      // [M, 6 H d]: q | k | v per token
+  void* y = ws + round256(static_cast<size_t>(M) * 6 * Hd * 2);        // [M, 2 H d]: normalised heads
+  float* lam = reinterpret_cast<float*>(static_cast<uint8_t*>(y) + round256(static_cast<size_t>(M) * 2 * Hd * 2));
+  // 1. X [W^Q | W^K | W^V]: per token the 2d columns of head i of each
+  //    projection hold Q_1 (first d) and Q_2 (last d), K_1 and K_2, and V.
+  if ((st = gemm_bf16(fn, x, D, w_qkv, D, static_cast<int>(M), static_cast<int>(6 * Hd), D, qkv, 6 * Hd,
+                      static_cast<int>(6 * Hd), nullptr, 0, status, s)) != DIFFATTN_OK)
+    return st;
+  // 2. lambda from its four vectors (one warp).
+  cudaError_t e = da::launch_lambda_reparam(lq1, lk1, lq2, lk2, d, lambda_init, lam, s);
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_layer_forward: lambda_reparam launch");
+  g_launches.fetch_add(1);
+  // 3. the operator with the per-head norm, reading the projections in place
+  //    through strided tensor maps.
+  const QKVViews v{qkv, bf16_at(qkv, d), bf16_at(qkv, 2 * Hd), bf16_at(qkv, 2 * Hd + d), bf16_at(qkv, 4 * Hd),
+                   2 * d, 6 * Hd, 2 * d, 6 * Hd, 2 * d, 6 * Hd};
+  if ((st = forward_v1_bf16(fn, v, B, H, static_cast<int>(n), d, lam, lambda_init, gamma, eps, causal, y, status,
+                            s)) != DIFFATTN_OK)
+    return st;
+  // 4. Concat(heads) W^O.
+  if ((st = gemm_bf16(fn, y, 2 * Hd, w_o, 2 * Hd, static_cast<int>(M), D, static_cast<int>(2 * Hd), out, D, D,
+                      nullptr, 0, status, s)) != DIFFATTN_OK)
+    return st;
+  return ok();
+}
+
+size_t diffattn_v2_layer_workspace(int B, int n, int Hq, int Hkv, int d) {
+  if (B < 0 || n < 0 || Hq < 0 || Hkv < 0 || d < 1) return 0;
+  const size_t M = static_cast<size_t>(B) * n, G = static_cast<size_t>(Hq) / 2;
+  const size_t nq = (static_cast<size_t>(Hq) + 2 * static_cast<size_t>(Hkv)) * d;
+  return round256(M * nq * 2) + round256(M * G * 4) + round256(M * G * d * 2);
+}
+
+diffattn_status diffattn_v2_layer_forward(int B, int n, int D, int Hq, int Hkv, int d, const void* x,
+                                          const void* w_qkvl, const void* w_o, int causal, void* out,
+                                          void* workspace, size_t workspace_bytes, void* stream) {
+  const char* fn = "diffattn_v2_layer_forward";
+  if (B < 0 || n < 0 || D < 1 || Hq < 2 || Hkv < 1 || d < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: bad sizes B=%d n=%d D=%d Hq=%d Hkv=%d d=%d", fn, B, n, D, Hq, Hkv, d);
+  if (Hq % 2 != 0 || Hq % Hkv != 0 || (Hq / Hkv) % 2 != 0)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need Hq even, Hq %% Hkv == 0 and Hq/Hkv even (Hq=%d Hkv=%d)", fn, Hq, Hkv);
+  if (d != 128) return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: d must be 128 (got %d)", fn, d);
+  if (D % 8 != 0) return fail(DIFFATTN_ERR_SHAPE, "%s: D must be a multiple of 8 (got %d)", fn, D);
+  if (B == 0 || n == 0) return ok();
+  if (!x || !w_qkvl || !w_o || !out || !workspace) return fail(DIFFATTN_ERR_NULL, "%s: NULL pointer", fn);
+  if (!aligned16(x) || !aligned16(w_qkvl) || !aligned16(w_o) || !aligned16(out))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: x, w_qkvl, w_o and out must be 16-byte aligned", fn);
+  const size_t need = diffattn_v2_layer_workspace(B, n, Hq, Hkv, d);
+  if (workspace_bytes < need)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: workspace of %zu bytes, %zu needed", fn, workspace_bytes, need);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(DIFFATTN_ERR_ALIGN, "%s: workspace not 256-byte aligned", fn);
+  const long long M = static_cast<long long>(B) * n, G = Hq / 2;
+  const long long nq = (static_cast<long long>(Hq) + 2ll * Hkv) * d;
+  if (M > 0x7fffffffll || nq + G > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "%s: too large", fn);
+  int* status = nullptr;
+  diffattn_status st = status_word(&status);
+  if (st != DIFFATTN_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* qkv = ws;                                                                   // [M, (Hq + 2 Hkv) d]
+  float* logits = reinterpret_cast<float*>(ws + round256(static_cast<size_t>(M) * nq * 2));  // [M, Hq / 2] fp32
+  void* y = reinterpret_cast<uint8_t*>(logits) + round256(static_cast<size_t>(M) * G * 4);   // [M, Hq / 2 d]
+  // 1. X [W^Q | W^K | W^V | W^lambda]: q, k, v in bf16, the pairs' lambda logits in fp32.
+  if ((st = gemm_bf16(fn, x, D, w_qkvl, D, static_cast<int>(M), static_cast<int>(nq + G), D, qkv, nq,
+                      static_cast<int>(nq), logits, G, status, s)) != DIFFATTN_OK)
+    return st;
+  // 2. the V2 operator, per token and pair logits (strides n G, G).
+  const QKVViews v{qkv, qkv, bf16_at(qkv, static_cast<long long>(Hq) * d), bf16_at(qkv, static_cast<long long>(Hq) * d),
+                   bf16_at(qkv, (static_cast<long long>(Hq) + Hkv) * d), d, nq, d, nq, d, nq};
+  const float scale = 1.f / std::sqrt(static_cast<float>(d));
+  if ((st = forward_v2_bf16(fn, v, B, Hq, Hkv, static_cast<int>(n), d, logits, static_cast<long long>(n) * G, G, scale,
+                            causal, y, status, s)) != DIFFATTN_OK)
+    return st;
+  // 3. Concat(pairs) W^O.
+  if ((st = gemm_bf16(fn, y, G * d, w_o, G * d, static_cast<int>(M), D, static_cast<int>(G * d), out, D, D, nullptr,
+                      0, status, s)) != DIFFATTN_OK)
+    return st;
+  return ok();
+}
+
+// ---- backward on the tensor cores (bf16 inputs, fp32 gradients)
+}  // extern "C"
+
+namespace {
+
+// V1 (d = 64): statistics pass, dK/dV/dQ kernel, reduction of dlambda and dgamma.
+diffattn_status backward_v1_tc(int B, int H, int n, const void* q1, const void* q2, const void* k1, const void* k2,
+                               const void* v, const float* lambda, float lambda_init, const float* gamma, float eps,
+                               int causal, const void* dy, void* dq1, void* dq2, void* dk1, void* dk2, void* dv,
+                               float* dlambda, float* dgamma, uint8_t* ws, int* status, cudaStream_t s) {
+  const char* fn = "diffattn_backward (bf16)";
+  constexpr int d = 64, dv_w = 128;
+  const size_t R = static_cast<size_t>(B) * H * n;
+  const int nt = (n + 127) / 128;
+  const long long stats_grid = static_cast<long long>(nt) * B * H;
+  if (stats_grid > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "%s: too many tiles", fn);
+  __nv_bfloat16* ws_do = reinterpret_cast<__nv_bfloat16*>(ws);
+  float* ws_row = reinterpret_cast<float*>(ws + round256(R * dv_w * 2));
+  float* ws_dg = reinterpret_cast<float*>(ws + round256(R * dv_w * 2) + round256(6 * R * 4));
+  const float sc = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  diffattn_status st;
+  // 1. statistics: the forward's maps, dy in; lse, Delta, shares, dO and dgamma shares out
+  da::TwoPassParams p;
+  memset(&p, 0, sizeof(p));
+  if ((st = make_map(&p.tm_q1, q1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&p.tm_q2, q2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&p.tm_k1, k1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&p.tm_k2, k2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&p.tm_v, v, B, n, H, dv_w, 64)) != DIFFATTN_OK) return st;
+  p.lambda = lambda;
+  p.gamma = gamma;
+  p.scale_log2 = sc;
+  p.scale2_log2 = sc;
+  p.norm_mult = 1.f - lambda_init;
+  p.eps = eps;
+  p.B = B;
+  p.n = n;
+  p.causal = causal ? 1 : 0;
+  p.units_per_batch = H;
+  p.group = 1;
+  p.num_q_tiles = nt;
+  p.order = pick_order(static_cast<long long>(B) * H, n, (2 * d + dv_w) * 2);
+  p.status = status;
+  p.dy = static_cast<const __nv_bfloat16*>(dy);
+  p.dO = ws_do;
+  p.row = ws_row;
+  p.dgp = ws_dg;
+  p.rows = static_cast<long long>(R);
+  cudaError_t e = cudaMemsetAsync(dq1, 0, R * d * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dq2, 0, R * d * 4, s);
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_backward: clearing dq");
+  if ((e = da::launch_bwd_stats(p, false, static_cast<int>(stats_grid), s)) != cudaSuccess) return cuda_fail(e, fn);
+  // 2. dK, dV, dQ
+  da::BwdTcParams t;
+  memset(&t, 0, sizeof(t));
+  if ((st = make_map(&t.tm_q1, q1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&t.tm_q2, q2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&t.tm_k1, k1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&t.tm_k2, k2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&t.tm_v, v, B, n, H, dv_w, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&t.tm_do, ws_do, B, n, H, dv_w, 128)) != DIFFATTN_OK) return st;
+  t.row = ws_row;
+  t.lambda = lambda;
+  t.dq1 = static_cast<float*>(dq1);
+  t.dq2 = static_cast<float*>(dq2);
+  t.dk1 = static_cast<float*>(dk1);
+  t.dk2 = static_cast<float*>(dk2);
+  t.dv = static_cast<float*>(dv);
+  t.scale_log2 = sc;
+  t.scale = 1.f / std::sqrt(static_cast<float>(d));
+  t.B = B;
+  t.n = n;
+  t.causal = causal ? 1 : 0;
+  t.heads_kv = H;
+  t.units = H;
+  t.group = 1;
+  t.num_tiles = nt;
+  t.rows = static_cast<long long>(R);
+  t.status = status;
+  if ((e = da::launch_bwd_tc(t, false, static_cast<int>(stats_grid), s)) != cudaSuccess) return cuda_fail(e, fn);
+  // 3. dlambda and dgamma in a fixed order
+  da::BwdParams r{};
+  r.row = ws_row;
+  r.dgp = ws_dg;
+  r.dlambda = dlambda;
+  r.dgamma = dgamma;
+  r.B = B;
+  r.n = n;
+  r.d = d;
+  r.dvw = dv_w;
+  r.v2 = 0;
+  r.units = H;
+  r.rows = static_cast<long long>(R);
+  r.n_row_ctas = static_cast<int>(stats_grid);
+  if ((e = da::launch_bwd_reduce(r, s)) != cudaSuccess) return cuda_fail(e, fn);
+  g_launches.fetch_add(4);
+  return DIFFATTN_OK;
+}
+
+// V2 (d = 128): statistics pass (dlogits of per-token logits written there), dK/dV/dQ
+// kernel, reduction of the logit gradients shared by tokens.
+diffattn_status backward_v2_tc(int B, int Hq, int Hkv, int n, const void* q, const void* k, const void* v,
+                               const float* lam_logits, long long sb, long long st_, float scale, int causal,
+                               const void* dy, void* dq, void* dk, void* dv, float* dlogits, bool dense, uint8_t* ws,
+                               int* status, cudaStream_t s) {
+  const char* fn = "diffattn_v2_backward (bf16)";
+  constexpr int d = 128;
+  const int G = Hq / 2;
+  const size_t R = static_cast<size_t>(B) * G * n;
+  const int nt = (n + 127) / 128;
+  const long long stats_grid = static_cast<long long>(nt) * B * G;
+  const long long tc_grid = static_cast<long long>(nt) * B * Hkv;
+  if (stats_grid > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "%s: too many tiles", fn);
+  float* ws_row = reinterpret_cast<float*>(ws);
+  const float sc = static_cast<float>(1.4426950408889634 * scale);
+  diffattn_status st;
   da::TwoPassParams p;
   memset(&p, 0, sizeof(p));
   if ((st = make_map(&p.tm_q1, q, B, n, Hq, d, 128)) != DIFFATTN_OK) return st;
   p.tm_q2 = p.tm_q1;
-  // Key and value tiles are 128 rows (one ring slot each).
   if ((st = make_map(&p.tm_k1, k, B, n, Hkv, d, 128)) != DIFFATTN_OK) return st;
   p.tm_k2 = p.tm_k1;
   if ((st = make_map(&p.tm_v, v, B, n, Hkv, d, 128)) != DIFFATTN_OK) return st;
-  if ((st = make_map_box(&p.tm_out, out, B, n, G, d, 32, 128)) != DIFFATTN_OK) return st;
-  p.out = static_cast<__nv_bfloat16*>(out);
   p.lam_logits = lam_logits;
   p.sb = sb;
   p.st = st_;
-  p.scale_log2 = static_cast<float>(1.4426950408889634 * scale);
+  p.scale_log2 = sc;
+  p.scale2_log2 = sc;
   p.norm_mult = 1.f;
-  p.eps = 0.f;
   p.B = B;
   p.n = n;
   p.causal = causal ? 1 : 0;
   p.units_per_batch = G;
   p.group = Hq / Hkv;
-  p.num_q_tiles = (n + 127) / 128;
-  // K/V bytes per pair: the pairs of one KV head share its stream.
+  p.num_q_tiles = nt;
   p.order = pick_order(static_cast<long long>(B) * Hkv, n, 2 * d * 2);
   p.status = status;
-  const long long grid = static_cast<long long>(p.num_q_tiles) * B * G;
-  if (grid > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_forward: too many tiles");
-  // V2 items are long (up to n / 128 key tiles): one CTA per item, so the
-  // hardware's dynamic CTA scheduling balances them (measured faster here).
-  cudaError_t e = da::launch_onepass_v2_d128(p, static_cast<int>(grid), s);
-  if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_forward (bf16) launch");
-  g_launches.fetch_add(1);
-  return ok();
+  p.dy = static_cast<const __nv_bfloat16*>(dy);
+  p.row = ws_row;
+  p.dlogits_dense = dense ? dlogits : nullptr;
+  p.rows = static_cast<long long>(R);
+  cudaError_t e = cudaMemsetAsync(dq, 0, static_cast<size_t>(B) * n * Hq * d * 4, s);
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_backward: clearing dq");
+  if ((e = da::launch_bwd_stats(p, true, static_cast<int>(stats_grid), s)) != cudaSuccess) return cuda_fail(e, fn);
+  da::BwdTcParams t;
+  memset(&t, 0, sizeof(t));
+  if ((st = make_map(&t.tm_q1, q, B, n, Hq, d, 128)) != DIFFATTN_OK) return st;
+  t.tm_q2 = t.tm_q1;
+  if ((st = make_map(&t.tm_k1, k, B, n, Hkv, d, 128)) != DIFFATTN_OK) return st;
+  t.tm_k2 = t.tm_k1;
+  if ((st = make_map(&t.tm_v, v, B, n, Hkv, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map(&t.tm_do, dy, B, n, G, d, 128)) != DIFFATTN_OK) return st;
+  t.row = ws_row;
+  t.dq1 = t.dq2 = static_cast<float*>(dq);
+  t.dk1 = static_cast<float*>(dk);
+  t.dv = static_cast<float*>(dv);
+  t.scale_log2 = sc;
+  t.scale = scale;
+  t.B = B;
+  t.n = n;
+  t.causal = causal ? 1 : 0;
+  t.heads_kv = Hkv;
+  t.units = G;
+  t.group = Hq / Hkv;
+  t.num_tiles = nt;
+  t.rows = static_cast<long long>(R);
+  t.status = status;
+  if ((e = da::launch_bwd_tc(t, true, static_cast<int>(tc_grid), s)) != cudaSuccess) return cuda_fail(e, fn);
+  int launches = 3;
+  if (!dense) {
+    da::BwdParams r{};
+    r.row = ws_row;
+    r.dlogits = dlogits;
+    r.sb = sb;
+    r.B = B;
+    r.n = n;
+    r.d = d;
+    r.dvw = d;
+    r.v2 = 1;
+    r.units = G;
+    r.rows = static_cast<long long>(R);
+    r.n_logit_outs = sb == 0 ? G : B * G;
+    if ((e = da::launch_bwd_reduce(r, s)) != cudaSuccess) return cuda_fail(e, fn);
+    ++launches;
+  }
+  g_launches.fetch_add(launches);
+  return DIFFATTN_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 // ---- backward (fp32, V1)
 static size_t bwd_rows(int B, int H, int n) { return static_cast<size_t>(B) * H * n; }
@@ -795,9 +1297,9 @@ diffattn_status diffattn_backward(diffattn_dtype dt, int B, int H, int n, int d,
     return fail(DIFFATTN_ERR_DTYPE, "diffattn_backward: bad dtype %d", (int)dt);
   if (B < 0 || H < 0 || n < 0 || d < 1)
     return fail(DIFFATTN_ERR_SHAPE, "diffattn_backward: bad sizes B=%d H=%d n=%d d=%d", B, H, n, d);
-  if (dt != DIFFATTN_F32 || d > da::kSimtMaxD)
-    return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_backward: f32 with d <= 128 only (got dtype %d, d=%d)", (int)dt,
-                d);
+  if ((dt == DIFFATTN_F32 && d > da::kSimtMaxD) || (dt == DIFFATTN_BF16 && d != 64))
+    return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_backward: f32 with d <= 128 or bf16 with d = 64 (got dtype %d, d=%d)",
+                (int)dt, d);
   if (!dlambda) return fail(DIFFATTN_ERR_NULL, "diffattn_backward: NULL dlambda");
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int dvw = 2 * d;
@@ -818,6 +1320,18 @@ diffattn_status diffattn_backward(diffattn_dtype dt, int B, int H, int n, int d,
   if (static_cast<long long>(B) * H * nqb8 > 0x7fffffffll)
     return fail(DIFFATTN_ERR_SHAPE, "diffattn_backward: too many (batch, head, row block) units");
   if (eps <= 0.f) eps = 1e-5f;
+  if (dt == DIFFATTN_BF16) {
+    if (!aligned16(q1) || !aligned16(q2) || !aligned16(k1) || !aligned16(k2) || !aligned16(v) || !aligned16(dy) ||
+        !aligned16(dq1) || !aligned16(dq2) || !aligned16(dk1) || !aligned16(dk2) || !aligned16(dv))
+      return fail(DIFFATTN_ERR_ALIGN, "diffattn_backward: bf16 path needs 16-byte aligned tensors");
+    int* status = nullptr;
+    diffattn_status st = status_word(&status);
+    if (st != DIFFATTN_OK) return st;
+    if ((st = backward_v1_tc(B, H, n, q1, q2, k1, k2, v, lambda, lambda_init, gamma, eps, causal, dy, dq1, dq2, dk1,
+                             dk2, dv, dlambda, dgamma, static_cast<uint8_t*>(workspace), status, s)) != DIFFATTN_OK)
+      return st;
+    return ok();
+  }
   const size_t R = bwd_rows(B, H, n);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* ws_do = reinterpret_cast<float*>(ws);
@@ -903,9 +1417,9 @@ diffattn_status diffattn_v2_backward(diffattn_dtype dt, int B, int Hq, int Hkv, 
   if (Hq % 2 != 0 || Hq % Hkv != 0 || (Hq / Hkv) % 2 != 0)
     return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_backward: need Hq even, Hq %% Hkv == 0 and Hq/Hkv even");
   if (sb < 0 || st < 0) return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_backward: negative logit stride");
-  if (dt != DIFFATTN_F32 || d > da::kSimtMaxD)
-    return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_v2_backward: f32 with d <= 128 only (got dtype %d, d=%d)",
-                (int)dt, d);
+  if ((dt == DIFFATTN_F32 && d > da::kSimtMaxD) || (dt == DIFFATTN_BF16 && d != 128))
+    return fail(DIFFATTN_ERR_UNSUPPORTED,
+                "diffattn_v2_backward: f32 with d <= 128 or bf16 with d = 128 (got dtype %d, d=%d)", (int)dt, d);
   const int G = Hq / 2;
   const bool dense = st == G && sb == static_cast<long long>(n) * G;  // one logit per token and pair
   if (!dense && !(st == 0 && (sb == 0 || sb == G)))
@@ -931,11 +1445,23 @@ diffattn_status diffattn_v2_backward(diffattn_dtype dt, int B, int Hq, int Hkv, 
   if (static_cast<long long>(B) * G * nqb8 > 0x7fffffffll)
     return fail(DIFFATTN_ERR_SHAPE, "diffattn_v2_backward: too many (batch, pair, row block) units");
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.f / std::sqrt(static_cast<float>(d));
+  if (dt == DIFFATTN_BF16) {
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dy) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dv))
+      return fail(DIFFATTN_ERR_ALIGN, "diffattn_v2_backward: bf16 path needs 16-byte aligned tensors");
+    int* status = nullptr;
+    diffattn_status stt = status_word(&status);
+    if (stt != DIFFATTN_OK) return stt;
+    if ((stt = backward_v2_tc(B, Hq, Hkv, n, q, k, v, lam_logits, sb, st, scale, causal, dy, dq, dk, dv, dlogits, dense,
+                              static_cast<uint8_t*>(workspace), status, s)) != DIFFATTN_OK)
+      return stt;
+    return ok();
+  }
   const size_t R = bwd_rows(B, G, n);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* ws_do = reinterpret_cast<float*>(ws);
   float* ws_row = reinterpret_cast<float*>(ws + round256(R * d * 4));
-  const float scale = softmax_scale > 0.f ? softmax_scale : 1.f / std::sqrt(static_cast<float>(d));
 
   da::SimtParams rp{};
   rp.q1 = rp.q2 = static_cast<const float*>(q);

@@ -23,6 +23,12 @@ cudaError_t launch_backward_f32(const BwdParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_bwd_reduce(const BwdParams& p, cudaStream_t s) {
+  const int nred = p.v2 ? p.n_logit_outs : 1 + (p.dgamma != nullptr ? p.dvw : 0);
+  if (nred > 0) bwd_reduce_kernel<<<nred, kBwdThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_lambda_reparam_bwd(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
                                       int dim, const float* dlambda, float* dlq1, float* dlk1, float* dlq2,
                                       float* dlk2, cudaStream_t s) {

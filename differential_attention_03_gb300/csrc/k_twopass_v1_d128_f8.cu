@@ -1,0 +1,7 @@
+#include "twopass_inst.cuh"
+namespace da {
+cudaError_t launch_twopass_v1_d128_f8(const TwoPassParams& p, int grid, bool persistent, cudaStream_t s) {
+  return persistent ? launch_twopass<128, 256, false, kEpiRmsNorm, 4, true, true>(p, grid, s)
+                    : launch_twopass<128, 256, false, kEpiRmsNorm, 4, false, true>(p, grid, s);
+}
+}  // namespace da

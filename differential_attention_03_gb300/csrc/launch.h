@@ -10,12 +10,16 @@ namespace da {
 struct DecodeParams;
 struct BwdParams;
 struct SimtBwdExtra;
+struct GemmParams;
+struct BwdTcParams;
 }
 
 namespace da {
 
 // V1, d = 128, value width 256: two sweeps, one accumulator.
 cudaError_t launch_twopass_v1_d128(const TwoPassParams& p, int grid, bool persistent, cudaStream_t s);
+// The same with e4m3 queries and keys (QK^T on kind::f8f6f4 MMAs; P.V in bf16).
+cudaError_t launch_twopass_v1_d128_f8(const TwoPassParams& p, int grid, bool persistent, cudaStream_t s);
 // V1, d = 64, value width 128: one sweep, two online-softmax states.
 cudaError_t launch_onepass_v1_d64(const TwoPassParams& p, int grid, bool persistent, cudaStream_t s);
 // V2, d = 128 (query/key/value width 128), one K/V head per query-head pair: one sweep.
@@ -37,6 +41,15 @@ cudaError_t launch_lambda_reparam_bwd(const float* lq1, const float* lk1, const 
                                       float* dlk2, cudaStream_t s);
 cudaError_t launch_lambda_reparam(const float* lq1, const float* lk1, const float* lq2, const float* lk2,
                                   int dim, float lambda_init, float* out, cudaStream_t s);
+// Tensor-core backward (bf16; V1 d = 64, V2 d = 128): the statistics pass
+// (one-sweep forward, one item per CTA, grid = items) and the dK/dV/dQ kernel
+// (grid = B * heads_kv * key tiles).
+cudaError_t launch_bwd_stats(const TwoPassParams& p, bool v2, int grid, cudaStream_t s);
+cudaError_t launch_bwd_tc(const BwdTcParams& p, bool v2, int grid, cudaStream_t s);
+// The fp32 backward's reduction of the dlambda / dlogit and dgamma shares alone.
+cudaError_t launch_bwd_reduce(const BwdParams& p, cudaStream_t s);
+// Projection GEMM C = A B^T (bf16, fp32 accumulation), `grid` persistent CTAs.
+cudaError_t launch_gemm_bf16(const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_wait_selftest(unsigned long long budget_cycles, int* status, cudaStream_t s);
 
 }  // namespace da

@@ -68,7 +68,7 @@
 
 namespace da {
 
-template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST>
+template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST, bool STATS = false>
 struct OnePassCfg {
   static constexpr int BM = 128;
   static constexpr int BN = 128;
@@ -114,6 +114,12 @@ struct OnePassCfg {
   // when P is in shared memory, else a quarter of the Q buffers.
   static constexpr int STG_BYTES = BM * 64;
   static_assert(PSM || 2 * Q_TILE >= 4 * STG_BYTES, "output staging in the Q buffers");
+  // STATS (the backward's statistics pass): one item per CTA; after the
+  // item's last MMA the Q buffers hold the epilogue's exchange of partial
+  // row sums ([6][4][128] floats) and the per-warp dgamma sums.
+  static_assert(!STATS || !PERSIST, "the statistics pass runs one item per CTA");
+  static constexpr int XCH_FLOATS = 6 * 4 * 128;
+  static_assert(!STATS || 2 * Q_TILE >= (XCH_FLOATS + 4 * 4 * 32) * 4, "statistics exchange in the Q buffers");
 };
 
 // 32 output channels of one row: y * rinv (* gamma), rounded to bf16 pairs.
@@ -130,9 +136,153 @@ __device__ __forceinline__ void pack_out_row(const float (&y)[32], float rinv, c
   }
 }
 
-template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST>
+// Epilogue of the backward's statistics pass (one item per CTA, every MMA of
+// it complete): instead of the output, each row's quantities the tensor-core
+// backward needs.  Thread = row `row` (token t) x channels [32 cb, +32) of
+// map `map` (its running maximum m_used); l1, l2 the final row sums, coef the
+// second map's coefficient (V1 lambda, V2 sigmoid of the row's logit).  With
+// O_r = O_r' / l_r the normalised map outputs and O = O_1 - coef O_2:
+//   V1: y = m gamma O r,  r = (mean O^2 + eps)^-1/2,  m = 1 - lambda_init;
+//       G = m gamma dy,  dO = r G - (r^3 / DV) (G . O) O   (bf16 to p.dO);
+//       dgamma share = dy m O r (per channel, summed over the CTA's rows).
+//   V2: dO = dy.
+//   Delta_1 = dO . O_1,  Delta_2 = -coef dO . O_2 (the row sums of the softmax
+//   gradients: dS_r = P_r (c_r dO V^T - Delta_r) with c_1 = 1, c_2 = -coef);
+//   lse_r = m_r + log2 l_r (scaled log2 domain);  share: V1 dL/dlambda of the
+//   row = -dO . O_2, V2 dL/dlogit = -s (1 - s) dO . O_2.
+// The four channel blocks of a row add their partial dot products through
+// the Q buffers (free once the item's MMAs are done).
+template <class C, int EPI>
+__device__ __forceinline__ void onepass_stats_epilogue(const TwoPassParams& p, const TileCoord& c, int t, int row,
+                                                       int lane, int warp, int cb, int map, float l1, float l2,
+                                                       float coef, float m_used, uint32_t tl, uint8_t* smem,
+                                                       const float* sgamma) {
+  constexpr int DV = C::DV;
+  constexpr bool V1 = EPI == kEpiRmsNorm;
+  constexpr int NX = V1 ? 6 : 2;  // partial sums exchanged per row
+  const bool live = t < p.n;
+  const long long orow = (static_cast<long long>(c.b) * p.n + t) * p.units_per_batch + c.u;
+  uint32_t o1[32], o2[32];
+  tmem_ld32(tl + C::TM_O1 + 32u * cb, o1);
+  tmem_ld32(tl + C::TM_O2 + 32u * cb, o2);
+  tmem_ld_wait2(o1, o2);
+  float dyv[32];
+  if (live) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.dy + orow * DV + 32 * cb);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint4 u = src[v];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        dyv[8 * v + 2 * e] = __uint_as_float(w[e] << 16);
+        dyv[8 * v + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int cc = 0; cc < 32; ++cc) dyv[cc] = 0.f;
+  }
+  const float il1 = 1.f / l1, il2 = 1.f / l2;
+  const float mult = p.norm_mult;
+  float part[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // V1: ss, G.O, G.O1, G.O2, O.O1, O.O2; V2: dy.O1, dy.O2
+#pragma unroll
+  for (int cc = 0; cc < 32; ++cc) {
+    const float x1 = __uint_as_float(o1[cc]) * il1, x2 = __uint_as_float(o2[cc]) * il2;
+    if constexpr (V1) {
+      const float o = fmaf(-coef, x2, x1);
+      const float g = mult * sgamma[32 * cb + cc] * dyv[cc];
+      o1[cc] = __float_as_uint(o);  // keep O and G for the second pass over the channels
+      o2[cc] = __float_as_uint(g);
+      part[0] = fmaf(o, o, part[0]);
+      part[1] = fmaf(g, o, part[1]);
+      part[2] = fmaf(g, x1, part[2]);
+      part[3] = fmaf(g, x2, part[3]);
+      part[4] = fmaf(o, x1, part[4]);
+      part[5] = fmaf(o, x2, part[5]);
+    } else {
+      part[0] = fmaf(dyv[cc], x1, part[0]);
+      part[1] = fmaf(dyv[cc], x2, part[1]);
+    }
+  }
+  float* xch = reinterpret_cast<float*>(smem + C::OFF_Q1);  // [NX][4][128]
+#pragma unroll
+  for (int k = 0; k < NX; ++k) xch[(k * 4 + cb) * 128 + row] = part[k];
+  named_bar_sync(1, 128 * C::NSMWG);
+  float tot[6];
+#pragma unroll
+  for (int k = 0; k < NX; ++k)
+    tot[k] = (xch[(k * 4) * 128 + row] + xch[(k * 4 + 1) * 128 + row]) +
+             (xch[(k * 4 + 2) * 128 + row] + xch[(k * 4 + 3) * 128 + row]);
+  float delta1, delta2, share;
+  if constexpr (V1) {
+    const float r = rsqrtf(tot[0] * (1.f / DV) + p.eps);
+    const float k3 = r * r * r * (1.f / DV) * tot[1];
+    const float dO1 = r * tot[2] - k3 * tot[4];  // dO . O_1
+    const float dO2 = r * tot[3] - k3 * tot[5];  // dO . O_2
+    delta1 = dO1;
+    delta2 = -coef * dO2;
+    share = -dO2;
+    // dO of the channel block, and its dgamma shares
+    uint32_t w[16];
+    float dg[32];
+#pragma unroll
+    for (int cc = 0; cc < 32; cc += 2) {
+      const float oa = __uint_as_float(o1[cc]), ob = __uint_as_float(o1[cc + 1]);
+      w[cc >> 1] = pack_bf16x2(r * __uint_as_float(o2[cc]) - k3 * oa, r * __uint_as_float(o2[cc + 1]) - k3 * ob);
+      dg[cc] = live ? dyv[cc] * mult * oa * r : 0.f;
+      dg[cc + 1] = live ? dyv[cc + 1] * mult * ob * r : 0.f;
+    }
+    if (live) {
+      uint4* dst = reinterpret_cast<uint4*>(p.dO + orow * DV + 32 * cb);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+    }
+    // Sum the 32 channels' shares over the warp's 32 rows (lane l ends with
+    // channel l: each step halves the channels a lane holds and doubles the
+    // rows they cover), then over the warpgroup's four warps.
+#pragma unroll
+    for (int sft = 16; sft >= 1; sft >>= 1) {
+      const bool upper = (lane & sft) != 0;
+#pragma unroll
+      for (int j = 0; j < sft; ++j) {
+        const float send = upper ? dg[j] : dg[j + sft];
+        const float keep = upper ? dg[j + sft] : dg[j];
+        dg[j] = keep + __shfl_xor_sync(0xffffffffu, send, sft);
+      }
+    }
+    float* wsum = xch + C::XCH_FLOATS;  // [4 channel blocks][4 warps][32]
+    wsum[(cb * 4 + (warp & 3)) * 32 + lane] = dg[0];
+    named_bar_sync(1, 128 * C::NSMWG);
+    if ((warp & 3) == 0) {
+      const float* ws = wsum + cb * 4 * 32;
+      p.dgp[static_cast<long long>(blockIdx.x) * DV + 32 * cb + lane] =
+          (ws[lane] + ws[32 + lane]) + (ws[64 + lane] + ws[96 + lane]);
+    }
+  } else {
+    delta1 = tot[0];
+    delta2 = -coef * tot[1];
+    share = -coef * (1.f - coef) * tot[1];
+  }
+  if (live) {
+    const long long ri = (static_cast<long long>(c.b) * p.units_per_batch + c.u) * p.n + t;
+    if (cb == 0) {  // map 1's running maximum lives in its warpgroups
+      p.row[ri] = m_used + log2f(l1);
+      p.row[2 * p.rows + ri] = delta1;
+      p.row[3 * p.rows + ri] = delta2;
+      p.row[4 * p.rows + ri] = share;
+      p.row[5 * p.rows + ri] = coef;
+      if (!V1 && p.dlogits_dense != nullptr) p.dlogits_dense[c.b * p.sb + static_cast<long long>(t) * p.st + c.u] = share;
+    } else if (cb == 2) {
+      p.row[p.rows + ri] = m_used + log2f(l2);
+    }
+  }
+  (void)map;
+}
+
+template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST, bool STATS = false>
 __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
-  using C = OnePassCfg<D, SHARED_K, EPI, NSLOT, PSM, PERSIST>;
+  using C = OnePassCfg<D, SHARED_K, EPI, NSLOT, PSM, PERSIST, STATS>;
   constexpr int BM = C::BM, BN = C::BN, DV = C::DV;
 
   extern __shared__ uint8_t smem_raw[];
@@ -559,6 +709,10 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
       if (EPI == kEpiV2) {
         const float lg = (t < p.n) ? p.lam_logits[c.b * p.sb + static_cast<long long>(t) * p.st + c.u] : 0.f;
         coef = 1.f / (1.f + expf(-lg));
+      }
+      if constexpr (STATS) {
+        onepass_stats_epilogue<C, EPI>(p, c, t, row, lane, warp, cb, map, l1, l2, coef, m_used, tl, smem, sgamma);
+        continue;
       }
       const float a1 = 1.f / l1, a2 = -coef / l2;
       float y[32];

@@ -19,7 +19,8 @@ struct TwoPassParams {
   const float* gamma;       // V1: [DV] or nullptr
   const float* lam_logits;  // V2: logit of (b, t, g) at b*sb + t*st + g
   long long sb, st;
-  float scale_log2;  // softmax scale * log2(e)
+  float scale_log2;  // softmax scale * log2(e) (map 1; both maps unless e4m3 inputs)
+  float scale2_log2; // e4m3 queries and keys only: map 2's, with its dequantisation scales
   float norm_mult;   // V1: 1 - lambda_init
   float eps;         // V1: RMSNorm epsilon
   int B, n, causal;
@@ -29,6 +30,14 @@ struct TwoPassParams {
   int order;  // 0: unit-major tile order, 1: query-tile-major
   int* status;
   CUtensorMap tm_out;  // output [B, n, units_per_batch, DV] for TMA stores
+  // Backward statistics (one-sweep kernel with STATS): dy in, per-row results
+  // out; row r = (b * units_per_batch + u) * n + t.
+  const __nv_bfloat16* dy;  // [B, n, units_per_batch, DV]
+  __nv_bfloat16* dO;        // V1: [B, n, units_per_batch, DV], the gradient of the pre-norm output
+  float* row;               // [6][rows]: lse_1, lse_2, Delta_1, Delta_2, lambda / logit share, coefficient
+  float* dgp;               // V1: [gridDim.x][DV], each CTA's share of dgamma
+  float* dlogits_dense;     // V2, one logit per token: dlogit of (b, t, pair) at b sb + t st + pair
+  long long rows;           // B * units_per_batch * n
 };
 
 // What work item `idx` of a tcgen05 launch computes: batch b, unit u (V1:

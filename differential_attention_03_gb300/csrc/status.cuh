@@ -7,6 +7,7 @@ namespace da {
 
 constexpr int kStatusOk = 0;
 constexpr int kStatusTimeout = 7;  // DIFFATTN_ERR_TIMEOUT
+constexpr int kStatusSmemAlign = 9;  // a kernel found its shared memory misaligned (read as DIFFATTN_ERR_CUDA)
 
 // Budget of one in-kernel wait, in SM clock cycles (about one second at the
 // 2.07 GHz maximum clock, two at 1 GHz).  Every legitimate wait in these

@@ -72,19 +72,22 @@
 
 namespace da {
 
-template <int D, int DV, bool SHARED_K, int EPI, int NSLOT, bool PERSIST>
+template <int D, int DV, bool SHARED_K, int EPI, int NSLOT, bool PERSIST, bool F8 = false>
 struct TwoPassCfg {
   static constexpr int BM = 128;   // queries per CTA (TMEM lanes)
   static constexpr int BN = 128;   // keys per tile
   static constexpr int NSMWG = 4;  // softmax warpgroups
   static constexpr int NTHREADS = (4 + 4 * NSMWG) * 32;
-  static constexpr int QB = D / 64;  // 128-byte swizzle boxes across a Q/K row
+  // F8: Q_1, Q_2, K_1, K_2 arrive as e4m3 bytes (one byte an element, a
+  // whole d = 128 row in one 128-byte box); V and P stay bf16.
+  static constexpr int QK_ES = F8 ? 1 : 2;  // bytes of a query/key element
+  static constexpr int QB = D * QK_ES / 128;  // 128-byte swizzle boxes across a Q/K row
   static constexpr int VB = DV / 64;
-  static constexpr int Q_TILE = BM * D * 2;
-  static constexpr int K_TILE = BN * D * 2;
+  static constexpr int Q_TILE = BM * D * QK_ES;
+  static constexpr int K_TILE = BN * D * QK_ES;
   static constexpr int V_TILE = BN * DV * 2;
   static constexpr int P_TILE = BM * BN * 2;  // bf16 P, two 64-key boxes
-  static constexpr int SLOT = K_TILE;
+  static constexpr int SLOT = BN * D * 2;  // a bf16 key tile (an e4m3 one fills half)
   static constexpr int VF = V_TILE / SLOT;  // slots per V tile
   static constexpr int VKEYS = BN / VF;     // keys per V slot
   static constexpr int OFF_Q1 = 0;
@@ -100,9 +103,11 @@ struct TwoPassCfg {
   static constexpr uint32_t TM_O = 0;
   static constexpr uint32_t TM_A = DV;
   static constexpr uint32_t TM_B = DV + 128;
-  static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false, false);
+  static constexpr uint32_t IDESC_QK = F8 ? idesc_e4m3(BM, BN) : idesc_bf16(BM, BN, false, false);
+  static constexpr int QK_STEPS = F8 ? D / 32 : D / 16;  // MMAs per QK^T tile (32 bytes of K each)
   static constexpr uint32_t IDESC_PV = idesc_bf16(BM, DV, false, true);
   static_assert(D == 64 || D == 128, "query/key width");
+  static_assert(!F8 || D == 128, "e4m3 queries and keys: d = 128 (one 128-byte box a row)");
   static_assert(DV == 256, "sweep-1 buffer ring assumes O spans two 128-column buffers");
   static_assert(V_TILE % SLOT == 0 && (VF == 1 || VF == 2), "value tile split");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -167,9 +172,9 @@ __device__ __forceinline__ void row_stats64(uint32_t (&r0)[32], uint32_t (&r1)[3
   m = m_new;
 }
 
-template <int D, int DV, bool SHARED_K, int EPI, int NSLOT, bool PERSIST>
+template <int D, int DV, bool SHARED_K, int EPI, int NSLOT, bool PERSIST, bool F8 = false>
 __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
-  using C = TwoPassCfg<D, DV, SHARED_K, EPI, NSLOT, PERSIST>;
+  using C = TwoPassCfg<D, DV, SHARED_K, EPI, NSLOT, PERSIST, F8>;
   constexpr int BM = C::BM, BN = C::BN;
 
   extern __shared__ uint8_t smem_raw[];
@@ -296,7 +301,7 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
           }
           uint64_t* bar = &full[o * NSLOT + s];
           uint8_t* dst = smem + C::OFF_RING + s * C::SLOT;
-          mbar_arrive_expect_tx(bar, C::SLOT);
+          mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nbox * rows * 128));
           for (int bx = 0; bx < nbox; ++bx) tma_load_4d(dst + bx * rows * 128, map, bar, bx * 64, c.hk, key0, c.b);
           last_o = (last_o & ~(1u << s)) | (static_cast<uint32_t>(o) << s);
           par ^= 1u << (o * NSLOT + s);  // now the parity after this fill; the fill's own is the flip of it
@@ -368,10 +373,15 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
     auto qk = [&](uint32_t dst, int f) {
       const uint64_t dk = dRingK + static_cast<uint64_t>(((f % NSLOT) * C::SLOT) >> 4);
 #pragma unroll
-      for (int k = 0; k < D / 16; ++k)
-        mma_ss_elect(dst, dQ + static_cast<uint64_t>((((k >> 2) * (BM * 128)) + (k & 3) * 32) >> 4),
-                     dk + static_cast<uint64_t>((((k >> 2) * (BN * 128)) + (k & 3) * 32) >> 4), C::IDESC_QK,
-                     k > 0 ? 1u : 0u);
+      for (int k = 0; k < C::QK_STEPS; ++k) {
+        // k-step k reads 32 bytes of each row: box k / 4, bytes 32 (k % 4) .. +31
+        const uint64_t a = dQ + static_cast<uint64_t>((((k >> 2) * (BM * 128)) + (k & 3) * 32) >> 4);
+        const uint64_t b = dk + static_cast<uint64_t>((((k >> 2) * (BN * 128)) + (k & 3) * 32) >> 4);
+        if constexpr (F8)
+          mma_ss_f8_elect(dst, a, b, C::IDESC_QK, k > 0 ? 1u : 0u);
+        else
+          mma_ss_elect(dst, a, b, C::IDESC_QK, k > 0 ? 1u : 0u);
+      }
     };
     constexpr int PER_TILE = 2 + C::VF;
     uint32_t use_lo = 0, use_hi = 0;  // sweep-1 writes so far of buffers mw and mw + 2
@@ -477,9 +487,13 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
     const int wq = warp & 3;         // TMEM lane quarter
     const int row = wq * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const float sc = p.scale_log2;
     const int map = wg >> 1;
     const int half = wg & 1;
+    // Softmax scale x log2(e) of each map; with e4m3 inputs each map's also
+    // carries its query and key dequantisation scales.
+    const float sc_a = p.scale_log2;
+    const float sc_b = F8 ? p.scale2_log2 : p.scale_log2;
+    const float sc = map == 0 ? sc_a : sc_b;
     const float lam = (EPI == kEpiRmsNorm) ? *p.lambda : 0.f;  // read once per CTA
     uint32_t g1 = 0;  // key tiles of earlier items (each sweep)
 
@@ -550,7 +564,7 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
       const float acoef = fabsf(coef);
       const float M2 = (acoef > 0.f) ? m2 + log2f(l2) - log2f(acoef) : INFINITY;
       const float neg2 = (coef >= 0.f) ? -1.f : 1.f;
-      const uint64_t sc2 = f2pack(sc, sc);
+      const uint64_t sc2a = f2pack(sc_a, sc_a), sc2b = f2pack(sc_b, sc_b);
       const uint64_t nM1 = f2pack(-M1, -M1), nM2 = f2pack(-M2, -M2), ng2 = f2pack(neg2, neg2);
       // This thread's P chunks: row `row`, keys [32 wg, +32) = 64-key box wg / 2,
       // 16-byte chunks 4 (wg % 2) .. 4 (wg % 2) + 3 of the 128-byte swizzled row.
@@ -573,7 +587,7 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) {
           float x0, x1;
-          f2unpack(fma2(f2pack(__uint_as_float(r[2 * cc]), __uint_as_float(r[2 * cc + 1])), sc2, nM2), x0, x1);
+          f2unpack(fma2(f2pack(__uint_as_float(r[2 * cc]), __uint_as_float(r[2 * cc + 1])), sc2b, nM2), x0, x1);
           e2[cc] = f2pack(ex2(x0), ex2(x1));
         }
         mbar_wait(a2_full, g & 1u, ab);
@@ -590,7 +604,7 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) {
           float x0, x1;
-          f2unpack(fma2(f2pack(__uint_as_float(r[2 * cc]), __uint_as_float(r[2 * cc + 1])), sc2, nM1), x0, x1);
+          f2unpack(fma2(f2pack(__uint_as_float(r[2 * cc]), __uint_as_float(r[2 * cc + 1])), sc2a, nM1), x0, x1);
           float p0, p1;
           f2unpack(fma2(e2[cc], ng2, f2pack(ex2(x0), ex2(x1))), p0, p1);
           if (2 * cc >= nvis) p0 = 0.f;

@@ -109,6 +109,31 @@ diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d,
                                  int causal, void* out, void* stream);
 
 /*
+ * diffattn_forward with the queries and keys in FP8: the low-bit attention
+ * that the "Differential Transformer" glossary page (section on the reported
+ * benefits) motivates by DIFF's smaller activation outliers, applied to the
+ * score products Q_r K_r^T on the tensor cores' e4m3 path (kind::f8f6f4,
+ * twice the bf16 rate); the values, P.V, the combine and the norm stay as in
+ * the bf16 forward.
+ *   q1, q2, k1, k2 : [B, n, H, d] device arrays of e4m3 bytes (OCP FP8 E4M3,
+ *                    "fn") holding Q_r / q_scale_r and K_r / k_scale_r, one
+ *                    scale per tensor (how they were quantised is the
+ *                    caller's; e.g. amax / 448).
+ *   q1_scale, q2_scale, k1_scale, k2_scale : finite and positive, else ERR_SHAPE.
+ *   v, out, lambda, lambda_init, gamma, eps, causal : as for diffattn_forward (bf16).
+ * The result is diffattn_forward's for Q_r = q_scale_r e4m3(q_r) and
+ * K_r = k_scale_r e4m3(k_r): every e4m3 product is exact in the fp32
+ * accumulator and each map's two scales fold into its softmax exponent.
+ * d = 128 only (one 128-byte row a box), else ERR_UNSUPPORTED.  Errors
+ * otherwise as for diffattn_forward.
+ */
+diffattn_status diffattn_forward_fp8qk(int B, int H, int n, int d, const void* q1, const void* q2,
+                                       const void* k1, const void* k2, float q1_scale,
+                                       float q2_scale, float k1_scale, float k2_scale, const void* v,
+                                       const float* lambda, float lambda_init, const float* gamma,
+                                       float eps, int causal, void* out, void* stream);
+
+/*
  * diffattn_forward on inputs and output in HOST memory: the call copies the
  * inputs in, runs the forward and copies the output back, pipelined over
  * chunks of the batch (the copy of chunk c + 1 in, the forward of chunk c
@@ -305,6 +330,83 @@ diffattn_status diffattn_v2_forward(diffattn_dtype dt, int B, int Hq, int Hkv, i
                                     const float* lam_logits, long long sb, long long st,
                                     float softmax_scale, int causal, void* out,
                                     void* stream);
+
+/*
+ * Projection on the tensor cores: c = a w^T, bf16 operands, fp32 accumulation,
+ * bf16 result rounded once to nearest.  The projections X W^Q, X W^K, X W^V
+ * (and X W^lambda for DIFF V2) and Concat(heads) W^O around the operator
+ * (news article section "差分注意力"; see diffattn_layer_forward) are this
+ * product with the weight stored as [out features, in features].
+ *   a : [M, K] device bf16;  w : [N, K] device bf16;  c : [M, N] device bf16,
+ *       all contiguous and 16-byte aligned.
+ *   K >= 1 and N multiples of 8 (16-byte rows), else ERR_SHAPE; M = 0 or
+ *   N = 0 is a no-op.  Asynchronous on `stream`.  Errors as for diffattn_forward.
+ */
+diffattn_status diffattn_projection(int M, int N, int K, const void* a, const void* w, void* c,
+                                    void* stream);
+
+/*
+ * The DIFF V1 attention layer around the operator (news article section
+ * "差分注意力": X is projected by W^Q, W^K, W^V with per-head matrices, every
+ * head's output is normalised on its own with the fixed multiplier
+ * (1 - lambda_init), the heads are concatenated along the channels and
+ * projected by W^O; lambda is re-parameterised from four vectors):
+ *
+ *   [Q | K | V] = X [W^Q | W^K | W^V];   head i: Q_1, Q_2 = first and last d of
+ *                 Q's 2d columns [2 d i, 2 d (i + 1)), the same for K; V's 2d
+ *   y_i = diffattn_forward of head i (lambda = lambda_reparam(lq1, lk1, lq2, lk2))
+ *   out = Concat(y_1 .. y_H) W^O
+ *
+ *   x     : [B, n, D] device bf16 (tokens).
+ *   w_qkv : [3 H 2d, D] device bf16: rows [0, H 2d) are the columns of W^Q
+ *           ([D, H 2d]), then those of W^K, then W^V (the weight of one fused
+ *           linear layer, [out features, in features]).
+ *   w_o   : [D, H 2d] device bf16 (W^O as [out features, in features]).
+ *   lq1, lk1, lq2, lk2 : device fp32 [d];  lambda_init, gamma, eps, causal:
+ *           as for diffattn_forward.
+ *   out   : [B, n, D] device bf16.
+ *   workspace : device memory the caller owns, at least
+ *           diffattn_layer_workspace(B, n, H, d) bytes, 256-byte aligned; it
+ *           holds the projections, the normalised heads and lambda.
+ * bf16 with d in {64, 128} (else ERR_UNSUPPORTED); D a multiple of 8; B = 0 or
+ * n = 0 is a no-op.  Four kernels in stream order (projection GEMM, lambda,
+ * the fused operator reading the projections in place, W^O GEMM);
+ * asynchronous on `stream`.  Errors as for diffattn_forward; a small or
+ * unaligned workspace -> ERR_SHAPE / ERR_ALIGN.
+ */
+size_t diffattn_layer_workspace(int B, int n, int H, int d);
+
+diffattn_status diffattn_layer_forward(int B, int n, int D, int H, int d, const void* x,
+                                       const void* w_qkv, const void* w_o, const float* lq1,
+                                       const float* lk1, const float* lq2, const float* lk2,
+                                       float lambda_init, const float* gamma, float eps, int causal,
+                                       void* out, void* workspace, size_t workspace_bytes,
+                                       void* stream);
+
+/*
+ * The DIFF V2 attention layer (DIFF V2 analysis page, sections "2. 커스텀 커널
+ * 제거", "5. 간소화된 λ 매개변수화" (lambda per token and head, a sigmoid of a
+ * projection of the token) and "GQA와의 호환성"):
+ *
+ *   [q | k | v | z] = X [W^Q | W^K | W^V | W^lambda]    z: one logit per token and pair
+ *   y   = diffattn_v2_forward(q, k, v, logits z per token, scale 1/sqrt(d))
+ *   out = Concat(pairs) W^O
+ *
+ *   x      : [B, n, D] device bf16.
+ *   w_qkvl : [(Hq + 2 Hkv) d + Hq/2, D] device bf16: the columns of W^Q
+ *            ([D, Hq d]), W^K, W^V ([D, Hkv d] each), then W^lambda ([D, Hq/2]).
+ *   w_o    : [D, Hq/2 d] device bf16.   out : [B, n, D] device bf16.
+ *   workspace : at least diffattn_v2_layer_workspace(B, n, Hq, Hkv, d) bytes,
+ *            256-byte aligned (projections, fp32 logits, pair outputs).
+ * bf16 with d = 128; Hq, Hkv rules as for diffattn_v2_forward; D a multiple of
+ * 8.  Three kernels in stream order; the logits leave the projection in fp32.
+ */
+size_t diffattn_v2_layer_workspace(int B, int n, int Hq, int Hkv, int d);
+
+diffattn_status diffattn_v2_layer_forward(int B, int n, int D, int Hq, int Hkv, int d,
+                                          const void* x, const void* w_qkvl, const void* w_o,
+                                          int causal, void* out, void* workspace,
+                                          size_t workspace_bytes, void* stream);
 
 /*
  * Backward pass of diffattn_forward (DIFF V1), fp32 on CUDA cores.  The pages

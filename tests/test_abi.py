@@ -35,8 +35,9 @@ def test_header_declares_the_entry_points():
                  "diffattn_device_status", "diffattn_last_error", "diffattn_forward_host",
                  "diffattn_forward_host_workspace", "diffattn_decode", "diffattn_v2_decode",
                  "diffattn_decode_workspace", "diffattn_v2_decode_workspace", "diffattn_decode_fp8k",
-                 "diffattn_v2_decode_fp8k", "diffattn_decode_noalloc", "diffattn_backward",
-                 "diffattn_backward_workspace",
+                 "diffattn_decode_noalloc", "diffattn_projection", "diffattn_forward_fp8qk", "diffattn_layer_forward",
+                 "diffattn_layer_workspace", "diffattn_v2_layer_forward", "diffattn_v2_layer_workspace",
+                 "diffattn_v2_decode_fp8k", "diffattn_backward", "diffattn_backward_workspace",
                  "lambda_reparam_backward", "diffattn_v2_backward", "diffattn_v2_backward_workspace"):
         assert want in names
 
@@ -222,7 +223,8 @@ def test_backward_host_validation(L):
         return L.diffattn_backward(dt, B, 3, n, d, q1, A, A, A, A, A, ctypes.c_float(0.2), None,
                                    ctypes.c_float(1e-5), 1, A, A, A, A, A, A, dlam, None, ws, nbytes, None)
     assert call(dt=7) == da.ERR_DTYPE
-    assert call(dt=1) == da.ERR_UNSUPPORTED  # bf16 backward is not provided
+    assert call(dt=1, d=32) == da.ERR_UNSUPPORTED   # bf16 (tensor cores): d = 64 only
+    assert call(dt=1, q1=MIS) == da.ERR_ALIGN       # bf16 tensors: 16-byte aligned
     assert call(d=129) == da.ERR_UNSUPPORTED
     assert call(n=-1) == da.ERR_SHAPE
     assert call(dlam=None) == da.ERR_NULL
@@ -255,6 +257,74 @@ def test_v2_backward_host_validation(L):
     assert call(dlog=None) == da.ERR_NULL
     assert call(nbytes=need - 1) == da.ERR_SHAPE
     assert call(ws=P(0x100008)) == da.ERR_ALIGN
+
+
+def test_fp8qk_forward_host_validation(L):
+    def call(B=1, n=8, d=128, q1=A, s=(1.0, 1.0, 1.0, 1.0), out=A):
+        return L.diffattn_forward_fp8qk(B, 2, n, d, q1, A, A, A, *(ctypes.c_float(x) for x in s), A, A,
+                                        ctypes.c_float(0.2), None, ctypes.c_float(1e-5), 1, out, None)
+    assert call(n=-1) == da.ERR_SHAPE
+    assert call(d=64) == da.ERR_UNSUPPORTED
+    assert call(B=0) == da.OK
+    assert call(q1=None) == da.ERR_NULL
+    for bad in (0.0, -2.0, float("nan"), float("inf")):
+        for i in range(4):
+            sc = [1.0] * 4
+            sc[i] = bad
+            assert call(s=tuple(sc)) == da.ERR_SHAPE
+    assert call(q1=MIS) == da.ERR_ALIGN
+    assert call(out=MIS) == da.ERR_ALIGN
+
+
+def test_projection_host_validation(L):
+    def call(M=4, N=8, K=8, a=A, w=A, c=A):
+        return L.diffattn_projection(M, N, K, a, w, c, None)
+    assert call(M=-1) == da.ERR_SHAPE
+    assert call(K=0) == da.ERR_SHAPE
+    assert call(M=0) == da.OK and call(N=0) == da.OK
+    assert call(a=None) == da.ERR_NULL
+    assert call(K=12) == da.ERR_SHAPE      # rows must be 16-byte multiples
+    assert call(N=12) == da.ERR_SHAPE
+    assert call(w=MIS) == da.ERR_ALIGN
+
+
+def test_layer_workspace_sizes(L):
+    r256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    M, H, d = 2 * 100, 3, 64
+    assert L.diffattn_layer_workspace(2, 100, H, d) == r256(M * 6 * H * d * 2) + r256(M * 2 * H * d * 2) + 256
+    Hq, Hkv, d = 8, 2, 128
+    nq = (Hq + 2 * Hkv) * d
+    assert L.diffattn_v2_layer_workspace(2, 100, Hq, Hkv, d) == r256(M * nq * 2) + r256(M * 4 * 4) + r256(
+        M * 4 * d * 2)
+    assert L.diffattn_layer_workspace(-1, 100, H, 64) == 0
+
+
+def test_layer_host_validation(L):
+    W = P(0x100000)
+    need = L.diffattn_layer_workspace(1, 8, 2, 64)
+
+    def v1(B=1, n=8, D=256, H=2, d=64, x=A, lq=A, ws=W, nbytes=need):
+        return L.diffattn_layer_forward(B, n, D, H, d, x, A, A, lq, A, A, A, ctypes.c_float(0.2), None,
+                                        ctypes.c_float(1e-5), 1, A, ws, nbytes, None)
+    assert v1(d=96) == da.ERR_UNSUPPORTED
+    assert v1(D=250) == da.ERR_SHAPE
+    assert v1(H=0) == da.ERR_SHAPE
+    assert v1(B=0) == da.OK and v1(n=0) == da.OK
+    assert v1(x=None) == da.ERR_NULL
+    assert v1(lq=None) == da.ERR_NULL
+    assert v1(x=MIS) == da.ERR_ALIGN
+    assert v1(nbytes=need - 1) == da.ERR_SHAPE
+    assert b"workspace" in L.diffattn_last_error()
+    assert v1(ws=P(0x100010)) == da.ERR_ALIGN
+    need2 = L.diffattn_v2_layer_workspace(1, 8, 4, 2, 128)
+
+    def v2(Hq=4, Hkv=2, d=128, D=256, x=A, nbytes=need2):
+        return L.diffattn_v2_layer_forward(1, 8, D, Hq, Hkv, d, x, A, A, 1, A, W, nbytes, None)
+    assert v2(Hq=6, Hkv=2) == da.ERR_SHAPE
+    assert v2(d=64) == da.ERR_UNSUPPORTED
+    assert v2(D=100) == da.ERR_SHAPE
+    assert v2(x=None) == da.ERR_NULL
+    assert v2(nbytes=need2 - 1) == da.ERR_SHAPE
 
 
 def test_v2_host_validation(L):

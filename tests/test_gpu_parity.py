@@ -670,3 +670,64 @@ def test_v2_backward_f32(B, Hq, Hkv, n, d, causal, gran):
         scale = max(1.0, float(np.max(np.abs(r))))
         err = _err(_np(got[key]), r)
         assert err <= TOL["f32"] * scale, f"{key}: max abs error {err} (scale {scale})"
+
+
+# --------------------------------------------------------------------------- FP8 (e4m3) queries and keys
+def _quantise_e4m3(t):
+    """One scale per tensor (amax / 448) and the e4m3 codes of t / scale (torch's round-to-nearest)."""
+    scale = float(t.float().abs().max()) / 448.0
+    return (t.float() / scale).to(torch.float8_e4m3fn), scale
+
+
+def _fp8_case(w, x):
+    codes, scales = {}, []
+    for k in ("q1", "q2", "k1", "k2"):
+        codes[k], sc = _quantise_e4m3(x[k])
+        scales.append(sc)
+    lin = da.lambda_init(w.layer)
+    lam = da.lambda_reparam(x["lq1"], x["lk1"], x["lq2"], x["lk2"], lin)
+    out = da.diffattn_forward_fp8qk(codes["q1"], codes["q2"], codes["k1"], codes["k2"], scales, x["v"], lam, lin,
+                                    gamma=x["gamma"], causal=w.causal)
+    da.device_status()
+    return out, codes, dict(zip(("q1", "q2", "k1", "k2"), scales))
+
+
+def _deq(codes, scales, sel=lambda a: a):
+    """The values the codes stand for (the oracle's pinned e4m3 decoder), after a selection."""
+    return {k: oracle.dequant_e4m3(sel(codes[k]).contiguous(), scales[k]) for k in codes}
+
+
+FP8_SMALL = [  # B, H, n, causal
+    (1, 1, 1, True), (1, 2, 129, True), (2, 2, 300, False), (1, 2, 1100, True), (2, 64, 300, True),
+]
+
+
+@pytest.mark.parametrize("B,H,n,causal", FP8_SMALL)
+def test_v1_fp8qk_small_full_compare(B, H, n, causal):
+    w = shrink(WORKLOADS[3], B=B, H=H, n=n, causal=causal, seed=200 + n + H)
+    x = make_v1(w, "cuda")
+    out, codes, scales = _fp8_case(w, x)
+    deq = _deq(codes, scales)
+    lin = oracle.lambda_init(w.layer)
+    lam = oracle.lambda_reparam(x["lq1"].cpu(), x["lk1"].cpu(), x["lq2"].cpu(), x["lk2"].cpu(), lin)
+    ref = oracle.diff_attn_v1(deq["q1"], deq["q2"], deq["k1"], deq["k2"], x["v"], lam, lin, x["gamma"].cpu(), 1e-5,
+                              causal)
+    assert _err(_np(out), ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("wid", [3, 4])
+def test_v1_fp8qk_full_size_sampled(wid):
+    w = WORKLOADS[wid]
+    x = make_v1(w, "cuda")
+    out, codes, scales = _fp8_case(w, x)
+    lin = oracle.lambda_init(w.layer)
+    lam = oracle.lambda_reparam(x["lq1"].cpu(), x["lk1"].cpu(), x["lq2"].cpu(), x["lk2"].cpu(), lin)
+    assert bool(torch.isfinite(out.float()).all())
+    rows = _sample_rows(w.n, 16, wid)
+    heads = sorted(set([0, w.H - 1]))
+    for b in sorted(set([0, w.B - 1])):
+        sel = lambda a: a[b:b + 1][:, :, heads]  # noqa: E731
+        deq = _deq(codes, scales, sel)
+        ref = oracle.diff_attn_v1(deq["q1"], deq["q2"], deq["k1"], deq["k2"], sel(x["v"]), lam, lin,
+                                  x["gamma"].cpu(), 1e-5, w.causal, rows)
+        assert _err(_np(out[b:b + 1][:, rows][:, :, heads]), ref) <= TOL["bf16"]
