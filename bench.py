@@ -645,11 +645,13 @@ def time_backward(da, flush, B, H, n, d, dtype="f32", runs=10):
     return statistics.median(ts)
 
 
-def backward_results(da, flush, sm_mhz, peaks=None):
+def backward_results(da, flush, sm_mhz, peaks=None, only=None):
     out = {}
     peaks = peaks or read_peaks()
     peak32 = 2 * FP32_LANES * sm_mhz * 1e6 / 1e12
     for name, B, H, n, d, dtype in BACKWARD_WORKLOADS:
+        if only and name not in only:
+            continue
         ms = time_backward(da, flush, B, H, n, d, dtype)
         tf = backward_flops(B, H, n, d) / (ms * 1e-3) / 1e12
         if dtype == "bf16":
@@ -732,7 +734,7 @@ def _median_ms(call, flush, runs=10):
     return statistics.median(ts)
 
 
-def layer_results(da, flush, peaks):
+def layer_results(da, flush, peaks, only=None):
     """Attention layers (projections, operator, W^O) and the projection GEMM alone: TFLOP/s against the
     measured burst bf16 peak."""
     import torch
@@ -742,6 +744,8 @@ def layer_results(da, flush, peaks):
     def rnd(*shape, scale=1.0):
         return (scale * torch.randn(shape, generator=g, device="cuda")).to(torch.bfloat16)
     for name, kind, B, n, D, H, d in LAYER_WORKLOADS:
+        if only and name not in only:
+            continue
         x = rnd(B, n, D)
         if kind == "v1":
             w_qkv, w_o = rnd(6 * H * d, D, scale=D ** -0.5), rnd(D, 2 * H * d, scale=(2 * H * d) ** -0.5)
@@ -768,6 +772,8 @@ def layer_results(da, flush, peaks):
         del x, ws, y
         torch.cuda.empty_cache()
     for name, M, N, K in PROJECTION_WORKLOADS:
+        if only and name not in only:
+            continue
         a, w = rnd(M, K), rnd(N, K)
         c = torch.empty((M, N), device="cuda", dtype=torch.bfloat16)
         ms = _median_ms(lambda: da.projection(a, w, out=c), flush)
@@ -780,9 +786,11 @@ def layer_results(da, flush, peaks):
     return out
 
 
-def decode_results(da, flush, peaks):
+def decode_results(da, flush, peaks, only=None):
     out = {}
     for name, B, H, n, d, keys in DECODE_WORKLOADS:
+        if only and name not in only:
+            continue
         ms, nb = time_decode(da, flush, B, H, n, d, keys)
         gbs = nb / (ms * 1e-3) / 1e9
         out[name] = {"us": round(ms * 1e3, 1), "hbm_gbs": round(gbs, 1), "bound": "hbm",
@@ -791,16 +799,16 @@ def decode_results(da, flush, peaks):
     return out
 
 
-def run_backward_only():
+def run_backward_only(only=None):
     import torch
     from differential_attention_03_gb300 import binding as da, build
     build.build()
     da.lib()
     flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
-    print(json.dumps({"backward": backward_results(da, flush, 2070)}), flush=True)
+    print(json.dumps({"backward": backward_results(da, flush, 2070, None, only)}), flush=True)
 
 
-def run_layer_only():
+def run_layer_only(only=None):
     import torch
     from differential_attention_03_gb300 import binding as da, build
     build.build()
@@ -808,17 +816,19 @@ def run_layer_only():
     flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
     from differential_attention_03_gb300.inputs import make_v1
     peaks = read_peaks()
-    print(json.dumps({"layer": layer_results(da, flush, peaks),
-                      "fp8": fp8_results(da, flush, peaks, lambda w: make_v1(w, "cuda"))}), flush=True)
+    line = {"layer": layer_results(da, flush, peaks, only)}
+    if not only:
+        line["fp8"] = fp8_results(da, flush, peaks, lambda w: make_v1(w, "cuda"))
+    print(json.dumps(line), flush=True)
 
 
-def run_decode_only():
+def run_decode_only(only=None):
     import torch
     from differential_attention_03_gb300 import binding as da, build
     build.build()
     da.lib()
     flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
-    print(json.dumps({"decode": decode_results(da, flush, read_peaks())}), flush=True)
+    print(json.dumps({"decode": decode_results(da, flush, read_peaks(), only)}), flush=True)
 
 
 def main(argv=None):
@@ -837,6 +847,8 @@ def main(argv=None):
                     help="time only the decode workloads (one JSON line with the 'decode' object)")
     ap.add_argument("--layer-only", action="store_true",
                     help="time only the attention layers, the projection GEMM and the FP8 forward (one JSON line)")
+    ap.add_argument("--workload", action="append", default=None,
+                    help="with --decode-only / --backward-only / --layer-only: time only the named workload(s)")
     ap.add_argument("--backward-only", action="store_true",
                     help="time only the fp32 backward workloads (one JSON line with the 'backward' object)")
     args = ap.parse_args(argv)
@@ -853,11 +865,11 @@ def main(argv=None):
     if args.impl == "reference":
         run_reference(args)
     elif args.decode_only:
-        run_decode_only()
+        run_decode_only(args.workload)
     elif args.backward_only:
-        run_backward_only()
+        run_backward_only(args.workload)
     elif args.layer_only:
-        run_layer_only()
+        run_layer_only(args.workload)
     else:
         run_ours(args)
 

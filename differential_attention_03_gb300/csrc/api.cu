@@ -158,6 +158,26 @@ diffattn_status make_map_2d(CUtensorMap* m, const void* base, long long rows, lo
   return DIFFATTN_OK;
 }
 
+// 4-D map over a contiguous BSHD fp32 tensor [B, n, heads, W]: box = 32 columns
+// (128 bytes, 128-byte swizzle) x 1 head x `rows` tokens x 1 batch (the
+// tensor-core backward adds dQ tiles into it with TMA reduce-adds).
+diffattn_status make_map_f32(CUtensorMap* m, const void* base, int B, int n, int heads, int W, int rows) {
+  EncodeTiledFn enc;
+  diffattn_status s = get_encoder(&enc);
+  if (s != DIFFATTN_OK) return s;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(heads),
+                              static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(W) * 4, static_cast<cuuint64_t>(W) * heads * 4,
+                                 static_cast<cuuint64_t>(W) * heads * n * 4};
+  const cuuint32_t box[4] = {32, 1, static_cast<cuuint32_t>(rows), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DIFFATTN_ERR_CUDA, "cuTensorMapEncodeTiled (f32) failed (CUresult %d)", (int)r);
+  return DIFFATTN_OK;
+}
+
 // Load maps: 64-column boxes (128-byte rows, 128-byte swizzle).
 diffattn_status make_map(CUtensorMap* m, const void* base, int B, int n, int heads, int W, int rows) {
   return make_map_box(m, base, B, n, heads, W, 64, rows);
@@ -1101,6 +1121,8 @@ diffattn_status backward_v1_tc(int B, int H, int n, const void* q1, const void* 
   __nv_bfloat16* ws_do = reinterpret_cast<__nv_bfloat16*>(ws);
   float* ws_row = reinterpret_cast<float*>(ws + round256(R * dv_w * 2));
   float* ws_dg = reinterpret_cast<float*>(ws + round256(R * dv_w * 2) + round256(6 * R * 4));
+  float* ws_dl = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws_dg) +
+                                          round256(static_cast<size_t>(stats_grid) * dv_w * 4));
   const float sc = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   diffattn_status st;
   // 1. statistics: the forward's maps, dy in; lse, Delta, shares, dO and dgamma shares out
@@ -1129,6 +1151,7 @@ diffattn_status backward_v1_tc(int B, int H, int n, const void* q1, const void* 
   p.dO = ws_do;
   p.row = ws_row;
   p.dgp = ws_dg;
+  p.dlam_part = ws_dl;
   p.rows = static_cast<long long>(R);
   cudaError_t e = cudaMemsetAsync(dq1, 0, R * d * 4, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(dq2, 0, R * d * 4, s);
@@ -1143,6 +1166,8 @@ diffattn_status backward_v1_tc(int B, int H, int n, const void* q1, const void* 
   if ((st = make_map(&t.tm_k2, k2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
   if ((st = make_map(&t.tm_v, v, B, n, H, dv_w, 128)) != DIFFATTN_OK) return st;
   if ((st = make_map(&t.tm_do, ws_do, B, n, H, dv_w, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_f32(&t.tm_dq1, dq1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_f32(&t.tm_dq2, dq2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
   t.row = ws_row;
   t.lambda = lambda;
   t.dq1 = static_cast<float*>(dq1);
@@ -1166,6 +1191,7 @@ diffattn_status backward_v1_tc(int B, int H, int n, const void* q1, const void* 
   da::BwdParams r{};
   r.row = ws_row;
   r.dgp = ws_dg;
+  r.dlam_parts = ws_dl;
   r.dlambda = dlambda;
   r.dgamma = dgamma;
   r.B = B;
@@ -1234,6 +1260,8 @@ diffattn_status backward_v2_tc(int B, int Hq, int Hkv, int n, const void* q, con
   t.tm_k2 = t.tm_k1;
   if ((st = make_map(&t.tm_v, v, B, n, Hkv, d, 128)) != DIFFATTN_OK) return st;
   if ((st = make_map(&t.tm_do, dy, B, n, G, d, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_f32(&t.tm_dq1, dq, B, n, Hq, d, 128)) != DIFFATTN_OK) return st;
+  t.tm_dq2 = t.tm_dq1;
   t.row = ws_row;
   t.dq1 = t.dq2 = static_cast<float*>(dq);
   t.dk1 = static_cast<float*>(dk);

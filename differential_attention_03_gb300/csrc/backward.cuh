@@ -379,6 +379,8 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_reduce_kernel(const BwdParams
       const float* sr = share + (static_cast<long long>(b) * p.units + g) * p.n;
       for (int t = threadIdx.x; t < p.n; t += kBwdThreads) a += sr[t];
     }
+  } else if (p.dlam_parts != nullptr) {
+    for (int k = threadIdx.x; k < p.n_row_ctas; k += kBwdThreads) a += p.dlam_parts[k];
   } else {
     for (long long r = threadIdx.x; r < p.rows; r += kBwdThreads) a += share[r];
   }

@@ -25,6 +25,7 @@ struct BwdParams {
   const float* dO;      // [B * units * n][dv] (row pass)
   const float* row;     // [6][B * units * n]: lse_1, lse_2, D_1, D_2, dlambda / dlogit share, coefficient
   const float* dgp;     // [n_row_ctas][dv]: dgamma shares (V1 row pass)
+  const float* dlam_parts;  // V1: [n_row_ctas] dlambda shares of whole CTAs, or nullptr (then the rows' shares)
   const float* lambda;  // V1 device scalar
   float* dq1;           // V1: [B, n, H, d]; V2: dq [B, n, Hq, d] (dq1 == dq2)
   float* dq2;

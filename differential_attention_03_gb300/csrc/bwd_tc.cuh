@@ -27,18 +27,23 @@
 //   warp 2      MMAs dP^T, dV += Pc^T dO (Pc^T from TMEM), dQ_1 = dS_1 K_1.
 //               (dQ_1 follows dV in the same warp, so it overwrites Pc^T only
 //               after dV has read it: MMAs of one thread run in order.)
-//   warps 4-11  two warpgroups, thread = key row; warpgroup h takes query
-//               columns [64 h, +64): phase 1 P_1, dS_1 (kept: P_1 as bf16
-//               pairs in registers, dS_1^T to shared memory); phase 2 P_2,
+//   warps 3-18  four warpgroups, thread = key row; warpgroup h takes query
+//               columns [32 h, +32): phase 1 P_1, dS_1 (dS_1^T to shared
+//               memory, P_1 kept as bf16 pairs in registers); phase 2 P_2,
 //               dS_2, Pc = P_1 + c_2 P_2 (Pc^T to TMEM over S_2^T); then the
-//               tile's dQ (thread = query row): scaled and added to the fp32
-//               dQ in global memory with vector atomics.
+//               tile's dQ (thread = query row): scaled, staged in the dS^T
+//               buffers and added to the fp32 dQ in global memory by TMA bulk
+//               reduce-adds; the next step's row statistics are fetched
+//               meanwhile.  (V1 issues the dQ MMAs before dV and dK, so dQ is
+//               read out while they run.)
 // dS^T tiles are bf16 [128 keys][128 queries] in two 64-query boxes (128-byte
 // rows, 128-byte swizzle): K-major A of dK += dS^T Q, and read as the
 // M-major A of dQ = dS K.  Every wait is bounded (abort flag, status word).
 #pragma once
 
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "bwd_tc_params.h"
 #include "ptx.cuh"
@@ -52,7 +57,7 @@ struct BwdTcCfg {
   static constexpr int D = V2 ? 128 : 64;
   static constexpr int DV = 128;
   static constexpr int NK = V2 ? 1 : 2;  // key tiles held (K_1, K_2 or the shared K)
-  static constexpr int NTHREADS = 384;
+  static constexpr int NTHREADS = 608;  // warp 0 TMA, warps 1-2 MMA, warps 3-18 softmax
   static constexpr int KT = 128 * D * 2;  // a 128-row query or key tile
   static constexpr int VT = 128 * DV * 2;
   static constexpr int ST = 128 * 128 * 2;  // a dS^T tile
@@ -62,17 +67,21 @@ struct BwdTcCfg {
   static constexpr int OFF_Q1 = OFF_V + VT;
   static constexpr int OFF_Q2 = OFF_Q1 + KT;
   static constexpr int OFF_DO = OFF_Q2 + KT;
-  static constexpr int OFF_DS1 = OFF_DO + VT;
+  // dO of the next query tile loads while the current one is in use (V1; V2 has no room for it).
+  static constexpr int NDO = V2 ? 1 : 2;
+  static constexpr int OFF_DS1 = OFF_DO + NDO * VT;
   static constexpr int OFF_DS2 = OFF_DS1 + ST;
   static constexpr int OFF_ST = OFF_DS2 + ST;  // float [5][128]: lse_1, lse_2, Delta_1, Delta_2, c_2 of the tile's queries
   static constexpr int OFF_BARS = OFF_ST + 5 * 128 * 4;
-  static constexpr int NBARS = 13;
+  static constexpr int NBARS = 20;
   static constexpr int OFF_MISC = OFF_BARS + NBARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16;  // the base is 1024-byte aligned (checked)
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TM_DV = 0, TM_DK1 = 128, TM_DK2 = 128 + D, TM_S = 256, TM_DP = 384;
-  static constexpr uint32_t TM_PC = TM_S;                    // Pc^T: 128 queries as 64 columns of bf16 pairs
-  static constexpr uint32_t TM_DQ1 = V2 ? TM_S : TM_S + 64;  // V1: beside Pc^T; V2: over it, after dV
+  // Pc^T as bf16 pairs over S_2^T, each warpgroup over its own S columns: queries [32 h, +32) at
+  // pair columns TM_S + 32 h + [0, 16), so k-step k (16 queries) of dV reads TM_S + 32 (k / 2) + 8 (k % 2).
+  static constexpr uint32_t TM_PC = TM_S;
+  static constexpr uint32_t TM_DQ1 = V2 ? TM_S : TM_DP + 64;  // V2: over Pc^T, after dV; V1: beside dQ_2
   static constexpr uint32_t TM_DQ2 = TM_DP;
   static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);  // S^T = K Q^T, dP^T = V dO^T
   static constexpr uint32_t IDESC_DV = idesc_bf16(128, DV, false, true);   // dV += Pc^T dO
@@ -88,25 +97,30 @@ __device__ __forceinline__ void bf16x2_unpack(uint32_t w, float& lo, float& hi) 
 }
 
 template <bool V2>
-__global__ void __launch_bounds__(384, 1) bwd_tc_kernel(const __grid_constant__ BwdTcParams p) {
+__global__ void __launch_bounds__(608, 1) bwd_tc_kernel(const __grid_constant__ BwdTcParams p) {
   using C = BwdTcCfg<V2>;
   constexpr int D = C::D, DV = C::DV;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
-  uint64_t* kv_full = bars + 0;   // K and V of the CTA landed
-  uint64_t* q_full = bars + 1;    // Q_1, Q_2, dO of the query tile landed
-  uint64_t* q_empty = bars + 2;   // both MMA warps' last reads of the tile's Q_1, Q_2, dO done (2)
-  uint64_t* s_full = bars + 3;    // S_1^T, then S_2^T, in the S columns (twice per tile)
-  uint64_t* dp_full = bars + 4;   // dP^T in the dP columns
-  uint64_t* s1_free = bars + 5;   // the softmax warps have loaded S_1^T (8)
-  uint64_t* p1_ready = bars + 6;  // dS_1^T in shared memory (8)
-  uint64_t* p2_ready = bars + 7;  // dS_2^T in shared memory, Pc^T in TMEM, dP^T loaded (8)
-  uint64_t* dq_full = bars + 8;   // dQ_1, dQ_2 of the tile complete (2)
-  uint64_t* dq_free = bars + 9;   // the softmax warps have read dQ_1, dQ_2 (8)
-  uint64_t* acc_done = bars + 10; // every MMA of the CTA complete (2)
-  uint64_t* mma_done = bars + 11; // [2] abort drain of each MMA warp
+  uint64_t* kv_full = bars + 0;    // K and V of the CTA landed
+  uint64_t* q1_full = bars + 1;    // Q_1 of the step landed
+  uint64_t* q2_full = bars + 2;    // Q_2 of the step landed
+  uint64_t* do_full = bars + 3;    // [2] dO of the step landed in buffer s % NDO
+  uint64_t* q1_empty = bars + 5;   // the MMAs reading Q_1 (S_1^T, dK of map 1) done
+  uint64_t* q2_empty = bars + 6;   // the MMAs reading Q_2 (S_2^T, dK of map 2) done
+  uint64_t* do_empty = bars + 7;   // [2] the MMAs reading dO buffer b (dP^T, dV) done
+  uint64_t* s_full = bars + 9;     // S_1^T, then S_2^T, in the S columns (twice per step)
+  uint64_t* dp_full = bars + 10;   // dP^T in the dP columns
+  uint64_t* s1_free = bars + 11;   // the softmax warps have loaded S_1^T (16)
+  uint64_t* p1_ready = bars + 12;  // dS_1^T in shared memory (16)
+  uint64_t* p2_ready = bars + 13;  // dS_2^T in shared memory, Pc^T in TMEM, dP^T loaded (16)
+  uint64_t* dq_full = bars + 14;   // dQ_1, dQ_2 of the step complete (2)
+  uint64_t* dq_free = bars + 15;   // the softmax warps have read dQ_1, dQ_2 (16)
+  uint64_t* acc_done = bars + 16;  // every MMA of the CTA complete (2)
+  uint64_t* mma_done = bars + 17;  // [2] abort drain of each MMA warp
+  uint64_t* ds_done = bars + 19;   // every MMA of the step reading dS^T, Pc^T complete (2)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   float* sst = reinterpret_cast<float*>(smem + C::OFF_ST);
@@ -133,18 +147,25 @@ __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 2);
+    mbar_init(q1_full, 1);
+    mbar_init(q2_full, 1);
+    mbar_init(q1_empty, 1);
+    mbar_init(q2_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&do_full[i], 1);
+      mbar_init(&do_empty[i], 1);
+    }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(s1_free, 8);
-    mbar_init(p1_ready, 8);
-    mbar_init(p2_ready, 8);
+    mbar_init(s1_free, 16);
+    mbar_init(p1_ready, 16);
+    mbar_init(p2_ready, 16);
     mbar_init(dq_full, 2);
-    mbar_init(dq_free, 8);
+    mbar_init(dq_free, 16);
     mbar_init(acc_done, 2);
     mbar_init(&mma_done[0], 1);
     mbar_init(&mma_done[1], 1);
+    mbar_init(ds_done, 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -171,23 +192,55 @@ __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(const __grid_constant__ 
         if (!V2) tma_load_4d(smem + C::OFF_K2 + bx * 16384, &p.tm_k2, kv_full, bx * 64, hk, j0, b);
       }
       for (int bx = 0; bx < DV / 64; ++bx) tma_load_4d(smem + C::OFF_V + bx * 16384, &p.tm_v, kv_full, bx * 64, hk, j0, b);
-      int loaded = 0;
-      for (int s = 0; s < nsteps; ++s) {
-        if (s > 0 && !mbar_wait(q_empty, static_cast<uint32_t>(s - 1) & 1u, ab)) break;
-        const int u = step_pair(s), q0 = step_tile(s) * 128;
-        const int hq1 = V2 ? 2 * u : u, hq2 = V2 ? 2 * u + 1 : u;
-        mbar_arrive_expect_tx(q_full, 2 * C::KT + C::VT);
-        for (int bx = 0; bx < D / 64; ++bx) {
-          tma_load_4d(smem + C::OFF_Q1 + bx * 16384, &p.tm_q1, q_full, bx * 64, hq1, q0, b);
-          tma_load_4d(smem + C::OFF_Q2 + bx * 16384, V2 ? &p.tm_q1 : &p.tm_q2, q_full, bx * 64, hq2, q0, b);
+      // Per step: Q_1 (released mid-step by map 1's dK), Q_2 (released by map 2's dK) and dO (released
+      // by dV; with two buffers the next step's loads during this one).
+      int nq1 = 0, nq2 = 0, ndo[2] = {0, 0};
+      bool ok = true;
+      auto load_q = [&](int st_, int r) {  // r = 0: Q_1, 1: Q_2
+        int& cnt = r == 0 ? nq1 : nq2;
+        if (cnt > 0 && !mbar_wait(r == 0 ? q1_empty : q2_empty, static_cast<uint32_t>(cnt - 1) & 1u, ab)) {
+          ok = false;
+          return;
         }
-        for (int bx = 0; bx < DV / 64; ++bx) tma_load_4d(smem + C::OFF_DO + bx * 16384, &p.tm_do, q_full, bx * 64, u, q0, b);
-        ++loaded;
+        const int u = step_pair(st_), q0 = step_tile(st_) * 128;
+        const int hq = V2 ? 2 * u + r : u;
+        uint64_t* bar = r == 0 ? q1_full : q2_full;
+        mbar_arrive_expect_tx(bar, C::KT);
+        for (int bx = 0; bx < D / 64; ++bx)
+          tma_load_4d(smem + (r == 0 ? C::OFF_Q1 : C::OFF_Q2) + bx * 16384, (V2 || r == 0) ? &p.tm_q1 : &p.tm_q2,
+                      bar, bx * 64, hq, q0, b);
+        ++cnt;
+      };
+      auto load_do = [&](int st_) {
+        const int db = st_ % C::NDO;
+        if (ndo[db] > 0 && !mbar_wait(&do_empty[db], static_cast<uint32_t>(ndo[db] - 1) & 1u, ab)) {
+          ok = false;
+          return;
+        }
+        const int u = step_pair(st_), q0 = step_tile(st_) * 128;
+        mbar_arrive_expect_tx(&do_full[db], C::VT);
+        for (int bx = 0; bx < DV / 64; ++bx)
+          tma_load_4d(smem + C::OFF_DO + db * C::VT + bx * 16384, &p.tm_do, &do_full[db], bx * 64, u, q0, b);
+        ++ndo[db];
+      };
+      for (int s = 0; ok && s < nsteps; ++s) {
+        // In the order the tiles are released: V1 dO (double-buffered) first, V2 Q_1 first.
+        if (V2) {
+          load_q(s, 0);
+          if (ok) load_do(s);
+        } else {
+          load_do(s);
+          if (ok) load_q(s, 0);
+        }
+        if (ok) load_q(s, 1);
       }
       if (*ab.flag) {
         // Aborted: the copies already issued land before the CTA exits.
         mbar_wait_drain(kv_full, 0, kWaitBudgetCycles);
-        if (loaded > 0) mbar_wait_drain(q_full, static_cast<uint32_t>(loaded - 1) & 1u, kWaitBudgetCycles);
+        if (nq1 > 0) mbar_wait_drain(q1_full, static_cast<uint32_t>(nq1 - 1) & 1u, kWaitBudgetCycles);
+        if (nq2 > 0) mbar_wait_drain(q2_full, static_cast<uint32_t>(nq2 - 1) & 1u, kWaitBudgetCycles);
+        for (int i = 0; i < 2; ++i)
+          if (ndo[i] > 0) mbar_wait_drain(&do_full[i], static_cast<uint32_t>(ndo[i] - 1) & 1u, kWaitBudgetCycles);
       }
     }
   } else if (warp == 1 || warp == 2) {
@@ -212,17 +265,17 @@ __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(const __grid_constant__ 
     bool ok = waitp(kv_full, 0);
     for (int s = 0; ok && s < nsteps; ++s) {
       const uint32_t ph = static_cast<uint32_t>(s) & 1u;
-      if (!waitp(q_full, ph) || (s > 0 && !waitp(dq_free, ph ^ 1u))) {
-        ok = false;
-        break;
-      }
       if (mw == 0) {
-        // S_1^T = K_1 Q_1^T, then (once the softmax has loaded it) S_2^T = K_2 Q_2^T
+        // S_1^T = K_1 Q_1^T; once the softmax has loaded it, S_2^T = K_2 Q_2^T (same columns)
+        if (!waitp(q1_full, ph) || (s > 0 && (!waitp(dq_free, ph ^ 1u) || !waitp(ds_done, ph ^ 1u)))) {
+          ok = false;
+          break;
+        }
 #pragma unroll
         for (int k = 0; k < D / 16; ++k)
           mma_ss_elect(tmem + C::TM_S, dK1 + kstep(k), dQ1 + kstep(k), C::IDESC_S, k > 0 ? 1u : 0u);
         tc_commit_elect(s_full);
-        if (!waitp(s1_free, ph)) {
+        if (!waitp(s1_free, ph) || !waitp(q2_full, ph)) {
           ok = false;
           break;
         }
@@ -230,239 +283,323 @@ __global__ void __launch_bounds__(384, 1) bwd_tc_kernel(const __grid_constant__ 
         for (int k = 0; k < D / 16; ++k)
           mma_ss_elect(tmem + C::TM_S, dK2 + kstep(k), dQ2 + kstep(k), C::IDESC_S, k > 0 ? 1u : 0u);
         tc_commit_elect(s_full);
-        const uint32_t acc0 = s > 0 ? 1u : 0u;
-        if (!V2) {
-          // dK_1 += dS_1^T Q_1 while the softmax works on map 2
-          if (!waitp(p1_ready, ph)) {
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ss_elect(tmem + C::TM_DK1, kS1 + kstep(k), mQ1 + mstep(k), C::IDESC_DK, (acc0 | k) ? 1u : 0u);
+        // dK += dS_1^T Q_1 while the softmax works on map 2; Q_1 is then free for the next step.
+        if (!waitp(p1_ready, ph)) {
+          ok = false;
+          break;
         }
+        const uint32_t acc0 = s > 0 ? 1u : 0u;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ss_elect(tmem + C::TM_DK1, kS1 + kstep(k), mQ1 + mstep(k), C::IDESC_DK, (acc0 | k) ? 1u : 0u);
+        tc_commit_elect(q1_empty);
         if (!waitp(p2_ready, ph)) {
           ok = false;
           break;
         }
-        if (V2) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ss_elect(tmem + C::TM_DK1, kS1 + kstep(k), mQ1 + mstep(k), C::IDESC_DK, (acc0 | k) ? 1u : 0u);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) mma_ss_elect(tmem + C::TM_DK1, kS2 + kstep(k), mQ2 + mstep(k), C::IDESC_DK, 1u);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_ss_elect(tmem + C::TM_DK2, kS2 + kstep(k), mQ2 + mstep(k), C::IDESC_DK, (acc0 | k) ? 1u : 0u);
-        }
-        tc_commit_elect(q_empty);
-        // dQ_2 = dS_2 K_2 over the dP columns (the softmax has loaded dP^T)
+        // dQ_2 = dS_2 K_2 over the dP columns (the softmax has loaded dP^T), first: the softmax
+        // warps read it out while dK accumulates.
 #pragma unroll
         for (int k = 0; k < 8; ++k) mma_ss_elect(tmem + C::TM_DQ2, mS2 + mstep(k), mK2 + mstep(k), C::IDESC_DQ, k > 0 ? 1u : 0u);
         tc_commit_elect(dq_full);
+        // dK of map 2: V1 its own accumulator, V2 the shared K's
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ss_elect(tmem + (V2 ? C::TM_DK1 : C::TM_DK2), kS2 + kstep(k), mQ2 + mstep(k), C::IDESC_DK,
+                       (V2 || acc0 || k) ? 1u : 0u);
+        tc_commit_elect(q2_empty);
+        tc_commit_elect(ds_done);
       } else {
         // dP^T = V dO^T
+        const int db = s % C::NDO;
+        const uint64_t dbo = static_cast<uint64_t>((db * C::VT) >> 4);
+        if (!waitp(&do_full[db], static_cast<uint32_t>(s / C::NDO) & 1u) || (s > 0 && !waitp(dq_free, ph ^ 1u))) {
+          ok = false;
+          break;
+        }
 #pragma unroll
         for (int k = 0; k < DV / 16; ++k)
-          mma_ss_elect(tmem + C::TM_DP, dV + kstep(k), dDO + kstep(k), C::IDESC_S, k > 0 ? 1u : 0u);
+          mma_ss_elect(tmem + C::TM_DP, dV + kstep(k), dDO + dbo + kstep(k), C::IDESC_S, k > 0 ? 1u : 0u);
         tc_commit_elect(dp_full);
         if (!waitp(p2_ready, ph)) {
           ok = false;
           break;
         }
-        // dV += Pc^T dO, Pc^T from TMEM (k-step k: queries 16 k .. 16 k + 15 = pair columns 8 k .. 8 k + 7)
+        // dV += Pc^T dO, Pc^T from TMEM, and dQ_1 = dS_1 K_1: V1 dQ_1 first (its columns are in the
+        // dP buffer), V2 after dV (dQ_1 overwrites Pc^T; MMAs of one thread run in order).
         const uint32_t acc0 = s > 0 ? 1u : 0u;
+        auto dq1_mmas = [&]() {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mma_ss_elect(tmem + C::TM_DQ1, mS1 + mstep(k), mK1 + mstep(k), C::IDESC_DQ, k > 0 ? 1u : 0u);
+          tc_commit_elect(dq_full);
+        };
+        if (!V2) dq1_mmas();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts_elect(tmem + C::TM_DV, tmem + C::TM_PC + 8u * k, mDO + mstep(k), C::IDESC_DV, (acc0 | k) ? 1u : 0u);
-        tc_commit_elect(q_empty);
-        // dQ_1 = dS_1 K_1 (after dV in this warp's order: it may overwrite Pc^T)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mma_ss_elect(tmem + C::TM_DQ1, mS1 + mstep(k), mK1 + mstep(k), C::IDESC_DQ, k > 0 ? 1u : 0u);
-        tc_commit_elect(dq_full);
+          mma_ts_elect(tmem + C::TM_DV, tmem + C::TM_PC + 32u * (k >> 1) + 8u * (k & 1), mDO + dbo + mstep(k),
+                       C::IDESC_DV, (acc0 | k) ? 1u : 0u);
+        tc_commit_elect(&do_empty[db]);
+        if (V2) dq1_mmas();
+        tc_commit_elect(ds_done);
       }
     }
     if (ok) tc_commit_elect(acc_done);
     tc_commit_elect(&mma_done[mw]);
     if (*ab.flag) mbar_wait_drain(&mma_done[mw], 0, kWaitBudgetCycles);
     __syncwarp();
-  } else if (warp >= 4) {
+  } else {
     // ================================================================ softmax, dQ, epilogue
-    const int h = (warp - 4) >> 2;  // query columns [64 h, +64)
-    const int wq = warp & 3;        // TMEM lane quarter
+    // Four warpgroups (warps 3-18): warpgroup h takes query columns [32 h, +32) of the step in two
+    // 16-column parts; thread = key row (TMEM lane quarter warp % 4).
+    const int h = (warp - 3) >> 2;
+    const int wq = warp & 3;
     const int kr = wq * 32 + lane;  // key row (softmax) / query row (dQ)
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const int key = j0 + kr;
     const bool key_ok = key < p.n;
     const float sc = p.scale_log2;
     const float lam_c2 = V2 ? 0.f : -*p.lambda;
-    const int t256 = threadIdx.x - 128;
-    uint8_t* const ds1_row = smem + C::OFF_DS1 + h * 16384 + kr * 128;
-    uint8_t* const ds2_row = smem + C::OFF_DS2 + h * 16384 + kr * 128;
-    // These warps meet at named barriers, so none leaves the loop early: after
-    // an abort every wait returns at once and the remaining steps run through
-    // (their results are not used).
+    const int t512 = threadIdx.x - 96;
+    const bool lead = (t512 & 127) == 0;  // issues the warpgroup's bulk reduce-adds
+    // The warpgroup's 32 columns in the dS^T tiles: 64-query box h / 2, 16-byte chunks 4 (h % 2) .. + 3.
+    uint8_t* const ds1_row = smem + C::OFF_DS1 + (h >> 1) * 16384 + kr * 128;
+    uint8_t* const ds2_row = smem + C::OFF_DS2 + (h >> 1) * 16384 + kr * 128;
+    const int chunk0 = 4 * (h & 1);
+    // These warps meet at named barriers, so none leaves the loop early: after an abort every wait
+    // returns at once and the remaining steps run through (their results are not used).
+    // The statistics of a step's 128 queries (lse_1, lse_2, Delta_1, Delta_2, c_2): each of the 512
+    // threads fetches up to two of the 640 values, for the next step while the current one ends.
+    auto fetch_stats = [&](int st_, float (&v)[2]) {
+      const int u_ = step_pair(st_), q0_ = step_tile(st_) * 128;
+      const long long r0 = (static_cast<long long>(b) * p.units + u_) * p.n + q0_;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int idx = t512 + 512 * e;
+        const int a = idx >> 7, qq = idx & 127;
+        const bool in = q0_ + qq < p.n;
+        float x = 0.f;
+        if (idx < 5 * 128) {
+          if (a < 4)
+            x = in ? p.row[a * p.rows + r0 + qq] : (a < 2 ? INFINITY : 0.f);
+          else
+            x = V2 ? (in ? -p.row[5 * p.rows + r0 + qq] : 0.f) : lam_c2;
+        }
+        v[e] = x;
+      }
+    };
+    float pre[2];
+    fetch_stats(0, pre);
     for (int s = 0; s < nsteps; ++s) {
       const uint32_t ph = static_cast<uint32_t>(s) & 1u;
       const int u = step_pair(s), q0 = step_tile(s) * 128;
-      // ---- the statistics of the tile's 128 queries -> shared memory
-      named_bar_sync(1, 256);  // everyone is done with the previous tile's
-      const long long r0 = (static_cast<long long>(b) * p.units + u) * p.n + q0;
-      for (int idx = t256; idx < 5 * 128; idx += 256) {
-        const int a = idx >> 7, qq = idx & 127;
-        const bool in = q0 + qq < p.n;
-        float v;
-        if (a < 4)
-          v = in ? p.row[a * p.rows + r0 + qq] : (a < 2 ? INFINITY : 0.f);
-        else
-          v = V2 ? (in ? -p.row[5 * p.rows + r0 + qq] : 0.f) : lam_c2;
-        sst[idx] = v;
+      // ---- the step's statistics -> shared memory (fetched during the previous step); the first
+      // barrier: every thread is done with the previous step's.
+      named_bar_sync(1, 512);
+      // Layout: (lse_1, Delta_1) pairs of the 128 queries, then (lse_2, Delta_2) pairs, then c_2.
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int idx = t512 + 512 * e;
+        if (idx < 5 * 128) {
+          const int a = idx >> 7, qq = idx & 127;
+          const int pos = a == 4 ? 512 + qq : (a & 1) * 256 + 2 * qq + (a >> 1);
+          sst[pos] = pre[e];
+        }
       }
-      named_bar_sync(1, 256);
-      const float* lse1 = sst + 64 * h;
-      const float* lse2 = lse1 + 128;
-      const float* del1 = lse1 + 256;
-      const float* del2 = lse1 + 384;
-      const float* cf2 = lse1 + 512;
-      const int qbase = q0 + 64 * h;  // first query of this thread's columns
+      named_bar_sync(1, 512);
+      const float4* st1 = reinterpret_cast<const float4*>(sst) + 16 * h;        // (lse_1, Delta_1) x 2 columns
+      const float4* st2 = reinterpret_cast<const float4*>(sst + 256) + 16 * h;  // (lse_2, Delta_2) x 2 columns
+      const float* cf2 = sst + 512 + 32 * h;
+      const int qbase = q0 + 32 * h;  // first query of this thread's columns
+      // Every key of the tile precedes every query (or no mask applies) and no row is past n: no
+      // per-column mask (every step except the diagonal and ragged ones).
+      const bool full = (!p.causal || q0 > j0) && q0 + 128 <= p.n && j0 + 128 <= p.n;
       auto visible = [&](int cidx) {
         const int tq = qbase + cidx;
         return key_ok && tq < p.n && (!p.causal || key <= tq);
       };
-      // ---- phase 1: P_1, dS_1 = P_1 (dP - Delta_1)
-      mbar_wait(s_full, 0, ab);
-      mbar_wait(dp_full, ph, ab);
-      __syncwarp();
-      tc_fence_after();
-      uint32_t sv[2][32];
-      tmem_ld32(tl + C::TM_S + 64u * h, sv[0]);
-      tmem_ld32(tl + C::TM_S + 64u * h + 32u, sv[1]);
-      tmem_ld_wait2(sv[0], sv[1]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s1_free);  // S_2^T may overwrite the S columns
-      __syncwarp();
-      uint32_t p1k[32];  // P_1 of the 64 columns as bf16 pairs
+      const uint64_t sc2 = f2pack(sc, sc);
+      // The two phases, compiled with and without the per-column mask (a branch in every column pair
+      // of the unrolled loops would split them into short blocks).
+      auto phases = [&](auto full_tag) {
+        constexpr bool FULL = decltype(full_tag)::value;
+        // P of columns c0, c0 + 1 (x = s sc - lse, exp2), with their Delta pair.
+        auto probs = [&](uint32_t sa, uint32_t sb, const float4& st, int c0, uint64_t& del) -> uint64_t {
+          float xa, xb;
+          f2unpack(fma2(f2pack(__uint_as_float(sa), __uint_as_float(sb)), sc2, f2pack(-st.x, -st.z)), xa, xb);
+          float pa = ex2(xa), pb = ex2(xb);
+          if constexpr (!FULL) {
+            if (!visible(c0)) pa = 0.f;
+            if (!visible(c0 + 1)) pb = 0.f;
+          }
+          del = f2pack(-st.y, -st.w);
+          return f2pack(pa, pb);
+        };
+        // ---- phase 1: P_1, dS_1 = P_1 (dP - Delta_1); dS_1^T to its buffer, P_1 kept as bf16 pairs.
+        uint32_t p1k[16];
+        mbar_wait(s_full, 0, ab);
+        mbar_wait(dp_full, ph, ab);
+        __syncwarp();
+        tc_fence_after();
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t dp[32];
-        tmem_ld32(tl + C::TM_DP + 64u * h + 32u * q, dp);
-        tmem_ld_wait(dp);
-        uint32_t dsk[16];
+        for (int q = 0; q < 2; ++q) {
+          uint32_t sv[16], dp[16];
+          tmem_ld16(tl + C::TM_S + 32u * h + 16u * q, sv);
+          tmem_ld16(tl + C::TM_DP + 32u * h + 16u * q, dp);
+          tmem_ld_wait16x2(sv, dp);
+          if (q == 1) {  // every S_1^T column of the thread is loaded: S_2^T may overwrite them
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s1_free);
+            __syncwarp();
+          }
+          uint32_t dsk[8];
 #pragma unroll
-        for (int cc = 0; cc < 32; cc += 2) {
-          const int c0 = 32 * q + cc;
-          const float pa = visible(c0) ? ex2(fmaf(__uint_as_float(sv[q][cc]), sc, -lse1[c0])) : 0.f;
-          const float pb = visible(c0 + 1) ? ex2(fmaf(__uint_as_float(sv[q][cc + 1]), sc, -lse1[c0 + 1])) : 0.f;
-          const float da = pa * (__uint_as_float(dp[cc]) - del1[c0]);
-          const float db = pb * (__uint_as_float(dp[cc + 1]) - del1[c0 + 1]);
-          p1k[16 * q + (cc >> 1)] = pack_bf16x2(pa, pb);
-          dsk[cc >> 1] = pack_bf16x2(da, db);
+          for (int cc = 0; cc < 16; cc += 2) {
+            const int c0 = 16 * q + cc;
+            uint64_t del;
+            const uint64_t pp = probs(sv[cc], sv[cc + 1], st1[c0 >> 1], c0, del);
+            const uint64_t ds = mul2(pp, add2(f2pack(__uint_as_float(dp[cc]), __uint_as_float(dp[cc + 1])), del));
+            float pa, pb, xa, xb;
+            f2unpack(pp, pa, pb);
+            f2unpack(ds, xa, xb);
+            p1k[8 * q + (cc >> 1)] = pack_bf16x2(pa, pb);
+            dsk[cc >> 1] = pack_bf16x2(xa, xb);
+          }
+          if (q == 0) {
+            // The dS_1^T buffer staged the previous step's dQ_1: its reduce-adds must have read it.
+            if (lead && h < 2) bulk_wait_read_all();
+            named_bar_sync(1, 512);
+          }
+          // 16-byte chunks chunk0 + 2 q + v of the row, swizzled by the row
+#pragma unroll
+          for (int v = 0; v < 2; ++v)
+            *reinterpret_cast<uint4*>(ds1_row + (((chunk0 + 2 * q + v) ^ (kr & 7)) << 4)) =
+                make_uint4(dsk[4 * v], dsk[4 * v + 1], dsk[4 * v + 2], dsk[4 * v + 3]);
         }
-        // 16-byte chunk 4 q + v of the row (queries 8 (4 q + v) ..), swizzled by the row
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p1_ready);
+        __syncwarp();
+        // ---- phase 2: P_2, dS_2 = P_2 (c_2 dP - Delta_2), Pc = P_1 + c_2 P_2.  Pc^T of the part goes
+        // over this thread's own, already loaded, S_2^T columns: no other thread reads them.
+        mbar_wait(s_full, 1, ab);
+        // The dS_2^T buffer staged the previous step's dQ_2: its reduce-adds must have read it (they
+        // have had all of phase 1).
+        if (lead && h >= 2) bulk_wait_read_all();
+        named_bar_sync(2, 512);
+        __syncwarp();
+        tc_fence_after();
 #pragma unroll
-        for (int v = 0; v < 4; ++v)
-          *reinterpret_cast<uint4*>(ds1_row + (((4 * q + v) ^ (kr & 7)) << 4)) =
-              make_uint4(dsk[4 * v], dsk[4 * v + 1], dsk[4 * v + 2], dsk[4 * v + 3]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p1_ready);
-      __syncwarp();
-      // ---- phase 2: P_2, dS_2 = P_2 (c_2 dP - Delta_2), Pc = P_1 + c_2 P_2
-      mbar_wait(s_full, 1, ab);
-      __syncwarp();
-      tc_fence_after();
-      tmem_ld32(tl + C::TM_S + 64u * h, sv[0]);
-      tmem_ld32(tl + C::TM_S + 64u * h + 32u, sv[1]);
-      tmem_ld_wait2(sv[0], sv[1]);
-      // Pc^T overwrites S columns [0, 64): both warpgroups must have loaded S_2^T first.
-      tc_fence_before();
-      named_bar_sync(2, 256);
-      tc_fence_after();
+        for (int q = 0; q < 2; ++q) {
+          uint32_t sv[16], dp[16];
+          tmem_ld16(tl + C::TM_S + 32u * h + 16u * q, sv);
+          tmem_ld16(tl + C::TM_DP + 32u * h + 16u * q, dp);
+          tmem_ld_wait16x2(sv, dp);
+          uint32_t dsk[8], pck[8];
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t dp[32];
-        tmem_ld32(tl + C::TM_DP + 64u * h + 32u * q, dp);
-        tmem_ld_wait(dp);
-        uint32_t dsk[16], pck[16];
+          for (int cc = 0; cc < 16; cc += 2) {
+            const int c0 = 16 * q + cc;
+            uint64_t del;
+            const uint64_t pp = probs(sv[cc], sv[cc + 1], st2[c0 >> 1], c0, del);
+            const uint64_t c2 = V2 ? f2pack(cf2[c0], cf2[c0 + 1]) : f2pack(lam_c2, lam_c2);
+            const uint64_t ds = mul2(pp, fma2(c2, f2pack(__uint_as_float(dp[cc]), __uint_as_float(dp[cc + 1])), del));
+            float p1a, p1b;
+            bf16x2_unpack(p1k[8 * q + (cc >> 1)], p1a, p1b);
+            float xa, xb, ya, yb;
+            f2unpack(ds, xa, xb);
+            f2unpack(fma2(c2, pp, f2pack(p1a, p1b)), ya, yb);
+            dsk[cc >> 1] = pack_bf16x2(xa, xb);
+            pck[cc >> 1] = pack_bf16x2(ya, yb);
+          }
 #pragma unroll
-        for (int cc = 0; cc < 32; cc += 2) {
-          const int c0 = 32 * q + cc;
-          const float pa = visible(c0) ? ex2(fmaf(__uint_as_float(sv[q][cc]), sc, -lse2[c0])) : 0.f;
-          const float pb = visible(c0 + 1) ? ex2(fmaf(__uint_as_float(sv[q][cc + 1]), sc, -lse2[c0 + 1])) : 0.f;
-          const float ca = cf2[c0], cb2 = cf2[c0 + 1];
-          const float da = pa * fmaf(ca, __uint_as_float(dp[cc]), -del2[c0]);
-          const float db = pb * fmaf(cb2, __uint_as_float(dp[cc + 1]), -del2[c0 + 1]);
-          float p1a, p1b;
-          bf16x2_unpack(p1k[16 * q + (cc >> 1)], p1a, p1b);
-          dsk[cc >> 1] = pack_bf16x2(da, db);
-          pck[cc >> 1] = pack_bf16x2(fmaf(ca, pa, p1a), fmaf(cb2, pb, p1b));
+          for (int v = 0; v < 2; ++v)
+            *reinterpret_cast<uint4*>(ds2_row + (((chunk0 + 2 * q + v) ^ (kr & 7)) << 4)) =
+                make_uint4(dsk[4 * v], dsk[4 * v + 1], dsk[4 * v + 2], dsk[4 * v + 3]);
+          tmem_st8(tl + C::TM_PC + 32u * h + 8u * q, pck);
         }
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-          *reinterpret_cast<uint4*>(ds2_row + (((4 * q + v) ^ (kr & 7)) << 4)) =
-              make_uint4(dsk[4 * v], dsk[4 * v + 1], dsk[4 * v + 2], dsk[4 * v + 3]);
-        tmem_st16(tl + C::TM_PC + 32u * h + 16u * q, pck);
-      }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p2_ready);
-      __syncwarp();
-      // ---- dQ of the tile: thread = query row kr; warpgroup h reads dQ_(h+1)
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p2_ready);
+        __syncwarp();
+      };
+      if (full)
+        phases(std::true_type{});
+      else
+        phases(std::false_type{});
+      if (s + 1 < nsteps) fetch_stats(s + 1, pre);  // consumed at the top of the next step
+      // ---- dQ of the step: thread = query row kr.  Warpgroup h takes dQ_(h / 2 + 1), columns
+      // [(d / 2) (h % 2), +d / 2), 32 a round: scaled and staged as one 128-byte swizzled fp32 box
+      // (128 rows x 32 columns) in its quarter of the dS^T buffers (free once the step's MMAs reading
+      // them are done), then added to the fp32 dQ in global memory by a TMA bulk reduce-add (rows
+      // past n are dropped).
       const bool dq_ok = __all_sync(0xffffffffu, mbar_wait(dq_full, ph, ab));
       tc_fence_after();
       {
-        const int tq = q0 + kr;
-        const int head = V2 ? 2 * u + h : u;
-        float* dst = (h == 0 ? p.dq1 : p.dq2) +
-                     ((static_cast<long long>(b) * p.n + tq) * (V2 ? 2 * p.units : p.units) + head) * D;
+        const int map = h >> 1;
+        const uint32_t tdq = tl + (map == 0 ? C::TM_DQ1 : C::TM_DQ2);
+        uint8_t* const stg = smem + (map == 0 ? C::OFF_DS1 : C::OFF_DS2) + (h & 1) * 16384;
+        const CUtensorMap* dqmap = (V2 || map == 0) ? &p.tm_dq1 : &p.tm_dq2;
+        const int head = V2 ? 2 * u + map : u;
+        constexpr int ROUNDS = D / 64;
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) {
+        for (int rd = 0; rd < ROUNDS; ++rd) {
+          const int col0 = (D / 2) * (h & 1) + 32 * rd;
           uint32_t r[32];
-          tmem_ld32(tl + (h == 0 ? C::TM_DQ1 : C::TM_DQ2) + 32u * ch, r);
+          tmem_ld32(tdq + static_cast<uint32_t>(col0), r);
           tmem_ld_wait(r);
-          if (dq_ok && tq < p.n) {
+          if (rd == ROUNDS - 1) {  // dQ is in registers: the next step's MMAs may overwrite its columns
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dq_free);
+            __syncwarp();
+          }
+          if (rd == 0) {
+            mbar_wait(ds_done, ph, ab);  // the MMAs reading dS^T of this step are done
+            __syncwarp();
+          } else {
+            if (lead) bulk_wait_read_all();  // the previous round's reduce-add has read the staging
+            named_bar_sync(3 + h, 128);
+          }
+          uint8_t* const srow = stg + kr * 128;
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              atomicAdd(reinterpret_cast<float4*>(dst + 32 * ch + 4 * v),
-                        make_float4(__uint_as_float(r[4 * v]) * p.scale, __uint_as_float(r[4 * v + 1]) * p.scale,
-                                    __uint_as_float(r[4 * v + 2]) * p.scale, __uint_as_float(r[4 * v + 3]) * p.scale));
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(srow + ((j ^ (kr & 7)) << 4)) =
+                make_float4(__uint_as_float(r[4 * j]) * p.scale, __uint_as_float(r[4 * j + 1]) * p.scale,
+                            __uint_as_float(r[4 * j + 2]) * p.scale, __uint_as_float(r[4 * j + 3]) * p.scale);
+          fence_proxy_async_smem();
+          named_bar_sync(3 + h, 128);
+          if (lead && dq_ok) {
+            tma_reduce_add_4d(dqmap, stg, col0, head, q0, b);
+            bulk_commit_group();
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_free);
-      __syncwarp();
     }
-    // ---- epilogue: dV and dK of the CTA's keys (thread = key row); warpgroup h
-    // writes dV columns [64 h, +64) and dK_(h+1) (V1) / dK columns [64 h, +64) (V2).
+    if (lead) bulk_wait_all();  // the dQ reduce-adds have completed
+    // ---- epilogue: dV and dK of the CTA's keys (thread = key row); warpgroup h writes dV columns
+    // [32 h, +32) and dK columns [32 h, +32) of (dK_1 | dK_2) (V1) or of dK (V2).
     if (__all_sync(0xffffffffu, mbar_wait(acc_done, 0, ab))) {
       tc_fence_after();
       const long long krow = static_cast<long long>(b) * p.n + key;
-      float* dvp = p.dv + (krow * p.heads_kv + hk) * DV + 64 * h;
-      float* dkp = V2 ? p.dk1 + (krow * p.heads_kv + hk) * D + 64 * h : (h == 0 ? p.dk1 : p.dk2) + (krow * p.heads_kv + hk) * D;
-      const uint32_t tk = V2 ? C::TM_DK1 + 64u * h : (h == 0 ? C::TM_DK1 : C::TM_DK2);
+      float* dvp = p.dv + (krow * p.heads_kv + hk) * DV + 32 * h;
+      float* dkp = V2 ? p.dk1 + (krow * p.heads_kv + hk) * D + 32 * h
+                      : (h < 2 ? p.dk1 : p.dk2) + (krow * p.heads_kv + hk) * D + 32 * (h & 1);
+      const uint32_t tk = V2 ? C::TM_DK1 + 32u * h : (h < 2 ? C::TM_DK1 : C::TM_DK2) + 32u * (h & 1);
+      uint32_t r[32], g[32];
+      tmem_ld32(tl + C::TM_DV + 32u * h, r);
+      tmem_ld32(tl + tk, g);
+      tmem_ld_wait2(r, g);
+      if (key_ok) {
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t r[32], g[32];
-        tmem_ld32(tl + C::TM_DV + 64u * h + 32u * ch, r);
-        tmem_ld32(tl + tk + 32u * ch, g);
-        tmem_ld_wait2(r, g);
-        if (key_ok) {
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            reinterpret_cast<float4*>(dvp + 32 * ch)[v] =
-                make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]), __uint_as_float(r[4 * v + 2]),
-                            __uint_as_float(r[4 * v + 3]));
-            reinterpret_cast<float4*>(dkp + 32 * ch)[v] =
-                make_float4(__uint_as_float(g[4 * v]) * p.scale, __uint_as_float(g[4 * v + 1]) * p.scale,
-                            __uint_as_float(g[4 * v + 2]) * p.scale, __uint_as_float(g[4 * v + 3]) * p.scale);
-          }
+        for (int v = 0; v < 8; ++v) {
+          reinterpret_cast<float4*>(dvp)[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                                          __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          reinterpret_cast<float4*>(dkp)[v] =
+              make_float4(__uint_as_float(g[4 * v]) * p.scale, __uint_as_float(g[4 * v + 1]) * p.scale,
+                          __uint_as_float(g[4 * v + 2]) * p.scale, __uint_as_float(g[4 * v + 3]) * p.scale);
         }
       }
     }

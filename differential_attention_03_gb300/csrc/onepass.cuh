@@ -119,7 +119,7 @@ struct OnePassCfg {
   // row sums ([6][4][128] floats) and the per-warp dgamma sums.
   static_assert(!STATS || !PERSIST, "the statistics pass runs one item per CTA");
   static constexpr int XCH_FLOATS = 6 * 4 * 128;
-  static_assert(!STATS || 2 * Q_TILE >= (XCH_FLOATS + 4 * 4 * 32) * 4, "statistics exchange in the Q buffers");
+  static_assert(!STATS || 2 * Q_TILE >= (XCH_FLOATS + 4 * 4 * 32 + 4) * 4, "statistics exchange in the Q buffers");
 };
 
 // 32 output channels of one row: y * rinv (* gamma), rounded to bf16 pairs.
@@ -162,47 +162,53 @@ __device__ __forceinline__ void onepass_stats_epilogue(const TwoPassParams& p, c
   constexpr int NX = V1 ? 6 : 2;  // partial sums exchanged per row
   const bool live = t < p.n;
   const long long orow = (static_cast<long long>(c.b) * p.n + t) * p.units_per_batch + c.u;
-  uint32_t o1[32], o2[32];
-  tmem_ld32(tl + C::TM_O1 + 32u * cb, o1);
-  tmem_ld32(tl + C::TM_O2 + 32u * cb, o2);
-  tmem_ld_wait2(o1, o2);
-  float dyv[32];
-  if (live) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.dy + orow * DV + 32 * cb);
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const uint4 u = src[v];
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        dyv[8 * v + 2 * e] = __uint_as_float(w[e] << 16);
-        dyv[8 * v + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int cc = 0; cc < 32; ++cc) dyv[cc] = 0.f;
-  }
   const float il1 = 1.f / l1, il2 = 1.f / l2;
   const float mult = p.norm_mult;
-  float part[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // V1: ss, G.O, G.O1, G.O2, O.O1, O.O2; V2: dy.O1, dy.O2
+  const uint4* dysrc = reinterpret_cast<const uint4*>(p.dy + orow * DV + 32 * cb);
+  // One half (16 channels) of the block: O_1, O_2 from TMEM and dy, unpacked to fp32.
+  auto load_half = [&](int hf, uint32_t (&x1)[16], uint32_t (&x2)[16], float (&dyh)[16]) {
+    tmem_ld16(tl + C::TM_O1 + 32u * cb + 16u * hf, x1);
+    tmem_ld16(tl + C::TM_O2 + 32u * cb + 16u * hf, x2);
+    uint4 u[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (live) {
+      u[0] = dysrc[2 * hf];
+      u[1] = dysrc[2 * hf + 1];
+    }
 #pragma unroll
-  for (int cc = 0; cc < 32; ++cc) {
-    const float x1 = __uint_as_float(o1[cc]) * il1, x2 = __uint_as_float(o2[cc]) * il2;
-    if constexpr (V1) {
-      const float o = fmaf(-coef, x2, x1);
-      const float g = mult * sgamma[32 * cb + cc] * dyv[cc];
-      o1[cc] = __float_as_uint(o);  // keep O and G for the second pass over the channels
-      o2[cc] = __float_as_uint(g);
-      part[0] = fmaf(o, o, part[0]);
-      part[1] = fmaf(g, o, part[1]);
-      part[2] = fmaf(g, x1, part[2]);
-      part[3] = fmaf(g, x2, part[3]);
-      part[4] = fmaf(o, x1, part[4]);
-      part[5] = fmaf(o, x2, part[5]);
-    } else {
-      part[0] = fmaf(dyv[cc], x1, part[0]);
-      part[1] = fmaf(dyv[cc], x2, part[1]);
+    for (int v = 0; v < 2; ++v) {
+      const uint32_t w[4] = {u[v].x, u[v].y, u[v].z, u[v].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        dyh[8 * v + 2 * e] = __uint_as_float(w[e] << 16);
+        dyh[8 * v + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+      }
+    }
+    tmem_ld_wait16x2(x1, x2);
+  };
+  // Pass 1: partial dot products of the block (V1: ss, G.O, G.O1, G.O2, O.O1, O.O2; V2: dy.O1, dy.O2),
+  // with O_r = O_r' / l_r, O = O_1 - coef O_2, G = m gamma dy.
+  float part[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    uint32_t o1[16], o2[16];
+    float dyh[16];
+    load_half(hf, o1, o2, dyh);
+#pragma unroll
+    for (int cc = 0; cc < 16; ++cc) {
+      const float x1 = __uint_as_float(o1[cc]) * il1, x2 = __uint_as_float(o2[cc]) * il2;
+      if constexpr (V1) {
+        const float o = fmaf(-coef, x2, x1);
+        const float g = mult * sgamma[32 * cb + 16 * hf + cc] * dyh[cc];
+        part[0] = fmaf(o, o, part[0]);
+        part[1] = fmaf(g, o, part[1]);
+        part[2] = fmaf(g, x1, part[2]);
+        part[3] = fmaf(g, x2, part[3]);
+        part[4] = fmaf(o, x1, part[4]);
+        part[5] = fmaf(o, x2, part[5]);
+      } else {
+        part[0] = fmaf(dyh[cc], x1, part[0]);
+        part[1] = fmaf(dyh[cc], x2, part[1]);
+      }
     }
   }
   float* xch = reinterpret_cast<float*>(smem + C::OFF_Q1);  // [NX][4][128]
@@ -223,41 +229,62 @@ __device__ __forceinline__ void onepass_stats_epilogue(const TwoPassParams& p, c
     delta1 = dO1;
     delta2 = -coef * dO2;
     share = -dO2;
-    // dO of the channel block, and its dgamma shares
-    uint32_t w[16];
-    float dg[32];
+    // Pass 2: dO of the block (bf16) and its dgamma shares, dg = dy m O r, each half summed over the
+    // warp's 32 rows: lane l ends with channel l % 16 of the half (each butterfly step halves the
+    // channels a lane holds and doubles the rows), the last step adds the two lane halves.
+    float dgw[2];
 #pragma unroll
-    for (int cc = 0; cc < 32; cc += 2) {
-      const float oa = __uint_as_float(o1[cc]), ob = __uint_as_float(o1[cc + 1]);
-      w[cc >> 1] = pack_bf16x2(r * __uint_as_float(o2[cc]) - k3 * oa, r * __uint_as_float(o2[cc + 1]) - k3 * ob);
-      dg[cc] = live ? dyv[cc] * mult * oa * r : 0.f;
-      dg[cc + 1] = live ? dyv[cc + 1] * mult * ob * r : 0.f;
-    }
-    if (live) {
-      uint4* dst = reinterpret_cast<uint4*>(p.dO + orow * DV + 32 * cb);
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t o1[16], o2[16];
+      float dyh[16], dg[16];
+      load_half(hf, o1, o2, dyh);
+      uint32_t w[8];
 #pragma unroll
-      for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
-    }
-    // Sum the 32 channels' shares over the warp's 32 rows (lane l ends with
-    // channel l: each step halves the channels a lane holds and doubles the
-    // rows they cover), then over the warpgroup's four warps.
+      for (int cc = 0; cc < 16; cc += 2) {
+        float ov[2], gv[2];
 #pragma unroll
-    for (int sft = 16; sft >= 1; sft >>= 1) {
-      const bool upper = (lane & sft) != 0;
-#pragma unroll
-      for (int j = 0; j < sft; ++j) {
-        const float send = upper ? dg[j] : dg[j + sft];
-        const float keep = upper ? dg[j + sft] : dg[j];
-        dg[j] = keep + __shfl_xor_sync(0xffffffffu, send, sft);
+        for (int e = 0; e < 2; ++e) {
+          const float x1 = __uint_as_float(o1[cc + e]) * il1, x2 = __uint_as_float(o2[cc + e]) * il2;
+          ov[e] = fmaf(-coef, x2, x1);
+          gv[e] = mult * sgamma[32 * cb + 16 * hf + cc + e] * dyh[cc + e];
+          dg[cc + e] = live ? dyh[cc + e] * mult * ov[e] * r : 0.f;
+        }
+        w[cc >> 1] = pack_bf16x2(r * gv[0] - k3 * ov[0], r * gv[1] - k3 * ov[1]);
       }
+      if (live) {
+        uint4* dst = reinterpret_cast<uint4*>(p.dO + orow * DV + 32 * cb + 16 * hf);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+#pragma unroll
+      for (int sft = 8; sft >= 1; sft >>= 1) {
+        const bool upper = (lane & sft) != 0;
+#pragma unroll
+        for (int j = 0; j < sft; ++j) {
+          const float send = upper ? dg[j] : dg[j + sft];
+          const float keep = upper ? dg[j + sft] : dg[j];
+          dg[j] = keep + __shfl_xor_sync(0xffffffffu, send, sft);
+        }
+      }
+      dgw[hf] = dg[0] + __shfl_xor_sync(0xffffffffu, dg[0], 16);  // channel 16 hf + lane % 16
     }
-    float* wsum = xch + C::XCH_FLOATS;  // [4 channel blocks][4 warps][32]
-    wsum[(cb * 4 + (warp & 3)) * 32 + lane] = dg[0];
+    // lanes 0..15 hold channels 0..15 (half 0) and 16..31 (half 1): lane l writes channel l
+    const float mine = lane < 16 ? dgw[0] : dgw[1];
+    float* wsum = xch + C::XCH_FLOATS;  // [4 channel blocks][4 warps][32], then [4 warps] dlambda sums
+    wsum[(cb * 4 + (warp & 3)) * 32 + lane] = mine;
+    if (cb == 0) {  // the rows' dlambda shares, summed over the warp's 32 rows
+      float sh = live ? -dO2 : 0.f;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sh += __shfl_xor_sync(0xffffffffu, sh, off);
+      if (lane == 0) wsum[16 * 32 + (warp & 3)] = sh;
+    }
     named_bar_sync(1, 128 * C::NSMWG);
     if ((warp & 3) == 0) {
       const float* ws = wsum + cb * 4 * 32;
       p.dgp[static_cast<long long>(blockIdx.x) * DV + 32 * cb + lane] =
           (ws[lane] + ws[32 + lane]) + (ws[64 + lane] + ws[96 + lane]);
+      if (cb == 0 && lane == 0)
+        p.dlam_part[blockIdx.x] = (wsum[16 * 32] + wsum[16 * 32 + 1]) + (wsum[16 * 32 + 2] + wsum[16 * 32 + 3]);
     }
   } else {
     delta1 = tot[0];

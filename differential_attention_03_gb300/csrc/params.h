@@ -36,6 +36,7 @@ struct TwoPassParams {
   __nv_bfloat16* dO;        // V1: [B, n, units_per_batch, DV], the gradient of the pre-norm output
   float* row;               // [6][rows]: lse_1, lse_2, Delta_1, Delta_2, lambda / logit share, coefficient
   float* dgp;               // V1: [gridDim.x][DV], each CTA's share of dgamma
+  float* dlam_part;         // V1: [gridDim.x], each CTA's share of dlambda
   float* dlogits_dense;     // V2, one logit per token: dlogit of (b, t, pair) at b sb + t st + pair
   long long rows;           // B * units_per_batch * n
 };
