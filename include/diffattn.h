@@ -409,7 +409,8 @@ diffattn_status diffattn_v2_layer_forward(int B, int n, int D, int Hq, int Hkv, 
                                           size_t workspace_bytes, void* stream);
 
 /*
- * Backward pass of diffattn_forward (DIFF V1), fp32 on CUDA cores.  The pages
+ * Backward pass of diffattn_forward (DIFF V1): fp32 inputs on CUDA cores, or
+ * bf16 inputs on the tensor cores (tcgen05; d = 64).  The pages
  * ("Differential Transformer" glossary page, "How differential attention
  * works"; news article section "差分注意力") define the forward and report
  * trained models; the gradients are the chain rule of that forward:
@@ -419,7 +420,11 @@ diffattn_status diffattn_v2_layer_forward(int B, int n, int D, int Hq, int Hkv, 
  *
  * Given dy = dL/dy it writes dL/dq1, dq2, dk1, dk2, dv, dL/dlambda and
  * dL/dgamma; the maps are recomputed, never stored.
- *   dt          : DIFFATTN_F32 (d in [1, 128]); DIFFATTN_BF16 -> ERR_UNSUPPORTED.
+ *   dt          : DIFFATTN_F32 (d in [1, 128]) or DIFFATTN_BF16 (d = 64; other d ->
+ *                 ERR_UNSUPPORTED).  q1, q2, k1, k2, v and dy are of type dt; the
+ *                 gradients dq1 .. dv are fp32 for both.  bf16: every tensor 16-byte
+ *                 aligned, else ERR_ALIGN; P, dS and dO are rounded to bf16 for the
+ *                 tensor cores, sums run in fp32.
  *   q1, q2, k1, k2, dq1, dq2, dk1, dk2 : [B, n, H, d] device; v, dy, dv : [B, n, H, 2d].
  *   lambda      : device scalar (as for the forward); lambda_init, eps, causal, gamma
  *                 (device [2d] or NULL for ones): as for diffattn_forward.
@@ -427,8 +432,11 @@ diffattn_status diffattn_v2_layer_forward(int B, int n, int D, int Hq, int Hkv, 
  *   workspace   : device memory of at least diffattn_backward_workspace(B, H, n, d)
  *                 bytes, 16-byte aligned (per-row statistics, dO, dgamma shares);
  *                 smaller -> ERR_SHAPE.  The library allocates nothing.
- * Sums for dlambda and dgamma run in a fixed order (same inputs, same bits).
- * Asynchronous on `stream` (four kernels).  Errors as for diffattn_forward.
+ * fp32: sums for dlambda and dgamma run in a fixed order (same inputs, same
+ * bits); bf16: dq is accumulated by TMA reduce-adds whose order varies from run
+ * to run (dlambda, dgamma, dk and dv still in a fixed order).  Asynchronous on
+ * `stream` (fp32: four kernels; bf16: two memsets and three kernels).  Errors as
+ * for diffattn_forward.
  */
 size_t diffattn_backward_workspace(int B, int H, int n, int d);
 
@@ -440,7 +448,8 @@ diffattn_status diffattn_backward(diffattn_dtype dt, int B, int H, int n, int d,
                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Backward pass of diffattn_v2_forward (DIFF V2), fp32 on CUDA cores: per head
+ * Backward pass of diffattn_v2_forward (DIFF V2), fp32 on CUDA cores or bf16
+ * (d = 128) on the tensor cores: per head
  * pair g of query heads 2g, 2g + 1 over KV head kv = 2g / (Hq / Hkv), with
  * s = sigmoid(logit) of the row, out = A_2g V - s A_2g+1 V (DIFF V2 analysis
  * page, "2. 커스텀 커널 제거", "5. 간소화된 λ 매개변수화", "GQA와의 호환성").
@@ -450,12 +459,15 @@ diffattn_status diffattn_backward(diffattn_dtype dt, int B, int H, int n, int d,
  * pair), (Hq/2, 0) (per sequence and pair) or (0, 0) (per pair), the
  * gradient summed over the tokens (and sequences) that share a logit; other
  * strides -> ERR_UNSUPPORTED.
- *   dt : DIFFATTN_F32 (d in [1, 128]); DIFFATTN_BF16 -> ERR_UNSUPPORTED.
+ *   dt : DIFFATTN_F32 (d in [1, 128]) or DIFFATTN_BF16 (d = 128, every tensor
+ *        16-byte aligned, else ERR_UNSUPPORTED / ERR_ALIGN); q, k, v, dy of type
+ *        dt, the gradients dq, dk, dv and dlogits fp32 for both.
  *   softmax_scale, causal, Hq / Hkv rules: as for diffattn_v2_forward.
  *   workspace : at least diffattn_v2_backward_workspace(B, Hq, n, d) bytes of
  *               device memory, 16-byte aligned; the library allocates nothing.
- * Fixed summation orders (same inputs, same bits).  Asynchronous on `stream`.
- * Errors as for diffattn_forward.
+ * fp32: fixed summation orders (same inputs, same bits); bf16: dq by TMA
+ * reduce-adds in a varying order.  Asynchronous on `stream`.  Errors as for
+ * diffattn_forward.
  */
 size_t diffattn_v2_backward_workspace(int B, int Hq, int n, int d);
 

@@ -137,3 +137,43 @@ def test_v2_backward_bf16_bench_size_sampled_pair():
             _close(got["dq"][b:b + 1, :, 2 * hk:2 * hk + 2], ref["dq"], f"dq b{b} kv{hk}")
             _close(got["dk"][b:b + 1, :, hk:hk + 1], ref["dk"], f"dk b{b} kv{hk}")
             _close(got["dv"][b:b + 1, :, hk:hk + 1], ref["dv"], f"dv b{b} kv{hk}")
+
+
+def test_v1_backward_bench_size_cross_head_sums():
+    """dlambda and dgamma are sums over every (sequence, head, row); at B4 H16 n2048 d64 the fp32
+    path gathers them from hundreds of row-pass blocks and the tensor-core path from its
+    statistics-pass blocks.  Both are compared with the sum of the oracle's per-head gradients over
+    all 64 heads, on the same bf16-exact inputs (fed to the fp32 path as fp32).  Bar: the path's
+    element tolerance (1e-4 fp32, 2e-2 bf16) times max(1, sum over heads of |per-head value|), the
+    magnitude the accumulation runs through."""
+    B, H, n, d = 4, 16, 2048, 64
+    g = torch.Generator(device="cuda").manual_seed(903)
+    x = {k: _rnd(g, B, n, H, d) for k in ("q1", "q2", "k1", "k2")}
+    x["v"], x["dy"] = _rnd(g, B, n, H, 2 * d), _rnd(g, B, n, H, 2 * d)
+    gam = 0.9 + 0.2 * torch.rand(2 * d, generator=g, device="cuda")
+    lam, lin = 0.3, 0.2
+    lam_t = torch.tensor([lam], device="cuda")
+    got = {"bf16": da.diffattn_backward(*(x[k] for k in ("q1", "q2", "k1", "k2", "v")), lam_t, lin, x["dy"],
+                                        gamma=gam)}
+    xf = {k: t.float() for k, t in x.items()}
+    got["f32"] = da.diffattn_backward(*(xf[k] for k in ("q1", "q2", "k1", "k2", "v")), lam_t, lin, xf["dy"],
+                                      gamma=gam)
+    da.device_status()
+    dlam, dlam_abs = 0.0, 0.0
+    dgam, dgam_abs = np.zeros(2 * d), np.zeros(2 * d)
+    gam_np = gam.cpu()
+    xc = {k: t.cpu() for k, t in x.items()}
+    for b in range(B):
+        for h in range(H):
+            sel = {k: t[b:b + 1, :, h:h + 1] for k, t in xc.items()}
+            ref = oracle.diff_attn_v1_backward(sel["q1"], sel["q2"], sel["k1"], sel["k2"], sel["v"], lam, lin,
+                                               gam_np, 1e-5, True, sel["dy"])
+            dlam += float(ref["dlam"])
+            dlam_abs += abs(float(ref["dlam"]))
+            dgam += np.asarray(ref["dgamma"], np.float64)
+            dgam_abs += np.abs(np.asarray(ref["dgamma"], np.float64))
+    for dt, tol in (("f32", 1e-4), ("bf16", 2e-2)):
+        e_lam = abs(float(got[dt]["dlam"][0]) - dlam)
+        assert e_lam <= tol * max(1.0, dlam_abs), f"{dt} dlambda: {e_lam} vs {dlam} (sum |.| {dlam_abs})"
+        e_gam = np.abs(got[dt]["dgamma"].cpu().double().numpy() - dgam)
+        assert np.all(e_gam <= tol * np.maximum(1.0, dgam_abs)), f"{dt} dgamma: max {float(e_gam.max())}"
