@@ -16,11 +16,14 @@ import threading
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libdiffattn.so")
+# DIFFATTN_DEBUG=1 loads the bounds-check build (every TMA coordinate, TMEM
+# address and global store of the kernels checked; see build.py) instead.
+BOUNDS = os.environ.get("DIFFATTN_DEBUG", "") == "1"
+LIB_PATH = os.path.join(_PKG, "libdiffattn_bounds.so" if BOUNDS else "libdiffattn.so")
 
-OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(8)
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BOUNDS = range(9)
 STATUS_NAMES = ["OK", "ERR_NULL", "ERR_SHAPE", "ERR_ALIGN", "ERR_DTYPE", "ERR_UNSUPPORTED", "ERR_CUDA",
-                "ERR_TIMEOUT"]
+                "ERR_TIMEOUT", "ERR_BOUNDS"]
 F32, BF16 = 0, 1
 
 _lock = threading.Lock()
@@ -43,7 +46,8 @@ def lib() -> ctypes.CDLL:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
                 raise RuntimeError(f"{LIB_PATH} is missing: build it with "
-                                   "`python -m differential_attention_03_gb300.build`")
+                                   "`python -m differential_attention_03_gb300.build`"
+                                   + (" --bounds" if BOUNDS else ""))
             L = ctypes.CDLL(LIB_PATH)
             vp, i, f, ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
             L.diffattn_lambda_init.argtypes = [i]
@@ -104,6 +108,10 @@ def lib() -> ctypes.CDLL:
             L.diffattn_v2_layer_forward.restype = i
             L.diffattn_device_status.argtypes = [vp]
             L.diffattn_device_status.restype = i
+            L.diffattn_bounds_checked.argtypes = []
+            L.diffattn_bounds_checked.restype = i
+            L.diffattn_debug_bounds_selftest.argtypes = [vp]
+            L.diffattn_debug_bounds_selftest.restype = i
             L.diffattn_last_error.argtypes = []
             L.diffattn_last_error.restype = ctypes.c_char_p
             L.diffattn_debug_wait_timeout.argtypes = [ll, vp]
@@ -644,6 +652,16 @@ def v2_layer_forward(x, w_qkvl, w_o, Hq: int, Hkv: int, causal: bool = True, out
     _check(lib().diffattn_v2_layer_forward(B, n, D, Hq, Hkv, d, _ptr(x), _ptr(w_qkvl), _ptr(w_o),
                                            1 if causal else 0, _ptr(out), wp, wn, _stream(stream)))
     return out
+
+
+def bounds_checked() -> bool:
+    """True when the loaded library is the bounds-check build."""
+    return bool(lib().diffattn_bounds_checked())
+
+
+def debug_bounds_selftest(stream=None) -> None:
+    """Bounds-check build: one checked store out of its limit (skipped and recorded)."""
+    _check(lib().diffattn_debug_bounds_selftest(_stream(stream)))
 
 
 def device_status(stream=None) -> int:

@@ -23,6 +23,27 @@
 // DIFFATTN_ERR_TIMEOUT here when a bounded wait runs out.
 __device__ int g_diffattn_status = 0;
 
+#ifdef DIFFATTN_BOUNDS
+namespace da {
+namespace {
+struct BoundsRegistry {
+  std::mutex mu;
+  BoundsReader readers[64];
+  int count = 0;
+};
+BoundsRegistry& bounds_registry() {
+  static BoundsRegistry r;
+  return r;
+}
+}  // namespace
+void bounds_register(BoundsReader reader) {
+  BoundsRegistry& r = bounds_registry();
+  std::lock_guard<std::mutex> lk(r.mu);
+  if (r.count < 64) r.readers[r.count++] = reader;
+}
+}  // namespace da
+#endif
+
 namespace {
 
 thread_local std::string t_last_error;
@@ -1574,12 +1595,61 @@ diffattn_status diffattn_device_status(void* stream) {
   const int zero = 0;
   e = cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+#ifdef DIFFATTN_BOUNDS
+  {  // the bounds-check build: every translation unit's record (a failed check usually ends in a timeout too)
+    da::BoundsRegistry& r = da::bounds_registry();
+    std::lock_guard<std::mutex> lk(r.mu);
+    long long failures = 0;
+    int first[3] = {0, 0, 0};
+    for (int i = 0; i < r.count; ++i) {
+      int rec[3] = {0, 0, 0};
+      const int n = r.readers[i](rec);
+      if (n < 0) return fail(DIFFATTN_ERR_CUDA, "reading a bounds-check record failed");
+      if (n > 0 && failures == 0) std::copy(rec, rec + 3, first);
+      failures += n;
+    }
+    if (failures > 0)
+      return fail(DIFFATTN_ERR_BOUNDS, "%lld bounds-check failures; first in file tag %d at line %d (value %d)",
+                  failures, first[1] / 100000, first[1] % 100000, first[2]);
+  }
+#endif
   if (host == DIFFATTN_ERR_TIMEOUT) return fail(DIFFATTN_ERR_TIMEOUT, "a bounded in-kernel wait ran out");
   if (host != 0) return fail(DIFFATTN_ERR_CUDA, "device status word holds %d", host);
   return ok();
 }
 
 const char* diffattn_last_error(void) { return t_last_error.c_str(); }
+
+#ifdef DIFFATTN_BOUNDS
+namespace {
+// Self-test of the checks: one thread stores through DA_STORE at index 5 with
+// a limit of 4.  The store is skipped and recorded; were it not, it would
+// still land inside this 8-element array.
+__device__ int g_bounds_selftest[8];
+__global__ void bounds_selftest_kernel() { DA_STORE(g_bounds_selftest, 5, 4, 1); }
+}  // namespace
+#endif
+
+diffattn_status diffattn_debug_bounds_selftest(void* stream) {
+#ifdef DIFFATTN_BOUNDS
+  bounds_selftest_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>();
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "diffattn_debug_bounds_selftest launch");
+  g_launches.fetch_add(1);
+  return ok();
+#else
+  (void)stream;
+  return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_debug_bounds_selftest: not the bounds-check build");
+#endif
+}
+
+int diffattn_bounds_checked(void) {
+#ifdef DIFFATTN_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
 
 diffattn_status diffattn_debug_wait_timeout(long long budget_ns, void* stream) {
   if (budget_ns < 1 || budget_ns > 1000000000ll)

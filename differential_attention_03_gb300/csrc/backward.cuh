@@ -35,8 +35,12 @@
 // slice when d % 32 == 0).
 #pragma once
 
+#include "bounds.cuh"
 #include "bwd_params.h"
 #include "stage.cuh"
+
+#undef DA_BOUNDS_FILE
+#define DA_BOUNDS_FILE 9
 
 namespace da {
 
@@ -261,7 +265,7 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dkdv_kernel(const BwdParams p
     }
   }
   const int key = k0 + lane;
-  if (key < p.n) {
+  if (key < p.n && DA_BOUNDS_V(b < p.B && hk < p.heads_kv, key)) {
     const size_t kr = (static_cast<size_t>(b) * p.n + key) * p.heads_kv + hk;
 #pragma unroll
     for (int k = 0; k < kBwdMaxCV; ++k) {
@@ -344,7 +348,7 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_dq_kernel(const BwdParams p) 
     }
   }
   const int t = q0 + lane;
-  if (t < p.n) {
+  if (t < p.n && DA_BOUNDS_V(b < p.B && hq1 < p.heads_q && hq2 < p.heads_q, t)) {
     const size_t qr = (static_cast<size_t>(b) * p.n + t) * p.heads_q;
 #pragma unroll
     for (int k = 0; k < kBwdMaxCK; ++k) {
@@ -391,10 +395,10 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_reduce_kernel(const BwdParams
     __syncthreads();
   }
   if (threadIdx.x != 0) return;
-  if (p.v2)
-    p.dlogits[static_cast<long long>(b0) * p.sb + g] = red[0];
-  else if (dgamma_cta)
-    p.dgamma[blockIdx.x - 1] = red[0];
+  if (p.v2) {
+    if (DA_BOUNDS_V(b0 < p.B && g < p.units, g)) p.dlogits[static_cast<long long>(b0) * p.sb + g] = red[0];
+  } else if (dgamma_cta)
+    DA_STORE(p.dgamma, blockIdx.x - 1, p.dvw, red[0]);
   else
     *p.dlambda = red[0];
 }

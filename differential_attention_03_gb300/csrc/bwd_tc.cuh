@@ -48,6 +48,9 @@
 #include "bwd_tc_params.h"
 #include "ptx.cuh"
 
+#undef DA_BOUNDS_FILE
+#define DA_BOUNDS_FILE 7
+
 namespace da {
 
 
@@ -187,11 +190,14 @@ __global__ void __launch_bounds__(608, 1) bwd_tc_kernel(const __grid_constant__ 
       tma_prefetch_desc(&p.tm_v);
       tma_prefetch_desc(&p.tm_do);
       mbar_arrive_expect_tx(kv_full, C::NK * C::KT + C::VT);
-      for (int bx = 0; bx < D / 64; ++bx) {
-        tma_load_4d(smem + C::OFF_K1 + bx * 16384, &p.tm_k1, kv_full, bx * 64, hk, j0, b);
-        if (!V2) tma_load_4d(smem + C::OFF_K2 + bx * 16384, &p.tm_k2, kv_full, bx * 64, hk, j0, b);
+      if (DA_BOUNDS_V(j0 < p.n && b < p.B && hk < p.heads_kv, j0)) {
+        for (int bx = 0; bx < D / 64; ++bx) {
+          tma_load_4d(smem + C::OFF_K1 + bx * 16384, &p.tm_k1, kv_full, bx * 64, hk, j0, b);
+          if (!V2) tma_load_4d(smem + C::OFF_K2 + bx * 16384, &p.tm_k2, kv_full, bx * 64, hk, j0, b);
+        }
+        for (int bx = 0; bx < DV / 64; ++bx)
+          tma_load_4d(smem + C::OFF_V + bx * 16384, &p.tm_v, kv_full, bx * 64, hk, j0, b);
       }
-      for (int bx = 0; bx < DV / 64; ++bx) tma_load_4d(smem + C::OFF_V + bx * 16384, &p.tm_v, kv_full, bx * 64, hk, j0, b);
       // Per step: Q_1 (released mid-step by map 1's dK), Q_2 (released by map 2's dK) and dO (released
       // by dV; with two buffers the next step's loads during this one).
       int nq1 = 0, nq2 = 0, ndo[2] = {0, 0};
@@ -206,6 +212,10 @@ __global__ void __launch_bounds__(608, 1) bwd_tc_kernel(const __grid_constant__ 
         const int hq = V2 ? 2 * u + r : u;
         uint64_t* bar = r == 0 ? q1_full : q2_full;
         mbar_arrive_expect_tx(bar, C::KT);
+        if (!DA_BOUNDS_V(q0 < p.n && b < p.B && hq < (V2 ? 2 : 1) * p.units, q0)) {
+          ok = false;
+          return;
+        }
         for (int bx = 0; bx < D / 64; ++bx)
           tma_load_4d(smem + (r == 0 ? C::OFF_Q1 : C::OFF_Q2) + bx * 16384, (V2 || r == 0) ? &p.tm_q1 : &p.tm_q2,
                       bar, bx * 64, hq, q0, b);
@@ -219,6 +229,10 @@ __global__ void __launch_bounds__(608, 1) bwd_tc_kernel(const __grid_constant__ 
         }
         const int u = step_pair(st_), q0 = step_tile(st_) * 128;
         mbar_arrive_expect_tx(&do_full[db], C::VT);
+        if (!DA_BOUNDS_V(q0 < p.n && b < p.B && u < p.units, q0)) {
+          ok = false;
+          return;
+        }
         for (int bx = 0; bx < DV / 64; ++bx)
           tma_load_4d(smem + C::OFF_DO + db * C::VT + bx * 16384, &p.tm_do, &do_full[db], bx * 64, u, q0, b);
         ++ndo[db];
@@ -571,7 +585,8 @@ __global__ void __launch_bounds__(608, 1) bwd_tc_kernel(const __grid_constant__ 
                             __uint_as_float(r[4 * j + 2]) * p.scale, __uint_as_float(r[4 * j + 3]) * p.scale);
           fence_proxy_async_smem();
           named_bar_sync(3 + h, 128);
-          if (lead && dq_ok) {
+          if (lead && dq_ok &&
+              DA_BOUNDS_V(col0 % 4 == 0 && col0 < D && q0 < p.n && b < p.B && head < (V2 ? 2 : 1) * p.units, col0)) {
             tma_reduce_add_4d(dqmap, stg, col0, head, q0, b);
             bulk_commit_group();
           }
@@ -592,7 +607,7 @@ __global__ void __launch_bounds__(608, 1) bwd_tc_kernel(const __grid_constant__ 
       tmem_ld32(tl + C::TM_DV + 32u * h, r);
       tmem_ld32(tl + tk, g);
       tmem_ld_wait2(r, g);
-      if (key_ok) {
+      if (key_ok && DA_BOUNDS_V(krow < static_cast<long long>(p.B) * p.n && hk < p.heads_kv, krow)) {
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           reinterpret_cast<float4*>(dvp)[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),

@@ -27,8 +27,9 @@
 //     the cache (C a multiple of the stage size) through a ring of NST
 //     stages filled by TMA (K_1, K_2 and V tiles of BK keys, 128-byte
 //     swizzled rows; 32 KB a stage).
-//   * Four warps per CTA, BK / 4 keys each per stage; PARTS lanes share a key
-//     (32 products of q . k each, combined by shuffles), so a warp scores its
+//   * NWARP warps per CTA (four; eight for V2 and for FP8 keys), BK / NWARP
+//     keys each per stage; PARTS lanes share a key (PE = 32 or 16 products of
+//     q . k each, combined by shuffles), so a warp scores its
 //     keys in one pass; every warp keeps its own online-softmax state per map
 //     (running maximum, per-lane partial sums, 2d / 32 output channels per
 //     lane for each map), rescaled only when the maximum grows.  Products
@@ -48,6 +49,9 @@
 
 #include "params.h"
 #include "ptx.cuh"
+
+#undef DA_BOUNDS_FILE
+#define DA_BOUNDS_FILE 5
 
 namespace da {
 
@@ -78,14 +82,17 @@ template <int D, bool V2 = false, bool K8 = false>
 struct DecodeCfg {
   static constexpr int MAX_CS = 8;  // CTAs per (b, h) cluster: chosen at launch, at most this (16-CTA
                                     // clusters measured slower: 5.5 vs 6.2 TB/s at B8 H8 n32768 d128)
-  static constexpr int NWARP = V2 ? 8 : 4;  // V2: eight warps, so that a stage is 64 keys (32 KB)
+  // Warps per CTA.  V2: eight, so that a stage is 64 keys (32 KB).  FP8 keys:
+  // eight, so that two CTAs per SM hide the latency of the longer per-byte
+  // instruction stream (a key is 6 d bytes instead of 8 d for the same work).
+  static constexpr int NWARP = (V2 || K8) ? 8 : 4;
   static constexpr int NTHREADS = NWARP * 32;
   static constexpr int DV = V2 ? D : 2 * D;     // value width
   static constexpr int NKT = V2 ? 1 : 2;         // key tiles a stage holds (V2: one K for both queries)
   static constexpr int BK = (V2 || D == 64) ? 64 : 32;  // keys per stage
   static constexpr int KW = BK / NWARP;         // keys per warp per stage
   static constexpr int PARTS = 32 / KW;         // lanes per key
-  static constexpr int PE = D / PARTS;          // q . k products per lane (32)
+  static constexpr int PE = D / PARTS;          // q . k products per lane (32, or 16 with FP8 keys in V1)
   static constexpr int KROW = K8 ? D : 128;  // bytes of a key row in one TMA box (bf16: 64 columns)
   static constexpr int QB = K8 ? 1 : D / 64;  // key boxes per row
   static constexpr int VB = DV / 64;
@@ -101,7 +108,7 @@ struct DecodeCfg {
   static constexpr int OFF_RED = OFF_PART + PART_FLOATS * 4;           // float [NWARP]
   static constexpr int SMEM_BYTES = OFF_RED + NWARP * 4 + 1024;        // + 1 KB alignment slack
   static_assert(D == 64 || D == 128, "query/key width");
-  static_assert(PE == 32 && PARTS * KW == 32, "lane split");
+  static_assert((PE == 32 || PE == 16) && PARTS * KW == 32, "lane split");
   static_assert(NST * STAGE == 98304, "stage ring");
   static_assert(STAGE % 1024 == 0 && K_BYTES % 1024 == 0, "swizzled boxes start on 1 KB");
   static_assert(!V2 || D == 128, "V2 decode: d = 128");
@@ -188,7 +195,7 @@ __device__ __forceinline__ void decode_finish(const DecodeParams& p, int b, int 
     const int c = threadIdx.x + t * NTHREADS;
     if (!has_ch) break;
     const float g = (!V2 && p.gamma) ? p.gamma[c] : 1.f;
-    orow[c] = __float2bfloat16_rn(y[t] * rinv * g);
+    if (DA_BOUNDS_V(b < p.B && h < p.H && c < DV, c)) orow[c] = __float2bfloat16_rn(y[t] * rinv * g);
   }
 }
 
@@ -277,6 +284,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
     uint8_t* st = smem + (i % NST) * C::STAGE;
     const int key0 = k_begin + i * BK;
     mbar_arrive_expect_tx(&full[i % NST], C::STAGE);
+    // (bounds build: KV heads V1 H, V2 2 H / group; the block starts inside the cache)
+    if (!DA_BOUNDS_V(key0 < p.n && b < p.B && hk < (V2 ? 2 * p.H / p.group : p.H), key0)) return;
     for (int bx = 0; bx < C::QB; ++bx) {  // (K8: one box of D bytes a row)
       tma_load_4d(st + bx * BK * C::KROW, &p.tm_k1, &full[i % NST], bx * 64, hk, key0, b);
       if (!V2) tma_load_4d(st + C::K_BYTES + bx * BK * C::KROW, &p.tm_k2, &full[i % NST], bx * 64, hk, key0, b);
@@ -292,17 +301,18 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
     for (; issued < NST && issued < nblk; ++issued) issue(issued);
   }
 
-  // This lane's 32 query products (pre-scaled into the log2 domain, and by
+  // This lane's PE query products (pre-scaled into the log2 domain, and by
   // the key scale of an e4m3 key cache).
+  constexpr int PE = C::PE;
   const int kk = lane / PARTS, prt = lane % PARTS;
   const float qs1 = K8 ? p.scale_log2 * p.k1_scale : p.scale_log2;
   const float qs2 = K8 ? p.scale_log2 * (V2 ? p.k1_scale : p.k2_scale) : p.scale_log2;
-  uint64_t q1r[16], q2r[16];  // pairs of query products
+  uint64_t q1r[PE / 2], q2r[PE / 2];  // pairs of query products
   {
-    const __nv_bfloat16* q1p = p.q1 + q1_off + prt * 32;
-    const __nv_bfloat16* q2p = (V2 ? p.q1 : p.q2) + q2_off + prt * 32;
+    const __nv_bfloat16* q1p = p.q1 + q1_off + prt * PE;
+    const __nv_bfloat16* q2p = (V2 ? p.q1 : p.q2) + q2_off + prt * PE;
 #pragma unroll
-    for (int i = 0; i < 32; i += 8) {
+    for (int i = 0; i < PE; i += 8) {
       const uint4 a = *reinterpret_cast<const uint4*>(q1p + i);
       const uint4 c = *reinterpret_cast<const uint4*>(q2p + i);
       const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wc[4] = {c.x, c.y, c.z, c.w};
@@ -318,9 +328,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
   uint64_t o1p[CH / 2], o2p[CH / 2];
 #pragma unroll
   for (int c = 0; c < CH / 2; ++c) o1p[c] = o2p[c] = 0ull;
-  // Byte offsets inside a stage that do not change: this lane's 32 key
+  // Byte offsets inside a stage that do not change: this lane's PE key
   // columns (box, first 16-byte chunk) and its CH value channels.
-  const int kbox = (prt * 32) / 64, kchunk0 = ((prt * 32) % 64) / 8;
+  const int kbox = (prt * PE) / 64, kchunk0 = ((prt * PE) % 64) / 8;
   const int vc0 = lane * CH, vbox = vc0 / 64, vbyte = (vc0 % 64) * 2;
 
   for (int i = 0; i < nblk; ++i) {
@@ -328,15 +338,15 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
     if (!mbar_wait(&full[s], static_cast<uint32_t>(i / NST) & 1u, ab)) break;
     const uint8_t* st = smem + s * C::STAGE;
     const int row = warp * KW + kk;  // this lane's key within the stage
-    // ---- scores: 32 products per lane, PARTS lanes per key
+    // ---- scores: PE products per lane, PARTS lanes per key
     uint64_t a1 = 0ull, a2 = 0ull, b1 = 0ull, b2 = 0ull;
     if constexpr (K8) {
-      // 32 e4m3 key values: 16-byte chunks 2 prt and 2 prt + 1 of the row
+      // PE e4m3 key values: 16-byte chunks (PE / 16) prt .. of the row
       // (128-byte rows: 128-byte swizzle, chunk ^ (row % 8); 64-byte rows:
       // 64-byte swizzle, chunk ^ ((row / 2) % 4)).
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int ch = 2 * prt + c;
+      for (int c = 0; c < PE / 16; ++c) {
+        const int ch = (PE / 16) * prt + c;
         const int pch = (C::KROW == 128) ? (ch ^ (row & 7)) : (ch ^ ((row >> 1) & 3));
         const int off = row * C::KROW + (pch << 4);
         const uint4 a = *reinterpret_cast<const uint4*>(st + off);
@@ -355,7 +365,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
       }
     } else {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < PE / 8; ++c) {
         const int off = kbox * BK * 128 + row * 128 + (((kchunk0 + c) ^ (row & 7)) << 4);
         const uint4 a = *reinterpret_cast<const uint4*>(st + off);
         const uint4 e = V2 ? a : *reinterpret_cast<const uint4*>(st + C::K_BYTES + off);  // V2: one key tile
@@ -441,7 +451,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
         o2p[c] = fma2(f2pack(w2, w2), vp, o2p[c]);
       }
     }
-    // ---- release the stage; thread 0 refills it once all four warps have
+    // ---- release the stage; thread 0 refills it once all the warps have
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
     if (threadIdx.x == 0 && issued < nblk) {
@@ -549,7 +559,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
     if (p.nsplit > 1) {
       // This cluster's state of the pair: the combine kernel finishes the row.
       float* dst = p.ws + (static_cast<size_t>(unit) * p.nsplit + split) * C::PART_FLOATS;
-      if (threadIdx.x == 0) {
+      if (!DA_BOUNDS_V(unit < p.B * p.H && split < p.nsplit, unit)) dst = nullptr;
+      if (dst == nullptr) {
+      } else if (threadIdx.x == 0) {
         dst[0] = M1;
         dst[1] = l1;
         dst[2] = M2;
@@ -558,7 +570,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
 #pragma unroll
       for (int t = 0; t < CPT; ++t) {
         const int c = threadIdx.x + t * C::NTHREADS;
-        if (!has_ch) break;
+        if (!has_ch || dst == nullptr) break;
         dst[4 + c] = y1[t];
         dst[4 + DV + c] = y2[t];
       }

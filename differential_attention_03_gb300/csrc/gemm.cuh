@@ -34,6 +34,9 @@
 #include "gemm_params.h"
 #include "ptx.cuh"
 
+#undef DA_BOUNDS_FILE
+#define DA_BOUNDS_FILE 6
+
 namespace da {
 
 struct GemmCfg {
@@ -124,8 +127,10 @@ __global__ void __launch_bounds__(GemmCfg::NTHREADS, 1) gemm_bf16_kernel(const _
           }
           uint8_t* dst = smem + s * C::STAGE_BYTES;
           mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-          tma_load_2d(dst, &p.tm_a, &full[s], kb * C::BK, mb * C::BM);
-          tma_load_2d(dst + C::A_BYTES, &p.tm_b, &full[s], kb * C::BK, nb * C::BN);
+          if (DA_BOUNDS(kb * C::BK < p.K && mb * C::BM < p.M && nb * C::BN < p.N)) {
+            tma_load_2d(dst, &p.tm_a, &full[s], kb * C::BK, mb * C::BM);
+            tma_load_2d(dst + C::A_BYTES, &p.tm_b, &full[s], kb * C::BK, nb * C::BN);
+          }
         }
       }
       if (*ab.flag) {
@@ -196,6 +201,7 @@ __global__ void __launch_bounds__(GemmCfg::NTHREADS, 1) gemm_bf16_kernel(const _
         const int c0 = nb * C::BN + ch * 32;
         if (!row_ok || c0 >= p.N) {
           // nothing of this chunk to store (the loads above stay warp-wide)
+        } else if (!DA_BOUNDS_V(row >= 0 && c0 >= 0, row)) {
         } else if (c0 + 32 <= p.n_main) {
           uint4* dst = reinterpret_cast<uint4*>(p.c + static_cast<long long>(row) * p.ldc + c0);
 #pragma unroll

@@ -26,7 +26,8 @@ static cudaError_t launch_decode(const DecodeParams& p, int units, int cs, cudaS
   e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return e;
   if (p.nsplit > 1) {  // merge the clusters' states of every (b, h) and finish the rows
-    decode_combine_kernel<D, V2><<<units, C::NTHREADS, 0, s>>>(p);
+    // (the combine kernel's own block size: the key type does not change its layout)
+    decode_combine_kernel<D, V2><<<units, DecodeCfg<D, V2>::NTHREADS, 0, s>>>(p);
   }
   return cudaGetLastError();
 }

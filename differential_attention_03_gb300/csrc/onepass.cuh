@@ -66,6 +66,9 @@
 #include "params.h"
 #include "ptx.cuh"
 
+#undef DA_BOUNDS_FILE
+#define DA_BOUNDS_FILE 4
+
 namespace da {
 
 template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST, bool STATS = false>
@@ -251,7 +254,7 @@ __device__ __forceinline__ void onepass_stats_epilogue(const TwoPassParams& p, c
         }
         w[cc >> 1] = pack_bf16x2(r * gv[0] - k3 * ov[0], r * gv[1] - k3 * ov[1]);
       }
-      if (live) {
+      if (live && DA_BOUNDS_V(orow >= 0 && orow < p.rows, orow)) {
         uint4* dst = reinterpret_cast<uint4*>(p.dO + orow * DV + 32 * cb + 16 * hf);
         dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
         dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -281,10 +284,11 @@ __device__ __forceinline__ void onepass_stats_epilogue(const TwoPassParams& p, c
     named_bar_sync(1, 128 * C::NSMWG);
     if ((warp & 3) == 0) {
       const float* ws = wsum + cb * 4 * 32;
-      p.dgp[static_cast<long long>(blockIdx.x) * DV + 32 * cb + lane] =
-          (ws[lane] + ws[32 + lane]) + (ws[64 + lane] + ws[96 + lane]);
+      DA_STORE(p.dgp, static_cast<long long>(blockIdx.x) * DV + 32 * cb + lane, static_cast<long long>(gridDim.x) * DV,
+               (ws[lane] + ws[32 + lane]) + (ws[64 + lane] + ws[96 + lane]));
       if (cb == 0 && lane == 0)
-        p.dlam_part[blockIdx.x] = (wsum[16 * 32] + wsum[16 * 32 + 1]) + (wsum[16 * 32 + 2] + wsum[16 * 32 + 3]);
+        DA_STORE(p.dlam_part, blockIdx.x, gridDim.x,
+                 (wsum[16 * 32] + wsum[16 * 32 + 1]) + (wsum[16 * 32 + 2] + wsum[16 * 32 + 3]));
     }
   } else {
     delta1 = tot[0];
@@ -293,7 +297,8 @@ __device__ __forceinline__ void onepass_stats_epilogue(const TwoPassParams& p, c
   }
   if (live) {
     const long long ri = (static_cast<long long>(c.b) * p.units_per_batch + c.u) * p.n + t;
-    if (cb == 0) {  // map 1's running maximum lives in its warpgroups
+    if (!DA_BOUNDS_V(ri >= 0 && ri < p.rows && c.b < p.B && t < p.n && c.u < p.units_per_batch, ri)) {
+    } else if (cb == 0) {  // map 1's running maximum lives in its warpgroups
       p.row[ri] = m_used + log2f(l1);
       p.row[2 * p.rows + ri] = delta1;
       p.row[3 * p.rows + ri] = delta2;
@@ -406,8 +411,12 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
         }
         mbar_arrive_expect_tx(q_full, 2 * C::Q_TILE);
         for (int bx = 0; bx < C::QB; ++bx) {
-          tma_load_4d(smem + C::OFF_Q1 + bx * BM * 128, &p.tm_q1, q_full, bx * 64, c.hq1, c.q0, c.b);
-          tma_load_4d(smem + C::OFF_Q2 + bx * BM * 128, &p.tm_q2, q_full, bx * 64, c.hq2, c.q0, c.b);
+          // (bounds build: query heads of the maps, V1 units, V2 2 units)
+          if (DA_BOUNDS(bx * 64 < D && c.b < p.B && c.q0 < p.n &&
+                        c.hq2 < (EPI == kEpiV2 ? 2 : 1) * p.units_per_batch)) {
+            tma_load_4d(smem + C::OFF_Q1 + bx * BM * 128, &p.tm_q1, q_full, bx * 64, c.hq1, c.q0, c.b);
+            tma_load_4d(smem + C::OFF_Q2 + bx * BM * 128, &p.tm_q2, q_full, bx * 64, c.hq2, c.q0, c.b);
+          }
         }
         ++qloads;
         auto load = [&](const CUtensorMap* map, int key0, int rows, int nbox) {
@@ -421,7 +430,9 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
           uint8_t* dst = smem + C::OFF_RING + s * C::SLOT;
           mbar_arrive_expect_tx(&full[s], C::SLOT);
           for (int bx = 0; bx < nbox; ++bx)
-            tma_load_4d(dst + bx * rows * 128, map, &full[s], bx * 64, c.hk, key0, c.b);
+            if (DA_BOUNDS(key0 < (p.n + 127) / 128 * 128 && c.b < p.B &&  // (a box past n reads zeros)
+                          c.hk < (EPI == kEpiV2 ? 2 * p.units_per_batch / p.group : p.units_per_batch)))
+              tma_load_4d(dst + bx * rows * 128, map, &full[s], bx * 64, c.hk, key0, c.b);
           ++fill;
         };
         // The fill order is the order in which both MMA warps walk the ring.
@@ -777,7 +788,7 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
         // Row stores straight from registers: they drain while the next
         // item starts (staging them for a TMA store put a warpgroup barrier
         // and a proxy fence on the item transition, measured slower).
-        if (t < p.n) {
+        if (t < p.n && DA_BOUNDS_V(c.b < p.B && c.u < p.units_per_batch, t)) {
           __nv_bfloat16* orow =
               p.out + ((static_cast<size_t>(c.b) * p.n + t) * p.units_per_batch + c.u) * DV + 32 * cb;
           uint32_t wv[16];
@@ -805,7 +816,8 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
         fence_proxy_async_smem();
         named_bar_sync(4 + cb, 128);
         if ((threadIdx.x & 127) == 96) {  // lane 0 of the warpgroup's first warp
-          tma_store_4d(&p.tm_out, stg, 32 * cb, c.u, c.q0, c.b);
+          if (DA_BOUNDS(32 * cb < DV && c.u < p.units_per_batch && c.q0 < p.n && c.b < p.B))
+            tma_store_4d(&p.tm_out, stg, 32 * cb, c.u, c.q0, c.b);
           bulk_commit_group();
         }
       }

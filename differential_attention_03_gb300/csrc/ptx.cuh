@@ -6,7 +6,11 @@
 #include <cuda.h>
 #include <cstdint>
 
+#include "bounds.cuh"
 #include "status.cuh"
+
+#undef DA_BOUNDS_FILE
+#define DA_BOUNDS_FILE 1
 
 namespace da {
 
@@ -113,6 +117,26 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
 }
 
 // ----------------------------------------------------------------- TMA
+// Bounds-check build: every tiled copy below checks that its shared-memory
+// box starts on 128 bytes and that no coordinate is negative (no copy of
+// this library starts before a tensor); the callers check the coordinates
+// against the tensors' extents and the innermost one against the 16-byte rule.
+#define DA_TMA_OK(saddr, c0, c1, c2, c3) \
+  DA_BOUNDS_V(((saddr) & 127u) == 0u && (c0) >= 0 && (c1) >= 0 && (c2) >= 0 && (c3) >= 0, (c0))
+
+// Bounds-check build: a 32x32b tensor-memory access of `ncols` columns at
+// `taddr` must address this warp's quarter of the lanes (warp w of a
+// warpgroup: lanes 32 (w % 4) ..) and stay inside the 512 columns that every
+// kernel of this library allocates.
+#define DA_TMEM_OK(taddr, ncols)                                                       \
+  DA_BOUNDS_V(((taddr) >> 16) == 32u * ((threadIdx.x >> 5) & 3u) &&                  \
+                  ((taddr) & 0xffffu) + static_cast<uint32_t>(ncols) <= 512u, (taddr))
+// An MMA's accumulator: lane 0, N = idesc bits 17-22 (x 8) columns inside the 512.
+#define DA_MMA_OK(d_tmem, idesc) \
+  DA_BOUNDS_V(((d_tmem) >> 16) == 0u && ((d_tmem) & 0xffffu) + (((idesc) >> 17) & 0x3fu) * 8u <= 512u, (d_tmem))
+// An A operand in tensor memory: lane 0, inside the 512 columns.
+#define DA_TMEM_A_OK(a_tmem) DA_BOUNDS_V(((a_tmem) >> 16) == 0u && ((a_tmem) & 0xffffu) < 512u, (a_tmem))
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -122,6 +146,7 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 // 16-bit data (16-byte rule), which every caller guarantees (0 or 64).
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
                                             int c2, int c3) {
+  if (!DA_TMA_OK(smem_u32(dst), c0, c1, c2, c3)) return;
   asm volatile(
       "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
@@ -132,6 +157,7 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
 // 2-D tiled load global -> shared, completion counted in bytes on `bar`; c0
 // (the innermost coordinate, elements) a multiple of 8 for 16-bit data.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+  if (!DA_TMA_OK(smem_u32(dst), c0, c1, 0, 0)) return;
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
@@ -145,6 +171,7 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
 // source must have been made visible to the async proxy (fence + barrier).
 __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int c0, int c1, int c2,
                                              int c3) {
+  if (!DA_TMA_OK(smem_u32(src), c0, c1, c2, c3)) return;
   asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
                "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
@@ -156,6 +183,7 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void*
 // dropped.  c0 a multiple of 4 (16-byte rule); no negative coordinates.
 __device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* map, const void* src, int c0, int c1, int c2,
                                                   int c3) {
+  if (!DA_TMA_OK(smem_u32(src), c0, c1, c2, c3)) return;
   asm volatile(
       "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
           reinterpret_cast<uint64_t>(map)),
@@ -219,6 +247,7 @@ __device__ __forceinline__ void tc_commit_elect(uint64_t* bar) {
 
 __device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                              uint32_t accumulate) {
+  if (!DA_MMA_OK(d_tmem, idesc)) return;
   asm volatile(
       "{\n\t.reg .pred p, e;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
@@ -230,6 +259,7 @@ __device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, u
 
 __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                              uint32_t accumulate) {
+  if (!DA_MMA_OK(d_tmem, idesc) || !DA_TMEM_A_OK(a_tmem)) return;
   asm volatile(
       "{\n\t.reg .pred p, e;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
@@ -242,6 +272,7 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
 // The same with e4m3 A and B (kind::f8f6f4; K = 32 per instruction).
 __device__ __forceinline__ void mma_ss_f8_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                                 uint32_t accumulate) {
+  if (!DA_MMA_OK(d_tmem, idesc)) return;
   asm volatile(
       "{\n\t.reg .pred p, e;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
@@ -254,6 +285,7 @@ __device__ __forceinline__ void mma_ss_f8_elect(uint32_t d_tmem, uint64_t a_desc
 // D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
+  if (!DA_MMA_OK(d_tmem, idesc)) return;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -265,6 +297,7 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
 // D[tmem] (+)= A[tmem] * B[smem]
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
+  if (!DA_MMA_OK(d_tmem, idesc) || !DA_TMEM_A_OK(a_tmem)) return;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -302,6 +335,7 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
 // 32 lanes x 32 columns of 32-bit data: thread t of the warp gets lane
 // (base lane + t), registers r[0..31] = columns (col .. col+31).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  if (!DA_TMEM_OK(taddr, 32)) return;
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
       "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -341,6 +375,7 @@ __device__ __forceinline__ void tmem_ld_wait2(uint32_t (&a)[32], uint32_t (&b)[3
 
 // 32 lanes x 16 columns store, registers v[0..15] -> columns col .. col+15.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  if (!DA_TMEM_OK(taddr, 16)) return;
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
       "%16};" ::"r"(taddr),
@@ -351,6 +386,7 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
 
 // Narrow variants: x16 loads; x8 / x4 loads fused with their wait; x16 / x2 / x1 stores.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  if (!DA_TMEM_OK(taddr, 16)) return;
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
@@ -372,6 +408,7 @@ __device__ __forceinline__ void tmem_ld_wait16x2(uint32_t (&a)[16], uint32_t (&b
 }
 
 __device__ __forceinline__ void tmem_ld8_wait(uint32_t taddr, uint32_t (&r)[8]) {
+  if (!DA_TMEM_OK(taddr, 8)) return;
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
       "tcgen05.wait::ld.sync.aligned;"
@@ -381,6 +418,7 @@ __device__ __forceinline__ void tmem_ld8_wait(uint32_t taddr, uint32_t (&r)[8]) 
 }
 
 __device__ __forceinline__ void tmem_ld4_wait(uint32_t taddr, uint32_t (&r)[4]) {
+  if (!DA_TMEM_OK(taddr, 4)) return;
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n\t"
       "tcgen05.wait::ld.sync.aligned;"
@@ -390,6 +428,7 @@ __device__ __forceinline__ void tmem_ld4_wait(uint32_t taddr, uint32_t (&r)[4]) 
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  if (!DA_TMEM_OK(taddr, 32)) return;
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
       "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
@@ -401,16 +440,19 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 }
 
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  if (!DA_TMEM_OK(taddr, 8)) return;
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                : "memory");
 }
 
 __device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t a, uint32_t b) {
+  if (!DA_TMEM_OK(taddr, 2)) return;
   asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};" ::"r"(taddr), "r"(a), "r"(b) : "memory");
 }
 
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t a) {
+  if (!DA_TMEM_OK(taddr, 1)) return;
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(a) : "memory");
 }
 

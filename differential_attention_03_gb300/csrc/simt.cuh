@@ -25,6 +25,9 @@
 #include "ptx.cuh"
 #include "stage.cuh"
 
+#undef DA_BOUNDS_FILE
+#define DA_BOUNDS_FILE 8
+
 namespace da {
 
 
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const Sim
       for (int c = 0; c < NC; ++c) {
         const int col = lane + 32 * c;
         if (col < dv) {
-          dorow[col] = dOv[c];
+          DA_STORE(dorow, col, (R_rows - ri) * dv, dOv[c]);
           dd1 = fmaf(dOv[c], o1n[c], dd1);
           dd2 = fmaf(dOv[c], o2n[c], dd2);
         }
@@ -235,7 +238,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const Sim
         dd1 += __shfl_xor_sync(0xffffffffu, dd1, off);
         dd2 += __shfl_xor_sync(0xffffffffu, dd2, off);
       }
-      if (lane == 0) {
+      if (lane == 0 && DA_BOUNDS_V(ri >= 0 && ri < R_rows && b < p.B && t < p.n && u < p.units_per_batch, ri)) {
         const float share = p.v2 ? -coef * (1.f - coef) * dd2 : -dd2;
         x.ws_row[ri] = m1[0] + logf(l1[0]);
         x.ws_row[R_rows + ri] = m2[0] + logf(l2[0]);
@@ -255,7 +258,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const Sim
         float a = 0.f;
 #pragma unroll
         for (int w = 0; w < kSimtWarps; ++w) a += sdg[w * dv + col];
-        x.ws_dgamma[static_cast<size_t>(blockIdx.x) * dv + col] = a;
+        DA_STORE(x.ws_dgamma, static_cast<size_t>(blockIdx.x) * dv + col, static_cast<size_t>(gridDim.x) * dv, a);
       }
     }
   } else {
@@ -291,7 +294,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) simt_fwd_f32_kernel(const Sim
       if (col < dv) {
         float v = y[c] * rinv;
         if (!p.v2 && p.gamma != nullptr) v *= p.gamma[col];
-        orow[col] = v;
+        if (DA_BOUNDS_V(b < p.B && u < p.units_per_batch, t)) orow[col] = v;
       }
     }
   }

@@ -70,6 +70,9 @@
 #include "params.h"
 #include "ptx.cuh"
 
+#undef DA_BOUNDS_FILE
+#define DA_BOUNDS_FILE 3
+
 namespace da {
 
 template <int D, int DV, bool SHARED_K, int EPI, int NSLOT, bool PERSIST, bool F8 = false>
@@ -286,8 +289,12 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
         }
         mbar_arrive_expect_tx(q_full, 2 * C::Q_TILE);
         for (int bx = 0; bx < C::QB; ++bx) {
-          tma_load_4d(smem + C::OFF_Q1 + bx * BM * 128, &p.tm_q1, q_full, bx * 64, c.hq1, c.q0, c.b);
-          tma_load_4d(smem + C::OFF_Q2 + bx * BM * 128, &p.tm_q2, q_full, bx * 64, c.hq2, c.q0, c.b);
+          // (bounds build: query heads of the maps, V1 units, V2 2 units)
+          if (DA_BOUNDS(bx * 64 < D && c.b < p.B && c.q0 < p.n &&
+                        c.hq2 < (EPI == kEpiV2 ? 2 : 1) * p.units_per_batch)) {
+            tma_load_4d(smem + C::OFF_Q1 + bx * BM * 128, &p.tm_q1, q_full, bx * 64, c.hq1, c.q0, c.b);
+            tma_load_4d(smem + C::OFF_Q2 + bx * BM * 128, &p.tm_q2, q_full, bx * 64, c.hq2, c.q0, c.b);
+          }
         }
         ++qloads;
         // One slot fill: `nbox` boxes of [rows][64 columns] at key row `key0`.
@@ -302,7 +309,10 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
           uint64_t* bar = &full[o * NSLOT + s];
           uint8_t* dst = smem + C::OFF_RING + s * C::SLOT;
           mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nbox * rows * 128));
-          for (int bx = 0; bx < nbox; ++bx) tma_load_4d(dst + bx * rows * 128, map, bar, bx * 64, c.hk, key0, c.b);
+          for (int bx = 0; bx < nbox; ++bx)
+            if (DA_BOUNDS(key0 < (p.n + 127) / 128 * 128 && c.b < p.B &&  // (a box past n reads zeros)
+                          c.hk < (EPI == kEpiV2 ? 2 * p.units_per_batch / p.group : p.units_per_batch)))
+              tma_load_4d(dst + bx * rows * 128, map, bar, bx * 64, c.hk, key0, c.b);
           last_o = (last_o & ~(1u << s)) | (static_cast<uint32_t>(o) << s);
           par ^= 1u << (o * NSLOT + s);  // now the parity after this fill; the fill's own is the flip of it
           ++fill;
@@ -704,7 +714,8 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
           fence_proxy_async_smem();
           named_bar_sync(2 + wg, 128);
           if ((threadIdx.x & 127) == 0) {
-            tma_store_4d(&p.tm_out, smem + C::OFF_P + wg * C::STG_BYTES, wg * QW + 32 * rd, c.u, c.q0, c.b);
+            if (DA_BOUNDS(wg * QW + 32 * rd < DV && c.u < p.units_per_batch && c.q0 < p.n && c.b < p.B))
+              tma_store_4d(&p.tm_out, smem + C::OFF_P + wg * C::STG_BYTES, wg * QW + 32 * rd, c.u, c.q0, c.b);
             bulk_commit_group();
           }
         }

@@ -46,7 +46,9 @@ typedef enum {
     DIFFATTN_ERR_UNSUPPORTED = 5, /* valid but not implemented (e.g. bf16 with d not
                                      in {64, 128})                                   */
     DIFFATTN_ERR_CUDA = 6,        /* a CUDA runtime/driver call failed               */
-    DIFFATTN_ERR_TIMEOUT = 7      /* a bounded in-kernel wait ran out                */
+    DIFFATTN_ERR_TIMEOUT = 7,     /* a bounded in-kernel wait ran out                */
+    DIFFATTN_ERR_BOUNDS = 8       /* bounds-check build only: an index check in a
+                                     kernel failed and the access was skipped       */
 } diffattn_status;
 
 typedef enum {
@@ -493,13 +495,33 @@ diffattn_status lambda_reparam_backward(const float* lq1, const float* lk1, cons
 /*
  * Synchronises `stream`, then reads and clears the library's device status
  * word on the current device.  Returns DIFFATTN_OK, DIFFATTN_ERR_TIMEOUT if a
- * bounded in-kernel wait ran out since the last call, or DIFFATTN_ERR_CUDA if
+ * bounded in-kernel wait ran out since the last call, DIFFATTN_ERR_BOUNDS (the
+ * bounds-check build only) if an index check failed, or DIFFATTN_ERR_CUDA if
  * the stream reported an error.
  */
 diffattn_status diffattn_device_status(void* stream);
 
 /* Message for the last non-OK status returned on this host thread ("" if none). */
 const char* diffattn_last_error(void);
+
+/*
+ * 1 if this library is the bounds-check build (libdiffattn_bounds.so, built
+ * with -DDIFFATTN_BOUNDS), else 0.  That build checks every TMA coordinate,
+ * tensor-memory address and global store of its kernels before the access;
+ * a failed check skips the access and diffattn_device_status returns
+ * DIFFATTN_ERR_BOUNDS with the first failing site in diffattn_last_error.  It
+ * is slower and meant for small cases; the results are otherwise identical.
+ */
+int diffattn_bounds_checked(void);
+
+/*
+ * Bounds-check build only (else ERR_UNSUPPORTED, nothing launched): launches
+ * one thread that stores through the checked store at index 5 of a limit of
+ * 4 (into a library-internal 8-element array, so the store could not leave
+ * it either way).  The check must skip the store, and the next
+ * diffattn_device_status must return DIFFATTN_ERR_BOUNDS.
+ */
+diffattn_status diffattn_debug_bounds_selftest(void* stream);
 
 /*
  * Diagnostics: launches one CTA whose thread waits on an mbarrier that nothing

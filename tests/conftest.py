@@ -24,3 +24,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _bounds_build_is_loaded_when_asked():
+    """With DIFFATTN_DEBUG=1 every test runs against the bounds-check build: make sure it is the one loaded."""
+    if os.environ.get("DIFFATTN_DEBUG", "") == "1":
+        from differential_attention_03_gb300 import binding
+        assert binding.BOUNDS and binding.LIB_PATH.endswith("libdiffattn_bounds.so")
+    yield

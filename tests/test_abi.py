@@ -47,6 +47,21 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), f"{name} not exported"
 
 
+def test_normal_build_has_no_bounds_checks(L):
+    assert L.diffattn_bounds_checked() == 0
+    assert L.diffattn_debug_bounds_selftest(None) == da.ERR_UNSUPPORTED  # refused on the host, nothing launched
+
+
+def test_bounds_build_compiles_and_exports_the_same_symbols():
+    path = build.build(bounds=True)
+    assert path.endswith("libdiffattn_bounds.so")
+    Lb = ctypes.CDLL(path)
+    for name in _declared():
+        assert hasattr(Lb, name), f"{name} not exported by the bounds-check build"
+    Lb.diffattn_bounds_checked.restype = ctypes.c_int
+    assert Lb.diffattn_bounds_checked() == 1
+
+
 def test_lambda_init_host(L):
     for l in (1, 4, 12, 20):
         assert da.lambda_init(l) == pytest.approx(oracle.lambda_init(l), abs=1e-7)
