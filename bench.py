@@ -55,10 +55,10 @@ def hbm_bytes(w) -> float:
 # kernel it was taken from: it is keyed to the hash of that kernel's source
 # files and reported while the hash still matches, null otherwise.
 KERNEL_FILES = {
-    "v1-bf16-B4H16-n2048-d64": ['onepass.cuh', 'onepass_inst.cuh', 'k_onepass_v1_d64.cu', 'params.h', 'ptx.cuh', 'status.cuh'],
-    "v1-bf16-B2H12-n4096-d128": ['twopass.cuh', 'twopass_inst.cuh', 'k_twopass_v1_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh'],
-    "v1-bf16-B1H12-n65536-d128": ['twopass.cuh', 'twopass_inst.cuh', 'k_twopass_v1_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh'],
-    "v2-bf16-B8Hq32Hkv16-n8192-d128": ['onepass.cuh', 'onepass_inst.cuh', 'k_onepass_v2_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh'],
+    "v1-bf16-B4H16-n2048-d64": ['onepass.cuh', 'onepass_inst.cuh', 'k_onepass_v1_d64.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh'],
+    "v1-bf16-B2H12-n4096-d128": ['twopass.cuh', 'twopass_inst.cuh', 'k_twopass_v1_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh'],
+    "v1-bf16-B1H12-n65536-d128": ['twopass.cuh', 'twopass_inst.cuh', 'k_twopass_v1_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh'],
+    "v2-bf16-B8Hq32Hkv16-n8192-d128": ['onepass.cuh', 'onepass_inst.cuh', 'k_onepass_v2_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh'],
 }
 NCU_TRAFFIC = {  # workload: (source hash of its kernel, bytes per launch)
     "v1-bf16-B4H16-n2048-d64": ("413f0242e5ff72fd", 136.099840e6 + 14.131200e6),
@@ -230,7 +230,7 @@ def time_e2e(w, x, da, steps):
 
     V1: diffattn_forward_host takes the step's inputs in page-locked host
     memory and returns the output there (copies in, forward and copies out
-    pipelined over batch chunks inside the library); lambda and gamma are
+    pipelined over batch or token chunks inside the library); lambda and gamma are
     layer parameters resident on the device.  V2: the inputs are copied in
     and the output back around diffattn_v2_forward.  Every step includes the
     copies of its inputs and output.
@@ -676,14 +676,30 @@ PROJECTION_WORKLOADS = [  # (name, M, N, K): c = a w^T alone
 
 
 def fp8_results(da, flush, peaks, inputs):
-    """The V1 forward with e4m3 queries and keys (one scale per tensor, amax / 448) on the d = 128
-    workloads: TFLOP/s (the same algorithmic FLOPs as bf16) against the measured burst bf16 peak."""
+    """The V1 and V2 forwards with e4m3 queries and keys (one scale per tensor, amax / 448) on the
+    d = 128 workloads: TFLOP/s (the same algorithmic FLOPs as bf16) against the measured burst bf16 peak."""
     import torch
     from differential_attention_03_gb300.inputs import WORKLOADS
     out = {}
-    for wid in (3, 4):
+    for wid in (3, 4, 5):
         w = WORKLOADS[wid]
         x = inputs(w)
+        if w.kind == "v2":
+            cq_sc = [float(x[k].float().abs().max()) / 448.0 for k in ("q", "k")]
+            cq, ck = ((x[k].float() / sc).to(torch.float8_e4m3fn) for k, sc in zip(("q", "k"), cq_sc))
+            y = torch.empty((w.B, w.n, w.Hq // 2, w.d), device="cuda", dtype=torch.bfloat16)
+
+            def call2():
+                da.diffattn_v2_forward_fp8qk(cq, ck, cq_sc, x["v"], x["lam_logits"], causal=w.causal, out=y)
+            ms = _median_ms(call2, flush, runs=10)
+            da.device_status()
+            tf = flops(w) / (ms * 1e-3) / 1e12
+            out["fp8qk-" + w.name] = {"ms": round(ms, 4), "tflops": round(tf, 2),
+                                      "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                                      "tokens_per_s": round(w.B * w.n / (ms * 1e-3), 1)}
+            del cq, ck, x, y
+            torch.cuda.empty_cache()
+            continue
         codes, scales = [], []
         for k in ("q1", "q2", "k1", "k2"):
             sc = float(x[k].float().abs().max()) / 448.0
@@ -814,11 +830,12 @@ def run_layer_only(only=None):
     build.build()
     da.lib()
     flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
-    from differential_attention_03_gb300.inputs import make_v1
+    from differential_attention_03_gb300.inputs import make_v1, make_v2
     peaks = read_peaks()
     line = {"layer": layer_results(da, flush, peaks, only)}
     if not only:
-        line["fp8"] = fp8_results(da, flush, peaks, lambda w: make_v1(w, "cuda"))
+        line["fp8"] = fp8_results(da, flush, peaks,
+                                  lambda w: make_v1(w, "cuda") if w.kind == "v1" else make_v2(w, "cuda"))
     print(json.dumps(line), flush=True)
 
 

@@ -95,6 +95,8 @@ def lib() -> ctypes.CDLL:
             L.diffattn_v2_forward.restype = i
             L.diffattn_forward_fp8qk.argtypes = [i, i, i, i, vp, vp, vp, vp, f, f, f, f, vp, vp, f, vp, f, i, vp, vp]
             L.diffattn_forward_fp8qk.restype = i
+            L.diffattn_v2_forward_fp8qk.argtypes = [i, i, i, i, i, vp, vp, f, f, vp, vp, ll, ll, f, i, vp, vp]
+            L.diffattn_v2_forward_fp8qk.restype = i
             L.diffattn_projection.argtypes = [i, i, i, vp, vp, vp, vp]
             L.diffattn_projection.restype = i
             L.diffattn_layer_workspace.argtypes = [i, i, i, i]
@@ -545,6 +547,43 @@ def lambda_reparam_backward(lq1, lk1, lq2, lk2, dlam, stream=None):
     return tuple(outs)
 
 
+def _logit_strides(lam_logits, B, n, G):
+    if lam_logits.shape == (G,):
+        return 0, 0
+    if lam_logits.shape == (n, G):
+        return 0, G
+    if lam_logits.shape == (B, n, G):
+        return n * G, G
+    raise ValueError(f"lam_logits must be [Hq/2], [n, Hq/2] or [B, n, Hq/2]; got {tuple(lam_logits.shape)}")
+
+
+def diffattn_v2_forward_fp8qk(q, k, scales, v, lam_logits, causal: bool = True, softmax_scale: float = 0.0,
+                              out=None, stream=None) -> torch.Tensor:
+    """DIFF V2 forward with e4m3 queries and keys (QK^T on the FP8 tensor-core path).
+
+    q: [B, n, Hq, 128], k: [B, n, Hkv, 128] e4m3 codes (torch.float8_e4m3fn or their bytes as uint8)
+    of Q / q_scale and K / k_scale; scales = (q_scale, k_scale); v bf16 [B, n, Hkv, 128]; lam_logits
+    as for diffattn_v2_forward.  The result is diffattn_v2_forward's for Q = q_scale e4m3(q),
+    K = k_scale e4m3(k).  Returns out [B, n, Hq/2, 128] bf16.
+    """
+    B, n, Hq, d = q.shape
+    Hkv = k.shape[2]
+    _need_fp8(q, "q", (B, n, Hq, d))
+    _need_fp8(k, "k", (B, n, Hkv, d))
+    _need(v, "v", torch.bfloat16, (B, n, Hkv, d))
+    G = Hq // 2
+    _need(lam_logits, "lam_logits", torch.float32)
+    sb, st = _logit_strides(lam_logits, B, n, G)
+    if out is None:
+        out = torch.empty((B, n, G, d), device=v.device, dtype=torch.bfloat16)
+    _need(out, "out", torch.bfloat16, (B, n, G, d))
+    qs, ks = (float(x) for x in scales)
+    _check(lib().diffattn_v2_forward_fp8qk(B, Hq, Hkv, n, d, _ptr(q), _ptr(k), qs, ks, _ptr(v), _ptr(lam_logits),
+                                           sb, st, float(softmax_scale), 1 if causal else 0, _ptr(out),
+                                           _stream(stream)))
+    return out
+
+
 def diffattn_v2_forward(q, k, v, lam_logits, causal: bool = True, softmax_scale: float = 0.0, out=None,
                         stream=None) -> torch.Tensor:
     """DIFF V2 forward: out_g = attn[2g] - sigmoid(logit) attn[2g+1]; BSHD tensors.
@@ -560,14 +599,7 @@ def diffattn_v2_forward(q, k, v, lam_logits, causal: bool = True, softmax_scale:
     _need(v, "v", dt, (B, n, Hkv, d))
     G = Hq // 2
     _need(lam_logits, "lam_logits", torch.float32)
-    if lam_logits.shape == (G,):
-        sb, st = 0, 0
-    elif lam_logits.shape == (n, G):
-        sb, st = 0, G
-    elif lam_logits.shape == (B, n, G):
-        sb, st = n * G, G
-    else:
-        raise ValueError(f"lam_logits must be [Hq/2], [n, Hq/2] or [B, n, Hq/2]; got {tuple(lam_logits.shape)}")
+    sb, st = _logit_strides(lam_logits, B, n, G)
     if out is None:
         out = torch.empty((B, n, G, d), device=q.device, dtype=dt)
     _need(out, "out", dt, (B, n, G, d))

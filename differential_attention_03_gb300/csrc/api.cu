@@ -253,9 +253,10 @@ struct QKVViews {
 // launches it: sc1 / sc2 are the two maps' softmax scales x log2(e); f8
 // selects the kernel that reads e4m3 queries and keys.  `out` is a
 // contiguous [B, n, H, 2d] tensor.
+// Query tiles [qt0, qt0 + nqt) of every (batch, head) (nqt < 0: all of them).
 diffattn_status launch_v1_tc(const char* fn, da::TwoPassParams& p, bool f8, int B, int H, int n, int d, float sc1,
                              float sc2, const float* lambda, float lambda_init, const float* gamma, float eps,
-                             int causal, void* out, int* status, cudaStream_t s) {
+                             int causal, void* out, int* status, cudaStream_t s, int qt0 = 0, int nqt = -1) {
   const int dv = 2 * d;
   diffattn_status st;
   // Output stores: boxes of 128 tokens x 32 channels.
@@ -273,7 +274,8 @@ diffattn_status launch_v1_tc(const char* fn, da::TwoPassParams& p, bool f8, int 
   p.causal = causal ? 1 : 0;
   p.units_per_batch = H;
   p.group = 1;
-  p.num_q_tiles = (n + 127) / 128;
+  p.num_q_tiles = nqt < 0 ? (n + 127) / 128 : nqt;
+  p.q_tile_begin = qt0;
   p.order = pick_order(static_cast<long long>(B) * H, n, (2 * d + dv) * 2);
   p.status = status;
   const long long grid = static_cast<long long>(p.num_q_tiles) * B * H;
@@ -284,7 +286,7 @@ diffattn_status launch_v1_tc(const char* fn, da::TwoPassParams& p, bool f8, int 
   // so each item's start overlaps the previous one's end.  Long items: one
   // CTA per item (the fixed cost is small against them, and the hardware's
   // dynamic CTA scheduling balances them; measured faster).
-  const bool persist = p.num_q_tiles <= 64;
+  const bool persist = qt0 + p.num_q_tiles <= 64;  // (the last tile's item length decides)
   const int g = static_cast<int>(persist ? persistent_grid(grid) : grid);
   cudaError_t e = f8 ? da::launch_twopass_v1_d128_f8(p, g, persist, s)
                      : (d == 64) ? da::launch_onepass_v1_d64(p, g, persist, s)
@@ -298,7 +300,7 @@ diffattn_status launch_v1_tc(const char* fn, da::TwoPassParams& p, bool f8, int 
 // is a contiguous [B, n, H, 2d] tensor.
 diffattn_status forward_v1_bf16(const char* fn, const QKVViews& x, int B, int H, int n, int d, const float* lambda,
                                 float lambda_init, const float* gamma, float eps, int causal, void* out, int* status,
-                                cudaStream_t s) {
+                                cudaStream_t s, int qt0 = 0, int nqt = -1) {
   const int dv = 2 * d;
   da::TwoPassParams p;
   memset(&p, 0, sizeof(p));
@@ -310,30 +312,25 @@ diffattn_status forward_v1_bf16(const char* fn, const QKVViews& x, int B, int H,
   if ((st = make_map_view(&p.tm_k2, x.k2, B, n, H, d, x.k_head, x.k_tok, 64, 128)) != DIFFATTN_OK) return st;
   if ((st = make_map_view(&p.tm_v, x.v, B, n, H, dv, x.v_head, x.v_tok, 64, 64)) != DIFFATTN_OK) return st;
   const float sc = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
-  return launch_v1_tc(fn, p, false, B, H, n, d, sc, sc, lambda, lambda_init, gamma, eps, causal, out, status, s);
+  return launch_v1_tc(fn, p, false, B, H, n, d, sc, sc, lambda, lambda_init, gamma, eps, causal, out, status, s, qt0,
+                      nqt);
 }
 
-// DIFF V2 bf16 forward (d = 128) on already validated views of q (Hq heads)
-// and k, v (Hkv heads); `out` is a contiguous [B, n, Hq / 2, d] tensor.
-diffattn_status forward_v2_bf16(const char* fn, const QKVViews& x, int B, int Hq, int Hkv, int n, int d,
-                                const float* lam_logits, long long sb, long long st_, float scale, int causal,
-                                void* out, int* status, cudaStream_t s) {
+// The DIFF V2 forward (d = 128) on tensor maps of q (Hq heads) and k, v (Hkv
+// heads) already in p (e4m3 q and k when f8); `out` is a contiguous
+// [B, n, Hq / 2, d] tensor; scale_log2 = softmax scale x log2(e) (x the
+// e4m3 dequantisation scales).
+diffattn_status launch_v2_tc(const char* fn, da::TwoPassParams& p, bool f8, int B, int Hq, int Hkv, int n, int d,
+                             const float* lam_logits, long long sb, long long st_, float scale_log2, int causal,
+                             void* out, int* status, cudaStream_t s) {
   const int G = Hq / 2;
-  da::TwoPassParams p;
-  memset(&p, 0, sizeof(p));
   diffattn_status st;
-  if ((st = make_map_view(&p.tm_q1, x.q1, B, n, Hq, d, x.q_head, x.q_tok, 64, 128)) != DIFFATTN_OK) return st;
-  p.tm_q2 = p.tm_q1;
-  // Key and value tiles are 128 rows (one ring slot each).
-  if ((st = make_map_view(&p.tm_k1, x.k1, B, n, Hkv, d, x.k_head, x.k_tok, 64, 128)) != DIFFATTN_OK) return st;
-  p.tm_k2 = p.tm_k1;
-  if ((st = make_map_view(&p.tm_v, x.v, B, n, Hkv, d, x.v_head, x.v_tok, 64, 128)) != DIFFATTN_OK) return st;
   if ((st = make_map_box(&p.tm_out, out, B, n, G, d, 32, 128)) != DIFFATTN_OK) return st;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lam_logits = lam_logits;
   p.sb = sb;
   p.st = st_;
-  p.scale_log2 = static_cast<float>(1.4426950408889634 * scale);
+  p.scale_log2 = scale_log2;
   p.norm_mult = 1.f;
   p.eps = 0.f;
   p.B = B;
@@ -349,10 +346,29 @@ diffattn_status forward_v2_bf16(const char* fn, const QKVViews& x, int B, int Hq
   if (grid > 0x7fffffffll) return fail(DIFFATTN_ERR_SHAPE, "%s: too many tiles", fn);
   // V2 items are long (up to n / 128 key tiles): one CTA per item, so the
   // hardware's dynamic CTA scheduling balances them (measured faster here).
-  cudaError_t e = da::launch_onepass_v2_d128(p, static_cast<int>(grid), s);
+  cudaError_t e = f8 ? da::launch_onepass_v2_d128_f8(p, static_cast<int>(grid), s)
+                     : da::launch_onepass_v2_d128(p, static_cast<int>(grid), s);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   g_launches.fetch_add(1);
   return DIFFATTN_OK;
+}
+
+// DIFF V2 bf16 forward (d = 128) on already validated views of q (Hq heads)
+// and k, v (Hkv heads); `out` is a contiguous [B, n, Hq / 2, d] tensor.
+diffattn_status forward_v2_bf16(const char* fn, const QKVViews& x, int B, int Hq, int Hkv, int n, int d,
+                                const float* lam_logits, long long sb, long long st_, float scale, int causal,
+                                void* out, int* status, cudaStream_t s) {
+  da::TwoPassParams p;
+  memset(&p, 0, sizeof(p));
+  diffattn_status st;
+  if ((st = make_map_view(&p.tm_q1, x.q1, B, n, Hq, d, x.q_head, x.q_tok, 64, 128)) != DIFFATTN_OK) return st;
+  p.tm_q2 = p.tm_q1;
+  // Key and value tiles are 128 rows (one ring slot each).
+  if ((st = make_map_view(&p.tm_k1, x.k1, B, n, Hkv, d, x.k_head, x.k_tok, 64, 128)) != DIFFATTN_OK) return st;
+  p.tm_k2 = p.tm_k1;
+  if ((st = make_map_view(&p.tm_v, x.v, B, n, Hkv, d, x.v_head, x.v_tok, 64, 128)) != DIFFATTN_OK) return st;
+  return launch_v2_tc(fn, p, false, B, Hq, Hkv, n, d, lam_logits, sb, st_,
+                      static_cast<float>(1.4426950408889634 * scale), causal, out, status, s);
 }
 
 }  // namespace
@@ -474,10 +490,48 @@ diffattn_status diffattn_forward_fp8qk(int B, int H, int n, int d, const void* q
   return ok();
 }
 
+// DIFF V2 forward with e4m3 queries and keys (d = 128): QK^T on kind::f8f6f4.
+diffattn_status diffattn_v2_forward_fp8qk(int B, int Hq, int Hkv, int n, int d, const void* q, const void* k,
+                                          float q_scale, float k_scale, const void* v, const float* lam_logits,
+                                          long long sb, long long st_, float softmax_scale, int causal, void* out,
+                                          void* stream) {
+  const char* fn = "diffattn_v2_forward_fp8qk";
+  if (B < 0 || Hq < 0 || Hkv < 1 || n < 0 || d < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: bad sizes B=%d Hq=%d Hkv=%d n=%d d=%d", fn, B, Hq, Hkv, n, d);
+  if (Hq % 2 != 0 || Hq % Hkv != 0 || (Hq / Hkv) % 2 != 0)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need Hq even, Hq %% Hkv == 0 and Hq/Hkv even (Hq=%d Hkv=%d)", fn, Hq, Hkv);
+  if (sb < 0 || st_ < 0) return fail(DIFFATTN_ERR_SHAPE, "%s: negative logit stride", fn);
+  if (d != 128) return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: d = 128 only (got %d)", fn, d);
+  if (B == 0 || Hq == 0 || n == 0) return ok();
+  if (!q || !k || !v || !lam_logits || !out) return fail(DIFFATTN_ERR_NULL, "%s: NULL pointer", fn);
+  for (float sc : {q_scale, k_scale})
+    if (!(std::isfinite(sc) && sc > 0.f)) return fail(DIFFATTN_ERR_SHAPE, "%s: scales must be finite and positive", fn);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  const double scale = softmax_scale > 0.f ? softmax_scale : 1.0 / std::sqrt(static_cast<double>(d));
+  int* status = nullptr;
+  diffattn_status st = status_word(&status);
+  if (st != DIFFATTN_OK) return st;
+  da::TwoPassParams p;
+  memset(&p, 0, sizeof(p));
+  // Query and key rows are 128 bytes: one box (128-byte swizzle) of 128 rows a tile.
+  if ((st = make_map_u8(&p.tm_q1, q, B, n, Hq, d, 128)) != DIFFATTN_OK) return st;
+  p.tm_q2 = p.tm_q1;
+  if ((st = make_map_u8(&p.tm_k1, k, B, n, Hkv, d, 128)) != DIFFATTN_OK) return st;
+  p.tm_k2 = p.tm_k1;
+  if ((st = make_map_box(&p.tm_v, v, B, n, Hkv, d, 64, 128)) != DIFFATTN_OK) return st;
+  // S = (q_scale k_scale) e4m3(q) e4m3(k)^T x scale: both scales fold into the exponent.
+  const float sc = static_cast<float>(1.4426950408889634 * scale * q_scale * k_scale);
+  if ((st = launch_v2_tc(fn, p, true, B, Hq, Hkv, n, d, lam_logits, sb, st_, sc, causal, out, status,
+                         static_cast<cudaStream_t>(stream))) != DIFFATTN_OK)
+    return st;
+  return ok();
+}
+
 // ---------------------------------------------------------------- host-buffer forward
 namespace {
 
-constexpr int kMaxChunks = 8;
+constexpr int kMaxChunks = 8;  // chunks per call (events per pipeline)
 
 // Copy streams and events of the host-buffer forward, created once per device
 // and reused by every call (enqueueing a call holds the mutex, so calls from
@@ -486,6 +540,7 @@ struct HostPipe {
   std::mutex mu;
   bool ready = false;
   cudaStream_t in = nullptr, out = nullptr;
+  cudaStream_t comp = nullptr;  // second compute stream: token chunks alternate between it and the caller's
   cudaEvent_t start = nullptr, last_out = nullptr;
   cudaEvent_t in_done[kMaxChunks] = {}, fwd_done[kMaxChunks] = {};
 };
@@ -504,6 +559,7 @@ diffattn_status host_pipe_init(HostPipe& hp) {
   if (hp.ready) return DIFFATTN_OK;
   cudaError_t e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.comp, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.last_out, cudaEventDisableTiming);
   for (int c = 0; e == cudaSuccess && c < kMaxChunks; ++c) {
@@ -569,6 +625,70 @@ diffattn_status diffattn_forward_host(diffattn_dtype dt, int B, int H, int n, in
   cudaError_t e = cudaEventRecord(hp->start, s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->in, hp->start, 0);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward_host: stream ordering");
+
+  // Few sequences of a causal bf16 forward: pipeline over token chunks instead
+  // of batch chunks.  Chunk c holds tokens [t0, t1) of every sequence (128-row
+  // tiles [c0, c1)); in BSHD those rows are contiguous per sequence.  The
+  // queries of chunk c see only keys < t1, all copied in by chunks 0 .. c, so
+  // its forward (query tiles [c0, c1) against the whole device buffer) starts
+  // once its own copies are in, while the next chunk's copies run.  The
+  // chunks' forwards write disjoint rows and depend only on copies, so they
+  // alternate between the caller's stream and a second compute stream: the
+  // next chunk's CTAs take the SMs that the previous launch's last CTAs leave
+  // idle.  Each query tile's item is the same as in one launch over every
+  // tile, so the results are identical to diffattn_forward's.
+  const int ntiles = (n + 127) / 128;
+  if (dt == DIFFATTN_BF16 && causal && B < 4 && ntiles >= 2) {
+    if (d != 64 && d != 128)
+      return fail(DIFFATTN_ERR_UNSUPPORTED, "diffattn_forward_host: bf16 needs d in {64, 128} (got %d)", d);
+    if (!std::isfinite(lambda_init)) return fail(DIFFATTN_ERR_SHAPE, "diffattn_forward_host: lambda_init not finite");
+    int* status = nullptr;
+    if ((st = status_word(&status)) != DIFFATTN_OK) return st;
+    if (eps <= 0.f) eps = 1e-5f;
+    const size_t qrow = static_cast<size_t>(H) * d * es, vrow = 2 * qrow;  // bytes of one token's row
+    const long long Hd = static_cast<long long>(H) * d;
+    const QKVViews x{dq1, dq2, dk1, dk2, dv, d, Hd, d, Hd, 2 * d, 2 * Hd};
+    const int nchunk = ntiles < kMaxChunks ? ntiles : kMaxChunks;
+    const uint8_t* hsrc[5] = {static_cast<const uint8_t*>(q1), static_cast<const uint8_t*>(q2),
+                              static_cast<const uint8_t*>(k1), static_cast<const uint8_t*>(k2),
+                              static_cast<const uint8_t*>(v)};
+    uint8_t* const ddst[5] = {dq1, dq2, dk1, dk2, dv};
+    for (int c = 0; c < nchunk; ++c) {
+      const int c0 = static_cast<int>(static_cast<long long>(ntiles) * c / nchunk);
+      const int c1 = static_cast<int>(static_cast<long long>(ntiles) * (c + 1) / nchunk);
+      const size_t t0 = static_cast<size_t>(c0) * 128, t1 = std::min(static_cast<size_t>(n), static_cast<size_t>(c1) * 128);
+      for (int b = 0; b < B && e == cudaSuccess; ++b) {
+        const size_t r0 = static_cast<size_t>(b) * n + t0;
+        for (int tsr = 0; tsr < 5 && e == cudaSuccess; ++tsr) {
+          const size_t rb = tsr == 4 ? vrow : qrow;
+          e = cudaMemcpyAsync(ddst[tsr] + r0 * rb, hsrc[tsr] + r0 * rb, (t1 - t0) * rb, cudaMemcpyHostToDevice,
+                              hp->in);
+        }
+      }
+      // (the second compute stream sees the caller's earlier work, lambda
+      // included, through the copy stream, which waited for it at `start`)
+      const cudaStream_t sc = (c & 1) ? hp->comp : s;
+      if (e == cudaSuccess) e = cudaEventRecord(hp->in_done[c], hp->in);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, hp->in_done[c], 0);
+      if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward_host: copy in");
+      if ((st = forward_v1_bf16("diffattn_forward_host", x, B, H, n, d, lambda, lambda_init, gamma, eps, causal, dout,
+                                status, sc, c0, c1 - c0)) != DIFFATTN_OK)
+        return st;
+      e = cudaEventRecord(hp->fwd_done[c], sc);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->fwd_done[c], 0);
+      for (int b = 0; b < B && e == cudaSuccess; ++b) {
+        const size_t r0 = static_cast<size_t>(b) * n + t0;
+        e = cudaMemcpyAsync(static_cast<uint8_t*>(out) + r0 * vrow, dout + r0 * vrow, (t1 - t0) * vrow,
+                            cudaMemcpyDeviceToHost, hp->out);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward_host: copy out");
+    }
+    e = cudaEventRecord(hp->last_out, hp->out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->last_out, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "diffattn_forward_host: stream ordering");
+    return ok();
+  }
+
   const int nchunk = B < kMaxChunks ? B : kMaxChunks;
   for (int c = 0; c < nchunk; ++c) {
     const int b0 = static_cast<int>(static_cast<long long>(B) * c / nchunk);

@@ -24,6 +24,8 @@ cudaError_t launch_twopass_v1_d128_f8(const TwoPassParams& p, int grid, bool per
 cudaError_t launch_onepass_v1_d64(const TwoPassParams& p, int grid, bool persistent, cudaStream_t s);
 // V2, d = 128 (query/key/value width 128), one K/V head per query-head pair: one sweep.
 cudaError_t launch_onepass_v2_d128(const TwoPassParams& p, int grid, cudaStream_t s);
+// The same with e4m3 queries and keys (tm_q1 / tm_k1 over bytes; scale_log2 carries their scales).
+cudaError_t launch_onepass_v2_d128_f8(const TwoPassParams& p, int grid, cudaStream_t s);
 
 cudaError_t launch_simt_f32(const SimtParams& p, cudaStream_t s);
 // V1 decode (one query per sequence over a key/value cache), d in {64, 128}:

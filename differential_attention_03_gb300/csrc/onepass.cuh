@@ -71,7 +71,7 @@
 
 namespace da {
 
-template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST, bool STATS = false>
+template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST, bool STATS = false, bool F8 = false>
 struct OnePassCfg {
   static constexpr int BM = 128;
   static constexpr int BN = 128;
@@ -79,12 +79,15 @@ struct OnePassCfg {
   static constexpr int NCTRL = 3;  // producer, two MMA warps
   static constexpr int NSMWG = 4;  // two softmax warpgroups per map
   static constexpr int NTHREADS = (NCTRL + 4 * NSMWG) * 32;
-  static constexpr int QB = D / 64;
+  // F8: queries and keys arrive as e4m3 bytes (a d = 128 row is one
+  // 128-byte box; a key fill takes half a ring slot); V and P stay bf16.
+  static constexpr int QK_ES = F8 ? 1 : 2;       // bytes of a query/key element
+  static constexpr int QB = D * QK_ES / 128;     // 128-byte boxes across a Q/K row
   static constexpr int VB = DV / 64;
-  static constexpr int Q_TILE = BM * D * 2;
-  static constexpr int K_TILE = BN * D * 2;
+  static constexpr int Q_TILE = BM * D * QK_ES;
+  static constexpr int K_TILE = BN * D * QK_ES;
   static constexpr int V_TILE = BN * DV * 2;
-  static constexpr int SLOT = K_TILE;
+  static constexpr int SLOT = BN * D * 2;  // a bf16 key tile
   static constexpr int VF = V_TILE / SLOT;
   static constexpr int VKEYS = BN / VF;
   static constexpr int OFF_Q1 = 0;
@@ -104,11 +107,13 @@ struct OnePassCfg {
   static constexpr int SMEM_BYTES = OFF_GAMMA + DV * 4 + 1024;    // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t TM_O1 = 0, TM_O2 = 128, TM_A = 256, TM_B = 384;
-  static constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, false, false);
+  static constexpr uint32_t IDESC_QK = F8 ? idesc_e4m3(BM, BN) : idesc_bf16(BM, BN, false, false);
+  static constexpr int QK_STEPS = D * QK_ES / 32;  // MMAs per QK^T tile (32 bytes of each row each)
   static constexpr uint32_t IDESC_PV = idesc_bf16(BM, DV, false, true);
   static constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units
   static constexpr int MAX_ITEMS = PERSIST ? 0x7fffffff : 1;  // work items per CTA
   static_assert(D == 64 || D == 128, "query/key width");
+  static_assert(!F8 || (D == 128 && SHARED_K && !STATS), "e4m3 queries and keys: the V2 forward, d = 128");
   static_assert(V_TILE % SLOT == 0 && (VF == 1 || VF == 2), "value tile split");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(NSLOT >= 4, "ring depth");
@@ -312,9 +317,9 @@ __device__ __forceinline__ void onepass_stats_epilogue(const TwoPassParams& p, c
   (void)map;
 }
 
-template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST, bool STATS = false>
+template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST, bool STATS = false, bool F8 = false>
 __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
-  using C = OnePassCfg<D, SHARED_K, EPI, NSLOT, PSM, PERSIST, STATS>;
+  using C = OnePassCfg<D, SHARED_K, EPI, NSLOT, PSM, PERSIST, STATS, F8>;
   constexpr int BM = C::BM, BN = C::BN, DV = C::DV;
 
   extern __shared__ uint8_t smem_raw[];
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
             return;
           }
           uint8_t* dst = smem + C::OFF_RING + s * C::SLOT;
-          mbar_arrive_expect_tx(&full[s], C::SLOT);
+          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nbox * rows * 128));
           for (int bx = 0; bx < nbox; ++bx)
             if (DA_BOUNDS(key0 < (p.n + 127) / 128 * 128 && c.b < p.B &&  // (a box past n reads zeros)
                           c.hk < (EPI == kEpiV2 ? 2 * p.units_per_batch / p.group : p.units_per_batch)))
@@ -497,10 +502,15 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
     auto qk = [&](int s) {
       const uint64_t dk = dRingK + static_cast<uint64_t>((s * C::SLOT) >> 4);
 #pragma unroll
-      for (int k = 0; k < D / 16; ++k)
-        mma_ss_elect(tS, dQ + static_cast<uint64_t>((((k >> 2) * (BM * 128)) + (k & 3) * 32) >> 4),
-                     dk + static_cast<uint64_t>((((k >> 2) * (BN * 128)) + (k & 3) * 32) >> 4), C::IDESC_QK,
-                     k > 0 ? 1u : 0u);
+      for (int k = 0; k < C::QK_STEPS; ++k) {
+        // k-step k reads 32 bytes of each row: box k / 4, bytes 32 (k % 4) .. +31
+        const uint64_t a = dQ + static_cast<uint64_t>((((k >> 2) * (BM * 128)) + (k & 3) * 32) >> 4);
+        const uint64_t b = dk + static_cast<uint64_t>((((k >> 2) * (BN * 128)) + (k & 3) * 32) >> 4);
+        if constexpr (F8)
+          mma_ss_f8_elect(tS, a, b, C::IDESC_QK, k > 0 ? 1u : 0u);
+        else
+          mma_ss_elect(tS, a, b, C::IDESC_QK, k > 0 ? 1u : 0u);
+      }
     };
     // K fills of the tile with global index g (tiles counted across items):
     // K (shared) or K_1 then K_2.  With P in shared memory QK_r(g) only waits

@@ -26,7 +26,8 @@ struct TwoPassParams {
   int B, n, causal;
   int units_per_batch;  // V1: H; V2: Hq / 2
   int group;            // V2: query heads per KV head
-  int num_q_tiles;
+  int num_q_tiles;   // query tiles per unit in this launch: [q_tile_begin, q_tile_begin + num_q_tiles)
+  int q_tile_begin;  // first query tile (0 unless a causal forward is run over token chunks)
   int order;  // 0: unit-major tile order, 1: query-tile-major
   int* status;
   CUtensorMap tm_out;  // output [B, n, units_per_batch, DV] for TMA stores
@@ -71,8 +72,8 @@ __device__ __forceinline__ TileCoord tile_coord(const TwoPassParams& p, int idx)
     c.hq2 = 2 * c.u + 1;
     c.hk = c.hq1 / p.group;
   }
-  c.qt = qt;
-  c.q0 = qt * 128;
+  c.qt = qt + p.q_tile_begin;
+  c.q0 = c.qt * 128;
   return c;
 }
 

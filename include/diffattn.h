@@ -136,11 +136,40 @@ diffattn_status diffattn_forward_fp8qk(int B, int H, int n, int d, const void* q
                                        float eps, int causal, void* out, void* stream);
 
 /*
+ * diffattn_v2_forward with the queries and keys in FP8 (e4m3), one
+ * dequantisation scale per tensor: the low-bit score products that the
+ * "Differential Transformer" glossary page (section on the reported
+ * benefits) motivates by the smaller activation outliers, as in
+ * diffattn_forward_fp8qk, applied to the DIFF V2 operator (DIFF V2 analysis page, "2. 커스텀 커널
+ * 제거", "GQA와의 호환성").  The two query heads of a pair score against
+ * their shared key head with kind::f8f6f4 MMAs (fp32 accumulation); P and V
+ * stay bf16.
+ *   q : [B, n, Hq, d] device bytes (e4m3 codes) holding q / q_scale;
+ *   k : [B, n, Hkv, d] device bytes holding k / k_scale;
+ *   q_scale, k_scale : finite and positive, else ERR_SHAPE.
+ *   v, lam_logits, sb, st, softmax_scale, causal, out : as for
+ *         diffattn_v2_forward with dt = DIFFATTN_BF16.
+ * The result is diffattn_v2_forward's for Q = q_scale e4m3(q) and
+ * K = k_scale e4m3(k).  d = 128 only, else ERR_UNSUPPORTED; errors otherwise
+ * as for diffattn_v2_forward.
+ */
+diffattn_status diffattn_v2_forward_fp8qk(int B, int Hq, int Hkv, int n, int d, const void* q, const void* k,
+                                          float q_scale, float k_scale, const void* v, const float* lam_logits,
+                                          long long sb, long long st, float softmax_scale, int causal,
+                                          void* out, void* stream);
+
+/*
  * diffattn_forward on inputs and output in HOST memory: the call copies the
  * inputs in, runs the forward and copies the output back, pipelined over
- * chunks of the batch (the copy of chunk c + 1 in, the forward of chunk c
- * and the copy of chunk c - 1 out overlap on internal copy streams).  Same
- * operation, layouts, arguments and errors as diffattn_forward, except:
+ * chunks (the copy of chunk c + 1 in, the forward of chunk c and the copy of
+ * chunk c - 1 out overlap on internal copy streams).  The chunks are batch
+ * entries, except for a causal bf16 forward of fewer than four sequences:
+ * then they are ranges of 128-token tiles of every sequence (the queries of
+ * a range see only keys copied in by it and the ranges before it), whose
+ * forwards alternate between `stream` and an internal compute stream; at
+ * most eight chunks.  The output is identical to diffattn_forward's either
+ * way.  Same operation, layouts, arguments and errors as diffattn_forward,
+ * except:
  *   q1, q2, k1, k2, v (in), out : host memory, [B, n, H, d] / [B, n, H, 2d];
  *                 page-locked (cudaHostAlloc / cudaHostRegister) for the
  *                 copies to be asynchronous; pageable memory still works

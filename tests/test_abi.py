@@ -36,6 +36,7 @@ def test_header_declares_the_entry_points():
                  "diffattn_forward_host_workspace", "diffattn_decode", "diffattn_v2_decode",
                  "diffattn_decode_workspace", "diffattn_v2_decode_workspace", "diffattn_decode_fp8k",
                  "diffattn_decode_noalloc", "diffattn_projection", "diffattn_forward_fp8qk", "diffattn_layer_forward",
+                 "diffattn_v2_forward_fp8qk", "diffattn_bounds_checked", "diffattn_debug_bounds_selftest",
                  "diffattn_layer_workspace", "diffattn_v2_layer_forward", "diffattn_v2_layer_workspace",
                  "diffattn_v2_decode_fp8k", "diffattn_backward", "diffattn_backward_workspace",
                  "lambda_reparam_backward", "diffattn_v2_backward", "diffattn_v2_backward_workspace"):
@@ -288,6 +289,24 @@ def test_fp8qk_forward_host_validation(L):
             sc[i] = bad
             assert call(s=tuple(sc)) == da.ERR_SHAPE
     assert call(q1=MIS) == da.ERR_ALIGN
+    assert call(out=MIS) == da.ERR_ALIGN
+
+
+def test_v2_fp8qk_forward_host_validation(L):
+    def call(B=1, Hq=4, Hkv=2, n=8, d=128, q=A, s=(1.0, 1.0), sb=0, st=0, out=A):
+        return L.diffattn_v2_forward_fp8qk(B, Hq, Hkv, n, d, q, A, *(ctypes.c_float(x) for x in s), A, A, sb, st,
+                                           ctypes.c_float(0.0), 1, out, None)
+    assert call(n=-1) == da.ERR_SHAPE
+    assert call(Hq=3) == da.ERR_SHAPE                # Hq odd
+    assert call(Hq=4, Hkv=4) == da.ERR_SHAPE         # Hq / Hkv odd
+    assert call(sb=-1) == da.ERR_SHAPE
+    assert call(d=64) == da.ERR_UNSUPPORTED
+    assert call(B=0) == da.OK
+    assert call(q=None) == da.ERR_NULL
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        assert call(s=(bad, 1.0)) == da.ERR_SHAPE
+        assert call(s=(1.0, bad)) == da.ERR_SHAPE
+    assert call(q=MIS) == da.ERR_ALIGN
     assert call(out=MIS) == da.ERR_ALIGN
 
 

@@ -232,17 +232,23 @@ def test_v2_wide_score_range():
     assert err <= TOL["bf16"] * scale, f"max abs error {err} (output scale {scale})"
 
 
-@pytest.mark.parametrize("B,H,n,d", [(5, 2, 300, 64), (3, 1, 260, 128), (9, 1, 130, 64), (1, 3, 129, 64)])
-def test_v1_host_buffers_match_device_path(B, H, n, d):
+@pytest.mark.parametrize("B,H,n,d,causal", [
+    (5, 2, 300, 64, True), (9, 1, 130, 64, True),        # batch chunks
+    (3, 1, 260, 128, True), (1, 3, 129, 64, True),       # token chunks (two and three tiles)
+    (1, 2, 2000, 128, True),                             # eight token chunks of two tiles, persistent launches
+    (2, 2, 9000, 64, True),                              # 71 tiles: the later chunks' items run one CTA each
+    (1, 2, 700, 64, False)])                             # non-causal: one batch chunk
+def test_v1_host_buffers_match_device_path(B, H, n, d, causal):
     # Inputs and output in page-locked host memory, copied and computed in
-    # batch chunks: every (batch, head, query tile) is computed by the same
+    # chunks (batch entries, or 128-token tiles for a causal forward of few
+    # sequences): every (batch, head, query tile) is computed by the same
     # kernel as on the device path, so the outputs are identical.
-    w = shrink(WORKLOADS[2], B=B, H=H, n=n, d=d, causal=True, gamma="uniform", layer=2, seed=60 + B)
+    w = shrink(WORKLOADS[2], B=B, H=H, n=n, d=d, causal=causal, gamma="uniform", layer=2, seed=60 + B)
     x = make_v1(w, "cuda")
     ref, lam = _v1_gpu(x, w)
     host = {k: x[k].cpu().pin_memory() for k in ("q1", "q2", "k1", "k2", "v")}
     out = da.diffattn_forward_host(host["q1"], host["q2"], host["k1"], host["k2"], host["v"], lam,
-                                   da.lambda_init(w.layer), gamma=x["gamma"], causal=True)
+                                   da.lambda_init(w.layer), gamma=x["gamma"], causal=causal)
     da.device_status()
     assert torch.equal(out, ref.cpu())
     if B * H * n <= 1500:
@@ -713,6 +719,73 @@ def test_v1_fp8qk_small_full_compare(B, H, n, causal):
     ref = oracle.diff_attn_v1(deq["q1"], deq["q2"], deq["k1"], deq["k2"], x["v"], lam, lin, x["gamma"].cpu(), 1e-5,
                               causal)
     assert _err(_np(out), ref) <= TOL["bf16"]
+
+
+FP8_V2_SMALL = [  # B, Hq, Hkv, n, causal, logit granularity
+    (1, 2, 1, 1, True, "pair"), (1, 4, 2, 129, True, "token"), (2, 4, 2, 300, False, "seq"),
+    (1, 8, 2, 1100, True, "pair"), (2, 8, 4, 257, True, "token"),
+]
+
+
+def _v2_logits(g, B, n, G, gran):
+    shape = {"token": (B, n, G), "seq": (n, G), "pair": (G,)}[gran]
+    lg = torch.randn(shape, generator=g, device="cuda")
+    dense = {"token": lambda: lg, "seq": lambda: lg.expand(B, n, G), "pair": lambda: lg.expand(B, n, G)}[gran]()
+    return lg, dense.cpu().double().numpy()
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,n,causal,gran", FP8_V2_SMALL)
+def test_v2_fp8qk_small_full_compare(B, Hq, Hkv, n, causal, gran):
+    # The V2 forward with e4m3 q and k against the fp64 V2 oracle on the values the codes stand for.
+    d, G = 128, Hq // 2
+    g = torch.Generator(device="cuda").manual_seed(300 + n + Hq)
+    q = torch.randn((B, n, Hq, d), generator=g, device="cuda")
+    k = torch.randn((B, n, Hkv, d), generator=g, device="cuda") * 2
+    v = torch.randn((B, n, Hkv, d), generator=g, device="cuda").to(torch.bfloat16)
+    lg, lg_dense = _v2_logits(g, B, n, G, gran)
+    cq, sq = _quantise_e4m3(q)
+    ck, sk = _quantise_e4m3(k)
+    out = da.diffattn_v2_forward_fp8qk(cq, ck, (sq, sk), v, lg, causal=causal)
+    da.device_status()
+    ref = oracle.diff_attn_v2(oracle.dequant_e4m3(cq, sq), oracle.dequant_e4m3(ck, sk), v, lg_dense, causal)
+    assert _err(_np(out), ref) <= TOL["bf16"]
+
+
+def test_v2_fp8qk_matches_bf16_path_on_exact_values():
+    # Codes whose values are exact in bf16 too: the e4m3 path and the bf16 V2 forward score the same
+    # products (each exact in the fp32 accumulator), so they differ only by the order of the fp32 sums.
+    B, Hq, Hkv, n, d = 1, 4, 2, 700, 128
+    g = torch.Generator(device="cuda").manual_seed(77)
+    cq = torch.randn((B, n, Hq, d), generator=g, device="cuda").to(torch.float8_e4m3fn)
+    ck = torch.randn((B, n, Hkv, d), generator=g, device="cuda").to(torch.float8_e4m3fn)
+    v = torch.randn((B, n, Hkv, d), generator=g, device="cuda").to(torch.bfloat16)
+    lg = torch.randn((Hq // 2,), generator=g, device="cuda")
+    out8 = da.diffattn_v2_forward_fp8qk(cq, ck, (0.25, 0.5), v, lg)
+    ref = da.diffattn_v2_forward((cq.float() * 0.25).to(torch.bfloat16), (ck.float() * 0.5).to(torch.bfloat16), v, lg)
+    da.device_status()
+    assert float((out8.float() - ref.float()).abs().max()) <= 1e-2
+
+
+def test_v2_fp8qk_full_size_sampled():
+    # C5's shape (B8 Hq32 Hkv16 n8192 d128, one logit per pair) on sampled rows of two KV heads.
+    w = WORKLOADS[5]
+    x = make_v2(w, "cuda")
+    cq, sq = _quantise_e4m3(x["q"])
+    ck, sk = _quantise_e4m3(x["k"])
+    out = da.diffattn_v2_forward_fp8qk(cq, ck, (sq, sk), x["v"], x["lam_logits"], causal=True)
+    da.device_status()
+    assert bool(torch.isfinite(out.float()).all())
+    rows = _sample_rows(w.n, 16, 55)
+    for b in (0, w.B - 1):
+        for kvh in (0, w.Hkv - 1):
+            hq = [2 * kvh, 2 * kvh + 1]
+            q = oracle.dequant_e4m3(cq[b:b + 1, :, hq].contiguous(), sq)
+            k = oracle.dequant_e4m3(ck[b:b + 1, :, kvh:kvh + 1].contiguous(), sk)
+            v = x["v"][b:b + 1, :, kvh:kvh + 1]
+            lg = np.broadcast_to(x["lam_logits"][kvh:kvh + 1].cpu().double().numpy(), (1, w.n, 1))
+            ref = oracle.diff_attn_v2(q, k, v, lg, True, rows=rows)
+            err = _err(_np(out[b:b + 1][:, rows][:, :, kvh:kvh + 1]), ref)
+            assert err <= TOL["bf16"], f"batch {b} pair {kvh}: max abs error {err}"
 
 
 @pytest.mark.parametrize("wid", [3, 4])
