@@ -580,6 +580,12 @@ def run_reference(args):
 BACKWARD_WORKLOADS = [  # (name, B, H or (Hq, Hkv), n, d, dtype): DIFF V1 / V2 backward, causal
     ("v1-bwd-bf16-B4H16-n2048-d64", 4, 16, 2048, 64, "bf16"),
     ("v2-bwd-bf16-B2Hq32Hkv16-n2048-d128", 2, (32, 16), 2048, 128, "bf16"),
+    # from a training forward's saved statistics (no second forward inside the backward)
+    ("v1-bwd-saved-bf16-B4H16-n2048-d64", 4, 16, 2048, 64, "bf16-saved"),
+    ("v2-bwd-saved-bf16-B2Hq32Hkv16-n2048-d128", 2, (32, 16), 2048, 128, "bf16-saved"),
+    # one training step of the layer's operator: training forward + backward from its statistics
+    ("v1-train-step-bf16-B4H16-n2048-d64", 4, 16, 2048, 64, "bf16-train"),
+    ("v2-train-step-bf16-B2Hq32Hkv16-n2048-d128", 2, (32, 16), 2048, 128, "bf16-train"),
     ("v1-bwd-f32-B4H16-n2048-d64", 4, 16, 2048, 64, "f32"),
     ("v1-bwd-f32-B1H1-n128-d64", 1, 1, 128, 64, "f32"),
     ("v2-bwd-f32-B2Hq32Hkv16-n2048-d128", 2, (32, 16), 2048, 128, "f32"),
@@ -602,12 +608,22 @@ def backward_flops(B, H, n, d):
     return B * H * pairs * 20 * d
 
 
+def train_step_flops(B, H, n, d):
+    """A training step of the operator: the forward (V1 12 d a visible pair per head, V2 8 d a pair per
+    head pair) plus the backward's algorithmic FLOPs (backward_flops)."""
+    pairs = n * (n + 1) // 2
+    fwd = B * (H[0] // 2) * pairs * 8 * d if isinstance(H, tuple) else B * H * pairs * 12 * d
+    return fwd + backward_flops(B, H, n, d)
+
+
 def time_backward(da, flush, B, H, n, d, dtype="f32", runs=10):
     """DIFF V1 / V2 backward: median CUDA-event time, L2 flushed.  fp32 inputs run on the CUDA cores,
-    bf16 inputs on the tensor cores (statistics pass, dK/dV/dQ kernel, reductions; fp32 gradients)."""
+    bf16 inputs on the tensor cores (statistics pass, dK/dV/dQ kernel, reductions; fp32 gradients).
+    "bf16-saved": the backward from a training forward's saved statistics (the forward runs once,
+    untimed); "bf16-train": the training forward and that backward, both timed."""
     import torch
     g = torch.Generator(device="cuda").manual_seed(3000 + n + d)
-    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
 
     def rnd(*shape):
         return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(tdt)
@@ -616,18 +632,34 @@ def time_backward(da, flush, B, H, n, d, dtype="f32", runs=10):
         q, k, v, dy = rnd(B, n, Hq, d), rnd(B, n, Hkv, d), rnd(B, n, Hkv, d), rnd(B, n, Hq // 2, d)
         lg = torch.randn(Hq // 2, generator=g, device="cuda")
         ws = torch.empty(da.v2_backward_workspace_bytes(B, Hq, n, d), dtype=torch.uint8, device="cuda")
+        if dtype in ("f32", "bf16"):
+            def call():
+                da.diffattn_v2_backward(q, k, v, lg, dy, workspace=ws)
+        else:
+            y = torch.empty((B, n, Hq // 2, d), device="cuda", dtype=torch.bfloat16)
+            _, saved = da.diffattn_v2_forward_train(q, k, v, lg, out=y)
 
-        def call():
-            da.diffattn_v2_backward(q, k, v, lg, dy, workspace=ws)
+            def call():
+                if dtype == "bf16-train":
+                    da.diffattn_v2_forward_train(q, k, v, lg, out=y, saved=saved)
+                da.diffattn_v2_backward_saved(q, k, v, lg, dy, saved, workspace=ws)
     else:
         q1, q2, k1, k2 = (rnd(B, n, H, d) for _ in range(4))
         v, dy = rnd(B, n, H, 2 * d), rnd(B, n, H, 2 * d)
         gamma = torch.ones(2 * d, device="cuda")
         lam = torch.tensor([0.3], device="cuda")
         ws = torch.empty(da.backward_workspace_bytes(B, H, n, d), dtype=torch.uint8, device="cuda")
+        if dtype in ("f32", "bf16"):
+            def call():
+                da.diffattn_backward(q1, q2, k1, k2, v, lam, 0.2, dy, gamma=gamma, workspace=ws)
+        else:
+            y = torch.empty((B, n, H, 2 * d), device="cuda", dtype=torch.bfloat16)
+            _, saved = da.diffattn_forward_train(q1, q2, k1, k2, v, lam, 0.2, gamma=gamma, out=y)
 
-        def call():
-            da.diffattn_backward(q1, q2, k1, k2, v, lam, 0.2, dy, gamma=gamma, workspace=ws)
+            def call():
+                if dtype == "bf16-train":
+                    da.diffattn_forward_train(q1, q2, k1, k2, v, lam, 0.2, gamma=gamma, out=y, saved=saved)
+                da.diffattn_backward_saved(q1, q2, k1, k2, v, lam, 0.2, dy, saved, gamma=gamma, workspace=ws)
     for _ in range(3):
         call()
     da.device_status()
@@ -653,8 +685,9 @@ def backward_results(da, flush, sm_mhz, peaks=None, only=None):
         if only and name not in only:
             continue
         ms = time_backward(da, flush, B, H, n, d, dtype)
-        tf = backward_flops(B, H, n, d) / (ms * 1e-3) / 1e12
-        if dtype == "bf16":
+        fl = train_step_flops(B, H, n, d) if dtype == "bf16-train" else backward_flops(B, H, n, d)
+        tf = fl / (ms * 1e-3) / 1e12
+        if dtype != "f32":
             out[name] = {"ms": round(ms, 4), "tflops": round(tf, 2), "bound": "tensor",
                          "peak_tflops": peaks["bf16_tflops"], "peak": "measured burst bf16 dense",
                          "frac": round(tf / peaks["bf16_tflops"], 4), "tokens_per_s": round(B * n / (ms * 1e-3), 1)}

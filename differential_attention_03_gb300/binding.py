@@ -97,6 +97,21 @@ def lib() -> ctypes.CDLL:
             L.diffattn_forward_fp8qk.restype = i
             L.diffattn_v2_forward_fp8qk.argtypes = [i, i, i, i, i, vp, vp, f, f, vp, vp, ll, ll, f, i, vp, vp]
             L.diffattn_v2_forward_fp8qk.restype = i
+            sz = ctypes.c_size_t
+            L.diffattn_forward_saved_bytes.argtypes = [i, i, i, i]
+            L.diffattn_forward_saved_bytes.restype = sz
+            L.diffattn_v2_forward_saved_bytes.argtypes = [i, i, i, i]
+            L.diffattn_v2_forward_saved_bytes.restype = sz
+            L.diffattn_forward_train.argtypes = [i, i, i, i, vp, vp, vp, vp, vp, vp, f, vp, f, i, vp, vp, sz, vp]
+            L.diffattn_forward_train.restype = i
+            L.diffattn_backward_saved.argtypes = [i, i, i, i, vp, vp, vp, vp, vp, vp, f, vp, f, i, vp, vp, sz,
+                                                  vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.diffattn_backward_saved.restype = i
+            L.diffattn_v2_forward_train.argtypes = [i, i, i, i, i, vp, vp, vp, vp, ll, ll, f, i, vp, vp, sz, vp]
+            L.diffattn_v2_forward_train.restype = i
+            L.diffattn_v2_backward_saved.argtypes = [i, i, i, i, i, vp, vp, vp, vp, ll, ll, f, i, vp, vp, sz,
+                                                     vp, vp, vp, vp, vp, sz, vp]
+            L.diffattn_v2_backward_saved.restype = i
             L.diffattn_projection.argtypes = [i, i, i, vp, vp, vp, vp]
             L.diffattn_projection.restype = i
             L.diffattn_layer_workspace.argtypes = [i, i, i, i]
@@ -533,6 +548,132 @@ def diffattn_v2_backward(q, k, v, lam_logits, dy, causal: bool = True, softmax_s
     _check(lib().diffattn_v2_backward(_dt(q), B, Hq, Hkv, n, d, _ptr(q), _ptr(k), _ptr(v), _ptr(lam_logits), sb, st,
                                       float(softmax_scale), 1 if causal else 0, _ptr(dy), _ptr(g["dq"]),
                                       _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dlogits"]), wp, wn, _stream(stream)))
+    return g
+
+
+# ----------------------------------------------------------------------------- training pair
+def forward_saved_bytes(B: int, H: int, n: int, d: int) -> int:
+    """Device bytes that diffattn_forward_train saves for the backward (V1)."""
+    return int(lib().diffattn_forward_saved_bytes(B, H, n, d))
+
+
+def v2_forward_saved_bytes(B: int, Hq: int, n: int, d: int) -> int:
+    """Device bytes that diffattn_v2_forward_train saves for the backward (V2)."""
+    return int(lib().diffattn_v2_forward_saved_bytes(B, Hq, n, d))
+
+
+def _saved_buf(saved, need, device):
+    if saved is None:
+        saved = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    if not saved.is_cuda or saved.dtype != torch.uint8 or saved.numel() < need:
+        raise ValueError(f"saved must be a device uint8 tensor of at least {need} bytes")
+    return saved
+
+
+def diffattn_forward_train(q1, q2, k1, k2, v, lam, lambda_init_value: float, gamma=None, eps: float = 1e-5,
+                           causal: bool = True, out=None, saved=None, stream=None):
+    """diffattn_forward (bf16, d = 64) that also saves each row's lse and O_1, O_2 for
+    diffattn_backward_saved.  Returns (out, saved)."""
+    B, n, H, d = q1.shape
+    for name, t, shp in (("q1", q1, (B, n, H, d)), ("q2", q2, (B, n, H, d)), ("k1", k1, (B, n, H, d)),
+                         ("k2", k2, (B, n, H, d)), ("v", v, (B, n, H, 2 * d))):
+        _need(t, name, torch.bfloat16, shp)
+    _need(lam, "lambda", torch.float32, (1,))
+    if gamma is not None:
+        _need(gamma, "gamma", torch.float32, (2 * d,))
+    if out is None:
+        out = torch.empty((B, n, H, 2 * d), device=q1.device, dtype=torch.bfloat16)
+    _need(out, "out", torch.bfloat16, (B, n, H, 2 * d))
+    need = forward_saved_bytes(B, H, n, d)
+    saved = _saved_buf(saved, need, q1.device)
+    _check(lib().diffattn_forward_train(B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v), _ptr(lam),
+                                        float(lambda_init_value), _ptr(gamma), float(eps), 1 if causal else 0,
+                                        _ptr(out), _ptr(saved), saved.numel(), _stream(stream)))
+    return out, saved
+
+
+def diffattn_backward_saved(q1, q2, k1, k2, v, lam, lambda_init_value: float, dy, saved, gamma=None,
+                            eps: float = 1e-5, causal: bool = True, workspace=None, stream=None) -> dict:
+    """diffattn_backward (bf16, d = 64) from the `saved` of diffattn_forward_train on the same inputs."""
+    B, n, H, d = q1.shape
+    for name, t, shp in (("q1", q1, (B, n, H, d)), ("q2", q2, (B, n, H, d)), ("k1", k1, (B, n, H, d)),
+                         ("k2", k2, (B, n, H, d)), ("v", v, (B, n, H, 2 * d)), ("dy", dy, (B, n, H, 2 * d))):
+        _need(t, name, torch.bfloat16, shp)
+    _need(lam, "lambda", torch.float32, (1,))
+    if gamma is not None:
+        _need(gamma, "gamma", torch.float32, (2 * d,))
+    need = backward_workspace_bytes(B, H, n, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q1.device)
+    wp, wn = _ws_args(workspace, need)
+    g = {k: torch.empty(t.shape, device=t.device, dtype=torch.float32)
+         for k, t in (("dq1", q1), ("dq2", q2), ("dk1", k1), ("dk2", k2), ("dv", v))}
+    g["dlam"] = torch.empty(1, device=q1.device, dtype=torch.float32)
+    g["dgamma"] = torch.empty(2 * d, device=q1.device, dtype=torch.float32)
+    _check(lib().diffattn_backward_saved(B, H, n, d, _ptr(q1), _ptr(q2), _ptr(k1), _ptr(k2), _ptr(v), _ptr(lam),
+                                         float(lambda_init_value), _ptr(gamma), float(eps), 1 if causal else 0,
+                                         _ptr(dy), _ptr(saved), saved.numel(), _ptr(g["dq1"]), _ptr(g["dq2"]),
+                                         _ptr(g["dk1"]), _ptr(g["dk2"]), _ptr(g["dv"]), _ptr(g["dlam"]),
+                                         _ptr(g["dgamma"]), wp, wn, _stream(stream)))
+    return g
+
+
+def _bwd_logit_strides(lam_logits, B, n, G):
+    """Strides of the logits as the V2 backward takes them: [B, n, Hq/2], [B, Hq/2] or [Hq/2]."""
+    f32 = torch.float32
+    if lam_logits.dim() == 3:
+        _need(lam_logits, "lam_logits", f32, (B, n, G))
+        return n * G, G
+    if lam_logits.dim() == 2:
+        _need(lam_logits, "lam_logits", f32, (B, G))
+        return G, 0
+    _need(lam_logits, "lam_logits", f32, (G,))
+    return 0, 0
+
+
+def diffattn_v2_forward_train(q, k, v, lam_logits, causal: bool = True, softmax_scale: float = 0.0, out=None,
+                              saved=None, stream=None):
+    """diffattn_v2_forward (bf16, d = 128) that also saves each row's lse and O_1, O_2 for
+    diffattn_v2_backward_saved; lam_logits [B, n, Hq/2], [B, Hq/2] or [Hq/2].  Returns (out, saved)."""
+    B, n, Hq, d = q.shape
+    Hkv = k.shape[2]
+    _need(q, "q", torch.bfloat16, (B, n, Hq, d))
+    _need(k, "k", torch.bfloat16, (B, n, Hkv, d))
+    _need(v, "v", torch.bfloat16, (B, n, Hkv, d))
+    G = Hq // 2
+    sb, st = _bwd_logit_strides(lam_logits, B, n, G)
+    if out is None:
+        out = torch.empty((B, n, G, d), device=q.device, dtype=torch.bfloat16)
+    _need(out, "out", torch.bfloat16, (B, n, G, d))
+    need = v2_forward_saved_bytes(B, Hq, n, d)
+    saved = _saved_buf(saved, need, q.device)
+    _check(lib().diffattn_v2_forward_train(B, Hq, Hkv, n, d, _ptr(q), _ptr(k), _ptr(v), _ptr(lam_logits), sb, st,
+                                           float(softmax_scale), 1 if causal else 0, _ptr(out), _ptr(saved),
+                                           saved.numel(), _stream(stream)))
+    return out, saved
+
+
+def diffattn_v2_backward_saved(q, k, v, lam_logits, dy, saved, causal: bool = True, softmax_scale: float = 0.0,
+                               workspace=None, stream=None) -> dict:
+    """diffattn_v2_backward (bf16, d = 128) from the `saved` of diffattn_v2_forward_train on the same inputs."""
+    B, n, Hq, d = q.shape
+    Hkv = k.shape[2]
+    for name, t, shp in (("q", q, (B, n, Hq, d)), ("k", k, (B, n, Hkv, d)), ("v", v, (B, n, Hkv, d)),
+                         ("dy", dy, (B, n, Hq // 2, d))):
+        _need(t, name, torch.bfloat16, shp)
+    G = Hq // 2
+    sb, st = _bwd_logit_strides(lam_logits, B, n, G)
+    need = v2_backward_workspace_bytes(B, Hq, n, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    wp, wn = _ws_args(workspace, need)
+    f32 = torch.float32
+    g = {"dq": torch.empty(q.shape, device=q.device, dtype=f32), "dk": torch.empty(k.shape, device=q.device, dtype=f32),
+         "dv": torch.empty(v.shape, device=q.device, dtype=f32), "dlogits": torch.empty_like(lam_logits)}
+    _check(lib().diffattn_v2_backward_saved(B, Hq, Hkv, n, d, _ptr(q), _ptr(k), _ptr(v), _ptr(lam_logits), sb, st,
+                                            float(softmax_scale), 1 if causal else 0, _ptr(dy), _ptr(saved),
+                                            saved.numel(), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
+                                            _ptr(g["dlogits"]), wp, wn, _stream(stream)))
     return g
 
 

@@ -13,6 +13,7 @@
 #include <string>
 
 #include "bwd_params.h"
+#include "bwd_prep.cuh"
 #include "bwd_tc_params.h"
 #include "decode.cuh"
 #include "gemm_params.h"
@@ -288,9 +289,11 @@ diffattn_status launch_v1_tc(const char* fn, da::TwoPassParams& p, bool f8, int 
   // dynamic CTA scheduling balances them; measured faster).
   const bool persist = qt0 + p.num_q_tiles <= 64;  // (the last tile's item length decides)
   const int g = static_cast<int>(persist ? persistent_grid(grid) : grid);
+  // (p.o1_save set: the training forward, d = 64, which also saves each row's statistics)
   cudaError_t e = f8 ? da::launch_twopass_v1_d128_f8(p, g, persist, s)
-                     : (d == 64) ? da::launch_onepass_v1_d64(p, g, persist, s)
-                                 : da::launch_twopass_v1_d128(p, g, persist, s);
+                  : (d == 64) ? (p.o1_save ? da::launch_onepass_v1_d64_save(p, g, persist, s)
+                                           : da::launch_onepass_v1_d64(p, g, persist, s))
+                              : da::launch_twopass_v1_d128(p, g, persist, s);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   g_launches.fetch_add(1);
   return DIFFATTN_OK;
@@ -347,7 +350,8 @@ diffattn_status launch_v2_tc(const char* fn, da::TwoPassParams& p, bool f8, int 
   // V2 items are long (up to n / 128 key tiles): one CTA per item, so the
   // hardware's dynamic CTA scheduling balances them (measured faster here).
   cudaError_t e = f8 ? da::launch_onepass_v2_d128_f8(p, static_cast<int>(grid), s)
-                     : da::launch_onepass_v2_d128(p, static_cast<int>(grid), s);
+                  : p.o1_save ? da::launch_onepass_v2_d128_save(p, static_cast<int>(grid), s)
+                              : da::launch_onepass_v2_d128(p, static_cast<int>(grid), s);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   g_launches.fetch_add(1);
   return DIFFATTN_OK;
@@ -1249,11 +1253,31 @@ diffattn_status diffattn_v2_layer_forward(int B, int n, int D, int Hq, int Hkv, 
 namespace {
 
 // V1 (d = 64): statistics pass, dK/dV/dQ kernel, reduction of dlambda and dgamma.
+// A training forward's saved statistics: lse [2][rows] fp32, then O_1 and O_2
+// [rows x value width] bf16 (BSHD row order), 256-byte aligned parts.
+struct SavedFwd {
+  const float* lse;
+  const __nv_bfloat16* o1;
+  const __nv_bfloat16* o2;
+};
+
+size_t saved_fwd_bytes(size_t rows, size_t dv) { return round256(2 * rows * 4) + 2 * round256(rows * dv * 2); }
+
+SavedFwd saved_fwd_views(const void* saved, size_t rows, size_t dv) {
+  const uint8_t* b = static_cast<const uint8_t*>(saved);
+  SavedFwd v;
+  v.lse = reinterpret_cast<const float*>(b);
+  v.o1 = reinterpret_cast<const __nv_bfloat16*>(b + round256(2 * rows * 4));
+  v.o2 = reinterpret_cast<const __nv_bfloat16*>(b + round256(2 * rows * 4) + round256(rows * dv * 2));
+  return v;
+}
+
 diffattn_status backward_v1_tc(int B, int H, int n, const void* q1, const void* q2, const void* k1, const void* k2,
                                const void* v, const float* lambda, float lambda_init, const float* gamma, float eps,
                                int causal, const void* dy, void* dq1, void* dq2, void* dk1, void* dk2, void* dv,
-                               float* dlambda, float* dgamma, uint8_t* ws, int* status, cudaStream_t s) {
-  const char* fn = "diffattn_backward (bf16)";
+                               float* dlambda, float* dgamma, uint8_t* ws, int* status, cudaStream_t s,
+                               const SavedFwd* saved = nullptr) {
+  const char* fn = saved ? "diffattn_backward_saved" : "diffattn_backward (bf16)";
   constexpr int d = 64, dv_w = 128;
   const size_t R = static_cast<size_t>(B) * H * n;
   const int nt = (n + 127) / 128;
@@ -1297,7 +1321,30 @@ diffattn_status backward_v1_tc(int B, int H, int n, const void* q1, const void* 
   cudaError_t e = cudaMemsetAsync(dq1, 0, R * d * 4, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(dq2, 0, R * d * 4, s);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_backward: clearing dq");
-  if ((e = da::launch_bwd_stats(p, false, static_cast<int>(stats_grid), s)) != cudaSuccess) return cuda_fail(e, fn);
+  int row_ctas = static_cast<int>(stats_grid);
+  if (saved) {  // the per-row results from the saved statistics instead of a second forward
+    da::BwdPrepParams q{};
+    q.dy = p.dy;
+    q.o1 = saved->o1;
+    q.o2 = saved->o2;
+    q.lse = saved->lse;
+    q.lambda = lambda;
+    q.gamma = gamma;
+    q.norm_mult = 1.f - lambda_init;
+    q.eps = eps;
+    q.B = B;
+    q.n = n;
+    q.units = H;
+    q.rows = static_cast<long long>(R);
+    q.dO = ws_do;
+    q.row = ws_row;
+    q.dgp = ws_dg;
+    q.dlam_part = ws_dl;
+    row_ctas = static_cast<int>((R + da::kPrepRowsPerCta - 1) / da::kPrepRowsPerCta);  // <= stats_grid
+    if ((e = da::launch_bwd_prep(q, false, row_ctas, s)) != cudaSuccess) return cuda_fail(e, fn);
+  } else if ((e = da::launch_bwd_stats(p, false, static_cast<int>(stats_grid), s)) != cudaSuccess) {
+    return cuda_fail(e, fn);
+  }
   // 2. dK, dV, dQ
   da::BwdTcParams t;
   memset(&t, 0, sizeof(t));
@@ -1342,7 +1389,7 @@ diffattn_status backward_v1_tc(int B, int H, int n, const void* q1, const void* 
   r.v2 = 0;
   r.units = H;
   r.rows = static_cast<long long>(R);
-  r.n_row_ctas = static_cast<int>(stats_grid);
+  r.n_row_ctas = row_ctas;
   if ((e = da::launch_bwd_reduce(r, s)) != cudaSuccess) return cuda_fail(e, fn);
   g_launches.fetch_add(4);
   return DIFFATTN_OK;
@@ -1353,8 +1400,8 @@ diffattn_status backward_v1_tc(int B, int H, int n, const void* q1, const void* 
 diffattn_status backward_v2_tc(int B, int Hq, int Hkv, int n, const void* q, const void* k, const void* v,
                                const float* lam_logits, long long sb, long long st_, float scale, int causal,
                                const void* dy, void* dq, void* dk, void* dv, float* dlogits, bool dense, uint8_t* ws,
-                               int* status, cudaStream_t s) {
-  const char* fn = "diffattn_v2_backward (bf16)";
+                               int* status, cudaStream_t s, const SavedFwd* saved = nullptr) {
+  const char* fn = saved ? "diffattn_v2_backward_saved" : "diffattn_v2_backward (bf16)";
   constexpr int d = 128;
   const int G = Hq / 2;
   const size_t R = static_cast<size_t>(B) * G * n;
@@ -1392,7 +1439,26 @@ diffattn_status backward_v2_tc(int B, int Hq, int Hkv, int n, const void* q, con
   p.rows = static_cast<long long>(R);
   cudaError_t e = cudaMemsetAsync(dq, 0, static_cast<size_t>(B) * n * Hq * d * 4, s);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_backward: clearing dq");
-  if ((e = da::launch_bwd_stats(p, true, static_cast<int>(stats_grid), s)) != cudaSuccess) return cuda_fail(e, fn);
+  if (saved) {  // the per-row results from the saved statistics instead of a second forward
+    da::BwdPrepParams q{};
+    q.dy = p.dy;
+    q.o1 = saved->o1;
+    q.o2 = saved->o2;
+    q.lse = saved->lse;
+    q.lam_logits = lam_logits;
+    q.sb = sb;
+    q.st = st_;
+    q.B = B;
+    q.n = n;
+    q.units = G;
+    q.rows = static_cast<long long>(R);
+    q.row = ws_row;
+    q.dlogits_dense = p.dlogits_dense;
+    const int row_ctas = static_cast<int>((R + da::kPrepRowsPerCta - 1) / da::kPrepRowsPerCta);
+    if ((e = da::launch_bwd_prep(q, true, row_ctas, s)) != cudaSuccess) return cuda_fail(e, fn);
+  } else if ((e = da::launch_bwd_stats(p, true, static_cast<int>(stats_grid), s)) != cudaSuccess) {
+    return cuda_fail(e, fn);
+  }
   da::BwdTcParams t;
   memset(&t, 0, sizeof(t));
   if ((st = make_map(&t.tm_q1, q, B, n, Hq, d, 128)) != DIFFATTN_OK) return st;
@@ -1687,6 +1753,191 @@ diffattn_status diffattn_v2_backward(diffattn_dtype dt, int B, int Hq, int Hkv, 
   if (e == cudaSuccess) e = da::launch_backward_f32(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_backward launch");
   g_launches.fetch_add(dense ? 3 : 4);
+  return ok();
+}
+
+// ---- training forward (saves each row's statistics) and the backward from them
+size_t diffattn_forward_saved_bytes(int B, int H, int n, int d) {
+  if (B < 0 || H < 0 || n < 0 || d < 1) return 0;
+  return saved_fwd_bytes(static_cast<size_t>(B) * H * n, 2 * static_cast<size_t>(d));
+}
+
+size_t diffattn_v2_forward_saved_bytes(int B, int Hq, int n, int d) {
+  if (B < 0 || Hq < 0 || n < 0 || d < 1) return 0;
+  return saved_fwd_bytes(static_cast<size_t>(B) * (Hq / 2) * n, static_cast<size_t>(d));
+}
+
+// Checks shared by the training entry points: bf16 tensors 16-byte aligned, the saved buffer's size and alignment.
+static diffattn_status check_saved(const char* fn, const void* saved, size_t saved_bytes, size_t need) {
+  if (!saved) return fail(DIFFATTN_ERR_NULL, "%s: NULL saved buffer", fn);
+  if (saved_bytes < need) return fail(DIFFATTN_ERR_SHAPE, "%s: saved buffer of %zu bytes, need %zu", fn, saved_bytes, need);
+  if ((reinterpret_cast<uintptr_t>(saved) & 255u) != 0) return fail(DIFFATTN_ERR_ALIGN, "%s: saved buffer not 256-byte aligned", fn);
+  return DIFFATTN_OK;
+}
+
+diffattn_status diffattn_forward_train(int B, int H, int n, int d, const void* q1, const void* q2, const void* k1,
+                                       const void* k2, const void* v, const float* lambda, float lambda_init,
+                                       const float* gamma, float eps, int causal, void* out, void* saved,
+                                       size_t saved_bytes, void* stream) {
+  const char* fn = "diffattn_forward_train";
+  if (B < 0 || H < 0 || n < 0 || d < 1) return fail(DIFFATTN_ERR_SHAPE, "%s: bad sizes B=%d H=%d n=%d d=%d", fn, B, H, n, d);
+  if (d != 64) return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: d = 64 only (got %d)", fn, d);
+  if (B == 0 || H == 0 || n == 0) return ok();
+  if (!q1 || !q2 || !k1 || !k2 || !v || !lambda || !out) return fail(DIFFATTN_ERR_NULL, "%s: NULL pointer", fn);
+  if (!std::isfinite(lambda_init)) return fail(DIFFATTN_ERR_SHAPE, "%s: lambda_init not finite", fn);
+  if (!aligned16(q1) || !aligned16(q2) || !aligned16(k1) || !aligned16(k2) || !aligned16(v) || !aligned16(out))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  const size_t R = static_cast<size_t>(B) * H * n;
+  diffattn_status st = check_saved(fn, saved, saved_bytes, diffattn_forward_saved_bytes(B, H, n, d));
+  if (st != DIFFATTN_OK) return st;
+  if (eps <= 0.f) eps = 1e-5f;
+  int* status = nullptr;
+  if ((st = status_word(&status)) != DIFFATTN_OK) return st;
+  const SavedFwd sv = saved_fwd_views(saved, R, 2 * d);
+  const long long Hd = static_cast<long long>(H) * d;
+  da::TwoPassParams p;
+  memset(&p, 0, sizeof(p));
+  if ((st = make_map_view(&p.tm_q1, q1, B, n, H, d, d, Hd, 64, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_view(&p.tm_q2, q2, B, n, H, d, d, Hd, 64, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_view(&p.tm_k1, k1, B, n, H, d, d, Hd, 64, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_view(&p.tm_k2, k2, B, n, H, d, d, Hd, 64, 128)) != DIFFATTN_OK) return st;
+  if ((st = make_map_view(&p.tm_v, v, B, n, H, 2 * d, 2 * d, 2 * Hd, 64, 64)) != DIFFATTN_OK) return st;
+  p.row = const_cast<float*>(sv.lse);
+  p.rows = static_cast<long long>(R);
+  p.o1_save = const_cast<__nv_bfloat16*>(sv.o1);
+  p.o2_save = const_cast<__nv_bfloat16*>(sv.o2);
+  const float sc = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  if ((st = launch_v1_tc(fn, p, false, B, H, n, d, sc, sc, lambda, lambda_init, gamma, eps, causal, out, status,
+                         static_cast<cudaStream_t>(stream))) != DIFFATTN_OK)
+    return st;
+  return ok();
+}
+
+diffattn_status diffattn_backward_saved(int B, int H, int n, int d, const void* q1, const void* q2, const void* k1,
+                                        const void* k2, const void* v, const float* lambda, float lambda_init,
+                                        const float* gamma, float eps, int causal, const void* dy, const void* saved,
+                                        size_t saved_bytes, void* dq1, void* dq2, void* dk1, void* dk2, void* dv,
+                                        float* dlambda, float* dgamma, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  const char* fn = "diffattn_backward_saved";
+  if (B < 0 || H < 0 || n < 0 || d < 1) return fail(DIFFATTN_ERR_SHAPE, "%s: bad sizes B=%d H=%d n=%d d=%d", fn, B, H, n, d);
+  if (d != 64) return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: d = 64 only (got %d)", fn, d);
+  if (!dlambda) return fail(DIFFATTN_ERR_NULL, "%s: NULL dlambda", fn);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (B == 0 || H == 0 || n == 0) {  // no rows: dlambda = 0, dgamma = 0
+    cudaError_t e = cudaMemsetAsync(dlambda, 0, sizeof(float), s);
+    if (e == cudaSuccess && dgamma) e = cudaMemsetAsync(dgamma, 0, 2 * d * sizeof(float), s);
+    if (e != cudaSuccess) return cuda_fail(e, "diffattn_backward_saved: clearing dlambda / dgamma");
+    return ok();
+  }
+  if (!q1 || !q2 || !k1 || !k2 || !v || !lambda || !dy || !dq1 || !dq2 || !dk1 || !dk2 || !dv || !workspace)
+    return fail(DIFFATTN_ERR_NULL, "%s: NULL pointer", fn);
+  if (!std::isfinite(lambda_init)) return fail(DIFFATTN_ERR_SHAPE, "%s: lambda_init not finite", fn);
+  const size_t need = diffattn_backward_workspace(B, H, n, d);
+  if (workspace_bytes < need) return fail(DIFFATTN_ERR_SHAPE, "%s: workspace of %zu bytes, need %zu", fn, workspace_bytes, need);
+  if (!aligned16(workspace) || !aligned16(q1) || !aligned16(q2) || !aligned16(k1) || !aligned16(k2) || !aligned16(v) ||
+      !aligned16(dy) || !aligned16(dq1) || !aligned16(dq2) || !aligned16(dk1) || !aligned16(dk2) || !aligned16(dv))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors and workspace must be 16-byte aligned", fn);
+  diffattn_status st = check_saved(fn, saved, saved_bytes, diffattn_forward_saved_bytes(B, H, n, d));
+  if (st != DIFFATTN_OK) return st;
+  const long long nqb = (static_cast<long long>(n) + 127) / 128;
+  if (static_cast<long long>(B) * H * nqb > 0x7fffffffll || static_cast<long long>(B) * H * n > 0x7fffffffll)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: too many rows", fn);
+  if (eps <= 0.f) eps = 1e-5f;
+  int* status = nullptr;
+  if ((st = status_word(&status)) != DIFFATTN_OK) return st;
+  const SavedFwd sv = saved_fwd_views(saved, static_cast<size_t>(B) * H * n, 2 * d);
+  if ((st = backward_v1_tc(B, H, n, q1, q2, k1, k2, v, lambda, lambda_init, gamma, eps, causal, dy, dq1, dq2, dk1, dk2,
+                           dv, dlambda, dgamma, static_cast<uint8_t*>(workspace), status, s, &sv)) != DIFFATTN_OK)
+    return st;
+  return ok();
+}
+
+diffattn_status diffattn_v2_forward_train(int B, int Hq, int Hkv, int n, int d, const void* q, const void* k,
+                                          const void* v, const float* lam_logits, long long sb, long long st_,
+                                          float softmax_scale, int causal, void* out, void* saved, size_t saved_bytes,
+                                          void* stream) {
+  const char* fn = "diffattn_v2_forward_train";
+  if (B < 0 || Hq < 0 || Hkv < 1 || n < 0 || d < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: bad sizes B=%d Hq=%d Hkv=%d n=%d d=%d", fn, B, Hq, Hkv, n, d);
+  if (Hq % 2 != 0 || Hq % Hkv != 0 || (Hq / Hkv) % 2 != 0)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need Hq even, Hq %% Hkv == 0 and Hq/Hkv even (Hq=%d Hkv=%d)", fn, Hq, Hkv);
+  if (sb < 0 || st_ < 0) return fail(DIFFATTN_ERR_SHAPE, "%s: negative logit stride", fn);
+  if (d != 128) return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: d = 128 only (got %d)", fn, d);
+  if (B == 0 || Hq == 0 || n == 0) return ok();
+  if (!q || !k || !v || !lam_logits || !out) return fail(DIFFATTN_ERR_NULL, "%s: NULL pointer", fn);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors must be 16-byte aligned", fn);
+  const int G = Hq / 2;
+  const size_t R = static_cast<size_t>(B) * G * n;
+  diffattn_status st = check_saved(fn, saved, saved_bytes, diffattn_v2_forward_saved_bytes(B, Hq, n, d));
+  if (st != DIFFATTN_OK) return st;
+  int* status = nullptr;
+  if ((st = status_word(&status)) != DIFFATTN_OK) return st;
+  const SavedFwd sv = saved_fwd_views(saved, R, d);
+  const double scale = softmax_scale > 0.f ? softmax_scale : 1.0 / std::sqrt(static_cast<double>(d));
+  da::TwoPassParams p;
+  memset(&p, 0, sizeof(p));
+  if ((st = make_map_box(&p.tm_q1, q, B, n, Hq, d, 64, 128)) != DIFFATTN_OK) return st;
+  p.tm_q2 = p.tm_q1;
+  if ((st = make_map_box(&p.tm_k1, k, B, n, Hkv, d, 64, 128)) != DIFFATTN_OK) return st;
+  p.tm_k2 = p.tm_k1;
+  if ((st = make_map_box(&p.tm_v, v, B, n, Hkv, d, 64, 128)) != DIFFATTN_OK) return st;
+  p.row = const_cast<float*>(sv.lse);
+  p.rows = static_cast<long long>(R);
+  p.o1_save = const_cast<__nv_bfloat16*>(sv.o1);
+  p.o2_save = const_cast<__nv_bfloat16*>(sv.o2);
+  if ((st = launch_v2_tc(fn, p, false, B, Hq, Hkv, n, d, lam_logits, sb, st_,
+                         static_cast<float>(1.4426950408889634 * scale), causal, out, status,
+                         static_cast<cudaStream_t>(stream))) != DIFFATTN_OK)
+    return st;
+  return ok();
+}
+
+diffattn_status diffattn_v2_backward_saved(int B, int Hq, int Hkv, int n, int d, const void* q, const void* k,
+                                           const void* v, const float* lam_logits, long long sb, long long st_,
+                                           float softmax_scale, int causal, const void* dy, const void* saved,
+                                           size_t saved_bytes, void* dq, void* dk, void* dv, float* dlogits,
+                                           void* workspace, size_t workspace_bytes, void* stream) {
+  const char* fn = "diffattn_v2_backward_saved";
+  if (B < 0 || Hq < 0 || Hkv < 1 || n < 0 || d < 1)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: bad sizes B=%d Hq=%d Hkv=%d n=%d d=%d", fn, B, Hq, Hkv, n, d);
+  if (Hq % 2 != 0 || Hq % Hkv != 0 || (Hq / Hkv) % 2 != 0)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: need Hq even, Hq %% Hkv == 0 and Hq/Hkv even", fn);
+  if (sb < 0 || st_ < 0) return fail(DIFFATTN_ERR_SHAPE, "%s: negative logit stride", fn);
+  if (d != 128) return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: d = 128 only (got %d)", fn, d);
+  const int G = Hq / 2;
+  const bool dense = st_ == G && sb == static_cast<long long>(n) * G;
+  if (!dense && !(st_ == 0 && (sb == 0 || sb == G)))
+    return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: logit strides (sb, st) must be (n*Hq/2, Hq/2), (Hq/2, 0) or (0, 0)", fn);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (B == 0 || Hq == 0 || n == 0) {  // no rows: a logit shared by tokens gets a zero gradient
+    const size_t shared = dense ? 0 : (sb == 0 ? static_cast<size_t>(G) : static_cast<size_t>(B) * G);
+    if (shared > 0 && dlogits != nullptr) {
+      cudaError_t e = cudaMemsetAsync(dlogits, 0, shared * sizeof(float), s);
+      if (e != cudaSuccess) return cuda_fail(e, "diffattn_v2_backward_saved: clearing dlogits");
+    }
+    return ok();
+  }
+  if (!q || !k || !v || !lam_logits || !dy || !dq || !dk || !dv || !dlogits || !workspace)
+    return fail(DIFFATTN_ERR_NULL, "%s: NULL pointer", fn);
+  const size_t need = diffattn_v2_backward_workspace(B, Hq, n, d);
+  if (workspace_bytes < need) return fail(DIFFATTN_ERR_SHAPE, "%s: workspace of %zu bytes, need %zu", fn, workspace_bytes, need);
+  if (!aligned16(workspace) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dy) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv))
+    return fail(DIFFATTN_ERR_ALIGN, "%s: tensors and workspace must be 16-byte aligned", fn);
+  diffattn_status st = check_saved(fn, saved, saved_bytes, diffattn_v2_forward_saved_bytes(B, Hq, n, d));
+  if (st != DIFFATTN_OK) return st;
+  const long long nqb = (static_cast<long long>(n) + 127) / 128;
+  if (static_cast<long long>(B) * G * nqb > 0x7fffffffll || static_cast<long long>(B) * G * n > 0x7fffffffll)
+    return fail(DIFFATTN_ERR_SHAPE, "%s: too many rows", fn);
+  int* status = nullptr;
+  if ((st = status_word(&status)) != DIFFATTN_OK) return st;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.f / std::sqrt(static_cast<float>(d));
+  const SavedFwd sv = saved_fwd_views(saved, static_cast<size_t>(B) * G * n, d);
+  if ((st = backward_v2_tc(B, Hq, Hkv, n, q, k, v, lam_logits, sb, st_, scale, causal, dy, dq, dk, dv, dlogits, dense,
+                           static_cast<uint8_t*>(workspace), status, s, &sv)) != DIFFATTN_OK)
+    return st;
   return ok();
 }
 

@@ -1,5 +1,6 @@
 // Launchers of the tensor-core backward: the statistics pass (the one-sweep
 // forward with its STATS epilogue) and the dK/dV/dQ kernel.
+#include "bwd_prep.cuh"
 #include "bwd_tc.cuh"
 #include "launch.h"
 #include "onepass_inst.cuh"
@@ -22,6 +23,14 @@ static cudaError_t launch_bwd_tc_t(const BwdTcParams& p, int grid, cudaStream_t 
 
 cudaError_t launch_bwd_tc(const BwdTcParams& p, bool v2, int grid, cudaStream_t s) {
   return v2 ? launch_bwd_tc_t<true>(p, grid, s) : launch_bwd_tc_t<false>(p, grid, s);
+}
+
+cudaError_t launch_bwd_prep(const BwdPrepParams& p, bool v2, int grid, cudaStream_t s) {
+  if (v2)
+    bwd_prep_kernel<true><<<grid, kPrepWarps * 32, 0, s>>>(p);
+  else
+    bwd_prep_kernel<false><<<grid, kPrepWarps * 32, 0, s>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace da

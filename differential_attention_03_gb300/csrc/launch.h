@@ -12,6 +12,7 @@ struct BwdParams;
 struct SimtBwdExtra;
 struct GemmParams;
 struct BwdTcParams;
+struct BwdPrepParams;
 }
 
 namespace da {
@@ -26,6 +27,9 @@ cudaError_t launch_onepass_v1_d64(const TwoPassParams& p, int grid, bool persist
 cudaError_t launch_onepass_v2_d128(const TwoPassParams& p, int grid, cudaStream_t s);
 // The same with e4m3 queries and keys (tm_q1 / tm_k1 over bytes; scale_log2 carries their scales).
 cudaError_t launch_onepass_v2_d128_f8(const TwoPassParams& p, int grid, cudaStream_t s);
+// The training forward (SAVE): the output plus lse_r and O_r of every row (see TwoPassParams).
+cudaError_t launch_onepass_v1_d64_save(const TwoPassParams& p, int grid, bool persistent, cudaStream_t s);
+cudaError_t launch_onepass_v2_d128_save(const TwoPassParams& p, int grid, cudaStream_t s);
 
 cudaError_t launch_simt_f32(const SimtParams& p, cudaStream_t s);
 // V1 decode (one query per sequence over a key/value cache), d in {64, 128}:
@@ -47,6 +51,8 @@ cudaError_t launch_lambda_reparam(const float* lq1, const float* lk1, const floa
 // (one-sweep forward, one item per CTA, grid = items) and the dK/dV/dQ kernel
 // (grid = B * heads_kv * key tiles).
 cudaError_t launch_bwd_stats(const TwoPassParams& p, bool v2, int grid, cudaStream_t s);
+// The same per-row results from a training forward's saved statistics (CUDA cores; 128 rows a CTA).
+cudaError_t launch_bwd_prep(const BwdPrepParams& p, bool v2, int grid, cudaStream_t s);
 cudaError_t launch_bwd_tc(const BwdTcParams& p, bool v2, int grid, cudaStream_t s);
 // The fp32 backward's reduction of the dlambda / dlogit and dgamma shares alone.
 cudaError_t launch_bwd_reduce(const BwdParams& p, cudaStream_t s);

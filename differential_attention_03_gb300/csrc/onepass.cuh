@@ -71,7 +71,8 @@
 
 namespace da {
 
-template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST, bool STATS = false, bool F8 = false>
+template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST, bool STATS = false, bool F8 = false,
+          bool SAVE = false>
 struct OnePassCfg {
   static constexpr int BM = 128;
   static constexpr int BN = 128;
@@ -114,6 +115,7 @@ struct OnePassCfg {
   static constexpr int MAX_ITEMS = PERSIST ? 0x7fffffff : 1;  // work items per CTA
   static_assert(D == 64 || D == 128, "query/key width");
   static_assert(!F8 || (D == 128 && SHARED_K && !STATS), "e4m3 queries and keys: the V2 forward, d = 128");
+  static_assert(!SAVE || (!STATS && !F8), "the training forward saves the bf16 forward's statistics");
   static_assert(V_TILE % SLOT == 0 && (VF == 1 || VF == 2), "value tile split");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
   static_assert(NSLOT >= 4, "ring depth");
@@ -317,9 +319,10 @@ __device__ __forceinline__ void onepass_stats_epilogue(const TwoPassParams& p, c
   (void)map;
 }
 
-template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST, bool STATS = false, bool F8 = false>
+template <int D, bool SHARED_K, int EPI, int NSLOT, bool PSM, bool PERSIST, bool STATS = false, bool F8 = false,
+          bool SAVE = false>
 __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
-  using C = OnePassCfg<D, SHARED_K, EPI, NSLOT, PSM, PERSIST, STATS, F8>;
+  using C = OnePassCfg<D, SHARED_K, EPI, NSLOT, PSM, PERSIST, STATS, F8, SAVE>;
   constexpr int BM = C::BM, BN = C::BN, DV = C::DV;
 
   extern __shared__ uint8_t smem_raw[];
@@ -769,6 +772,32 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
         tmem_ld32(tl + C::TM_O1 + 32u * cb, o1);
         tmem_ld32(tl + C::TM_O2 + 32u * cb, o2);
         tmem_ld_wait2(o1, o2);
+        if constexpr (SAVE) {
+          // Training forward: the row's normalised map outputs O_r = O_r' / l_r
+          // (bf16, this warpgroup's 32 channels) and, from the warpgroups that
+          // hold each map's running maximum, lse_r = m_r + log2 l_r.
+          if (t < p.n && DA_BOUNDS_V(c.b < p.B && c.u < p.units_per_batch, t)) {
+            const long long orow = (static_cast<long long>(c.b) * p.n + t) * p.units_per_batch + c.u;
+            const float il2 = 1.f / l2;
+            uint4* s1 = reinterpret_cast<uint4*>(p.o1_save + orow * DV + 32 * cb);
+            uint4* s2 = reinterpret_cast<uint4*>(p.o2_save + orow * DV + 32 * cb);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t w1[4], w2[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int cc = 8 * v + 2 * e;
+                w1[e] = pack_bf16x2(__uint_as_float(o1[cc]) * a1, __uint_as_float(o1[cc + 1]) * a1);
+                w2[e] = pack_bf16x2(__uint_as_float(o2[cc]) * il2, __uint_as_float(o2[cc + 1]) * il2);
+              }
+              s1[v] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+              s2[v] = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+            }
+            const long long ri = (static_cast<long long>(c.b) * p.units_per_batch + c.u) * p.n + t;
+            if (cb == 0) p.row[ri] = m_used + log2f(l1);
+            if (cb == 2) p.row[p.rows + ri] = m_used + log2f(l2);
+          }
+        }
         if constexpr (PERSIST) {
           // O is in registers: the next item's first PV may overwrite it.
           tc_fence_before();

@@ -40,6 +40,11 @@ struct TwoPassParams {
   float* dlam_part;         // V1: [gridDim.x], each CTA's share of dlambda
   float* dlogits_dense;     // V2, one logit per token: dlogit of (b, t, pair) at b sb + t st + pair
   long long rows;           // B * units_per_batch * n
+  // Training forward (one-sweep kernel with SAVE): besides the output, each
+  // row's lse_1, lse_2 (to row[ri], row[rows + ri]) and its normalised map
+  // outputs O_1, O_2 in bf16, [B, n, units_per_batch, DV] each.
+  __nv_bfloat16* o1_save;
+  __nv_bfloat16* o2_save;
 };
 
 // What work item `idx` of a tcgen05 launch computes: batch b, unit u (V1:

@@ -510,6 +510,62 @@ diffattn_status diffattn_v2_backward(diffattn_dtype dt, int B, int Hq, int Hkv, 
                                      size_t workspace_bytes, void* stream);
 
 /*
+ * Training forward and the backward from its saved statistics (bf16, tensor
+ * cores).  The pages describe the forward and report trained models; how a
+ * training step splits its work between forward and backward is this
+ * library's: as in the usual attention backward, the forward keeps what the
+ * backward would otherwise recompute.
+ *
+ * diffattn_forward_train: diffattn_forward (bf16, d = 64; same arguments,
+ * same output bits) that also writes, per (batch, head, token) row, lse_1 and
+ * lse_2 (the base-2 log-sum-exp of each map's scaled scores) and the
+ * normalised map outputs O_1 = A_1 V and O_2 = A_2 V in bf16 to `saved`:
+ *   saved : device memory of at least diffattn_forward_saved_bytes(B, H, n, d)
+ *           bytes, 256-byte aligned (else ERR_SHAPE / ERR_ALIGN); the caller
+ *           keeps it until the backward of this forward.
+ * diffattn_backward_saved: diffattn_backward with dt = DIFFATTN_BF16 (same
+ * arguments, gradients and workspace) given the same inputs and the `saved`
+ * of their training forward; it does not recompute the forward's maps (a
+ * per-row pass turns dy, O_1, O_2 into dO and the softmax-gradient row sums),
+ * so it takes less time.  The result equals diffattn_backward's up to the
+ * bf16 rounding of O_1, O_2.
+ * The V2 pair is the same for diffattn_v2_forward / diffattn_v2_backward
+ * (bf16, d = 128; rows are (batch, head pair, token)).  Other d ->
+ * ERR_UNSUPPORTED; errors otherwise as for the calls they extend.
+ */
+size_t diffattn_forward_saved_bytes(int B, int H, int n, int d);
+
+diffattn_status diffattn_forward_train(int B, int H, int n, int d, const void* q1, const void* q2,
+                                       const void* k1, const void* k2, const void* v,
+                                       const float* lambda, float lambda_init, const float* gamma,
+                                       float eps, int causal, void* out, void* saved,
+                                       size_t saved_bytes, void* stream);
+
+diffattn_status diffattn_backward_saved(int B, int H, int n, int d, const void* q1, const void* q2,
+                                        const void* k1, const void* k2, const void* v,
+                                        const float* lambda, float lambda_init, const float* gamma,
+                                        float eps, int causal, const void* dy, const void* saved,
+                                        size_t saved_bytes, void* dq1, void* dq2, void* dk1,
+                                        void* dk2, void* dv, float* dlambda, float* dgamma,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
+size_t diffattn_v2_forward_saved_bytes(int B, int Hq, int n, int d);
+
+diffattn_status diffattn_v2_forward_train(int B, int Hq, int Hkv, int n, int d, const void* q,
+                                          const void* k, const void* v, const float* lam_logits,
+                                          long long sb, long long st, float softmax_scale,
+                                          int causal, void* out, void* saved, size_t saved_bytes,
+                                          void* stream);
+
+diffattn_status diffattn_v2_backward_saved(int B, int Hq, int Hkv, int n, int d, const void* q,
+                                           const void* k, const void* v, const float* lam_logits,
+                                           long long sb, long long st, float softmax_scale,
+                                           int causal, const void* dy, const void* saved,
+                                           size_t saved_bytes, void* dq, void* dk, void* dv,
+                                           float* dlogits, void* workspace, size_t workspace_bytes,
+                                           void* stream);
+
+/*
  * Gradients of lambda = exp(<lq1, lk1>) - exp(<lq2, lk2>) + lambda_init
  * (news article section "差分注意力") with respect to the four vectors of
  * length dim, given the device scalar dlambda: dlq1 = dlambda exp(<lq1, lk1>) lk1,

@@ -37,6 +37,8 @@ def test_header_declares_the_entry_points():
                  "diffattn_decode_workspace", "diffattn_v2_decode_workspace", "diffattn_decode_fp8k",
                  "diffattn_decode_noalloc", "diffattn_projection", "diffattn_forward_fp8qk", "diffattn_layer_forward",
                  "diffattn_v2_forward_fp8qk", "diffattn_bounds_checked", "diffattn_debug_bounds_selftest",
+                 "diffattn_forward_train", "diffattn_backward_saved", "diffattn_forward_saved_bytes",
+                 "diffattn_v2_forward_train", "diffattn_v2_backward_saved", "diffattn_v2_forward_saved_bytes",
                  "diffattn_layer_workspace", "diffattn_v2_layer_forward", "diffattn_v2_layer_workspace",
                  "diffattn_v2_decode_fp8k", "diffattn_backward", "diffattn_backward_workspace",
                  "lambda_reparam_backward", "diffattn_v2_backward", "diffattn_v2_backward_workspace"):
@@ -308,6 +310,61 @@ def test_v2_fp8qk_forward_host_validation(L):
         assert call(s=(1.0, bad)) == da.ERR_SHAPE
     assert call(q=MIS) == da.ERR_ALIGN
     assert call(out=MIS) == da.ERR_ALIGN
+
+
+def test_training_pair_host_validation(L):
+    sz = ctypes.c_size_t
+    need = L.diffattn_forward_saved_bytes(1, 2, 8, 64)
+    assert need >= 2 * 16 * 4 + 2 * 16 * 128 * 2
+    SAVED = P(0x200000)  # 256-byte aligned fake device address
+
+    def fwd(d=64, saved=SAVED, nbytes=None, q1=A):
+        nb = need if nbytes is None else nbytes
+        return L.diffattn_forward_train(1, 2, 8, d, q1, A, A, A, A, A, ctypes.c_float(0.2), None, ctypes.c_float(1e-5),
+                                        1, A, saved, sz(nb), None)
+    assert fwd(d=128) == da.ERR_UNSUPPORTED
+    assert fwd(q1=None) == da.ERR_NULL
+    assert fwd(saved=None) == da.ERR_NULL
+    assert fwd(nbytes=need - 1) == da.ERR_SHAPE
+    assert fwd(saved=P(0x200010)) == da.ERR_ALIGN
+    assert fwd(q1=MIS) == da.ERR_ALIGN
+    wneed = L.diffattn_backward_workspace(1, 2, 8, 64)
+
+    def bwd(d=64, saved=SAVED, nbytes=None, ws=A, wbytes=None, dlam=A):
+        nb = need if nbytes is None else nbytes
+        wb = wneed if wbytes is None else wbytes
+        return L.diffattn_backward_saved(1, 2, 8, d, A, A, A, A, A, A, ctypes.c_float(0.2), None,
+                                         ctypes.c_float(1e-5), 1, A, saved, sz(nb), A, A, A, A, A, dlam, None, ws,
+                                         sz(wb), None)
+    assert bwd(d=128) == da.ERR_UNSUPPORTED
+    assert bwd(dlam=None) == da.ERR_NULL
+    assert bwd(saved=None) == da.ERR_NULL
+    assert bwd(nbytes=need - 1) == da.ERR_SHAPE
+    assert bwd(wbytes=wneed - 1) == da.ERR_SHAPE
+    assert bwd(ws=MIS) == da.ERR_ALIGN
+    need2 = L.diffattn_v2_forward_saved_bytes(1, 4, 8, 128)
+
+    def fwd2(Hq=4, Hkv=2, d=128, saved=SAVED, nbytes=None, sb=0, st=0):
+        nb = need2 if nbytes is None else nbytes
+        return L.diffattn_v2_forward_train(1, Hq, Hkv, 8, d, A, A, A, A, sb, st, ctypes.c_float(0.0), 1, A, saved,
+                                           sz(nb), None)
+    assert fwd2(d=64) == da.ERR_UNSUPPORTED
+    assert fwd2(Hq=3) == da.ERR_SHAPE
+    assert fwd2(sb=-1) == da.ERR_SHAPE
+    assert fwd2(saved=None) == da.ERR_NULL
+    assert fwd2(nbytes=need2 - 1) == da.ERR_SHAPE
+    w2 = L.diffattn_v2_backward_workspace(1, 4, 8, 128)
+
+    def bwd2(d=128, sb=0, st=0, saved=SAVED, nbytes=None, wbytes=None):
+        nb = need2 if nbytes is None else nbytes
+        wb = w2 if wbytes is None else wbytes
+        return L.diffattn_v2_backward_saved(1, 4, 2, 8, d, A, A, A, A, sb, st, ctypes.c_float(0.0), 1, A, saved,
+                                            sz(nb), A, A, A, A, A, sz(wb), None)
+    assert bwd2(d=64) == da.ERR_UNSUPPORTED
+    assert bwd2(sb=3, st=1) == da.ERR_UNSUPPORTED  # not one of the three logit layouts
+    assert bwd2(saved=None) == da.ERR_NULL
+    assert bwd2(nbytes=need2 - 1) == da.ERR_SHAPE
+    assert bwd2(wbytes=w2 - 1) == da.ERR_SHAPE
 
 
 def test_projection_host_validation(L):
