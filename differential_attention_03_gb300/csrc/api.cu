@@ -1254,21 +1254,28 @@ namespace {
 
 // V1 (d = 64): statistics pass, dK/dV/dQ kernel, reduction of dlambda and dgamma.
 // A training forward's saved statistics: lse [2][rows] fp32, then O_1 and O_2
-// [rows x value width] bf16 (BSHD row order), 256-byte aligned parts.
+// in bf16, each in 128-token tiles: [units of all batches][tiles][4 channel
+// blocks][128 rows][32 channels] (the layout the forward's epilogue writes
+// with whole 64-byte rows per thread), 256-byte aligned parts.  `units` =
+// batches x heads (V1) or head pairs (V2); `n` tokens.
 struct SavedFwd {
   const float* lse;
   const __nv_bfloat16* o1;
   const __nv_bfloat16* o2;
 };
 
-size_t saved_fwd_bytes(size_t rows, size_t dv) { return round256(2 * rows * 4) + 2 * round256(rows * dv * 2); }
+size_t saved_fwd_bytes(size_t units, size_t n, size_t dv) {
+  const size_t rows = units * n, padded = units * ((n + 127) / 128) * 128;
+  return round256(2 * rows * 4) + 2 * round256(padded * dv * 2);
+}
 
-SavedFwd saved_fwd_views(const void* saved, size_t rows, size_t dv) {
+SavedFwd saved_fwd_views(const void* saved, size_t units, size_t n, size_t dv) {
+  const size_t rows = units * n, padded = units * ((n + 127) / 128) * 128;
   const uint8_t* b = static_cast<const uint8_t*>(saved);
   SavedFwd v;
   v.lse = reinterpret_cast<const float*>(b);
   v.o1 = reinterpret_cast<const __nv_bfloat16*>(b + round256(2 * rows * 4));
-  v.o2 = reinterpret_cast<const __nv_bfloat16*>(b + round256(2 * rows * 4) + round256(rows * dv * 2));
+  v.o2 = reinterpret_cast<const __nv_bfloat16*>(b + round256(2 * rows * 4) + round256(padded * dv * 2));
   return v;
 }
 
@@ -1759,12 +1766,12 @@ diffattn_status diffattn_v2_backward(diffattn_dtype dt, int B, int Hq, int Hkv, 
 // ---- training forward (saves each row's statistics) and the backward from them
 size_t diffattn_forward_saved_bytes(int B, int H, int n, int d) {
   if (B < 0 || H < 0 || n < 0 || d < 1) return 0;
-  return saved_fwd_bytes(static_cast<size_t>(B) * H * n, 2 * static_cast<size_t>(d));
+  return saved_fwd_bytes(static_cast<size_t>(B) * H, static_cast<size_t>(n), 2 * static_cast<size_t>(d));
 }
 
 size_t diffattn_v2_forward_saved_bytes(int B, int Hq, int n, int d) {
   if (B < 0 || Hq < 0 || n < 0 || d < 1) return 0;
-  return saved_fwd_bytes(static_cast<size_t>(B) * (Hq / 2) * n, static_cast<size_t>(d));
+  return saved_fwd_bytes(static_cast<size_t>(B) * (Hq / 2), static_cast<size_t>(n), static_cast<size_t>(d));
 }
 
 // Checks shared by the training entry points: bf16 tensors 16-byte aligned, the saved buffer's size and alignment.
@@ -1793,7 +1800,7 @@ diffattn_status diffattn_forward_train(int B, int H, int n, int d, const void* q
   if (eps <= 0.f) eps = 1e-5f;
   int* status = nullptr;
   if ((st = status_word(&status)) != DIFFATTN_OK) return st;
-  const SavedFwd sv = saved_fwd_views(saved, R, 2 * d);
+  const SavedFwd sv = saved_fwd_views(saved, static_cast<size_t>(B) * H, static_cast<size_t>(n), 2 * d);
   const long long Hd = static_cast<long long>(H) * d;
   da::TwoPassParams p;
   memset(&p, 0, sizeof(p));
@@ -1846,7 +1853,7 @@ diffattn_status diffattn_backward_saved(int B, int H, int n, int d, const void* 
   if (eps <= 0.f) eps = 1e-5f;
   int* status = nullptr;
   if ((st = status_word(&status)) != DIFFATTN_OK) return st;
-  const SavedFwd sv = saved_fwd_views(saved, static_cast<size_t>(B) * H * n, 2 * d);
+  const SavedFwd sv = saved_fwd_views(saved, static_cast<size_t>(B) * H, static_cast<size_t>(n), 2 * d);
   if ((st = backward_v1_tc(B, H, n, q1, q2, k1, k2, v, lambda, lambda_init, gamma, eps, causal, dy, dq1, dq2, dk1, dk2,
                            dv, dlambda, dgamma, static_cast<uint8_t*>(workspace), status, s, &sv)) != DIFFATTN_OK)
     return st;
@@ -1874,7 +1881,7 @@ diffattn_status diffattn_v2_forward_train(int B, int Hq, int Hkv, int n, int d, 
   if (st != DIFFATTN_OK) return st;
   int* status = nullptr;
   if ((st = status_word(&status)) != DIFFATTN_OK) return st;
-  const SavedFwd sv = saved_fwd_views(saved, R, d);
+  const SavedFwd sv = saved_fwd_views(saved, static_cast<size_t>(B) * G, static_cast<size_t>(n), d);
   const double scale = softmax_scale > 0.f ? softmax_scale : 1.0 / std::sqrt(static_cast<double>(d));
   da::TwoPassParams p;
   memset(&p, 0, sizeof(p));
@@ -1934,7 +1941,7 @@ diffattn_status diffattn_v2_backward_saved(int B, int Hq, int Hkv, int n, int d,
   int* status = nullptr;
   if ((st = status_word(&status)) != DIFFATTN_OK) return st;
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.f / std::sqrt(static_cast<float>(d));
-  const SavedFwd sv = saved_fwd_views(saved, static_cast<size_t>(B) * G * n, d);
+  const SavedFwd sv = saved_fwd_views(saved, static_cast<size_t>(B) * G, static_cast<size_t>(n), d);
   if ((st = backward_v2_tc(B, Hq, Hkv, n, q, k, v, lam_logits, sb, st_, scale, causal, dy, dq, dk, dv, dlogits, dense,
                            static_cast<uint8_t*>(workspace), status, s, &sv)) != DIFFATTN_OK)
     return st;

@@ -33,8 +33,8 @@ namespace da {
 
 struct BwdPrepParams {
   const __nv_bfloat16* dy;  // [B, n, units, 128]
-  const __nv_bfloat16* o1;  // saved O_1, same layout
-  const __nv_bfloat16* o2;  // saved O_2
+  const __nv_bfloat16* o1;  // saved O_1: [B units][128-row tiles][4 channel blocks][128 rows][32 channels]
+  const __nv_bfloat16* o2;  // saved O_2, same layout
   const float* lse;         // saved [2][rows]: lse_1, lse_2 (row ri = (b units + u) n + t)
   const float* lambda;      // V1: device scalar
   const float* gamma;       // V1: [128] or nullptr
@@ -105,13 +105,18 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 3) bwd_prep_kernel(const __gr
     }
     uint2 wdy[kPrepIlp], wo1[kPrepIlp], wo2[kPrepIlp];
     float lse_v[kPrepIlp];  // lanes 0, 1: lse_1, lse_2 of the row
+    const int ntiles = (p.n + 127) / 128;
 #pragma unroll
     for (int jj = 0; jj < kPrepIlp; ++jj) {
       const bool in = ob + jj < p.rows;
       const long long o = in ? ob + jj : ob;
+      // this lane's 4 channels c0 .. c0 + 3: block c0 / 32 of the row's tile
+      const long long so =
+          ((((static_cast<long long>(bs[jj]) * p.units + us[jj]) * ntiles + ts[jj] / 128) * 4 + (c0 >> 5)) * 128 +
+           ts[jj] % 128) * 32 + (c0 & 31);
       wdy[jj] = *reinterpret_cast<const uint2*>(p.dy + o * DV + c0);
-      wo1[jj] = *reinterpret_cast<const uint2*>(p.o1 + o * DV + c0);
-      wo2[jj] = *reinterpret_cast<const uint2*>(p.o2 + o * DV + c0);
+      wo1[jj] = *reinterpret_cast<const uint2*>(p.o1 + so);
+      wo2[jj] = *reinterpret_cast<const uint2*>(p.o2 + so);
       lse_v[jj] = (lane < 2 && in) ? p.lse[lane * p.rows + ris[jj]] : 0.f;
     }
 #pragma unroll

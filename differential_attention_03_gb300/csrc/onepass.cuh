@@ -772,32 +772,6 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
         tmem_ld32(tl + C::TM_O1 + 32u * cb, o1);
         tmem_ld32(tl + C::TM_O2 + 32u * cb, o2);
         tmem_ld_wait2(o1, o2);
-        if constexpr (SAVE) {
-          // Training forward: the row's normalised map outputs O_r = O_r' / l_r
-          // (bf16, this warpgroup's 32 channels) and, from the warpgroups that
-          // hold each map's running maximum, lse_r = m_r + log2 l_r.
-          if (t < p.n && DA_BOUNDS_V(c.b < p.B && c.u < p.units_per_batch, t)) {
-            const long long orow = (static_cast<long long>(c.b) * p.n + t) * p.units_per_batch + c.u;
-            const float il2 = 1.f / l2;
-            uint4* s1 = reinterpret_cast<uint4*>(p.o1_save + orow * DV + 32 * cb);
-            uint4* s2 = reinterpret_cast<uint4*>(p.o2_save + orow * DV + 32 * cb);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t w1[4], w2[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int cc = 8 * v + 2 * e;
-                w1[e] = pack_bf16x2(__uint_as_float(o1[cc]) * a1, __uint_as_float(o1[cc + 1]) * a1);
-                w2[e] = pack_bf16x2(__uint_as_float(o2[cc]) * il2, __uint_as_float(o2[cc + 1]) * il2);
-              }
-              s1[v] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-              s2[v] = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-            }
-            const long long ri = (static_cast<long long>(c.b) * p.units_per_batch + c.u) * p.n + t;
-            if (cb == 0) p.row[ri] = m_used + log2f(l1);
-            if (cb == 2) p.row[p.rows + ri] = m_used + log2f(l2);
-          }
-        }
         if constexpr (PERSIST) {
           // O is in registers: the next item's first PV may overwrite it.
           tc_fence_before();
@@ -805,8 +779,44 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
           if (lane == 0) mbar_arrive(o_free);
           __syncwarp();
         }
+        if constexpr (SAVE) {
+          // Training forward: the row's normalised map outputs O_r = O_r' / l_r
+          // (bf16, this warpgroup's 32 channels), packed and stored 8 channels
+          // at a time alongside y, and, from the warpgroups that hold each
+          // map's running maximum, lse_r = m_r + log2 l_r.  Saved layout:
+          // [unit][128-row tile][channel block cb][row][32 channels], so the
+          // warp's 32 rows of a block are 2 KB in a row.
+          const bool live = t < p.n && DA_BOUNDS_V(c.b < p.B && c.u < p.units_per_batch, t);
+          const long long blk =
+              ((static_cast<long long>(c.b) * p.units_per_batch + c.u) * ((p.n + 127) / 128) + c.qt) * 4 + cb;
+          const long long off = (blk * 128 + row) * 32;
+          const float il2 = 1.f / l2;
 #pragma unroll
-        for (int cc = 0; cc < 32; ++cc) y[cc] = fmaf(__uint_as_float(o2[cc]), a2, __uint_as_float(o1[cc]) * a1);
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w1[4], w2[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int cc = 8 * v + 2 * e;
+              const float x1a = __uint_as_float(o1[cc]) * a1, x1b = __uint_as_float(o1[cc + 1]) * a1;
+              y[cc] = fmaf(__uint_as_float(o2[cc]), a2, x1a);
+              y[cc + 1] = fmaf(__uint_as_float(o2[cc + 1]), a2, x1b);
+              w1[e] = pack_bf16x2(x1a, x1b);
+              w2[e] = pack_bf16x2(__uint_as_float(o2[cc]) * il2, __uint_as_float(o2[cc + 1]) * il2);
+            }
+            if (live) {
+              reinterpret_cast<uint4*>(p.o1_save + off)[v] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+              reinterpret_cast<uint4*>(p.o2_save + off)[v] = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+            }
+          }
+          if (live) {
+            const long long ri = (static_cast<long long>(c.b) * p.units_per_batch + c.u) * p.n + t;
+            if (cb == 0) p.row[ri] = m_used + log2f(l1);
+            if (cb == 2) p.row[p.rows + ri] = m_used + log2f(l2);
+          }
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < 32; ++cc) y[cc] = fmaf(__uint_as_float(o2[cc]), a2, __uint_as_float(o1[cc]) * a1);
+        }
       }
       float rinv = 1.f;
       if (EPI == kEpiRmsNorm) {

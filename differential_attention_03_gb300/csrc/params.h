@@ -20,14 +20,12 @@ struct TwoPassParams {
   const float* lam_logits;  // V2: logit of (b, t, g) at b*sb + t*st + g
   long long sb, st;
   float scale_log2;  // softmax scale * log2(e) (map 1; both maps unless e4m3 inputs)
-  float scale2_log2; // e4m3 queries and keys only: map 2's, with its dequantisation scales
   float norm_mult;   // V1: 1 - lambda_init
   float eps;         // V1: RMSNorm epsilon
   int B, n, causal;
   int units_per_batch;  // V1: H; V2: Hq / 2
   int group;            // V2: query heads per KV head
   int num_q_tiles;   // query tiles per unit in this launch: [q_tile_begin, q_tile_begin + num_q_tiles)
-  int q_tile_begin;  // first query tile (0 unless a causal forward is run over token chunks)
   int order;  // 0: unit-major tile order, 1: query-tile-major
   int* status;
   CUtensorMap tm_out;  // output [B, n, units_per_batch, DV] for TMA stores
@@ -42,9 +40,12 @@ struct TwoPassParams {
   long long rows;           // B * units_per_batch * n
   // Training forward (one-sweep kernel with SAVE): besides the output, each
   // row's lse_1, lse_2 (to row[ri], row[rows + ri]) and its normalised map
-  // outputs O_1, O_2 in bf16, [B, n, units_per_batch, DV] each.
+  // outputs O_1, O_2 in bf16, each laid out [B units_per_batch][128-row
+  // tiles][4 blocks of 32 channels][128 rows][32 channels].
   __nv_bfloat16* o1_save;
   __nv_bfloat16* o2_save;
+  float scale2_log2;  // e4m3 queries and keys only: map 2's softmax scale, with its dequantisation scales
+  int q_tile_begin;   // first query tile (0 unless a causal forward is run over token chunks)
 };
 
 // What work item `idx` of a tcgen05 launch computes: batch b, unit u (V1:

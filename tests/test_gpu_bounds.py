@@ -3,9 +3,10 @@
 That build checks every TMA coordinate, tensor-memory address and global store of the kernels
 before the access and reports a failed check as DIFFATTN_ERR_BOUNDS.  Here it is built, shown to
 catch a checked store out of its limit (a self-test whose store lands inside its own array either
-way), and then the small-size parity tests (forward V1 / V2 incl. FP8 QK^T, decode incl. FP8 keys
-and split states, backward fp32 and bf16, projections and layers: n <= 1100) run against it in a
-child process with DIFFATTN_DEBUG=1: each of them reads the device status after its kernels, so a
+way), and then the small-size parity tests (forward V1 / V2 incl. FP8 QK^T and the host-buffer
+pipeline, decode incl. FP8 keys and split states, backward fp32 and bf16 incl. the training pair,
+projections and layers: n <= 1100, and the host pipeline's token chunks up to n = 9000) run against
+it in a child process with DIFFATTN_DEBUG=1: each of them reads the device status after its kernels, so a
 failed check fails the test.
 """
 
@@ -20,7 +21,8 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 SMALL = ("(small_full_compare or test_v1_decode or test_v2_decode or backward_f32 or backward_bf16 "
-         "or layer_matches or projection_matches or lambda_outside or zero_tokens) and not bench and not long")
+         "or layer_matches or projection_matches or lambda_outside or zero_tokens or train_pair or host_buffers) "
+         "and not bench and not long")
 
 
 def _child_env():
@@ -61,7 +63,8 @@ def test_bounds_build_catches_a_checked_store():
 
 def test_small_parity_cases_pass_under_bounds_checks():
     cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
-           "tests/test_gpu_parity.py", "tests/test_gpu_backward_tc.py", "tests/test_gpu_layer.py", "-k", SMALL]
+           "tests/test_gpu_parity.py", "tests/test_gpu_backward_tc.py", "tests/test_gpu_layer.py",
+           "tests/test_gpu_train.py", "-k", SMALL]
     r = subprocess.run(cmd, cwd=ROOT, env=_child_env(), capture_output=True, text=True, timeout=3000)
     tail = (r.stdout + r.stderr)[-4000:]
     assert r.returncode == 0, tail
