@@ -60,10 +60,11 @@ KERNEL_FILES = {
     "v1-bf16-B1H12-n65536-d128": ['twopass.cuh', 'twopass_inst.cuh', 'k_twopass_v1_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh'],
     "v2-bf16-B8Hq32Hkv16-n8192-d128": ['onepass.cuh', 'onepass_inst.cuh', 'k_onepass_v2_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh'],
 }
-NCU_TRAFFIC = {  # workload: (source hash of its kernel, bytes per launch)
-    "v1-bf16-B4H16-n2048-d64": ("413f0242e5ff72fd", 136.099840e6 + 14.131200e6),
-    "v1-bf16-B2H12-n4096-d128": ("292777c78dab3bb4", 329.992448e6 + 29.970432e6),
-    "v2-bf16-B8Hq32Hkv16-n8192-d128": ("bdd09c4f5ca33d5a", 1074.024e6 + 255.850240e6),
+NCU_TRAFFIC = {  # workload: (source hash of its kernel, bytes per launch: dram__bytes_read.sum + dram__bytes_write.sum)
+    "v1-bf16-B4H16-n2048-d64": ("3a09f68d8964d17d", 137819136 + 12754688),
+    "v1-bf16-B2H12-n4096-d128": ("dfe882014fe2b468", 327775744 + 28875776),
+    "v1-bf16-B1H12-n65536-d128": ("dfe882014fe2b468", 1761651456 + 405597696),
+    "v2-bf16-B8Hq32Hkv16-n8192-d128": ("df2ce3ab30bc8ec1", 1073809408 + 254875904),
 }
 
 
