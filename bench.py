@@ -287,6 +287,7 @@ DECODE_WORKLOADS = [  # (name, B, H or (Hq, Hkv), n, d, key cache): one new toke
     ("v1-decode-bf16-B1H16-n131072-d64-workspace", 1, 16, 131072, 64, "bf16"),
     # FP8 (e4m3) key caches, bf16 values
     ("v1-decode-fp8k-B8H16-n32768-d64", 8, 16, 32768, 64, "e4m3"),
+    ("v1-decode-fp8k-B8H8-n32768-d128", 8, 8, 32768, 128, "e4m3"),
     ("v2-decode-fp8k-B8Hq32Hkv16-n32768-d128", 8, (32, 16), 32768, 128, "e4m3"),
 ]
 

@@ -82,10 +82,13 @@ template <int D, bool V2 = false, bool K8 = false>
 struct DecodeCfg {
   static constexpr int MAX_CS = 8;  // CTAs per (b, h) cluster: chosen at launch, at most this (16-CTA
                                     // clusters measured slower: 5.5 vs 6.2 TB/s at B8 H8 n32768 d128)
-  // Warps per CTA.  V2: eight, so that a stage is 64 keys (32 KB).  FP8 keys:
-  // eight, so that two CTAs per SM hide the latency of the longer per-byte
-  // instruction stream (a key is 6 d bytes instead of 8 d for the same work).
-  static constexpr int NWARP = (V2 || K8) ? 8 : 4;
+  // Warps per CTA.  V2: eight, so that a stage is 64 keys (32 KB).  V1 with
+  // FP8 keys at d = 64: eight (PE = 16 products a lane), so that two CTAs per
+  // SM hide the latency of the longer per-byte instruction stream (a key is
+  // 6 d bytes instead of 8 d for the same work).  At d = 128 (32-key stages)
+  // eight warps would leave 4 keys a warp and 8 lanes a key: measured at half
+  // the bandwidth of four warps, so V1 d = 128 keeps four.
+  static constexpr int NWARP = (V2 || (K8 && D == 64)) ? 8 : 4;
   static constexpr int NTHREADS = NWARP * 32;
   static constexpr int DV = V2 ? D : 2 * D;     // value width
   static constexpr int NKT = V2 ? 1 : 2;         // key tiles a stage holds (V2: one K for both queries)
