@@ -804,7 +804,9 @@ static diffattn_status decode_v1(const char* fn, diffattn_dtype dt, int B, int H
   if (st != DIFFATTN_OK) return st;
   da::DecodeParams p;
   memset(&p, 0, sizeof(p));
-  const int bk = (d == 64) ? da::DecodeCfg<64>::BK : da::DecodeCfg<128>::BK;  // (the same with K8)
+  // keys per stage (= TMA box rows) of the kernel that runs
+  const int bk = k8 ? ((d == 64) ? da::DecodeCfg<64, false, true>::BK : da::DecodeCfg<128, false, true>::BK)
+                    : ((d == 64) ? da::DecodeCfg<64>::BK : da::DecodeCfg<128>::BK);
   const int nn = n > 0 ? n : 1;  // an empty cache still needs a valid map (no key is read)
   if (k8) {
     if ((st = make_map_u8(&p.tm_k1, k1, B, nn, H, d, bk)) != DIFFATTN_OK) return st;
@@ -958,7 +960,7 @@ static diffattn_status decode_v2(const char* fn, diffattn_dtype dt, int B, int H
   if (st != DIFFATTN_OK) return st;
   da::DecodeParams p;
   memset(&p, 0, sizeof(p));
-  constexpr int bk = da::DecodeCfg<128, true>::BK;
+  const int bk = k8 ? da::DecodeCfg<128, true, true>::BK : da::DecodeCfg<128, true>::BK;  // keys per stage (box rows)
   const int nn = n > 0 ? n : 1;  // an empty cache still needs a valid map (no key is read)
   if ((st = k8 ? make_map_u8(&p.tm_k1, k, B, nn, Hkv, d, bk) : make_map(&p.tm_k1, k, B, nn, Hkv, d, bk)) !=
       DIFFATTN_OK)
