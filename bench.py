@@ -61,10 +61,10 @@ KERNEL_FILES = {
     "v2-bf16-B8Hq32Hkv16-n8192-d128": ['onepass.cuh', 'onepass_inst.cuh', 'k_onepass_v2_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh'],
 }
 NCU_TRAFFIC = {  # workload: (source hash of its kernel, bytes per launch: dram__bytes_read.sum + dram__bytes_write.sum)
-    "v1-bf16-B4H16-n2048-d64": ("3a09f68d8964d17d", 137819136 + 12754688),
+    "v1-bf16-B4H16-n2048-d64": ("62cf361661a5de12", 134964992 + 13048064),
     "v1-bf16-B2H12-n4096-d128": ("dfe882014fe2b468", 327775744 + 28875776),
     "v1-bf16-B1H12-n65536-d128": ("dfe882014fe2b468", 1761651456 + 405597696),
-    "v2-bf16-B8Hq32Hkv16-n8192-d128": ("df2ce3ab30bc8ec1", 1073809408 + 254875904),
+    "v2-bf16-B8Hq32Hkv16-n8192-d128": ("9c6381a8498e1ae4", 1073854464 + 254917632),
 }
 
 
@@ -712,11 +712,12 @@ PROJECTION_WORKLOADS = [  # (name, M, N, K): c = a w^T alone
 
 def fp8_results(da, flush, peaks, inputs):
     """The V1 and V2 forwards with e4m3 queries and keys (one scale per tensor, amax / 448) on the
-    d = 128 workloads: TFLOP/s (the same algorithmic FLOPs as bf16) against the measured burst bf16 peak."""
+    tensor-core workloads (d = 64 and d = 128): TFLOP/s (the same algorithmic FLOPs as bf16) against the
+    measured burst bf16 peak."""
     import torch
     from differential_attention_03_gb300.inputs import WORKLOADS
     out = {}
-    for wid in (3, 4, 5):
+    for wid in (2, 3, 4, 5):
         w = WORKLOADS[wid]
         x = inputs(w)
         if w.kind == "v2":

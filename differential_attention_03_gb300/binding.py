@@ -217,10 +217,10 @@ def diffattn_forward_fp8qk(q1, q2, k1, k2, scales, v, lam, lambda_init_value: fl
                            causal: bool = True, out=None, stream=None) -> torch.Tensor:
     """DIFF V1 forward with e4m3 queries and keys (QK^T on the FP8 tensor-core path).
 
-    q1, q2, k1, k2: [B, n, H, 128] e4m3 codes (torch.float8_e4m3fn or their bytes as uint8) of
-    Q_r / q_scale_r and K_r / k_scale_r; scales = (q1_scale, q2_scale, k1_scale, k2_scale).  The
-    result is diffattn_forward's for Q_r = q_scale_r e4m3(q_r), K_r = k_scale_r e4m3(k_r); v bf16
-    [B, n, H, 256].  Returns out [B, n, H, 256] bf16.
+    q1, q2, k1, k2: [B, n, H, d] e4m3 codes (torch.float8_e4m3fn or their bytes as uint8) of
+    Q_r / q_scale_r and K_r / k_scale_r, d = 128, or d = 64 with H >= 2; scales = (q1_scale,
+    q2_scale, k1_scale, k2_scale).  The result is diffattn_forward's for Q_r = q_scale_r e4m3(q_r),
+    K_r = k_scale_r e4m3(k_r); v bf16 [B, n, H, 2d].  Returns out [B, n, H, 2d] bf16.
     """
     B, n, H, d = q1.shape
     for name, t in (("q1", q1), ("q2", q2), ("k1", k1), ("k2", k2)):

@@ -28,7 +28,7 @@ BOUNDS_LIB = os.path.join(PKG, "libdiffattn_bounds.so")
 
 SOURCES = ["api.cu", "k_simt.cu", "k_twopass_v1_d128.cu", "k_onepass_v1_d64.cu", "k_onepass_v2_d128.cu",
            "k_decode.cu", "k_backward.cu", "k_gemm.cu",
-           "k_twopass_v1_d128_f8.cu", "k_onepass_v2_d128_f8.cu", "k_onepass_save.cu", "k_bwd_tc.cu"]
+           "k_twopass_v1_d128_f8.cu", "k_onepass_v2_d128_f8.cu", "k_onepass_v1_d64_f8.cu", "k_onepass_save.cu", "k_bwd_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -225,6 +225,25 @@ diffattn_status make_map_u8(CUtensorMap* m, const void* base, int B, int n, int 
   return DIFFATTN_OK;
 }
 
+// 4-D map over e4m3 codes [B, n, heads, W] viewed as {heads W bytes, 1, n, B}, boxes of 128 bytes x
+// `rows`: a head's W = 64-byte row is read together with the next head's (zeros past the last one), so
+// the box has the 128-byte swizzled rows the MMA operands use.
+diffattn_status make_map_u8_wide(CUtensorMap* m, const void* base, int B, int n, int heads, int W, int rows) {
+  EncodeTiledFn enc;
+  diffattn_status s = get_encoder(&enc);
+  if (s != DIFFATTN_OK) return s;
+  const cuuint64_t row = static_cast<cuuint64_t>(W) * heads;
+  const cuuint64_t dims[4] = {row, 1, static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {row, row, row * static_cast<cuuint64_t>(n)};
+  const cuuint32_t box[4] = {128, 1, static_cast<cuuint32_t>(rows), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DIFFATTN_ERR_CUDA, "cuTensorMapEncodeTiled (u8, wide) failed (CUresult %d)", (int)r);
+  return DIFFATTN_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Tile order: unit-major keeps all query tiles of one head together so that its
@@ -290,7 +309,8 @@ diffattn_status launch_v1_tc(const char* fn, da::TwoPassParams& p, bool f8, int 
   const bool persist = qt0 + p.num_q_tiles <= 64;  // (the last tile's item length decides)
   const int g = static_cast<int>(persist ? persistent_grid(grid) : grid);
   // (p.o1_save set: the training forward, d = 64, which also saves each row's statistics)
-  cudaError_t e = f8 ? da::launch_twopass_v1_d128_f8(p, g, persist, s)
+  cudaError_t e = f8 ? ((d == 64) ? da::launch_onepass_v1_d64_f8(p, g, persist, s)
+                                   : da::launch_twopass_v1_d128_f8(p, g, persist, s))
                   : (d == 64) ? (p.o1_save ? da::launch_onepass_v1_d64_save(p, g, persist, s)
                                            : da::launch_onepass_v1_d64(p, g, persist, s))
                               : da::launch_twopass_v1_d128(p, g, persist, s);
@@ -334,6 +354,7 @@ diffattn_status launch_v2_tc(const char* fn, da::TwoPassParams& p, bool f8, int 
   p.sb = sb;
   p.st = st_;
   p.scale_log2 = scale_log2;
+  p.scale2_log2 = scale_log2;  // (both maps score against the same key head with the same scale)
   p.norm_mult = 1.f;
   p.eps = 0.f;
   p.B = B;
@@ -464,8 +485,10 @@ diffattn_status diffattn_forward_fp8qk(int B, int H, int n, int d, const void* q
   const char* fn = "diffattn_forward_fp8qk";
   if (B < 0 || H < 0 || n < 0 || d < 1)
     return fail(DIFFATTN_ERR_SHAPE, "%s: bad sizes B=%d H=%d n=%d d=%d", fn, B, H, n, d);
-  if (d != 128) return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: d = 128 only (got %d)", fn, d);
+  if (d != 128 && d != 64) return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: d = 64 or 128 only (got %d)", fn, d);
   if (B == 0 || H == 0 || n == 0) return ok();
+  if (d == 64 && H < 2)  // (the 128-byte boxes span two heads' rows)
+    return fail(DIFFATTN_ERR_UNSUPPORTED, "%s: d = 64 needs at least two heads (got H = %d)", fn, H);
   if (!q1 || !q2 || !k1 || !k2 || !v || !lambda || !out) return fail(DIFFATTN_ERR_NULL, "%s: NULL pointer", fn);
   if (!std::isfinite(lambda_init)) return fail(DIFFATTN_ERR_SHAPE, "%s: lambda_init not finite", fn);
   for (float sc : {q1_scale, q2_scale, k1_scale, k2_scale})
@@ -479,11 +502,15 @@ diffattn_status diffattn_forward_fp8qk(int B, int H, int n, int d, const void* q
   const int dv = 2 * d;
   da::TwoPassParams p;
   memset(&p, 0, sizeof(p));
-  // Query and key rows are 128 bytes: one box (128-byte swizzle) of 128 rows a tile.
-  if ((st = make_map_u8(&p.tm_q1, q1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
-  if ((st = make_map_u8(&p.tm_q2, q2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
-  if ((st = make_map_u8(&p.tm_k1, k1, B, n, H, d, 128)) != DIFFATTN_OK) return st;
-  if ((st = make_map_u8(&p.tm_k2, k2, B, n, H, d, 128)) != DIFFATTN_OK) return st;
+  // Query and key rows: d = 128, 128 bytes, one box (128-byte swizzle) of 128 rows a tile; d = 64, a
+  // 128-byte box over this head's row and the next one's.  V: 64-row boxes (the ring's half slots).
+  auto qk_map = [&](CUtensorMap* m, const void* base) {
+    return d == 128 ? make_map_u8(m, base, B, n, H, d, 128) : make_map_u8_wide(m, base, B, n, H, d, 128);
+  };
+  if ((st = qk_map(&p.tm_q1, q1)) != DIFFATTN_OK) return st;
+  if ((st = qk_map(&p.tm_q2, q2)) != DIFFATTN_OK) return st;
+  if ((st = qk_map(&p.tm_k1, k1)) != DIFFATTN_OK) return st;
+  if ((st = qk_map(&p.tm_k2, k2)) != DIFFATTN_OK) return st;
   if ((st = make_map_box(&p.tm_v, v, B, n, H, dv, 64, 64)) != DIFFATTN_OK) return st;
   // S_r = (q_scale_r k_scale_r) e4m3(q_r) e4m3(k_r)^T / sqrt(d): the scales fold into each map's exponent.
   const double c = 1.4426950408889634 / std::sqrt(static_cast<double>(d));

@@ -27,6 +27,8 @@ cudaError_t launch_onepass_v1_d64(const TwoPassParams& p, int grid, bool persist
 cudaError_t launch_onepass_v2_d128(const TwoPassParams& p, int grid, cudaStream_t s);
 // The same with e4m3 queries and keys (tm_q1 / tm_k1 over bytes; scale_log2 carries their scales).
 cudaError_t launch_onepass_v2_d128_f8(const TwoPassParams& p, int grid, cudaStream_t s);
+// V1, d = 64, e4m3 queries and keys (each Q/K map {H d bytes, 1, n, B} with 128-byte boxes).
+cudaError_t launch_onepass_v1_d64_f8(const TwoPassParams& p, int grid, bool persistent, cudaStream_t s);
 // The training forward (SAVE): the output plus lse_r and O_r of every row (see TwoPassParams).
 cudaError_t launch_onepass_v1_d64_save(const TwoPassParams& p, int grid, bool persistent, cudaStream_t s);
 cudaError_t launch_onepass_v2_d128_save(const TwoPassParams& p, int grid, cudaStream_t s);

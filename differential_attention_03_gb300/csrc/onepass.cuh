@@ -80,13 +80,19 @@ struct OnePassCfg {
   static constexpr int NCTRL = 3;  // producer, two MMA warps
   static constexpr int NSMWG = 4;  // two softmax warpgroups per map
   static constexpr int NTHREADS = (NCTRL + 4 * NSMWG) * 32;
-  // F8: queries and keys arrive as e4m3 bytes (a d = 128 row is one
-  // 128-byte box; a key fill takes half a ring slot); V and P stay bf16.
+  // F8: queries and keys arrive as e4m3 bytes; V and P stay bf16.  At d = 128
+  // a row is one 128-byte box (a key fill takes half a ring slot).  At d = 64
+  // (WIDE) a row's 64 bytes are read as a 128-byte box that also holds the
+  // next head's 64 bytes (zeros past the last head), so the tile keeps the
+  // 128-byte-swizzled layout of every other QK^T operand; the MMAs read the
+  // first 64 bytes of each row only.
   static constexpr int QK_ES = F8 ? 1 : 2;       // bytes of a query/key element
-  static constexpr int QB = D * QK_ES / 128;     // 128-byte boxes across a Q/K row
+  static constexpr bool WIDE = F8 && D == 64;
+  static constexpr int QK_ROW = WIDE ? 128 : D * QK_ES;  // bytes of a Q/K tile row in shared memory
+  static constexpr int QB = QK_ROW / 128;        // 128-byte boxes across a Q/K row
   static constexpr int VB = DV / 64;
-  static constexpr int Q_TILE = BM * D * QK_ES;
-  static constexpr int K_TILE = BN * D * QK_ES;
+  static constexpr int Q_TILE = BM * QK_ROW;
+  static constexpr int K_TILE = BN * QK_ROW;
   static constexpr int V_TILE = BN * DV * 2;
   static constexpr int SLOT = BN * D * 2;  // a bf16 key tile
   static constexpr int VF = V_TILE / SLOT;
@@ -114,7 +120,8 @@ struct OnePassCfg {
   static constexpr float RESCALE_THRESHOLD = 8.f;  // log2 units
   static constexpr int MAX_ITEMS = PERSIST ? 0x7fffffff : 1;  // work items per CTA
   static_assert(D == 64 || D == 128, "query/key width");
-  static_assert(!F8 || (D == 128 && SHARED_K && !STATS), "e4m3 queries and keys: the V2 forward, d = 128");
+  static_assert(!F8 || (!STATS && ((D == 128 && SHARED_K) || (D == 64 && !SHARED_K))),
+                "e4m3 queries and keys: the V2 forward at d = 128, the V1 forward at d = 64");
   static_assert(!SAVE || (!STATS && !F8), "the training forward saves the bf16 forward's statistics");
   static_assert(V_TILE % SLOT == 0 && (VF == 1 || VF == 2), "value tile split");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -422,8 +429,11 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
           // (bounds build: query heads of the maps, V1 units, V2 2 units)
           if (DA_BOUNDS(bx * 64 < D && c.b < p.B && c.q0 < p.n &&
                         c.hq2 < (EPI == kEpiV2 ? 2 : 1) * p.units_per_batch)) {
-            tma_load_4d(smem + C::OFF_Q1 + bx * BM * 128, &p.tm_q1, q_full, bx * 64, c.hq1, c.q0, c.b);
-            tma_load_4d(smem + C::OFF_Q2 + bx * BM * 128, &p.tm_q2, q_full, bx * 64, c.hq2, c.q0, c.b);
+            // (WIDE maps are {H d bytes, 1, n, B}: a head's row starts at byte h d)
+            tma_load_4d(smem + C::OFF_Q1 + bx * BM * 128, &p.tm_q1, q_full, C::WIDE ? c.hq1 * D : bx * 64,
+                        C::WIDE ? 0 : c.hq1, c.q0, c.b);
+            tma_load_4d(smem + C::OFF_Q2 + bx * BM * 128, &p.tm_q2, q_full, C::WIDE ? c.hq2 * D : bx * 64,
+                        C::WIDE ? 0 : c.hq2, c.q0, c.b);
           }
         }
         ++qloads;
@@ -440,7 +450,9 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
           for (int bx = 0; bx < nbox; ++bx)
             if (DA_BOUNDS(key0 < (p.n + 127) / 128 * 128 && c.b < p.B &&  // (a box past n reads zeros)
                           c.hk < (EPI == kEpiV2 ? 2 * p.units_per_batch / p.group : p.units_per_batch)))
-              tma_load_4d(dst + bx * rows * 128, map, &full[s], bx * 64, c.hk, key0, c.b);
+              tma_load_4d(dst + bx * rows * 128, map, &full[s],
+                          (C::WIDE && map != &p.tm_v) ? c.hk * D : bx * 64,
+                          (C::WIDE && map != &p.tm_v) ? 0 : c.hk, key0, c.b);
           ++fill;
         };
         // The fill order is the order in which both MMA warps walk the ring.
@@ -602,7 +614,8 @@ __global__ void __launch_bounds__(608, 1) onepass_fwd_kernel(const __grid_consta
     const int wq = warp & 3;          // TMEM lane quarter
     const int row = wq * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    const float sc = p.scale_log2;
+    // softmax scale x log2(e) of this warp's map (e4m3 inputs: with that map's dequantisation scales)
+    const float sc = (F8 && map) ? p.scale2_log2 : p.scale_log2;
     const uint32_t tS = tl + (map ? C::TM_B : C::TM_A);
     const uint32_t tOr = tl + (map ? C::TM_O2 : C::TM_O1);
     const uint64_t sc2 = f2pack(sc, sc);

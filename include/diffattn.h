@@ -126,8 +126,10 @@ diffattn_status diffattn_forward(diffattn_dtype dt, int B, int H, int n, int d,
  * The result is diffattn_forward's for Q_r = q_scale_r e4m3(q_r) and
  * K_r = k_scale_r e4m3(k_r): every e4m3 product is exact in the fp32
  * accumulator and each map's two scales fold into its softmax exponent.
- * d = 128 only (one 128-byte row a box), else ERR_UNSUPPORTED.  Errors
- * otherwise as for diffattn_forward.
+ * d = 128 (one 128-byte row a box) or d = 64 with H >= 2 (a 128-byte box
+ * covers a head's 64-byte row and the next head's, whose bytes the MMAs do
+ * not read; the last head's box ends in zeros), else ERR_UNSUPPORTED.
+ * Errors otherwise as for diffattn_forward.
  */
 diffattn_status diffattn_forward_fp8qk(int B, int H, int n, int d, const void* q1, const void* q2,
                                        const void* k1, const void* k2, float q1_scale,

@@ -278,11 +278,14 @@ def test_v2_backward_host_validation(L):
 
 
 def test_fp8qk_forward_host_validation(L):
-    def call(B=1, n=8, d=128, q1=A, s=(1.0, 1.0, 1.0, 1.0), out=A):
-        return L.diffattn_forward_fp8qk(B, 2, n, d, q1, A, A, A, *(ctypes.c_float(x) for x in s), A, A,
+    def call(B=1, H=2, n=8, d=128, q1=A, s=(1.0, 1.0, 1.0, 1.0), out=A):
+        return L.diffattn_forward_fp8qk(B, H, n, d, q1, A, A, A, *(ctypes.c_float(x) for x in s), A, A,
                                         ctypes.c_float(0.2), None, ctypes.c_float(1e-5), 1, out, None)
     assert call(n=-1) == da.ERR_SHAPE
-    assert call(d=64) == da.ERR_UNSUPPORTED
+    assert call(d=96) == da.ERR_UNSUPPORTED
+    assert call(d=64, H=1) == da.ERR_UNSUPPORTED  # d = 64 reads two heads' rows a box
+    assert call(d=64, q1=None) == da.ERR_NULL
+    assert call(d=64, B=0) == da.OK
     assert call(B=0) == da.OK
     assert call(q1=None) == da.ERR_NULL
     for bad in (0.0, -2.0, float("nan"), float("inf")):

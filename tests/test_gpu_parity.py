@@ -703,14 +703,18 @@ def _deq(codes, scales, sel=lambda a: a):
     return {k: oracle.dequant_e4m3(sel(codes[k]).contiguous(), scales[k]) for k in codes}
 
 
-FP8_SMALL = [  # B, H, n, causal
-    (1, 1, 1, True), (1, 2, 129, True), (2, 2, 300, False), (1, 2, 1100, True), (2, 64, 300, True),
+FP8_SMALL = [  # B, H, n, causal, d
+    (1, 1, 1, True, 128), (1, 2, 129, True, 128), (2, 2, 300, False, 128), (1, 2, 1100, True, 128),
+    (2, 64, 300, True, 128),
+    # d = 64 (at least two heads: a 128-byte box holds a head's row and the next one's)
+    (1, 2, 1, True, 64), (1, 2, 129, True, 64), (2, 3, 300, False, 64), (1, 2, 1100, True, 64),
+    (2, 16, 257, True, 64),
 ]
 
 
-@pytest.mark.parametrize("B,H,n,causal", FP8_SMALL)
-def test_v1_fp8qk_small_full_compare(B, H, n, causal):
-    w = shrink(WORKLOADS[3], B=B, H=H, n=n, causal=causal, seed=200 + n + H)
+@pytest.mark.parametrize("B,H,n,causal,d", FP8_SMALL)
+def test_v1_fp8qk_small_full_compare(B, H, n, causal, d):
+    w = shrink(WORKLOADS[3 if d == 128 else 2], B=B, H=H, n=n, causal=causal, seed=200 + n + H + d)
     x = make_v1(w, "cuda")
     out, codes, scales = _fp8_case(w, x)
     deq = _deq(codes, scales)
@@ -788,7 +792,24 @@ def test_v2_fp8qk_full_size_sampled():
             assert err <= TOL["bf16"], f"batch {b} pair {kvh}: max abs error {err}"
 
 
-@pytest.mark.parametrize("wid", [3, 4])
+def test_v1_fp8qk_d64_matches_bf16_path_on_exact_values():
+    # d = 64: codes whose values are exact in bf16 as well (power-of-two scales), so the e4m3 path and
+    # the bf16 forward score the same products and differ only by the order of the fp32 sums.  The last
+    # head's boxes run past the row's end (zeros), the others read the next head's bytes unused.
+    B, H, n, d = 2, 3, 700, 64
+    g = torch.Generator(device="cuda").manual_seed(78)
+    c = [torch.randn((B, n, H, d), generator=g, device="cuda").to(torch.float8_e4m3fn) for _ in range(4)]
+    v = torch.randn((B, n, H, 2 * d), generator=g, device="cuda").to(torch.bfloat16)
+    sc = (0.25, 0.5, 0.125, 0.5)
+    lam = torch.tensor([0.6], device="cuda")
+    out8 = da.diffattn_forward_fp8qk(*c, sc, v, lam, 0.2)
+    bf = [(t.float() * s).to(torch.bfloat16) for t, s in zip(c, sc)]
+    ref = da.diffattn_forward(*bf, v, lam, 0.2)
+    da.device_status()
+    assert float((out8.float() - ref.float()).abs().max()) <= 1e-2
+
+
+@pytest.mark.parametrize("wid", [2, 3, 4])
 def test_v1_fp8qk_full_size_sampled(wid):
     w = WORKLOADS[wid]
     x = make_v1(w, "cuda")
