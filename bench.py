@@ -498,9 +498,10 @@ def run_ours(args):
                 del xc
             torch.cuda.empty_cache()
 
-    decode, backward, layer, fp8 = {}, {}, {}, {}
+    decode, backward, layer, fp8, graphs = {}, {}, {}, {}, {}
     if rank == 0 and world == 1 and not args.no_all_configs:
         decode = decode_results(da, flush, peaks)
+        graphs = graph_results(da)
         backward = backward_results(da, flush, (clocks or {}).get("sm_mhz") or 2070, peaks)
         layer = layer_results(da, flush, peaks)
         fp8 = fp8_results(da, flush, peaks, inputs)
@@ -531,6 +532,8 @@ def run_ours(args):
         line["layer"] = layer
     if fp8:
         line["fp8"] = fp8
+    if graphs:
+        line["graphs"] = graphs
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(w, x)
         cb.pop("seconds", None)
@@ -710,6 +713,65 @@ PROJECTION_WORKLOADS = [  # (name, M, N, K): c = a w^T alone
 ]
 
 
+GRAPH_DECODE = ("v1-decode-bf16-B1H16-n4096-d64-x8-layers", 1, 16, 4096, 64, 8)  # name, B, H, n, d, layers
+
+
+def graph_results(da):
+    """A decode step short enough to be bound by launches: one new token over eight layers' caches
+    (B1 H16 n4096 d64, 33.5 MB of keys and values a layer), eight library calls per token.  Timed
+    back to back (CUDA events around 50 tokens) as eager calls through the binding and as one CUDA-graph
+    replay of the same eight calls; the caches (268 MB) exceed L2, so no flush is needed."""
+    import torch
+    name, B, H, n, d, layers = GRAPH_DECODE
+    g = torch.Generator(device="cuda").manual_seed(77)
+
+    def rnd(*shape):
+        return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    cache = [(rnd(B, n, H, d), rnd(B, n, H, d), rnd(B, n, H, 2 * d)) for _ in range(layers)]
+    qs = [(rnd(B, H, d), rnd(B, H, d)) for _ in range(layers)]
+    lam = torch.tensor([0.3], device="cuda")
+    ws = torch.empty(da.decode_workspace_bytes(B, H, d), dtype=torch.uint8, device="cuda")
+    outs = [torch.empty((B, H, 2 * d), device="cuda", dtype=torch.bfloat16) for _ in range(layers)]
+
+    def token():
+        for i in range(layers):
+            k1, k2, v = cache[i]
+            da.diffattn_decode(qs[i][0], qs[i][1], k1, k2, v, lam, 0.2, out=outs[i], workspace=ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            token()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    da.device_status()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        token()
+
+    def timed(fn, tokens=50):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(tokens):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (tokens * layers)  # us per decode call
+    eager = statistics.median(timed(token) for _ in range(3))
+    replay = statistics.median(timed(graph.replay) for _ in range(3))
+    da.device_status()
+    nbytes = B * H * n * d * 8 + B * H * 4 * d * 2  # K1, K2, V once; q in, out
+    del graph
+    torch.cuda.empty_cache()
+    return {name: {"eager_us_per_call": round(eager, 2), "graph_us_per_call": round(replay, 2),
+                   "speedup": round(eager / replay, 2),
+                   "graph_tb_s": round(nbytes / (replay * 1e-6) / 1e12, 3),
+                   "calls_per_token": layers}}
+
+
 def fp8_results(da, flush, peaks, inputs):
     """The V1 and V2 forwards with e4m3 queries and keys (one scale per tensor, amax / 448) on the
     tensor-core workloads (d = 64 and d = 128): TFLOP/s (the same algorithmic FLOPs as bf16) against the
@@ -881,7 +943,8 @@ def run_decode_only(only=None):
     build.build()
     da.lib()
     flush = torch.empty(FLUSH_BYTES // 4, device="cuda", dtype=torch.float32)
-    print(json.dumps({"decode": decode_results(da, flush, read_peaks(), only)}), flush=True)
+    print(json.dumps({"decode": decode_results(da, flush, read_peaks(), only), "graphs": graph_results(da)}),
+          flush=True)
 
 
 def main(argv=None):
