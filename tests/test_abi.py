@@ -3,8 +3,11 @@ symbol include/diffattn.h declares, and rejects bad arguments on the host
 before any CUDA call (these calls never reach the device)."""
 
 import ctypes
+import glob
 import os
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -27,6 +30,29 @@ def _declared():
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\(", text, flags=re.M)
     return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_is_strict_c99_and_a_c_program_links(L, tmp_path):
+    # The header alone compiles as pedantic C99; the plain C consumer of the GPU tests
+    # (tests/c/abi_consumer.c) compiles warning-free and links against libdiffattn.so.
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "h.c"
+    src.write_text('#include "diffattn.h"\nint main(void) { return (int)DIFFATTN_OK + (int)DIFFATTN_BF16 - 1; }\n')
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I",
+                        os.path.join(ROOT, "include"), str(src), "-o", str(tmp_path / "h")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    home = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    libs = glob.glob(os.path.join(home, "lib64", "libcudart.so")) + glob.glob(
+        os.path.join(home, "targets", "*", "lib", "libcudart.so"))
+    if not libs:
+        pytest.skip("libcudart.so not found")
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-I", os.path.join(home, "include"), os.path.join(ROOT, "tests", "c", "abi_consumer.c"),
+                        "-o", str(tmp_path / "consumer"), "-L", os.path.dirname(build.LIB), "-ldiffattn",
+                        "-L", os.path.dirname(libs[0]), "-lcudart"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
 
 
 def test_header_declares_the_entry_points():
