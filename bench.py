@@ -55,16 +55,16 @@ def hbm_bytes(w) -> float:
 # kernel it was taken from: it is keyed to the hash of that kernel's source
 # files and reported while the hash still matches, null otherwise.
 KERNEL_FILES = {
-    "v1-bf16-B4H16-n2048-d64": ['onepass.cuh', 'onepass_inst.cuh', 'k_onepass_v1_d64.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh'],
-    "v1-bf16-B2H12-n4096-d128": ['twopass.cuh', 'twopass_inst.cuh', 'k_twopass_v1_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh'],
-    "v1-bf16-B1H12-n65536-d128": ['twopass.cuh', 'twopass_inst.cuh', 'k_twopass_v1_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh'],
-    "v2-bf16-B8Hq32Hkv16-n8192-d128": ['onepass.cuh', 'onepass_inst.cuh', 'k_onepass_v2_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh'],
+    "v1-bf16-B4H16-n2048-d64": ['onepass.cuh', 'onepass_inst.cuh', 'k_onepass_v1_d64.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh', 'api.cu'],
+    "v1-bf16-B2H12-n4096-d128": ['twopass.cuh', 'twopass_inst.cuh', 'k_twopass_v1_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh', 'api.cu'],
+    "v1-bf16-B1H12-n65536-d128": ['twopass.cuh', 'twopass_inst.cuh', 'k_twopass_v1_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh', 'api.cu'],
+    "v2-bf16-B8Hq32Hkv16-n8192-d128": ['onepass.cuh', 'onepass_inst.cuh', 'k_onepass_v2_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh', 'api.cu'],
 }
 NCU_TRAFFIC = {  # workload: (source hash of its kernel, bytes per launch: dram__bytes_read.sum + dram__bytes_write.sum)
-    "v1-bf16-B4H16-n2048-d64": ("62cf361661a5de12", 134964992 + 13048064),
-    "v1-bf16-B2H12-n4096-d128": ("dfe882014fe2b468", 327775744 + 28875776),
-    "v1-bf16-B1H12-n65536-d128": ("dfe882014fe2b468", 1761651456 + 405597696),
-    "v2-bf16-B8Hq32Hkv16-n8192-d128": ("9c6381a8498e1ae4", 1073854464 + 254917632),
+    "v1-bf16-B4H16-n2048-d64": ("4df540f48cbf3a0f", 137763328 + 12744448),
+    "v1-bf16-B2H12-n4096-d128": ("e043abfad4c1087d", 152508928 + 29984512),
+    "v1-bf16-B1H12-n65536-d128": ("e043abfad4c1087d", 1759340288 + 405261312),
+    "v2-bf16-B8Hq32Hkv16-n8192-d128": ("304202e121d54910", 1073950976 + 254695680),
 }
 
 

@@ -129,6 +129,8 @@ def lib() -> ctypes.CDLL:
             L.diffattn_bounds_checked.restype = i
             L.diffattn_debug_bounds_selftest.argtypes = [vp]
             L.diffattn_debug_bounds_selftest.restype = i
+            L.diffattn_debug_item_plan.argtypes = [i, ll, i, i, i, i, ll, vp, vp]
+            L.diffattn_debug_item_plan.restype = i
             L.diffattn_last_error.argtypes = []
             L.diffattn_last_error.restype = ctypes.c_char_p
             L.diffattn_debug_wait_timeout.argtypes = [ll, vp]
@@ -835,6 +837,17 @@ def bounds_checked() -> bool:
 def debug_bounds_selftest(stream=None) -> None:
     """Bounds-check build: one checked store out of its limit (skipped and recorded)."""
     _check(lib().diffattn_debug_bounds_selftest(_stream(stream)))
+
+
+def debug_item_plan(grid: int, units: int, nqt: int, qt0: int, n: int, causal: bool, kv_unit_bytes: int):
+    """The host's item plan of a persistent d = 128 forward: (first [grid + 1], items [units nqt]) as
+    numpy uint16 arrays, or None when the launch is too large for a plan."""
+    import numpy as np
+    first = np.zeros(max(grid, 0) + 1, dtype=np.uint16)
+    items = np.zeros(max(units * nqt, 1), dtype=np.uint16)
+    cnt = lib().diffattn_debug_item_plan(grid, units, nqt, qt0, n, 1 if causal else 0, kv_unit_bytes,
+                                         first.ctypes.data_as(ctypes.c_void_p), items.ctypes.data_as(ctypes.c_void_p))
+    return None if cnt == 0 else (first, items)
 
 
 def device_status(stream=None) -> int:

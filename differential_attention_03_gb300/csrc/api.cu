@@ -9,8 +9,12 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <functional>
 #include <mutex>
+#include <queue>
 #include <string>
+#include <utility>
+#include <vector>
 
 #include "bwd_params.h"
 #include "bwd_prep.cuh"
@@ -244,6 +248,54 @@ diffattn_status make_map_u8_wide(CUtensorMap* m, const void* base, int B, int n,
   return DIFFATTN_OK;
 }
 
+// Per-CTA item lists for a persistent launch of `units` units x `nqt` query
+// tiles (tiles [qt0, qt0 + nqt) of each sequence), as indices of the
+// unit-major item map.  The units are taken in groups whose K/V streams
+// together stay within 32 MiB (so the group's streams stay in L2), the
+// heaviest causal tile of every unit of a group first; each item goes to the
+// CTA whose planned work ends first, an item counting as its key tiles plus a
+// fixed cost of two tiles (greedy list scheduling, as a shared work counter
+// would hand items out, without one).  Measured on B2 H12 n4096 d128 (96 MiB of
+// K/V): query-tile-major order over all heads in the snake order reads 2.2x the
+// input bytes from HBM and takes 0.243 ms; this plan with groups of 8 heads
+// 0.231 ms (groups of 12: 0.236 ms and 1.1x the bytes; of 6: 0.238 ms).
+// Returns false (plan.count = 0: the kernel's snake order) past the plan's size.
+bool plan_items(da::ItemPlan& plan, int grid, long long units, int nqt, int qt0, int n, int causal,
+                long long kv_unit_bytes) {
+  plan.count = 0;
+  const long long nitems = units * nqt;
+  if (grid < 1 || grid > da::kPlanMaxCtas || nitems < 1 || nitems > da::kPlanMaxItems) return false;
+  const long long budget = 32ll << 20;
+  const long long ngroups = std::max(1ll, (units * kv_unit_bytes + budget - 1) / budget);
+  const long long ug = (units + ngroups - 1) / ngroups;
+  const int ntiles = (n + 127) / 128;
+  thread_local std::vector<std::vector<unsigned short>> lists;
+  lists.assign(static_cast<size_t>(grid), {});
+  using Slot = std::pair<long long, int>;  // (planned end, CTA): the earliest end first, then the lowest CTA
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
+  for (int c = 0; c < grid; ++c) free_at.push({0ll, c});
+  for (long long g0 = 0; g0 < units; g0 += ug) {
+    const long long g1 = std::min(units, g0 + ug);
+    for (int ql = nqt - 1; ql >= 0; --ql) {
+      const int T = causal ? std::min(ntiles, qt0 + ql + 1) : ntiles;
+      for (long long u = g0; u < g1; ++u) {
+        const Slot f = free_at.top();
+        free_at.pop();
+        lists[static_cast<size_t>(f.second)].push_back(static_cast<unsigned short>(u * nqt + (nqt - 1 - ql)));
+        free_at.push({f.first + T + 2, f.second});
+      }
+    }
+  }
+  int a = 0;
+  for (int c = 0; c < grid; ++c) {
+    plan.first[c] = static_cast<unsigned short>(a);
+    for (unsigned short it : lists[static_cast<size_t>(c)]) plan.items[a++] = it;
+  }
+  plan.first[grid] = static_cast<unsigned short>(a);
+  plan.count = grid;
+  return true;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Tile order: unit-major keeps all query tiles of one head together so that its
@@ -308,12 +360,19 @@ diffattn_status launch_v1_tc(const char* fn, da::TwoPassParams& p, bool f8, int 
   // dynamic CTA scheduling balances them; measured faster).
   const bool persist = qt0 + p.num_q_tiles <= 64;  // (the last tile's item length decides)
   const int g = static_cast<int>(persist ? persistent_grid(grid) : grid);
+  // d = 128 persistent: the host's item plan (unit-major item map) instead of the snake order.
+  thread_local da::ItemPlan plan;
+  plan.count = 0;
+  if (persist && d == 128 &&
+      plan_items(plan, g, static_cast<long long>(B) * H, p.num_q_tiles, qt0, n, causal,
+                 static_cast<long long>(n) * (2 * d + dv) * 2))
+    p.order = 0;
   // (p.o1_save set: the training forward, d = 64, which also saves each row's statistics)
   cudaError_t e = f8 ? ((d == 64) ? da::launch_onepass_v1_d64_f8(p, g, persist, s)
-                                   : da::launch_twopass_v1_d128_f8(p, g, persist, s))
+                                   : da::launch_twopass_v1_d128_f8(p, plan, g, persist, s))
                   : (d == 64) ? (p.o1_save ? da::launch_onepass_v1_d64_save(p, g, persist, s)
                                            : da::launch_onepass_v1_d64(p, g, persist, s))
-                              : da::launch_twopass_v1_d128(p, g, persist, s);
+                              : da::launch_twopass_v1_d128(p, plan, g, persist, s);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   g_launches.fetch_add(1);
   return DIFFATTN_OK;
@@ -2036,6 +2095,16 @@ __device__ int g_bounds_selftest[8];
 __global__ void bounds_selftest_kernel() { DA_STORE(g_bounds_selftest, 5, 4, 1); }
 }  // namespace
 #endif
+
+int diffattn_debug_item_plan(int grid, long long units, int nqt, int qt0, int n, int causal, long long kv_unit_bytes,
+                             unsigned short* first, unsigned short* items) {
+  if (!first || !items || units < 1 || nqt < 1 || n < 1) return 0;
+  thread_local da::ItemPlan plan;
+  if (!plan_items(plan, grid, units, nqt, qt0, n, causal, kv_unit_bytes)) return 0;
+  for (int c = 0; c <= grid; ++c) first[c] = plan.first[c];
+  for (int a = 0; a < plan.first[grid]; ++a) items[a] = plan.items[a];
+  return plan.count;
+}
 
 diffattn_status diffattn_debug_bounds_selftest(void* stream) {
 #ifdef DIFFATTN_BOUNDS

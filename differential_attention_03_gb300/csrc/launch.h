@@ -18,9 +18,12 @@ struct BwdPrepParams;
 namespace da {
 
 // V1, d = 128, value width 256: two sweeps, one accumulator.
-cudaError_t launch_twopass_v1_d128(const TwoPassParams& p, int grid, bool persistent, cudaStream_t s);
+// plan: the persistent form's per-CTA item lists (plan.count == 0: snake order).
+cudaError_t launch_twopass_v1_d128(const TwoPassParams& p, const ItemPlan& plan, int grid, bool persistent,
+                                   cudaStream_t s);
 // The same with e4m3 queries and keys (QK^T on kind::f8f6f4 MMAs; P.V in bf16).
-cudaError_t launch_twopass_v1_d128_f8(const TwoPassParams& p, int grid, bool persistent, cudaStream_t s);
+cudaError_t launch_twopass_v1_d128_f8(const TwoPassParams& p, const ItemPlan& plan, int grid, bool persistent,
+                                      cudaStream_t s);
 // V1, d = 64, value width 128: one sweep, two online-softmax states.
 cudaError_t launch_onepass_v1_d64(const TwoPassParams& p, int grid, bool persistent, cudaStream_t s);
 // V2, d = 128 (query/key/value width 128), one K/V head per query-head pair: one sweep.

@@ -48,6 +48,18 @@ struct TwoPassParams {
   int q_tile_begin;   // first query tile (0 unless a causal forward is run over token chunks)
 };
 
+// Work plan of a persistent launch, computed on the host: CTA c takes the
+// items items[first[c]] .. items[first[c + 1] - 1] in that order (indices of
+// the unit-major item map).  count == 0: no plan (the snake order).  Passed
+// by value as a second kernel parameter, so a launch needs no device memory
+// or shared state for it.
+constexpr int kPlanMaxCtas = 256, kPlanMaxItems = 4096;
+struct ItemPlan {
+  int count;  // CTAs with a list (the launch's grid), or 0
+  unsigned short first[kPlanMaxCtas + 1];
+  unsigned short items[kPlanMaxItems];
+};
+
 // What work item `idx` of a tcgen05 launch computes: batch b, unit u (V1:
 // head; V2: query-head pair), its query heads and K/V head, query tile qt
 // (first row q0).  Items are ordered heaviest causal first: unit-major keeps

@@ -176,7 +176,8 @@ __device__ __forceinline__ void row_stats64(uint32_t (&r0)[32], uint32_t (&r1)[3
 }
 
 template <int D, int DV, bool SHARED_K, int EPI, int NSLOT, bool PERSIST, bool F8 = false>
-__global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_constant__ TwoPassParams p) {
+__global__ void __launch_bounds__(640, 1)
+    twopass_fwd_kernel(const __grid_constant__ TwoPassParams p, const __grid_constant__ ItemPlan plan) {
   using C = TwoPassCfg<D, DV, SHARED_K, EPI, NSLOT, PERSIST, F8>;
   constexpr int BM = C::BM, BN = C::BN;
 
@@ -205,12 +206,16 @@ __global__ void __launch_bounds__(640, 1) twopass_fwd_kernel(const __grid_consta
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
-  // ---- this CTA's work items: round k takes item k G + blockIdx.x, or
-  // k G + G - 1 - blockIdx.x on odd rounds; the list ends at the first one
-  // past the last item (later rounds start further on).
+  // ---- this CTA's work items: its list in the host's plan, else round k
+  // takes item k G + blockIdx.x, or k G + G - 1 - blockIdx.x on odd rounds;
+  // the list ends at the first one past the last item.
   const int nitems = p.num_q_tiles * p.B * p.units_per_batch;
   const int G = static_cast<int>(gridDim.x);
   auto item_of = [&](int k) -> int {
+    if (PERSIST && plan.count > 0) {
+      const int a = plan.first[blockIdx.x] + k;
+      return a < plan.first[blockIdx.x + 1] ? static_cast<int>(plan.items[a]) : nitems;
+    }
     return k * G + ((k & 1) ? (G - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x));
   };
   auto tiles_of = [&](const TileCoord& c) -> int {

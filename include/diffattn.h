@@ -611,6 +611,22 @@ int diffattn_bounds_checked(void);
 diffattn_status diffattn_debug_bounds_selftest(void* stream);
 
 /*
+ * Host only (nothing launched): the item plan that a persistent d = 128
+ * forward over `units` (batch, head) units and query tiles
+ * [qt0, qt0 + nqt) of an n-token sequence would run on `grid` CTAs, for the
+ * tests.  Items are indices of the unit-major item map (unit u, query tile
+ * qt0 + nqt - 1 - (item mod nqt) for item = u nqt + ...); CTA c runs
+ * items[first[c]] .. items[first[c + 1] - 1] in that order.
+ *   first : host array of at least grid + 1 entries (written);
+ *   items : host array of at least units * nqt entries (written);
+ *   kv_unit_bytes : K/V bytes of one unit (it sets the group size).
+ * Returns the number of CTAs with a list (grid), or 0 when the launch is too
+ * large for a plan (more than 256 CTAs or 4096 items: the snake order runs).
+ */
+int diffattn_debug_item_plan(int grid, long long units, int nqt, int qt0, int n, int causal,
+                             long long kv_unit_bytes, unsigned short* first, unsigned short* items);
+
+/*
  * Diagnostics: launches one CTA whose thread waits on an mbarrier that nothing
  * arrives on, with a budget of about `budget_ns` nanoseconds (1 .. 1e9; the
  * kernel counts 2 SM clock cycles per nanosecond).  The wait

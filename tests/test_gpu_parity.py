@@ -256,6 +256,26 @@ def test_v1_host_buffers_match_device_path(B, H, n, d, causal):
         assert err <= TOL["bf16"], f"max abs error {err}"
 
 
+@pytest.mark.parametrize("B,H,n,causal", [(1, 40, 1024, True), (2, 20, 1024, False), (1, 12, 4000, True)])
+def test_v1_d128_planned_item_groups(B, H, n, causal):
+    # Persistent d = 128 launches with more items than SMs run the host's item plan, heads in groups
+    # of at most 32 MiB of K/V (here 2 groups of 20 heads, 2 of 20 units, and 2 of 6 heads with a
+    # ragged last tile).  Every head on sampled rows against the oracle, and the whole output bit for
+    # bit against the host-buffer path, whose token-range launches each run their own plan.
+    w = shrink(WORKLOADS[3], B=B, H=H, n=n, causal=causal, seed=70 + H)
+    x = make_v1(w, "cuda")
+    out, lam = _v1_gpu(x, w)
+    rows = _sample_rows(n, 24, 71 + H)
+    ref = _v1_oracle(x, w, rows=rows)
+    err = _err(_np(out[:, rows]), ref)
+    assert err <= TOL["bf16"], f"max abs error {err}"
+    host = {k: x[k].cpu().pin_memory() for k in ("q1", "q2", "k1", "k2", "v")}
+    out_h = da.diffattn_forward_host(host["q1"], host["q2"], host["k1"], host["k2"], host["v"], lam,
+                                     da.lambda_init(w.layer), gamma=x["gamma"], causal=causal)
+    da.device_status()
+    assert torch.equal(out_h, out.cpu())
+
+
 # --------------------------------------------------------------------------- decode
 DECODE = [  # B, H, n, d, lens
     (2, 2, 300, 64, None),
