@@ -5,7 +5,8 @@ before the access and reports a failed check as DIFFATTN_ERR_BOUNDS.  Here it is
 catch a checked store out of its limit (a self-test whose store lands inside its own array either
 way), and then the small-size parity tests (forward V1 / V2 incl. FP8 QK^T and the host-buffer
 pipeline, decode incl. FP8 keys and split states, backward fp32 and bf16 incl. the training pair,
-projections and layers: n <= 1100, and the host pipeline's token chunks up to n = 9000) run against
+projections and layers: n <= 1100, the host pipeline's token chunks up to n = 9000, and the
+persistent d = 128 forward on host item plans of two head groups) run against
 it in a child process with DIFFATTN_DEBUG=1: each of them reads the device status after its kernels, so a
 failed check fails the test.
 """
@@ -21,8 +22,8 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 SMALL = ("(small_full_compare or test_v1_decode or test_v2_decode or backward_f32 or backward_bf16 "
-         "or layer_matches or projection_matches or lambda_outside or zero_tokens or train_pair or host_buffers) "
-         "and not bench and not long")
+         "or layer_matches or projection_matches or lambda_outside or zero_tokens or train_pair or host_buffers "
+         "or planned_item_groups) and not bench and not long")
 
 
 def _child_env():
