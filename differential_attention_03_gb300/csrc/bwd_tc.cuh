@@ -404,6 +404,19 @@ __global__ void __launch_bounds__(608, 1) bwd_tc_kernel(const __grid_constant__ 
     };
     float pre[2];
     fetch_stats(0, pre);
+    // dQ_2's last reduce-add of a step is issued one phase later (pend_*: its column, head and first
+    // query; pend_col < 0: none), after the next step's first phase has passed its barrier, so that
+    // dQ_1's reduce-add, whose staging the next phase 1 overwrites, has the L2's reduction bandwidth
+    // to itself; phase 2 waits for dQ_2's read before it overwrites that staging.
+    int pend_col = -1, pend_head = 0, pend_q0 = 0;
+    auto issue_pending = [&]() {
+      if (lead && h >= 2 && pend_col >= 0) {
+        tma_reduce_add_4d(V2 ? &p.tm_dq1 : &p.tm_dq2, smem + C::OFF_DS2 + (h & 1) * 16384, pend_col, pend_head,
+                          pend_q0, b);
+        bulk_commit_group();
+        pend_col = -1;
+      }
+    };
     for (int s = 0; s < nsteps; ++s) {
       const uint32_t ph = static_cast<uint32_t>(s) & 1u;
       const int u = step_pair(s), q0 = step_tile(s) * 128;
@@ -484,6 +497,7 @@ __global__ void __launch_bounds__(608, 1) bwd_tc_kernel(const __grid_constant__ 
             // The dS_1^T buffer staged the previous step's dQ_1: its reduce-adds must have read it.
             if (lead && h < 2) bulk_wait_read_all();
             named_bar_sync(1, 512);
+            issue_pending();  // the previous step's deferred dQ_2 reduce-add
           }
           // 16-byte chunks chunk0 + 2 q + v of the row, swizzled by the row
 #pragma unroll
@@ -587,12 +601,19 @@ __global__ void __launch_bounds__(608, 1) bwd_tc_kernel(const __grid_constant__ 
           named_bar_sync(3 + h, 128);
           if (lead && dq_ok &&
               DA_BOUNDS_V(col0 % 4 == 0 && col0 < D && q0 < p.n && b < p.B && head < (V2 ? 2 : 1) * p.units, col0)) {
-            tma_reduce_add_4d(dqmap, stg, col0, head, q0, b);
-            bulk_commit_group();
+            if (map == 1 && rd == ROUNDS - 1) {
+              pend_col = col0;
+              pend_head = head;
+              pend_q0 = q0;
+            } else {
+              tma_reduce_add_4d(dqmap, stg, col0, head, q0, b);
+              bulk_commit_group();
+            }
           }
         }
       }
     }
+    issue_pending();
     if (lead) bulk_wait_all();  // the dQ reduce-adds have completed
     // ---- epilogue: dV and dK of the CTA's keys (thread = key row); warpgroup h writes dV columns
     // [32 h, +32) and dK columns [32 h, +32) of (dK_1 | dK_2) (V1) or of dK (V2).
