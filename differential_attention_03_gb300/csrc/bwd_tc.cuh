@@ -585,7 +585,10 @@ __global__ void __launch_bounds__(608, 1) bwd_tc_kernel(const __grid_constant__ 
             __syncwarp();
           }
           if (rd == 0) {
-            mbar_wait(ds_done, ph, ab);  // the MMAs reading dS^T of this step are done
+            // The MMAs reading this map's dS^T buffer are done: for dS_1 (dK_1 and dQ_1) dq_full
+            // already implies it (each MMA warp's commit covers its earlier MMAs); dS_2 is also read
+            // by dK_2, issued after dQ_2.
+            if (map == 1) mbar_wait(ds_done, ph, ab);
             __syncwarp();
           } else {
             if (lead) bulk_wait_read_all();  // the previous round's reduce-add has read the staging
