@@ -157,3 +157,35 @@ def test_graph_backward():
         for k in ("dq1", "dq2"):
             err = float((captured[k] - ref[k]).abs().max())
             assert err <= 1e-5 * max(1.0, float(ref[k].abs().max())), f"replay {it}: {k} {err}"
+
+
+@pytest.mark.parametrize("B,n", [(1, 2000), (3, 300)])
+def test_graph_host_buffer_forward(B, n):
+    # diffattn_forward_host forks its copies and (token-range) forwards onto internal streams with
+    # events and joins them back into the caller's stream, which stream capture records as a fork
+    # and join: the graph holds the host->device copies, the forwards and the copies back.  New
+    # inputs written into the same page-locked buffers are picked up by the next replay.
+    H, d = 2, 128
+    g = torch.Generator(device="cuda").manual_seed(14 + n)
+    host = {k: torch.empty((B, n, H, d), dtype=torch.bfloat16).pin_memory() for k in ("q1", "q2", "k1", "k2")}
+    host["v"] = torch.empty((B, n, H, 2 * d), dtype=torch.bfloat16).pin_memory()
+    out = torch.empty((B, n, H, 2 * d), dtype=torch.bfloat16).pin_memory()
+    lam = torch.tensor([0.45], device="cuda")
+    ws = torch.empty(da.forward_host_workspace_bytes(torch.bfloat16, B, H, n, d), dtype=torch.uint8, device="cuda")
+
+    def fill():
+        for t in host.values():
+            t.copy_(torch.randn(t.shape, generator=g, device="cuda").to(torch.bfloat16).cpu())
+
+    fill()
+    graph, _ = _capture(lambda: da.diffattn_forward_host(host["q1"], host["q2"], host["k1"], host["k2"], host["v"],
+                                                         lam, 0.2, out=out, workspace=ws))
+    for it in range(2):
+        fill()
+        graph.replay()
+        torch.cuda.synchronize()
+        dev = {k: t.cuda() for k, t in host.items()}
+        ref = da.diffattn_forward(dev["q1"], dev["q2"], dev["k1"], dev["k2"], dev["v"], lam, 0.2)
+        torch.cuda.synchronize()
+        da.device_status()
+        assert torch.equal(out, ref.cpu()), f"replay {it}"
