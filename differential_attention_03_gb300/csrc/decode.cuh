@@ -207,6 +207,9 @@ __device__ __forceinline__ void decode_finish(const DecodeParams& p, int b, int 
 template <int D, bool V2>
 __global__ void __launch_bounds__(DecodeCfg<D, V2>::NTHREADS) decode_combine_kernel(const __grid_constant__ DecodeParams p) {
   using C = DecodeCfg<D, V2>;  // (the key type does not change the state layout)
+  // Launched as a programmatic dependent of decode_kernel: its CTAs may be resident before that
+  // grid ends; the states it reads are complete and visible after this wait.
+  grid_dep_wait();
   constexpr int DV = C::DV;
   constexpr int CPT = DV > C::NTHREADS ? DV / C::NTHREADS : 1;
   __shared__ float red[C::NWARP];
@@ -242,6 +245,8 @@ template <int D, bool V2, bool K8>
 __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
     decode_kernel(const __grid_constant__ DecodeParams p) {
   using C = DecodeCfg<D, V2, K8>;
+  // The combine kernel (split form) may be scheduled now; it waits for this grid to finish.
+  grid_dep_launch_dependents();
   constexpr int BK = C::BK, KW = C::KW, PARTS = C::PARTS, DV = C::DV, CH = C::CH, NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

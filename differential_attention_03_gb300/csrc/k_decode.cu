@@ -26,8 +26,21 @@ static cudaError_t launch_decode(const DecodeParams& p, int units, int cs, cudaS
   e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e != cudaSuccess) return e;
   if (p.nsplit > 1) {  // merge the clusters' states of every (b, h) and finish the rows
-    // (the combine kernel's own block size: the key type does not change its layout)
-    decode_combine_kernel<D, V2><<<units, DecodeCfg<D, V2>::NTHREADS, 0, s>>>(p);
+    // (the combine kernel's own block size: the key type does not change its layout).  A
+    // programmatic dependent launch: its CTAs are scheduled while the last clusters finish and
+    // wait in grid_dep_wait() for the states, which hides the launch between the two kernels.
+    cudaLaunchConfig_t cc = {};
+    cc.gridDim = dim3(static_cast<unsigned>(units), 1, 1);
+    cc.blockDim = dim3(DecodeCfg<D, V2>::NTHREADS, 1, 1);
+    cc.dynamicSmemBytes = 0;
+    cc.stream = s;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cc.attrs = pdl;
+    cc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cc, decode_combine_kernel<D, V2>, p);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

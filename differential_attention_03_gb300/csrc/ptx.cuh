@@ -458,6 +458,17 @@ __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t a) {
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before the previous kernel on its stream has
+// finished; grid_dep_wait() blocks until that kernel has completed and its
+// memory operations are visible.  grid_dep_launch_dependents() lets the next
+// such kernel be scheduled once every CTA of this grid has issued it (or
+// exited); it does not relax that wait.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- math
 // Hardware base-2 exponential (MUFU); ex2(-inf) = +0.
 __device__ __forceinline__ float ex2(float x) {
