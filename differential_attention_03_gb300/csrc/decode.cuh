@@ -245,8 +245,12 @@ template <int D, bool V2, bool K8>
 __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
     decode_kernel(const __grid_constant__ DecodeParams p) {
   using C = DecodeCfg<D, V2, K8>;
-  // The combine kernel (split form) may be scheduled now; it waits for this grid to finish.
+  // Launched as a programmatic dependent of whatever kernel precedes it on the stream (which may
+  // write the queries, the cache, the lengths or the output): nothing global is touched before
+  // this wait, so only the launch overlaps that kernel's end.  The next dependent (the combine
+  // kernel of the split form, or the next call's decode) may be scheduled now.
   grid_dep_launch_dependents();
+  grid_dep_wait();
   constexpr int BK = C::BK, KW = C::KW, PARTS = C::PARTS, DV = C::DV, CH = C::CH, NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
