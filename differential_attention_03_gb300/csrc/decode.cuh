@@ -20,21 +20,26 @@
 //
 // The step is bound by HBM: every visible key's k_1, k_2 and v are read
 // exactly once (V once for both maps), 8 d bytes per key, against ~12 d
-// flops.  So no tensor cores: the work is spread so that enough bytes are in
-// flight on every SM.
+// flops.  The design spends itself on bytes in flight on every SM, and on
+// keeping the instructions a key costs low enough that issue never limits
+// the stream:
 //   * A cluster of CS CTAs per (b, h) (CS from 1 to 8, chosen by the host so
 //     that the grid fills the GPU); CTA c streams keys [c C, c C + C) of
 //     the cache (C a multiple of the stage size) through a ring of NST
 //     stages filled by TMA (K_1, K_2 and V tiles of BK keys, 128-byte
 //     swizzled rows; 32 KB a stage).
-//   * NWARP warps per CTA (four; eight for V2 and for FP8 keys), BK / NWARP
-//     keys each per stage; PARTS lanes share a key (PE = 32 or 16 products of
-//     q . k each, combined by shuffles), so a warp scores its
-//     keys in one pass; every warp keeps its own online-softmax state per map
-//     (running maximum, per-lane partial sums, 2d / 32 output channels per
-//     lane for each map), rescaled only when the maximum grows.  Products
-//     and value accumulations run as packed f32x2 FMAs (two lanes of fp32
-//     arithmetic per instruction), which halves the instructions a key costs.
+//   * Four warps per CTA, BK / 4 keys each per stage (16, or 8 at d = 128).
+//     A warp scores its keys with warp-wide MMAs (mma.sync: bf16 m16n8k16,
+//     or e4m3 m16n8k32 for FP8 keys), transposed so that the keys are the
+//     MMA's rows and the queries two of its eight columns: S^T = K [q_1 q_2].
+//     Its online-softmax state per map (running maximum, row sums) is
+//     rescaled only when the maximum grows, and the weights go back through
+//     the tensor cores as O^T += V^T P^T (bf16 P, fp32 accumulation; V read
+//     once for both maps by transposed ldmatrix loads).  Against scalar
+//     FMAs this cuts the instructions a key costs about fourfold: the
+//     tensor pipe is not the bound (it runs at a few per cent of its rate);
+//     instruction issue was, measured at 0.83-0.85 of the HBM copy with FP8
+//     keys.
 //   * The CTA merges its warps' states in shared memory; the cluster's CTAs
 //     then merge theirs through distributed shared memory in CTA rank 0,
 //     which applies the combine and the per-head RMSNorm and stores the row.
@@ -46,6 +51,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "params.h"
 #include "ptx.cuh"
@@ -82,27 +88,22 @@ template <int D, bool V2 = false, bool K8 = false>
 struct DecodeCfg {
   static constexpr int MAX_CS = 8;  // CTAs per (b, h) cluster: chosen at launch, at most this (16-CTA
                                     // clusters measured slower: 5.5 vs 6.2 TB/s at B8 H8 n32768 d128)
-  // Warps per CTA.  V2: eight, so that a stage is 64 keys (32 KB).  V1 with
-  // FP8 keys at d = 64: eight (PE = 16 products a lane), so that two CTAs per
-  // SM hide the latency of the longer per-byte instruction stream (a key is
-  // 6 d bytes instead of 8 d for the same work).  At d = 128 (32-key stages)
-  // eight warps would leave 4 keys a warp and 8 lanes a key: measured at half
-  // the bandwidth of four warps, so V1 d = 128 keeps four.
-  static constexpr int NWARP = (V2 || (K8 && D == 64)) ? 8 : 4;
+  // Warps per CTA: four.  A warp scores 16 keys of a stage (one MMA tile of rows); at d = 128's
+  // 32-key stages two warps share each 16 keys and split the value channels between them.
+  static constexpr int NWARP = 4;
   static constexpr int NTHREADS = NWARP * 32;
   static constexpr int DV = V2 ? D : 2 * D;     // value width
   static constexpr int NKT = V2 ? 1 : 2;         // key tiles a stage holds (V2: one K for both queries)
   static constexpr int BK = (V2 || D == 64) ? 64 : 32;  // keys per stage
-  static constexpr int KW = BK / NWARP;         // keys per warp per stage
-  static constexpr int PARTS = 32 / KW;         // lanes per key
-  static constexpr int PE = D / PARTS;          // q . k products per lane (32, or 16 with FP8 keys in V1)
+  static constexpr int WPG = NWARP / (BK / 16);  // warps per 16 keys (1, or 2 at d = 128), splitting the channels
+  static constexpr int KS = K8 ? D / 32 : D / 16;  // MMA k-steps over the query/key width
+  static constexpr int MT = (V2 ? D : 2 * D) / 16;  // 16-channel tiles of the value width
   static constexpr int KROW = K8 ? D : 128;  // bytes of a key row in one TMA box (bf16: 64 columns)
   static constexpr int QB = K8 ? 1 : D / 64;  // key boxes per row
   static constexpr int VB = DV / 64;
   static constexpr int K_BYTES = QB * BK * KROW, V_BYTES = VB * BK * 128;
   static constexpr int STAGE = NKT * K_BYTES + V_BYTES;  // 32 KB (K8: 24 KB)
   static constexpr int NST = 98304 / STAGE;              // 96 KB of stages in flight
-  static constexpr int CH = DV / 32;  // output channels per lane and map
   static constexpr int PART_FLOATS = 2 * (DV + 2);  // per map: max, sum, DV channels
   static constexpr int OFF_BARS = NST * STAGE;
   static constexpr int OFF_FLAG = OFF_BARS + 2 * NST * 8;
@@ -111,7 +112,7 @@ struct DecodeCfg {
   static constexpr int OFF_RED = OFF_PART + PART_FLOATS * 4;           // float [NWARP]
   static constexpr int SMEM_BYTES = OFF_RED + NWARP * 4 + 1024;        // + 1 KB alignment slack
   static_assert(D == 64 || D == 128, "query/key width");
-  static_assert((PE == 32 || PE == 16) && PARTS * KW == 32, "lane split");
+  static_assert(WPG >= 1 && WPG * (BK / 16) == NWARP && MT % WPG == 0, "warps tile the stage's keys and channels");
   static_assert(NST * STAGE == 98304, "stage ring");
   static_assert(STAGE % 1024 == 0 && K_BYTES % 1024 == 0, "swizzled boxes start on 1 KB");
   static_assert(!V2 || D == 128, "V2 decode: d = 128");
@@ -143,20 +144,51 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t a, uint32_t rank) {
   return v;
 }
 
-// Four e4m3 values (bytes 0..3 of w, byte 0 first) to floats; exact (every
-// e4m3 value is an f16 value).
-__device__ __forceinline__ void e4m3x4_to_f32(uint32_t w, float (&f)[4]) {
-  uint32_t h01, h23;
-  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
-      : "=r"(h01), "=r"(h23)
-      : "r"(w));
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-  const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-  f[0] = a.x;
-  f[1] = a.y;
-  f[2] = c.x;
-  f[3] = c.y;
+// Warp-wide tensor-core operations of the decode loop (mma.sync: the step is bound by HBM, the
+// MMAs only cut the instructions a key costs).  Fragment layouts are the PTX ISA's for
+// m16n8k16 (bf16) and m16n8k32 (e4m3) with lane = 4 g + t: A rows g and g + 8, B column g,
+// C rows g, g + 8 x columns 2 t, 2 t + 1.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_e4m3_16832(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One k-step of the score MMA: bf16 keys (16 dims) or e4m3 keys (32 dims).
+template <bool K8>
+__device__ __forceinline__ void mma_keys(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (K8)
+    mma_e4m3_16832(c, a, b0, b1);
+  else
+    mma_bf16_16816(c, a, b0, b1);
+}
+
+// Two floats as bf16 (round to nearest even), lo in bits 0..15.
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -251,7 +283,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
   // kernel of the split form, or the next call's decode) may be scheduled now.
   grid_dep_launch_dependents();
   grid_dep_wait();
-  constexpr int BK = C::BK, KW = C::KW, PARTS = C::PARTS, DV = C::DV, CH = C::CH, NST = C::NST;
+  constexpr int BK = C::BK, DV = C::DV, NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
@@ -313,155 +345,209 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
     for (; issued < NST && issued < nblk; ++issued) issue(issued);
   }
 
-  // This lane's PE query products (pre-scaled into the log2 domain, and by
-  // the key scale of an e4m3 key cache).
-  constexpr int PE = C::PE;
-  const int kk = lane / PARTS, prt = lane % PARTS;
-  const float qs1 = K8 ? p.scale_log2 * p.k1_scale : p.scale_log2;
-  const float qs2 = K8 ? p.scale_log2 * (V2 ? p.k1_scale : p.k2_scale) : p.scale_log2;
-  uint64_t q1r[PE / 2], q2r[PE / 2];  // pairs of query products
-  {
-    const __nv_bfloat16* q1p = p.q1 + q1_off + prt * PE;
-    const __nv_bfloat16* q2p = (V2 ? p.q1 : p.q2) + q2_off + prt * PE;
+  // ---- the operands that stay in registers: the queries as the B operand of the score MMAs.
+  // Scores are computed transposed, S^T = K Q (16 keys x 8 columns per warp-wide MMA): column 0
+  // collects map 1 (the K_1 MMA sees q_1 there and zeros elsewhere), column 1 map 2 (the K_2 MMA
+  // sees q_2 there), so both maps land in one accumulator.  Lane (g, t) = (lane / 4, lane % 4)
+  // holds column g of the B fragments.
+  constexpr int KS = C::KS, WPG = C::WPG, MTW = C::MT / WPG;
+  const int g = lane >> 2, tq = lane & 3;
+  constexpr int NT = K8 ? 2 : 1;      // query terms (e4m3: hi and lo)
+  uint32_t qa[NT][KS][2], qb[NT][KS][2];  // B fragments of the K_1 (V2: the shared K) and K_2 MMAs
+  float qs1, qs2;                 // what turns column 0 / 1 of S^T into log2-domain scores
+  if constexpr (!K8) {
+    // bf16 queries as they are (m16n8k16: rows 2t, 2t + 1 and 2t + 8, 2t + 9 of column g).
+    const uint32_t* w1 = reinterpret_cast<const uint32_t*>(p.q1 + q1_off);
+    const uint32_t* w2 = reinterpret_cast<const uint32_t*>((V2 ? p.q1 : p.q2) + q2_off);
 #pragma unroll
-    for (int i = 0; i < PE; i += 8) {
-      const uint4 a = *reinterpret_cast<const uint4*>(q1p + i);
-      const uint4 c = *reinterpret_cast<const uint4*>(q2p + i);
-      const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wc[4] = {c.x, c.y, c.z, c.w};
+    for (int ks = 0; ks < KS; ++ks) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        q1r[i / 2 + e] = f2pack(bf16_lo(wa[e]) * qs1, bf16_hi(wa[e]) * qs1);
-        q2r[i / 2 + e] = f2pack(bf16_lo(wc[e]) * qs2, bf16_hi(wc[e]) * qs2);
+      for (int j = 0; j < 2; ++j) {
+        const int w = 8 * ks + tq + 4 * j;  // 32-bit word: dims 16 ks + 8 j + 2 t, + 1
+        const uint32_t a = w1[w], c = w2[w];
+        qa[0][ks][j] = (g == 0) ? a : ((V2 && g == 1) ? c : 0u);
+        qb[0][ks][j] = (!V2 && g == 1) ? c : 0u;
       }
     }
+    qs1 = qs2 = p.scale_log2;
+  } else {
+    // e4m3 keys meet e4m3 queries (m16n8k32).  Each query row is scaled by a power of two that
+    // puts its largest magnitude in [128, 256) and split into two e4m3 terms, hi = e4m3(x) and
+    // lo = e4m3(x - hi): a bf16 value has eight significant bits and each term holds four, so
+    // the pair is exact for every element down to 2^-10 of the row's largest (smaller ones
+    // keep an absolute error below 2^-18 of it).  The two terms are two MMAs into the same
+    // column: V1 q_1 in column 0 (the K_1 MMAs), q_2 in column 1 (the K_2 MMAs); V2 q_even in 0,
+    // q_odd in 1.  Lane (g, t) holds dims 32 ks + 4 t .. + 3 and 32 ks + 16 + 4 t .. + 3 of
+    // column g's row.
+    const __nv_bfloat16* qv = (g & 1) ? ((V2 ? p.q1 : p.q2) + q2_off) : (p.q1 + q1_off);
+    float x[KS][8];
+    float amax = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint2 w = *reinterpret_cast<const uint2*>(qv + 32 * ks + 16 * j + 4 * tq);
+        x[ks][4 * j] = bf16_lo(w.x);
+        x[ks][4 * j + 1] = bf16_hi(w.x);
+        x[ks][4 * j + 2] = bf16_lo(w.y);
+        x[ks][4 * j + 3] = bf16_hi(w.y);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[ks][e]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // the four lanes of a column hold its row
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int bexp = (__float_as_int(amax) >> 23) & 0xff;  // amax in [2^(bexp - 127), 2^(bexp - 126))
+    const int sh = (amax > 0.f) ? max(-100, min(100, 134 - bexp)) : 0;
+    const float mul = __int_as_float((127 + sh) << 23), inv = __int_as_float((127 - sh) << 23);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        uint32_t whi = 0, wlo = 0;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const float v0 = x[ks][4 * j + 2 * h2] * mul, v1 = x[ks][4 * j + 2 * h2 + 1] * mul;
+          const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3);
+          const float2 hf = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3)));
+          const __nv_fp8x2_storage_t lo =
+              __nv_cvt_float2_to_fp8x2(make_float2(v0 - hf.x, v1 - hf.y), __NV_SATFINITE, __NV_E4M3);
+          whi |= static_cast<uint32_t>(hi) << (16 * h2);
+          wlo |= static_cast<uint32_t>(lo) << (16 * h2);
+        }
+        const bool in_a = V2 ? (g < 2) : (g == 0), in_b = !V2 && g == 1;
+        qa[0][ks][j] = in_a ? whi : 0u;
+        qa[NT - 1][ks][j] = in_a ? wlo : 0u;
+        qb[0][ks][j] = in_b ? whi : 0u;
+        qb[NT - 1][ks][j] = in_b ? wlo : 0u;
+      }
+    }
+    // Column 0's row scale is lane 0's, column 1's lane 4's.
+    qs1 = p.scale_log2 * p.k1_scale * __shfl_sync(0xffffffffu, inv, 0);
+    qs2 = p.scale_log2 * (V2 ? p.k1_scale : p.k2_scale) * __shfl_sync(0xffffffffu, inv, 4);
   }
 
+  // ---- the warp's 16 keys kb .. kb + 15 of every stage and its MTW 16-channel tiles from mt0;
+  // ldmatrix rows of this lane (matrix mi = lane / 8, row mr = lane % 8): the score MMA's A = K
+  // (keys x dims) takes keys + 8 for matrices 1 and 3, the P.V MMA's A = V^T (channels x keys, a
+  // transposed load) keys + 8 for matrices 2 and 3.  (kb + 15 < BK: the warps tile the stage.)
+  const int mi = lane >> 3, mr = lane & 7;
+  const int kb = (warp / WPG) * 16, mt0 = (warp % WPG) * MTW;
+  const int s_row = kb + mr + (mi & 1) * 8;
+  const int v_row = kb + mr + (mi >> 1) * 8;
+
+  constexpr float kRescaleLog2 = 8.f;  // how far a score may exceed the reference maximum
   float m1 = -INFINITY, m2 = -INFINITY, ls1 = 0.f, ls2 = 0.f;
-  uint64_t o1p[CH / 2], o2p[CH / 2];
+  float o[MTW][4];  // O^T tiles: lanes t = 0 hold channel 16 (mt0 + mt) + g (+ 8) of map 1 ([0], [2]) and map 2 ([1], [3])
 #pragma unroll
-  for (int c = 0; c < CH / 2; ++c) o1p[c] = o2p[c] = 0ull;
-  // Byte offsets inside a stage that do not change: this lane's PE key
-  // columns (box, first 16-byte chunk) and its CH value channels.
-  const int kbox = (prt * PE) / 64, kchunk0 = ((prt * PE) % 64) / 8;
-  const int vc0 = lane * CH, vbox = vc0 / 64, vbyte = (vc0 % 64) * 2;
+  for (int mt = 0; mt < MTW; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
   for (int i = 0; i < nblk; ++i) {
     const int s = i % NST;
     if (!mbar_wait(&full[s], static_cast<uint32_t>(i / NST) & 1u, ab)) break;
-    const uint8_t* st = smem + s * C::STAGE;
-    const int row = warp * KW + kk;  // this lane's key within the stage
-    // ---- scores: PE products per lane, PARTS lanes per key
-    uint64_t a1 = 0ull, a2 = 0ull, b1 = 0ull, b2 = 0ull;
-    if constexpr (K8) {
-      // PE e4m3 key values: 16-byte chunks (PE / 16) prt .. of the row
-      // (128-byte rows: 128-byte swizzle, chunk ^ (row % 8); 64-byte rows:
-      // 64-byte swizzle, chunk ^ ((row / 2) % 4)).
+    const uint32_t st = smem_u32(smem + s * C::STAGE);
+    // ---- scores S^T of the warp's 16 key rows (fp32 accumulation on the tensor cores), in four
+    // independent accumulator chains: V1 (map, parity of the MMA), V2 the MMA's index % 4
+    float acc[4][4];
 #pragma unroll
-      for (int c = 0; c < PE / 16; ++c) {
-        const int ch = (PE / 16) * prt + c;
-        const int pch = (C::KROW == 128) ? (ch ^ (row & 7)) : (ch ^ ((row >> 1) & 3));
-        const int off = row * C::KROW + (pch << 4);
-        const uint4 a = *reinterpret_cast<const uint4*>(st + off);
-        const uint4 e = V2 ? a : *reinterpret_cast<const uint4*>(st + C::K_BYTES + off);  // V2: one key tile
-        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, we[4] = {e.x, e.y, e.z, e.w};
+    for (int c = 0; c < 4; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          float fa[4], fe[4];
-          e4m3x4_to_f32(wa[t], fa);
-          e4m3x4_to_f32(we[t], fe);
-          a1 = fma2(q1r[8 * c + 2 * t], f2pack(fa[0], fa[1]), a1);
-          b1 = fma2(q1r[8 * c + 2 * t + 1], f2pack(fa[2], fa[3]), b1);
-          a2 = fma2(q2r[8 * c + 2 * t], f2pack(fe[0], fe[1]), a2);
-          b2 = fma2(q2r[8 * c + 2 * t + 1], f2pack(fe[2], fe[3]), b2);
-        }
+    for (int ks = 0; ks < KS; ++ks) {
+      const int ch = 2 * ks + (mi >> 1);  // 16-byte chunk of the key row
+      uint32_t off;
+      if constexpr (K8)  // rows of D bytes: 128-byte swizzle (chunk ^ row % 8) or 64-byte (chunk ^ (row / 2) % 4)
+        off = s_row * C::KROW + (((C::KROW == 128) ? (ch ^ (s_row & 7)) : (ch ^ ((s_row >> 1) & 3))) << 4);
+      else  // boxes of 64 bf16 columns, 128-byte rows, 128-byte swizzle
+        off = (ch >> 3) * BK * 128 + s_row * 128 + (((ch & 7) ^ (s_row & 7)) << 4);
+      uint32_t a[4];
+      ldsm_x4(a, st + off);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int u = ks * NT + t;
+        mma_keys<K8>(acc[V2 ? (u & 3) : (u & 1)], a, qa[t][ks][0], qa[t][ks][1]);
       }
+      if constexpr (!V2) {
+        ldsm_x4(a, st + C::K_BYTES + off);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) mma_keys<K8>(acc[2 + ((ks * NT + t) & 1)], a, qb[t][ks][0], qb[t][ks][1]);
+      }
+    }
+    float sc[4];  // columns 0 (map 1) and 1 (map 2) of rows g ([0], [1]) and g + 8 ([2], [3])
+    if constexpr (V2) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) sc[j] = (acc[0][j] + acc[1][j]) + (acc[2][j] + acc[3][j]);
     } else {
+      sc[0] = acc[0][0] + acc[1][0];
+      sc[1] = acc[2][1] + acc[3][1];
+      sc[2] = acc[0][2] + acc[1][2];
+      sc[3] = acc[2][3] + acc[3][3];
+    }
+    // Lanes t = 0 now hold key kb + g ([0] map 1, [1] map 2) and key kb + g + 8 ([2], [3]).
+    const int key = k_begin + i * BK + kb + g;
+    float s1a = sc[0] * qs1, s2a = sc[1] * qs2, s1b = sc[2] * qs1, s2b = sc[3] * qs2;
+    if (key >= k_end) s1a = s2a = -INFINITY;  // past this CTA's keys or the length
+    if (key + 8 >= k_end) s1b = s2b = -INFINITY;
+    // ---- online softmax of the warp's keys.  The reference maxima m1, m2 move only when a score
+    // exceeds them by more than 2^8 (log2 domain: weights up to 256, safe in bf16 and in the fp32
+    // sums), found by one vote; only then is the tile maximum reduced over lanes t = 0 and
+    // broadcast, so the rescale branches stay uniform across the warp.
+    float x1 = fmaxf(s1a, s1b), x2 = fmaxf(s2a, s2b);
+    if (__any_sync(0xffffffffu, tq == 0 && (x1 > m1 + kRescaleLog2 || x2 > m2 + kRescaleLog2))) {
 #pragma unroll
-      for (int c = 0; c < PE / 8; ++c) {
-        const int off = kbox * BK * 128 + row * 128 + (((kchunk0 + c) ^ (row & 7)) << 4);
-        const uint4 a = *reinterpret_cast<const uint4*>(st + off);
-        const uint4 e = V2 ? a : *reinterpret_cast<const uint4*>(st + C::K_BYTES + off);  // V2: one key tile
-        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, we[4] = {e.x, e.y, e.z, e.w};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          if (t & 1) {
-            b1 = fma2(q1r[4 * c + t], f2pack(bf16_lo(wa[t]), bf16_hi(wa[t])), b1);
-            b2 = fma2(q2r[4 * c + t], f2pack(bf16_lo(we[t]), bf16_hi(we[t])), b2);
-          } else {
-            a1 = fma2(q1r[4 * c + t], f2pack(bf16_lo(wa[t]), bf16_hi(wa[t])), a1);
-            a2 = fma2(q2r[4 * c + t], f2pack(bf16_lo(we[t]), bf16_hi(we[t])), a2);
-          }
-        }
+      for (int x = 4; x < 32; x <<= 1) {
+        x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, x));
+        x2 = fmaxf(x2, __shfl_xor_sync(0xffffffffu, x2, x));
       }
-    }
-    float s1, s2;
-    {
-      const uint64_t t1 = add2(a1, b1), t2 = add2(a2, b2);
-      float l, h;
-      f2unpack(t1, l, h);
-      s1 = l + h;
-      f2unpack(t2, l, h);
-      s2 = l + h;
-    }
-#pragma unroll
-    for (int x = 1; x < PARTS; x <<= 1) {
-      s1 += __shfl_xor_sync(0xffffffffu, s1, x);
-      s2 += __shfl_xor_sync(0xffffffffu, s2, x);
-    }
-    if (k_begin + i * BK + row >= k_end) s1 = s2 = -INFINITY;  // past this CTA's keys or the length
-    // ---- online softmax of this warp's keys
-    float x1 = s1, x2 = s2;
-#pragma unroll
-    for (int x = PARTS; x < 32; x <<= 1) {
-      x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, x));
-      x2 = fmaxf(x2, __shfl_xor_sync(0xffffffffu, x2, x));
+      x1 = __shfl_sync(0xffffffffu, x1, 0);
+      x2 = __shfl_sync(0xffffffffu, x2, 0);
+    } else {
+      x1 = m1;
+      x2 = m2;
     }
     if (x1 > m1) {
       const float f = (m1 == -INFINITY) ? 0.f : ex2(m1 - x1);
       m1 = x1;
       ls1 *= f;
 #pragma unroll
-      for (int c = 0; c < CH / 2; ++c) o1p[c] = fma2(o1p[c], f2pack(f, f), 0ull);
+      for (int mt = 0; mt < MTW; ++mt) {
+        o[mt][0] *= f;
+        o[mt][2] *= f;
+      }
     }
     if (x2 > m2) {
       const float f = (m2 == -INFINITY) ? 0.f : ex2(m2 - x2);
       m2 = x2;
       ls2 *= f;
 #pragma unroll
-      for (int c = 0; c < CH / 2; ++c) o2p[c] = fma2(o2p[c], f2pack(f, f), 0ull);
-    }
-    const float p1 = (s1 == -INFINITY) ? 0.f : ex2(s1 - m1);
-    const float p2 = (s2 == -INFINITY) ? 0.f : ex2(s2 - m2);
-    if (prt == 0) {
-      ls1 += p1;
-      ls2 += p2;
-    }
-    // ---- P.V: every lane accumulates its CH channels over the warp's keys
-    const uint8_t* vb = st + C::NKT * C::K_BYTES + vbox * BK * 128;
-#pragma unroll
-    for (int k2 = 0; k2 < KW; ++k2) {
-      const float w1 = __shfl_sync(0xffffffffu, p1, k2 * PARTS);
-      const float w2 = __shfl_sync(0xffffffffu, p2, k2 * PARTS);
-      const int r = warp * KW + k2;
-      const uint8_t* vr = vb + r * 128 + ((((vbyte >> 4)) ^ (r & 7)) << 4) + (vbyte & 15);
-      uint32_t vw[CH / 2];
-      if constexpr (CH == 4) {
-        const uint2 t = *reinterpret_cast<const uint2*>(vr);
-        vw[0] = t.x;
-        vw[1] = t.y;
-      } else {
-        const uint4 t = *reinterpret_cast<const uint4*>(vr);
-        vw[0] = t.x;
-        vw[1] = t.y;
-        vw[2] = t.z;
-        vw[3] = t.w;
+      for (int mt = 0; mt < MTW; ++mt) {
+        o[mt][1] *= f;
+        o[mt][3] *= f;
       }
+    }
+    const float p1a = (s1a == -INFINITY) ? 0.f : ex2(s1a - m1), p1b = (s1b == -INFINITY) ? 0.f : ex2(s1b - m1);
+    const float p2a = (s2a == -INFINITY) ? 0.f : ex2(s2a - m2), p2b = (s2b == -INFINITY) ? 0.f : ex2(s2b - m2);
+    ls1 += p1a + p1b;  // (meaningful in lanes t = 0)
+    ls2 += p2a + p2b;
+    // ---- P^T as the B operand (keys x columns; column 0 map 1, column 1 map 2) in bf16: lane
+    // (g, t) needs keys 2t, 2t + 1 (b0) and 2t + 8, 2t + 9 (b1) of its column, held by lanes 8t
+    // and 8t + 4 as (key, key + 8) pairs.
+    uint32_t b0, b1;
+    {
+      const uint32_t u = bf16x2_bits(p1a, p1b), w = bf16x2_bits(p2a, p2b);
+      const uint32_t ua = __shfl_sync(0xffffffffu, u, 8 * tq), ub = __shfl_sync(0xffffffffu, u, 8 * tq + 4);
+      const uint32_t wa = __shfl_sync(0xffffffffu, w, 8 * tq), wb = __shfl_sync(0xffffffffu, w, 8 * tq + 4);
+      const uint32_t xa = (g == 1) ? wa : ua, xb = (g == 1) ? wb : ub;
+      b0 = __byte_perm(xa, xb, 0x5410);
+      b1 = __byte_perm(xa, xb, 0x7632);
+    }
+    // ---- O^T += V^T P^T over the warp's keys, 16 channels a tile
 #pragma unroll
-      for (int c = 0; c < CH / 2; ++c) {
-        const uint64_t vp = f2pack(bf16_lo(vw[c]), bf16_hi(vw[c]));
-        o1p[c] = fma2(f2pack(w1, w1), vp, o1p[c]);
-        o2p[c] = fma2(f2pack(w2, w2), vp, o2p[c]);
-      }
+    for (int mt = 0; mt < MTW; ++mt) {
+      const int ch = 2 * (mt0 + mt) + (mi & 1);  // 16-byte chunk (8 channels) of the value row
+      const uint32_t off = C::NKT * C::K_BYTES + (ch >> 3) * BK * 128 + v_row * 128 + (((ch & 7) ^ (v_row & 7)) << 4);
+      uint32_t a[4];
+      ldsm_x4_trans(a, st + off);
+      mma_bf16_16816(o[mt], a, b0, b1);
     }
     // ---- release the stage; thread 0 refills it once all the warps have
     __syncwarp();
@@ -480,26 +566,35 @@ __global__ void __launch_bounds__(DecodeCfg<D, V2, K8>::NTHREADS, 2)
 
   // ---- merge the warps' states (shared memory), then the cluster's (rank 0)
 #pragma unroll
-  for (int x = 1; x < 32; x <<= 1) {
+  for (int x = 4; x < 32; x <<= 1) {  // row sums over lanes t = 0
     ls1 += __shfl_xor_sync(0xffffffffu, ls1, x);
     ls2 += __shfl_xor_sync(0xffffffffu, ls2, x);
   }
   float* wp = wpart + warp * C::PART_FLOATS;  // [m1, l1, m2, l2, o1[DV], o2[DV]]
+  // (Warps that share keys have the same maxima and sums: the first of them reports the sums, and
+  // each reports zeros for the channels the others hold.)
   if (lane == 0) {
     wp[0] = m1;
-    wp[1] = ls1;
+    wp[1] = (warp % WPG == 0) ? ls1 : 0.f;
     wp[2] = m2;
-    wp[3] = ls2;
+    wp[3] = (warp % WPG == 0) ? ls2 : 0.f;
   }
+  if (tq == 0) {
 #pragma unroll
-  for (int c = 0; c < CH / 2; ++c) {
-    float l, h;
-    f2unpack(o1p[c], l, h);
-    wp[4 + vc0 + 2 * c] = l;
-    wp[4 + vc0 + 2 * c + 1] = h;
-    f2unpack(o2p[c], l, h);
-    wp[4 + DV + vc0 + 2 * c] = l;
-    wp[4 + DV + vc0 + 2 * c + 1] = h;
+    for (int mt = 0; mt < MTW; ++mt) {
+      const int c0 = 16 * (mt0 + mt) + g;
+      wp[4 + c0] = o[mt][0];
+      wp[4 + c0 + 8] = o[mt][2];
+      wp[4 + DV + c0] = o[mt][1];
+      wp[4 + DV + c0 + 8] = o[mt][3];
+    }
+  }
+  if constexpr (WPG > 1) {
+    for (int c = lane; c < DV; c += 32) {
+      if (c / (16 * MTW) == warp % WPG) continue;
+      wp[4 + c] = 0.f;
+      wp[4 + DV + c] = 0.f;
+    }
   }
   __syncthreads();
   {
