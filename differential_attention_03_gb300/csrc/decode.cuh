@@ -36,10 +36,10 @@
 //     rescaled only when the maximum grows, and the weights go back through
 //     the tensor cores as O^T += V^T P^T (bf16 P, fp32 accumulation; V read
 //     once for both maps by transposed ldmatrix loads).  Against scalar
-//     FMAs this cuts the instructions a key costs about fourfold: the
-//     tensor pipe is not the bound (it runs at a few per cent of its rate);
-//     instruction issue was, measured at 0.83-0.85 of the HBM copy with FP8
-//     keys.
+//     FMAs this cuts the instructions a key costs about fourfold.  HBM stays
+//     the bound (ncu: the tensor pipe active 17-27 % of the time, issue
+//     22-34 %); instruction issue was the limit of the scalar form, measured
+//     at 0.83-0.85 of the HBM copy with FP8 keys.
 //   * The CTA merges its warps' states in shared memory; the cluster's CTAs
 //     then merge theirs through distributed shared memory in CTA rank 0,
 //     which applies the combine and the per-head RMSNorm and stores the row.
