@@ -61,10 +61,10 @@ KERNEL_FILES = {
     "v2-bf16-B8Hq32Hkv16-n8192-d128": ['onepass.cuh', 'onepass_inst.cuh', 'k_onepass_v2_d128.cu', 'params.h', 'ptx.cuh', 'status.cuh', 'bounds.cuh', 'api.cu'],
 }
 NCU_TRAFFIC = {  # workload: (source hash of its kernel, bytes per launch: dram__bytes_read.sum + dram__bytes_write.sum)
-    "v1-bf16-B4H16-n2048-d64": ("4df540f48cbf3a0f", 137763328 + 12744448),
-    "v1-bf16-B2H12-n4096-d128": ("e043abfad4c1087d", 152508928 + 29984512),
-    "v1-bf16-B1H12-n65536-d128": ("e043abfad4c1087d", 1759340288 + 405261312),
-    "v2-bf16-B8Hq32Hkv16-n8192-d128": ("304202e121d54910", 1073950976 + 254695680),
+    "v1-bf16-B4H16-n2048-d64": ("eda8ec60b9e91f7f", 139291648 + 12816640),
+    "v1-bf16-B2H12-n4096-d128": ("a645e087502723ac", 152373248 + 30054400),
+    "v1-bf16-B1H12-n65536-d128": ("a645e087502723ac", 1761939968 + 405562368),
+    "v2-bf16-B8Hq32Hkv16-n8192-d128": ("ae8a8492959243df", 1073912832 + 254664704),
 }
 
 
