@@ -579,6 +579,7 @@ BWD = [  # B, H, n, d, causal, lambda, gamma
     (2, 1, 77, 32, False, 1.2, True),      # non-causal, lambda > 1
     (1, 1, 130, 128, True, 0.6, True),     # d = 128: value width 256
     (1, 2, 65, 30, True, 0.5, True),       # d % 4 != 0: scalar staging
+    (2, 8, 1024, 64, True, 0.35, True),    # many row-pass CTAs: dlambda and dgamma summed over 16 (b, h)
 ]
 
 
