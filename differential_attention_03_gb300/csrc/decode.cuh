@@ -28,7 +28,8 @@
 //     the cache (C a multiple of the stage size) through a ring of NST
 //     stages filled by TMA (K_1, K_2 and V tiles of BK keys, 128-byte
 //     swizzled rows; 32 KB a stage).
-//   * Four warps per CTA, BK / 4 keys each per stage (16, or 8 at d = 128).
+//   * Four warps per CTA, BK / 4 keys each per stage (16, or 8 at the
+//     32-key stages of bf16 V1 d = 128).
 //     A warp scores its keys with warp-wide MMAs (mma.sync: bf16 m16n8k16,
 //     or e4m3 m16n8k32 for FP8 keys), transposed so that the keys are the
 //     MMA's rows and the queries two of its eight columns: S^T = K [q_1 q_2].
@@ -88,13 +89,16 @@ template <int D, bool V2 = false, bool K8 = false>
 struct DecodeCfg {
   static constexpr int MAX_CS = 8;  // CTAs per (b, h) cluster: chosen at launch, at most this (16-CTA
                                     // clusters measured slower: 5.5 vs 6.2 TB/s at B8 H8 n32768 d128)
-  // Warps per CTA: four.  A warp scores 16 keys of a stage (one MMA tile of rows); at d = 128's
-  // 32-key stages two warps share each 16 keys and split the value channels between them.
+  // Warps per CTA: four.  A warp scores 16 keys of a stage (one MMA tile of rows); at the 32-key
+  // stages of bf16 V1 d = 128 two warps share each 16 keys and split the value channels.
   static constexpr int NWARP = 4;
   static constexpr int NTHREADS = NWARP * 32;
   static constexpr int DV = V2 ? D : 2 * D;     // value width
   static constexpr int NKT = V2 ? 1 : 2;         // key tiles a stage holds (V2: one K for both queries)
-  static constexpr int BK = (V2 || D == 64) ? 64 : 32;  // keys per stage
+  // Keys per stage: 64; bf16 V1 d = 128 (a 64 KB key row set) 32.  FP8 V1 d = 128 takes 64-key
+  // stages of 48 KB in a two-stage ring: 1.00 of the HBM copy against 0.90 with 32-key stages of
+  // 24 KB in four (B8 H8 n32768).
+  static constexpr int BK = (V2 || D == 64 || K8) ? 64 : 32;
   static constexpr int WPG = NWARP / (BK / 16);  // warps per 16 keys (1, or 2 at d = 128), splitting the channels
   static constexpr int KS = K8 ? D / 32 : D / 16;  // MMA k-steps over the query/key width
   static constexpr int MT = (V2 ? D : 2 * D) / 16;  // 16-channel tiles of the value width
@@ -102,7 +106,7 @@ struct DecodeCfg {
   static constexpr int QB = K8 ? 1 : D / 64;  // key boxes per row
   static constexpr int VB = DV / 64;
   static constexpr int K_BYTES = QB * BK * KROW, V_BYTES = VB * BK * 128;
-  static constexpr int STAGE = NKT * K_BYTES + V_BYTES;  // 32 KB (K8: 24 KB)
+  static constexpr int STAGE = NKT * K_BYTES + V_BYTES;  // 32 KB (K8: 24 KB; V1 K8 d = 128: 48 KB)
   static constexpr int NST = 98304 / STAGE;              // 96 KB of stages in flight
   static constexpr int PART_FLOATS = 2 * (DV + 2);  // per map: max, sum, DV channels
   static constexpr int OFF_BARS = NST * STAGE;
